@@ -1,0 +1,145 @@
+"""Pins for the oracle's grouped GEMM (fwd / dgrad / wgrad), SwiGLU and the
+whole-layer backward (CPU)."""
+import numpy as np
+import pytest
+
+import oracle as O
+
+
+def _triple_loop(A, B):
+    M, K = A.shape
+    N = B.shape[1]
+    D = np.zeros((M, N))
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for kk in range(K):
+                s += A[i, kk] * B[kk, j]
+            D[i, j] = s
+    return D
+
+
+def test_grouped_gemm_brute_force_with_empty_groups():
+    rng = np.random.default_rng(20)
+    sizes = [3, 0, 1, 5, 0]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    A = rng.standard_normal((offs[-1] + 2, 6))        # 2 rows belong to no group
+    B = rng.standard_normal((len(sizes), 6, 4))
+    D = O.grouped_gemm(A, B, offs)
+    for g, m in enumerate(sizes):
+        lo, hi = offs[g], offs[g + 1]
+        if m:
+            assert np.allclose(D[lo:hi], _triple_loop(A[lo:hi], B[g]), rtol=1e-13)
+    assert np.all(D[offs[-1]:] == 0)                  # no output rows outside groups
+
+
+def test_all_tokens_to_one_expert_is_dense_gemm():
+    rng = np.random.default_rng(21)
+    A = rng.standard_normal((9, 5))
+    B = rng.standard_normal((4, 5, 3))
+    offs = np.array([0, 0, 0, 9, 9])                  # every row in group 2
+    assert np.allclose(O.grouped_gemm(A, B, offs), _triple_loop(A, B[2]), rtol=1e-13)
+
+
+def test_identity_and_permutation_weights_are_exact():
+    rng = np.random.default_rng(22)
+    A = np.round(rng.standard_normal((10, 8)) * 16) / 16
+    P = np.eye(8)[rng.permutation(8)]
+    B = np.stack([np.eye(8), P, 2.0 * np.eye(8)])
+    offs = np.array([0, 4, 7, 10])
+    D = O.grouped_gemm(A, B, offs)
+    assert np.array_equal(D[:4], A[:4])
+    assert np.array_equal(D[4:7], A[4:7] @ P)
+    assert np.array_equal(D[7:], 2 * A[7:])
+
+
+def test_wgrad_brute_force_and_empty_group_zero():
+    rng = np.random.default_rng(23)
+    sizes = [4, 0, 7]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    A = rng.standard_normal((offs[-1], 3))
+    G = rng.standard_normal((offs[-1], 5))
+    dB = O.grouped_gemm_wgrad(A, G, offs)
+    assert dB.shape == (3, 3, 5)
+    assert np.all(dB[1] == 0)
+    for g in (0, 2):
+        lo, hi = offs[g], offs[g + 1]
+        assert np.allclose(dB[g], _triple_loop(A[lo:hi].T.copy(), G[lo:hi]), rtol=1e-13)
+    one = O.grouped_gemm_wgrad(A, G, np.array([0, offs[-1]]))
+    assert np.allclose(one[0], _triple_loop(A.T.copy(), G), rtol=1e-13)
+
+
+def test_swiglu_special_values():
+    a = np.array([[0.0, 3.0, 5.0, 0.0], [40.0, -40.0, 2.0, 3.0]])   # f = 2: [g | u]
+    h = O.swiglu(a)
+    assert h[0, 0] == 0.0 and h[0, 1] == 0.0          # g = 0 or u = 0
+    assert np.isclose(h[1, 0], 40.0 * 2.0, rtol=1e-15)  # silu(40) ~ 40
+    assert abs(h[1, 1]) < 1e-15                        # silu(-40) ~ 0
+    g = 1.3
+    assert np.isclose(O.swiglu(np.array([[g, 2.0]]))[0, 0], g / (1 + np.exp(-g)) * 2.0, rtol=1e-15)
+
+
+def test_swiglu_bwd_finite_differences():
+    rng = np.random.default_rng(24)
+    a = rng.standard_normal((5, 8)) * 2
+    dh = rng.standard_normal((5, 4))
+    da = O.swiglu_bwd(a, dh)
+    eps = 1e-6
+    for i in range(5):
+        for j in range(8):
+            ap, am = a.copy(), a.copy()
+            ap[i, j] += eps
+            am[i, j] -= eps
+            fd = np.sum((O.swiglu(ap) - O.swiglu(am)) * dh) / (2 * eps)
+            assert np.isclose(fd, da[i, j], rtol=1e-6, atol=1e-9)
+
+
+@pytest.mark.parametrize("score", ["softmax", "sigmoid"])
+def test_layer_backward_finite_differences(score):
+    """The whole unquantized layer: gradients of L = <out, dout> with respect
+    to x, logits, W1 and W2 against central differences."""
+    rng = np.random.default_rng(25)
+    T, d, E, k, f = 12, 6, 4, 2, 5
+    x = rng.standard_normal((T, d))
+    # well separated logits so the top-k choice cannot flip under eps
+    logits = np.stack([rng.permutation(E) * 1.0 for _ in range(T)]) + 0.1 * rng.standard_normal((T, E))
+    W1 = rng.standard_normal((E, d, 2 * f)) * 0.5
+    W2 = rng.standard_normal((E, f, d)) * 0.5
+    dout = rng.standard_normal((T, d))
+    out, saved = O.layer_forward(x, logits, W1, W2, k, score, True, align=1)
+    g = O.layer_backward(dout, logits, W1, W2, k, saved, score, True)
+
+    def loss(x_, l_, W1_, W2_):
+        o, _ = O.layer_forward(x_, l_, W1_, W2_, k, score, True, align=1)
+        return np.sum(o * dout)
+
+    eps = 1e-6
+    args = [x, logits, W1, W2]
+    grads = [g["dx"], g["dlogits"], g["dW1"], g["dW2"]]
+    for which in range(4):
+        flat = args[which].reshape(-1)
+        for pos in rng.choice(flat.size, size=min(12, flat.size), replace=False):
+            p = [a.copy() for a in args]
+            m = [a.copy() for a in args]
+            p[which].reshape(-1)[pos] += eps
+            m[which].reshape(-1)[pos] -= eps
+            fd = (loss(*p) - loss(*m)) / (2 * eps)
+            an = grads[which].reshape(-1)[pos]
+            assert np.isclose(fd, an, rtol=1e-5, atol=1e-7), (which, pos, fd, an)
+
+
+def test_layer_padding_does_not_change_results():
+    rng = np.random.default_rng(26)
+    T, d, E, k, f = 30, 8, 4, 2, 4
+    x = rng.standard_normal((T, d))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    W1 = rng.standard_normal((E, d, 2 * f))
+    W2 = rng.standard_normal((E, f, d))
+    dout = rng.standard_normal((T, d))
+    o1, s1 = O.layer_forward(x, logits, W1, W2, k, align=1)
+    o2, s2 = O.layer_forward(x, logits, W1, W2, k, align=128)
+    assert np.allclose(o1, o2, rtol=1e-13)
+    g1 = O.layer_backward(dout, logits, W1, W2, k, s1)
+    g2 = O.layer_backward(dout, logits, W1, W2, k, s2)
+    for key in ("dx", "dlogits", "dW1", "dW2"):
+        assert np.allclose(g1[key], g2[key], rtol=1e-12, atol=1e-12)
