@@ -1,0 +1,453 @@
+"""Benchmark: one dropless-MoE layer fwd+bwd step (route, permute, MXFP8
+quantize, grouped GEMMs with fused SwiGLU, combine, and the backward of each)
+on the DeepSeek-V3-shaped workload: T = 24576 tokens (6 x 4096), d = 7168,
+E = 256 routed experts, top-8 sigmoid routing with normalised weights,
+f = 2048, R = T*k = 196,608 routed rows, bf16 activations, MXFP8 operands.
+
+Prints ONE JSON line (rank 0).  `value` = fwd+bwd grouped-GEMM TFLOPS
+(18*R*d*f algorithmic FLOPs per step / device time per step), whole job.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload deepseek-v3|mixtral|tiny] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (plain fp64 numpy) on a bounded sample
+of the same workload: the only other place this file runs oracle code.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: T, d, E, k, f, score, normalize, zipf
+    "deepseek-v3": dict(T=24576, d=7168, E=256, k=8, f=2048, score="sigmoid", normalize=True, zipf=None,
+                        desc="DeepSeek-V3-shaped routed-expert layer fwd+bwd: T=24576 (6x4096), d=7168, E=256, "
+                             "top-8 sigmoid normalised, f=2048"),
+    "mixtral": dict(T=8192, d=4096, E=8, k=2, f=14336, score="softmax", normalize=True, zipf=None,
+                    desc="Mixtral-shaped layer fwd+bwd: T=8192, d=4096, E=8, top-2 softmax, f=14336"),
+    "tiny": dict(T=256, d=512, E=8, k=2, f=256, score="softmax", normalize=True, zipf=None,
+                 desc="tiny layer fwd+bwd: T=256, d=512, E=8, top-2, f=256"),
+}
+METRIC = "MoE layer fwd+bwd TFLOPS (MXFP8 grouped GEMM) and % of dense peak, 1 GB300"
+KERNELS_PER_STEP = 25       # libmoe kernel launches in one fwd+bwd step (see layer.MoELayer)
+GEMMS_PER_STEP = 6
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms in a thread."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.idx)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in self.rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows), "power_w_max": max(pw) if pw else None}
+
+
+# --------------------------------------------------------------------- GPU --
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    from grouped_gemm_top_gb300 import build as _b
+    if not os.path.exists(_b.LIB):
+        _b.build()
+    from grouped_gemm_top_gb300 import synth
+    from grouped_gemm_top_gb300.layer import MoELayer
+
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    w = WORKLOADS[args.workload]
+    T, d, E, k, f = w["T"], w["d"], w["E"], w["k"], w["f"]
+    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev)
+    inp = synth.make_layer_inputs(T, d, E, f, dev, zipf_s=w["zipf"], seed_offset=rank)
+    L.set_weights(inp["W1"], inp["W2"])
+    del inp["W1"], inp["W2"]
+    L.logits.copy_(inp["logits"])
+    L.x.copy_(inp["x"])
+    L.dout.copy_(inp["dout"])
+    torch.cuda.synchronize()
+    flops = L.flops_per_step()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # per-GEMM events: the GEMM launches of a step, in issue order
+    gemm_names = ["up_fwd_swiglu", "down_fwd", "down_dgrad_swiglu_bwd", "down_wgrad", "up_dgrad", "up_wgrad"]
+    gemm_flops = [4 * L.R * d * f, 2 * L.R * d * f, 2 * L.R * d * f, 2 * L.R * d * f, 4 * L.R * d * f,
+                  4 * L.R * d * f]
+    for _ in range(args.warmup):
+        L.step_()
+    torch.cuda.synchronize()
+    L.check_err()
+
+    # ---- timed region: K eager steps, events around every GEMM launch
+    ev_pairs = []
+    L.gemm_events = ev_pairs
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for _ in range(args.steps):
+            L.step_()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    L.gemm_events = None
+    L.check_err()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    gemm_ms = [0.0] * GEMMS_PER_STEP
+    for i, (s, e) in enumerate(ev_pairs):
+        gemm_ms[i % GEMMS_PER_STEP] += s.elapsed_time(e)
+    gemm_ms = [x / args.steps for x in gemm_ms]
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+
+    # ---- CUDA-graph replay of the same step (the whole step in one graph)
+    L.capture()
+    for _ in range(2):
+        L.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        L.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    L.check_err()
+    graph_ms = g0.elapsed_time(g1) / args.steps
+
+    # ---- end to end through the public API from pinned host buffers
+    h_x = inp["x"].cpu().pin_memory()
+    h_l = inp["logits"].cpu().pin_memory()
+    h_d = inp["dout"].cpu().pin_memory()
+    h_out = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    h_dx = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    h_dl = torch.empty((T, E), dtype=torch.float32).pin_memory()
+    L.step(h_x, h_l, h_d, h_out, h_dx, h_dl)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        L.step(h_x, h_l, h_d, h_out, h_dx, h_dl)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = h_x.numel() * 2 + h_l.numel() * 4 + h_d.numel() * 2
+    d2h = h_out.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
+
+    peaks, psrc = _peaks()
+    mx_peak = 2.0 * peaks["bf16_tflops_sustained"]     # nominal fp8/bf16 dense ratio 4.5/2.25
+    sum_gemm_ms = sum(gemm_ms)
+    achieved = sum(gemm_flops) / (sum_gemm_ms * 1e-3) / 1e12
+    per_launch = {n: {"ms": round(t, 4), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
+                  for n, t, fl in zip(gemm_names, gemm_ms, gemm_flops)}
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp8(e4m3,e8m0) x mxfp8 -> fp32 acc -> bf16",
+        "data": "synthetic (seeded N(0,1) activations/logits, N(0,0.02^2) weights, random-init)",
+        "config": {"workload": w["desc"], "global_batch": T * world, "seq_len": 4096,
+                   "parallelism": f"replicas x{world} (no collectives)", "routed_rows": L.R,
+                   "row_capacity": L.row_cap,
+                   "l2": "no flush: inputs and weights (~45 GB) far exceed the 129 MB L2"},
+        "tokens_per_s": round(world * T / (ms_per_step * 1e-3), 1),
+        "frac_of_dense_mxfp8_peak": round(value / mx_peak, 4),
+        "graph_ms_per_step": round(graph_ms, 4),
+        "gemm_per_launch": per_launch,
+        "roofline": {"bound": "tensor", "kernel": "k_grouped_gemm (all 6 launches of a step)",
+                     "achieved": round(achieved, 1), "peak": round(mx_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / mx_peak, 4),
+                     "peak_source": f"2 x {psrc} bf16 sustained ({peaks['bf16_tflops_sustained']} TF/s), "
+                                    "nominal MXFP8/bf16 dense ratio 4.5/2.25",
+                     "traffic": None},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+    }
+    return result, L
+
+
+# --------------------------------------------------------------------- CPU --
+
+def oracle_sample(workload, n_experts, seed=0):
+    """Time the oracle on a bounded sample of the workload: routing of all
+    tokens, then the full fwd+bwd chain (quantize, GEMMs, SwiGLU, combine
+    pieces) for the routed rows of `n_experts` experts.  Returns (flops of
+    the sample, seconds, description)."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    from grouped_gemm_top_gb300 import synth
+
+    w = WORKLOADS[workload]
+    T, d, E, k, f = w["T"], w["d"], w["E"], w["k"], w["f"]
+    logits = synth.make_logits(T, E, 0, "cpu").numpy()
+    x = synth.make_normal_bf16((T, d), synth.SEED_X, "cpu")
+    dout = synth.make_normal_bf16((T, d), synth.SEED_DOUT, "cpu")
+    rng = np.random.default_rng(seed)
+    experts = rng.choice(E, size=n_experts, replace=False)
+    # Expert weights are drawn directly as MXFP8 values (random E4M3 codes
+    # times 2^-12), so both quantized copies of a weight equal the weight and
+    # no weight quantization runs before or inside the timed region.
+    wops = []
+    finite = np.array([c for c in range(256) if np.isfinite(O.E4M3_VALUES[c])])
+    for _ in experts:
+        W1e = O.E4M3_VALUES[rng.choice(finite, size=(d, 2 * f))] * 2.0 ** -12
+        W2e = O.E4M3_VALUES[rng.choice(finite, size=(f, d))] * 2.0 ** -12
+        wops.append((W1e[None], W2e[None], W2e.T[None], W1e.T[None]))
+    xn, dn = x.double().numpy(), dout.double().numpy()
+    t0 = time.perf_counter()
+    idx, wts = O.route_topk(logits, k, w["score"], w["normalize"])
+    flops = 0.0
+    for e, (B1, B2, B2t, B1t) in zip(experts, wops):
+        tok, j = np.nonzero(idx == e)
+        m = len(tok)
+        if m == 0:
+            continue
+        offs = np.array([0, m])
+        xp = xn[tok]
+        q, s = O.mxfp8_quantize_rows(xp)
+        A = O.grouped_gemm(O.mxfp8_dequantize_rows(q, s), B1, offs)
+        h = O.bf16_round(O.swiglu(A))
+        hq, hs = O.mxfp8_quantize_rows(h)
+        O.grouped_gemm(O.mxfp8_dequantize_rows(hq, hs), B2, offs)
+        dy = O.bf16_round(wts[tok, j][:, None] * dn[tok])
+        dq, ds = O.mxfp8_quantize_rows(dy)
+        dH = O.grouped_gemm(O.mxfp8_dequantize_rows(dq, ds), B2t, offs)
+        dA = O.bf16_round(O.swiglu_bwd(O.bf16_round(A), dH))
+        hT, hTs, _ = O.mxfp8_quantize_cols_grouped(h, offs)
+        dyT, dyTs, _ = O.mxfp8_quantize_cols_grouped(dy, offs)
+        O.grouped_gemm_wgrad(O.mxfp8_dequantize_cols(hT, hTs), O.mxfp8_dequantize_cols(dyT, dyTs), offs)
+        daq, das = O.mxfp8_quantize_rows(dA)
+        O.grouped_gemm(O.mxfp8_dequantize_rows(daq, das), B1t, offs)
+        xT, xTs, _ = O.mxfp8_quantize_cols_grouped(xp, offs)
+        aT, aTs, _ = O.mxfp8_quantize_cols_grouped(dA, offs)
+        O.grouped_gemm_wgrad(O.mxfp8_dequantize_cols(xT, xTs), O.mxfp8_dequantize_cols(aT, aTs), offs)
+        flops += 18.0 * m * d * f
+    secs = time.perf_counter() - t0
+    desc = (f"routing of all {T} tokens + fwd/bwd chain (MXFP8 quantize, 6 GEMMs, SwiGLU) for the routed rows of "
+            f"{n_experts} of {E} experts ({workload}); fp64 numpy")
+    return flops, secs, desc
+
+
+def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0"):
+    """Standalone grouped GEMM fwd (sweep point): G groups whose sizes are a
+    Dirichlet(0.3) split of M_total rows, N = K = NK, A and B ~ N(0,1) ->
+    MXFP8, bf16 out.  Returns a dict with TFLOPS and roofline fractions."""
+    import numpy as np
+    import torch
+
+    from grouped_gemm_top_gb300 import ops, synth
+    ops.moe_init(torch.device(device).index or 0)
+    sizes = synth.dirichlet_group_sizes(G, M_total, 0.3, seed)
+    gofs = np.concatenate([[0], np.cumsum((sizes + 127) // 128 * 128)])
+    M = int(gofs[-1])
+    x = torch.zeros((M, NK), dtype=torch.bfloat16, device=device)
+    src = synth.make_normal_bf16((M_total, NK), seed + 100, device)
+    r = 0
+    for g, m in enumerate(sizes):
+        x[int(gofs[g]):int(gofs[g]) + int(m)] = src[r:r + int(m)]
+        r += int(m)
+    del src
+    gofs_t = torch.tensor(gofs, dtype=torch.int32, device=device)
+    xq, xs = ops.mxfp8_group_quantize(x, ops.MOE_QUANT_ROWWISE, gofs_t, G)
+    del x
+    W = synth.make_normal_bf16((G * NK, NK), seed + 200, device)
+    wg = torch.arange(0, (G + 1) * NK, NK, dtype=torch.int32, device=device)
+    bq, bs = ops.mxfp8_group_quantize(W, ops.MOE_QUANT_COLWISE_GROUPED, wg, G)
+    del W
+    d = torch.empty((M, NK), dtype=torch.bfloat16, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def launch():
+        ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, ops.MOE_B_NGK, gofs_t, G, M, NK, NK, d=d, err=err)
+
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, int(err.item())
+    ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    flops = 2.0 * M_total * NK * NK
+    byts = G * NK * NK * (1 + 1 / 32) + M_total * NK * (1 + 1 / 32) + M_total * NK * 2
+    peaks, psrc = _peaks()
+    mx_peak = 2.0 * peaks["bf16_tflops"]          # kernel timed alone: burst
+    t_roof = max(flops / (mx_peak * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+    return {"G": G, "M_total": M_total, "N": NK, "K": NK, "ms": round(ms, 4),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 1), "frac_flops": round(flops / (ms * 1e-3) / 1e12 / mx_peak, 4),
+            "frac_roofline": round(t_roof / (ms * 1e-3), 4), "algorithmic_gb": round(byts / 1e9, 3),
+            "peak_tflops": mx_peak, "peak_source": f"2 x {psrc} bf16 burst", "empty_groups": int((sizes == 0).sum())}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores (bounded sample)."""
+    n_exp = 1 if args.workload == "deepseek-v3" else 1
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, n_exp, seed=0)
+    tot_f, tot_s = 0.0, 0.0
+    desc = ""
+    for i in range(args.steps):
+        fl, s, desc = oracle_sample(args.workload, n_exp, seed=i + 1)
+        tot_f += fl
+        tot_s += s
+    value = tot_f / tot_s / 1e12
+    w = WORKLOADS[args.workload]
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_s / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": w["desc"], "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="deepseek-v3", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-experts", type=int, default=2)
+    ap.add_argument("--gemm-point", nargs=3, type=int, metavar=("G", "M_TOTAL", "NK"),
+                    help="time one standalone grouped GEMM fwd and print its line")
+    ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
+    args = ap.parse_args()
+    if args.gemm_point or args.sweep:
+        pts = [tuple(args.gemm_point)] if args.gemm_point else \
+            [(G, M, NK) for G in (8, 64, 256) for NK in (2048, 7168) for M in (16384, 65536, 262144)]
+        for i, (G, M, NK) in enumerate(pts):
+            r = run_gemm_point(G, M, NK, seed=i, steps=args.steps, warmup=max(args.warmup, 3))
+            print(json.dumps({"sweep_point": r}), flush=True)
+            import torch
+            torch.cuda.empty_cache()
+        return
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    result, L = run_gpu(args, rank, world, local_rank)
+    del L
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            fl, secs, desc = oracle_sample(args.workload, args.cpu_experts)
+            result["cpu_baseline"] = {"value": round(fl / secs / 1e12, 6), "unit": "TFLOPS", "cores": cpu_cores(),
+                                      "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+        else:
+            result["cpu_baseline"] = None
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

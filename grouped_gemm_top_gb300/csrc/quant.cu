@@ -1,0 +1,183 @@
+// MXFP8 quantization: 1x32 blocks, E8M0 scales, E4M3 codes.
+// [TE-JAX] "What specialized optimizations are required for dropless MoE?"
+// (a group-aware MXFP8 quantization) and "Optimization 1" (MXFP8 block
+// scaling); [CH1] "低精度格式的缩放机制" (per-block scaling, blocks of 32) and
+// §1.1 (E4M3 = 1+4+3 bits).
+//
+// Both kernels work on 128x128 tiles so that one CTA produces exactly one
+// 512-byte scale atom (the tensor core's native scale order, see moe.h) and
+// writes it with one coalesced 512-byte store.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kQT = 128;   // tile edge
+
+__device__ bool gofs_valid(const int32_t* gofs, int G, int64_t rows) {
+    if (gofs[0] != 0) return false;
+    for (int g = 0; g < G; ++g) {
+        const int a = gofs[g], b = gofs[g + 1];
+        if (b < a || (b & 127) != 0) return false;
+    }
+    return (int64_t)gofs[G] <= rows;
+}
+
+// Rowwise: tile = 128 rows x 128 cols.  256 threads; a thread owns 8
+// consecutive elements, four neighbouring threads form one 32-element block.
+__global__ void __launch_bounds__(256) k_quant_rows(const uint4* __restrict__ x, int64_t rows, int cols,
+                                                    const int32_t* __restrict__ gofs, int G,
+                                                    uint2* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                    int32_t* err) {
+    __shared__ __align__(16) uint8_t s_atom[512];
+    const int64_t r0 = (int64_t)blockIdx.y * kQT;
+    const int c0 = blockIdx.x * kQT;
+    if (gofs != nullptr && r0 >= (int64_t)gofs[G]) return;
+    const int tc = threadIdx.x & 15;         // 16 threads per row (8 elements each)
+    const int tr = threadIdx.x >> 4;         // 16 rows per pass
+    const int cols8 = cols >> 3;
+    uint4 v[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int64_t r = r0 + tr + 16 * p;
+        v[p] = __ldg(x + r * cols8 + (c0 >> 3) + tc);
+    }
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        float f[8];
+        unpack8(v[p], f);
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        const uint32_t b = e8m0_scale_byte(amax);
+        const float inv = e8m0_inv_scale(b);
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = cvt_e4m3x2(f[2 * i] * inv, f[2 * i + 1] * inv);
+        const int rl = tr + 16 * p;          // local row
+        const int64_t r = r0 + rl;
+        codes[(r * cols + c0) / 8 + tc] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+        if ((tc & 3) == 0) {
+            const int kb = tc >> 2;          // local block 0..3
+            s_atom[(rl & 31) * 16 + ((rl >> 5) & 3) * 4 + kb] = (uint8_t)b;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int64_t atom = (int64_t)(c0 / kQT) * (rows / kQT) + r0 / kQT;
+        reinterpret_cast<uint4*>(scales + atom * 512)[threadIdx.x] = reinterpret_cast<const uint4*>(s_atom)[threadIdx.x];
+    }
+    (void)err;
+}
+
+// Columnwise, group-aware: tile = 128 input rows (4 blocks of 32 rows, all in
+// one group because groups start at multiples of 128) x 128 input columns.
+// Output is transposed: codes [cols, rows].
+__global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x, int64_t rows, int cols,
+                                                    const int32_t* __restrict__ gofs, int G,
+                                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                    int32_t* err) {
+    // the input tile [row][col] and, after it has been consumed, the output
+    // codes tile [col][row] share one buffer
+    __shared__ __align__(16) uint8_t s_buf[kQT * (kQT + 8) * 2];
+    __shared__ __align__(16) uint8_t s_atom[512];
+    auto s_x = reinterpret_cast<uint16_t(*)[kQT + 8]>(s_buf);
+    auto s_q = reinterpret_cast<uint8_t(*)[kQT + 16]>(s_buf);
+    __shared__ int s_ok;
+    const int64_t r0 = (int64_t)blockIdx.y * kQT;
+    const int c0 = blockIdx.x * kQT;
+    if (gofs != nullptr) {
+        if (threadIdx.x == 0) {
+            const bool ok = gofs_valid(gofs, G, rows);
+            s_ok = ok;
+            if (!ok && blockIdx.x == 0 && blockIdx.y == 0) set_err(err, MOE_ERR_BAD_OFFSETS);
+        }
+        __syncthreads();
+        if (!s_ok || r0 >= (int64_t)gofs[G]) return;
+    }
+    const int cols8 = cols >> 3;
+    // load 128 x 128 bf16: 16 uint4 per row, 2048 uint4, 8 per thread
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int idx = threadIdx.x + 256 * p;
+        const int rl = idx >> 4, cv = idx & 15;
+        const uint4 v = __ldg(x + (r0 + rl) * cols8 + (c0 >> 3) + cv);
+        *reinterpret_cast<uint4*>(&s_x[rl][cv * 8]) = v;
+    }
+    __syncthreads();
+    // each thread: 2 (column, block) pairs; a warp covers 32 consecutive columns
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t w[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int pair = warp + 8 * h;        // 0..15
+        const int col = (pair & 3) * 32 + lane;
+        const int blk = pair >> 2;            // 32-row block 0..3
+        float f[32];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            f[i] = bf16_bits_to_float(s_x[blk * 32 + i][col]);
+            amax = fmaxf(amax, fabsf(f[i]));
+        }
+        const uint32_t b = e8m0_scale_byte(amax);
+        const float inv = e8m0_inv_scale(b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = cvt_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
+            const uint32_t hi = cvt_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+            w[h][i] = lo | (hi << 16);
+        }
+        s_atom[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b;
+    }
+    __syncthreads();     // every thread is done reading the input tile
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int pair = warp + 8 * h;
+        const int col = (pair & 3) * 32 + lane;
+        const int blk = pair >> 2;
+        uint4* dst = reinterpret_cast<uint4*>(&s_q[col][blk * 32]);
+        dst[0] = make_uint4(w[h][0], w[h][1], w[h][2], w[h][3]);
+        dst[1] = make_uint4(w[h][4], w[h][5], w[h][6], w[h][7]);
+    }
+    __syncthreads();
+    // write codes: output row (c0 + col), bytes [r0, r0 + 128): 8 uint4 per row
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int idx = threadIdx.x + 256 * p;    // 0..1023
+        const int col = idx >> 3, cv = idx & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(&s_q[col][cv * 16]);
+        *reinterpret_cast<uint4*>(codes + (int64_t)(c0 + col) * rows + r0 + cv * 16) = v;
+    }
+    if (threadIdx.x < 32) {
+        const int64_t atom = (r0 / kQT) * (int64_t)(cols / kQT) + c0 / kQT;
+        reinterpret_cast<uint4*>(scales + atom * 512)[threadIdx.x] = reinterpret_cast<const uint4*>(s_atom)[threadIdx.x];
+    }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols, int axis, const int32_t* gofs,
+                                             int G, uint8_t* codes, uint8_t* scales, int32_t* err, void* stream) {
+    MOE_REQUIRE(x && codes && scales, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(rows >= 0 && cols > 0, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(rows % kQT == 0 && cols % kQT == 0, MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(rows / kQT <= 65535, MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(axis == MOE_QUANT_ROWWISE || axis == MOE_QUANT_COLWISE_GROUPED, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(gofs == nullptr || (G >= 1 && G <= 4096), MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(moe_aligned16(x) && moe_aligned16(codes) && moe_aligned16(scales), MOE_ERR_ALIGNMENT);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    if (rows == 0) return MOE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    dim3 grid(cols / kQT, (unsigned)(rows / kQT));
+    if (axis == MOE_QUANT_ROWWISE) {
+        k_quant_rows<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, (uint2*)codes, scales, err);
+    } else {
+        k_quant_cols<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, codes, scales, err);
+    }
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}

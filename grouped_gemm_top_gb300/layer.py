@@ -1,0 +1,198 @@
+"""MoELayer: the dropless-MoE fwd+bwd step as a fixed sequence of libmoe calls.
+
+Every buffer is allocated once, sized from (T, d, E, k, f) and the static row
+capacity, so the step allocates nothing, never reads counts on the host and
+can be captured in one CUDA graph ([TE-JAX] "What specialized optimizations
+are required for dropless MoE?": shapes must work while invisible to the CPU,
+to enable CUDA graphs).  The step follows [TE-JAX] Figure 3 (route, dispatch,
+two grouped GEMMs, combine) plus its backward.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import ops
+
+_SCORES = {"softmax": ops.MOE_SCORE_SOFTMAX, "sigmoid": ops.MOE_SCORE_SIGMOID}
+
+
+class MoELayer:
+    def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0"):
+        self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
+        self.score = _SCORES[score]
+        self.normalize = bool(normalize)
+        self.device = torch.device(device)
+        ops.moe_init(self.device.index or 0)
+        self.R = T * k
+        self.row_cap = ops.moe_row_capacity(T, E, k)
+        M, dev = self.row_cap, self.device
+
+        def z(shape, dtype):
+            return torch.zeros(shape, dtype=dtype, device=dev)
+
+        # inputs (resident)
+        self.logits = z((T, E), torch.float32)
+        self.x = z((T, d), torch.bfloat16)
+        self.dout = z((T, d), torch.bfloat16)
+        # routing / layout
+        self.err = z((1,), torch.int32)
+        self.topk_idx = z((T, k), torch.int32)
+        self.topk_w = z((T, k), torch.float32)
+        self.counts = z((E,), torch.int32)
+        self.offsets = z((E + 1,), torch.int32)
+        self.gofs = z((E + 1,), torch.int32)
+        self.slot_of = z((T, k), torch.int32)
+        self.row_id = z((M,), torch.int32)
+        self.ws_route = z((ops.moe_route_workspace_size(T, E),), torch.uint8)
+        self.ws_perm = z((ops.moe_permute_workspace_size(T, E),), torch.uint8)
+        # forward activations
+        self.x_perm = z((M, d), torch.bfloat16)
+        self.xq, self.xs = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
+        self.a_pre = z((M, 2 * f), torch.bfloat16)
+        self.h = z((M, f), torch.bfloat16)
+        self.hq, self.hs = z((M, f), torch.uint8), z((ops.sf_bytes(M, f),), torch.uint8)
+        self.y_perm = z((M, d), torch.bfloat16)
+        self.out = z((T, d), torch.bfloat16)
+        # backward activations
+        self.dy_perm = z((M, d), torch.bfloat16)
+        self.dw = z((T, k), torch.float32)
+        self.dyq, self.dys = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
+        self.dyqT, self.dysT = z((d, M), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
+        self.hqT, self.hsT = z((f, M), torch.uint8), z((ops.sf_bytes(M, f),), torch.uint8)
+        self.dA = z((M, 2 * f), torch.bfloat16)
+        self.dAq, self.dAs = z((M, 2 * f), torch.uint8), z((ops.sf_bytes(M, 2 * f),), torch.uint8)
+        self.dAqT, self.dAsT = z((2 * f, M), torch.uint8), z((ops.sf_bytes(M, 2 * f),), torch.uint8)
+        self.xqT, self.xsT = z((d, M), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
+        self.dx_perm = z((M, d), torch.bfloat16)
+        self.dx = z((T, d), torch.bfloat16)
+        self.dlogits = z((T, E), torch.float32)
+        self.dW1 = z((E, d, 2 * f), torch.bfloat16)
+        self.dW2 = z((E, f, d), torch.bfloat16)
+        self.graph = None
+        self.weights_ready = False
+        # when a list, every grouped-GEMM launch of a step appends a pair of
+        # CUDA events recorded around it on the current stream
+        self.gemm_events = None
+
+    # ------------------------------------------------------------ weights --
+    def set_weights(self, W1, W2):
+        """Quantize bf16 W1 [E, d, 2f] and W2 [E, f, d] along both axes (done
+        once per weight update, outside the step)."""
+        E, d, f = self.E, self.d, self.f
+        dev = self.device
+        gofs_d = torch.arange(0, (E + 1) * d, d, dtype=torch.int32, device=dev)
+        gofs_f = torch.arange(0, (E + 1) * f, f, dtype=torch.int32, device=dev)
+        W1v = W1.reshape(E * d, 2 * f)
+        W2v = W2.reshape(E * f, d)
+        # fwd operands: blocks along the contraction axis (d for W1, f for W2)
+        self.W1f, self.W1f_s = ops.mxfp8_group_quantize(W1v, ops.MOE_QUANT_COLWISE_GROUPED, gofs_d, E, err=self.err)
+        self.W2f, self.W2f_s = ops.mxfp8_group_quantize(W2v, ops.MOE_QUANT_COLWISE_GROUPED, gofs_f, E, err=self.err)
+        # dgrad operands: blocks along the other axis (2f for W1, d for W2)
+        self.W1d, self.W1d_s = ops.mxfp8_group_quantize(W1v, ops.MOE_QUANT_ROWWISE, err=self.err)
+        self.W2d, self.W2d_s = ops.mxfp8_group_quantize(W2v, ops.MOE_QUANT_ROWWISE, err=self.err)
+        self.weights_ready = True
+
+    def _gemm(self, *args):
+        if self.gemm_events is None:
+            return ops.grouped_gemm_mxfp8(*args)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        r = ops.grouped_gemm_mxfp8(*args)
+        e.record()
+        self.gemm_events.append((s, e))
+        return r
+
+    # ------------------------------------------------------------- step ----
+    def forward_(self):
+        E, k, d, f, M = self.E, self.k, self.d, self.f, self.row_cap
+        err = self.err
+        ops.moe_route_topk(self.logits, k, self.score, self.normalize, self.topk_idx, self.topk_w, self.counts,
+                           self.offsets, self.ws_route, err)
+        ops.moe_permute(self.x, self.topk_idx, E, M, self.gofs, self.slot_of, self.row_id, self.x_perm, True,
+                        self.ws_perm, err)
+        ops.mxfp8_group_quantize(self.x_perm, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.xq, self.xs, err)
+        self._gemm(ops.MOE_GEMM_FWD, self.xq, self.xs, self.W1f, self.W1f_s, ops.MOE_B_NGK, self.gofs,
+                               E, M, 2 * f, d, ops.MOE_EPI_SWIGLU, None, self.a_pre, self.h, err)
+        ops.mxfp8_group_quantize(self.h, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.hq, self.hs, err)
+        self._gemm(ops.MOE_GEMM_FWD, self.hq, self.hs, self.W2f, self.W2f_s, ops.MOE_B_NGK, self.gofs,
+                               E, M, d, f, ops.MOE_EPI_NONE, None, self.y_perm, None, err)
+        ops.moe_unpermute_combine(self.y_perm, self.slot_of, self.topk_w, self.out, err)
+
+    def backward_(self):
+        E, d, f, M = self.E, self.d, self.f, self.row_cap
+        err = self.err
+        ops.moe_combine_bwd(self.dout, self.y_perm, self.slot_of, self.topk_w, self.row_id, self.gofs, E,
+                            self.dy_perm, self.dw, err)
+        ops.mxfp8_group_quantize(self.dy_perm, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.dyq, self.dys, err)
+        ops.mxfp8_group_quantize(self.dy_perm, ops.MOE_QUANT_COLWISE_GROUPED, self.gofs, E, self.dyqT, self.dysT,
+                                 err)
+        ops.mxfp8_group_quantize(self.h, ops.MOE_QUANT_COLWISE_GROUPED, self.gofs, E, self.hqT, self.hsT, err)
+        # dH = dY W2^T with the SwiGLU backward fused: dA = [dgate | dup]
+        self._gemm(ops.MOE_GEMM_DGRAD, self.dyq, self.dys, self.W2d, self.W2d_s, ops.MOE_B_GNK,
+                               self.gofs, E, M, f, d, ops.MOE_EPI_SWIGLU_BWD, self.a_pre, self.dA, None, err)
+        # dW2_g = H_g^T dY_g
+        self._gemm(ops.MOE_GEMM_WGRAD, self.hqT, self.hsT, self.dyqT, self.dysT, 0, self.gofs, E, f,
+                               d, M, ops.MOE_EPI_NONE, None, self.dW2, None, err)
+        ops.mxfp8_group_quantize(self.dA, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.dAq, self.dAs, err)
+        ops.mxfp8_group_quantize(self.dA, ops.MOE_QUANT_COLWISE_GROUPED, self.gofs, E, self.dAqT, self.dAsT, err)
+        ops.mxfp8_group_quantize(self.x_perm, ops.MOE_QUANT_COLWISE_GROUPED, self.gofs, E, self.xqT, self.xsT,
+                                 err)
+        # dX_perm = dA W1^T
+        self._gemm(ops.MOE_GEMM_DGRAD, self.dAq, self.dAs, self.W1d, self.W1d_s, ops.MOE_B_GNK,
+                               self.gofs, E, M, d, 2 * f, ops.MOE_EPI_NONE, None, self.dx_perm, None, err)
+        # dW1_g = X_g^T dA_g
+        self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, 0, self.gofs, E, d,
+                               2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, err)
+        ops.moe_unpermute_combine(self.dx_perm, self.slot_of, None, self.dx, err)
+        ops.moe_route_bwd(self.logits, self.topk_idx, self.dw, self.score, self.normalize, self.dlogits, err)
+
+    def step_(self):
+        """One fwd+bwd pass over the resident inputs (no allocation, no sync)."""
+        assert self.weights_ready, "set_weights() first"
+        self.forward_()
+        self.backward_()
+
+    # ------------------------------------------------------ CUDA graphs ----
+    def capture(self, warmup=1):
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                self.step_()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step_()
+        self.graph = g
+        return g
+
+    def replay(self):
+        if self.graph is None:
+            self.step_()
+        else:
+            self.graph.replay()
+
+    # ------------------------------------------------------- public API ----
+    def step(self, x, logits, dout, out_host=None, dx_host=None, dlogits_host=None):
+        """End-to-end step from host (or device) tensors: copy the inputs in,
+        run fwd+bwd, copy out, dx and dlogits back.  Returns those three."""
+        self.x.copy_(x, non_blocking=True)
+        self.logits.copy_(logits, non_blocking=True)
+        self.dout.copy_(dout, non_blocking=True)
+        self.replay()
+        outs = []
+        for dev_t, host_t in ((self.out, out_host), (self.dx, dx_host), (self.dlogits, dlogits_host)):
+            if host_t is None:
+                outs.append(dev_t.to("cpu"))
+            else:
+                host_t.copy_(dev_t, non_blocking=True)
+                outs.append(host_t)
+        return tuple(outs)
+
+    def check_err(self):
+        v = int(self.err.item())
+        if v != 0:
+            raise ops.MoEError("device", v)
+
+    def flops_per_step(self):
+        return 18.0 * self.R * self.d * self.f

@@ -1,0 +1,227 @@
+"""ctypes binding of libmoe.so: the same entry points as include/moe.h.
+
+Argument marshalling only -- every step runs in the library's CUDA kernels.
+Torch is used for device memory and the current stream.  If the shared
+library is missing the import of this module fails loudly; there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+# status codes (include/moe.h)
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_ALIGNMENT = 3
+MOE_ERR_WORKSPACE = 4
+MOE_ERR_CUDA = 5
+MOE_ERR_NOT_INITIALIZED = 6
+MOE_ERR_BAD_EXPERT = 16
+MOE_ERR_BAD_OFFSETS = 17
+MOE_ERR_DEVICE_TIMEOUT = 18
+MOE_ERR_CAPACITY = 19
+
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
+MOE_QUANT_ROWWISE, MOE_QUANT_COLWISE_GROUPED = 0, 1
+MOE_GEMM_FWD, MOE_GEMM_DGRAD, MOE_GEMM_WGRAD = 0, 1, 2
+MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD = 0, 1, 2
+MOE_B_GNK, MOE_B_NGK = 0, 1
+
+EXPORTS = [
+    "moe_abi_version", "moe_status_string", "moe_init", "moe_row_capacity",
+    "moe_route_workspace_size", "moe_permute_workspace_size", "moe_route_topk",
+    "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
+    "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd",
+]
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+
+_SIGS = {
+    "moe_abi_version": (_i32, []),
+    "moe_status_string": (ctypes.c_char_p, [_i32]),
+    "moe_init": (_i32, [_i32]),
+    "moe_row_capacity": (_i64, [_i32, _i32, _i32]),
+    "moe_route_workspace_size": (_sz, [_i32, _i32]),
+    "moe_permute_workspace_size": (_sz, [_i32, _i32]),
+    "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "moe_permute": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "mxfp8_group_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "grouped_gemm_mxfp8": (_i32, [_i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _i32, _vp, _vp,
+                                  _vp, _vp, _vp]),
+    "moe_unpermute_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_combine_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp]),
+    "moe_route_bwd": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: status {status} ({status_string(status)})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmoe.so not found at {LIB_PATH}; build it with grouped_gemm_top_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.moe_status_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != MOE_OK:
+        raise MoEError(fn, status)
+
+
+def _p(t):
+    """Device pointer of a tensor (or None for NULL)."""
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------ entry points --
+
+def moe_abi_version() -> int:
+    return lib.moe_abi_version()
+
+
+def moe_init(device: int = 0) -> None:
+    _check("moe_init", lib.moe_init(int(device)))
+
+
+def moe_row_capacity(T: int, E: int, k: int) -> int:
+    return int(lib.moe_row_capacity(T, E, k))
+
+
+def moe_route_workspace_size(T: int, E: int) -> int:
+    return int(lib.moe_route_workspace_size(T, E))
+
+
+def moe_permute_workspace_size(T: int, E: int) -> int:
+    return int(lib.moe_permute_workspace_size(T, E))
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def moe_route_topk(logits, k, score=MOE_SCORE_SOFTMAX, normalize=True, topk_idx=None, topk_w=None,
+                   counts=None, offsets=None, ws=None, err=None, stream=None):
+    T, E = logits.shape
+    topk_idx = topk_idx if topk_idx is not None else _empty((T, k), torch.int32, logits)
+    topk_w = topk_w if topk_w is not None else _empty((T, k), torch.float32, logits)
+    counts = counts if counts is not None else _empty((E,), torch.int32, logits)
+    offsets = offsets if offsets is not None else _empty((E + 1,), torch.int32, logits)
+    ws = ws if ws is not None else _empty((moe_route_workspace_size(T, E),), torch.uint8, logits)
+    _check("moe_route_topk", lib.moe_route_topk(_p(logits), T, E, k, int(score), int(bool(normalize)),
+                                                _p(topk_idx), _p(topk_w), _p(counts), _p(offsets), _p(ws),
+                                                ws.numel(), _p(err), _stream(stream)))
+    return topk_idx, topk_w, counts, offsets
+
+
+def moe_permute(x, topk_idx, E, row_cap=None, gofs=None, slot_of=None, row_id=None, x_perm=None,
+                want_x_perm=True, ws=None, err=None, stream=None):
+    T, k = topk_idx.shape
+    d = x.shape[1] if x is not None else 0
+    row_cap = row_cap if row_cap is not None else moe_row_capacity(T, E, k)
+    like = topk_idx
+    gofs = gofs if gofs is not None else _empty((E + 1,), torch.int32, like)
+    slot_of = slot_of if slot_of is not None else _empty((T, k), torch.int32, like)
+    row_id = row_id if row_id is not None else _empty((row_cap,), torch.int32, like)
+    if want_x_perm and x_perm is None:
+        x_perm = _empty((row_cap, d), torch.bfloat16, like)
+    ws = ws if ws is not None else _empty((moe_permute_workspace_size(T, E),), torch.uint8, like)
+    _check("moe_permute", lib.moe_permute(_p(x), T, d, E, k, _p(topk_idx), row_cap, _p(gofs), _p(slot_of),
+                                          _p(row_id), _p(x_perm) if want_x_perm else None, _p(ws), ws.numel(),
+                                          _p(err), _stream(stream)))
+    return gofs, slot_of, row_id, x_perm
+
+
+def sf_bytes(rows: int, cols: int) -> int:
+    """Bytes of the scale array of a [rows, cols] matrix quantized along cols."""
+    return rows * (cols // 32)
+
+
+def mxfp8_group_quantize(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, codes=None, scales=None, err=None,
+                         stream=None):
+    rows, cols = x.shape
+    if axis == MOE_QUANT_ROWWISE:
+        codes = codes if codes is not None else _empty((rows, cols), torch.uint8, x)
+    else:
+        codes = codes if codes is not None else _empty((cols, rows), torch.uint8, x)
+    scales = scales if scales is not None else _empty((sf_bytes(rows, cols),), torch.uint8, x)
+    _check("mxfp8_group_quantize", lib.mxfp8_group_quantize(_p(x), rows, cols, int(axis), _p(gofs), int(G),
+                                                            _p(codes), _p(scales), _p(err), _stream(stream)))
+    return codes, scales
+
+
+def grouped_gemm_mxfp8(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilogue=MOE_EPI_NONE,
+                       epi_aux=None, d=None, d2=None, err=None, stream=None):
+    """See include/moe.h.  Allocates d (and d2 for SwiGLU) when not given."""
+    if d is None:
+        if mode == MOE_GEMM_WGRAD:
+            d = _empty((G, M, N), torch.bfloat16, a)
+        elif epilogue == MOE_EPI_SWIGLU_BWD:
+            d = _empty((M, 2 * N), torch.bfloat16, a)
+        else:
+            d = _empty((M, N), torch.bfloat16, a)
+    if epilogue == MOE_EPI_SWIGLU and d2 is None:
+        d2 = _empty((M, N // 2), torch.bfloat16, a)
+    _check("grouped_gemm_mxfp8", lib.grouped_gemm_mxfp8(int(mode), _p(a), _p(a_sf), _p(b), _p(b_sf), int(b_layout),
+                                                        _p(gofs), int(G), int(M), int(N), int(K), int(epilogue),
+                                                        _p(epi_aux), _p(d), _p(d2), _p(err), _stream(stream)))
+    return (d, d2) if epilogue == MOE_EPI_SWIGLU else d
+
+
+def moe_unpermute_combine(y_perm, slot_of, topk_w, out=None, err=None, stream=None):
+    T, k = slot_of.shape
+    d = y_perm.shape[1]
+    out = out if out is not None else _empty((T, d), torch.bfloat16, y_perm)
+    _check("moe_unpermute_combine", lib.moe_unpermute_combine(_p(y_perm), _p(slot_of), _p(topk_w), T, d, k,
+                                                              _p(out), _p(err), _stream(stream)))
+    return out
+
+
+def moe_combine_bwd(dout, y_perm, slot_of, topk_w, row_id, gofs, E, dy_perm=None, dw=None, err=None, stream=None):
+    T, k = slot_of.shape
+    d = dout.shape[1]
+    row_cap = row_id.shape[0]
+    dy_perm = dy_perm if dy_perm is not None else _empty((row_cap, d), torch.bfloat16, dout)
+    dw = dw if dw is not None else _empty((T, k), torch.float32, dout)
+    _check("moe_combine_bwd", lib.moe_combine_bwd(_p(dout), _p(y_perm), _p(slot_of), _p(topk_w), _p(row_id),
+                                                  _p(gofs), T, d, k, E, row_cap, _p(dy_perm), _p(dw), _p(err),
+                                                  _stream(stream)))
+    return dy_perm, dw
+
+
+def moe_route_bwd(logits, topk_idx, dw, score=MOE_SCORE_SOFTMAX, normalize=True, dlogits=None, err=None,
+                  stream=None):
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    dlogits = dlogits if dlogits is not None else _empty((T, E), torch.float32, logits)
+    _check("moe_route_bwd", lib.moe_route_bwd(_p(logits), _p(topk_idx), _p(dw), T, E, k, int(score),
+                                              int(bool(normalize)), _p(dlogits), _p(err), _stream(stream)))
+    return dlogits

@@ -1,0 +1,261 @@
+/*
+ * moe.h -- C ABI of libmoe: the single-GPU hot path of dropless
+ * Mixture-of-Experts training on GB300 (sm_103a).
+ *
+ * Sources (by page title and section):
+ *   [TE-JAX] "NVIDIA Accelerates Dropless MoE Training in JAX Using Transformer
+ *            Engine": "What specialized optimizations are required for
+ *            dropless MoE?" (Figure 3), "Optimization 1: Grouped GEMM",
+ *            "Optimization 2: Expert parallelism to integrate Dispatch and
+ *            Combine".
+ *   [CH1]    AI Systems Performance Engineering ch.1 ("第一章：介绍与 AI 系统
+ *            概览"): §1.1 "数据精度" (FP8 E4M3 = 1+4+3 bits) and
+ *            "低精度格式的缩放机制" (MXFP8: one scale per block of 32);
+ *            §2.3.2 "MoE 推理优化" (combine = router-weighted sum).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer is DEVICE memory owned by the caller unless stated.  The
+ *   library never allocates, frees, synchronizes or copies to the host on
+ *   these calls, so each one may be captured in a CUDA graph.  `stream` is a
+ *   cudaStream_t (NULL = legacy default stream).  Grid sizes depend only on
+ *   the host integers passed in and on the SM count, never on device data.
+ * - Host-checkable problems (NULL pointers, sizes, 16-byte alignment,
+ *   workspace too small) return a status synchronously and launch nothing.
+ * - Problems found on the device (an expert index out of range, offsets that
+ *   are not monotone or not multiples of 128, a bounded wait that ran out)
+ *   are written once into the caller's int32 word `*err` with atomicCAS
+ *   (first error wins; the caller zeroes it and reads it when it chooses).
+ *   `err` may be NULL.  A kernel that detects such a problem skips the work
+ *   it cannot do safely; it never traps.
+ * - bf16 tensors are passed as void* (IEEE bfloat16, row-major).
+ * - Per-expert token counts stay on the device; nothing here reads them on
+ *   the host ([TE-JAX] "What specialized optimizations...": shapes must work
+ *   when they are not visible to the CPU, to allow CUDA graphs).
+ *
+ * Row layout of the permuted (expert-grouped) buffers
+ * ---------------------------------------------------
+ * Group (expert) e occupies rows [gofs[e], gofs[e+1]) of every permuted
+ * buffer, gofs[e] = sum_{h<e} ceil128(counts[h]).  Its first counts[e] rows
+ * are the routed (token, choice) pairs in token order; the rest (< 128 rows)
+ * are zero padding, so a 128-row GEMM tile never straddles two groups and a
+ * 32-row quantization block never crosses a group boundary.  An empty group
+ * has no rows.  Buffers are sized for moe_row_capacity(T, E, k) rows; rows at
+ * or beyond gofs[E] are never read or written by any call.
+ *
+ * MXFP8 tensors
+ * -------------
+ * codes: uint8 FP8 E4M3 (bias 7, max 448, S.1111.111 = NaN).
+ * scales: uint8 E8M0 (value 2^(b-127)), one per block of 32 elements along
+ * the quantized axis.  Scale rule: b = e + 127 with e the smallest integer
+ * such that amax <= 448 * 2^e (clamped to [-127, 127]); an all-zero block has
+ * b = 0.  Codes are round-to-nearest-even of x * 2^-e, sign kept.
+ *
+ * Scale layout ("atom layout", the tensor core's native order).  For a
+ * quantized matrix Q with R rows (R % 128 == 0) whose rows are split into
+ * 32-element blocks along C columns (C % 128 == 0), the scale of row r,
+ * block b (= column / 32) is at byte
+ *     ((b / 4) * (R / 128) + r / 128) * 512
+ *       + (r % 32) * 16 + ((r / 32) % 4) * 4 + (b % 4)
+ * i.e. one 512-byte atom per 128 rows x 4 blocks, atoms ordered by block
+ * group first.  A columnwise-quantized matrix is stored transposed (Q = X^T)
+ * and uses the same formula on Q.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL pointer or size out of range          */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape the kernels do not handle            */
+    MOE_ERR_ALIGNMENT = 3,     /* pointer or stride not 16-byte aligned      */
+    MOE_ERR_WORKSPACE = 4,     /* workspace too small                        */
+    MOE_ERR_CUDA = 5,          /* a CUDA runtime call failed                 */
+    MOE_ERR_NOT_INITIALIZED = 6, /* moe_init was not called for this device  */
+    /* device-side codes, written to *err */
+    MOE_ERR_BAD_EXPERT = 16,   /* topk_idx outside [0, E) or repeated in a row */
+    MOE_ERR_BAD_OFFSETS = 17,  /* group offsets not monotone / not 128-aligned /
+                                  beyond the buffer                         */
+    MOE_ERR_DEVICE_TIMEOUT = 18, /* a bounded wait inside a kernel gave up   */
+    MOE_ERR_CAPACITY = 19      /* padded rows exceed the buffer capacity     */
+} moe_status_t;
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
+typedef enum { MOE_QUANT_ROWWISE = 0, MOE_QUANT_COLWISE_GROUPED = 1 } moe_quant_axis_t;
+typedef enum { MOE_GEMM_FWD = 0, MOE_GEMM_DGRAD = 1, MOE_GEMM_WGRAD = 2 } moe_gemm_mode_t;
+typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1, MOE_EPI_SWIGLU_BWD = 2 } moe_epilogue_t;
+typedef enum {
+    MOE_B_GNK = 0,  /* codes [G][N][K]: rowwise-quantized (scales: atom layout of
+                       the [G*N, K] matrix)                                    */
+    MOE_B_NGK = 1   /* codes [N][G*K]: the columnwise (transposed) output of a
+                       [G*K, N] weight with group offsets g*K (scales: atom
+                       layout of the [N, G*K] matrix)                          */
+} moe_b_layout_t;
+
+/* Version of this ABI (major*100 + minor). */
+MOE_API int moe_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(int status);
+
+/* Select `device`, cache its SM count and set kernel attributes (large shared
+ * memory).  Idempotent; call it once per device before the first call on
+ * that device and outside any stream capture. */
+MOE_API moe_status_t moe_init(int device);
+
+/* Rows a permuted buffer needs: ceil128(T*k + 127*min(E, T*k)). */
+MOE_API int64_t moe_row_capacity(int T, int E, int k);
+
+/* Workspace bytes for moe_route_topk / moe_permute (device memory, any
+ * content on entry, clobbered). */
+MOE_API size_t moe_route_workspace_size(int T, int E);
+MOE_API size_t moe_permute_workspace_size(int T, int E);
+
+/*
+ * moe_route_topk -- the router's top-k ([TE-JAX] intro and "Optimization 2":
+ * the fused router kernels assign each token to its Top-K experts).
+ *   logits   [T, E] fp32.
+ *   topk_idx [T, k] int32 out: the k largest logits per token, in
+ *            descending order; equal logits go to the lower expert index.
+ *   topk_w   [T, k] fp32 out: score = softmax over all E (score 0) or
+ *            sigmoid (score 1); normalize != 0 divides by the sum over the
+ *            k chosen.
+ *   counts   [E] int32 out: pairs routed to each expert (sum = T*k).
+ *   offsets  [E+1] int32 out: exclusive prefix sum of counts (unpadded).
+ *   ws       >= moe_route_workspace_size(T, E) bytes.
+ * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), T >= 0.
+ */
+MOE_API moe_status_t moe_route_topk(const float* logits, int T, int E, int k, int score, int normalize,
+                            int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                            void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/*
+ * moe_permute -- local half of dispatch ([TE-JAX] "Optimization 2": tokens
+ * are permuted to their experts; local reordering part only).
+ *   x          [T, d] bf16 (d % 8 == 0, 16-byte aligned).
+ *   topk_idx   [T, k] int32 (from moe_route_topk or the caller).
+ *   row_cap    rows of the permuted buffers, >= moe_row_capacity(T, E, k).
+ *   gofs       [E+1] int32 out: padded group offsets (multiples of 128).
+ *   slot_of    [T, k] int32 out: row of pair (t, j) in the permuted buffers,
+ *              slot = gofs[e] + #{t' < t : e in topk_idx[t']} (token order).
+ *   row_id     [row_cap] int32 out: t*k + j for the row of pair (t, j), -1
+ *              for padding rows; rows >= gofs[E] untouched.
+ *   x_perm     [row_cap, d] bf16 out (may be NULL): x_perm[slot_of[t,j]] =
+ *              x[t]; padding rows are zero; rows >= gofs[E] untouched.
+ *   ws         >= moe_permute_workspace_size(T, E) bytes.
+ */
+MOE_API moe_status_t moe_permute(const void* x, int T, int d, int E, int k, const int32_t* topk_idx,
+                         int64_t row_cap, int32_t* gofs, int32_t* slot_of, int32_t* row_id,
+                         void* x_perm, void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/*
+ * mxfp8_group_quantize -- MXFP8 quantization, 1x32 blocks, E8M0 scales
+ * ([TE-JAX] "What specialized optimizations...": a group-aware MXFP8
+ * quantization; [CH1] "低精度格式的缩放机制").
+ *   x      [rows, cols] bf16, rows % 128 == 0, cols % 128 == 0.
+ *   axis   MOE_QUANT_ROWWISE: blocks along each row.  codes [rows, cols],
+ *          scales in the atom layout of the [rows, cols] matrix.
+ *          MOE_QUANT_COLWISE_GROUPED: blocks of 32 rows of one group along
+ *          each column.  codes [cols, rows] (transposed), scales in the atom
+ *          layout of that [cols, rows] matrix.  Each group's rows start at a
+ *          multiple of 128, so blocks restart at every group boundary and
+ *          the padding rows inside a group (zeros) pad its tail block.
+ *   gofs   [G+1] int32 (device) or NULL.  If given, rows >= gofs[G] are not
+ *          read and their codes/scales are not written; for the columnwise
+ *          axis gofs is validated (monotone, multiples of 128, <= rows).
+ */
+MOE_API moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols, int axis,
+                                  const int32_t* gofs, int G, uint8_t* codes, uint8_t* scales,
+                                  int32_t* err, void* stream);
+
+/*
+ * grouped_gemm_mxfp8 -- one launch for all experts' GEMMs, each over its own
+ * rows only ([TE-JAX] "Optimization 1: Grouped GEMM"), MXFP8 block-scaled
+ * operands, fp32 accumulation, bf16 output.  Group offsets are read on the
+ * device (no host copy of counts).  K-major fp8 operands; K % 128 == 0.
+ *
+ * MOE_GEMM_FWD / MOE_GEMM_DGRAD (same kernel; dgrad passes the weight copy
+ * quantized along the other axis):
+ *   a, a_sf   [M, K] rowwise codes/scales of the permuted activations;
+ *             M = row capacity (% 128 == 0); rows of group g are
+ *             [gofs[g], gofs[g+1]).
+ *   b, b_sf   the group weights B_g as [N, K] K-major blocks, b_layout.
+ *   out       row r of group g: D[r, n] = sum_k A[r, k] * B_g[n, k].
+ *   epilogue  MOE_EPI_NONE:       d = D [M, N] bf16.
+ *             MOE_EPI_SWIGLU:     (fwd up/gate) N = 2f with the gate in
+ *                                 B rows [0, f) and up in [f, 2f); d = a_pre
+ *                                 [M, N] bf16 (the GEMM result), d2 = h
+ *                                 [M, N/2] bf16, h = silu(gate) * up computed
+ *                                 from the fp32 accumulators.  f % 128 == 0.
+ *             MOE_EPI_SWIGLU_BWD: (dgrad down) N = f, D = dH;
+ *                                 epi_aux = a_pre [M, 2N] bf16; d = dA
+ *                                 [M, 2N] bf16 = [dgate | dup] with
+ *                                 dgate = dH*u*s*(1+g*(1-s)), dup = dH*g*s,
+ *                                 s = sigmoid(g).
+ *             N % 256 == 0 for every epilogue.
+ * MOE_GEMM_WGRAD:
+ *   a, a_sf   [M, K] columnwise codes (the transposed left operand, e.g.
+ *             h^T); K = row capacity; group g contracts over columns
+ *             [gofs[g], gofs[g+1]).
+ *   b, b_sf   [N, K] columnwise codes of the right operand (b_layout unused).
+ *   d         [G, M, N] bf16: d[g] = A_g * B_g^T over the group's rows;
+ *             an empty group writes zeros.  M % 128 == 0, N % 256 == 0.
+ * d, d2, epi_aux: 16-byte aligned.  Launch: one persistent CTA per SM.
+ */
+MOE_API moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t* a_sf,
+                                const uint8_t* b, const uint8_t* b_sf, int b_layout,
+                                const int32_t* gofs, int G, int64_t M, int N, int64_t K,
+                                int epilogue, const void* epi_aux, void* d, void* d2,
+                                int32_t* err, void* stream);
+
+/*
+ * moe_unpermute_combine -- local half of combine ([TE-JAX] "Optimization 2":
+ * per-expert results are accumulated and restored to token order; [CH1]
+ * §2.3.2: a sum weighted by the routing weights).
+ *   out[t] = sum_{j<k} w[t, j] * y_perm[slot_of[t, j]]  (fp32 sum in j
+ *   order, bf16 out).  topk_w == NULL means weights of 1 (the unpermute-sum
+ *   used for dx).  y_perm [*, d] bf16, out [T, d] bf16, d % 8 == 0.
+ */
+MOE_API moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t* slot_of, const float* topk_w,
+                                   int T, int d, int k, void* out, int32_t* err, void* stream);
+
+/*
+ * moe_combine_bwd -- adjoint of the weighted combine.
+ *   dy_perm[slot_of[t, j]] = bf16(w[t, j] * dout[t]); padding rows (row_id
+ *   == -1, below gofs[E]) are written as zeros.
+ *   dw[t, j] = <dout[t], y_perm[slot_of[t, j]]> (fp32).
+ */
+MOE_API moe_status_t moe_combine_bwd(const void* dout, const void* y_perm, const int32_t* slot_of,
+                             const float* topk_w, const int32_t* row_id, const int32_t* gofs,
+                             int T, int d, int k, int E, int64_t row_cap, void* dy_perm, float* dw,
+                             int32_t* err, void* stream);
+
+/*
+ * moe_route_bwd -- gradient of the routing weights with respect to the
+ * logits.  dlogits [T, E] fp32 out (every entry written).
+ *   softmax+normalize: dl_i = w_i (dw_i - sum_j w_j dw_j) on the chosen, 0 else
+ *   softmax raw:       dl_m = p_m ([m chosen] dw_m - sum_j p_j dw_j) for all m
+ *   sigmoid+normalize: dl_i = s_i (1-s_i) (dw_i - sum_j w_j dw_j) / sum s
+ *   sigmoid raw:       dl_i = s_i (1-s_i) dw_i on the chosen, 0 else
+ */
+MOE_API moe_status_t moe_route_bwd(const float* logits, const int32_t* topk_idx, const float* dw,
+                           int T, int E, int k, int score, int normalize, float* dlogits,
+                           int32_t* err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,106 @@
+"""Test-side helpers: layout conversions documented in include/moe.h and the
+comparison rules of the parity tests.  No step of the method lives here."""
+from __future__ import annotations
+
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import oracle as O  # noqa: E402
+
+
+def atoms_to_rowmajor(atoms, rows, cols):
+    """Scale atoms (moe.h "atom layout") of a [rows, cols] matrix quantized
+    along cols -> canonical [rows, cols/32] uint8."""
+    atoms = np.asarray(atoms, dtype=np.uint8).reshape(-1)
+    nb = cols // 32
+    r = np.arange(rows)[:, None]
+    b = np.arange(nb)[None, :]
+    off = ((b // 4) * (rows // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
+    return atoms[off]
+
+
+def atoms_rows_subset(atoms, rows, cols, row_idx):
+    """Canonical scales of selected rows only."""
+    atoms = np.asarray(atoms, dtype=np.uint8).reshape(-1)
+    nb = cols // 32
+    r = np.asarray(row_idx)[:, None]
+    b = np.arange(nb)[None, :]
+    off = ((b // 4) * (rows // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
+    return atoms[off]
+
+
+def to_np(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy()
+
+
+def assert_bf16_close(gpu, ref64, rel_frob=1e-3, elem=1e-2, what=""):
+    """GPU bf16 result vs the fp64 oracle.
+
+    Rule: relative Frobenius error <= 1e-3 against the oracle rounded once to
+    the output type (bf16), and per element |gpu - ref| <= 1e-2 (|ref| +
+    rms(ref)) against the unrounded fp64 oracle.
+    """
+    g = gpu if isinstance(gpu, np.ndarray) else to_np(gpu)
+    ref64 = np.asarray(ref64, dtype=np.float64)
+    assert g.shape == ref64.shape, (what, g.shape, ref64.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU values"
+    nref = np.linalg.norm(ref64)
+    if nref == 0:
+        assert np.all(g == 0), f"{what}: expected zeros"
+        return 0.0
+    frob = np.linalg.norm(g - O.bf16_round(ref64)) / nref
+    rms = np.sqrt(np.mean(ref64 ** 2))
+    bad = np.abs(g - ref64) > elem * (np.abs(ref64) + rms)
+    assert frob <= rel_frob, f"{what}: relative Frobenius error {frob:.3e} > {rel_frob}"
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside 1e-2(|ref|+rms); first at "
+                           f"{np.argwhere(bad)[0]}: gpu {g[tuple(np.argwhere(bad)[0])]} ref "
+                           f"{ref64[tuple(np.argwhere(bad)[0])]}")
+    return frob
+
+
+def build_lib():
+    from grouped_gemm_top_gb300 import build
+    return build.build()
+
+
+def deq_rows(codes, atoms, rows_total, cols, row_idx):
+    """fp64 dequantized rows `row_idx` of a rowwise-quantized [rows_total,
+    cols] matrix stored as codes + scale atoms (oracle dequantizer)."""
+    codes = np.asarray(codes)
+    row_idx = np.asarray(row_idx)
+    sc = atoms_rows_subset(atoms, rows_total, cols, row_idx)
+    return O.mxfp8_dequantize_rows(codes[row_idx], sc)
+
+
+def gpu_ops():
+    """Build (if needed), load and initialise libmoe on cuda:0."""
+    build_lib()
+    from grouped_gemm_top_gb300 import ops
+    ops.moe_init(0)
+    return ops
+
+
+def padded_layout(sizes, align=128):
+    sizes = np.asarray(sizes, dtype=np.int64)
+    gofs = np.concatenate([[0], np.cumsum((sizes + align - 1) // align * align)])
+    return gofs
+
+
+def assert_fp32_close(gpu, ref64, rel_frob=1e-5, what=""):
+    """fp32 GPU result (no bf16 output rounding) vs the fp64 oracle:
+    relative Frobenius error <= 1e-5 (fp32 accumulation order only)."""
+    g = np.asarray(gpu if isinstance(gpu, np.ndarray) else gpu.double().cpu().numpy(), dtype=np.float64)
+    ref64 = np.asarray(ref64, dtype=np.float64)
+    assert g.shape == ref64.shape and np.all(np.isfinite(g)), what
+    frob = np.linalg.norm(g - ref64) / max(np.linalg.norm(ref64), 1e-300)
+    assert frob <= rel_frob, f"{what}: relative Frobenius error {frob:.3e} > {rel_frob}"
+    return frob

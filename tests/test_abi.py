@@ -1,0 +1,76 @@
+"""CPU checks of the C ABI: the library builds, loads, and exports every
+entry point declared in include/moe.h; host-side argument checks work
+without a GPU (no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from helpers import ROOT, build_lib
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    return build_lib()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_header_declares_the_entry_points():
+    names = set(_declared())
+    for n in ("moe_route_topk", "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
+              "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_init"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_binding_matches_header(lib_path):
+    from grouped_gemm_top_gb300 import ops
+    assert set(ops.EXPORTS) == set(_declared())
+    assert ops.moe_abi_version() == 100
+
+
+def test_host_only_calls_and_argument_checks(lib_path):
+    from grouped_gemm_top_gb300 import ops
+    lib = ops.lib
+    assert ops.moe_row_capacity(256, 8, 2) == 1536            # ceil128(512 + 127*8)
+    assert ops.moe_row_capacity(24576, 256, 8) == 229120
+    assert ops.moe_row_capacity(1, 8, 2) == 256               # 2 pairs: at most 2 groups of 128 rows
+    assert ops.moe_route_workspace_size(24576, 256) == 192 * 256 * 4
+    assert ops.status_string(ops.MOE_ERR_BAD_OFFSETS).startswith("group offsets")
+    # NULL pointers / bad sizes are rejected before any device work
+    st = lib.moe_route_topk(None, 16, 8, 2, 0, 1, None, None, None, None, None, 0, None, None)
+    assert st == ops.MOE_ERR_INVALID_ARG
+    st = lib.moe_route_topk(None, 16, 8, 9, 0, 1, None, None, None, None, None, 0, None, None)
+    assert st == ops.MOE_ERR_INVALID_ARG
+    st = lib.mxfp8_group_quantize(ctypes.c_void_p(16), 100, 128, 0, None, 0, ctypes.c_void_p(16),
+                                  ctypes.c_void_p(16), None, None)
+    assert st == ops.MOE_ERR_UNSUPPORTED                       # rows % 128 != 0
+    st = lib.grouped_gemm_mxfp8(0, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                ctypes.c_void_p(16), 0, ctypes.c_void_p(16), 4, 256, 200, 256, 0, None,
+                                ctypes.c_void_p(16), None, None, None)
+    assert st == ops.MOE_ERR_UNSUPPORTED                       # N % 256 != 0
+    st = lib.grouped_gemm_mxfp8(0, ctypes.c_void_p(8), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                ctypes.c_void_p(16), 0, ctypes.c_void_p(16), 4, 256, 256, 256, 0, None,
+                                ctypes.c_void_p(16), None, None, None)
+    assert st == ops.MOE_ERR_ALIGNMENT
+
+
+def test_product_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "grouped_gemm_top_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                with open(os.path.join(dirpath, fn)) as f:
+                    src = f.read()
+                assert "oracle" not in re.sub(r"#.*|//.*", "", src).lower() or fn == "__init__.py", fn

@@ -1,0 +1,277 @@
+"""The whole layer (MoELayer: fwd + bwd) stage by stage against the oracle,
+CUDA-graph replay, and the larger workloads on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import (assert_bf16_close, assert_fp32_close, atoms_to_rowmajor, deq_rows, gpu_ops, to_np)
+from grouped_gemm_top_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    return gpu_ops()
+
+
+def _layer(ops, T, d, E, k, f, score, norm, zipf=None, seed_offset=0):
+    from grouped_gemm_top_gb300.layer import MoELayer
+    L = MoELayer(T, d, E, k, f, score, norm)
+    inp = synth.make_layer_inputs(T, d, E, f, "cuda", zipf_s=zipf, seed_offset=seed_offset)
+    L.set_weights(inp["W1"], inp["W2"])
+    L.logits.copy_(inp["logits"])
+    L.x.copy_(inp["x"])
+    L.dout.copy_(inp["dout"])
+    return L, inp
+
+
+def _w_fwd(L, which):
+    """Oracle B [E, K, N] from the fwd weight operand (columnwise codes)."""
+    E, d, f = L.E, L.d, L.f
+    if which == 1:
+        q, s, K, N = L.W1f, L.W1f_s, d, 2 * f
+    else:
+        q, s, K, N = L.W2f, L.W2f_s, f, d
+    deq = O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), N, E * K))
+    return deq.T.reshape(E, K, N)
+
+
+def _w_dgrad(L, which):
+    """Oracle B [E, K, N] for dgrad from the rowwise weight copy."""
+    E, d, f = L.E, L.d, L.f
+    if which == 1:     # dXp = dA W1^T: B_g = W1_g^T, [2f, d]
+        q, s, R, C = L.W1d, L.W1d_s, E * d, 2 * f
+        W = O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), R, C)).reshape(E, d, 2 * f)
+    else:              # dH = dY W2^T: B_g = W2_g^T, [d, f]
+        q, s, R, C = L.W2d, L.W2d_s, E * f, d
+        W = O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), R, C)).reshape(E, f, d)
+    return np.transpose(W, (0, 2, 1))
+
+
+def _deq_act(q, s, M, C):
+    return O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), M, C))
+
+
+def _deq_actT(q, s, C, M, Rp):
+    return O.mxfp8_dequantize_cols(q.cpu().numpy()[:, :Rp], atoms_to_rowmajor(s.cpu().numpy(), C, M)[:, :Rp // 32])
+
+
+@pytest.mark.parametrize("score,norm", [("softmax", True), ("sigmoid", True)])
+def test_tiny_layer_stagewise(ops, score, norm):
+    """Tiny dropless layer (T=256, d=512, E=8, top-2, f=256): every stage of
+    fwd and bwd against the oracle applied to the GPU's own stage inputs."""
+    T, d, E, k, f = 256, 512, 8, 2, 256
+    L, inp = _layer(ops, T, d, E, k, f, score, norm)
+    L.step_()
+    torch.cuda.synchronize()
+    L.check_err()
+    M = L.row_cap
+    logits = inp["logits"].cpu().numpy()
+    idx, w = O.route_topk(logits, k, score, norm)
+    assert np.array_equal(L.topk_idx.cpu().numpy(), idx)
+    assert np.max(np.abs(L.topk_w.cpu().numpy() - w)) <= 1e-6
+    slot_of, row_id = O.permute_slots(idx, E, 128)
+    gofs = O.aligned_group_offsets(O.group_counts(idx, E), 128)
+    Rp = int(gofs[-1])
+    assert np.array_equal(L.gofs.cpu().numpy(), gofs)
+    assert np.array_equal(L.slot_of.cpu().numpy(), slot_of)
+    xp = O.permute(to_np(inp["x"]), row_id, k)
+    assert np.array_equal(to_np(L.x_perm)[:Rp], xp)
+    # rowwise quantization of x_perm
+    rq, rs = O.mxfp8_quantize_rows(xp)
+    assert np.array_equal(L.xq.cpu().numpy()[:Rp], rq)
+    assert np.array_equal(atoms_to_rowmajor(L.xs.cpu().numpy(), M, d)[:Rp], rs)
+    # up/gate GEMM + SwiGLU
+    A = O.grouped_gemm(O.mxfp8_dequantize_rows(rq, rs), _w_fwd(L, 1), gofs)
+    assert_bf16_close(L.a_pre[:Rp], A, what="a_pre")
+    assert_bf16_close(L.h[:Rp], O.swiglu(A), what="h")
+    # h quantized from the GPU's bf16 h
+    hq, hs = O.mxfp8_quantize_rows(to_np(L.h)[:Rp])
+    assert np.array_equal(L.hq.cpu().numpy()[:Rp], hq)
+    Y = O.grouped_gemm(O.mxfp8_dequantize_rows(hq, hs), _w_fwd(L, 2), gofs)
+    assert_bf16_close(L.y_perm[:Rp], Y, what="y_perm")
+    wg = L.topk_w.cpu().numpy().astype(np.float64)
+    assert_bf16_close(L.out, O.combine(to_np(L.y_perm)[:Rp], slot_of, wg), what="out")
+    # ---- backward
+    dy, dw = O.combine_bwd(to_np(inp["dout"]), to_np(L.y_perm)[:Rp], slot_of, wg, Rp)
+    assert_bf16_close(L.dy_perm[:Rp], dy, what="dy_perm")
+    assert_fp32_close(L.dw, dw, what="dw")
+    dyg = to_np(L.dy_perm)[:Rp]
+    dq, ds = O.mxfp8_quantize_rows(dyg)
+    assert np.array_equal(L.dyq.cpu().numpy()[:Rp], dq)
+    dH = O.grouped_gemm(O.mxfp8_dequantize_rows(dq, ds), _w_dgrad(L, 2), gofs)
+    dA = O.swiglu_bwd(to_np(L.a_pre)[:Rp], dH)
+    assert_bf16_close(L.dA[:Rp], dA, what="dA")
+    # wgrad dW2 = h^T dy per group (columnwise operands)
+    Hh = _deq_actT(L.hqT, L.hsT, f, M, Rp)
+    DYh = _deq_actT(L.dyqT, L.dysT, d, M, Rp)
+    rq2, rs2, _ = O.mxfp8_quantize_cols_grouped(to_np(L.h)[:Rp], gofs)
+    assert np.array_equal(L.hqT.cpu().numpy()[:, :Rp], rq2)
+    dW2 = O.grouped_gemm_wgrad(Hh, DYh, gofs)
+    for g in range(E):
+        assert_bf16_close(L.dW2[g], dW2[g], what=f"dW2[{g}]")
+    daq, das = O.mxfp8_quantize_rows(to_np(L.dA)[:Rp])
+    assert np.array_equal(L.dAq.cpu().numpy()[:Rp], daq)
+    dXp = O.grouped_gemm(O.mxfp8_dequantize_rows(daq, das), _w_dgrad(L, 1), gofs)
+    assert_bf16_close(L.dx_perm[:Rp], dXp, what="dx_perm")
+    Xh = _deq_actT(L.xqT, L.xsT, d, M, Rp)
+    DAh = _deq_actT(L.dAqT, L.dAsT, 2 * f, M, Rp)
+    dW1 = O.grouped_gemm_wgrad(Xh, DAh, gofs)
+    for g in range(E):
+        assert_bf16_close(L.dW1[g], dW1[g], what=f"dW1[{g}]")
+    assert_bf16_close(L.dx, O.combine(to_np(L.dx_perm)[:Rp], slot_of, None), what="dx")
+    dl = O.route_bwd(logits, idx, L.dw.double().cpu().numpy(), score, norm)
+    got = L.dlogits.double().cpu().numpy()
+    assert np.max(np.abs(got - dl)) <= 1e-5 * (np.abs(dl).max() + 1e-30) + 1e-7
+
+
+def test_graph_replay_matches_eager(ops):
+    T, d, E, k, f = 256, 512, 8, 2, 256
+    L, inp = _layer(ops, T, d, E, k, f, "softmax", True)
+    L.step_()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (L.out, L.dx, L.dlogits, L.dW1, L.dW2)]
+    L.capture()
+    # new inputs through the captured buffers, then back to the first ones
+    L.logits.copy_(synth.make_logits(T, E, 5, "cuda"))
+    L.replay()
+    torch.cuda.synchronize()
+    assert not torch.equal(L.out, ref[0])
+    L.logits.copy_(inp["logits"])
+    L.replay()
+    torch.cuda.synchronize()
+    L.check_err()
+    for a, b in zip((L.out, L.dx, L.dlogits, L.dW1, L.dW2), ref):
+        assert torch.equal(a, b)
+
+
+def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
+    """Large workloads: exact routing/permute, sampled GEMM rows and
+    sampled wgrad entries (each over its full contraction)."""
+    T, d, E, k, f, M = L.T, L.d, L.E, L.k, L.f, L.row_cap
+    rng = np.random.default_rng(seed)
+    logits = inp["logits"].cpu().numpy()
+    idx, w = O.route_topk(logits, k, score, norm)
+    assert np.array_equal(L.topk_idx.cpu().numpy(), idx)
+    assert np.max(np.abs(L.topk_w.cpu().numpy() - w)) <= 1e-6
+    counts = O.group_counts(idx, E)
+    gofs = O.aligned_group_offsets(counts, 128)
+    assert np.array_equal(L.gofs.cpu().numpy(), gofs)
+    slot_of, row_id = O.permute_slots(idx, E, 128)
+    assert np.array_equal(L.slot_of.cpu().numpy(), slot_of)
+    Rp = int(gofs[-1])
+    gl = L.row_id[:Rp].cpu().numpy()
+    assert np.array_equal(gl, row_id)
+    valid = np.nonzero(row_id >= 0)[0]
+    rows = np.sort(rng.choice(valid, size=min(n_rows, len(valid)), replace=False))
+    grp = np.searchsorted(gofs, rows, side="right") - 1
+    rt = torch.from_numpy(rows).cuda()
+    # permute + quantize of the sampled rows
+    xp = O.permute(to_np(inp["x"]), row_id[rows], k)
+    assert np.array_equal(to_np(L.x_perm[rt]), xp)
+    rq, rs = O.mxfp8_quantize_rows(xp)
+    assert np.array_equal(L.xq[rt].cpu().numpy(), rq)
+    # per sampled row: the row's group weights
+    W1f, W2f = L.W1f.cpu().numpy(), L.W2f.cpu().numpy()
+    W1f_s, W2f_s = L.W1f_s.cpu().numpy(), L.W2f_s.cpu().numpy()
+    W1d, W2d = L.W1d.cpu().numpy(), L.W2d.cpu().numpy()
+    W1d_s, W2d_s = L.W1d_s.cpu().numpy(), L.W2d_s.cpu().numpy()
+
+    def b_fwd(q, s, g, K, N):   # columnwise codes [N, E*K] -> [K, N] of group g
+        cols = np.arange(g * K, (g + 1) * K)
+        sc = atoms_to_rowmajor(s, N, E * K)[:, g * K // 32:(g + 1) * K // 32]
+        return O.mxfp8_dequantize_rows(q[:, cols], sc).T
+
+    def b_dgrad(q, s, g, Rw, C):  # rowwise [E*Rw, C] -> B = W_g^T [C, Rw]
+        r = np.arange(g * Rw, (g + 1) * Rw)
+        return deq_rows(q, s, E * Rw, C, r).T
+
+    A_rows = O.mxfp8_dequantize_rows(rq, rs)
+    a_pre = np.zeros((len(rows), 2 * f))
+    y = np.zeros((len(rows), d))
+    hq_rows = L.hq[rt].cpu().numpy()
+    h_rows = to_np(L.h[rt])
+    hq_ref, hs_ref = O.mxfp8_quantize_rows(h_rows)
+    assert np.array_equal(hq_rows, hq_ref)
+    Hd = O.mxfp8_dequantize_rows(hq_ref, hs_ref)
+    dq_ref, ds_ref = O.mxfp8_quantize_rows(to_np(L.dy_perm[rt]))
+    assert np.array_equal(L.dyq[rt].cpu().numpy(), dq_ref)
+    DYd = O.mxfp8_dequantize_rows(dq_ref, ds_ref)
+    daq_ref, das_ref = O.mxfp8_quantize_rows(to_np(L.dA[rt]))
+    assert np.array_equal(L.dAq[rt].cpu().numpy(), daq_ref)
+    DAd = O.mxfp8_dequantize_rows(daq_ref, das_ref)
+    dH = np.zeros((len(rows), f))
+    dxp = np.zeros((len(rows), d))
+    for g in np.unique(grp):
+        sel = grp == g
+        a_pre[sel] = A_rows[sel] @ b_fwd(W1f, W1f_s, g, d, 2 * f)
+        y[sel] = Hd[sel] @ b_fwd(W2f, W2f_s, g, f, d)
+        dH[sel] = DYd[sel] @ b_dgrad(W2d, W2d_s, g, f, d)
+        dxp[sel] = DAd[sel] @ b_dgrad(W1d, W1d_s, g, d, 2 * f)
+    assert_bf16_close(L.a_pre[rt], a_pre, what="a_pre rows")
+    assert_bf16_close(L.h[rt], O.swiglu(a_pre), what="h rows")
+    assert_bf16_close(L.y_perm[rt], y, what="y_perm rows")
+    assert_bf16_close(L.dA[rt], O.swiglu_bwd(to_np(L.a_pre[rt]), dH), what="dA rows")
+    assert_bf16_close(L.dx_perm[rt], dxp, what="dx_perm rows")
+    # combine + combine bwd on sampled tokens
+    tok = np.sort(rng.choice(T, size=min(256, T), replace=False))
+    sl = slot_of[tok]
+    need = np.unique(sl.reshape(-1))
+    yfull = np.zeros((Rp, d))
+    yfull[need] = to_np(L.y_perm[torch.from_numpy(need).cuda()])
+    wg = L.topk_w.cpu().numpy().astype(np.float64)[tok]
+    assert_bf16_close(to_np(L.out)[tok], O.combine(yfull, sl, wg), what="out tokens")
+    _, rdw = O.combine_bwd(to_np(L.dout)[tok], yfull, sl, wg, Rp)
+    assert_fp32_close(L.dw.double().cpu().numpy()[tok], rdw, what="dw tokens")
+    dxf = np.zeros((Rp, d))
+    dxf[need] = to_np(L.dx_perm[torch.from_numpy(need).cuda()])
+    assert_bf16_close(to_np(L.dx)[tok], O.combine(dxf, sl, None), what="dx tokens")
+    # wgrad: sampled (g, m, n) entries over the full group contraction
+    nonempty = np.nonzero(counts)[0]
+    for which in (2, 1):
+        if which == 2:
+            aT, asT, bT, bsT, Mo, No, dW = L.hqT, L.hsT, L.dyqT, L.dysT, f, d, L.dW2
+        else:
+            aT, asT, bT, bsT, Mo, No, dW = L.xqT, L.xsT, L.dAqT, L.dAsT, d, 2 * f, L.dW1
+        gs = rng.choice(nonempty, size=min(4, len(nonempty)), replace=False)
+        for g in gs:
+            lo, hi = int(gofs[g]), int(gofs[g + 1])
+            ms = rng.choice(Mo, size=8, replace=False)
+            ns = rng.choice(No, size=8, replace=False)
+            aq = aT[torch.from_numpy(ms).cuda(), lo:hi].cpu().numpy()
+            bq = bT[torch.from_numpy(ns).cuda(), lo:hi].cpu().numpy()
+            asc = np.stack([atoms_to_rowmajor_rows(asT.cpu().numpy(), Mo, M, m, lo, hi) for m in ms])
+            bsc = np.stack([atoms_to_rowmajor_rows(bsT.cpu().numpy(), No, M, n, lo, hi) for n in ns])
+            Ah = O.mxfp8_dequantize_rows(aq, asc)      # [8, rows of g]
+            Bh = O.mxfp8_dequantize_rows(bq, bsc)
+            ref = Ah @ Bh.T
+            got = to_np(dW[g][torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()])
+            rms = np.sqrt(np.mean(ref ** 2)) + 1e-30
+            assert np.all(np.abs(got - ref) <= 1e-2 * (np.abs(ref) + rms)), (which, g)
+            assert np.linalg.norm(got - O.bf16_round(ref)) <= 1e-3 * np.linalg.norm(ref) + 1e-30
+        empty = np.nonzero(counts == 0)[0]
+        for g in empty[:3]:
+            assert torch.all(dW[g] == 0)
+
+
+def atoms_to_rowmajor_rows(atoms, rows, cols, r, lo, hi):
+    b = np.arange(lo // 32, hi // 32)
+    off = ((b // 4) * (rows // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
+    return atoms[off]
+
+
+@pytest.mark.parametrize("name,T,d,E,k,f,score,zipf", [
+    ("mixtral-shaped", 8192, 4096, 8, 2, 14336, "softmax", None),
+    ("deepseek-v3-shaped", 24576, 7168, 256, 8, 2048, "sigmoid", None),
+    ("deepseek-v3-zipf", 24576, 7168, 256, 8, 2048, "sigmoid", 1.2),
+])
+def test_large_layer_sampled(ops, name, T, d, E, k, f, score, zipf):
+    L, inp = _layer(ops, T, d, E, k, f, score, True, zipf=zipf)
+    L.step_()
+    torch.cuda.synchronize()
+    L.check_err()
+    _sampled_checks(L, inp, score, True)
+    del L, inp
+    torch.cuda.empty_cache()

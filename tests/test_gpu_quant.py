@@ -1,0 +1,124 @@
+"""MXFP8 quantization kernels vs the oracle: bit-exact codes and scales."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import atoms_to_rowmajor, atoms_rows_subset, gpu_ops, padded_layout, to_np
+from grouped_gemm_top_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    return gpu_ops()
+
+
+def _varied(rows, cols, seed):
+    """bf16 values whose 32-blocks span many binades, with zero blocks,
+    negative zeros and tiny values."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    x = torch.randn((rows, cols), generator=g, device="cuda")
+    blk_scale = torch.exp2(torch.randint(-40, 40, (rows, cols // 32), generator=g, device="cuda").float())
+    x = x * blk_scale.repeat_interleave(32, dim=1)
+    x[0, :32] = 0.0
+    x[1, :32] = -0.0
+    x[2, 32:64] *= 1e-36
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,cols", [(128, 128), (256, 512), (384, 7168)])
+def test_rowwise_bit_exact(ops, rows, cols):
+    x = _varied(rows, cols, seed=rows + cols)
+    q, s = ops.mxfp8_group_quantize(x, ops.MOE_QUANT_ROWWISE)
+    torch.cuda.synchronize()
+    rq, rs = O.mxfp8_quantize_rows(to_np(x))
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(atoms_to_rowmajor(s.cpu().numpy(), rows, cols), rs)
+
+
+def test_rowwise_every_bf16_value_at_unit_scale(ops):
+    """Every bf16 with |v| <= 448, in blocks whose max is 448 (scale 2^0): the
+    codes are the E4M3 round-to-nearest-even of each value."""
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    v = bits[torch.isfinite(bits) & (bits.abs() <= 448)]
+    n = v.numel()
+    per = 31
+    nblk = (n + per - 1) // per
+    blocks = torch.zeros((nblk, 32))
+    blocks[:, 0] = 448.0
+    flat = torch.zeros(nblk * per)
+    flat[:n] = v
+    blocks[:, 1:] = flat.view(nblk, per)
+    rows = ((nblk * 32 + 127) // 128 + 127) // 128 * 128
+    x = torch.zeros(rows * 128)
+    x[:nblk * 32] = blocks.reshape(-1)
+    x = x.view(rows, 128).to(torch.bfloat16).cuda()
+    q, s = ops.mxfp8_group_quantize(x, ops.MOE_QUANT_ROWWISE)
+    torch.cuda.synchronize()
+    rq, rs = O.mxfp8_quantize_rows(to_np(x))
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(atoms_to_rowmajor(s.cpu().numpy(), rows, 128), rs)
+
+
+def test_rowwise_skips_rows_beyond_groups(ops):
+    x = _varied(512, 256, seed=3)
+    gofs = torch.tensor([0, 128, 256], dtype=torch.int32, device="cuda")
+    q = torch.full((512, 256), 0xAB, dtype=torch.uint8, device="cuda")
+    s = torch.full((512 * 8,), 0xCD, dtype=torch.uint8, device="cuda")
+    ops.mxfp8_group_quantize(x, ops.MOE_QUANT_ROWWISE, gofs, 2, q, s)
+    torch.cuda.synchronize()
+    rq, rs = O.mxfp8_quantize_rows(to_np(x)[:256])
+    assert np.array_equal(q[:256].cpu().numpy(), rq)
+    assert torch.all(q[256:] == 0xAB)
+    assert np.array_equal(atoms_rows_subset(s.cpu().numpy(), 512, 256, np.arange(256)), rs)
+    assert np.all(atoms_rows_subset(s.cpu().numpy(), 512, 256, np.arange(256, 512)) == 0xCD)
+
+
+@pytest.mark.parametrize("sizes,cols", [([128], 128), ([5, 0, 130, 127, 1], 256), ([1000, 0, 300], 7168)])
+def test_colwise_grouped_bit_exact(ops, sizes, cols):
+    gofs = padded_layout(sizes)
+    Rp = int(gofs[-1])
+    rows = Rp + 256                                   # rows beyond the groups are not read
+    x = torch.zeros((rows, cols), dtype=torch.bfloat16, device="cuda")
+    src = _varied(max(128, (sum(sizes) + 127) // 128 * 128), cols, seed=7)
+    r = 0
+    for g, m in enumerate(sizes):
+        x[gofs[g]:gofs[g] + m] = src[r:r + m]
+        r += m
+    x[Rp:] = float("nan")                              # must not be read
+    gt = torch.tensor(gofs, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, s = ops.mxfp8_group_quantize(x, ops.MOE_QUANT_COLWISE_GROUPED, gt, len(sizes), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # oracle on the unpadded rows with the unpadded offsets: blocks restart at
+    # every group start, tails are zero padded
+    raw_offs = np.concatenate([[0], np.cumsum(sizes)])
+    xr = np.concatenate([to_np(x)[gofs[g]:gofs[g] + m] for g, m in enumerate(sizes)])
+    rq, rs, padded = O.mxfp8_quantize_cols_grouped(xr, raw_offs)
+    # the oracle pads each group to 32, the GPU layout to 128: compare block by block
+    qn = q.cpu().numpy()
+    sn = atoms_to_rowmajor(s.cpu().numpy(), cols, rows)
+    for g, m in enumerate(sizes):
+        nb = (m + 31) // 32
+        assert np.array_equal(qn[:, gofs[g]:gofs[g] + 32 * nb], rq[:, padded[g]:padded[g] + 32 * nb])
+        assert np.array_equal(sn[:, gofs[g] // 32:gofs[g] // 32 + nb], rs[:, padded[g] // 32:padded[g] // 32 + nb])
+        # whole padding blocks after the tail block are zero codes, scale byte 0
+        assert np.all(qn[:, gofs[g] + 32 * nb:gofs[g + 1]] == 0)
+        assert np.all(sn[:, gofs[g] // 32 + nb:gofs[g + 1] // 32] == 0)
+
+
+def test_colwise_rejects_bad_offsets(ops):
+    x = _varied(256, 128, seed=9)
+    q = torch.full((128, 256), 0xAB, dtype=torch.uint8, device="cuda")
+    s = torch.full((256 * 4,), 0xCD, dtype=torch.uint8, device="cuda")
+    for bad in ([0, 100, 256], [0, 256, 128], [0, 128, 384], [64, 128, 256]):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ops.mxfp8_group_quantize(x, ops.MOE_QUANT_COLWISE_GROUPED,
+                                 torch.tensor(bad, dtype=torch.int32, device="cuda"), 2, q, s, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == ops.MOE_ERR_BAD_OFFSETS
+        assert torch.all(q == 0xAB) and torch.all(s == 0xCD)
