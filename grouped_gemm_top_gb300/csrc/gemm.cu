@@ -24,41 +24,56 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <stdlib.h>
+
 #include "common.cuh"
 
 namespace moe {
 namespace gg {
 
-constexpr int BM = 128, BN = 256, BK = 128;   // BK in fp8 elements (= bytes)
-constexpr int STAGES = 4;
-constexpr int A_STAGE = BM * BK;              // 16 KB
-constexpr int B_STAGE = BN * BK;              // 32 KB
+constexpr int BM = 128, BK = 128;             // BK in fp8 elements (= bytes)
 constexpr int SFA_STAGE = 512;
-constexpr int SFB_STAGE = 1024;
-constexpr int THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM columns: accumulator 0..255; per pipeline stage s the scales of A at
-// 256 + 16 s (4 columns) and of B at 260 + 16 s (8 columns), so a stage's
-// scale columns are rewritten only after the MMAs that read them completed.
-constexpr uint32_t TMEM_ACC = 0, TMEM_SF0 = 256, TMEM_SF_STRIDE = 16;
-constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+constexpr uint32_t TMEM_SF_STRIDE = 16;       // TMEM columns of scales per pipeline stage
 constexpr int BAND = 8;                       // m-tiles per raster band
 constexpr int MAX_G = 1024;
+constexpr int EPI_WARPS = 8;                  // two warps per TMEM lane quarter
+constexpr int THREADS = 128 + 32 * EPI_WARPS;
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
-constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;   // full[S], empty[S], tmem_full, tmem_empty, drain
-constexpr int OFF_MISC = OFF_BAR + 8 * (2 * STAGES + 3);
-constexpr int OFF_GOFS = OFF_MISC + 16;
-constexpr int SMEM_BYTES = OFF_GOFS + (MAX_G + 1) * 4 + 1024;   // + alignment slack
+// Tile configurations.  BN = 128 keeps two accumulators in TMEM so the
+// epilogue of one tile overlaps the mainloop of the next; BN = 256 halves
+// the A re-reads but has a single accumulator.
+template <int BN_>
+struct Cfg {
+    static constexpr int BN = BN_;
+    static constexpr int NACC = BN_ == 128 ? 2 : 1;
+    static constexpr int STAGES = BN_ == 128 ? 6 : 4;
+    static constexpr int A_STAGE = BM * BK;
+    static constexpr int B_STAGE = BN_ * BK;
+    static constexpr int SFB_STAGE = (BN_ / 128) * 512;
+    static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+    // TMEM: accumulators at [0, NACC*BN); stage s scales at SF0 + 16 s (A: 4
+    // columns, B: BN/32 columns), so a stage's scale columns are rewritten
+    // only after the MMAs that read them completed.
+    static constexpr uint32_t SF0 = NACC * BN_;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
+    static constexpr int NBAR = 2 * STAGES + 2 * NACC + 1;
+    static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+    static constexpr int OFF_GOFS = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = OFF_GOFS + (MAX_G + 1) * 4 + 1024;   // + alignment slack
+    static_assert(SF0 + STAGES * TMEM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 struct Params {
     int mode, epi, G;
     int N;
     int64_t M, K;
-    int n_tiles;        // tiles along N (256 output columns, or 128 gate + 128 up)
+    int n_tiles;        // tiles along N
     int m_tiles;        // WGRAD: tiles along M per group
     const int32_t* gofs;
     const uint8_t* a_sf;
@@ -169,7 +184,8 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
 }
 
 // Instruction descriptor: E4M3 x E4M3, fp32 accumulate, K-major A and B,
-// E8M0 scales, M = 128, N = 256, scale byte `sf_id` of each 32-bit TMEM cell.
+// E8M0 scales, M = 128, N = BN, scale byte `sf_id` of each 32-bit TMEM cell.
+template <int BN>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
     return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
 }
@@ -222,11 +238,11 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v) {
 struct Tile {
     int g;            // group of the B operand (FWD/DGRAD) / output group (WGRAD)
     int64_t a_row;    // first row of the A box
-    int b_row0, b_row1;
+    int b_row;        // first row of the B boxes (BN consecutive rows)
     int64_t kbeg;     // first k-step (units of 128 along K)
     int nk;           // number of k-steps
     int64_t out_row;  // first output row
-    int out_col;      // first output column (gate column for SWIGLU)
+    int nt;           // tile index along N
 };
 
 __device__ __forceinline__ void band_decode(int64_t l, int64_t mtiles, int ntiles, int64_t& mt, int& nt) {
@@ -249,6 +265,7 @@ __device__ __forceinline__ int find_group(const int* s_gofs, int G, int64_t row)
     return lo;
 }
 
+template <int BN>
 __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int64_t total_mt, int64_t t, Tile& ti) {
     int64_t mt;
     int nt;
@@ -258,15 +275,6 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
         ti.g = find_group(s_gofs, p.G, row);
         ti.a_row = row;
         ti.out_row = row;
-        if (p.epi == MOE_EPI_SWIGLU) {
-            ti.b_row0 = nt * 128;
-            ti.b_row1 = p.N / 2 + nt * 128;
-            ti.out_col = nt * 128;
-        } else {
-            ti.b_row0 = nt * BN;
-            ti.b_row1 = nt * BN + 128;
-            ti.out_col = nt * BN;
-        }
         ti.kbeg = 0;
         ti.nk = (int)(p.K / BK);
     } else {
@@ -275,42 +283,45 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
         band_decode(t - (int64_t)g * tpg, p.m_tiles, p.n_tiles, mt, nt);
         ti.g = g;
         ti.a_row = mt * BM;
-        ti.b_row0 = nt * BN;
-        ti.b_row1 = nt * BN + 128;
         ti.kbeg = s_gofs[g] / BK;
         ti.nk = (s_gofs[g + 1] - s_gofs[g]) / BK;
         ti.out_row = (int64_t)g * p.M + mt * BM;
-        ti.out_col = nt * BN;
     }
+    ti.b_row = nt * BN;
+    ti.nt = nt;
 }
 
 // --------------------------------------------------------------- kernel ----
 
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    using C = Cfg<BN>;
+    constexpr int STAGES = C::STAGES, NACC = C::NACC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t tmem_full_bar = bar0 + 8u * (2 * STAGES);
-    const uint32_t tmem_empty_bar = bar0 + 8u * (2 * STAGES + 1);
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-    volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
-    int* s_gofs = reinterpret_cast<int*>(smem + OFF_GOFS);
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + NACC + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * NACC);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+    int* s_gofs = reinterpret_cast<int*>(smem + C::OFF_GOFS);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(tmem_full_bar, 1);
-        mbar_init(tmem_empty_bar, 4);
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), EPI_WARPS);
+        }
         mbar_init(drain_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *abort_flag = 0;
@@ -347,10 +358,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer ----
-        uint8_t* sA = smem + OFF_A;
-        uint8_t* sB = smem + OFF_B;
-        uint8_t* sSFA = smem + OFF_SFA;
-        uint8_t* sSFB = smem + OFF_SFB;
+        uint8_t* sA = smem + C::OFF_A;
+        uint8_t* sB = smem + C::OFF_B;
+        uint8_t* sSFA = smem + C::OFF_SFA;
+        uint8_t* sSFB = smem + C::OFF_SFB;
         int pend[STAGES];
         for (int s = 0; s < STAGES; ++s) pend[s] = -1;
         int stage = 0;
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool aborted = false;
         for (int64_t t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
             Tile ti;
-            get_tile(p, s_gofs, total_mt, t, ti);
+            get_tile<BN>(p, s_gofs, total_mt, t, ti);
             const int gB = p.mode == MOE_GEMM_WGRAD ? 0 : ti.g;
             for (int ks = 0; ks < ti.nk; ++ks) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, p, abort_flag)) {
@@ -368,15 +379,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t kg = ti.kbeg + ks;
                 const int kx = (int)(kg * BK);
                 const uint32_t fb = full_bar(stage);
-                mbar_expect_tx(fb, STAGE_TX);
-                tma_load_2d(smem_u32(sA + stage * A_STAGE), &tmA, kx, (int)ti.a_row, fb);
-                tma_load_3d(smem_u32(sB + stage * B_STAGE), &tmB, kx, ti.b_row0, gB, fb);
-                tma_load_3d(smem_u32(sB + stage * B_STAGE + B_STAGE / 2), &tmB, kx, ti.b_row1, gB, fb);
+                mbar_expect_tx(fb, C::STAGE_TX);
+                tma_load_2d(smem_u32(sA + stage * C::A_STAGE), &tmA, kx, (int)ti.a_row, fb);
                 const uint8_t* sfa = p.a_sf + kg * p.a_sf_kstride + (ti.a_row / 128) * 512;
                 const uint8_t* sfb = p.b_sf + (int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride;
                 bulk_load(smem_u32(sSFA + stage * SFA_STAGE), sfa, 512, fb);
-                bulk_load(smem_u32(sSFB + stage * SFB_STAGE), sfb + (int64_t)(ti.b_row0 / 128) * 512, 512, fb);
-                bulk_load(smem_u32(sSFB + stage * SFB_STAGE + 512), sfb + (int64_t)(ti.b_row1 / 128) * 512, 512, fb);
+#pragma unroll
+                for (int h = 0; h < BN / 128; ++h) {
+                    const int brow = ti.b_row + 128 * h;
+                    tma_load_3d(smem_u32(sB + stage * C::B_STAGE + h * 16384), &tmB, kx, brow, gB, fb);
+                    bulk_load(smem_u32(sSFB + stage * C::SFB_STAGE + h * 512), sfb + (int64_t)(brow / 128) * 512,
+                              512, fb);
+                }
                 pend[stage] = (int)phase;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -394,42 +408,43 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // --------------------------------------------------- MMA issuer ----
-        const uint8_t* sA = smem + OFF_A;
-        const uint8_t* sB = smem + OFF_B;
-        const uint8_t* sSFA = smem + OFF_SFA;
-        const uint8_t* sSFB = smem + OFF_SFB;
-        int stage = 0;
+        const uint8_t* sA = smem + C::OFF_A;
+        const uint8_t* sB = smem + C::OFF_B;
+        const uint8_t* sSFA = smem + C::OFF_SFA;
+        const uint8_t* sSFB = smem + C::OFF_SFB;
+        int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool aborted = false;
         bool issued = false;
         for (int64_t t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
             Tile ti;
-            get_tile(p, s_gofs, total_mt, t, ti);
+            get_tile<BN>(p, s_gofs, total_mt, t, ti);
             if (ti.nk == 0) continue;
-            if (!mbar_wait(tmem_empty_bar, acc_phase ^ 1u, p, abort_flag)) {
+            if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, p, abort_flag)) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int ks = 0; ks < ti.nk; ++ks) {
                 if (!mbar_wait(full_bar(stage), phase, p, abort_flag)) {
                     aborted = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t t_sfa = tmem_base + TMEM_SF0 + TMEM_SF_STRIDE * stage;
+                const uint32_t t_sfa = tmem_base + C::SF0 + TMEM_SF_STRIDE * stage;
                 const uint32_t t_sfb = t_sfa + 4;
                 tc_cp_sf(t_sfa, desc_sf(smem_u32(sSFA + stage * SFA_STAGE)));
-                tc_cp_sf(t_sfb, desc_sf(smem_u32(sSFB + stage * SFB_STAGE)));
-                tc_cp_sf(t_sfb + 4, desc_sf(smem_u32(sSFB + stage * SFB_STAGE + 512)));
-                const uint64_t adesc = desc_sw128(smem_u32(sA + stage * A_STAGE));
-                const uint64_t bdesc = desc_sw128(smem_u32(sB + stage * B_STAGE));
+#pragma unroll
+                for (int h = 0; h < BN / 128; ++h)
+                    tc_cp_sf(t_sfb + 4 * h, desc_sf(smem_u32(sSFB + stage * C::SFB_STAGE + 512 * h)));
+                const uint64_t adesc = desc_sw128(smem_u32(sA + stage * C::A_STAGE));
+                const uint64_t bdesc = desc_sw128(smem_u32(sB + stage * C::B_STAGE));
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk) {
                     // advance 32 bytes along K inside the 128-byte swizzled row
-                    tc_mma(tmem_base + TMEM_ACC, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
-                           make_idesc((uint32_t)kk), t_sfa, t_sfb,
-                           (ks | kk) != 0 ? 1u : 0u);
+                    tc_mma(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                           make_idesc<BN>((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
                 }
                 issued = true;
                 tc_commit(empty_bar(stage));
@@ -439,8 +454,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (aborted) break;
-            tc_commit(tmem_full_bar);
-            acc_phase ^= 1u;
+            tc_commit(tfull_bar(acc));
+            if (++acc == NACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
         }
         if (issued) {
             // every MMA issued by this thread completes before TMEM is freed
@@ -452,45 +470,54 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp >= 4) {
         // ----------------------------------------------------- epilogue ----
+        // warp (4 + e): TMEM lane quarter e % 4, column half e / 4
         const int ew = warp - 4;
+        const int quarter = ew & 3, half = ew >> 2;
+        int acc = 0;
         uint32_t acc_phase = 0;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(ew * 32) << 16);
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
             Tile ti;
-            get_tile(p, s_gofs, total_mt, t, ti);
-            const int64_t row = ti.out_row + ew * 32 + lane;
+            get_tile<BN>(p, s_gofs, total_mt, t, ti);
+            const int64_t row = ti.out_row + quarter * 32 + lane;
             if (ti.nk == 0) {   // WGRAD of an empty group: the gradient is zero
                 float z[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) z[i] = 0.f;
-                for (int c = 0; c < BN / 32; ++c) store_row32(p.d + row * p.N + ti.out_col + 32 * c, z);
+                for (int c = 0; c < BN / 64; ++c)
+                    store_row32(p.d + row * p.N + ti.nt * BN + half * (BN / 2) + 32 * c, z);
                 continue;
             }
-            if (!mbar_wait(tmem_full_bar, acc_phase, p, abort_flag)) break;
+            if (!mbar_wait(tfull_bar(acc), acc_phase, p, abort_flag)) break;
             tc_fence_after();
+            const uint32_t tacc = lane_base + (uint32_t)(acc * BN);
             float v[32];
             if (p.epi == MOE_EPI_SWIGLU) {
+                // B rows interleave gate/up in 64-row chunks: accumulator
+                // columns [128q, 128q+64) are gate, [128q+64, 128q+128) up
                 const int64_t N = p.N, f = p.N / 2;
-                for (int c = 0; c < 4; ++c) {
-                    float u[32], h[32];
-                    tmem_ld32(lane_base + TMEM_ACC + 32 * c, v);          // gate
-                    tmem_ld32(lane_base + TMEM_ACC + 128 + 32 * c, u);    // up
-                    const int64_t col = ti.out_col + 32 * c;
-                    store_row32(p.d + row * N + col, v);
-                    store_row32(p.d + row * N + f + col, u);
+                for (int u = half * (BN / 128); u < (half + 1) * (BN / 128); ++u) {
+                    const int q = u >> 1, c = u & 1;
+                    float up[32], h[32];
+                    tmem_ld32(tacc + 128 * q + 32 * c, v);
+                    tmem_ld32(tacc + 128 * q + 64 + 32 * c, up);
+                    const int64_t hcol = (int64_t)ti.nt * (BN / 2) + 64 * q + 32 * c;
+                    store_row32(p.d + row * N + hcol, v);
+                    store_row32(p.d + row * N + f + hcol, up);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const float s = 1.f / (1.f + expf(-v[i]));
-                        h[i] = v[i] * s * u[i];
+                        h[i] = v[i] * s * up[i];
                     }
-                    store_row32(p.d2 + row * f + col, h);
+                    store_row32(p.d2 + row * f + hcol, h);
                 }
             } else if (p.epi == MOE_EPI_SWIGLU_BWD) {
                 const int64_t N = p.N, ld = 2 * (int64_t)p.N;
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < BN / 64; ++c) {
                     float g[32], u[32], dg[32], du[32];
-                    tmem_ld32(lane_base + TMEM_ACC + 32 * c, v);          // dH
-                    const int64_t col = ti.out_col + 32 * c;
+                    const int col32 = half * (BN / 2) + 32 * c;
+                    tmem_ld32(tacc + col32, v);          // dH
+                    const int64_t col = (int64_t)ti.nt * BN + col32;
                     load_row32(p.aux + row * ld + col, g);
                     load_row32(p.aux + row * ld + N + col, u);
 #pragma unroll
@@ -503,15 +530,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                     store_row32(p.d + row * ld + N + col, du);
                 }
             } else {
-                for (int c = 0; c < BN / 32; ++c) {
-                    tmem_ld32(lane_base + TMEM_ACC + 32 * c, v);
-                    store_row32(p.d + row * p.N + ti.out_col + 32 * c, v);
+                for (int c = 0; c < BN / 64; ++c) {
+                    const int col32 = half * (BN / 2) + 32 * c;
+                    tmem_ld32(tacc + col32, v);
+                    store_row32(p.d + row * p.N + (int64_t)ti.nt * BN + col32, v);
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tmem_empty_bar);
-            acc_phase ^= 1u;
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == NACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
         }
     }
 
@@ -539,7 +570,22 @@ cudaError_t gemm_init_driver() {
 }
 
 cudaError_t gemm_set_attributes() {
-    return cudaFuncSetAttribute(gg::k_grouped_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gg::k_grouped_gemm<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         gg::Cfg<128>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gg::k_grouped_gemm<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gg::Cfg<256>::SMEM_BYTES);
+}
+
+// Tile width used by grouped_gemm_mxfp8: 128 (two TMEM accumulators) unless
+// the environment variable MOE_GEMM_BN=256 selects the single-accumulator
+// 256-wide tile (kept for measurement).
+static int gemm_bn() {
+    static int bn = [] {
+        const char* e = getenv("MOE_GEMM_BN");
+        return (e != nullptr && atoi(e) == 256) ? 256 : 128;
+    }();
+    return bn;
 }
 
 // rank-2/3 uint8 tensor map, 128x128 boxes, 128-byte swizzle
@@ -566,7 +612,8 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD || mode == MOE_GEMM_WGRAD, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(a && a_sf && b && b_sf && gofs && d, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(G >= 1 && G <= MAX_G && M > 0 && N > 0 && K > 0, MOE_ERR_INVALID_ARG);
-    MOE_REQUIRE(M % 128 == 0 && K % BK == 0 && N % BN == 0, MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(M % 128 == 0 && K % BK == 0 && N % 128 == 0, MOE_ERR_UNSUPPORTED);
+    const int BN = (gemm_bn() == 256 && N % 256 == 0) ? 256 : 128;
     MOE_REQUIRE(K <= 0x7FFFFF80LL && M <= 0x7FFFFF80LL, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(moe_aligned16(a) && moe_aligned16(b) && moe_aligned16(a_sf) && moe_aligned16(b_sf) &&
                     moe_aligned16(d) && (d2 == nullptr || moe_aligned16(d2)) &&
@@ -578,7 +625,7 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
         MOE_REQUIRE(b_layout == MOE_B_GNK || b_layout == MOE_B_NGK, MOE_ERR_INVALID_ARG);
         MOE_REQUIRE(epilogue == MOE_EPI_NONE || epilogue == MOE_EPI_SWIGLU || epilogue == MOE_EPI_SWIGLU_BWD,
                     MOE_ERR_INVALID_ARG);
-        if (epilogue == MOE_EPI_SWIGLU) MOE_REQUIRE(d2 != nullptr && (N / 2) % 128 == 0, MOE_ERR_INVALID_ARG);
+        if (epilogue == MOE_EPI_SWIGLU) MOE_REQUIRE(d2 != nullptr, MOE_ERR_INVALID_ARG);
         if (epilogue == MOE_EPI_SWIGLU_BWD) MOE_REQUIRE(epi_aux != nullptr, MOE_ERR_INVALID_ARG);
     }
     MOE_REQUIRE(device_initialized() && g_encode != nullptr, MOE_ERR_NOT_INITIALIZED);
@@ -634,7 +681,10 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     const int sms = device_sm_count();
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     const int grid = (int)(upper_tiles < sms ? (upper_tiles > 0 ? upper_tiles : 1) : sms);
-    k_grouped_gemm<<<grid, THREADS, SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);
+    if (BN == 256)
+        k_grouped_gemm<256><<<grid, THREADS, Cfg<256>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);
+    else
+        k_grouped_gemm<128><<<grid, THREADS, Cfg<128>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }

@@ -73,9 +73,13 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint4* __restrict__ x,
 
 // Columnwise, group-aware: tile = 128 input rows (4 blocks of 32 rows, all in
 // one group because groups start at multiples of 128) x 128 input columns.
-// Output is transposed: codes [cols, rows].
+// Output is transposed: codes [cols, rows]; CTA x writes output rows
+// [128 x, 128 x + 128).  With `glu`, output rows interleave the two column
+// halves in 64-row chunks: output rows [128 j, 128 j + 64) are input columns
+// [64 j, 64 j + 64) and rows [128 j + 64, 128 j + 128) are input columns
+// [cols/2 + 64 j, cols/2 + 64 j + 64).
 __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x, int64_t rows, int cols,
-                                                    const int32_t* __restrict__ gofs, int G,
+                                                    const int32_t* __restrict__ gofs, int G, int glu,
                                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                     int32_t* err) {
     // the input tile [row][col] and, after it has been consumed, the output
@@ -102,7 +106,9 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x,
     for (int p = 0; p < 8; ++p) {
         const int idx = threadIdx.x + 256 * p;
         const int rl = idx >> 4, cv = idx & 15;
-        const uint4 v = __ldg(x + (r0 + rl) * cols8 + (c0 >> 3) + cv);
+        const int src8 = glu ? (cv < 8 ? 8 * blockIdx.x + cv : (cols >> 4) + 8 * blockIdx.x + cv - 8)
+                             : (c0 >> 3) + cv;
+        const uint4 v = __ldg(x + (r0 + rl) * cols8 + src8);
         *reinterpret_cast<uint4*>(&s_x[rl][cv * 8]) = v;
     }
     __syncthreads();
@@ -166,7 +172,8 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
     MOE_REQUIRE(rows >= 0 && cols > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(rows % kQT == 0 && cols % kQT == 0, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(rows / kQT <= 65535, MOE_ERR_UNSUPPORTED);
-    MOE_REQUIRE(axis == MOE_QUANT_ROWWISE || axis == MOE_QUANT_COLWISE_GROUPED, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(axis == MOE_QUANT_ROWWISE || axis == MOE_QUANT_COLWISE_GROUPED || axis == MOE_QUANT_COLWISE_GLU,
+                MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(gofs == nullptr || (G >= 1 && G <= 4096), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(moe_aligned16(x) && moe_aligned16(codes) && moe_aligned16(scales), MOE_ERR_ALIGNMENT);
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
@@ -176,7 +183,8 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
     if (axis == MOE_QUANT_ROWWISE) {
         k_quant_rows<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, (uint2*)codes, scales, err);
     } else {
-        k_quant_cols<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, codes, scales, err);
+        k_quant_cols<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, axis == MOE_QUANT_COLWISE_GLU ? 1 : 0,
+                                          codes, scales, err);
     }
     MOE_CHECK_LAUNCH();
     return MOE_OK;

@@ -85,7 +85,8 @@ class MoELayer:
         W1v = W1.reshape(E * d, 2 * f)
         W2v = W2.reshape(E * f, d)
         # fwd operands: blocks along the contraction axis (d for W1, f for W2)
-        self.W1f, self.W1f_s = ops.mxfp8_group_quantize(W1v, ops.MOE_QUANT_COLWISE_GROUPED, gofs_d, E, err=self.err)
+        # (W1's gate/up halves interleaved in 64-row chunks for the SwiGLU epilogue)
+        self.W1f, self.W1f_s = ops.mxfp8_group_quantize(W1v, ops.MOE_QUANT_COLWISE_GLU, gofs_d, E, err=self.err)
         self.W2f, self.W2f_s = ops.mxfp8_group_quantize(W2v, ops.MOE_QUANT_COLWISE_GROUPED, gofs_f, E, err=self.err)
         # dgrad operands: blocks along the other axis (2f for W1, d for W2)
         self.W1d, self.W1d_s = ops.mxfp8_group_quantize(W1v, ops.MOE_QUANT_ROWWISE, err=self.err)

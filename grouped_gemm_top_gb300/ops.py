@@ -29,7 +29,7 @@ MOE_ERR_DEVICE_TIMEOUT = 18
 MOE_ERR_CAPACITY = 19
 
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
-MOE_QUANT_ROWWISE, MOE_QUANT_COLWISE_GROUPED = 0, 1
+MOE_QUANT_ROWWISE, MOE_QUANT_COLWISE_GROUPED, MOE_QUANT_COLWISE_GLU = 0, 1, 2
 MOE_GEMM_FWD, MOE_GEMM_DGRAD, MOE_GEMM_WGRAD = 0, 1, 2
 MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD = 0, 1, 2
 MOE_B_GNK, MOE_B_NGK = 0, 1

@@ -94,7 +94,7 @@ typedef enum {
 } moe_status_t;
 
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
-typedef enum { MOE_QUANT_ROWWISE = 0, MOE_QUANT_COLWISE_GROUPED = 1 } moe_quant_axis_t;
+typedef enum { MOE_QUANT_ROWWISE = 0, MOE_QUANT_COLWISE_GROUPED = 1, MOE_QUANT_COLWISE_GLU = 2 } moe_quant_axis_t;
 typedef enum { MOE_GEMM_FWD = 0, MOE_GEMM_DGRAD = 1, MOE_GEMM_WGRAD = 2 } moe_gemm_mode_t;
 typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1, MOE_EPI_SWIGLU_BWD = 2 } moe_epilogue_t;
 typedef enum {
@@ -173,6 +173,12 @@ MOE_API moe_status_t moe_permute(const void* x, int T, int d, int E, int k, cons
  *          layout of that [cols, rows] matrix.  Each group's rows start at a
  *          multiple of 128, so blocks restart at every group boundary and
  *          the padding rows inside a group (zeros) pad its tail block.
+ *          MOE_QUANT_COLWISE_GLU: as COLWISE_GROUPED, but the output rows
+ *          interleave the two column halves in 64-row chunks: output rows
+ *          [128j, 128j+64) are input columns [64j, 64j+64) and rows
+ *          [128j+64, 128j+128) are input columns [cols/2+64j, cols/2+64j+64).
+ *          This is the layout the SwiGLU epilogue of grouped_gemm_mxfp8
+ *          expects for the fused gate/up weight (gate = first half).
  *   gofs   [G+1] int32 (device) or NULL.  If given, rows >= gofs[G] are not
  *          read and their codes/scales are not written; for the columnwise
  *          axis gofs is validated (monotone, multiples of 128, <= rows).
@@ -195,24 +201,27 @@ MOE_API moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols,
  *   b, b_sf   the group weights B_g as [N, K] K-major blocks, b_layout.
  *   out       row r of group g: D[r, n] = sum_k A[r, k] * B_g[n, k].
  *   epilogue  MOE_EPI_NONE:       d = D [M, N] bf16.
- *             MOE_EPI_SWIGLU:     (fwd up/gate) N = 2f with the gate in
- *                                 B rows [0, f) and up in [f, 2f); d = a_pre
+ *             MOE_EPI_SWIGLU:     (fwd up/gate) N = 2f; B must be in the
+ *                                 MOE_QUANT_COLWISE_GLU row order (gate and
+ *                                 up rows interleaved in 64-row chunks, the
+ *                                 gate is logical column n < f); d = a_pre
  *                                 [M, N] bf16 (the GEMM result), d2 = h
  *                                 [M, N/2] bf16, h = silu(gate) * up computed
- *                                 from the fp32 accumulators.  f % 128 == 0.
+ *                                 from the fp32 accumulators, in the
+ *                                 logical [gate | up] column order.
  *             MOE_EPI_SWIGLU_BWD: (dgrad down) N = f, D = dH;
  *                                 epi_aux = a_pre [M, 2N] bf16; d = dA
  *                                 [M, 2N] bf16 = [dgate | dup] with
  *                                 dgate = dH*u*s*(1+g*(1-s)), dup = dH*g*s,
  *                                 s = sigmoid(g).
- *             N % 256 == 0 for every epilogue.
+ *             N % 128 == 0 for every epilogue.
  * MOE_GEMM_WGRAD:
  *   a, a_sf   [M, K] columnwise codes (the transposed left operand, e.g.
  *             h^T); K = row capacity; group g contracts over columns
  *             [gofs[g], gofs[g+1]).
  *   b, b_sf   [N, K] columnwise codes of the right operand (b_layout unused).
  *   d         [G, M, N] bf16: d[g] = A_g * B_g^T over the group's rows;
- *             an empty group writes zeros.  M % 128 == 0, N % 256 == 0.
+ *             an empty group writes zeros.  M % 128 == 0, N % 128 == 0.
  * d, d2, epi_aux: 16-byte aligned.  Launch: one persistent CTA per SM.
  */
 MOE_API moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t* a_sf,

@@ -104,3 +104,11 @@ def assert_fp32_close(gpu, ref64, rel_frob=1e-5, what=""):
     frob = np.linalg.norm(g - ref64) / max(np.linalg.norm(ref64), 1e-300)
     assert frob <= rel_frob, f"{what}: relative Frobenius error {frob:.3e} > {rel_frob}"
     return frob
+
+
+def glu_perm(n):
+    """Row r of a MOE_QUANT_COLWISE_GLU output holds input column glu_perm(n)[r]
+    (moe.h: gate/up halves interleaved in 64-row chunks)."""
+    r = np.arange(n)
+    j, w = r // 128, r % 128
+    return np.where(w < 64, 64 * j + w, n // 2 + 64 * j + (w - 64))

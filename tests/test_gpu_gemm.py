@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import assert_bf16_close, atoms_to_rowmajor, gpu_ops, padded_layout, to_np
+from helpers import assert_bf16_close, atoms_to_rowmajor, glu_perm, gpu_ops, padded_layout, to_np
 from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -39,20 +39,25 @@ def _quant_rows(ops, x, gofs_t=None, G=0):
     return q, s, O.mxfp8_dequantize_rows(codes, sc)
 
 
-def _weights(ops, G, K, N, seed, layout):
+def _weights(ops, G, K, N, seed, layout, glu=False):
     """bf16 weights W [G, K, N]; returns the device operand (codes, scales)
-    and the oracle's dequantized B [G, K, N] from those codes."""
+    and the oracle's dequantized B [G, K, N] from those codes (in logical
+    column order also for the gate/up-interleaved layout)."""
     W = synth.make_normal_bf16((G, K, N), seed, "cuda", std=0.5)
     Wv = W.reshape(G * K, N)
     if layout == ops.MOE_B_NGK:
         gofs = torch.arange(0, (G + 1) * K, K, dtype=torch.int32, device="cuda")
-        q, s = ops.mxfp8_group_quantize(Wv, ops.MOE_QUANT_COLWISE_GROUPED, gofs, G)
+        axis = ops.MOE_QUANT_COLWISE_GLU if glu else ops.MOE_QUANT_COLWISE_GROUPED
+        q, s = ops.mxfp8_group_quantize(Wv, axis, gofs, G)
         qn = q.cpu().numpy()                          # [N, G*K]
-        deq = O.mxfp8_dequantize_rows(qn, atoms_to_rowmajor(s.cpu().numpy(), N, G * K))   # [N, G*K]
-        B = deq.T.reshape(G, K, N)
+        sn = atoms_to_rowmajor(s.cpu().numpy(), N, G * K)
+        perm = glu_perm(N) if glu else np.arange(N)
         # codes bit-exact against the oracle's group-aware columnwise quantizer
         rq, rs, _ = O.mxfp8_quantize_cols_grouped(to_np(Wv), np.arange(0, (G + 1) * K, K))
-        assert np.array_equal(qn, rq) and np.array_equal(atoms_to_rowmajor(s.cpu().numpy(), N, G * K), rs)
+        assert np.array_equal(qn, rq[perm]) and np.array_equal(sn, rs[perm])
+        deq = np.empty((N, G * K))
+        deq[perm] = O.mxfp8_dequantize_rows(qn, sn)   # back to logical column order
+        B = deq.T.reshape(G, K, N)
         return q, s, B
     # GNK: the operand is W^T per group: B_g[n, k] = W[g][n-th row...]; here the
     # weight is read as [G, N', K'] = W itself (rows = K index of W, cols = N)
@@ -67,6 +72,7 @@ def _weights(ops, G, K, N, seed, layout):
     ([128, 0, 256, 384], 512, 512),       # empty group, several m/n tiles
     ([5, 0, 130, 127, 1, 0], 256, 768),   # tiny groups, padding rows
     ([1000, 24], 1024, 1024),
+    ([200, 90], 384, 384),                # N not a multiple of 256
 ])
 def test_fwd_ngk(ops, sizes, K, N):
     G = len(sizes)
@@ -107,13 +113,13 @@ def test_dgrad_gnk(ops, sizes, K, N):
     assert_bf16_close(d[:Rp], O.grouped_gemm(A, B, gofs)[:Rp], what="dgrad")
 
 
-def test_swiglu_epilogue(ops):
-    sizes, K, f = [150, 0, 300], 512, 256
+@pytest.mark.parametrize("sizes,K,f", [([150, 0, 300], 512, 256), ([77, 500], 256, 128), ([129], 1024, 384)])
+def test_swiglu_epilogue(ops, sizes, K, f):
     G, N = len(sizes), 2 * f
     x, gofs_t, gofs = _act(sizes, K, seed=31)
     M = x.shape[0]
     xq, xs, A = _quant_rows(ops, x)
-    bq, bs, B = _weights(ops, G, K, N, seed=32, layout=ops.MOE_B_NGK)
+    bq, bs, B = _weights(ops, G, K, N, seed=32, layout=ops.MOE_B_NGK, glu=True)
     a_pre, h = ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, ops.MOE_B_NGK, gofs_t, G, M, N, K,
                                       ops.MOE_EPI_SWIGLU)
     torch.cuda.synchronize()
@@ -123,8 +129,8 @@ def test_swiglu_epilogue(ops):
     assert_bf16_close(h[:Rp], O.swiglu(ref), what="h")
 
 
-def test_swiglu_bwd_epilogue(ops):
-    sizes, K, f = [140, 260], 512, 256
+@pytest.mark.parametrize("sizes,K,f", [([140, 260], 512, 256), ([300, 0, 5], 256, 384)])
+def test_swiglu_bwd_epilogue(ops, sizes, K, f):
     G, N = len(sizes), f
     dy, gofs_t, gofs = _act(sizes, K, seed=41)
     M = dy.shape[0]

@@ -5,7 +5,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (assert_bf16_close, assert_fp32_close, atoms_to_rowmajor, deq_rows, gpu_ops, to_np)
+from helpers import (assert_bf16_close, assert_fp32_close, atoms_to_rowmajor, deq_rows, glu_perm, gpu_ops,
+                     to_np)
 from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -34,7 +35,9 @@ def _w_fwd(L, which):
         q, s, K, N = L.W1f, L.W1f_s, d, 2 * f
     else:
         q, s, K, N = L.W2f, L.W2f_s, f, d
-    deq = O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), N, E * K))
+    deq = np.empty((N, E * K))
+    perm = glu_perm(N) if which == 1 else np.arange(N)   # W1: gate/up interleaved rows
+    deq[perm] = O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), N, E * K))
     return deq.T.reshape(E, K, N)
 
 
@@ -173,20 +176,26 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     assert np.array_equal(to_np(L.x_perm[rt]), xp)
     rq, rs = O.mxfp8_quantize_rows(xp)
     assert np.array_equal(L.xq[rt].cpu().numpy(), rq)
-    # per sampled row: the row's group weights
-    W1f, W2f = L.W1f.cpu().numpy(), L.W2f.cpu().numpy()
-    W1f_s, W2f_s = L.W1f_s.cpu().numpy(), L.W2f_s.cpu().numpy()
-    W1d, W2d = L.W1d.cpu().numpy(), L.W2d.cpu().numpy()
-    W1d_s, W2d_s = L.W1d_s.cpu().numpy(), L.W2d_s.cpu().numpy()
+    # per sampled row: the row's group weights, fetched group by group
 
-    def b_fwd(q, s, g, K, N):   # columnwise codes [N, E*K] -> [K, N] of group g
-        cols = np.arange(g * K, (g + 1) * K)
-        sc = atoms_to_rowmajor(s, N, E * K)[:, g * K // 32:(g + 1) * K // 32]
-        return O.mxfp8_dequantize_rows(q[:, cols], sc).T
+    def take_sf(atoms_t, rows_total, r_idx, b_lo, b_hi):
+        r = np.asarray(r_idx)[:, None]
+        b = np.arange(b_lo, b_hi)[None, :]
+        off = ((b // 4) * (rows_total // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
+        return atoms_t[torch.from_numpy(off.reshape(-1)).cuda()].cpu().numpy().reshape(off.shape)
+
+    def b_fwd(q, s, g, K, N, glu):   # columnwise codes [N, E*K] -> [K, N] of group g
+        codes = q[:, g * K:(g + 1) * K].cpu().numpy()
+        sc = take_sf(s, N, np.arange(N), g * K // 32, (g + 1) * K // 32)
+        deq = np.empty((N, K))
+        perm = glu_perm(N) if glu else np.arange(N)
+        deq[perm] = O.mxfp8_dequantize_rows(codes, sc)
+        return deq.T
 
     def b_dgrad(q, s, g, Rw, C):  # rowwise [E*Rw, C] -> B = W_g^T [C, Rw]
         r = np.arange(g * Rw, (g + 1) * Rw)
-        return deq_rows(q, s, E * Rw, C, r).T
+        codes = q[g * Rw:(g + 1) * Rw].cpu().numpy()
+        return O.mxfp8_dequantize_rows(codes, take_sf(s, E * Rw, r, 0, C // 32)).T
 
     A_rows = O.mxfp8_dequantize_rows(rq, rs)
     a_pre = np.zeros((len(rows), 2 * f))
@@ -206,10 +215,10 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     dxp = np.zeros((len(rows), d))
     for g in np.unique(grp):
         sel = grp == g
-        a_pre[sel] = A_rows[sel] @ b_fwd(W1f, W1f_s, g, d, 2 * f)
-        y[sel] = Hd[sel] @ b_fwd(W2f, W2f_s, g, f, d)
-        dH[sel] = DYd[sel] @ b_dgrad(W2d, W2d_s, g, f, d)
-        dxp[sel] = DAd[sel] @ b_dgrad(W1d, W1d_s, g, d, 2 * f)
+        a_pre[sel] = A_rows[sel] @ b_fwd(L.W1f, L.W1f_s, g, d, 2 * f, True)
+        y[sel] = Hd[sel] @ b_fwd(L.W2f, L.W2f_s, g, f, d, False)
+        dH[sel] = DYd[sel] @ b_dgrad(L.W2d, L.W2d_s, g, f, d)
+        dxp[sel] = DAd[sel] @ b_dgrad(L.W1d, L.W1d_s, g, d, 2 * f)
     assert_bf16_close(L.a_pre[rt], a_pre, what="a_pre rows")
     assert_bf16_close(L.h[rt], O.swiglu(a_pre), what="h rows")
     assert_bf16_close(L.y_perm[rt], y, what="y_perm rows")
@@ -217,17 +226,16 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     assert_bf16_close(L.dx_perm[rt], dxp, what="dx_perm rows")
     # combine + combine bwd on sampled tokens
     tok = np.sort(rng.choice(T, size=min(256, T), replace=False))
-    sl = slot_of[tok]
-    need = np.unique(sl.reshape(-1))
-    yfull = np.zeros((Rp, d))
-    yfull[need] = to_np(L.y_perm[torch.from_numpy(need).cuda()])
+    need = np.unique(slot_of[tok].reshape(-1))          # rows those tokens read
+    sl = np.searchsorted(need, slot_of[tok])            # slots into the compact row set
+    need_t = torch.from_numpy(need).cuda()
+    tok_t = torch.from_numpy(tok).cuda()
+    ysub = to_np(L.y_perm[need_t])
     wg = L.topk_w.cpu().numpy().astype(np.float64)[tok]
-    assert_bf16_close(to_np(L.out)[tok], O.combine(yfull, sl, wg), what="out tokens")
-    _, rdw = O.combine_bwd(to_np(L.dout)[tok], yfull, sl, wg, Rp)
+    assert_bf16_close(to_np(L.out[tok_t]), O.combine(ysub, sl, wg), what="out tokens")
+    _, rdw = O.combine_bwd(to_np(L.dout[tok_t]), ysub, sl, wg, len(need))
     assert_fp32_close(L.dw.double().cpu().numpy()[tok], rdw, what="dw tokens")
-    dxf = np.zeros((Rp, d))
-    dxf[need] = to_np(L.dx_perm[torch.from_numpy(need).cuda()])
-    assert_bf16_close(to_np(L.dx)[tok], O.combine(dxf, sl, None), what="dx tokens")
+    assert_bf16_close(to_np(L.dx[tok_t]), O.combine(to_np(L.dx_perm[need_t]), sl, None), what="dx tokens")
     # wgrad: sampled (g, m, n) entries over the full group contraction
     nonempty = np.nonzero(counts)[0]
     for which in (2, 1):
@@ -242,8 +250,8 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
             ns = rng.choice(No, size=8, replace=False)
             aq = aT[torch.from_numpy(ms).cuda(), lo:hi].cpu().numpy()
             bq = bT[torch.from_numpy(ns).cuda(), lo:hi].cpu().numpy()
-            asc = np.stack([atoms_to_rowmajor_rows(asT.cpu().numpy(), Mo, M, m, lo, hi) for m in ms])
-            bsc = np.stack([atoms_to_rowmajor_rows(bsT.cpu().numpy(), No, M, n, lo, hi) for n in ns])
+            asc = take_sf(asT, Mo, ms, lo // 32, hi // 32)
+            bsc = take_sf(bsT, No, ns, lo // 32, hi // 32)
             Ah = O.mxfp8_dequantize_rows(aq, asc)      # [8, rows of g]
             Bh = O.mxfp8_dequantize_rows(bq, bsc)
             ref = Ah @ Bh.T
@@ -254,12 +262,6 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
         empty = np.nonzero(counts == 0)[0]
         for g in empty[:3]:
             assert torch.all(dW[g] == 0)
-
-
-def atoms_to_rowmajor_rows(atoms, rows, cols, r, lo, hi):
-    b = np.arange(lo // 32, hi // 32)
-    off = ((b // 4) * (rows // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
-    return atoms[off]
 
 
 @pytest.mark.parametrize("name,T,d,E,k,f,score,zipf", [

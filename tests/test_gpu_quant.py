@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import atoms_to_rowmajor, atoms_rows_subset, gpu_ops, padded_layout, to_np
+from helpers import atoms_to_rowmajor, atoms_rows_subset, glu_perm, gpu_ops, padded_layout, to_np
 from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -122,3 +122,17 @@ def test_colwise_rejects_bad_offsets(ops):
         torch.cuda.synchronize()
         assert int(err.item()) == ops.MOE_ERR_BAD_OFFSETS
         assert torch.all(q == 0xAB) and torch.all(s == 0xCD)
+
+
+@pytest.mark.parametrize("G,K,N", [(1, 128, 256), (4, 256, 512), (3, 128, 1152)])
+def test_colwise_glu_interleaved_rows(ops, G, K, N):
+    """The gate/up-interleaved columnwise layout is the plain columnwise
+    quantization with output rows permuted (moe.h MOE_QUANT_COLWISE_GLU)."""
+    x = _varied(G * K, N, seed=G + K)
+    gofs = torch.arange(0, (G + 1) * K, K, dtype=torch.int32, device="cuda")
+    q, s = ops.mxfp8_group_quantize(x, ops.MOE_QUANT_COLWISE_GLU, gofs, G)
+    torch.cuda.synchronize()
+    rq, rs, _ = O.mxfp8_quantize_cols_grouped(to_np(x), np.arange(0, (G + 1) * K, K))
+    perm = glu_perm(N)
+    assert np.array_equal(q.cpu().numpy(), rq[perm])
+    assert np.array_equal(atoms_to_rowmajor(s.cpu().numpy(), N, G * K), rs[perm])
