@@ -32,6 +32,9 @@ WORKLOADS = {
     "deepseek-v3": dict(T=24576, d=7168, E=256, k=8, f=2048, score="sigmoid", normalize=True, zipf=None,
                         desc="DeepSeek-V3-shaped routed-expert layer fwd+bwd: T=24576 (6x4096), d=7168, E=256, "
                              "top-8 sigmoid normalised, f=2048"),
+    "deepseek-v3-small": dict(T=1536, d=7168, E=16, k=8, f=2048, score="sigmoid", normalize=True, zipf=None,
+                              desc="DeepSeek-V3 expert shapes with 16 experts and 1536 tokens (same 768 rows per "
+                                   "expert; profiling case): d=7168, top-8 sigmoid, f=2048"),
     "mixtral": dict(T=8192, d=4096, E=8, k=2, f=14336, score="softmax", normalize=True, zipf=None,
                     desc="Mixtral-shaped layer fwd+bwd: T=8192, d=4096, E=8, top-2 softmax, f=14336"),
     "tiny": dict(T=256, d=512, E=8, k=2, f=256, score="softmax", normalize=True, zipf=None,

@@ -577,13 +577,14 @@ cudaError_t gemm_set_attributes() {
                                 gg::Cfg<256>::SMEM_BYTES);
 }
 
-// Tile width used by grouped_gemm_mxfp8: 128 (two TMEM accumulators) unless
-// the environment variable MOE_GEMM_BN=256 selects the single-accumulator
-// 256-wide tile (kept for measurement).
+// Tile width used by grouped_gemm_mxfp8: 256 (one TMEM accumulator; on
+// GB300 the 128-wide MMA is operand-bandwidth bound and ran at ~0.64x the
+// 256-wide rate) unless the environment variable MOE_GEMM_BN=128 selects the
+// double-buffered 128-wide tile (kept for measurement).
 static int gemm_bn() {
     static int bn = [] {
         const char* e = getenv("MOE_GEMM_BN");
-        return (e != nullptr && atoi(e) == 256) ? 256 : 128;
+        return (e != nullptr && atoi(e) == 128) ? 128 : 256;
     }();
     return bn;
 }
