@@ -71,13 +71,17 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint4* __restrict__ x,
     (void)err;
 }
 
-// Columnwise, group-aware: tile = 128 input rows (4 blocks of 32 rows, all in
-// one group because groups start at multiples of 128) x 128 input columns.
-// Output is transposed: codes [cols, rows]; CTA x writes output rows
-// [128 x, 128 x + 128).  With `glu`, output rows interleave the two column
-// halves in 64-row chunks: output rows [128 j, 128 j + 64) are input columns
-// [64 j, 64 j + 64) and rows [128 j + 64, 128 j + 128) are input columns
-// [cols/2 + 64 j, cols/2 + 64 j + 64).
+// Columnwise, group-aware: a CTA owns 128 input columns (= 128 output rows)
+// and kColTiles consecutive 128-row tiles (4 blocks of 32 rows each, all in
+// one group because groups start at multiples of 128).  Output is
+// transposed: codes [cols, rows]; each CTA writes kColTiles*128 contiguous
+// bytes of each of its 128 output rows, and the CTAs that run together
+// (consecutive blockIdx.x) continue the same rows, so the writes stream.
+// With `glu`, output rows interleave the two column halves in 64-row chunks:
+// output rows [128 j, 128 j + 64) are input columns [64 j, 64 j + 64) and
+// rows [128 j + 64, 128 j + 128) are input columns [cols/2 + 64 j, ... + 64).
+constexpr int kColTiles = 4;
+
 __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x, int64_t rows, int cols,
                                                     const int32_t* __restrict__ gofs, int G, int glu,
                                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
@@ -89,8 +93,9 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x,
     auto s_x = reinterpret_cast<uint16_t(*)[kQT + 8]>(s_buf);
     auto s_q = reinterpret_cast<uint8_t(*)[kQT + 16]>(s_buf);
     __shared__ int s_ok;
-    const int64_t r0 = (int64_t)blockIdx.y * kQT;
-    const int c0 = blockIdx.x * kQT;
+    const int ct = blockIdx.y;                       // column tile = output row tile
+    const int c0 = ct * kQT;
+    int64_t row_end = rows;
     if (gofs != nullptr) {
         if (threadIdx.x == 0) {
             const bool ok = gofs_valid(gofs, G, rows);
@@ -98,67 +103,78 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x,
             if (!ok && blockIdx.x == 0 && blockIdx.y == 0) set_err(err, MOE_ERR_BAD_OFFSETS);
         }
         __syncthreads();
-        if (!s_ok || r0 >= (int64_t)gofs[G]) return;
+        if (!s_ok) return;
+        row_end = (int64_t)gofs[G];
     }
     const int cols8 = cols >> 3;
-    // load 128 x 128 bf16: 16 uint4 per row, 2048 uint4, 8 per thread
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const int idx = threadIdx.x + 256 * p;
-        const int rl = idx >> 4, cv = idx & 15;
-        const int src8 = glu ? (cv < 8 ? 8 * blockIdx.x + cv : (cols >> 4) + 8 * blockIdx.x + cv - 8)
-                             : (c0 >> 3) + cv;
-        const uint4 v = __ldg(x + (r0 + rl) * cols8 + src8);
-        *reinterpret_cast<uint4*>(&s_x[rl][cv * 8]) = v;
-    }
-    __syncthreads();
-    // each thread: 2 (column, block) pairs; a warp covers 32 consecutive columns
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t w[2][8];
+    for (int it = 0; it < kColTiles; ++it) {
+        const int64_t r0 = ((int64_t)blockIdx.x * kColTiles + it) * kQT;
+        if (r0 >= row_end) break;
+        // load 128 x 128 bf16: 16 uint4 per row, 2048 uint4, 8 per thread
+        uint4 v[8];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int pair = warp + 8 * h;        // 0..15
-        const int col = (pair & 3) * 32 + lane;
-        const int blk = pair >> 2;            // 32-row block 0..3
-        float f[32];
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            f[i] = bf16_bits_to_float(s_x[blk * 32 + i][col]);
-            amax = fmaxf(amax, fabsf(f[i]));
+        for (int p = 0; p < 8; ++p) {
+            const int idx = threadIdx.x + 256 * p;
+            const int rl = idx >> 4, cv = idx & 15;
+            const int src8 = glu ? (cv < 8 ? 8 * ct + cv : (cols >> 4) + 8 * ct + cv - 8) : (c0 >> 3) + cv;
+            v[p] = __ldg(x + (r0 + rl) * cols8 + src8);
         }
-        const uint32_t b = e8m0_scale_byte(amax);
-        const float inv = e8m0_inv_scale(b);
+        __syncthreads();      // previous iteration is done with the buffer
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t lo = cvt_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
-            const uint32_t hi = cvt_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
-            w[h][i] = lo | (hi << 16);
+        for (int p = 0; p < 8; ++p) {
+            const int idx = threadIdx.x + 256 * p;
+            *reinterpret_cast<uint4*>(&s_x[idx >> 4][(idx & 15) * 8]) = v[p];
         }
-        s_atom[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b;
-    }
-    __syncthreads();     // every thread is done reading the input tile
+        __syncthreads();
+        // each thread: 2 (column, block) pairs; a warp covers 32 consecutive columns
+        uint32_t w[2][8];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int pair = warp + 8 * h;
-        const int col = (pair & 3) * 32 + lane;
-        const int blk = pair >> 2;
-        uint4* dst = reinterpret_cast<uint4*>(&s_q[col][blk * 32]);
-        dst[0] = make_uint4(w[h][0], w[h][1], w[h][2], w[h][3]);
-        dst[1] = make_uint4(w[h][4], w[h][5], w[h][6], w[h][7]);
-    }
-    __syncthreads();
-    // write codes: output row (c0 + col), bytes [r0, r0 + 128): 8 uint4 per row
+        for (int h = 0; h < 2; ++h) {
+            const int pair = warp + 8 * h;        // 0..15
+            const int col = (pair & 3) * 32 + lane;
+            const int blk = pair >> 2;            // 32-row block 0..3
+            float f[32];
+            float amax = 0.f;
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const int idx = threadIdx.x + 256 * p;    // 0..1023
-        const int col = idx >> 3, cv = idx & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(&s_q[col][cv * 16]);
-        *reinterpret_cast<uint4*>(codes + (int64_t)(c0 + col) * rows + r0 + cv * 16) = v;
-    }
-    if (threadIdx.x < 32) {
-        const int64_t atom = (r0 / kQT) * (int64_t)(cols / kQT) + c0 / kQT;
-        reinterpret_cast<uint4*>(scales + atom * 512)[threadIdx.x] = reinterpret_cast<const uint4*>(s_atom)[threadIdx.x];
+            for (int i = 0; i < 32; ++i) {
+                f[i] = bf16_bits_to_float(s_x[blk * 32 + i][col]);
+                amax = fmaxf(amax, fabsf(f[i]));
+            }
+            const uint32_t b = e8m0_scale_byte(amax);
+            const float inv = e8m0_inv_scale(b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t lo = cvt_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv);
+                const uint32_t hi = cvt_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+                w[h][i] = lo | (hi << 16);
+            }
+            s_atom[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b;
+        }
+        __syncthreads();     // every thread is done reading the input tile
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int pair = warp + 8 * h;
+            const int col = (pair & 3) * 32 + lane;
+            const int blk = pair >> 2;
+            uint4* dst = reinterpret_cast<uint4*>(&s_q[col][blk * 32]);
+            dst[0] = make_uint4(w[h][0], w[h][1], w[h][2], w[h][3]);
+            dst[1] = make_uint4(w[h][4], w[h][5], w[h][6], w[h][7]);
+        }
+        __syncthreads();
+        // write codes: output row (c0 + col), bytes [r0, r0 + 128): 8 uint4 per row
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int idx = threadIdx.x + 256 * p;    // 0..1023
+            const int col = idx >> 3, cv = idx & 7;
+            const uint4 q = *reinterpret_cast<const uint4*>(&s_q[col][cv * 16]);
+            *reinterpret_cast<uint4*>(codes + (int64_t)(c0 + col) * rows + r0 + cv * 16) = q;
+        }
+        if (threadIdx.x < 32) {
+            const int64_t atom = (r0 / kQT) * (int64_t)(cols / kQT) + ct;
+            reinterpret_cast<uint4*>(scales + atom * 512)[threadIdx.x] =
+                reinterpret_cast<const uint4*>(s_atom)[threadIdx.x];
+        }
     }
 }
 
@@ -171,7 +187,7 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
     MOE_REQUIRE(x && codes && scales, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(rows >= 0 && cols > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(rows % kQT == 0 && cols % kQT == 0, MOE_ERR_UNSUPPORTED);
-    MOE_REQUIRE(rows / kQT <= 65535, MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(rows / kQT <= 65535 && cols / kQT <= 65535, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(axis == MOE_QUANT_ROWWISE || axis == MOE_QUANT_COLWISE_GROUPED || axis == MOE_QUANT_COLWISE_GLU,
                 MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(gofs == nullptr || (G >= 1 && G <= 4096), MOE_ERR_INVALID_ARG);
@@ -179,10 +195,11 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
     if (rows == 0) return MOE_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    dim3 grid(cols / kQT, (unsigned)(rows / kQT));
     if (axis == MOE_QUANT_ROWWISE) {
+        dim3 grid(cols / kQT, (unsigned)(rows / kQT));
         k_quant_rows<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, (uint2*)codes, scales, err);
     } else {
+        dim3 grid((unsigned)((rows / kQT + kColTiles - 1) / kColTiles), cols / kQT);
         k_quant_cols<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, axis == MOE_QUANT_COLWISE_GLU ? 1 : 0,
                                           codes, scales, err);
     }
