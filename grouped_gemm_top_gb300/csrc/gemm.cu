@@ -36,7 +36,6 @@ constexpr int SFA_STAGE = 512;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_STRIDE = 16;       // TMEM columns of scales per pipeline stage
 constexpr int BAND = 8;                       // m-tiles per raster band
-constexpr int PREFETCH = 4;                   // k-steps prefetched into L2 ahead of the smem stages
 constexpr int MAX_G = 1024;
 constexpr int EPI_WARPS = 8;                  // two warps per TMEM lane quarter
 constexpr int THREADS = 128 + 32 * EPI_WARPS;
@@ -153,17 +152,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
-}
-
-__device__ __forceinline__ void l2_prefetch_2d(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y) : "memory");
-}
-__device__ __forceinline__ void l2_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -383,29 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             Tile ti;
             get_tile<BN>(p, s_gofs, total_mt, t, ti);
             const int gB = p.mode == MOE_GEMM_WGRAD ? 0 : ti.g;
-            // Pull the k-step PREFETCH ahead of the one being loaded into L2
-            // (continuing into this CTA's next tile), so the smem stages
-            // mostly wait on L2 hits rather than on DRAM.
-            Tile tn;
-            const bool has_next = t + gridDim.x < total;
-            if (has_next) get_tile<BN>(p, s_gofs, total_mt, t + gridDim.x, tn);
-            auto prefetch = [&](const Tile& tt, int ks) {
-                const int gg = p.mode == MOE_GEMM_WGRAD ? 0 : tt.g;
-                const int64_t kg = tt.kbeg + ks;
-                const int kx = (int)(kg * BK);
-                l2_prefetch_2d(&tmA, kx, (int)tt.a_row);
-                l2_prefetch(p.a_sf + kg * p.a_sf_kstride + (tt.a_row / 128) * 512, 512);
-                const uint8_t* sfb = p.b_sf + (int64_t)gg * p.b_sf_gstride + kg * p.b_sf_kstride;
-#pragma unroll
-                for (int h = 0; h < BN / 128; ++h) {
-                    l2_prefetch_3d(&tmB, kx, tt.b_row + 128 * h, gg);
-                    l2_prefetch(sfb + (int64_t)((tt.b_row + 128 * h) / 128) * 512, 512);
-                }
-            };
             for (int ks = 0; ks < ti.nk; ++ks) {
-                const int pk = ks + PREFETCH;
-                if (pk < ti.nk) prefetch(ti, pk);
-                else if (has_next && pk - ti.nk < tn.nk) prefetch(tn, pk - ti.nk);
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, p, abort_flag)) {
                     aborted = true;
                     break;
