@@ -1,0 +1,454 @@
+// Grouped MXFP8 GEMM on a CTA pair (tcgen05 cta_group::2), sm_103a.
+//
+// Same contract as the 1-SM kernel in gemm.cu ([TE-JAX] "Optimization 1:
+// Grouped GEMM": one launch for every expert, each over its own rows, MXFP8
+// block scaling), with the tile split over two SMs of a cluster:
+//
+//   pair tile = 256 rows x 256 columns; CTA r of the pair holds A rows
+//   [128 r, 128 r + 128) of the tile and B rows [128 r, 128 r + 128) (half of
+//   N) in its own shared memory, and the scales of its A rows and of all 256
+//   B rows.  The leader CTA (rank 0) issues tcgen05.mma.cta_group::2 with
+//   M = 256, N = 256: each SM's tensor core multiplies its own A rows by the
+//   whole B, reading the peer's B half over the cluster.  Per SM and k-step
+//   this moves 32 KB through the TMA and 32 KB of operand reads instead of
+//   48 + 48 KB for a 128 x 256 tile on one SM, which is what bounds the 1-SM
+//   mainloop.
+//
+// Synchronisation (all waits bounded, as in gemm.cu):
+//   full[s]   each CTA's TMA bytes land on its own barrier; the follower's
+//             MMA warp (idle otherwise) waits for its stage and arrives on
+//             the leader's full[s] (count 2), so the leader's MMA starts once
+//             both halves are in shared memory.
+//   empty[s]  tcgen05.commit multicast from the leader to both CTAs.
+//   tfull     tcgen05.commit multicast: the accumulator halves are ready.
+//   tempty    in the leader, count 2 x 8 epilogue warps (the follower's
+//             warps arrive remotely).
+// A group's rows are 128-aligned, so a 256-row pair tile may have only its
+// first half inside the group; the second CTA then multiplies duplicate rows
+// and discards them (its stores are skipped).
+#include "gemm_common.cuh"
+
+namespace moe {
+namespace gg {
+namespace sm2 {
+
+constexpr int BN = 256;                       // pair tile width
+constexpr int STAGES = 6;
+constexpr int A_STAGE = BM * BK;              // 16 KB: this CTA's 128 A rows
+constexpr int B_STAGE = 128 * BK;             // 16 KB: this CTA's half of B
+constexpr int SFA_BYTES = 512;
+constexpr int SFB_BYTES = 1024;               // scales of all 256 B rows
+constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_BYTES + SFB_BYTES;
+constexpr uint32_t SF0 = 256;                 // TMEM: accumulator [0, 256), scales from 256
+constexpr int BAND2 = 4;                      // pair m-tiles per raster band
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;   // full[S], empty[S], tfull, tempty, drain
+constexpr int NBAR = 2 * STAGES + 3;
+constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+constexpr int OFF_GOFS = OFF_MISC + 16;
+constexpr int OFF_PT = OFF_GOFS + (MAX_G + 1) * 4;
+constexpr int SMEM_BYTES = OFF_PT + (MAX_G + 1) * 4 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(SF0 + STAGES * TMEM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of `addr` (a shared::cta address) in CTA `rank`
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait whose arrivals may come from the peer CTA.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const Params& p,
+                                                  volatile int* abort_flag) {
+    uint64_t start = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (*abort_flag) return false;
+            const uint64_t now = globaltimer_ns();
+            if (start == 0) {
+                start = now;
+            } else if (now - start > p.timeout_ns) {
+                set_err(p.err, MOE_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_cp_sf2(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+__device__ __forceinline__ void tc_mma2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+// arrive on the barrier at the same shared offset in both CTAs of the pair
+// once every tcgen05 op issued so far by this thread has completed
+__device__ __forceinline__ void tc_commit_both(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                     "r"(bar),
+                 "h"(mask)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_commit_local2(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// M = 256 (two CTAs x 128 rows), N = 256
+__device__ __forceinline__ uint32_t make_idesc2(uint32_t sf_id) {
+    return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
+}
+
+struct Tile2 {
+    int g;
+    int64_t a_row;      // first A row this CTA loads
+    int b_row_pair;     // first of the 256 B rows of the pair tile
+    int64_t kbeg;
+    int nk;
+    int64_t out_row;    // first output row of this CTA
+    bool valid;         // this CTA's rows belong to the tile's group
+    int nt;
+};
+
+__device__ __forceinline__ void band_decode2(int64_t l, int64_t mtiles, int ntiles, int64_t& mt, int& nt) {
+    const int64_t band_tiles = (int64_t)BAND2 * ntiles;
+    const int64_t b = l / band_tiles;
+    const int64_t rem = l - b * band_tiles;
+    const int64_t m0 = b * BAND2;
+    const int64_t bw = min((int64_t)BAND2, mtiles - m0);
+    mt = m0 + rem % bw;
+    nt = (int)(rem / bw);
+}
+
+__device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, const int* s_pt, int64_t total_pm,
+                                          int64_t t, uint32_t rank, Tile2& ti) {
+    int64_t pm;
+    int nt;
+    if (p.mode != MOE_GEMM_WGRAD) {
+        band_decode2(t, total_pm, p.n_tiles, pm, nt);
+        const int g = find_group(s_pt, p.G, pm);
+        const int64_t base = (int64_t)s_gofs[g] + 256 * (pm - s_pt[g]);
+        const int64_t mine = base + 128 * rank;
+        ti.g = g;
+        ti.valid = mine < (int64_t)s_gofs[g + 1];
+        ti.a_row = ti.valid ? mine : base;
+        ti.out_row = mine;
+        ti.kbeg = 0;
+        ti.nk = (int)(p.K / BK);
+    } else {
+        const int64_t mp = p.M / 256;
+        const int64_t tpg = mp * p.n_tiles;
+        const int g = (int)(t / tpg);
+        band_decode2(t - (int64_t)g * tpg, mp, p.n_tiles, pm, nt);
+        ti.g = g;
+        ti.valid = true;
+        ti.a_row = pm * 256 + 128 * rank;
+        ti.out_row = (int64_t)g * p.M + ti.a_row;
+        ti.kbeg = s_gofs[g] / BK;
+        ti.nk = (s_gofs[g + 1] - s_gofs[g]) / BK;
+    }
+    ti.b_row_pair = nt * BN;
+    ti.nt = nt;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    const uint32_t bar0 = smem_u32(smem + OFF_BAR);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
+    const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
+    int* s_gofs = reinterpret_cast<int*>(smem + OFF_GOFS);
+    int* s_pt = reinterpret_cast<int*>(smem + OFF_PT);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), leader ? 2 : 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, 2 * EPI_WARPS);
+        mbar_init(drain_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        *abort_flag = 0;
+        *bad_flag = 0;
+    }
+    for (int i = threadIdx.x; i <= p.G; i += THREADS) s_gofs[i] = p.gofs[i];
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // offsets: start at 0, monotone, 128-aligned, inside the buffer
+        bool ok = s_gofs[0] == 0;
+        for (int g = 0; g < p.G && ok; ++g) ok = s_gofs[g + 1] >= s_gofs[g] && (s_gofs[g + 1] % BM) == 0;
+        const int64_t limit = p.mode == MOE_GEMM_WGRAD ? p.K : p.M;
+        ok = ok && (int64_t)s_gofs[p.G] <= limit;
+        if (!ok) {
+            *bad_flag = 1;
+            if (blockIdx.x == 0) set_err(p.err, MOE_ERR_BAD_OFFSETS);
+        }
+        // pair tiles per group: ceil(rows / 256)
+        int acc = 0;
+        for (int g = 0; g < p.G; ++g) {
+            s_pt[g] = acc;
+            acc += ok ? (s_gofs[g + 1] - s_gofs[g] + 255) / 256 : 0;
+        }
+        s_pt[p.G] = acc;
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // the peer's barriers are initialised and TMEM is allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const bool bad = *bad_flag != 0;
+    const int64_t total_pm = p.mode == MOE_GEMM_WGRAD ? 0 : (int64_t)s_pt[p.G];
+    const int64_t total = bad ? 0
+                              : (p.mode == MOE_GEMM_WGRAD ? (int64_t)p.G * (p.M / 256) * p.n_tiles
+                                                          : total_pm * p.n_tiles);
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer ----
+        int pend[STAGES];
+        for (int s = 0; s < STAGES; ++s) pend[s] = -1;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool aborted = false;
+        for (int64_t t = pair; t < total && !aborted; t += npairs) {
+            Tile2 ti;
+            get_tile2(p, s_gofs, s_pt, total_pm, t, rank, ti);
+            const int gB = p.mode == MOE_GEMM_WGRAD ? 0 : ti.g;
+            for (int ks = 0; ks < ti.nk; ++ks) {
+                // freed by the leader's MMA completion (commit multicast)
+                if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, p, abort_flag)) {
+                    aborted = true;
+                    break;
+                }
+                const int64_t kg = ti.kbeg + ks;
+                const int kx = (int)(kg * BK);
+                const uint32_t fb = full_bar(stage);
+                mbar_expect_tx(fb, STAGE_TX);
+                tma_load_2d(smem_u32(smem + OFF_A + stage * A_STAGE), &tmA, kx, (int)ti.a_row, fb);
+                tma_load_3d(smem_u32(smem + OFF_B + stage * B_STAGE), &tmB, kx, ti.b_row_pair + 128 * (int)rank, gB,
+                            fb);
+                bulk_load(smem_u32(smem + OFF_SFA + stage * SFA_BYTES),
+                          p.a_sf + kg * p.a_sf_kstride + (ti.a_row / 128) * 512, SFA_BYTES, fb);
+                // the two B scale atoms of the pair tile are adjacent in every layout
+                bulk_load(smem_u32(smem + OFF_SFB + stage * SFB_BYTES),
+                          p.b_sf + (int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride +
+                              (int64_t)(ti.b_row_pair / 128) * 512,
+                          SFB_BYTES, fb);
+                pend[stage] = (int)phase;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (aborted) {
+            Params q = p;
+            q.timeout_ns = 200000000ull;
+            volatile int no_abort = 0;
+            for (int s = 0; s < STAGES; ++s)
+                if (pend[s] >= 0) mbar_wait(full_bar(s), (uint32_t)pend[s], q, &no_abort);
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ---------------------------------------- MMA issuer (leader) ----
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool aborted = false, issued = false;
+        for (int64_t t = pair; t < total && !aborted; t += npairs) {
+            Tile2 ti;
+            get_tile2(p, s_gofs, s_pt, total_pm, t, rank, ti);
+            if (ti.nk == 0) continue;
+            if (!mbar_wait_cluster(tempty_bar, acc_phase ^ 1u, p, abort_flag)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            for (int ks = 0; ks < ti.nk; ++ks) {
+                if (!mbar_wait_cluster(full_bar(stage), phase, p, abort_flag)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t t_sfa = tmem_base + SF0 + TMEM_SF_STRIDE * stage;
+                const uint32_t t_sfb = t_sfa + 4;
+                const uint32_t s_sfb = smem_u32(smem + OFF_SFB + stage * SFB_BYTES);
+                tc_cp_sf2(t_sfa, desc_sf(smem_u32(smem + OFF_SFA + stage * SFA_BYTES)));
+                tc_cp_sf2(t_sfb, desc_sf(s_sfb));
+                tc_cp_sf2(t_sfb + 4, desc_sf(s_sfb + 512));
+                const uint64_t adesc = desc_sw128(smem_u32(smem + OFF_A + stage * A_STAGE));
+                const uint64_t bdesc = desc_sw128(smem_u32(smem + OFF_B + stage * B_STAGE));
+#pragma unroll
+                for (int kk = 0; kk < BK / 32; ++kk)
+                    tc_mma2(tmem_base, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                            make_idesc2((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
+                issued = true;
+                tc_commit_both(empty_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (aborted) break;
+            tc_commit_both(tfull_bar);
+            acc_phase ^= 1u;
+        }
+        if (issued) {
+            tc_commit_local2(drain_bar);
+            Params q = p;
+            q.timeout_ns = 200000000ull;
+            volatile int no_abort = 0;
+            mbar_wait(drain_bar, 0, q, &no_abort);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------- follower: forward stage arrivals to leader ----
+        int stage = 0;
+        uint32_t phase = 0;
+        bool aborted = false;
+        for (int64_t t = pair; t < total && !aborted; t += npairs) {
+            Tile2 ti;
+            get_tile2(p, s_gofs, s_pt, total_pm, t, rank, ti);
+            for (int ks = 0; ks < ti.nk; ++ks) {
+                if (!mbar_wait(full_bar(stage), phase, p, abort_flag)) {
+                    aborted = true;
+                    break;
+                }
+                mbar_arrive_remote(mapa(full_bar(stage), 0));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ----------------------------------------------------- epilogue ----
+        const int ew = warp - 4;
+        const int quarter = ew & 3, half = ew >> 2;
+        uint32_t acc_phase = 0;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t tempty_leader = mapa(tempty_bar, 0);
+        for (int64_t t = pair; t < total; t += npairs) {
+            Tile2 ti;
+            get_tile2(p, s_gofs, s_pt, total_pm, t, rank, ti);
+            const int64_t row = ti.out_row + quarter * 32 + lane;
+            if (ti.nk == 0) {
+                epilogue_zero<BN>(p, row, ti.nt, half);
+                continue;
+            }
+            if (!mbar_wait_cluster(tfull_bar, acc_phase, p, abort_flag)) break;
+            tc_fence_after();
+            if (ti.valid) epilogue_tile<BN>(p, lane_base, row, ti.nt, half);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(tempty_leader);
+            acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // both CTAs are done with TMEM and with each other's barriers
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    }
+}
+
+}  // namespace sm2
+}  // namespace gg
+
+static int g_max_clusters = 0;
+
+cudaError_t gemm_set_attributes_2sm() {
+    cudaError_t e = cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         gg::sm2::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    (void)e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 1024, 1, 1);
+    cfg.blockDim = dim3(gg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = gg::sm2::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gg::sm2::k_grouped_gemm_2sm, &cfg);
+    if (e != cudaSuccess) return e;
+    g_max_clusters = n;
+    return cudaSuccess;
+}
+
+int gemm_max_clusters_2sm() { return g_max_clusters; }
+
+cudaError_t gemm_launch_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const gg::Params& p, int clusters,
+                            cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(gg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = gg::sm2::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm, tmA, tmB, p);
+}
+
+}  // namespace moe

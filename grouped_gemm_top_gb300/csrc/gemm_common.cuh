@@ -1,0 +1,279 @@
+// Shared pieces of the grouped MXFP8 GEMM kernels (1-SM and 2-SM): launch
+// parameters, PTX wrappers for TMA / mbarrier / tcgen05, the tile schedule
+// helpers and the fused epilogues.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int BM = 128, BK = 128;             // BK in fp8 elements (= bytes)
+constexpr int SFA_STAGE = 512;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_SF_STRIDE = 16;       // TMEM columns of scales per pipeline stage
+constexpr int BAND = 8;                       // m-tiles per raster band
+constexpr int MAX_G = 1024;
+constexpr int EPI_WARPS = 8;                  // two warps per TMEM lane quarter
+constexpr int THREADS = 128 + 32 * EPI_WARPS;
+
+struct Params {
+    int mode, epi, G;
+    int N;
+    int64_t M, K;
+    int n_tiles;        // tiles along N
+    int m_tiles;        // WGRAD: tiles along M per group
+    const int32_t* gofs;
+    const uint8_t* a_sf;
+    const uint8_t* b_sf;
+    int64_t a_sf_kstride, b_sf_kstride, b_sf_gstride;   // bytes
+    __nv_bfloat16* d;
+    __nv_bfloat16* d2;
+    const __nv_bfloat16* aux;
+    int32_t* err;
+    uint64_t timeout_ns;
+};
+
+// ---------------------------------------------------------------- PTX ----
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait.  Returns false when the CTA is aborting (timeout here or
+// elsewhere in the CTA).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Params& p, volatile int* abort_flag) {
+    uint64_t start = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (*abort_flag) return false;
+            const uint64_t now = globaltimer_ns();
+            if (start == 0) {
+                start = now;
+            } else if (now - start > p.timeout_ns) {
+                set_err(p.err, MOE_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128
+// bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;              // descriptor version
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+// Descriptor of a 32-row x 16-byte scale atom (no swizzle, 8-row core
+// matrices of 128 contiguous bytes).
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor: E4M3 x E4M3, fp32 accumulate, K-major A and B,
+// E8M0 scales, M = 128, N = BN, scale byte `sf_id` of each 32-bit TMEM cell.
+template <int BN>
+__device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
+    return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// 32 lanes x 32 columns of fp32 from TMEM (this warp's lane quarter).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 floats -> 32 bf16 (RNE) -> four 16-byte stores.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* v) {
+    uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = pack8(v + 8 * q);
+}
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v) {
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) unpack8(__ldg(s + q), v + 8 * q);
+}
+
+// ------------------------------------------------------------ schedule ----
+
+__device__ __forceinline__ void band_decode(int64_t l, int64_t mtiles, int ntiles, int64_t& mt, int& nt) {
+    const int64_t band_tiles = (int64_t)BAND * ntiles;
+    const int64_t b = l / band_tiles;
+    const int64_t rem = l - b * band_tiles;
+    const int64_t m0 = b * BAND;
+    const int64_t bw = min((int64_t)BAND, mtiles - m0);
+    mt = m0 + rem % bw;
+    nt = (int)(rem / bw);
+}
+
+__device__ __forceinline__ int find_group(const int* s_gofs, int G, int64_t row) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)s_gofs[mid] <= row) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ------------------------------------------------------------- epilogue ----
+// One TMEM accumulator of BN columns, 128 lanes: the calling warp owns lane
+// quarter `quarter` (rows quarter*32 + lane of the tile) and column half
+// `half` of the tile.  `row` is this thread's output row, `nt` the tile
+// index along N.  Writes bf16 results with the fused activation.
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, int64_t row, int nt, int half) {
+    float v[32];
+    if (p.epi == MOE_EPI_SWIGLU) {
+        // B rows interleave gate/up in 64-row chunks: accumulator columns
+        // [128q, 128q+64) are gate, [128q+64, 128q+128) up
+        const int64_t N = p.N, f = p.N / 2;
+        for (int u = half * (BN / 128); u < (half + 1) * (BN / 128); ++u) {
+            const int q = u >> 1, c = u & 1;
+            float up[32], h[32];
+            tmem_ld32(tacc + 128 * q + 32 * c, v);
+            tmem_ld32(tacc + 128 * q + 64 + 32 * c, up);
+            const int64_t hcol = (int64_t)nt * (BN / 2) + 64 * q + 32 * c;
+            store_row32(p.d + row * N + hcol, v);
+            store_row32(p.d + row * N + f + hcol, up);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float s = 1.f / (1.f + expf(-v[i]));
+                h[i] = v[i] * s * up[i];
+            }
+            store_row32(p.d2 + row * f + hcol, h);
+        }
+    } else if (p.epi == MOE_EPI_SWIGLU_BWD) {
+        const int64_t N = p.N, ld = 2 * (int64_t)p.N;
+        for (int c = 0; c < BN / 64; ++c) {
+            float g[32], u[32], dg[32], du[32];
+            const int col32 = half * (BN / 2) + 32 * c;
+            tmem_ld32(tacc + col32, v);          // dH
+            const int64_t col = (int64_t)nt * BN + col32;
+            load_row32(p.aux + row * ld + col, g);
+            load_row32(p.aux + row * ld + N + col, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float s = 1.f / (1.f + expf(-g[i]));
+                dg[i] = v[i] * u[i] * s * (1.f + g[i] * (1.f - s));
+                du[i] = v[i] * g[i] * s;
+            }
+            store_row32(p.d + row * ld + col, dg);
+            store_row32(p.d + row * ld + N + col, du);
+        }
+    } else {
+        for (int c = 0; c < BN / 64; ++c) {
+            const int col32 = half * (BN / 2) + 32 * c;
+            tmem_ld32(tacc + col32, v);
+            store_row32(p.d + row * p.N + (int64_t)nt * BN + col32, v);
+        }
+    }
+}
+
+// WGRAD of an empty group: the gradient is the empty sum, zero.
+template <int BN>
+__device__ __forceinline__ void epilogue_zero(const Params& p, int64_t row, int nt, int half) {
+    float z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+    for (int c = 0; c < BN / 64; ++c) store_row32(p.d + row * p.N + (int64_t)nt * BN + half * (BN / 2) + 32 * c, z);
+}
+
+}  // namespace gg
+
+// Host side (gemm.cu)
+cudaError_t gemm_set_attributes_2sm();   // gemm2sm.cu
+int gemm_max_clusters_2sm();              // co-resident CTA pairs (after gemm_set_attributes_2sm)
+cudaError_t gemm_launch_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const gg::Params& p, int clusters,
+                            cudaStream_t stream);
+}  // namespace moe
