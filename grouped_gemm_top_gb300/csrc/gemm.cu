@@ -357,6 +357,17 @@ static int gemm_bn() {
     return bn;
 }
 
+// Scale atoms (512 bytes each) seen as a 2-D uint8 tensor of 256-byte rows:
+// `atoms` atoms, boxes of `box_rows` rows (2 = one atom, 4 = two atoms).
+static bool make_sf_map(CUtensorMap* m, const void* base, int64_t atoms, int box_rows) {
+    cuuint64_t gdim[2] = {256, (cuuint64_t)(2 * atoms)}, gstr[1] = {256};
+    cuuint32_t box[2] = {256, (cuuint32_t)box_rows}, estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstr, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // rank-2/3 uint8 tensor map, 128x128 boxes, 128-byte swizzle
 static bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes) {
     cuuint64_t gdim[3], gstr[2];
@@ -455,7 +466,15 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     if (two_sm) {
         const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles : upper_tiles;
         const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm());
-        if (gemm_launch_2sm(tmA, tmB, p, clusters, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+        // atoms in the scale arrays (bounds of the scale tensor maps)
+        const int64_t atoms_a = (K / 128) * (M / 128);
+        int64_t atoms_b;
+        if (mode == MOE_GEMM_WGRAD) atoms_b = (K / 128) * (N / 128);
+        else atoms_b = (int64_t)G * (K / 128) * (N / 128);
+        CUtensorMap tmSFA, tmSFB;
+        MOE_REQUIRE(make_sf_map(&tmSFA, a_sf, atoms_a, 2) && make_sf_map(&tmSFB, b_sf, atoms_b, 4), MOE_ERR_CUDA);
+        if (gemm_launch_2sm(tmA, tmB, tmSFA, tmSFB, p, clusters, (cudaStream_t)stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
     } else if (BN == 256)
         k_grouped_gemm<256><<<grid, THREADS, Cfg<256>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);
     else

@@ -15,10 +15,11 @@
 //   mainloop.
 //
 // Synchronisation (all waits bounded, as in gemm.cu):
-//   full[s]   each CTA's TMA bytes land on its own barrier; the follower's
-//             MMA warp (idle otherwise) waits for its stage and arrives on
-//             the leader's full[s] (count 2), so the leader's MMA starts once
-//             both halves are in shared memory.
+//   full[s]   in the leader: both CTAs' TMA loads (cta_group::2 form, which
+//             lets a load complete on the peer CTA's barrier) count their
+//             bytes on it, so the leader's MMA starts once both halves are in
+//             shared memory.  Scale atoms come through small TMA tensor maps
+//             (rows of 256 bytes) for the same reason.
 //   empty[s]  tcgen05.commit multicast from the leader to both CTAs.
 //   tfull     tcgen05.commit multicast: the accumulator halves are ready.
 //   tempty    in the leader, count 2 x 8 epilogue warps (the follower's
@@ -26,6 +27,9 @@
 // A group's rows are 128-aligned, so a 256-row pair tile may have only its
 // first half inside the group; the second CTA then multiplies duplicate rows
 // and discards them (its stores are skipped).
+#include <stdio.h>
+#include <stdlib.h>
+
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -97,6 +101,23 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
             }
         }
     }
+}
+// TMA loads into this CTA's shared memory whose completion is counted on a
+// barrier that may live in the peer CTA (cta_group::2 form).
+__device__ __forceinline__ void tma2_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma2_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                             uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+        "%3, %4}], [%5];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -185,6 +206,7 @@ __device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, co
 
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                        const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -207,7 +229,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), leader ? 2 : 1);
+            mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
         mbar_init(tfull_bar, 1);
@@ -255,6 +277,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer ----
+        uint32_t leader_full[STAGES];
+        for (int s = 0; s < STAGES; ++s) leader_full[s] = mapa(full_bar(s), 0);
         int pend[STAGES];
         for (int s = 0; s < STAGES; ++s) pend[s] = -1;
         int stage = 0;
@@ -272,18 +296,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 const int64_t kg = ti.kbeg + ks;
                 const int kx = (int)(kg * BK);
-                const uint32_t fb = full_bar(stage);
-                mbar_expect_tx(fb, STAGE_TX);
-                tma_load_2d(smem_u32(smem + OFF_A + stage * A_STAGE), &tmA, kx, (int)ti.a_row, fb);
-                tma_load_3d(smem_u32(smem + OFF_B + stage * B_STAGE), &tmB, kx, ti.b_row_pair + 128 * (int)rank, gB,
-                            fb);
-                bulk_load(smem_u32(smem + OFF_SFA + stage * SFA_BYTES),
-                          p.a_sf + kg * p.a_sf_kstride + (ti.a_row / 128) * 512, SFA_BYTES, fb);
-                // the two B scale atoms of the pair tile are adjacent in every layout
-                bulk_load(smem_u32(smem + OFF_SFB + stage * SFB_BYTES),
-                          p.b_sf + (int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride +
-                              (int64_t)(ti.b_row_pair / 128) * 512,
-                          SFB_BYTES, fb);
+                // both CTAs' bytes complete on the leader's full barrier
+                const uint32_t fb = leader_full[stage];
+                if (leader) mbar_expect_tx(full_bar(stage), 2 * STAGE_TX);
+                tma2_load_2d(smem_u32(smem + OFF_A + stage * A_STAGE), &tmA, kx, (int)ti.a_row, fb);
+                tma2_load_3d(smem_u32(smem + OFF_B + stage * B_STAGE), &tmB, kx, ti.b_row_pair + 128 * (int)rank, gB,
+                             fb);
+                // scale atoms as rows of 256 bytes: atom i = rows 2i, 2i+1; the
+                // two B atoms of the pair tile are adjacent in every layout
+                const int64_t atom_a = (kg * p.a_sf_kstride) / 512 + ti.a_row / 128;
+                const int64_t atom_b = ((int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride) / 512 + ti.b_row_pair / 128;
+                tma2_load_2d(smem_u32(smem + OFF_SFA + stage * SFA_BYTES), &tmSFA, 0, (int)(2 * atom_a), fb);
+                tma2_load_2d(smem_u32(smem + OFF_SFB + stage * SFB_BYTES), &tmSFB, 0, (int)(2 * atom_b), fb);
                 pend[stage] = (int)phase;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -291,12 +315,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
-        if (aborted) {
+        if (aborted && leader) {
+            // the leader's full barriers count both CTAs' bytes; the follower
+            // leaves only after the closing cluster barrier, i.e. after this
             Params q = p;
             q.timeout_ns = 200000000ull;
             volatile int no_abort = 0;
             for (int s = 0; s < STAGES; ++s)
-                if (pend[s] >= 0) mbar_wait(full_bar(s), (uint32_t)pend[s], q, &no_abort);
+                if (pend[s] >= 0) mbar_wait_cluster(full_bar(s), (uint32_t)pend[s], q, &no_abort);
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ---------------------------------------- MMA issuer (leader) ----
@@ -347,26 +373,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             q.timeout_ns = 200000000ull;
             volatile int no_abort = 0;
             mbar_wait(drain_bar, 0, q, &no_abort);
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------------- follower: forward stage arrivals to leader ----
-        int stage = 0;
-        uint32_t phase = 0;
-        bool aborted = false;
-        for (int64_t t = pair; t < total && !aborted; t += npairs) {
-            Tile2 ti;
-            get_tile2(p, s_gofs, s_pt, total_pm, t, rank, ti);
-            for (int ks = 0; ks < ti.nk; ++ks) {
-                if (!mbar_wait(full_bar(stage), phase, p, abort_flag)) {
-                    aborted = true;
-                    break;
-                }
-                mbar_arrive_remote(mapa(full_bar(stage), 0));
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
         }
     } else if (warp >= 4) {
         // ----------------------------------------------------- epilogue ----
@@ -429,13 +435,14 @@ cudaError_t gemm_set_attributes_2sm() {
     e = cudaOccupancyMaxActiveClusters(&n, gg::sm2::k_grouped_gemm_2sm, &cfg);
     if (e != cudaSuccess) return e;
     g_max_clusters = n;
+    if (getenv("MOE_DEBUG") != nullptr) fprintf(stderr, "libmoe: %d co-resident CTA pairs\n", n);
     return cudaSuccess;
 }
 
 int gemm_max_clusters_2sm() { return g_max_clusters; }
 
-cudaError_t gemm_launch_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const gg::Params& p, int clusters,
-                            cudaStream_t stream) {
+cudaError_t gemm_launch_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                            const CUtensorMap& tmSFB, const gg::Params& p, int clusters, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(gg::THREADS, 1, 1);
@@ -448,7 +455,7 @@ cudaError_t gemm_launch_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm, tmA, tmB, p);
+    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm, tmA, tmB, tmSFA, tmSFB, p);
 }
 
 }  // namespace moe
