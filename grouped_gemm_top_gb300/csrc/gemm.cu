@@ -334,15 +334,19 @@ cudaError_t gemm_set_attributes() {
     return gemm_set_attributes_2sm();
 }
 
-// The CTA-pair kernel (gemm2sm.cu) is used for 256-wide tiles unless the
-// environment variable MOE_GEMM_2SM=0 selects the 1-SM kernel (kept for
-// measurement and as the path for WGRAD with M % 256 != 0).
-static bool gemm_use_2sm() {
-    static bool on = [] {
+// Kernel choice.  Default: the CTA-pair kernel (gemm2sm.cu) with 256 x 128
+// pair tiles and two TMEM accumulators per CTA.  The environment variable
+// MOE_GEMM_2SM selects another variant for measurement: 256 = CTA pairs with
+// 256 x 256 tiles, 0 = the 1-SM kernel (tile width from MOE_GEMM_BN).  The
+// 1-SM kernel also serves WGRAD when M % 256 != 0.
+static int gemm_2sm_mode() {
+    static int mode = [] {
         const char* e = getenv("MOE_GEMM_2SM");
-        return !(e != nullptr && atoi(e) == 0);
+        if (e == nullptr) return 128;
+        const int v = atoi(e);
+        return v == 0 ? 0 : (v == 256 ? 256 : 128);
     }();
-    return on;
+    return mode;
 }
 
 // Tile width used by grouped_gemm_mxfp8: 256 (one TMEM accumulator; on
@@ -369,9 +373,10 @@ static bool make_sf_map(CUtensorMap* m, const void* base, int64_t atoms, int box
 }
 
 // rank-2/3 uint8 tensor map, 128x128 boxes, 128-byte swizzle
-static bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes) {
+static bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                     int box_rows = 128) {
     cuuint64_t gdim[3], gstr[2];
-    cuuint32_t box[3] = {128, 128, 1}, estr[3] = {1, 1, 1};
+    cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1}, estr[3] = {1, 1, 1};
     for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
     for (int i = 0; i < rank - 1; ++i) gstr[i] = strides_bytes[i];
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstr,
@@ -461,19 +466,40 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     const int sms = device_sm_count();
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     const int grid = (int)(upper_tiles < sms ? (upper_tiles > 0 ? upper_tiles : 1) : sms);
-    const bool two_sm = BN == 256 && gemm_use_2sm() && gemm_max_clusters_2sm() > 0 &&
+    const int bn2 = gemm_2sm_mode() == 256 && N % 256 == 0 ? 256 : 128;
+    const bool two_sm = gemm_2sm_mode() != 0 && gemm_max_clusters_2sm(bn2) > 0 &&
                         (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {
-        const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles : upper_tiles;
-        const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm());
+        p.n_tiles = N / bn2;
+        const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles
+                                                           : (M / BM) * (int64_t)p.n_tiles;
+        const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm(bn2));
+        // B boxes of bn2/2 rows (each CTA of the pair loads half of the tile's B rows)
+        CUtensorMap tmB2;
+        if (mode == MOE_GEMM_WGRAD) {
+            const uint64_t db[3] = {(uint64_t)K, (uint64_t)N, 1}, sb[2] = {(uint64_t)K, (uint64_t)K * N};
+            MOE_REQUIRE(make_map(&tmB2, b, 3, db, sb, bn2 / 2), MOE_ERR_CUDA);
+        } else {
+            const uint64_t db[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)G};
+            uint64_t sb[2];
+            if (b_layout == MOE_B_GNK) {
+                sb[0] = (uint64_t)K;
+                sb[1] = (uint64_t)N * K;
+            } else {
+                sb[0] = (uint64_t)G * K;
+                sb[1] = (uint64_t)K;
+            }
+            MOE_REQUIRE(make_map(&tmB2, b, 3, db, sb, bn2 / 2), MOE_ERR_CUDA);
+        }
         // atoms in the scale arrays (bounds of the scale tensor maps)
         const int64_t atoms_a = (K / 128) * (M / 128);
         int64_t atoms_b;
         if (mode == MOE_GEMM_WGRAD) atoms_b = (K / 128) * (N / 128);
         else atoms_b = (int64_t)G * (K / 128) * (N / 128);
         CUtensorMap tmSFA, tmSFB;
-        MOE_REQUIRE(make_sf_map(&tmSFA, a_sf, atoms_a, 2) && make_sf_map(&tmSFB, b_sf, atoms_b, 4), MOE_ERR_CUDA);
-        if (gemm_launch_2sm(tmA, tmB, tmSFA, tmSFB, p, clusters, (cudaStream_t)stream) != cudaSuccess)
+        MOE_REQUIRE(make_sf_map(&tmSFA, a_sf, atoms_a, 2) && make_sf_map(&tmSFB, b_sf, atoms_b, 2 * (bn2 / 128)),
+                    MOE_ERR_CUDA);
+        if (gemm_launch_2sm(bn2, tmA, tmB2, tmSFA, tmSFB, p, clusters, (cudaStream_t)stream) != cudaSuccess)
             return MOE_ERR_CUDA;
     } else if (BN == 256)
         k_grouped_gemm<256><<<grid, THREADS, Cfg<256>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);

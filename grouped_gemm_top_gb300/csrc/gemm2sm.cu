@@ -36,27 +36,35 @@ namespace moe {
 namespace gg {
 namespace sm2 {
 
-constexpr int BN = 256;                       // pair tile width
-constexpr int STAGES = 6;
-constexpr int A_STAGE = BM * BK;              // 16 KB: this CTA's 128 A rows
-constexpr int B_STAGE = 128 * BK;             // 16 KB: this CTA's half of B
-constexpr int SFA_BYTES = 512;
-constexpr int SFB_BYTES = 1024;               // scales of all 256 B rows
-constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_BYTES + SFB_BYTES;
-constexpr uint32_t SF0 = 256;                 // TMEM: accumulator [0, 256), scales from 256
+// Pair-tile configurations: N = 256 (one accumulator per CTA) or N = 128
+// (two accumulators per CTA, so the epilogue of one tile overlaps the
+// mainloop of the next).  Each CTA loads BN/2 rows of B.
+template <int BN_>
+struct C2 {
+    static constexpr int BN = BN_;
+    static constexpr int BH = BN_ / 2;                  // B rows per CTA
+    static constexpr int NACC = BN_ == 128 ? 2 : 1;
+    static constexpr int STAGES = BN_ == 128 ? 8 : 6;
+    static constexpr int A_STAGE = BM * BK;             // this CTA's 128 A rows
+    static constexpr int B_STAGE = BH * BK;             // this CTA's half of B
+    static constexpr int SFA_BYTES = 512;
+    static constexpr int SFB_BYTES = (BN_ / 128) * 512; // scales of all BN B rows
+    static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_BYTES + SFB_BYTES;
+    static constexpr uint32_t SF0 = NACC * BN_;         // TMEM: accumulators, then scales
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;  // full[S], empty[S], tfull[A], tempty[A], drain
+    static constexpr int NBAR = 2 * STAGES + 2 * NACC + 1;
+    static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+    static constexpr int OFF_GOFS = OFF_MISC + 16;
+    static constexpr int OFF_PT = OFF_GOFS + (MAX_G + 1) * 4;
+    static constexpr int SMEM_BYTES = OFF_PT + (MAX_G + 1) * 4 + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(SF0 + STAGES * TMEM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
+};
 constexpr int BAND2 = 4;                      // pair m-tiles per raster band
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
-constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;   // full[S], empty[S], tfull, tempty, drain
-constexpr int NBAR = 2 * STAGES + 3;
-constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
-constexpr int OFF_GOFS = OFF_MISC + 16;
-constexpr int OFF_PT = OFF_GOFS + (MAX_G + 1) * 4;
-constexpr int SMEM_BYTES = OFF_PT + (MAX_G + 1) * 4 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(SF0 + STAGES * TMEM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -147,7 +155,8 @@ __device__ __forceinline__ void tc_commit_both(uint32_t bar) {
 __device__ __forceinline__ void tc_commit_local2(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// M = 256 (two CTAs x 128 rows), N = 256
+// M = 256 (two CTAs x 128 rows), N = BN
+template <int BN>
 __device__ __forceinline__ uint32_t make_idesc2(uint32_t sf_id) {
     return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
 }
@@ -155,7 +164,7 @@ __device__ __forceinline__ uint32_t make_idesc2(uint32_t sf_id) {
 struct Tile2 {
     int g;
     int64_t a_row;      // first A row this CTA loads
-    int b_row_pair;     // first of the 256 B rows of the pair tile
+    int b_row_pair;     // first of the BN B rows of the pair tile
     int64_t kbeg;
     int nk;
     int64_t out_row;    // first output row of this CTA
@@ -173,6 +182,7 @@ __device__ __forceinline__ void band_decode2(int64_t l, int64_t mtiles, int ntil
     nt = (int)(rem / bw);
 }
 
+template <int BN>
 __device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, const int* s_pt, int64_t total_pm,
                                           int64_t t, uint32_t rank, Tile2& ti) {
     int64_t pm;
@@ -204,10 +214,16 @@ __device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, co
     ti.nt = nt;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                        const Params p) {
+    using C = C2<BN>;
+    constexpr int STAGES = C::STAGES, NACC = C::NACC, BH = C::BH;
+    constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_SFA = C::OFF_SFA, OFF_SFB = C::OFF_SFB;
+    constexpr int OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC, OFF_GOFS = C::OFF_GOFS, OFF_PT = C::OFF_PT;
+    constexpr int A_STAGE = C::A_STAGE, B_STAGE = C::B_STAGE, SFA_BYTES = C::SFA_BYTES, SFB_BYTES = C::SFB_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -218,9 +234,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
-    const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + NACC + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * NACC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
@@ -232,8 +248,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(tfull_bar, 1);
-        mbar_init(tempty_bar, 2 * EPI_WARPS);
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * EPI_WARPS);
+        }
         mbar_init(drain_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         *abort_flag = 0;
@@ -286,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool aborted = false;
         for (int64_t t = pair; t < total && !aborted; t += npairs) {
             Tile2 ti;
-            get_tile2(p, s_gofs, s_pt, total_pm, t, rank, ti);
+            get_tile2<BN>(p, s_gofs, s_pt, total_pm, t, rank, ti);
             const int gB = p.mode == MOE_GEMM_WGRAD ? 0 : ti.g;
             for (int ks = 0; ks < ti.nk; ++ks) {
                 // freed by the leader's MMA completion (commit multicast)
@@ -298,9 +316,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int kx = (int)(kg * BK);
                 // both CTAs' bytes complete on the leader's full barrier
                 const uint32_t fb = leader_full[stage];
-                if (leader) mbar_expect_tx(full_bar(stage), 2 * STAGE_TX);
+                if (leader) mbar_expect_tx(full_bar(stage), 2 * C::STAGE_TX);
                 tma2_load_2d(smem_u32(smem + OFF_A + stage * A_STAGE), &tmA, kx, (int)ti.a_row, fb);
-                tma2_load_3d(smem_u32(smem + OFF_B + stage * B_STAGE), &tmB, kx, ti.b_row_pair + 128 * (int)rank, gB,
+                tma2_load_3d(smem_u32(smem + OFF_B + stage * B_STAGE), &tmB, kx, ti.b_row_pair + BH * (int)rank, gB,
                              fb);
                 // scale atoms as rows of 256 bytes: atom i = rows 2i, 2i+1; the
                 // two B atoms of the pair tile are adjacent in every layout
@@ -326,36 +344,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ---------------------------------------- MMA issuer (leader) ----
-        int stage = 0;
+        int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool aborted = false, issued = false;
         for (int64_t t = pair; t < total && !aborted; t += npairs) {
             Tile2 ti;
-            get_tile2(p, s_gofs, s_pt, total_pm, t, rank, ti);
+            get_tile2<BN>(p, s_gofs, s_pt, total_pm, t, rank, ti);
             if (ti.nk == 0) continue;
-            if (!mbar_wait_cluster(tempty_bar, acc_phase ^ 1u, p, abort_flag)) {
+            if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, p, abort_flag)) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int ks = 0; ks < ti.nk; ++ks) {
                 if (!mbar_wait_cluster(full_bar(stage), phase, p, abort_flag)) {
                     aborted = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t t_sfa = tmem_base + SF0 + TMEM_SF_STRIDE * stage;
+                const uint32_t t_sfa = tmem_base + C::SF0 + TMEM_SF_STRIDE * stage;
                 const uint32_t t_sfb = t_sfa + 4;
                 const uint32_t s_sfb = smem_u32(smem + OFF_SFB + stage * SFB_BYTES);
                 tc_cp_sf2(t_sfa, desc_sf(smem_u32(smem + OFF_SFA + stage * SFA_BYTES)));
-                tc_cp_sf2(t_sfb, desc_sf(s_sfb));
-                tc_cp_sf2(t_sfb + 4, desc_sf(s_sfb + 512));
+#pragma unroll
+                for (int h = 0; h < BN / 128; ++h) tc_cp_sf2(t_sfb + 4 * h, desc_sf(s_sfb + 512 * h));
                 const uint64_t adesc = desc_sw128(smem_u32(smem + OFF_A + stage * A_STAGE));
                 const uint64_t bdesc = desc_sw128(smem_u32(smem + OFF_B + stage * B_STAGE));
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk)
-                    tc_mma2(tmem_base, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
-                            make_idesc2((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
+                    tc_mma2(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                            make_idesc2<BN>((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
                 issued = true;
                 tc_commit_both(empty_bar(stage));
                 if (++stage == STAGES) {
@@ -364,8 +383,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (aborted) break;
-            tc_commit_both(tfull_bar);
-            acc_phase ^= 1u;
+            tc_commit_both(tfull_bar(acc));
+            if (++acc == NACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
         }
         if (issued) {
             tc_commit_local2(drain_bar);
@@ -378,24 +400,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ----------------------------------------------------- epilogue ----
         const int ew = warp - 4;
         const int quarter = ew & 3, half = ew >> 2;
+        int acc = 0;
         uint32_t acc_phase = 0;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t tempty_leader = mapa(tempty_bar, 0);
         for (int64_t t = pair; t < total; t += npairs) {
             Tile2 ti;
-            get_tile2(p, s_gofs, s_pt, total_pm, t, rank, ti);
+            get_tile2<BN>(p, s_gofs, s_pt, total_pm, t, rank, ti);
             const int64_t row = ti.out_row + quarter * 32 + lane;
             if (ti.nk == 0) {
                 epilogue_zero<BN>(p, row, ti.nt, half);
                 continue;
             }
-            if (!mbar_wait_cluster(tfull_bar, acc_phase, p, abort_flag)) break;
+            if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, p, abort_flag)) break;
             tc_fence_after();
-            if (ti.valid) epilogue_tile<BN>(p, lane_base, row, ti.nt, half);
+            if (ti.valid) epilogue_tile<BN>(p, lane_base + (uint32_t)(acc * BN), row, ti.nt, half);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(tempty_leader);
-            acc_phase ^= 1u;
+            if (lane == 0) mbar_arrive_remote(mapa(tempty_bar(acc), 0));
+            if (++acc == NACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
         }
     }
 
@@ -412,50 +437,56 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace sm2
 }  // namespace gg
 
-static int g_max_clusters = 0;
+static int g_max_clusters[2] = {0, 0};   // [N = 128, N = 256]
 
-cudaError_t gemm_set_attributes_2sm() {
-    cudaError_t e = cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gg::sm2::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    (void)e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * 1024, 1, 1);
-    cfg.blockDim = dim3(gg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = gg::sm2::SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gg::sm2::k_grouped_gemm_2sm, &cfg);
-    if (e != cudaSuccess) return e;
-    g_max_clusters = n;
-    if (getenv("MOE_DEBUG") != nullptr) fprintf(stderr, "libmoe: %d co-resident CTA pairs\n", n);
-    return cudaSuccess;
-}
-
-int gemm_max_clusters_2sm() { return g_max_clusters; }
-
-cudaError_t gemm_launch_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                            const CUtensorMap& tmSFB, const gg::Params& p, int clusters, cudaStream_t stream) {
+template <int BN>
+static cudaLaunchConfig_t launch_cfg(int clusters, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(gg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = gg::sm2::SMEM_BYTES;
+    cfg.dynamicSmemBytes = gg::sm2::C2<BN>::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm, tmA, tmB, tmSFA, tmSFB, p);
+    return cfg;
+}
+
+template <int BN>
+static cudaError_t set_attr_2sm(int* max_clusters) {
+    cudaError_t e = cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         gg::sm2::C2<BN>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_cfg<BN>(1024, nullptr, attr);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gg::sm2::k_grouped_gemm_2sm<BN>, &cfg);
+    if (e != cudaSuccess) return e;
+    *max_clusters = n;
+    if (getenv("MOE_DEBUG") != nullptr) fprintf(stderr, "libmoe: N=%d pair tiles: %d co-resident CTA pairs\n", BN, n);
+    return cudaSuccess;
+}
+
+cudaError_t gemm_set_attributes_2sm() {
+    cudaError_t e = set_attr_2sm<128>(&g_max_clusters[0]);
+    if (e != cudaSuccess) return e;
+    return set_attr_2sm<256>(&g_max_clusters[1]);
+}
+
+int gemm_max_clusters_2sm(int bn) { return g_max_clusters[bn == 256 ? 1 : 0]; }
+
+cudaError_t gemm_launch_2sm(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                            const CUtensorMap& tmSFB, const gg::Params& p, int clusters, cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    if (bn == 256) {
+        cudaLaunchConfig_t cfg = launch_cfg<256>(clusters, stream, attr);
+        return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<256>, tmA, tmB, tmSFA, tmSFB, p);
+    }
+    cudaLaunchConfig_t cfg = launch_cfg<128>(clusters, stream, attr);
+    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<128>, tmA, tmB, tmSFA, tmSFB, p);
 }
 
 }  // namespace moe

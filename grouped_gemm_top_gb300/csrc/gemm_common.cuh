@@ -273,7 +273,7 @@ __device__ __forceinline__ void epilogue_zero(const Params& p, int64_t row, int 
 
 // Host side (gemm.cu)
 cudaError_t gemm_set_attributes_2sm();   // gemm2sm.cu
-int gemm_max_clusters_2sm();              // co-resident CTA pairs (after gemm_set_attributes_2sm)
-cudaError_t gemm_launch_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+int gemm_max_clusters_2sm(int bn);        // co-resident CTA pairs for N = bn pair tiles
+cudaError_t gemm_launch_2sm(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
                             const CUtensorMap& tmSFB, const gg::Params& p, int clusters, cudaStream_t stream);
 }  // namespace moe
