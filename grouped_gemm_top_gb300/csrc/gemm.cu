@@ -290,10 +290,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!mbar_wait(tfull_bar(acc), acc_phase, p, abort_flag)) break;
             tc_fence_after();
-            epilogue_tile<BN>(p, lane_base + (uint32_t)(acc * BN), row, ti.nt, half);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            const uint32_t tacc = lane_base + (uint32_t)(acc * BN);
+            const uint32_t tempty = tempty_bar(acc);
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+            };
+            if (BN == 256 && p.epi != MOE_EPI_SWIGLU_BWD) {
+                epilogue_tile_staged(p, tacc, row, ti.nt, half, release);
+            } else {
+                epilogue_tile<BN>(p, tacc, row, ti.nt, half);
+                release();
+            }
             if (++acc == NACC) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -334,17 +343,17 @@ cudaError_t gemm_set_attributes() {
     return gemm_set_attributes_2sm();
 }
 
-// Kernel choice.  Default: the CTA-pair kernel (gemm2sm.cu) with 256 x 128
-// pair tiles and two TMEM accumulators per CTA.  The environment variable
-// MOE_GEMM_2SM selects another variant for measurement: 256 = CTA pairs with
-// 256 x 256 tiles, 0 = the 1-SM kernel (tile width from MOE_GEMM_BN).  The
-// 1-SM kernel also serves WGRAD when M % 256 != 0.
+// Kernel choice.  Default: the 1-SM kernel with 128 x 256 tiles (tile width
+// from MOE_GEMM_BN).  The environment variable MOE_GEMM_2SM selects a CTA-pair
+// variant (gemm2sm.cu) for measurement: 256 = 256 x 256 pair tiles, 128 =
+// 256 x 128 pair tiles with two TMEM accumulators per CTA.  WGRAD with
+// M % 256 != 0 always uses the 1-SM kernel.
 static int gemm_2sm_mode() {
     static int mode = [] {
         const char* e = getenv("MOE_GEMM_2SM");
-        if (e == nullptr) return 128;
+        if (e == nullptr) return 0;
         const int v = atoi(e);
-        return v == 0 ? 0 : (v == 256 ? 256 : 128);
+        return v == 256 ? 256 : (v == 128 ? 128 : 0);
     }();
     return mode;
 }

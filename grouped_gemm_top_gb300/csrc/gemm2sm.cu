@@ -413,10 +413,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, p, abort_flag)) break;
             tc_fence_after();
-            if (ti.valid) epilogue_tile<BN>(p, lane_base + (uint32_t)(acc * BN), row, ti.nt, half);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(mapa(tempty_bar(acc), 0));
+            const uint32_t tacc = lane_base + (uint32_t)(acc * BN);
+            const uint32_t tempty = mapa(tempty_bar(acc), 0);
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(tempty);
+            };
+            if (!ti.valid) {
+                release();
+            } else if (BN == 256 && p.epi != MOE_EPI_SWIGLU_BWD) {
+                epilogue_tile_staged(p, tacc, row, ti.nt, half, release);
+            } else {
+                epilogue_tile<BN>(p, tacc, row, ti.nt, half);
+                release();
+            }
             if (++acc == NACC) {
                 acc = 0;
                 acc_phase ^= 1u;

@@ -260,6 +260,66 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
     }
 }
 
+// Register-staged epilogue for 256-wide tiles: the calling thread drains
+// its 128 accumulator columns (column half `half`) into registers as packed
+// bf16, calls release() so the MMA warp can reuse TMEM, and only then writes
+// global memory, overlapped with the next tile's MMAs.  SwiGLU-backward
+// needs its fp32 dH next to two bf16 inputs and keeps epilogue_tile.
+template <typename Release>
+__device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t tacc, int64_t row, int nt, int half,
+                                                     Release release) {
+    float v[32];
+    if (p.epi == MOE_EPI_SWIGLU) {
+        // units u = 2*half, 2*half+1: gate columns [128q + 32c, +32) and up
+        // columns [128q + 64 + 32c, +32) with q = u / 2 = half, c = u % 2
+        uint32_t pg[32], pu[32], ph[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float up[32];
+            tmem_ld32(tacc + 128 * half + 32 * c, v);
+            tmem_ld32(tacc + 128 * half + 64 + 32 * c, up);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float h0 = v[2 * i] / (1.f + expf(-v[2 * i])) * up[2 * i];
+                const float h1 = v[2 * i + 1] / (1.f + expf(-v[2 * i + 1])) * up[2 * i + 1];
+                __nv_bfloat162 g2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                __nv_bfloat162 u2 = __floats2bfloat162_rn(up[2 * i], up[2 * i + 1]);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(h0, h1);
+                pg[16 * c + i] = *reinterpret_cast<uint32_t*>(&g2);
+                pu[16 * c + i] = *reinterpret_cast<uint32_t*>(&u2);
+                ph[16 * c + i] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+        }
+        release();
+        const int64_t N = p.N, f = p.N / 2;
+        const int64_t hcol = (int64_t)nt * 128 + 64 * half;     // 64 h columns of this thread
+        uint4* dg = reinterpret_cast<uint4*>(p.d + row * N + hcol);
+        uint4* du = reinterpret_cast<uint4*>(p.d + row * N + f + hcol);
+        uint4* dh = reinterpret_cast<uint4*>(p.d2 + row * f + hcol);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            dg[q] = make_uint4(pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
+            du[q] = make_uint4(pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
+            dh[q] = make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+        }
+    } else {
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tacc + 128 * half + 32 * c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                pk[16 * c + i] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+        }
+        release();
+        uint4* dst = reinterpret_cast<uint4*>(p.d + row * p.N + (int64_t)nt * 256 + 128 * half);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+}
+
 // WGRAD of an empty group: the gradient is the empty sum, zero.
 template <int BN>
 __device__ __forceinline__ void epilogue_zero(const Params& p, int64_t row, int nt, int half) {
