@@ -260,6 +260,14 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
     }
 }
 
+// 32 bytes (one L2 sector) per store.
+__device__ __forceinline__ void st_global_v8(void* dst, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 // Register-staged epilogue for 256-wide tiles: the calling thread drains
 // its 128 accumulator columns (column half `half`) into registers as packed
 // bf16, calls release() so the MMA warp can reuse TMEM, and only then writes
@@ -293,14 +301,17 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
         release();
         const int64_t N = p.N, f = p.N / 2;
         const int64_t hcol = (int64_t)nt * 128 + 64 * half;     // 64 h columns of this thread
-        uint4* dg = reinterpret_cast<uint4*>(p.d + row * N + hcol);
-        uint4* du = reinterpret_cast<uint4*>(p.d + row * N + f + hcol);
-        uint4* dh = reinterpret_cast<uint4*>(p.d2 + row * f + hcol);
+        uint32_t* dg = reinterpret_cast<uint32_t*>(p.d + row * N + hcol);
+        uint32_t* du = reinterpret_cast<uint32_t*>(p.d + row * N + f + hcol);
+        uint32_t* dh = reinterpret_cast<uint32_t*>(p.d2 + row * f + hcol);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            dg[q] = make_uint4(pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
-            du[q] = make_uint4(pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
-            dh[q] = make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) {
+            st_global_v8(dg + 8 * q, pg[8 * q], pg[8 * q + 1], pg[8 * q + 2], pg[8 * q + 3], pg[8 * q + 4],
+                         pg[8 * q + 5], pg[8 * q + 6], pg[8 * q + 7]);
+            st_global_v8(du + 8 * q, pu[8 * q], pu[8 * q + 1], pu[8 * q + 2], pu[8 * q + 3], pu[8 * q + 4],
+                         pu[8 * q + 5], pu[8 * q + 6], pu[8 * q + 7]);
+            st_global_v8(dh + 8 * q, ph[8 * q], ph[8 * q + 1], ph[8 * q + 2], ph[8 * q + 3], ph[8 * q + 4],
+                         ph[8 * q + 5], ph[8 * q + 6], ph[8 * q + 7]);
         }
     } else {
         uint32_t pk[64];
@@ -314,9 +325,11 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
             }
         }
         release();
-        uint4* dst = reinterpret_cast<uint4*>(p.d + row * p.N + (int64_t)nt * 256 + 128 * half);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.d + row * p.N + (int64_t)nt * 256 + 128 * half);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int q = 0; q < 8; ++q)
+            st_global_v8(dst + 8 * q, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2], pk[8 * q + 3], pk[8 * q + 4],
+                         pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
     }
 }
 
