@@ -343,15 +343,20 @@ cudaError_t gemm_set_attributes() {
     return gemm_set_attributes_2sm();
 }
 
-// Kernel choice.  Default: the 1-SM kernel with 128 x 256 tiles (tile width
-// from MOE_GEMM_BN).  The environment variable MOE_GEMM_2SM selects a CTA-pair
-// variant (gemm2sm.cu) for measurement: 256 = 256 x 256 pair tiles, 128 =
-// 256 x 128 pair tiles with two TMEM accumulators per CTA.  WGRAD with
-// M % 256 != 0 always uses the 1-SM kernel.
+// Kernel choice (host integers only, never device data).  By default the
+// CTA-pair kernel with 256 x 256 tiles serves FWD/DGRAD GEMMs that are
+// weight-traffic bound -- a long contraction (K >= 6144) over groups of at
+// most 2048 rows on average -- because each SM then loads half of every B
+// tile; everything else uses the 1-SM kernel with 128 x 256 tiles, whose
+// epilogue overlaps the next tile better.  (Measured on GB300: the pair kernel
+// is 1.2-1.3x faster on the first kind and 0.9-1.0x on the rest.)  The
+// environment variable MOE_GEMM_2SM overrides the choice for measurement:
+// 0 = 1-SM kernel only, 256 = pair kernel with 256 x 256 tiles wherever it
+// applies, 128 = pair kernel with 256 x 128 tiles.
 static int gemm_2sm_mode() {
     static int mode = [] {
         const char* e = getenv("MOE_GEMM_2SM");
-        if (e == nullptr) return 0;
+        if (e == nullptr) return -1;
         const int v = atoi(e);
         return v == 256 ? 256 : (v == 128 ? 128 : 0);
     }();
@@ -475,9 +480,14 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     const int sms = device_sm_count();
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     const int grid = (int)(upper_tiles < sms ? (upper_tiles > 0 ? upper_tiles : 1) : sms);
-    const int bn2 = gemm_2sm_mode() == 256 && N % 256 == 0 ? 256 : 128;
-    const bool two_sm = gemm_2sm_mode() != 0 && gemm_max_clusters_2sm(bn2) > 0 &&
-                        (mode != MOE_GEMM_WGRAD || M % 256 == 0);
+    int sel = gemm_2sm_mode();
+    if (sel < 0)
+        sel = (mode != MOE_GEMM_WGRAD && epilogue != MOE_EPI_SWIGLU_BWD && N % 256 == 0 && K >= 6144 &&
+               M / G <= 2048)
+                  ? 256
+                  : 0;
+    const int bn2 = sel == 256 && N % 256 == 0 ? 256 : 128;
+    const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {
         p.n_tiles = N / bn2;
         const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles
