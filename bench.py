@@ -401,12 +401,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="deepseek-v3", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-experts", type=int, default=2)
+    ap.add_argument("--cpu-experts", type=int, default=6)
     ap.add_argument("--gemm-point", nargs=3, type=int, metavar=("G", "M_TOTAL", "NK"),
                     help="time one standalone grouped GEMM fwd and print its line")
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
