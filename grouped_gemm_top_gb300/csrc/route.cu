@@ -9,6 +9,8 @@
 // deterministic and never leave the device.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -280,6 +282,61 @@ extern "C" moe_status_t moe_route_bwd(const float* logits, const int32_t* topk_i
     const int grid = (T + warps_per_cta - 1) / warps_per_cta;
     MOE_ROUTE_DISPATCH(route_epl(E), k_route_bwd, grid, kRouteThreads, 0, s, logits, topk_idx, dw, T, E, k, score,
                        normalize, dlogits, err);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// moe_route_topk_noalloc: moe_route_topk without a caller workspace.
+//
+// Some callers have no way to give the library device memory: code behind a
+// plugin or operator interface that passes only input and output pointers,
+// processes whose device memory is owned by a fixed pool they cannot grow,
+// and code that must not call cudaMalloc because it can synchronise the
+// device or is not allowed while a stream is being captured.  For them the
+// per-CTA expert histograms (the only scratch routing needs) live in this
+// fixed device array, compiled into the library and kept by every GPU that
+// loads it until the process exits.
+namespace moe {
+constexpr size_t kRouteScratchInts = (size_t)1 << 18;   // 1 MiB: ceil(T / 128) * E <= 262,144
+static __device__ __align__(256) int32_t g_route_scratch[kRouteScratchInts];
+static int32_t* g_route_scratch_dev[64] = {nullptr};     // device address of the array, per device
+static std::mutex g_route_scratch_mu;
+}  // namespace moe
+
+extern "C" moe_status_t moe_route_topk_noalloc(const float* logits, int T, int E, int k, int score, int normalize,
+                                               int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                               int32_t* err, void* stream) {
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 32, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(score == MOE_SCORE_SOFTMAX || score == MOE_SCORE_SIGMOID, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(counts && offsets, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(T == 0 || (logits && topk_idx && topk_w), MOE_ERR_INVALID_ARG);
+    const int nblk = (T + kRouteTokPerCta - 1) / kRouteTokPerCta;
+    // sizes whose histograms do not fit the fixed array are refused
+    MOE_REQUIRE((size_t)nblk * (size_t)E <= kRouteScratchInts, MOE_ERR_WORKSPACE);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    {
+        // first call on this device: host code cannot use the array's name as
+        // a device pointer, so look its address up once (device current)
+        std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+        if (g_route_scratch_dev[dev] == nullptr) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_route_scratch) != cudaSuccess || ptr == nullptr) return MOE_ERR_CUDA;
+            g_route_scratch_dev[dev] = static_cast<int32_t*>(ptr);
+        }
+    }
+    int32_t* hist = g_route_scratch_dev[dev];
+    cudaStream_t s = (cudaStream_t)stream;
+    // every histogram entry read below is written first in the same call, so
+    // what a previous call left in the array does not matter
+    if (nblk > 0) {
+        MOE_ROUTE_DISPATCH(route_epl(E), k_route_topk, nblk, kRouteThreads, E * sizeof(int), s, logits, T, E, k,
+                           score, normalize, topk_idx, topk_w, hist);
+        MOE_CHECK_LAUNCH();
+    }
+    k_route_offsets<<<1, 1024, 0, s>>>(hist, nblk, E, counts, offsets);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }

@@ -38,7 +38,7 @@ EXPORTS = [
     "moe_abi_version", "moe_status_string", "moe_init", "moe_row_capacity",
     "moe_route_workspace_size", "moe_permute_workspace_size", "moe_route_topk",
     "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
-    "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd",
+    "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_route_topk_noalloc",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -58,6 +58,7 @@ _SIGS = {
     "moe_unpermute_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_combine_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _vp, _vp, _vp, _vp]),
     "moe_route_bwd": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_route_topk_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -225,3 +226,20 @@ def moe_route_bwd(logits, topk_idx, dw, score=MOE_SCORE_SOFTMAX, normalize=True,
     _check("moe_route_bwd", lib.moe_route_bwd(_p(logits), _p(topk_idx), _p(dw), T, E, k, int(score),
                                               int(bool(normalize)), _p(dlogits), _p(err), _stream(stream)))
     return dlogits
+
+
+def moe_route_topk_noalloc(logits, k, score=MOE_SCORE_SOFTMAX, normalize=True, topk_idx=None, topk_w=None,
+                           counts=None, offsets=None, err=None, stream=None):
+    """moe_route_topk for callers that cannot allocate device scratch: the
+    library uses a fixed internal array instead of a workspace (limit
+    ceil(T/128) * E <= 262144; calls must not overlap on the GPU).  The
+    output tensors are allocated here only when not passed in."""
+    T, E = logits.shape
+    topk_idx = topk_idx if topk_idx is not None else _empty((T, k), torch.int32, logits)
+    topk_w = topk_w if topk_w is not None else _empty((T, k), torch.float32, logits)
+    counts = counts if counts is not None else _empty((E,), torch.int32, logits)
+    offsets = offsets if offsets is not None else _empty((E + 1,), torch.int32, logits)
+    _check("moe_route_topk_noalloc", lib.moe_route_topk_noalloc(_p(logits), T, E, k, int(score),
+                                                                int(bool(normalize)), _p(topk_idx), _p(topk_w),
+                                                                _p(counts), _p(offsets), _p(err), _stream(stream)))
+    return topk_idx, topk_w, counts, offsets

@@ -264,6 +264,33 @@ MOE_API moe_status_t moe_route_bwd(const float* logits, const int32_t* topk_idx,
                            int T, int E, int k, int score, int normalize, float* dlogits,
                            int32_t* err, void* stream);
 
+/*
+ * moe_route_topk_noalloc -- moe_route_topk for callers that cannot allocate.
+ * (The pages have no counterpart: this is a calling convention, not a step of
+ * the method.)  Some callers cannot hand the library any device memory
+ * beyond their inputs and outputs: code behind a plugin or operator
+ * interface that passes only tensor pointers, processes whose device memory
+ * belongs to a fixed pool they cannot grow, and code that must not call
+ * cudaMalloc because it can synchronise the device or is not allowed while
+ * a stream is being captured.  This entry point takes the same arguments as
+ * moe_route_topk minus the workspace and computes the same results; its
+ * scratch (one histogram of E counters per 128 tokens) is a fixed 1 MiB
+ * device array inside the library, which every GPU that loads the library
+ * keeps until the process exits.
+ *   Limit: ceil(T / 128) * E <= 262144 (e.g. T = 131072 with E = 256);
+ *   larger sizes return MOE_ERR_WORKSPACE without launching anything.
+ *   It calls no allocator.  Its first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress); make that first call before any
+ *   stream capture.  moe_init must have been called for the device.
+ *   Every call uses the same array, so calls that may overlap on the GPU
+ *   (different streams, or several host threads) race with each other; order
+ *   them on one stream.  The array keeps the previous call's contents, which
+ *   is harmless: each call writes every entry it reads.
+ */
+MOE_API moe_status_t moe_route_topk_noalloc(const float* logits, int T, int E, int k, int score, int normalize,
+                                            int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                            int32_t* err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
