@@ -311,10 +311,13 @@ def oracle_sample(workload, n_experts, seed=0):
     return flops, secs, desc
 
 
-def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0"):
+def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0", K=None, b_layout="ngk"):
     """Standalone grouped GEMM fwd (sweep point): G groups whose sizes are a
-    Dirichlet(0.3) split of M_total rows, N = K = NK, A and B ~ N(0,1) ->
-    MXFP8, bf16 out.  Returns a dict with TFLOPS and roofline fractions."""
+    Dirichlet(0.3) split of M_total rows, N = NK, K = NK (or K), A and B ~
+    N(0,1) -> MXFP8, bf16 out; B in the [N][G*K] (ngk) or [G][N][K] (gnk)
+    layout.  Returns a dict with TFLOPS and roofline fractions."""
+    N = NK
+    K = NK if K is None else K
     import numpy as np
     import torch
 
@@ -323,8 +326,8 @@ def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0"):
     sizes = synth.dirichlet_group_sizes(G, M_total, 0.3, seed)
     gofs = np.concatenate([[0], np.cumsum((sizes + 127) // 128 * 128)])
     M = int(gofs[-1])
-    x = torch.zeros((M, NK), dtype=torch.bfloat16, device=device)
-    src = synth.make_normal_bf16((M_total, NK), seed + 100, device)
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device=device)
+    src = synth.make_normal_bf16((M_total, K), seed + 100, device)
     r = 0
     for g, m in enumerate(sizes):
         x[int(gofs[g]):int(gofs[g]) + int(m)] = src[r:r + int(m)]
@@ -333,15 +336,21 @@ def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0"):
     gofs_t = torch.tensor(gofs, dtype=torch.int32, device=device)
     xq, xs = ops.mxfp8_group_quantize(x, ops.MOE_QUANT_ROWWISE, gofs_t, G)
     del x
-    W = synth.make_normal_bf16((G * NK, NK), seed + 200, device)
-    wg = torch.arange(0, (G + 1) * NK, NK, dtype=torch.int32, device=device)
-    bq, bs = ops.mxfp8_group_quantize(W, ops.MOE_QUANT_COLWISE_GROUPED, wg, G)
+    if b_layout == "gnk":
+        W = synth.make_normal_bf16((G * N, K), seed + 200, device)
+        bq, bs = ops.mxfp8_group_quantize(W, ops.MOE_QUANT_ROWWISE)
+        lay = ops.MOE_B_GNK
+    else:
+        W = synth.make_normal_bf16((G * K, N), seed + 200, device)
+        wg = torch.arange(0, (G + 1) * K, K, dtype=torch.int32, device=device)
+        bq, bs = ops.mxfp8_group_quantize(W, ops.MOE_QUANT_COLWISE_GROUPED, wg, G)
+        lay = ops.MOE_B_NGK
     del W
-    d = torch.empty((M, NK), dtype=torch.bfloat16, device=device)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
 
     def launch():
-        ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, ops.MOE_B_NGK, gofs_t, G, M, NK, NK, d=d, err=err)
+        ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, lay, gofs_t, G, M, N, K, d=d, err=err)
 
     for _ in range(warmup):
         launch()
@@ -356,12 +365,12 @@ def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0"):
     torch.cuda.synchronize()
     assert int(err.item()) == 0, int(err.item())
     ms = sum(a.elapsed_time(b) for a, b in evs) / steps
-    flops = 2.0 * M_total * NK * NK
-    byts = G * NK * NK * (1 + 1 / 32) + M_total * NK * (1 + 1 / 32) + M_total * NK * 2
+    flops = 2.0 * M_total * N * K
+    byts = G * N * K * (1 + 1 / 32) + M_total * K * (1 + 1 / 32) + M_total * N * 2
     peaks, psrc = _peaks()
     mx_peak = 2.0 * peaks["bf16_tflops"]          # kernel timed alone: burst
     t_roof = max(flops / (mx_peak * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
-    return {"G": G, "M_total": M_total, "N": NK, "K": NK, "ms": round(ms, 4),
+    return {"G": G, "M_total": M_total, "N": N, "K": K, "b_layout": b_layout, "ms": round(ms, 4),
             "tflops": round(flops / (ms * 1e-3) / 1e12, 1), "frac_flops": round(flops / (ms * 1e-3) / 1e12 / mx_peak, 4),
             "frac_roofline": round(t_roof / (ms * 1e-3), 4), "algorithmic_gb": round(byts / 1e9, 3),
             "peak_tflops": mx_peak, "peak_source": f"2 x {psrc} bf16 burst", "empty_groups": int((sizes == 0).sum())}
@@ -407,15 +416,20 @@ def main():
     ap.add_argument("--workload", default="deepseek-v3", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-experts", type=int, default=6)
-    ap.add_argument("--gemm-point", nargs=3, type=int, metavar=("G", "M_TOTAL", "NK"),
-                    help="time one standalone grouped GEMM fwd and print its line")
+    ap.add_argument("--gemm-point", nargs="+", type=int, metavar="G M_TOTAL N [K]",
+                    help="time one standalone grouped GEMM fwd (K = N unless given) and print its line")
+    ap.add_argument("--b-layout", default="ngk", choices=["ngk", "gnk"])
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
     args = ap.parse_args()
     if args.gemm_point or args.sweep:
-        pts = [tuple(args.gemm_point)] if args.gemm_point else \
-            [(G, M, NK) for G in (8, 64, 256) for NK in (2048, 7168) for M in (16384, 65536, 262144)]
-        for i, (G, M, NK) in enumerate(pts):
-            r = run_gemm_point(G, M, NK, seed=i, steps=args.steps, warmup=max(args.warmup, 3))
+        if args.gemm_point:
+            gp = list(args.gemm_point)
+            pts = [(gp[0], gp[1], gp[2], gp[3] if len(gp) > 3 else gp[2])]
+        else:
+            pts = [(G, M, NK, NK) for G in (8, 64, 256) for NK in (2048, 7168) for M in (16384, 65536, 262144)]
+        for i, (G, M, N, K) in enumerate(pts):
+            r = run_gemm_point(G, M, N, seed=i, steps=args.steps, warmup=max(args.warmup, 3), K=K,
+                               b_layout=args.b_layout)
             print(json.dumps({"sweep_point": r}), flush=True)
             import torch
             torch.cuda.empty_cache()

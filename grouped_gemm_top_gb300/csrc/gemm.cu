@@ -74,7 +74,7 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
     int64_t mt;
     int nt;
     if (p.mode != MOE_GEMM_WGRAD) {
-        band_decode(t, total_mt, p.n_tiles, mt, nt);
+        band_decode(t, total_mt, p.n_tiles, p.band, mt, nt);
         const int64_t row = mt * BM;
         ti.g = find_group(s_gofs, p.G, row);
         ti.a_row = row;
@@ -84,7 +84,7 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
     } else {
         const int64_t tpg = (int64_t)p.m_tiles * p.n_tiles;
         const int g = (int)(t / tpg);
-        band_decode(t - (int64_t)g * tpg, p.m_tiles, p.n_tiles, mt, nt);
+        band_decode(t - (int64_t)g * tpg, p.m_tiles, p.n_tiles, p.band, mt, nt);
         ti.g = g;
         ti.a_row = mt * BM;
         ti.kbeg = s_gofs[g] / BK;
@@ -445,6 +445,8 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     p.aux = (const __nv_bfloat16*)epi_aux;
     p.err = err;
     p.timeout_ns = 2000000000ull;   // 2 s per wait
+    p.band = 8;                       // (the pair kernel overrides it below)
+    if (const char* e = getenv("MOE_GEMM_BAND")) p.band = std::max(1, atoi(e));
     p.n_tiles = N / BN;
     int64_t upper_tiles;
     if (mode == MOE_GEMM_WGRAD) {
@@ -490,6 +492,7 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {
         p.n_tiles = N / bn2;
+        if (getenv("MOE_GEMM_BAND") == nullptr) p.band = 4;
         const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles
                                                            : (M / BM) * (int64_t)p.n_tiles;
         const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm(bn2));

@@ -64,7 +64,6 @@ struct C2 {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SF0 + STAGES * TMEM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
 };
-constexpr int BAND2 = 4;                      // pair m-tiles per raster band
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -172,23 +171,13 @@ struct Tile2 {
     int nt;
 };
 
-__device__ __forceinline__ void band_decode2(int64_t l, int64_t mtiles, int ntiles, int64_t& mt, int& nt) {
-    const int64_t band_tiles = (int64_t)BAND2 * ntiles;
-    const int64_t b = l / band_tiles;
-    const int64_t rem = l - b * band_tiles;
-    const int64_t m0 = b * BAND2;
-    const int64_t bw = min((int64_t)BAND2, mtiles - m0);
-    mt = m0 + rem % bw;
-    nt = (int)(rem / bw);
-}
-
 template <int BN>
 __device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, const int* s_pt, int64_t total_pm,
                                           int64_t t, uint32_t rank, Tile2& ti) {
     int64_t pm;
     int nt;
     if (p.mode != MOE_GEMM_WGRAD) {
-        band_decode2(t, total_pm, p.n_tiles, pm, nt);
+        band_decode(t, total_pm, p.n_tiles, p.band, pm, nt);
         const int g = find_group(s_pt, p.G, pm);
         const int64_t base = (int64_t)s_gofs[g] + 256 * (pm - s_pt[g]);
         const int64_t mine = base + 128 * rank;
@@ -202,7 +191,7 @@ __device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, co
         const int64_t mp = p.M / 256;
         const int64_t tpg = mp * p.n_tiles;
         const int g = (int)(t / tpg);
-        band_decode2(t - (int64_t)g * tpg, mp, p.n_tiles, pm, nt);
+        band_decode(t - (int64_t)g * tpg, mp, p.n_tiles, p.band, pm, nt);
         ti.g = g;
         ti.valid = true;
         ti.a_row = pm * 256 + 128 * rank;

@@ -15,7 +15,6 @@ constexpr int BM = 128, BK = 128;             // BK in fp8 elements (= bytes)
 constexpr int SFA_STAGE = 512;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_STRIDE = 16;       // TMEM columns of scales per pipeline stage
-constexpr int BAND = 8;                       // m-tiles per raster band
 constexpr int MAX_G = 1024;
 constexpr int EPI_WARPS = 8;                  // two warps per TMEM lane quarter
 constexpr int THREADS = 128 + 32 * EPI_WARPS;
@@ -35,6 +34,7 @@ struct Params {
     const __nv_bfloat16* aux;
     int32_t* err;
     uint64_t timeout_ns;
+    int band;           // m-tiles per raster band (consecutive tiles share the B tile)
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -186,12 +186,12 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v) {
 
 // ------------------------------------------------------------ schedule ----
 
-__device__ __forceinline__ void band_decode(int64_t l, int64_t mtiles, int ntiles, int64_t& mt, int& nt) {
-    const int64_t band_tiles = (int64_t)BAND * ntiles;
+__device__ __forceinline__ void band_decode(int64_t l, int64_t mtiles, int ntiles, int band, int64_t& mt, int& nt) {
+    const int64_t band_tiles = (int64_t)band * ntiles;
     const int64_t b = l / band_tiles;
     const int64_t rem = l - b * band_tiles;
-    const int64_t m0 = b * BAND;
-    const int64_t bw = min((int64_t)BAND, mtiles - m0);
+    const int64_t m0 = b * band;
+    const int64_t bw = min((int64_t)band, mtiles - m0);
     mt = m0 + rem % bw;
     nt = (int)(rem / bw);
 }
