@@ -311,7 +311,7 @@ def oracle_sample(workload, n_experts, seed=0):
     return flops, secs, desc
 
 
-def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0", K=None, b_layout="ngk"):
+def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0", K=None, b_layout="gnk"):
     """Standalone grouped GEMM fwd (sweep point): G groups whose sizes are a
     Dirichlet(0.3) split of M_total rows, N = NK, K = NK (or K), A and B ~
     N(0,1) -> MXFP8, bf16 out; B in the [N][G*K] (ngk) or [G][N][K] (gnk)
@@ -418,7 +418,7 @@ def main():
     ap.add_argument("--cpu-experts", type=int, default=6)
     ap.add_argument("--gemm-point", nargs="+", type=int, metavar="G M_TOTAL N [K]",
                     help="time one standalone grouped GEMM fwd (K = N unless given) and print its line")
-    ap.add_argument("--b-layout", default="ngk", choices=["ngk", "gnk"])
+    ap.add_argument("--b-layout", default="gnk", choices=["ngk", "gnk"])
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
     args = ap.parse_args()
     if args.gemm_point or args.sweep:

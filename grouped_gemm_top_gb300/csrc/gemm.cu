@@ -343,16 +343,13 @@ cudaError_t gemm_set_attributes() {
     return gemm_set_attributes_2sm();
 }
 
-// Kernel choice (host integers only, never device data).  By default the
-// CTA-pair kernel with 256 x 256 tiles serves FWD/DGRAD GEMMs that are
-// weight-traffic bound -- a long contraction (K >= 6144) over groups of at
-// most 2048 rows on average -- because each SM then loads half of every B
-// tile; everything else uses the 1-SM kernel with 128 x 256 tiles, whose
-// epilogue overlaps the next tile better.  (Measured on GB300: the pair kernel
-// is 1.2-1.3x faster on the first kind and 0.9-1.0x on the rest.)  The
-// environment variable MOE_GEMM_2SM overrides the choice for measurement:
-// 0 = 1-SM kernel only, 256 = pair kernel with 256 x 256 tiles wherever it
-// applies, 128 = pair kernel with 256 x 128 tiles.
+// Kernel choice.  By default every GEMM runs on the 1-SM kernel with
+// 128 x 256 tiles: with per-expert weight operands (MOE_B_GNK) it matched or
+// beat the CTA-pair kernel on every measured shape.  The environment variable
+// MOE_GEMM_2SM selects the CTA-pair kernel (gemm2sm.cu) instead, for
+// measurement: 256 = 256 x 256 pair tiles, 128 = 256 x 128 pair tiles with
+// two TMEM accumulators per CTA.  WGRAD with M % 256 != 0 always uses the
+// 1-SM kernel.
 static int gemm_2sm_mode() {
     static int mode = [] {
         const char* e = getenv("MOE_GEMM_2SM");
@@ -483,11 +480,7 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     const int grid = (int)(upper_tiles < sms ? (upper_tiles > 0 ? upper_tiles : 1) : sms);
     int sel = gemm_2sm_mode();
-    if (sel < 0)
-        sel = (mode != MOE_GEMM_WGRAD && epilogue != MOE_EPI_SWIGLU_BWD && N % 256 == 0 && K >= 6144 &&
-               M / G <= 2048)
-                  ? 256
-                  : 0;
+    if (sel < 0) sel = 0;
     const int bn2 = sel == 256 && N % 256 == 0 ? 256 : 128;
     const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {

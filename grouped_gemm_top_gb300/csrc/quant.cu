@@ -82,10 +82,13 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint4* __restrict__ x,
 // rows [128 j + 64, 128 j + 128) are input columns [cols/2 + 64 j, ... + 64).
 constexpr int kColTiles = 4;
 
+// With batch_rows = Kg > 0 the input is G equal groups of Kg rows and the
+// output is batched per group: codes [G][cols][Kg] (each group's transposed
+// block contiguous) and scales in the atom layout of the [G*cols, Kg] matrix.
 __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x, int64_t rows, int cols,
                                                     const int32_t* __restrict__ gofs, int G, int glu,
-                                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                    int32_t* err) {
+                                                    int64_t batch_rows, uint8_t* __restrict__ codes,
+                                                    uint8_t* __restrict__ scales, int32_t* err) {
     // the input tile [row][col] and, after it has been consumed, the output
     // codes tile [col][row] share one buffer
     __shared__ __align__(16) uint8_t s_buf[kQT * (kQT + 8) * 2];
@@ -168,10 +171,23 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x,
             const int idx = threadIdx.x + 256 * p;    // 0..1023
             const int col = idx >> 3, cv = idx & 7;
             const uint4 q = *reinterpret_cast<const uint4*>(&s_q[col][cv * 16]);
-            *reinterpret_cast<uint4*>(codes + (int64_t)(c0 + col) * rows + r0 + cv * 16) = q;
+            int64_t dst;
+            if (batch_rows > 0) {
+                const int64_t g = r0 / batch_rows, kk = r0 - g * batch_rows;
+                dst = ((g * cols + c0 + col) * batch_rows) + kk + cv * 16;
+            } else {
+                dst = (int64_t)(c0 + col) * rows + r0 + cv * 16;
+            }
+            *reinterpret_cast<uint4*>(codes + dst) = q;
         }
         if (threadIdx.x < 32) {
-            const int64_t atom = (r0 / kQT) * (int64_t)(cols / kQT) + ct;
+            int64_t atom;
+            if (batch_rows > 0) {
+                const int64_t g = r0 / batch_rows, kk = r0 - g * batch_rows;
+                atom = (kk / kQT) * ((int64_t)G * (cols / kQT)) + g * (cols / kQT) + ct;
+            } else {
+                atom = (r0 / kQT) * (int64_t)(cols / kQT) + ct;
+            }
             reinterpret_cast<uint4*>(scales + atom * 512)[threadIdx.x] =
                 reinterpret_cast<const uint4*>(s_atom)[threadIdx.x];
         }
@@ -188,8 +204,11 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
     MOE_REQUIRE(rows >= 0 && cols > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(rows % kQT == 0 && cols % kQT == 0, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(rows / kQT <= 65535 && cols / kQT <= 65535, MOE_ERR_UNSUPPORTED);
-    MOE_REQUIRE(axis == MOE_QUANT_ROWWISE || axis == MOE_QUANT_COLWISE_GROUPED || axis == MOE_QUANT_COLWISE_GLU,
+    MOE_REQUIRE(axis == MOE_QUANT_ROWWISE || axis == MOE_QUANT_COLWISE_GROUPED || axis == MOE_QUANT_COLWISE_GLU ||
+                    axis == MOE_QUANT_COLWISE_BATCHED || axis == MOE_QUANT_COLWISE_BATCHED_GLU,
                 MOE_ERR_INVALID_ARG);
+    const bool batched = axis == MOE_QUANT_COLWISE_BATCHED || axis == MOE_QUANT_COLWISE_BATCHED_GLU;
+    if (batched) MOE_REQUIRE(G >= 1 && rows % G == 0 && (rows / G) % kQT == 0, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(gofs == nullptr || (G >= 1 && G <= 4096), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(moe_aligned16(x) && moe_aligned16(codes) && moe_aligned16(scales), MOE_ERR_ALIGNMENT);
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
@@ -200,8 +219,10 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
         k_quant_rows<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, (uint2*)codes, scales, err);
     } else {
         dim3 grid((unsigned)((rows / kQT + kColTiles - 1) / kColTiles), cols / kQT);
-        k_quant_cols<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, axis == MOE_QUANT_COLWISE_GLU ? 1 : 0,
-                                          codes, scales, err);
+        const int glu = (axis == MOE_QUANT_COLWISE_GLU || axis == MOE_QUANT_COLWISE_BATCHED_GLU) ? 1 : 0;
+        // batched outputs use equal groups of rows / G rows (gofs, if given, only bounds the rows read)
+        k_quant_cols<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, batched ? nullptr : gofs, G, glu,
+                                          batched ? rows / G : 0, codes, scales, err);
     }
     MOE_CHECK_LAUNCH();
     return MOE_OK;

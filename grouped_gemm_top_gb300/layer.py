@@ -80,14 +80,14 @@ class MoELayer:
         once per weight update, outside the step)."""
         E, d, f = self.E, self.d, self.f
         dev = self.device
-        gofs_d = torch.arange(0, (E + 1) * d, d, dtype=torch.int32, device=dev)
-        gofs_f = torch.arange(0, (E + 1) * f, f, dtype=torch.int32, device=dev)
         W1v = W1.reshape(E * d, 2 * f)
         W2v = W2.reshape(E * f, d)
-        # fwd operands: blocks along the contraction axis (d for W1, f for W2)
-        # (W1's gate/up halves interleaved in 64-row chunks for the SwiGLU epilogue)
-        self.W1f, self.W1f_s = ops.mxfp8_group_quantize(W1v, ops.MOE_QUANT_COLWISE_GLU, gofs_d, E, err=self.err)
-        self.W2f, self.W2f_s = ops.mxfp8_group_quantize(W2v, ops.MOE_QUANT_COLWISE_GROUPED, gofs_f, E, err=self.err)
+        # fwd operands: blocks along the contraction axis (d for W1, f for W2),
+        # stored per expert as [E][N][K] (W1's gate/up halves interleaved in
+        # 64-row chunks for the SwiGLU epilogue)
+        self.W1f, self.W1f_s = ops.mxfp8_group_quantize(W1v, ops.MOE_QUANT_COLWISE_BATCHED_GLU, None, E,
+                                                        err=self.err)
+        self.W2f, self.W2f_s = ops.mxfp8_group_quantize(W2v, ops.MOE_QUANT_COLWISE_BATCHED, None, E, err=self.err)
         # dgrad operands: blocks along the other axis (2f for W1, d for W2)
         self.W1d, self.W1d_s = ops.mxfp8_group_quantize(W1v, ops.MOE_QUANT_ROWWISE, err=self.err)
         self.W2d, self.W2d_s = ops.mxfp8_group_quantize(W2v, ops.MOE_QUANT_ROWWISE, err=self.err)
@@ -112,10 +112,10 @@ class MoELayer:
         ops.moe_permute(self.x, self.topk_idx, E, M, self.gofs, self.slot_of, self.row_id, self.x_perm, True,
                         self.ws_perm, err)
         ops.mxfp8_group_quantize(self.x_perm, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.xq, self.xs, err)
-        self._gemm(ops.MOE_GEMM_FWD, self.xq, self.xs, self.W1f, self.W1f_s, ops.MOE_B_NGK, self.gofs,
+        self._gemm(ops.MOE_GEMM_FWD, self.xq, self.xs, self.W1f, self.W1f_s, ops.MOE_B_GNK, self.gofs,
                                E, M, 2 * f, d, ops.MOE_EPI_SWIGLU, None, self.a_pre, self.h, err)
         ops.mxfp8_group_quantize(self.h, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.hq, self.hs, err)
-        self._gemm(ops.MOE_GEMM_FWD, self.hq, self.hs, self.W2f, self.W2f_s, ops.MOE_B_NGK, self.gofs,
+        self._gemm(ops.MOE_GEMM_FWD, self.hq, self.hs, self.W2f, self.W2f_s, ops.MOE_B_GNK, self.gofs,
                                E, M, d, f, ops.MOE_EPI_NONE, None, self.y_perm, None, err)
         ops.moe_unpermute_combine(self.y_perm, self.slot_of, self.topk_w, self.out, err)
 

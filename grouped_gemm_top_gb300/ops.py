@@ -30,6 +30,7 @@ MOE_ERR_CAPACITY = 19
 
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_QUANT_ROWWISE, MOE_QUANT_COLWISE_GROUPED, MOE_QUANT_COLWISE_GLU = 0, 1, 2
+MOE_QUANT_COLWISE_BATCHED, MOE_QUANT_COLWISE_BATCHED_GLU = 3, 4
 MOE_GEMM_FWD, MOE_GEMM_DGRAD, MOE_GEMM_WGRAD = 0, 1, 2
 MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD = 0, 1, 2
 MOE_B_GNK, MOE_B_NGK = 0, 1
@@ -171,6 +172,8 @@ def mxfp8_group_quantize(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, codes=None, 
     rows, cols = x.shape
     if axis == MOE_QUANT_ROWWISE:
         codes = codes if codes is not None else _empty((rows, cols), torch.uint8, x)
+    elif axis in (MOE_QUANT_COLWISE_BATCHED, MOE_QUANT_COLWISE_BATCHED_GLU):
+        codes = codes if codes is not None else _empty((G, cols, rows // G), torch.uint8, x)
     else:
         codes = codes if codes is not None else _empty((cols, rows), torch.uint8, x)
     scales = scales if scales is not None else _empty((sf_bytes(rows, cols),), torch.uint8, x)

@@ -94,7 +94,13 @@ typedef enum {
 } moe_status_t;
 
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
-typedef enum { MOE_QUANT_ROWWISE = 0, MOE_QUANT_COLWISE_GROUPED = 1, MOE_QUANT_COLWISE_GLU = 2 } moe_quant_axis_t;
+typedef enum {
+    MOE_QUANT_ROWWISE = 0,
+    MOE_QUANT_COLWISE_GROUPED = 1,
+    MOE_QUANT_COLWISE_GLU = 2,
+    MOE_QUANT_COLWISE_BATCHED = 3,
+    MOE_QUANT_COLWISE_BATCHED_GLU = 4
+} moe_quant_axis_t;
 typedef enum { MOE_GEMM_FWD = 0, MOE_GEMM_DGRAD = 1, MOE_GEMM_WGRAD = 2 } moe_gemm_mode_t;
 typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1, MOE_EPI_SWIGLU_BWD = 2 } moe_epilogue_t;
 typedef enum {
@@ -179,6 +185,15 @@ MOE_API moe_status_t moe_permute(const void* x, int T, int d, int E, int k, cons
  *          [128j+64, 128j+128) are input columns [cols/2+64j, cols/2+64j+64).
  *          This is the layout the SwiGLU epilogue of grouped_gemm_mxfp8
  *          expects for the fused gate/up weight (gate = first half).
+ *          MOE_QUANT_COLWISE_BATCHED[_GLU]: for G equal groups of
+ *          Kg = rows / G rows (a stack of per-expert weights [G][Kg][cols],
+ *          Kg % 128 == 0): each group is quantized along its rows and stored
+ *          transposed on its own, codes [G][cols][Kg] (row order interleaved
+ *          as above for _GLU), scales in the atom layout of the
+ *          [G*cols, Kg] matrix.  This is the MOE_B_GNK operand of
+ *          grouped_gemm_mxfp8 built from a [G][K][N] weight; gofs is
+ *          ignored.  (One expert's operand is contiguous, which on GB300
+ *          halves the DRAM traffic of the forward GEMMs against MOE_B_NGK.)
  *   gofs   [G+1] int32 (device) or NULL.  If given, rows >= gofs[G] are not
  *          read and their codes/scales are not written; for the columnwise
  *          axis gofs is validated (monotone, multiples of 128, <= rows).

@@ -112,3 +112,16 @@ def glu_perm(n):
     r = np.arange(n)
     j, w = r // 128, r % 128
     return np.where(w < 64, 64 * j + w, n // 2 + 64 * j + (w - 64))
+
+
+def batched_weight_operand(q, s, G, cols, Kg, glu=False):
+    """Dequantize a MOE_QUANT_COLWISE_BATCHED[_GLU] operand (codes
+    [G][cols][Kg], scales in the atom layout of [G*cols, Kg]) back to the
+    logical weight [G, Kg, cols] (moe.h)."""
+    qn = np.asarray(q).reshape(G * cols, Kg)
+    sc = atoms_to_rowmajor(np.asarray(s), G * cols, Kg)
+    deq = O.mxfp8_dequantize_rows(qn, sc).reshape(G, cols, Kg)
+    perm = glu_perm(cols) if glu else np.arange(cols)
+    out = np.empty_like(deq)
+    out[:, perm, :] = deq
+    return np.transpose(out, (0, 2, 1))

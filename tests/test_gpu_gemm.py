@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import assert_bf16_close, atoms_to_rowmajor, glu_perm, gpu_ops, padded_layout, to_np
+from helpers import (assert_bf16_close, atoms_to_rowmajor, batched_weight_operand, glu_perm, gpu_ops,
+                     padded_layout, to_np)
 from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -59,11 +60,11 @@ def _weights(ops, G, K, N, seed, layout, glu=False):
         deq[perm] = O.mxfp8_dequantize_rows(qn, sn)   # back to logical column order
         B = deq.T.reshape(G, K, N)
         return q, s, B
-    # GNK: the operand is W^T per group: B_g[n, k] = W[g][n-th row...]; here the
-    # weight is read as [G, N', K'] = W itself (rows = K index of W, cols = N)
-    q, s = ops.mxfp8_group_quantize(Wv, ops.MOE_QUANT_ROWWISE)
-    deq = O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), G * K, N))
-    return q, s, deq.reshape(G, K, N)
+    # GNK from the [G][K][N] weight: per-group transposed blocks (batched)
+    axis = ops.MOE_QUANT_COLWISE_BATCHED_GLU if glu else ops.MOE_QUANT_COLWISE_BATCHED
+    q, s = ops.mxfp8_group_quantize(Wv, axis, None, G)
+    B = batched_weight_operand(q.cpu().numpy(), s.cpu().numpy(), G, N, K, glu)
+    return q, s, B
 
 
 @pytest.mark.parametrize("sizes,K,N", [
@@ -94,6 +95,19 @@ def test_fwd_ngk(ops, sizes, K, N):
         assert torch.all(d[gofs[g] + m:gofs[g + 1]] == 0)
 
 
+@pytest.mark.parametrize("sizes,K,N", [([300, 0, 5], 512, 256), ([1000, 24], 1024, 768)])
+def test_fwd_gnk_batched_weights(ops, sizes, K, N):
+    G = len(sizes)
+    x, gofs_t, gofs = _act(sizes, K, seed=71)
+    M = x.shape[0]
+    xq, xs, A = _quant_rows(ops, x)
+    bq, bs, B = _weights(ops, G, K, N, seed=72, layout=ops.MOE_B_GNK)
+    d = ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, ops.MOE_B_GNK, gofs_t, G, M, N, K)
+    torch.cuda.synchronize()
+    Rp = int(gofs[-1])
+    assert_bf16_close(d[:Rp], O.grouped_gemm(A, B, gofs)[:Rp], what="fwd gnk")
+
+
 @pytest.mark.parametrize("sizes,K,N", [([200, 0, 77], 512, 256), ([128, 128], 256, 512)])
 def test_dgrad_gnk(ops, sizes, K, N):
     """DGRAD reads the weight copy quantized along the other axis: B_g is the
@@ -113,14 +127,15 @@ def test_dgrad_gnk(ops, sizes, K, N):
     assert_bf16_close(d[:Rp], O.grouped_gemm(A, B, gofs)[:Rp], what="dgrad")
 
 
+@pytest.mark.parametrize("layout", [0, 1])       # MOE_B_GNK (batched weight quantization), MOE_B_NGK
 @pytest.mark.parametrize("sizes,K,f", [([150, 0, 300], 512, 256), ([77, 500], 256, 128), ([129], 1024, 384)])
-def test_swiglu_epilogue(ops, sizes, K, f):
+def test_swiglu_epilogue(ops, sizes, K, f, layout):
     G, N = len(sizes), 2 * f
     x, gofs_t, gofs = _act(sizes, K, seed=31)
     M = x.shape[0]
     xq, xs, A = _quant_rows(ops, x)
-    bq, bs, B = _weights(ops, G, K, N, seed=32, layout=ops.MOE_B_NGK, glu=True)
-    a_pre, h = ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, ops.MOE_B_NGK, gofs_t, G, M, N, K,
+    bq, bs, B = _weights(ops, G, K, N, seed=32, layout=layout, glu=True)
+    a_pre, h = ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, layout, gofs_t, G, M, N, K,
                                       ops.MOE_EPI_SWIGLU)
     torch.cuda.synchronize()
     Rp = int(gofs[-1])

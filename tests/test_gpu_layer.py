@@ -5,8 +5,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (assert_bf16_close, assert_fp32_close, atoms_to_rowmajor, deq_rows, glu_perm, gpu_ops,
-                     to_np)
+from helpers import (assert_bf16_close, assert_fp32_close, atoms_to_rowmajor, batched_weight_operand, deq_rows,
+                     glu_perm, gpu_ops, to_np)
 from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -35,10 +35,8 @@ def _w_fwd(L, which):
         q, s, K, N = L.W1f, L.W1f_s, d, 2 * f
     else:
         q, s, K, N = L.W2f, L.W2f_s, f, d
-    deq = np.empty((N, E * K))
-    perm = glu_perm(N) if which == 1 else np.arange(N)   # W1: gate/up interleaved rows
-    deq[perm] = O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), N, E * K))
-    return deq.T.reshape(E, K, N)
+    # per-expert operands [E][N][K] (W1: gate/up interleaved rows)
+    return batched_weight_operand(q.cpu().numpy(), s.cpu().numpy(), E, N, K, glu=(which == 1))
 
 
 def _w_dgrad(L, which):
@@ -184,9 +182,9 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
         off = ((b // 4) * (rows_total // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
         return atoms_t[torch.from_numpy(off.reshape(-1)).cuda()].cpu().numpy().reshape(off.shape)
 
-    def b_fwd(q, s, g, K, N, glu):   # columnwise codes [N, E*K] -> [K, N] of group g
-        codes = q[:, g * K:(g + 1) * K].cpu().numpy()
-        sc = take_sf(s, N, np.arange(N), g * K // 32, (g + 1) * K // 32)
+    def b_fwd(q, s, g, K, N, glu):   # per-expert codes [E][N][K] -> logical [K, N] of group g
+        codes = q[g].cpu().numpy()
+        sc = take_sf(s, E * N, np.arange(g * N, (g + 1) * N), 0, K // 32)
         deq = np.empty((N, K))
         perm = glu_perm(N) if glu else np.arange(N)
         deq[perm] = O.mxfp8_dequantize_rows(codes, sc)

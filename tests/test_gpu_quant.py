@@ -136,3 +136,22 @@ def test_colwise_glu_interleaved_rows(ops, G, K, N):
     perm = glu_perm(N)
     assert np.array_equal(q.cpu().numpy(), rq[perm])
     assert np.array_equal(atoms_to_rowmajor(s.cpu().numpy(), N, G * K), rs[perm])
+
+
+@pytest.mark.parametrize("G,K,N,glu", [(1, 128, 256, False), (4, 256, 512, True), (3, 384, 1152, False),
+                                       (2, 128, 384, True)])
+def test_colwise_batched_per_group_blocks(ops, G, K, N, glu):
+    """Batched layout: group g's transposed block is contiguous, codes
+    [G][N][K], scales in the atom layout of [G*N, K] (moe.h)."""
+    x = _varied(G * K, N, seed=G * 7 + K)
+    axis = ops.MOE_QUANT_COLWISE_BATCHED_GLU if glu else ops.MOE_QUANT_COLWISE_BATCHED
+    q, s = ops.mxfp8_group_quantize(x, axis, None, G)
+    torch.cuda.synchronize()
+    assert tuple(q.shape) == (G, N, K)
+    xn = to_np(x)
+    qn = q.cpu().numpy()
+    sn = atoms_to_rowmajor(s.cpu().numpy(), G * N, K).reshape(G, N, K // 32)
+    perm = glu_perm(N) if glu else np.arange(N)
+    for g in range(G):
+        rq, rs, _ = O.mxfp8_quantize_cols_grouped(xn[g * K:(g + 1) * K], np.array([0, K]))
+        assert np.array_equal(qn[g], rq[perm]) and np.array_equal(sn[g], rs[perm])
