@@ -45,6 +45,25 @@ KERNELS_PER_STEP = 25       # libmoe kernel launches in one fwd+bwd step (see la
 GEMMS_PER_STEP = 6
 
 
+def _gemm_traffic():
+    """DRAM bytes per grouped-GEMM launch from the committed ncu summary
+    (profiles/gemm_traffic.json), only if the GEMM sources are unchanged
+    since those counters were taken; else None."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_traffic.json")) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for fn in ["common.cuh", "gemm_common.cuh", "gemm.cu", "gemm2sm.cu"]:
+            with open(os.path.join(ROOT, "grouped_gemm_top_gb300", "csrc", fn), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != rec["kernel_source_hash"]:
+            return None
+        return rec["gemm_launches"]
+    except Exception:
+        return None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -207,6 +226,16 @@ def run_gpu(args, rank, world, local_rank):
 
     peaks, psrc = _peaks()
     mx_peak = 2.0 * peaks["bf16_tflops_sustained"]     # nominal fp8/bf16 dense ratio 4.5/2.25
+    traffic = _gemm_traffic() if args.workload == "deepseek-v3" else None
+    # algorithmic bytes of the six GEMMs: fp8 operands (+1/32 scales) once,
+    # bf16 outputs (and the SwiGLU-bwd input a_pre) once
+    R, q = L.R, 1 + 1 / 32
+    algo_bytes = (R * d * q + E * d * 2 * f * q + R * 2 * f * 2 + R * f * 2            # up fwd + SwiGLU
+                  + R * f * q + E * f * d * q + R * d * 2                               # down fwd
+                  + R * d * q + E * f * d * q + R * 2 * f * 2 * 2                       # down dgrad + SwiGLU bwd
+                  + R * f * q + R * d * q + E * f * d * 2                               # dW2
+                  + R * 2 * f * q + E * d * 2 * f * q + R * d * 2                       # up dgrad
+                  + R * d * q + R * 2 * f * q + E * d * 2 * f * 2)                      # dW1
     sum_gemm_ms = sum(gemm_ms)
     achieved = sum(gemm_flops) / (sum_gemm_ms * 1e-3) / 1e12
     per_launch = {n: {"ms": round(t, 4), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
@@ -238,7 +267,10 @@ def run_gpu(args, rank, world, local_rank):
                      "frac": round(achieved / mx_peak, 4),
                      "peak_source": f"2 x {psrc} bf16 sustained ({peaks['bf16_tflops_sustained']} TF/s), "
                                     "nominal MXFP8/bf16 dense ratio 4.5/2.25",
-                     "traffic": None},
+                     "traffic": (None if traffic is None else
+                                 round(sum(t["dram_read"] + t["dram_write"] for t in traffic) / len(traffic))),
+                     "traffic_unit": "bytes per launch (DRAM read+write, ncu, mean of the step's 6 launches)",
+                     "algorithmic_bytes_per_launch": round(algo_bytes / GEMMS_PER_STEP)},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
