@@ -41,7 +41,7 @@ WORKLOADS = {
                  desc="tiny layer fwd+bwd: T=256, d=512, E=8, top-2, f=256"),
 }
 METRIC = "MoE layer fwd+bwd TFLOPS (MXFP8 grouped GEMM) and % of dense peak, 1 GB300"
-KERNELS_PER_STEP = 25       # libmoe kernel launches in one fwd+bwd step (see layer.MoELayer)
+KERNELS_PER_STEP = 19       # libmoe kernel launches in one fwd+bwd step (see layer.MoELayer)
 GEMMS_PER_STEP = 6
 
 

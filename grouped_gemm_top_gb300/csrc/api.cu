@@ -11,6 +11,7 @@ static bool g_init[kMaxDevices] = {false};
 static std::mutex g_mu;
 
 cudaError_t gemm_set_attributes();   // gemm.cu
+cudaError_t quant_set_attributes();  // quant.cu
 cudaError_t gemm_init_driver();      // gemm.cu
 
 int device_sm_count() {
@@ -60,6 +61,7 @@ extern "C" moe_status_t moe_init(int device) {
     if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;   // built for sm_103a only
     if (gemm_init_driver() != cudaSuccess) return MOE_ERR_CUDA;
     if (gemm_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+    if (quant_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
     g_sm_count[device] = sms;
     g_init[device] = true;
     return MOE_OK;

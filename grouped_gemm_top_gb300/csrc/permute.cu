@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(128) k_combine_bwd(const uint4* __restrict__ d
                         part[jj] = fmaf(g[i], f[i], part[jj]);
                         o[i] = wj * g[i];
                     }
-                    dy[(int64_t)s_slot[j] * d8 + c] = pack8(o);
+                    if (dy != nullptr) dy[(int64_t)s_slot[j] * d8 + c] = pack8(o);
                 }
             }
         }
@@ -338,7 +338,7 @@ extern "C" moe_status_t moe_combine_bwd(const void* dout, const void* y_perm, co
                                         void* stream) {
     (void)err;
     MOE_REQUIRE(T >= 0 && d > 0 && k >= 1 && k <= 32 && E >= 1 && row_cap > 0, MOE_ERR_INVALID_ARG);
-    MOE_REQUIRE(row_id && gofs && dy_perm, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(dy_perm == nullptr || (row_id && gofs), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(T == 0 || (dout && y_perm && slot_of && topk_w && dw), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(d % 8 == 0 && moe_aligned16(dy_perm) && (T == 0 || (moe_aligned16(dout) && moe_aligned16(y_perm))),
                 MOE_ERR_ALIGNMENT);
@@ -349,6 +349,7 @@ extern "C" moe_status_t moe_combine_bwd(const void* dout, const void* y_perm, co
                                         (uint4*)dy_perm, dw);
         MOE_CHECK_LAUNCH();
     }
+    if (dy_perm == nullptr) return MOE_OK;
     k_zero_padding_rows<<<rows_grid(row_cap), 256, 0, s>>>(row_id, gofs + E, row_cap, d / 8, (uint4*)dy_perm);
     MOE_CHECK_LAUNCH();
     return MOE_OK;

@@ -45,8 +45,8 @@ class MoELayer:
         self.row_id = z((M,), torch.int32)
         self.ws_route = z((ops.moe_route_workspace_size(T, E),), torch.uint8)
         self.ws_perm = z((ops.moe_permute_workspace_size(T, E),), torch.uint8)
-        # forward activations
-        self.x_perm = z((M, d), torch.bfloat16)
+        # forward activations (x_perm and dy_perm never exist in bf16: both
+        # are quantized, along both axes, straight from x and dout)
         self.xq, self.xs = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.a_pre = z((M, 2 * f), torch.bfloat16)
         self.h = z((M, f), torch.bfloat16)
@@ -54,7 +54,6 @@ class MoELayer:
         self.y_perm = z((M, d), torch.bfloat16)
         self.out = z((T, d), torch.bfloat16)
         # backward activations
-        self.dy_perm = z((M, d), torch.bfloat16)
         self.dw = z((T, k), torch.float32)
         self.dyq, self.dys = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.dyqT, self.dysT = z((d, M), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
@@ -109,41 +108,43 @@ class MoELayer:
         err = self.err
         ops.moe_route_topk(self.logits, k, self.score, self.normalize, self.topk_idx, self.topk_w, self.counts,
                            self.offsets, self.ws_route, err)
-        ops.moe_permute(self.x, self.topk_idx, E, M, self.gofs, self.slot_of, self.row_id, self.x_perm, True,
+        ops.moe_permute(self.x, self.topk_idx, E, M, self.gofs, self.slot_of, self.row_id, None, False,
                         self.ws_perm, err)
-        ops.mxfp8_group_quantize(self.x_perm, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.xq, self.xs, err)
+        # x_perm = x[row_id // k], both axes: rowwise for the up GEMM, the
+        # columnwise copy for the dW1 wgrad of the backward
+        ops.mxfp8_gather_quantize(self.x, self.gofs, E, M, self.row_id, k, None, True, True, self.xq, self.xs,
+                                  self.xqT, self.xsT, err)
         self._gemm(ops.MOE_GEMM_FWD, self.xq, self.xs, self.W1f, self.W1f_s, ops.MOE_B_GNK, self.gofs,
-                               E, M, 2 * f, d, ops.MOE_EPI_SWIGLU, None, self.a_pre, self.h, err)
-        ops.mxfp8_group_quantize(self.h, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.hq, self.hs, err)
+                   E, M, 2 * f, d, ops.MOE_EPI_SWIGLU, None, self.a_pre, self.h, err)
+        ops.mxfp8_gather_quantize(self.h, self.gofs, E, M, None, 1, None, True, True, self.hq, self.hs,
+                                  self.hqT, self.hsT, err)
         self._gemm(ops.MOE_GEMM_FWD, self.hq, self.hs, self.W2f, self.W2f_s, ops.MOE_B_GNK, self.gofs,
-                               E, M, d, f, ops.MOE_EPI_NONE, None, self.y_perm, None, err)
+                   E, M, d, f, ops.MOE_EPI_NONE, None, self.y_perm, None, err)
         ops.moe_unpermute_combine(self.y_perm, self.slot_of, self.topk_w, self.out, err)
 
     def backward_(self):
-        E, d, f, M = self.E, self.d, self.f, self.row_cap
+        E, k, d, f, M = self.E, self.k, self.d, self.f, self.row_cap
         err = self.err
-        ops.moe_combine_bwd(self.dout, self.y_perm, self.slot_of, self.topk_w, self.row_id, self.gofs, E,
-                            self.dy_perm, self.dw, err)
-        ops.mxfp8_group_quantize(self.dy_perm, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.dyq, self.dys, err)
-        ops.mxfp8_group_quantize(self.dy_perm, ops.MOE_QUANT_COLWISE_GROUPED, self.gofs, E, self.dyqT, self.dysT,
-                                 err)
-        ops.mxfp8_group_quantize(self.h, ops.MOE_QUANT_COLWISE_GROUPED, self.gofs, E, self.hqT, self.hsT, err)
+        # dw = <dout, y_perm> per (token, choice); dy_perm = w * dout is only
+        # ever materialised as its MXFP8 codes (both axes)
+        ops.moe_combine_bwd(self.dout, self.y_perm, self.slot_of, self.topk_w, None, None, E, None, self.dw, err,
+                            want_dy=False)
+        ops.mxfp8_gather_quantize(self.dout, self.gofs, E, M, self.row_id, k, self.topk_w, True, True, self.dyq,
+                                  self.dys, self.dyqT, self.dysT, err)
         # dH = dY W2^T with the SwiGLU backward fused: dA = [dgate | dup]
         self._gemm(ops.MOE_GEMM_DGRAD, self.dyq, self.dys, self.W2d, self.W2d_s, ops.MOE_B_GNK,
-                               self.gofs, E, M, f, d, ops.MOE_EPI_SWIGLU_BWD, self.a_pre, self.dA, None, err)
+                   self.gofs, E, M, f, d, ops.MOE_EPI_SWIGLU_BWD, self.a_pre, self.dA, None, err)
         # dW2_g = H_g^T dY_g
         self._gemm(ops.MOE_GEMM_WGRAD, self.hqT, self.hsT, self.dyqT, self.dysT, 0, self.gofs, E, f,
-                               d, M, ops.MOE_EPI_NONE, None, self.dW2, None, err)
-        ops.mxfp8_group_quantize(self.dA, ops.MOE_QUANT_ROWWISE, self.gofs, E, self.dAq, self.dAs, err)
-        ops.mxfp8_group_quantize(self.dA, ops.MOE_QUANT_COLWISE_GROUPED, self.gofs, E, self.dAqT, self.dAsT, err)
-        ops.mxfp8_group_quantize(self.x_perm, ops.MOE_QUANT_COLWISE_GROUPED, self.gofs, E, self.xqT, self.xsT,
-                                 err)
+                   d, M, ops.MOE_EPI_NONE, None, self.dW2, None, err)
+        ops.mxfp8_gather_quantize(self.dA, self.gofs, E, M, None, 1, None, True, True, self.dAq, self.dAs,
+                                  self.dAqT, self.dAsT, err)
         # dX_perm = dA W1^T
         self._gemm(ops.MOE_GEMM_DGRAD, self.dAq, self.dAs, self.W1d, self.W1d_s, ops.MOE_B_GNK,
-                               self.gofs, E, M, d, 2 * f, ops.MOE_EPI_NONE, None, self.dx_perm, None, err)
+                   self.gofs, E, M, d, 2 * f, ops.MOE_EPI_NONE, None, self.dx_perm, None, err)
         # dW1_g = X_g^T dA_g
         self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, 0, self.gofs, E, d,
-                               2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, err)
+                   2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, err)
         ops.moe_unpermute_combine(self.dx_perm, self.slot_of, None, self.dx, err)
         ops.moe_route_bwd(self.logits, self.topk_idx, self.dw, self.score, self.normalize, self.dlogits, err)
 

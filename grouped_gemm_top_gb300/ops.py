@@ -40,6 +40,7 @@ EXPORTS = [
     "moe_route_workspace_size", "moe_permute_workspace_size", "moe_route_topk",
     "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
     "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_route_topk_noalloc",
+    "mxfp8_gather_quantize",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -54,6 +55,8 @@ _SIGS = {
     "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_permute": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "mxfp8_group_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "mxfp8_gather_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp,
+                                     _vp]),
     "grouped_gemm_mxfp8": (_i32, [_i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _i32, _vp, _vp,
                                   _vp, _vp, _vp]),
     "moe_unpermute_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
@@ -182,6 +185,32 @@ def mxfp8_group_quantize(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, codes=None, 
     return codes, scales
 
 
+def mxfp8_gather_quantize(src, gofs, G, rows, row_id=None, k=1, row_w=None, rowwise=True, colwise=True,
+                          codes_row=None, scales_row=None, codes_col=None, scales_col=None, err=None, stream=None):
+    """Rowwise and/or group-aware columnwise MXFP8 codes of the permuted
+    matrix whose row s is src[row_id[s] // k] (times row_w[row_id[s]]), or
+    src[s] without row_id.  See include/moe.h.  Returns
+    (codes_row, scales_row, codes_col, scales_col), None for an axis not
+    asked for."""
+    cols = src.shape[1]
+    if rowwise:
+        codes_row = codes_row if codes_row is not None else _empty((rows, cols), torch.uint8, src)
+        scales_row = scales_row if scales_row is not None else _empty((sf_bytes(rows, cols),), torch.uint8, src)
+    else:
+        codes_row = scales_row = None
+    if colwise:
+        codes_col = codes_col if codes_col is not None else _empty((cols, rows), torch.uint8, src)
+        scales_col = scales_col if scales_col is not None else _empty((sf_bytes(rows, cols),), torch.uint8, src)
+    else:
+        codes_col = scales_col = None
+    _check("mxfp8_gather_quantize", lib.mxfp8_gather_quantize(_p(src), src.shape[0], cols, int(k), _p(row_id),
+                                                              _p(row_w), _p(gofs),
+                                                              int(G), int(rows), _p(codes_row), _p(scales_row),
+                                                              _p(codes_col), _p(scales_col), _p(err),
+                                                              _stream(stream)))
+    return codes_row, scales_row, codes_col, scales_col
+
+
 def grouped_gemm_mxfp8(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilogue=MOE_EPI_NONE,
                        epi_aux=None, d=None, d2=None, err=None, stream=None):
     """See include/moe.h.  Allocates d (and d2 for SwiGLU) when not given."""
@@ -209,11 +238,17 @@ def moe_unpermute_combine(y_perm, slot_of, topk_w, out=None, err=None, stream=No
     return out
 
 
-def moe_combine_bwd(dout, y_perm, slot_of, topk_w, row_id, gofs, E, dy_perm=None, dw=None, err=None, stream=None):
+def moe_combine_bwd(dout, y_perm, slot_of, topk_w, row_id, gofs, E, dy_perm=None, dw=None, err=None, stream=None,
+                    want_dy=True):
+    """dy_perm (unless want_dy is False: then dw only, dy_perm is None) and dw."""
     T, k = slot_of.shape
     d = dout.shape[1]
-    row_cap = row_id.shape[0]
-    dy_perm = dy_perm if dy_perm is not None else _empty((row_cap, d), torch.bfloat16, dout)
+    row_cap = row_id.shape[0] if row_id is not None else 0
+    if want_dy:
+        dy_perm = dy_perm if dy_perm is not None else _empty((row_cap, d), torch.bfloat16, dout)
+    else:
+        dy_perm = None
+        row_cap = max(row_cap, 1)
     dw = dw if dw is not None else _empty((T, k), torch.float32, dout)
     _check("moe_combine_bwd", lib.moe_combine_bwd(_p(dout), _p(y_perm), _p(slot_of), _p(topk_w), _p(row_id),
                                                   _p(gofs), T, d, k, E, row_cap, _p(dy_perm), _p(dw), _p(err),

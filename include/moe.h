@@ -203,6 +203,40 @@ MOE_API moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols,
                                   int32_t* err, void* stream);
 
 /*
+ * mxfp8_gather_quantize -- the rowwise and the group-aware columnwise MXFP8
+ * quantization of one (virtual) permuted matrix, from a single read of its
+ * rows ([TE-JAX] "What specialized optimizations...": group-aware
+ * quantization; "Optimization 2": the local permute feeding the grouped
+ * GEMM).  Row s of the matrix P [rows, cols] is
+ *   row_id == NULL:         P[s] = src[s]                 (src [rows, cols])
+ *   row_id[s] < 0:          P[s] = 0                      (padding row)
+ *   row_w == NULL:          P[s] = src[row_id[s] / k]     (src [T, cols])
+ *   otherwise:              P[s] = bf16(row_w[row_id[s]] * src[row_id[s] / k])
+ * so P is x_perm when src = x (a gather) and dy_perm of moe_combine_bwd
+ * when src = dout and row_w = topk_w; neither is ever stored in bf16.
+ *   src       [src_rows, cols] bf16, 16-byte aligned; cols % 128 == 0.
+ *             Without row_id, src_rows must equal rows.
+ *   row_id    [rows] int32 (from moe_permute) or NULL; k its tokens' top-k.
+ *             An entry with row_id[s] / k >= src_rows (below gofs[G]) sets
+ *             MOE_ERR_INVALID_ARG in *err and its row is read as zero.
+ *   gofs      [G+1] int32 group offsets (multiples of 128, monotone,
+ *             gofs[G] <= rows; validated, MOE_ERR_BAD_OFFSETS in *err and
+ *             nothing written if not).  Rows >= gofs[G] are not read and
+ *             their outputs are not written.
+ *   rows      the row capacity, % 128 == 0.
+ *   codes_row, scales_row   exactly MOE_QUANT_ROWWISE's output for P, or
+ *             both NULL.
+ *   codes_col, scales_col   exactly MOE_QUANT_COLWISE_GROUPED's output for
+ *             P (codes [cols, rows]), or both NULL.  At least one pair.
+ * All pointers are device pointers; outputs 16-byte aligned.
+ */
+MOE_API moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, int cols, int k,
+                                   const int32_t* row_id,
+                                   const float* row_w, const int32_t* gofs, int G, int64_t rows,
+                                   uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
+                                   uint8_t* scales_col, int32_t* err, void* stream);
+
+/*
  * grouped_gemm_mxfp8 -- one launch for all experts' GEMMs, each over its own
  * rows only ([TE-JAX] "Optimization 1: Grouped GEMM"), MXFP8 block-scaled
  * operands, fp32 accumulation, bf16 output.  Group offsets are read on the
@@ -261,6 +295,9 @@ MOE_API moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t* sl
  *   dy_perm[slot_of[t, j]] = bf16(w[t, j] * dout[t]); padding rows (row_id
  *   == -1, below gofs[E]) are written as zeros.
  *   dw[t, j] = <dout[t], y_perm[slot_of[t, j]]> (fp32).
+ *   dy_perm may be NULL: only dw is computed (row_id and gofs may then be
+ *   NULL too); mxfp8_gather_quantize then builds the quantized dy_perm
+ *   straight from dout.
  */
 MOE_API moe_status_t moe_combine_bwd(const void* dout, const void* y_perm, const int32_t* slot_of,
                              const float* topk_w, const int32_t* row_id, const int32_t* gofs,

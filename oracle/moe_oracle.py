@@ -38,7 +38,7 @@ __all__ = [
     "MXFP8_BLOCK", "E4M3_MAX", "bf16_round", "e4m3_value", "E4M3_VALUES", "e4m3_encode", "e8m0_exponent",
     "e8m0_byte", "e8m0_value", "mxfp8_quantize_rows", "mxfp8_quantize_cols_grouped",
     "mxfp8_dequantize_rows", "mxfp8_dequantize_cols", "route_topk", "group_counts",
-    "group_offsets", "aligned_group_offsets", "permute_slots", "permute",
+    "group_offsets", "aligned_group_offsets", "permute_slots", "permute", "fp32_round", "permute_scaled_bf16",
     "grouped_gemm", "grouped_gemm_wgrad", "swiglu", "swiglu_bwd", "combine",
     "combine_bwd", "route_bwd", "layer_forward", "layer_backward",
 ]
@@ -313,6 +313,34 @@ def permute(x, row_id, k):
     out = np.zeros((row_id.shape[0], x.shape[1]), dtype=np.float64)
     valid = row_id >= 0
     out[valid] = x[row_id[valid] // k]
+    return out
+
+
+def fp32_round(x):
+    """Round fp64 values to the nearest fp32 value, ties to even (IEEE-754
+    binary32: 24 significant bits)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def permute_scaled_bf16(src, row_id, k, w):
+    """The permuted, router-weighted rows as stored in bf16:
+    P[s] = bf16(fp32(w[t, j] * src[t])) with t*k + j = row_id[s], zero on
+    padding rows.  This is the dy_perm of ``combine_bwd`` (src = dout) in
+    the precision the step keeps it in.
+
+    Reading: the pages fix neither the precision of dy_perm nor of the
+    product; the activations of the step are bf16 and the routing weights
+    fp32, so the product of an fp32 weight and a bf16 gradient is formed in
+    fp32 (rounded once, ties to even) and stored as bf16 (rounded again).
+    The second rounding decides MXFP8 codes, so it is part of the
+    definition, not an error term."""
+    src = np.asarray(src, dtype=np.float64)
+    row_id = np.asarray(row_id, dtype=np.int64)
+    w = np.asarray(w, dtype=np.float64).reshape(-1)
+    out = np.zeros((row_id.shape[0], src.shape[1]), dtype=np.float64)
+    valid = row_id >= 0
+    rid = row_id[valid]
+    out[valid] = bf16_round(fp32_round(w[rid][:, None] * src[rid // k]))
     return out
 
 

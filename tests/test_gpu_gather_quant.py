@@ -1,0 +1,196 @@
+"""mxfp8_gather_quantize vs the oracle: both MXFP8 axes of the permuted (and
+router-weighted) rows, bit-exact codes and scales."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import atoms_rows_subset, atoms_to_rowmajor, gpu_ops, padded_layout, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    return gpu_ops()
+
+
+def _varied(rows, cols, seed):
+    """bf16 rows spanning many binades, with zero and tiny rows."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    x = torch.randn((rows, cols), generator=g, device="cuda")
+    x = x * torch.exp2(torch.randint(-30, 30, (rows, 1), generator=g, device="cuda").float())
+    x[0] = 0.0
+    if rows > 2:
+        x[2] *= 1e-36
+    return x.to(torch.bfloat16)
+
+
+def _routing(T, E, k, seed, skew=0.0):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits += (skew * -np.log1p(np.arange(E))).astype(np.float32)   # uneven load, some empty experts
+    idx, w = O.route_topk(logits, k)
+    slot_of, row_id = O.permute_slots(idx, E, 128)
+    gofs = O.aligned_group_offsets(O.group_counts(idx, E), 128)
+    return idx, w.astype(np.float32), slot_of, row_id, gofs
+
+
+def _dev(a, dtype):
+    return torch.tensor(np.ascontiguousarray(a), dtype=dtype, device="cuda")
+
+
+def _check_axes(ops, P, gofs, rows, cols, res):
+    """res = (codes_row, scales_row, codes_col, scales_col) of the GPU."""
+    Rp = int(gofs[-1])
+    cr, sr, cc, sc = res
+    if cr is not None:
+        rq, rs = O.mxfp8_quantize_rows(P)
+        assert np.array_equal(cr[:Rp].cpu().numpy(), rq)
+        assert np.array_equal(atoms_rows_subset(sr.cpu().numpy(), rows, cols, np.arange(Rp)), rs)
+    if cc is not None:
+        # groups start at multiples of 128 and their padding rows are zero,
+        # so the oracle's per-group blocks line up with the GPU layout
+        cq, cs, padded = O.mxfp8_quantize_cols_grouped(P, gofs)
+        assert np.array_equal(padded, gofs)
+        assert np.array_equal(cc[:, :Rp].cpu().numpy(), cq)
+        assert np.array_equal(atoms_to_rowmajor(sc.cpu().numpy(), cols, rows)[:, :Rp // 32], cs)
+
+
+@pytest.mark.parametrize("T,E,k,d,skew", [(1, 4, 2, 128, 0.0), (300, 8, 2, 256, 0.0), (1000, 16, 8, 512, 1.5),
+                                          (64, 64, 8, 128, 3.0), (517, 32, 4, 1152, 0.5)])
+def test_gather_both_axes(ops, T, E, k, d, skew):
+    """x_perm quantized straight from x through row_id (oracle: permute,
+    then each axis); ragged groups, empty groups, a single token."""
+    idx, w, slot_of, row_id, gofs = _routing(T, E, k, seed=T + E, skew=skew)
+    rows = ops.moe_row_capacity(T, E, k)
+    rid = np.full(rows, -1, dtype=np.int64)
+    rid[:len(row_id)] = row_id
+    x = _varied(T, d, seed=T * 7 + d)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = ops.mxfp8_gather_quantize(x, _dev(gofs, torch.int32), E, rows, row_id=_dev(rid, torch.int32), k=k,
+                                    err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    P = O.permute(to_np(x), row_id, k)
+    _check_axes(ops, P, gofs, rows, d, res)
+
+
+@pytest.mark.parametrize("T,E,k,d", [(200, 8, 2, 256), (1000, 16, 8, 512), (33, 5, 3, 384)])
+def test_gather_scaled_both_axes(ops, T, E, k, d):
+    """dy_perm = bf16(fp32(w * dout)) quantized straight from dout (oracle:
+    permute_scaled_bf16, then each axis)."""
+    idx, w, slot_of, row_id, gofs = _routing(T, E, k, seed=3 * T + k)
+    rows = ops.moe_row_capacity(T, E, k)
+    rid = np.full(rows, -1, dtype=np.int64)
+    rid[:len(row_id)] = row_id
+    dout = _varied(T, d, seed=T + 11)
+    res = ops.mxfp8_gather_quantize(dout, _dev(gofs, torch.int32), E, rows, row_id=_dev(rid, torch.int32), k=k,
+                                    row_w=_dev(w, torch.float32))
+    torch.cuda.synchronize()
+    P = O.permute_scaled_bf16(to_np(dout), row_id, k, w.astype(np.float64))
+    _check_axes(ops, P, gofs, rows, d, res)
+
+
+def test_gather_scaled_double_rounding_case(ops):
+    """The hand-worked fp32-then-bf16 rounding case of the oracle pins gives
+    the same MXFP8 code on the GPU (E4M3 0x3A, not 0x3B)."""
+    T, d, k = 1, 128, 1
+    src = torch.zeros((T, d), dtype=torch.float32)
+    src[0, 0] = float.fromhex("0x1.02p1")
+    src[0, 1] = 512.0
+    w = np.array([[float.fromhex("0x1.4e633ap-1")]], dtype=np.float32)
+    row_id = np.array([0] + [-1] * 127)
+    gofs = np.array([0, 128])
+    res = ops.mxfp8_gather_quantize(src.to(torch.bfloat16).cuda(), _dev(gofs, torch.int32), 1, 128,
+                                    row_id=_dev(row_id, torch.int32), k=k, row_w=_dev(w, torch.float32),
+                                    colwise=False)
+    torch.cuda.synchronize()
+    assert int(res[0][0, 0].item()) == 0x3A
+    P = O.permute_scaled_bf16(src.double().numpy(), row_id, k, w.astype(np.float64))
+    _check_axes(ops, P, gofs, 128, d, res)
+
+
+@pytest.mark.parametrize("sizes,cols", [([128], 128), ([5, 0, 130, 127, 1], 256), ([1000, 0, 300], 2048)])
+def test_plain_both_axes_skip_tail(ops, sizes, cols):
+    """Without row_id: both axes of src itself; rows >= gofs[G] are neither
+    read (NaN there) nor written (sentinels survive)."""
+    gofs = padded_layout(sizes)
+    Rp = int(gofs[-1])
+    rows = Rp + 256
+    x = torch.zeros((rows, cols), dtype=torch.bfloat16, device="cuda")
+    src = _varied(max(128, Rp), cols, seed=5 + cols)
+    for g, m in enumerate(sizes):
+        x[gofs[g]:gofs[g] + m] = src[gofs[g]:gofs[g] + m]
+    x[Rp:] = float("nan")
+    cr = torch.full((rows, cols), 0xAB, dtype=torch.uint8, device="cuda")
+    sr = torch.full((rows * cols // 32,), 0xCD, dtype=torch.uint8, device="cuda")
+    cc = torch.full((cols, rows), 0xAB, dtype=torch.uint8, device="cuda")
+    sc = torch.full((rows * cols // 32,), 0xCD, dtype=torch.uint8, device="cuda")
+    res = ops.mxfp8_gather_quantize(x, _dev(gofs, torch.int32), len(sizes), rows, codes_row=cr, scales_row=sr,
+                                    codes_col=cc, scales_col=sc)
+    torch.cuda.synchronize()
+    _check_axes(ops, to_np(x)[:Rp], gofs, rows, cols, res)
+    assert torch.all(cr[Rp:] == 0xAB) and torch.all(cc[:, Rp:] == 0xAB)
+    assert np.all(atoms_rows_subset(sr.cpu().numpy(), rows, cols, np.arange(Rp, rows)) == 0xCD)
+    assert np.all(atoms_to_rowmajor(sc.cpu().numpy(), cols, rows)[:, Rp // 32:] == 0xCD)
+
+
+@pytest.mark.parametrize("rowwise,colwise", [(True, False), (False, True)])
+def test_single_axis(ops, rowwise, colwise):
+    idx, w, slot_of, row_id, gofs = _routing(400, 8, 2, seed=21)
+    rows = ops.moe_row_capacity(400, 8, 2)
+    rid = np.full(rows, -1, dtype=np.int64)
+    rid[:len(row_id)] = row_id
+    x = _varied(400, 256, seed=22)
+    res = ops.mxfp8_gather_quantize(x, _dev(gofs, torch.int32), 8, rows, row_id=_dev(rid, torch.int32), k=2,
+                                    rowwise=rowwise, colwise=colwise)
+    torch.cuda.synchronize()
+    assert (res[0] is None) != rowwise and (res[2] is None) != colwise
+    _check_axes(ops, O.permute(to_np(x), row_id, 2), gofs, rows, 256, res)
+
+
+def test_rejects_bad_offsets(ops):
+    x = _varied(256, 128, seed=9)
+    cr = torch.full((256, 128), 0xAB, dtype=torch.uint8, device="cuda")
+    sr = torch.full((256 * 4,), 0xCD, dtype=torch.uint8, device="cuda")
+    for bad in ([0, 100, 256], [0, 256, 128], [0, 128, 384], [64, 128, 256]):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ops.mxfp8_gather_quantize(x, _dev(np.array(bad), torch.int32), 2, 256, colwise=False, codes_row=cr,
+                                  scales_row=sr, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == ops.MOE_ERR_BAD_OFFSETS
+        assert torch.all(cr == 0xAB) and torch.all(sr == 0xCD)
+
+
+def test_host_argument_checks(ops):
+    x = _varied(256, 128, seed=1)
+    gofs = _dev(np.array([0, 256]), torch.int32)
+    with pytest.raises(ops.MoEError):          # rows not a multiple of 128
+        ops.mxfp8_gather_quantize(x, gofs, 1, 200)
+    with pytest.raises(ops.MoEError):          # row_w without row_id
+        ops.mxfp8_gather_quantize(x, gofs, 1, 256, row_w=torch.ones(256, device="cuda"))
+    with pytest.raises(ops.MoEError):          # no output at all
+        ops.mxfp8_gather_quantize(x, gofs, 1, 256, rowwise=False, colwise=False)
+
+
+def test_row_id_beyond_src_is_reported(ops):
+    """A row_id naming a token past src's rows is an error in *err; that row
+    reads as zero and every other row is unaffected."""
+    T, E, k, d = 100, 4, 2, 128
+    idx, w, slot_of, row_id, gofs = _routing(T, E, k, seed=31)
+    rows = ops.moe_row_capacity(T, E, k)
+    rid = np.full(rows, -1, dtype=np.int64)
+    rid[:len(row_id)] = row_id
+    bad = int(slot_of[7, 1])
+    rid[bad] = T * k + 3
+    x = _varied(T, d, seed=32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = ops.mxfp8_gather_quantize(x, _dev(gofs, torch.int32), E, rows, row_id=_dev(rid, torch.int32), k=k,
+                                    colwise=False, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == ops.MOE_ERR_INVALID_ARG
+    ref_rid = row_id.copy()
+    ref_rid[bad] = -1
+    _check_axes(ops, O.permute(to_np(x), ref_rid, k), gofs, rows, d, res)

@@ -78,12 +78,15 @@ def test_tiny_layer_stagewise(ops, score, norm):
     Rp = int(gofs[-1])
     assert np.array_equal(L.gofs.cpu().numpy(), gofs)
     assert np.array_equal(L.slot_of.cpu().numpy(), slot_of)
+    assert np.array_equal(L.row_id.cpu().numpy()[:Rp], row_id)
+    # x_perm (never stored) quantized along both axes straight from x
     xp = O.permute(to_np(inp["x"]), row_id, k)
-    assert np.array_equal(to_np(L.x_perm)[:Rp], xp)
-    # rowwise quantization of x_perm
     rq, rs = O.mxfp8_quantize_rows(xp)
     assert np.array_equal(L.xq.cpu().numpy()[:Rp], rq)
     assert np.array_equal(atoms_to_rowmajor(L.xs.cpu().numpy(), M, d)[:Rp], rs)
+    xcq, xcs, _ = O.mxfp8_quantize_cols_grouped(xp, gofs)
+    assert np.array_equal(L.xqT.cpu().numpy()[:, :Rp], xcq)
+    assert np.array_equal(atoms_to_rowmajor(L.xsT.cpu().numpy(), d, M)[:, :Rp // 32], xcs)
     # up/gate GEMM + SwiGLU
     A = O.grouped_gemm(O.mxfp8_dequantize_rows(rq, rs), _w_fwd(L, 1), gofs)
     assert_bf16_close(L.a_pre[:Rp], A, what="a_pre")
@@ -97,11 +100,15 @@ def test_tiny_layer_stagewise(ops, score, norm):
     assert_bf16_close(L.out, O.combine(to_np(L.y_perm)[:Rp], slot_of, wg), what="out")
     # ---- backward
     dy, dw = O.combine_bwd(to_np(inp["dout"]), to_np(L.y_perm)[:Rp], slot_of, wg, Rp)
-    assert_bf16_close(L.dy_perm[:Rp], dy, what="dy_perm")
     assert_fp32_close(L.dw, dw, what="dw")
-    dyg = to_np(L.dy_perm)[:Rp]
+    # dy_perm (never stored) = bf16(fp32(w * dout)), quantized both ways
+    dyg = O.permute_scaled_bf16(to_np(inp["dout"]), row_id, k, wg)
+    assert_bf16_close(dyg, dy, what="dy_perm")
     dq, ds = O.mxfp8_quantize_rows(dyg)
     assert np.array_equal(L.dyq.cpu().numpy()[:Rp], dq)
+    dcq, dcs, _ = O.mxfp8_quantize_cols_grouped(dyg, gofs)
+    assert np.array_equal(L.dyqT.cpu().numpy()[:, :Rp], dcq)
+    assert np.array_equal(atoms_to_rowmajor(L.dysT.cpu().numpy(), d, M)[:, :Rp // 32], dcs)
     dH = O.grouped_gemm(O.mxfp8_dequantize_rows(dq, ds), _w_dgrad(L, 2), gofs)
     dA = O.swiglu_bwd(to_np(L.a_pre)[:Rp], dH)
     assert_bf16_close(L.dA[:Rp], dA, what="dA")
@@ -115,6 +122,8 @@ def test_tiny_layer_stagewise(ops, score, norm):
         assert_bf16_close(L.dW2[g], dW2[g], what=f"dW2[{g}]")
     daq, das = O.mxfp8_quantize_rows(to_np(L.dA)[:Rp])
     assert np.array_equal(L.dAq.cpu().numpy()[:Rp], daq)
+    dacq, _, _ = O.mxfp8_quantize_cols_grouped(to_np(L.dA)[:Rp], gofs)
+    assert np.array_equal(L.dAqT.cpu().numpy()[:, :Rp], dacq)
     dXp = O.grouped_gemm(O.mxfp8_dequantize_rows(daq, das), _w_dgrad(L, 1), gofs)
     assert_bf16_close(L.dx_perm[:Rp], dXp, what="dx_perm")
     Xh = _deq_actT(L.xqT, L.xsT, d, M, Rp)
@@ -171,7 +180,6 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     rt = torch.from_numpy(rows).cuda()
     # permute + quantize of the sampled rows
     xp = O.permute(to_np(inp["x"]), row_id[rows], k)
-    assert np.array_equal(to_np(L.x_perm[rt]), xp)
     rq, rs = O.mxfp8_quantize_rows(xp)
     assert np.array_equal(L.xq[rt].cpu().numpy(), rq)
     # per sampled row: the row's group weights, fetched group by group
@@ -203,7 +211,8 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     hq_ref, hs_ref = O.mxfp8_quantize_rows(h_rows)
     assert np.array_equal(hq_rows, hq_ref)
     Hd = O.mxfp8_dequantize_rows(hq_ref, hs_ref)
-    dq_ref, ds_ref = O.mxfp8_quantize_rows(to_np(L.dy_perm[rt]))
+    wall = L.topk_w.cpu().numpy().astype(np.float64)
+    dq_ref, ds_ref = O.mxfp8_quantize_rows(O.permute_scaled_bf16(to_np(inp["dout"]), row_id[rows], k, wall))
     assert np.array_equal(L.dyq[rt].cpu().numpy(), dq_ref)
     DYd = O.mxfp8_dequantize_rows(dq_ref, ds_ref)
     daq_ref, das_ref = O.mxfp8_quantize_rows(to_np(L.dA[rt]))

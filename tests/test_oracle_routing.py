@@ -173,6 +173,55 @@ def test_combine_bwd_is_adjoint_and_fd():
         assert np.isclose(fd, dw[t, j], rtol=1e-6, atol=1e-9)
 
 
+def test_fp32_round_ties_and_spacing():
+    one = 1.0
+    assert O.fp32_round(one + 2.0 ** -24) == one                 # tie -> even
+    assert O.fp32_round(one + 3 * 2.0 ** -24) == one + 2.0 ** -22  # tie -> even (up)
+    assert O.fp32_round(one + 2.0 ** -24 + 2.0 ** -40) == one + 2.0 ** -23
+    assert O.fp32_round(2.0 ** -149) == 2.0 ** -149              # smallest subnormal
+    assert O.fp32_round(2.0 ** -151) == 0.0
+    assert np.isinf(O.fp32_round(3.5e38))
+
+
+def test_permute_scaled_bf16_special_cases():
+    rng = np.random.default_rng(13)
+    T, E, k, d = 40, 6, 3, 16
+    idx, w = O.route_topk(rng.standard_normal((T, E)).astype(np.float32), k)
+    slot_of, row_id = O.permute_slots(idx, E, 32)
+    src = O.bf16_round(rng.standard_normal((T, d)))
+    # unit weights: exactly the permute; powers of two: exactly w * src
+    assert np.array_equal(O.permute_scaled_bf16(src, row_id, k, np.ones((T, k))), O.permute(src, row_id, k))
+    p2 = 2.0 ** rng.integers(-6, 3, size=(T, k)).astype(np.float64)
+    dy_exact, _ = O.combine_bwd(src, np.zeros((len(row_id), d)), slot_of, p2, len(row_id))
+    assert np.array_equal(O.permute_scaled_bf16(src, row_id, k, p2), dy_exact)
+    # general weights: within one bf16 rounding of the fp64 combine_bwd rows
+    dy_ref, _ = O.combine_bwd(src, np.zeros((len(row_id), d)), slot_of, w, len(row_id))
+    got = O.permute_scaled_bf16(src, row_id, k, w)
+    assert np.all(got[row_id < 0] == 0)
+    assert np.all(np.abs(got - dy_ref) <= 2.0 ** -8 * np.abs(dy_ref) * (1 + 1e-6))
+
+
+def test_permute_scaled_bf16_double_rounding_by_hand():
+    # src = 0x1.02p1 (bf16), w = 0x1.4e633ap-1 (fp32).  The exact product
+    # 0x1.51000074p0 lies just above the bf16 tie 0x1.51p0 (fraction bits
+    # 0101 0001); its fp32 rounding drops the tail (fraction bit 24 is 0)
+    # and lands exactly on the tie, which bf16 rounds to even: 0x1.50p0 =
+    # 1.3125.  A single rounding of the exact product gives 0x1.52p0.
+    src = np.array([[float.fromhex("0x1.02p1"), 512.0] + [0.0] * 30])
+    w = np.array([[float.fromhex("0x1.4e633ap-1")]])
+    got = O.permute_scaled_bf16(src, np.array([0]), 1, w)
+    assert got[0, 0] == 1.3125
+    assert O.bf16_round(src[0, 0] * w[0, 0]) == float.fromhex("0x1.52p0")
+    # the rounding reaches the MXFP8 code: the block max 512 w ~ 334.4 gives
+    # scale 2^0, and 1.3125 is the E4M3 tie between 1.25 (0x3A, even) and
+    # 1.375 (0x3B); 0x1.52p0 = 1.328125 would round up to 0x3B.
+    codes, scales = O.mxfp8_quantize_rows(got)
+    assert scales[0, 0] == 127 and codes[0, 0] == 0x3A
+    alt = got.copy()
+    alt[0, 0] = float.fromhex("0x1.52p0")
+    assert O.mxfp8_quantize_rows(alt)[0][0, 0] == 0x3B
+
+
 @pytest.mark.parametrize("score,normalize", [("softmax", True), ("softmax", False),
                                              ("sigmoid", True), ("sigmoid", False)])
 def test_route_bwd_finite_differences(score, normalize):
