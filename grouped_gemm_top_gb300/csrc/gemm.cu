@@ -6,7 +6,7 @@
 // [TE-JAX] Figure 3: the grouped MLP is two grouped GEMMs (up/gate, down);
 // the SwiGLU between them is fused into the up/gate epilogue here.
 //
-// Design (one persistent CTA per SM, 256 threads, warp-specialised):
+// Design (one persistent CTA per SM, 384 threads, warp-specialised):
 //   warp 0 lane 0   TMA producer: per k-step one 128x128 A box, two 128x128
 //                   B boxes (N = 256) and the three 512-byte scale atoms, all
 //                   completing on one mbarrier (expect_tx).
@@ -14,7 +14,8 @@
 //                   tcgen05.cp (scales smem -> TMEM) and 4 x
 //                   tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each) per
 //                   k-step into a 128x256 fp32 accumulator in TMEM.
-//   warps 4..7      epilogue: tcgen05.ld of their 32 TMEM lanes, bf16
+//   warps 4..11     epilogue, two warps per TMEM lane quarter (one per
+//                   128-column half): tcgen05.ld of their 32 lanes, bf16
 //                   conversion, fused SwiGLU / SwiGLU-backward, stores.
 // The tile list is derived on the device from the group offsets (multiples
 // of 128), so a tile never straddles two groups and the host never sees the
@@ -288,6 +289,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 epilogue_zero<BN>(p, row, ti.nt, half);
                 continue;
             }
+            ApreChunk apre;
+            if (p.epi == MOE_EPI_SWIGLU_BWD) {
+                if (t + gridDim.x < total) {      // FWD/DGRAD only: rows = m-tile * 128
+                    int64_t mt;
+                    int nt;
+                    band_decode(t + gridDim.x, total_mt, p.n_tiles, p.band, mt, nt);
+                    swiglu_bwd_prefetch_l2<BN>(p, mt * BM + quarter * 32 + lane, nt, half);
+                }
+                swiglu_bwd_prefetch<BN>(p, row, ti.nt, half, 0, apre);
+            }
             if (!mbar_wait(tfull_bar(acc), acc_phase, p, abort_flag)) break;
             tc_fence_after();
             const uint32_t tacc = lane_base + (uint32_t)(acc * BN);
@@ -297,7 +308,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty);
             };
-            if (BN == 256 && p.epi != MOE_EPI_SWIGLU_BWD) {
+            if (p.epi == MOE_EPI_SWIGLU_BWD) {
+                epilogue_swiglu_bwd<BN>(p, tacc, row, ti.nt, half, release, apre);
+            } else if (BN == 256) {
                 epilogue_tile_staged(p, tacc, row, ti.nt, half, release);
             } else {
                 epilogue_tile<BN>(p, tacc, row, ti.nt, half);
@@ -343,13 +356,16 @@ cudaError_t gemm_set_attributes() {
     return gemm_set_attributes_2sm();
 }
 
-// Kernel choice.  By default every GEMM runs on the 1-SM kernel with
-// 128 x 256 tiles: with per-expert weight operands (MOE_B_GNK) it matched or
-// beat the CTA-pair kernel on every measured shape.  The environment variable
-// MOE_GEMM_2SM selects the CTA-pair kernel (gemm2sm.cu) instead, for
-// measurement: 256 = 256 x 256 pair tiles, 128 = 256 x 128 pair tiles with
-// two TMEM accumulators per CTA.  WGRAD with M % 256 != 0 always uses the
-// 1-SM kernel.
+// Kernel choice.  WGRAD runs on the CTA-pair kernel (gemm2sm.cu, 256 x 256
+// pair tiles, TMA-store epilogue): its short contraction (one group's rows)
+// makes the 1-SM kernel wait on operand loads, and the pair halves each SM's
+// operand traffic.  FWD and DGRAD run on the 1-SM kernel with 128 x 256
+// tiles: a group's last 128-row tile would leave half of a 256-row pair tile
+// idle, which cost more than the pair kernel saved on these shapes.  The
+// environment variable MOE_GEMM_2SM forces one kernel for every mode, for
+// measurement: 0 = 1-SM, 256 = 256 x 256 pair tiles, 128 = 256 x 128 pair
+// tiles with two TMEM accumulators per CTA.  WGRAD with M % 256 != 0 always
+// uses the 1-SM kernel.
 static int gemm_2sm_mode() {
     static int mode = [] {
         const char* e = getenv("MOE_GEMM_2SM");
@@ -381,6 +397,27 @@ static bool make_sf_map(CUtensorMap* m, const void* base, int64_t atoms, int box
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// bf16 output [rows, N] for TMA stores: 32-row x 64-column boxes (128-byte
+// rows, 128-byte swizzle).
+static bool make_d_map(CUtensorMap* m, void* base, int64_t rows, int N) {
+    cuuint64_t gdim[2] = {(cuuint64_t)N, (cuuint64_t)rows}, gstr[1] = {(cuuint64_t)N * 2};
+    cuuint32_t box[2] = {64, 32}, estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstr, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// TMA-store epilogue of the pair kernel (MOE_EPI_NONE, N = 256): on unless
+// the environment variable MOE_GEMM_TMA_STORE=0 (kept for measurement).
+static bool gemm_tma_store() {
+    static bool on = [] {
+        const char* e = getenv("MOE_GEMM_TMA_STORE");
+        return e == nullptr || atoi(e) != 0;
+    }();
+    return on;
 }
 
 // rank-2/3 uint8 tensor map, 128x128 boxes, 128-byte swizzle
@@ -480,7 +517,7 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     const int grid = (int)(upper_tiles < sms ? (upper_tiles > 0 ? upper_tiles : 1) : sms);
     int sel = gemm_2sm_mode();
-    if (sel < 0) sel = 0;
+    if (sel < 0) sel = mode == MOE_GEMM_WGRAD ? 256 : 0;
     const int bn2 = sel == 256 && N % 256 == 0 ? 256 : 128;
     const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {
@@ -514,7 +551,14 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
         CUtensorMap tmSFA, tmSFB;
         MOE_REQUIRE(make_sf_map(&tmSFA, a_sf, atoms_a, 2) && make_sf_map(&tmSFB, b_sf, atoms_b, 2 * (bn2 / 128)),
                     MOE_ERR_CUDA);
-        if (gemm_launch_2sm(bn2, tmA, tmB2, tmSFA, tmSFB, p, clusters, (cudaStream_t)stream) != cudaSuccess)
+        // D through the TMA: bf16 [rows, N] in 32-row x 64-column boxes
+        CUtensorMap tmD = tmA;
+        p.tma_store = bn2 == 256 && epilogue == MOE_EPI_NONE && gemm_tma_store();
+        if (p.tma_store) {
+            const int64_t drows = mode == MOE_GEMM_WGRAD ? (int64_t)G * M : M;
+            MOE_REQUIRE(make_d_map(&tmD, d, drows, N), MOE_ERR_CUDA);
+        }
+        if (gemm_launch_2sm(bn2, tmA, tmB2, tmSFA, tmSFB, tmD, p, clusters, (cudaStream_t)stream) != cudaSuccess)
             return MOE_ERR_CUDA;
     } else if (BN == 256)
         k_grouped_gemm<256><<<grid, THREADS, Cfg<256>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);

@@ -44,16 +44,19 @@ struct C2 {
     static constexpr int BN = BN_;
     static constexpr int BH = BN_ / 2;                  // B rows per CTA
     static constexpr int NACC = BN_ == 128 ? 2 : 1;
-    static constexpr int STAGES = BN_ == 128 ? 8 : 6;
+    static constexpr int STAGES = BN_ == 128 ? 8 : 5;
     static constexpr int A_STAGE = BM * BK;             // this CTA's 128 A rows
     static constexpr int B_STAGE = BH * BK;             // this CTA's half of B
     static constexpr int SFA_BYTES = 512;
     static constexpr int SFB_BYTES = (BN_ / 128) * 512; // scales of all BN B rows
     static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_BYTES + SFB_BYTES;
     static constexpr uint32_t SF0 = NACC * BN_;         // TMEM: accumulators, then scales
+    // TMA-store staging of the epilogue (N = 256): 4 KB per epilogue warp
+    static constexpr int EPI_BYTES = BN_ == 256 ? EPI_WARPS * 4096 : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
-    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;       // 1024-byte aligned
+    static constexpr int OFF_SFA = OFF_EPI + EPI_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;  // full[S], empty[S], tfull[A], tempty[A], drain
     static constexpr int NBAR = 2 * STAGES + 2 * NACC + 1;
@@ -63,6 +66,7 @@ struct C2 {
     static constexpr int SMEM_BYTES = OFF_PT + (MAX_G + 1) * 4 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SF0 + STAGES * TMEM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
+    static_assert(OFF_EPI % 1024 == 0, "swizzled staging alignment");
 };
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -207,7 +211,7 @@ template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                       const Params p) {
+                       const __grid_constant__ CUtensorMap tmD, const Params p) {
     using C = C2<BN>;
     constexpr int STAGES = C::STAGES, NACC = C::NACC, BH = C::BH;
     constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_SFA = C::OFF_SFA, OFF_SFB = C::OFF_SFB;
@@ -400,6 +404,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 epilogue_zero<BN>(p, row, ti.nt, half);
                 continue;
             }
+            ApreChunk apre;
+            if (p.epi == MOE_EPI_SWIGLU_BWD && ti.valid) {
+                if (t + npairs < total) {
+                    Tile2 tn;
+                    get_tile2<BN>(p, s_gofs, s_pt, total_pm, t + npairs, rank, tn);
+                    if (tn.valid) swiglu_bwd_prefetch_l2<BN>(p, tn.out_row + quarter * 32 + lane, tn.nt, half);
+                }
+                swiglu_bwd_prefetch<BN>(p, row, ti.nt, half, 0, apre);
+            }
             if (!mbar_wait_cluster(tfull_bar(acc), acc_phase, p, abort_flag)) break;
             tc_fence_after();
             const uint32_t tacc = lane_base + (uint32_t)(acc * BN);
@@ -411,7 +424,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             };
             if (!ti.valid) {
                 release();
-            } else if (BN == 256 && p.epi != MOE_EPI_SWIGLU_BWD) {
+            } else if (p.epi == MOE_EPI_SWIGLU_BWD) {
+                epilogue_swiglu_bwd<BN>(p, tacc, row, ti.nt, half, release, apre);
+            } else if (BN == 256 && p.tma_store) {
+                epilogue_tile_tma(&tmD, smem_u32(smem + C::OFF_EPI + 4096 * ew), tacc, row - lane, ti.nt, half, lane,
+                                  release);
+            } else if (BN == 256) {
                 epilogue_tile_staged(p, tacc, row, ti.nt, half, release);
             } else {
                 epilogue_tile<BN>(p, tacc, row, ti.nt, half);
@@ -422,6 +440,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
+        // the TMA stores issued from this warp's staging buffer are complete
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -479,14 +500,15 @@ cudaError_t gemm_set_attributes_2sm() {
 int gemm_max_clusters_2sm(int bn) { return g_max_clusters[bn == 256 ? 1 : 0]; }
 
 cudaError_t gemm_launch_2sm(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                            const CUtensorMap& tmSFB, const gg::Params& p, int clusters, cudaStream_t stream) {
+                            const CUtensorMap& tmSFB, const CUtensorMap& tmD, const gg::Params& p, int clusters,
+                            cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     if (bn == 256) {
         cudaLaunchConfig_t cfg = launch_cfg<256>(clusters, stream, attr);
-        return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<256>, tmA, tmB, tmSFA, tmSFB, p);
+        return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<256>, tmA, tmB, tmSFA, tmSFB, tmD, p);
     }
     cudaLaunchConfig_t cfg = launch_cfg<128>(clusters, stream, attr);
-    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<128>, tmA, tmB, tmSFA, tmSFB, p);
+    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<128>, tmA, tmB, tmSFA, tmSFB, tmD, p);
 }
 
 }  // namespace moe

@@ -35,6 +35,7 @@ struct Params {
     int32_t* err;
     uint64_t timeout_ns;
     int band;           // m-tiles per raster band (consecutive tiles share the B tile)
+    int tma_store;      // pair kernel, BN = 256, MOE_EPI_NONE: write D through the TMA (tensor map tmD)
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -105,6 +106,27 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
+// TMA store of a shared-memory box (bulk-group completion) and its fences.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the bulk stores committed so far have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// the bulk stores committed so far are complete
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// this thread's shared-memory writes become visible to the TMA (async proxy)
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -154,6 +176,32 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit words from TMEM (this warp's lane
+// quarter), without waiting: the registers are valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// sigmoid(x) with the fast exponential and division; x is clamped at -80
+// so that 1 + exp(-x) stays finite (sigmoid(-80) ~ 2e-35).
+__device__ __forceinline__ float fast_sigmoid(float x) {
+    return __fdividef(1.f, 1.f + __expf(-fmaxf(x, -80.f)));
+}
+
+// Two bf16 (RNE) packed into one word, `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // 32 lanes x 32 columns of fp32 from TMEM (this warp's lane quarter).
@@ -227,10 +275,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
             store_row32(p.d + row * N + hcol, v);
             store_row32(p.d + row * N + f + hcol, up);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float s = 1.f / (1.f + expf(-v[i]));
-                h[i] = v[i] * s * up[i];
-            }
+            for (int i = 0; i < 32; ++i) h[i] = v[i] * fast_sigmoid(v[i]) * up[i];
             store_row32(p.d2 + row * f + hcol, h);
         }
     } else if (p.epi == MOE_EPI_SWIGLU_BWD) {
@@ -244,7 +289,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
             load_row32(p.aux + row * ld + N + col, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float s = 1.f / (1.f + expf(-g[i]));
+                const float s = fast_sigmoid(g[i]);
                 dg[i] = v[i] * u[i] * s * (1.f + g[i] * (1.f - s));
                 du[i] = v[i] * g[i] * s;
             }
@@ -270,66 +315,200 @@ __device__ __forceinline__ void st_global_v8(void* dst, uint32_t a0, uint32_t a1
 
 // Register-staged epilogue for 256-wide tiles: the calling thread drains
 // its 128 accumulator columns (column half `half`) into registers as packed
-// bf16, calls release() so the MMA warp can reuse TMEM, and only then writes
-// global memory, overlapped with the next tile's MMAs.  SwiGLU-backward
-// needs its fp32 dH next to two bf16 inputs and keeps epilogue_tile.
+// bf16 (two TMEM loads in flight per wait), calls release() so the MMA warp
+// can reuse TMEM, and only then writes global memory, overlapped with the
+// next tile's MMAs.  SwiGLU-backward has its own pipelined epilogue below.
 template <typename Release>
 __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t tacc, int64_t row, int nt, int half,
                                                      Release release) {
-    float v[32];
+    uint32_t ra[32], rb[32];
     if (p.epi == MOE_EPI_SWIGLU) {
         // units u = 2*half, 2*half+1: gate columns [128q + 32c, +32) and up
-        // columns [128q + 64 + 32c, +32) with q = u / 2 = half, c = u % 2
-        uint32_t pg[32], pu[32], ph[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            float up[32];
-            tmem_ld32(tacc + 128 * half + 32 * c, v);
-            tmem_ld32(tacc + 128 * half + 64 + 32 * c, up);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float h0 = v[2 * i] / (1.f + expf(-v[2 * i])) * up[2 * i];
-                const float h1 = v[2 * i + 1] / (1.f + expf(-v[2 * i + 1])) * up[2 * i + 1];
-                __nv_bfloat162 g2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                __nv_bfloat162 u2 = __floats2bfloat162_rn(up[2 * i], up[2 * i + 1]);
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(h0, h1);
-                pg[16 * c + i] = *reinterpret_cast<uint32_t*>(&g2);
-                pu[16 * c + i] = *reinterpret_cast<uint32_t*>(&u2);
-                ph[16 * c + i] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-        }
-        release();
+        // columns [128q + 64 + 32c, +32) with q = u / 2 = half, c = u % 2.
+        // Chunk 0 is converted while chunk 1 is still in TMEM and written
+        // after the release, so at most one chunk of fp32 is live.
         const int64_t N = p.N, f = p.N / 2;
         const int64_t hcol = (int64_t)nt * 128 + 64 * half;     // 64 h columns of this thread
         uint32_t* dg = reinterpret_cast<uint32_t*>(p.d + row * N + hcol);
         uint32_t* du = reinterpret_cast<uint32_t*>(p.d + row * N + f + hcol);
         uint32_t* dh = reinterpret_cast<uint32_t*>(p.d2 + row * f + hcol);
+        uint32_t pg[16], pu[16], ph[16];
+        auto convert = [&]() {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            st_global_v8(dg + 8 * q, pg[8 * q], pg[8 * q + 1], pg[8 * q + 2], pg[8 * q + 3], pg[8 * q + 4],
-                         pg[8 * q + 5], pg[8 * q + 6], pg[8 * q + 7]);
-            st_global_v8(du + 8 * q, pu[8 * q], pu[8 * q + 1], pu[8 * q + 2], pu[8 * q + 3], pu[8 * q + 4],
-                         pu[8 * q + 5], pu[8 * q + 6], pu[8 * q + 7]);
-            st_global_v8(dh + 8 * q, ph[8 * q], ph[8 * q + 1], ph[8 * q + 2], ph[8 * q + 3], ph[8 * q + 4],
-                         ph[8 * q + 5], ph[8 * q + 6], ph[8 * q + 7]);
-        }
+            for (int i = 0; i < 16; ++i) {
+                const float g0 = __uint_as_float(ra[2 * i]), g1 = __uint_as_float(ra[2 * i + 1]);
+                const float u0 = __uint_as_float(rb[2 * i]), u1 = __uint_as_float(rb[2 * i + 1]);
+                pg[i] = pack_bf16x2(g0, g1);
+                pu[i] = pack_bf16x2(u0, u1);
+                ph[i] = pack_bf16x2(g0 * fast_sigmoid(g0) * u0, g1 * fast_sigmoid(g1) * u1);
+            }
+        };
+        auto store = [&](int c) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int o = 16 * c + 8 * q;
+                st_global_v8(dg + o, pg[8 * q], pg[8 * q + 1], pg[8 * q + 2], pg[8 * q + 3], pg[8 * q + 4],
+                             pg[8 * q + 5], pg[8 * q + 6], pg[8 * q + 7]);
+                st_global_v8(du + o, pu[8 * q], pu[8 * q + 1], pu[8 * q + 2], pu[8 * q + 3], pu[8 * q + 4],
+                             pu[8 * q + 5], pu[8 * q + 6], pu[8 * q + 7]);
+                st_global_v8(dh + o, ph[8 * q], ph[8 * q + 1], ph[8 * q + 2], ph[8 * q + 3], ph[8 * q + 4],
+                             ph[8 * q + 5], ph[8 * q + 6], ph[8 * q + 7]);
+            }
+        };
+        tmem_ld32_issue(tacc + 128 * half, ra);
+        tmem_ld32_issue(tacc + 128 * half + 64, rb);
+        tmem_wait_ld();
+        convert();
+        tmem_ld32_issue(tacc + 128 * half + 32, ra);
+        tmem_ld32_issue(tacc + 128 * half + 96, rb);
+        tmem_wait_ld();
+        release();
+        store(0);
+        convert();
+        store(1);
     } else {
         uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tacc + 128 * half + 32 * c, v);
+        for (int c = 0; c < 4; c += 2) {
+            tmem_ld32_issue(tacc + 128 * half + 32 * c, ra);
+            tmem_ld32_issue(tacc + 128 * half + 32 * (c + 1), rb);
+            tmem_wait_ld();
+            if (c == 2) release();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                pk[16 * c + i] = *reinterpret_cast<uint32_t*>(&b2);
+                pk[16 * c + i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+                pk[16 * (c + 1) + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
             }
         }
-        release();
         uint32_t* dst = reinterpret_cast<uint32_t*>(p.d + row * p.N + (int64_t)nt * 256 + 128 * half);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             st_global_v8(dst + 8 * q, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2], pk[8 * q + 3], pk[8 * q + 4],
                          pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
+    }
+}
+
+// TMA-store epilogue for 256-wide tiles without activation: the warp drains
+// its 32 rows x 128 columns into registers as packed bf16 and releases TMEM
+// (as epilogue_tile_staged), then writes two 32 x 64 boxes through its
+// 4 KB staging buffer `buf` (1024-byte aligned, 128-byte swizzle: 16-byte
+// chunk c of row r sits at chunk c ^ (r % 8), which is also conflict-free
+// for the row-per-lane shared stores) with TMA stores.  The TMA writes whole
+// 128-byte lines; the warp's stores are asynchronous and the buffer is
+// reused once the previous store has read it.  `row0` is the warp's first
+// output row.
+template <typename Release>
+__device__ __forceinline__ void epilogue_tile_tma(const CUtensorMap* tmD, uint32_t buf, uint32_t tacc, int64_t row0,
+                                                  int nt, int half, int lane, Release release) {
+    uint32_t ra[32], rb[32], pk[64];
+#pragma unroll
+    for (int c = 0; c < 4; c += 2) {
+        tmem_ld32_issue(tacc + 128 * half + 32 * c, ra);
+        tmem_ld32_issue(tacc + 128 * half + 32 * (c + 1), rb);
+        tmem_wait_ld();
+        if (c == 2) release();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            pk[16 * c + i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+            pk[16 * (c + 1) + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+        }
+    }
+    const uint32_t rowaddr = buf + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            st_shared_v4(rowaddr + ((uint32_t)(c ^ (lane & 7)) << 4), pk[32 * j + 4 * c], pk[32 * j + 4 * c + 1],
+                         pk[32 * j + 4 * c + 2], pk[32 * j + 4 * c + 3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmD, buf, nt * 256 + 128 * half + 64 * j, (int)row0);
+            bulk_commit_group();
+        }
+    }
+}
+
+// SwiGLU-backward epilogue, software-pipelined: the bf16 gate/up values of
+// a 32-column chunk (a_pre, global memory) are loaded one chunk ahead, the
+// first chunk before the accumulator is ready (swiglu_bwd_prefetch), so the
+// TMEM accumulator is held only for the TMEM loads and the arithmetic.
+struct ApreChunk {
+    uint4 g[4], u[4];   // 32 bf16 gate, 32 bf16 up
+};
+template <int BN>
+__device__ __forceinline__ void swiglu_bwd_prefetch(const Params& p, int64_t row, int nt, int half, int c,
+                                                    ApreChunk& a) {
+    const int64_t N = p.N, ld = 2 * (int64_t)p.N;
+    const int64_t col = (int64_t)nt * BN + half * (BN / 2) + 32 * c;
+    const uint4* sg = reinterpret_cast<const uint4*>(p.aux + row * ld + col);
+    const uint4* su = reinterpret_cast<const uint4*>(p.aux + row * ld + N + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        a.g[q] = __ldg(sg + q);
+        a.u[q] = __ldg(su + q);
+    }
+}
+// L2 prefetch of the gate/up values a thread's epilogue reads for a tile
+// (issued one tile ahead, so that the loads of swiglu_bwd_prefetch hit L2).
+template <int BN>
+__device__ __forceinline__ void swiglu_bwd_prefetch_l2(const Params& p, int64_t row, int nt, int half) {
+    const int64_t N = p.N, ld = 2 * (int64_t)p.N;
+    const int64_t col = (int64_t)nt * BN + half * (BN / 2);
+    const char* g = reinterpret_cast<const char*>(p.aux + row * ld + col);
+    const char* u = reinterpret_cast<const char*>(p.aux + row * ld + N + col);
+#pragma unroll
+    for (int i = 0; i < BN; i += 128) {      // BN / 2 columns = BN bytes per operand
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(g + i));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(u + i));
+    }
+}
+__device__ __forceinline__ uint32_t uint4_word(const uint4& v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+template <int BN, typename Release>
+__device__ __forceinline__ void epilogue_swiglu_bwd(const Params& p, uint32_t tacc, int64_t row, int nt, int half,
+                                                    Release release, ApreChunk& a) {
+    constexpr int NC = BN / 64;             // 32-column chunks per thread
+    const int64_t N = p.N, ld = 2 * (int64_t)p.N;
+    uint32_t r[32];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        tmem_ld32_issue(tacc + half * (BN / 2) + 32 * c, r);     // dH
+        tmem_wait_ld();
+        if (c == NC - 1) release();
+        ApreChunk nx;
+        if (c + 1 < NC) swiglu_bwd_prefetch<BN>(p, row, nt, half, c + 1, nx);
+        uint32_t pdg[16], pdu[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t gw = uint4_word(a.g[i >> 2], i & 3), uw = uint4_word(a.u[i >> 2], i & 3);
+            float dg[2], du[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float g = __uint_as_float(e ? (gw & 0xFFFF0000u) : (gw << 16));
+                const float u = __uint_as_float(e ? (uw & 0xFFFF0000u) : (uw << 16));
+                const float dh = __uint_as_float(r[2 * i + e]);
+                const float s = fast_sigmoid(g);
+                dg[e] = dh * u * s * (1.f + g * (1.f - s));
+                du[e] = dh * g * s;
+            }
+            pdg[i] = pack_bf16x2(dg[0], dg[1]);
+            pdu[i] = pack_bf16x2(du[0], du[1]);
+        }
+        const int64_t col = (int64_t)nt * BN + half * (BN / 2) + 32 * c;
+        uint32_t* og = reinterpret_cast<uint32_t*>(p.d + row * ld + col);
+        uint32_t* ou = reinterpret_cast<uint32_t*>(p.d + row * ld + N + col);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            st_global_v8(og + 8 * q, pdg[8 * q], pdg[8 * q + 1], pdg[8 * q + 2], pdg[8 * q + 3], pdg[8 * q + 4],
+                         pdg[8 * q + 5], pdg[8 * q + 6], pdg[8 * q + 7]);
+            st_global_v8(ou + 8 * q, pdu[8 * q], pdu[8 * q + 1], pdu[8 * q + 2], pdu[8 * q + 3], pdu[8 * q + 4],
+                         pdu[8 * q + 5], pdu[8 * q + 6], pdu[8 * q + 7]);
+        }
+        if (c + 1 < NC) a = nx;
     }
 }
 
@@ -348,5 +527,6 @@ __device__ __forceinline__ void epilogue_zero(const Params& p, int64_t row, int 
 cudaError_t gemm_set_attributes_2sm();   // gemm2sm.cu
 int gemm_max_clusters_2sm(int bn);        // co-resident CTA pairs for N = bn pair tiles
 cudaError_t gemm_launch_2sm(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                            const CUtensorMap& tmSFB, const gg::Params& p, int clusters, cudaStream_t stream);
+                            const CUtensorMap& tmSFB, const CUtensorMap& tmD, const gg::Params& p, int clusters,
+                            cudaStream_t stream);
 }  // namespace moe
