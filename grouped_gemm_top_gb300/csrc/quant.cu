@@ -239,20 +239,27 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
 // combine backward), so neither bf16 permuted matrix is written and read
 // back; h and dA are read once for both axes.
 //
-// A CTA owns one 128-row tile and a run of 128-column tiles: it checks the
-// group offsets once (in parallel), looks up its 128 source rows once, and
-// streams its column tiles through a two-stage cp.async pipeline (the copy
-// of tile c+1 is in flight while tile c is quantized; padding rows are
-// zero-filled by the copy).  Per tile it writes the rowwise codes and scale
-// atom of its 128 rows and the columnwise (transposed) codes and atom of its
-// 128 columns.
+// A CTA owns one 128-column tile and a run of kQBRowTiles 128-row tiles: it
+// checks the group offsets once (in parallel), looks up the source row and
+// weight of all its rows once, and streams its row tiles through a
+// three-stage cp.async pipeline (the copies of tiles i+1 and i+2 are in
+// flight while tile i is quantized; padding rows are zero-filled by the
+// copy; the transposed codes of tile i are staged in tile i's own buffer).  Per
+// tile it writes the rowwise codes and scale atom of its 128 rows and the
+// columnwise (transposed) codes and atom of its 128 columns.  Consecutive
+// CTAs take consecutive row runs of the same column tile, so the CTAs
+// resident at a time cover all rows of one or two column tiles: a gathered
+// source row, read by up to k row tiles, is re-read from L2 (one column tile
+// of x is 6 MB at T = 24576).
 namespace moe {
 
 constexpr int kQBThreads = 256;
-constexpr int kQBColTiles = 8;                      // column tiles per CTA (at most)
+constexpr int kQBRowTiles = 8;                      // row tiles per CTA (at most)
+constexpr int kQBStages = 3;                        // tiles in shared memory: one quantized, two in flight
 constexpr int kQBInBytes = kQT * kQT * 2;           // one bf16 tile, unpadded
 constexpr int kQBQPitch = kQT + 16;                 // transposed-code rows (bytes)
-constexpr int kQBSmem = 2 * kQBInBytes + kQT * kQBQPitch + 2 * 512 + 512 + kQT * 8 + kQT * 4;
+constexpr int kQBSmem = kQBStages * kQBInBytes + 2 * 512 + 512 + kQBRowTiles * kQT * (4 + 4);
+static_assert(kQT * kQBQPitch <= kQBInBytes, "transposed codes reuse the tile's buffer");
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t nbytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(g), "r"(nbytes) : "memory");
@@ -261,8 +268,7 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
 __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __restrict__ src, int64_t src_rows,
-                                                              int cols, int k,
-                                                              const int32_t* __restrict__ row_id,
+                                                              int cols, int k, const int32_t* __restrict__ row_id,
                                                               const float* __restrict__ row_w,
                                                               const int32_t* __restrict__ gofs, int G,
                                                               int64_t rows, uint2* __restrict__ codes_r,
@@ -270,17 +276,15 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
                                                               uint8_t* __restrict__ codes_c,
                                                               uint8_t* __restrict__ sf_c, int32_t* err) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint16_t* s_in = reinterpret_cast<uint16_t*>(smem);                       // [2][128][128]
-    uint8_t* s_q = smem + 2 * kQBInBytes;                                     // [128][kQBQPitch]
-    uint8_t* s_atom_r = s_q + kQT * kQBQPitch;                                // [2][512]
+    uint16_t* s_in = reinterpret_cast<uint16_t*>(smem);                       // [kQBStages][128][128]
+    uint8_t* s_atom_r = smem + kQBStages * kQBInBytes;                        // [2][512]
     uint8_t* s_atom_c = s_atom_r + 2 * 512;                                   // [512]
-    int64_t* s_src = reinterpret_cast<int64_t*>(s_atom_c + 512);              // [128]
-    float* s_w = reinterpret_cast<float*>(s_src + kQT);                       // [128]
+    int32_t* s_src = reinterpret_cast<int32_t*>(s_atom_c + 512);              // [kQBRowTiles * 128]
+    float* s_w = reinterpret_cast<float*>(s_src + kQBRowTiles * kQT);         // [kQBRowTiles * 128]
     const int tid = threadIdx.x;
-    const int64_t r0 = (int64_t)blockIdx.x * kQT;
+    const int ct = blockIdx.y;
+    const int64_t rt0 = (int64_t)blockIdx.x * kQBRowTiles;
     const int ntiles = cols / kQT;
-    const int ct0 = blockIdx.y * kQBColTiles;
-    const int nct = min(kQBColTiles, ntiles - ct0);
 
     // group offsets: gofs[0] == 0, monotone, multiples of 128, gofs[G] <= rows
     bool ok = true;
@@ -294,9 +298,12 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
         if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) set_err(err, MOE_ERR_BAD_OFFSETS);
         return;
     }
-    if (r0 >= (int64_t)gofs[G]) return;
-    if (tid < kQT) {
-        const int64_t s = r0 + tid;
+    const int nrt = (int)min((int64_t)kQBRowTiles, (int64_t)gofs[G] / kQT - rt0);   // row tiles below gofs[G]
+    if (nrt <= 0) return;
+
+    // source row and weight of every row of the CTA's row tiles, up front
+    for (int j = tid; j < nrt * kQT; j += kQBThreads) {
+        const int64_t s = rt0 * kQT + j;
         int64_t sr = s;
         float w = 1.f;
         if (row_id != nullptr) {
@@ -308,33 +315,33 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
             }
             if (sr >= 0 && row_w != nullptr) w = row_w[id];
         }
-        s_src[tid] = sr;
-        s_w[tid] = w;
+        s_src[j] = (int32_t)sr;                // < 2^31: checked on the host
+        s_w[j] = w;
     }
-    __syncthreads();
-
     // copy assignment: chunk p of a thread = row tr + 16p, 8 columns at tc*8
     const int tc = tid & 15, tr = tid >> 4;
     const uint32_t s_in_addr = (uint32_t)__cvta_generic_to_shared(s_in);
-    auto issue = [&](int ct, int buf) {
+    auto issue = [&](int i) {
+        const int buf = i % kQBStages;
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             const int rl = tr + 16 * p;
-            const int64_t sr = s_src[rl];
+            const int64_t sr = s_src[i * kQT + rl];
             const uint16_t* g = src + (sr >= 0 ? sr : 0) * cols + (int64_t)ct * kQT + tc * 8;
             cp_async16(s_in_addr + (uint32_t)(buf * kQBInBytes + (rl * kQT + tc * 8) * 2), g, sr >= 0 ? 16u : 0u);
         }
     };
-    issue(ct0, 0);
+    __syncthreads();                          // the gather plan is complete
+    issue(0);
+    cp_async_commit();
+    if (nrt > 1) issue(1);
     cp_async_commit();
     const int lane = tid & 31, warp = tid >> 5;
-    for (int c = 0; c < nct; ++c) {
-        const int ct = ct0 + c;
-        const int buf = c & 1;
-        if (c + 1 < nct) issue(ct + 1, buf ^ 1);
-        cp_async_commit();
-        cp_async_wait1();                     // this thread's copies of tile c have landed
-        uint16_t* tile = s_in + buf * (kQT * kQT);
+    for (int i = 0; i < nrt; ++i) {
+        const int b = i & 1;
+        const int64_t r0 = (rt0 + i) * kQT;
+        uint16_t* tile = s_in + (i % kQBStages) * (kQT * kQT);
+        cp_async_wait1();                     // this thread's copies of tile i have landed
         // rowwise, over this thread's own chunks (scaled in place first)
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
@@ -343,9 +350,9 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
             float f[8];
             unpack8(*cp, f);
             if (row_w != nullptr) {
-                const float w = s_w[rl];
+                const float w = s_w[i * kQT + rl];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] *= w;
+                for (int e = 0; e < 8; ++e) f[e] *= w;
                 const uint4 v = pack8(f);
                 *cp = v;
                 unpack8(v, f);
@@ -353,55 +360,62 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
             if (codes_r != nullptr) {
                 float amax = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
                 amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
                 amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-                const uint32_t b = e8m0_scale_byte(amax);
-                const float inv = e8m0_inv_scale(b);
+                const uint32_t sb = e8m0_scale_byte(amax);
+                const float inv = e8m0_inv_scale(sb);
                 uint32_t q[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) q[i] = cvt_e4m3x2(f[2 * i] * inv, f[2 * i + 1] * inv);
+                for (int e = 0; e < 4; ++e) q[e] = cvt_e4m3x2(f[2 * e] * inv, f[2 * e + 1] * inv);
                 codes_r[((r0 + rl) * cols + (int64_t)ct * kQT) / 8 + tc] =
                     make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
                 if ((tc & 3) == 0)
-                    s_atom_r[buf * 512 + (rl & 31) * 16 + ((rl >> 5) & 3) * 4 + (tc >> 2)] = (uint8_t)b;
+                    s_atom_r[b * 512 + (rl & 31) * 16 + ((rl >> 5) & 3) * 4 + (tc >> 2)] = (uint8_t)sb;
             }
         }
-        __syncthreads();                      // the whole tile (scaled) is in shared memory
+        __syncthreads();                      // A: tile i (scaled) complete; tile i - 1 fully done
+        // the buffer of tile i - 1 is free (its transposed codes were stored
+        // before barrier A): start tile i + 2 there
+        if (i + 2 < nrt) issue(i + 2);
+        cp_async_commit();
+        uint32_t w0[8], w1[8];
+        const int blk = warp & 3;                       // 32-row block
+        const int col = (warp >> 2) * 64 + 2 * lane;    // two columns per lane
         if (codes_c != nullptr) {
-            // warp w: 32-row block w & 3, column pair half w >> 2; lane: 2 columns
-            const int blk = warp & 3;
-            const int col = (warp >> 2) * 64 + 2 * lane;
             float f0[32], f1[32];
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const uint32_t v = *reinterpret_cast<const uint32_t*>(tile + (blk * 32 + i) * kQT + col);
-                f0[i] = __uint_as_float(v << 16);
-                f1[i] = __uint_as_float(v & 0xFFFF0000u);
-                a0 = fmaxf(a0, fabsf(f0[i]));
-                a1 = fmaxf(a1, fabsf(f1[i]));
+            for (int e = 0; e < 32; ++e) {
+                const uint32_t v = *reinterpret_cast<const uint32_t*>(tile + (blk * 32 + e) * kQT + col);
+                f0[e] = __uint_as_float(v << 16);
+                f1[e] = __uint_as_float(v & 0xFFFF0000u);
+                a0 = fmaxf(a0, fabsf(f0[e]));
+                a1 = fmaxf(a1, fabsf(f1[e]));
             }
             const uint32_t b0 = e8m0_scale_byte(a0), b1 = e8m0_scale_byte(a1);
             const float i0 = e8m0_inv_scale(b0), i1 = e8m0_inv_scale(b1);
-            uint32_t w0[8], w1[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                w0[i] = cvt_e4m3x2(f0[4 * i] * i0, f0[4 * i + 1] * i0) |
-                        (cvt_e4m3x2(f0[4 * i + 2] * i0, f0[4 * i + 3] * i0) << 16);
-                w1[i] = cvt_e4m3x2(f1[4 * i] * i1, f1[4 * i + 1] * i1) |
-                        (cvt_e4m3x2(f1[4 * i + 2] * i1, f1[4 * i + 3] * i1) << 16);
+            for (int e = 0; e < 8; ++e) {
+                w0[e] = cvt_e4m3x2(f0[4 * e] * i0, f0[4 * e + 1] * i0) |
+                        (cvt_e4m3x2(f0[4 * e + 2] * i0, f0[4 * e + 3] * i0) << 16);
+                w1[e] = cvt_e4m3x2(f1[4 * e] * i1, f1[4 * e + 1] * i1) |
+                        (cvt_e4m3x2(f1[4 * e + 2] * i1, f1[4 * e + 3] * i1) << 16);
             }
+            s_atom_c[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b0;
+            s_atom_c[((col + 1) & 31) * 16 + (((col + 1) >> 5) & 3) * 4 + blk] = (uint8_t)b1;
+        }
+        __syncthreads();                      // B: every thread is done reading tile i
+        uint8_t* s_q = reinterpret_cast<uint8_t*>(tile);   // [128][kQBQPitch] over tile i's buffer
+        if (codes_c != nullptr) {
             uint4* d0 = reinterpret_cast<uint4*>(s_q + col * kQBQPitch + blk * 32);
             uint4* d1 = reinterpret_cast<uint4*>(s_q + (col + 1) * kQBQPitch + blk * 32);
             d0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
             d0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
             d1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
             d1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
-            s_atom_c[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b0;
-            s_atom_c[((col + 1) & 31) * 16 + (((col + 1) >> 5) & 3) * 4 + blk] = (uint8_t)b1;
         }
-        __syncthreads();                      // transposed codes and both atoms complete
+        __syncthreads();                      // C: transposed codes and both atoms complete
         if (codes_c != nullptr) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
             if (codes_r != nullptr) {
                 const int64_t atom = (int64_t)ct * (rows / kQT) + r0 / kQT;
                 reinterpret_cast<uint4*>(sf_r + atom * 512)[lane] =
-                    reinterpret_cast<const uint4*>(s_atom_r + buf * 512)[lane];
+                    reinterpret_cast<const uint4*>(s_atom_r + b * 512)[lane];
             }
         } else if (warp == 1) {
             if (codes_c != nullptr) {
@@ -433,30 +447,29 @@ cudaError_t quant_set_attributes() {
 }  // namespace moe
 
 extern "C" moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, int cols, int k,
-                                              const int32_t* row_id,
-                                              const float* row_w, const int32_t* gofs, int G, int64_t rows,
-                                              uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
-                                              uint8_t* scales_col, int32_t* err, void* stream) {
+                                              const int32_t* row_id, const float* row_w, const int32_t* gofs, int G,
+                                              int64_t rows, uint8_t* codes_row, uint8_t* scales_row,
+                                              uint8_t* codes_col, uint8_t* scales_col, int32_t* err, void* stream) {
     using namespace moe;
     MOE_REQUIRE(src && gofs && G >= 1 && G <= 4096 && cols > 0 && rows > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(row_id != nullptr || row_w == nullptr, MOE_ERR_INVALID_ARG);
-    MOE_REQUIRE(row_id == nullptr || (k >= 1 && src_rows >= 0), MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(row_id == nullptr || (k >= 1 && src_rows >= 0 && src_rows <= 0x7FFFFFFF), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(row_id != nullptr || src_rows == rows, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE((codes_row != nullptr) == (scales_row != nullptr), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE((codes_col != nullptr) == (scales_col != nullptr), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(codes_row != nullptr || codes_col != nullptr, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(rows % kQT == 0 && cols % kQT == 0, MOE_ERR_UNSUPPORTED);
-    MOE_REQUIRE(rows / kQT <= 0x7FFFFFFF, MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(cols / kQT <= 65535 && rows <= 0x7FFFFFFF, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(moe_aligned16(src) && (codes_row == nullptr || (moe_aligned16(codes_row) && moe_aligned16(scales_row))) &&
                     (codes_col == nullptr || (moe_aligned16(codes_col) && moe_aligned16(scales_col))),
                 MOE_ERR_ALIGNMENT);
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
-    const int ntiles = cols / kQT;
-    dim3 grid((unsigned)(rows / kQT), (unsigned)((ntiles + kQBColTiles - 1) / kQBColTiles));
+    const int64_t row_runs = (rows / kQT + kQBRowTiles - 1) / kQBRowTiles;
+    MOE_REQUIRE(row_runs <= 0x7FFFFFFF, MOE_ERR_UNSUPPORTED);
+    dim3 grid((unsigned)row_runs, (unsigned)(cols / kQT));
     k_quant_both<<<grid, kQBThreads, kQBSmem, (cudaStream_t)stream>>>((const uint16_t*)src, src_rows, cols, k, row_id,
-                                                                     row_w,
-                                                                     gofs, G, rows, (uint2*)codes_row, scales_row,
-                                                                     codes_col, scales_col, err);
+                                                                     row_w, gofs, G, rows, (uint2*)codes_row,
+                                                                     scales_row, codes_col, scales_col, err);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }
