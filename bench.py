@@ -41,7 +41,7 @@ WORKLOADS = {
                  desc="tiny layer fwd+bwd: T=256, d=512, E=8, top-2, f=256"),
 }
 METRIC = "MoE layer fwd+bwd TFLOPS (MXFP8 grouped GEMM) and % of dense peak, 1 GB300"
-KERNELS_PER_STEP = 19       # libmoe kernel launches in one fwd+bwd step (see layer.MoELayer)
+KERNELS_PER_STEP = 18       # libmoe kernel launches in one fwd+bwd step (see layer.MoELayer)
 GEMMS_PER_STEP = 6
 
 
@@ -228,9 +228,10 @@ def run_gpu(args, rank, world, local_rank):
     mx_peak = 2.0 * peaks["bf16_tflops_sustained"]     # nominal fp8/bf16 dense ratio 4.5/2.25
     traffic = _gemm_traffic() if args.workload == "deepseek-v3" else None
     # algorithmic bytes of the six GEMMs: fp8 operands (+1/32 scales) once,
-    # bf16 outputs (and the SwiGLU-bwd input a_pre) once
+    # bf16 outputs (and the SwiGLU-bwd input a_pre) once, h as its MXFP8
+    # codes on both axes
     R, q = L.R, 1 + 1 / 32
-    algo_bytes = (R * d * q + E * d * 2 * f * q + R * 2 * f * 2 + R * f * 2            # up fwd + SwiGLU
+    algo_bytes = (R * d * q + E * d * 2 * f * q + R * 2 * f * 2 + 2 * R * f * q        # up fwd + SwiGLU + MXFP8(h)
                   + R * f * q + E * f * d * q + R * d * 2                               # down fwd
                   + R * d * q + E * f * d * q + R * 2 * f * 2 * 2                       # down dgrad + SwiGLU bwd
                   + R * f * q + R * d * q + E * f * d * 2                               # dW2

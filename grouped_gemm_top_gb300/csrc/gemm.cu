@@ -437,10 +437,18 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
 
 using namespace moe;
 
-extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
-                                           const uint8_t* b_sf, int b_layout, const int32_t* gofs, int G, int64_t M,
-                                           int N, int64_t K, int epilogue, const void* epi_aux, void* d, void* d2,
-                                           int32_t* err, void* stream) {
+// MXFP8 outputs of h for the SwiGLU epilogue (all NULL: not produced)
+struct HQuantOut {
+    uint8_t* codes_row;
+    uint8_t* scales_row;
+    uint8_t* codes_col;
+    uint8_t* scales_col;
+};
+
+static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
+                             int b_layout, const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
+                             const void* epi_aux, void* d, void* d2, const HQuantOut& hq, int32_t* err,
+                             void* stream) {
     using namespace gg;
     MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD || mode == MOE_GEMM_WGRAD, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(a && a_sf && b && b_sf && gofs && d, MOE_ERR_INVALID_ARG);
@@ -458,7 +466,7 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
         MOE_REQUIRE(b_layout == MOE_B_GNK || b_layout == MOE_B_NGK, MOE_ERR_INVALID_ARG);
         MOE_REQUIRE(epilogue == MOE_EPI_NONE || epilogue == MOE_EPI_SWIGLU || epilogue == MOE_EPI_SWIGLU_BWD,
                     MOE_ERR_INVALID_ARG);
-        if (epilogue == MOE_EPI_SWIGLU) MOE_REQUIRE(d2 != nullptr, MOE_ERR_INVALID_ARG);
+        if (epilogue == MOE_EPI_SWIGLU) MOE_REQUIRE(d2 != nullptr || hq.codes_row != nullptr, MOE_ERR_INVALID_ARG);
         if (epilogue == MOE_EPI_SWIGLU_BWD) MOE_REQUIRE(epi_aux != nullptr, MOE_ERR_INVALID_ARG);
     }
     MOE_REQUIRE(device_initialized() && g_encode != nullptr, MOE_ERR_NOT_INITIALIZED);
@@ -476,6 +484,10 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
     p.b_sf = b_sf;
     p.d = (__nv_bfloat16*)d;
     p.d2 = (__nv_bfloat16*)d2;
+    p.hq_r = hq.codes_row;
+    p.hs_r = hq.scales_row;
+    p.hq_c = hq.codes_col;
+    p.hs_c = hq.scales_col;
     p.aux = (const __nv_bfloat16*)epi_aux;
     p.err = err;
     p.timeout_ns = 2000000000ull;   // 2 s per wait
@@ -566,4 +578,27 @@ extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uin
         k_grouped_gemm<128><<<grid, THREADS, Cfg<128>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
+}
+
+extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                                           const uint8_t* b_sf, int b_layout, const int32_t* gofs, int G, int64_t M,
+                                           int N, int64_t K, int epilogue, const void* epi_aux, void* d, void* d2,
+                                           int32_t* err, void* stream) {
+    if (epilogue == MOE_EPI_SWIGLU && d2 == nullptr) return MOE_ERR_INVALID_ARG;
+    const HQuantOut none = {nullptr, nullptr, nullptr, nullptr};
+    return gemm_run(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilogue, epi_aux, d, d2, none, err, stream);
+}
+
+extern "C" moe_status_t grouped_gemm_mxfp8_swiglu_quant(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                                                        const uint8_t* b_sf, int b_layout, const int32_t* gofs, int G,
+                                                        int64_t M, int N, int64_t K, void* a_pre, void* h,
+                                                        uint8_t* h_codes_row, uint8_t* h_scales_row,
+                                                        uint8_t* h_codes_col, uint8_t* h_scales_col, int32_t* err,
+                                                        void* stream) {
+    MOE_REQUIRE(h_codes_row && h_scales_row && h_codes_col && h_scales_col, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(N > 0 && N % 256 == 0, MOE_ERR_UNSUPPORTED);      // f = N/2 a multiple of 128
+    MOE_REQUIRE((reinterpret_cast<uintptr_t>(h_codes_row) & 31) == 0, MOE_ERR_ALIGNMENT);
+    const HQuantOut hq = {h_codes_row, h_scales_row, h_codes_col, h_scales_col};
+    return gemm_run(MOE_GEMM_FWD, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, MOE_EPI_SWIGLU, nullptr, a_pre, h, hq,
+                    err, stream);
 }

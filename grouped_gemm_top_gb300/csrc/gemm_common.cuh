@@ -36,6 +36,12 @@ struct Params {
     uint64_t timeout_ns;
     int band;           // m-tiles per raster band (consecutive tiles share the B tile)
     int tma_store;      // pair kernel, BN = 256, MOE_EPI_NONE: write D through the TMA (tensor map tmD)
+    // MOE_EPI_SWIGLU: MXFP8 of h (NULL = not produced): rowwise codes
+    // [M, N/2] + scale atoms, columnwise (transposed) codes [N/2, M] + atoms
+    uint8_t* hq_r;
+    uint8_t* hs_r;
+    uint8_t* hq_c;
+    uint8_t* hs_c;
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -254,7 +260,65 @@ __device__ __forceinline__ int find_group(const int* s_gofs, int G, int64_t row)
     return lo;
 }
 
+// 32 bytes (one L2 sector) per store.
+__device__ __forceinline__ void st_global_v8(void* dst, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 // ------------------------------------------------------------- epilogue ----
+
+// MXFP8 of one 32-column block of h in the SwiGLU epilogue ([TE-JAX] "What
+// specialized optimizations...": group-aware MXFP8 quantization; fused into
+// the producing GEMM).  `ph` holds this thread's 32 bf16-rounded h values of
+// row `row`, columns [hcol, hcol + 32) (hcol % 32 == 0), as 16 packed pairs;
+// the warp's 32 lanes hold 32 consecutive rows starting at a multiple of 32.
+// Rowwise: the block is this thread's own 32 values.  Columnwise: each
+// column's block is the warp's 32 rows (tiles start at group offsets, which
+// are multiples of 128, so a block never crosses a group), reduced with one
+// warp max per column.  Codes, scales and layouts are those of
+// mxfp8_gather_quantize for h.
+__device__ __forceinline__ void h_quant_chunk(const Params& p, int64_t row, int64_t hcol, const uint32_t* ph,
+                                              int lane) {
+    const int64_t f = p.N / 2, M = p.M;
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = __vmaxu2(m, ph[i] & 0x7FFF7FFFu);
+    const uint32_t sb = e8m0_scale_byte(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16));
+    const float inv = e8m0_inv_scale(sb);
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t a = ph[2 * i], b = ph[2 * i + 1];
+        const uint32_t lo = cvt_e4m3x2(__uint_as_float(a << 16) * inv, __uint_as_float(a & 0xFFFF0000u) * inv);
+        const uint32_t hi = cvt_e4m3x2(__uint_as_float(b << 16) * inv, __uint_as_float(b & 0xFFFF0000u) * inv);
+        q[i] = lo | (hi << 16);
+    }
+    st_global_v8(p.hq_r + row * f + hcol, q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+    const int64_t blk = hcol >> 5;
+    p.hs_r[((blk >> 2) * (M >> 7) + (row >> 7)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (blk & 3)] =
+        (uint8_t)sb;
+    uint32_t my_sb = 0;      // scale of column hcol + lane
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t a = ph[i];
+        const uint32_t s0 = e8m0_scale_byte(__uint_as_float(__reduce_max_sync(0xFFFFFFFFu, a & 0x7FFFu) << 16));
+        const uint32_t s1 =
+            e8m0_scale_byte(__uint_as_float(__reduce_max_sync(0xFFFFFFFFu, (a >> 16) & 0x7FFFu) << 16));
+        if (lane == 2 * i) my_sb = s0;
+        if (lane == 2 * i + 1) my_sb = s1;
+        const uint32_t c = cvt_e4m3x2(__uint_as_float(a << 16) * e8m0_inv_scale(s0),
+                                      __uint_as_float(a & 0xFFFF0000u) * e8m0_inv_scale(s1));
+        p.hq_c[(hcol + 2 * i) * M + row] = (uint8_t)(c & 0xFFu);
+        p.hq_c[(hcol + 2 * i + 1) * M + row] = (uint8_t)(c >> 8);
+    }
+    const int64_t col = hcol + lane, rb = (row - lane) >> 5;
+    p.hs_c[((rb >> 2) * (f >> 7) + (col >> 7)) * 512 + (col & 31) * 16 + ((col >> 5) & 3) * 4 + (rb & 3)] =
+        (uint8_t)my_sb;
+}
+
 // One TMEM accumulator of BN columns, 128 lanes: the calling warp owns lane
 // quarter `quarter` (rows quarter*32 + lane of the tile) and column half
 // `half` of the tile.  `row` is this thread's output row, `nt` the tile
@@ -276,7 +340,13 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
             store_row32(p.d + row * N + f + hcol, up);
 #pragma unroll
             for (int i = 0; i < 32; ++i) h[i] = v[i] * fast_sigmoid(v[i]) * up[i];
-            store_row32(p.d2 + row * f + hcol, h);
+            if (p.d2 != nullptr) store_row32(p.d2 + row * f + hcol, h);
+            if (p.hq_r != nullptr) {
+                uint32_t ph[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ph[i] = pack_bf16x2(h[2 * i], h[2 * i + 1]);
+                h_quant_chunk(p, row, hcol, ph, (int)(threadIdx.x & 31));
+            }
         }
     } else if (p.epi == MOE_EPI_SWIGLU_BWD) {
         const int64_t N = p.N, ld = 2 * (int64_t)p.N;
@@ -305,13 +375,6 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
     }
 }
 
-// 32 bytes (one L2 sector) per store.
-__device__ __forceinline__ void st_global_v8(void* dst, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                             uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0), "r"(a1), "r"(a2),
-                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
-                 : "memory");
-}
 
 // Register-staged epilogue for 256-wide tiles: the calling thread drains
 // its 128 accumulator columns (column half `half`) into registers as packed
@@ -351,8 +414,9 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
                              pg[8 * q + 5], pg[8 * q + 6], pg[8 * q + 7]);
                 st_global_v8(du + o, pu[8 * q], pu[8 * q + 1], pu[8 * q + 2], pu[8 * q + 3], pu[8 * q + 4],
                              pu[8 * q + 5], pu[8 * q + 6], pu[8 * q + 7]);
-                st_global_v8(dh + o, ph[8 * q], ph[8 * q + 1], ph[8 * q + 2], ph[8 * q + 3], ph[8 * q + 4],
-                             ph[8 * q + 5], ph[8 * q + 6], ph[8 * q + 7]);
+                if (p.d2 != nullptr)
+                    st_global_v8(dh + o, ph[8 * q], ph[8 * q + 1], ph[8 * q + 2], ph[8 * q + 3], ph[8 * q + 4],
+                                 ph[8 * q + 5], ph[8 * q + 6], ph[8 * q + 7]);
             }
         };
         tmem_ld32_issue(tacc + 128 * half, ra);
@@ -364,8 +428,16 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
         tmem_wait_ld();
         release();
         store(0);
+        uint32_t ph0[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ph0[i] = ph[i];
         convert();
         store(1);
+        if (p.hq_r != nullptr) {      // MXFP8 of h, after the stores, with no fp32 accumulator live
+            const int lane = (int)(threadIdx.x & 31);
+            h_quant_chunk(p, row, hcol, ph0, lane);
+            h_quant_chunk(p, row, hcol + 32, ph, lane);
+        }
     } else {
         uint32_t pk[64];
 #pragma unroll

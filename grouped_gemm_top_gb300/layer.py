@@ -17,7 +17,9 @@ _SCORES = {"softmax": ops.MOE_SCORE_SOFTMAX, "sigmoid": ops.MOE_SCORE_SIGMOID}
 
 
 class MoELayer:
-    def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0"):
+    def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_h=False):
+        """store_h: also write h in bf16 (the step itself only needs its MXFP8
+        codes, which the up/gate GEMM's epilogue produces)."""
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
         self.score = _SCORES[score]
         self.normalize = bool(normalize)
@@ -49,7 +51,7 @@ class MoELayer:
         # are quantized, along both axes, straight from x and dout)
         self.xq, self.xs = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.a_pre = z((M, 2 * f), torch.bfloat16)
-        self.h = z((M, f), torch.bfloat16)
+        self.h = z((M, f), torch.bfloat16) if store_h else None
         self.hq, self.hs = z((M, f), torch.uint8), z((ops.sf_bytes(M, f),), torch.uint8)
         self.y_perm = z((M, d), torch.bfloat16)
         self.out = z((T, d), torch.bfloat16)
@@ -92,15 +94,21 @@ class MoELayer:
         self.W2d, self.W2d_s = ops.mxfp8_group_quantize(W2v, ops.MOE_QUANT_ROWWISE, err=self.err)
         self.weights_ready = True
 
-    def _gemm(self, *args):
+    def _timed(self, fn, *args):
         if self.gemm_events is None:
-            return ops.grouped_gemm_mxfp8(*args)
+            return fn(*args)
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
-        r = ops.grouped_gemm_mxfp8(*args)
+        r = fn(*args)
         e.record()
         self.gemm_events.append((s, e))
         return r
+
+    def _gemm(self, *args):
+        return self._timed(ops.grouped_gemm_mxfp8, *args)
+
+    def _gemm_swiglu_quant(self, *args):
+        return self._timed(ops.grouped_gemm_mxfp8_swiglu_quant, *args)
 
     # ------------------------------------------------------------- step ----
     def forward_(self):
@@ -114,10 +122,10 @@ class MoELayer:
         # columnwise copy for the dW1 wgrad of the backward
         ops.mxfp8_gather_quantize(self.x, self.gofs, E, M, self.row_id, k, None, True, True, self.xq, self.xs,
                                   self.xqT, self.xsT, err)
-        self._gemm(ops.MOE_GEMM_FWD, self.xq, self.xs, self.W1f, self.W1f_s, ops.MOE_B_GNK, self.gofs,
-                   E, M, 2 * f, d, ops.MOE_EPI_SWIGLU, None, self.a_pre, self.h, err)
-        ops.mxfp8_gather_quantize(self.h, self.gofs, E, M, None, 1, None, True, True, self.hq, self.hs,
-                                  self.hqT, self.hsT, err)
+        # up/gate GEMM; its SwiGLU epilogue writes a_pre and h's MXFP8 codes
+        # on both axes (h itself only if store_h)
+        self._gemm_swiglu_quant(self.xq, self.xs, self.W1f, self.W1f_s, ops.MOE_B_GNK, self.gofs, E, M, 2 * f, d,
+                                self.a_pre, self.h, False, self.hq, self.hs, self.hqT, self.hsT, err)
         self._gemm(ops.MOE_GEMM_FWD, self.hq, self.hs, self.W2f, self.W2f_s, ops.MOE_B_GNK, self.gofs,
                    E, M, d, f, ops.MOE_EPI_NONE, None, self.y_perm, None, err)
         ops.moe_unpermute_combine(self.y_perm, self.slot_of, self.topk_w, self.out, err)

@@ -40,7 +40,7 @@ EXPORTS = [
     "moe_route_workspace_size", "moe_permute_workspace_size", "moe_route_topk",
     "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
     "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_route_topk_noalloc",
-    "mxfp8_gather_quantize",
+    "mxfp8_gather_quantize", "grouped_gemm_mxfp8_swiglu_quant",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -57,6 +57,8 @@ _SIGS = {
     "mxfp8_group_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
     "mxfp8_gather_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp,
                                      _vp]),
+    "grouped_gemm_mxfp8_swiglu_quant": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _vp, _vp, _vp,
+                                               _vp, _vp, _vp, _vp, _vp]),
     "grouped_gemm_mxfp8": (_i32, [_i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _i32, _vp, _vp,
                                   _vp, _vp, _vp]),
     "moe_unpermute_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
@@ -227,6 +229,29 @@ def grouped_gemm_mxfp8(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilo
                                                         _p(gofs), int(G), int(M), int(N), int(K), int(epilogue),
                                                         _p(epi_aux), _p(d), _p(d2), _p(err), _stream(stream)))
     return (d, d2) if epilogue == MOE_EPI_SWIGLU else d
+
+
+def grouped_gemm_mxfp8_swiglu_quant(a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, a_pre=None, h=None, want_h=False,
+                                    h_codes_row=None, h_scales_row=None, h_codes_col=None, h_scales_col=None,
+                                    err=None, stream=None):
+    """Up/gate GEMM with the SwiGLU epilogue writing a_pre [M, N] and the
+    MXFP8 codes of h on both axes (h bf16 [M, N/2] only if want_h or h is
+    given).  See include/moe.h.  Returns (a_pre, h or None, codes_row,
+    scales_row, codes_col, scales_col)."""
+    f = N // 2
+    a_pre = a_pre if a_pre is not None else _empty((M, N), torch.bfloat16, a)
+    if h is None and want_h:
+        h = _empty((M, f), torch.bfloat16, a)
+    h_codes_row = h_codes_row if h_codes_row is not None else _empty((M, f), torch.uint8, a)
+    h_scales_row = h_scales_row if h_scales_row is not None else _empty((sf_bytes(M, f),), torch.uint8, a)
+    h_codes_col = h_codes_col if h_codes_col is not None else _empty((f, M), torch.uint8, a)
+    h_scales_col = h_scales_col if h_scales_col is not None else _empty((sf_bytes(M, f),), torch.uint8, a)
+    _check("grouped_gemm_mxfp8_swiglu_quant",
+           lib.grouped_gemm_mxfp8_swiglu_quant(_p(a), _p(a_sf), _p(b), _p(b_sf), int(b_layout), _p(gofs), int(G),
+                                               int(M), int(N), int(K), _p(a_pre), _p(h), _p(h_codes_row),
+                                               _p(h_scales_row), _p(h_codes_col), _p(h_scales_col), _p(err),
+                                               _stream(stream)))
+    return a_pre, h, h_codes_row, h_scales_row, h_codes_col, h_scales_col
 
 
 def moe_unpermute_combine(y_perm, slot_of, topk_w, out=None, err=None, stream=None):

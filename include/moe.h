@@ -280,6 +280,28 @@ MOE_API moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_
                                 int32_t* err, void* stream);
 
 /*
+ * grouped_gemm_mxfp8_swiglu_quant -- the up/gate GEMM (MOE_GEMM_FWD,
+ * MOE_EPI_SWIGLU) with the MXFP8 quantization of h fused into its epilogue
+ * ([TE-JAX] "What specialized optimizations...": group-aware MXFP8
+ * quantization; "What is the training performance impact...": quantization
+ * fused with the GEMM is listed there as planned work).  Arguments as for
+ * grouped_gemm_mxfp8 with mode FWD and epilogue SWIGLU (N % 256 == 0), and:
+ *   a_pre        [M, N] bf16, written (the GEMM result).
+ *   h            [M, N/2] bf16 or NULL: written only if given.
+ *   h_codes_row, h_scales_row   exactly mxfp8_gather_quantize's rowwise
+ *                output for h (codes [M, N/2], 32-byte aligned).
+ *   h_codes_col, h_scales_col   exactly its columnwise output for h (codes
+ *                [N/2, M]).
+ * Every code is computed from the bf16-rounded h (the value `h` holds when
+ * given).  Rows >= gofs[G] are not written.
+ */
+MOE_API moe_status_t grouped_gemm_mxfp8_swiglu_quant(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                                             const uint8_t* b_sf, int b_layout, const int32_t* gofs, int G,
+                                             int64_t M, int N, int64_t K, void* a_pre, void* h,
+                                             uint8_t* h_codes_row, uint8_t* h_scales_row, uint8_t* h_codes_col,
+                                             uint8_t* h_scales_col, int32_t* err, void* stream);
+
+/*
  * moe_unpermute_combine -- local half of combine ([TE-JAX] "Optimization 2":
  * per-expert results are accumulated and restored to token order; [CH1]
  * §2.3.2: a sum weighted by the routing weights).

@@ -6,8 +6,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (assert_bf16_close, atoms_to_rowmajor, batched_weight_operand, glu_perm, gpu_ops,
-                     padded_layout, to_np)
+from helpers import (assert_bf16_close, atoms_rows_subset, atoms_to_rowmajor, batched_weight_operand, glu_perm,
+                     gpu_ops, padded_layout, to_np)
 from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -142,6 +142,45 @@ def test_swiglu_epilogue(ops, sizes, K, f, layout):
     ref = O.grouped_gemm(A, B, gofs)[:Rp]
     assert_bf16_close(a_pre[:Rp], ref, what="a_pre")
     assert_bf16_close(h[:Rp], O.swiglu(ref), what="h")
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("sizes,K,f", [([150, 0, 300], 512, 256), ([77, 500], 256, 128), ([129, 3], 1024, 384)])
+def test_swiglu_quant_epilogue(ops, sizes, K, f, layout):
+    """h's MXFP8 codes from the SwiGLU epilogue: bit-exact against the
+    oracle's rowwise and group-aware columnwise quantization of the GPU's own
+    bf16 h; the same codes whether or not h is also written; rows beyond the
+    groups untouched."""
+    G, N = len(sizes), 2 * f
+    x, gofs_t, gofs = _act(sizes, K, seed=51)
+    M = x.shape[0]
+    xq, xs, A = _quant_rows(ops, x)
+    bq, bs, B = _weights(ops, G, K, N, seed=52, layout=layout, glu=True)
+    Rp = int(gofs[-1])
+    sent = dict(h_codes_row=torch.full((M, f), 0xAB, dtype=torch.uint8, device="cuda"),
+                h_codes_col=torch.full((f, M), 0xAB, dtype=torch.uint8, device="cuda"))
+    a_pre, h, cr, sr, cc, sc = ops.grouped_gemm_mxfp8_swiglu_quant(xq, xs, bq, bs, layout, gofs_t, G, M, N, K,
+                                                                    want_h=True, **sent)
+    torch.cuda.synchronize()
+    ref = O.grouped_gemm(A, B, gofs)[:Rp]
+    assert_bf16_close(a_pre[:Rp], ref, what="a_pre")
+    assert_bf16_close(h[:Rp], O.swiglu(ref), what="h")
+    hn = to_np(h)[:Rp]
+    rq, rs = O.mxfp8_quantize_rows(hn)
+    assert np.array_equal(cr[:Rp].cpu().numpy(), rq)
+    assert np.array_equal(atoms_rows_subset(sr.cpu().numpy(), M, f, np.arange(Rp)), rs)
+    cq, cs, padded = O.mxfp8_quantize_cols_grouped(hn, gofs)
+    assert np.array_equal(padded, gofs)
+    assert np.array_equal(cc[:, :Rp].cpu().numpy(), cq)
+    assert np.array_equal(atoms_to_rowmajor(sc.cpu().numpy(), f, M)[:, :Rp // 32], cs)
+    assert torch.all(cr[Rp:] == 0xAB) and torch.all(cc[:, Rp:] == 0xAB)
+    # without h: identical codes and scales
+    a2, h2, cr2, sr2, cc2, sc2 = ops.grouped_gemm_mxfp8_swiglu_quant(xq, xs, bq, bs, layout, gofs_t, G, M, N, K)
+    torch.cuda.synchronize()
+    assert h2 is None
+    assert torch.equal(a2[:Rp], a_pre[:Rp]) and torch.equal(cr2[:Rp], cr[:Rp]) and torch.equal(cc2[:, :Rp], cc[:, :Rp])
+    assert np.array_equal(atoms_rows_subset(sr2.cpu().numpy(), M, f, np.arange(Rp)), rs)
+    assert np.array_equal(atoms_to_rowmajor(sc2.cpu().numpy(), f, M)[:, :Rp // 32], cs)
 
 
 @pytest.mark.parametrize("sizes,K,f", [([140, 260], 512, 256), ([300, 0, 5], 256, 384)])

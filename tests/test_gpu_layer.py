@@ -19,7 +19,7 @@ def ops():
 
 def _layer(ops, T, d, E, k, f, score, norm, zipf=None, seed_offset=0):
     from grouped_gemm_top_gb300.layer import MoELayer
-    L = MoELayer(T, d, E, k, f, score, norm)
+    L = MoELayer(T, d, E, k, f, score, norm, store_h=True)
     inp = synth.make_layer_inputs(T, d, E, f, "cuda", zipf_s=zipf, seed_offset=seed_offset)
     L.set_weights(inp["W1"], inp["W2"])
     L.logits.copy_(inp["logits"])
