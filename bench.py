@@ -440,6 +440,36 @@ def run_reference(args):
     }
 
 
+def run_hbm_probe(nbytes=4 << 30, reps=10):
+    """Write-only and read+write HBM bandwidth on this GPU, measured with
+    PyTorch's fill and copy kernels (a measuring tool, not the product): the
+    ceilings for the write-heavy quantization kernels.  CUDA events, 3
+    warm-ups; buffers of 4 GB (written) and 2 GB + 2 GB (copied), far above L2."""
+    import torch
+    a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    b = torch.empty(nbytes // 2, dtype=torch.uint8, device="cuda")
+    c = torch.zeros(nbytes // 2, dtype=torch.uint8, device="cuda")
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    fill_ms = timed(lambda: a.fill_(7))
+    copy_ms = timed(lambda: b.copy_(c))
+    peaks, src = _peaks()
+    return {"write_only_gbs": round(nbytes / fill_ms / 1e6, 1), "copy_gbs": round(nbytes / copy_ms / 1e6, 1),
+            "copy_peak_file_gbs": peaks["hbm_gbs"], "peak_source": src,
+            "method": "torch fill_ of 4 GB (write-only) and copy_ of 2 GB into 2 GB (read+write bytes)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,7 +483,12 @@ def main():
                     help="time one standalone grouped GEMM fwd (K = N unless given) and print its line")
     ap.add_argument("--b-layout", default="gnk", choices=["ngk", "gnk"])
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
+    ap.add_argument("--hbm-probe", action="store_true",
+                    help="measure write-only and copy HBM bandwidth (PyTorch fill/copy kernels) and print one line")
     args = ap.parse_args()
+    if args.hbm_probe:
+        print(json.dumps({"hbm_probe": run_hbm_probe()}), flush=True)
+        return
     if args.gemm_point or args.sweep:
         if args.gemm_point:
             gp = list(args.gemm_point)

@@ -242,9 +242,12 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
 // A CTA owns one 128-column tile and a run of kQBRowTiles 128-row tiles: it
 // checks the group offsets once (in parallel), looks up the source row and
 // weight of all its rows once, and streams its row tiles through a
-// three-stage cp.async pipeline (the copies of tiles i+1 and i+2 are in
-// flight while tile i is quantized; padding rows are zero-filled by the
-// copy; the transposed codes of tile i are staged in tile i's own buffer).  Per
+// two-stage cp.async pipeline (the copy of tile i+1 is in flight while tile
+// i is quantized; padding rows are zero-filled by the copy; the transposed
+// codes of tile i are staged in tile i's own buffer), three CTAs per SM.
+// Block maxima are taken on the packed bf16 bits (two values per
+// instruction); a column block is read twice from shared memory (maximum,
+// then codes) to keep registers low enough for three CTAs per SM.  Per
 // tile it writes the rowwise codes and scale atom of its 128 rows and the
 // columnwise (transposed) codes and atom of its 128 columns.  Consecutive
 // CTAs take consecutive row runs of the same column tile, so the CTAs
@@ -255,10 +258,9 @@ namespace moe {
 
 constexpr int kQBThreads = 256;
 constexpr int kQBRowTiles = 8;                      // row tiles per CTA (at most)
-constexpr int kQBStages = 3;                        // tiles in shared memory: one quantized, two in flight
 constexpr int kQBInBytes = kQT * kQT * 2;           // one bf16 tile, unpadded
 constexpr int kQBQPitch = kQT + 16;                 // transposed-code rows (bytes)
-constexpr int kQBSmem = kQBStages * kQBInBytes + 2 * 512 + 512 + kQBRowTiles * kQT * (4 + 4);
+constexpr int kQBSmem = 2 * kQBInBytes + 2 * 512 + 512 + kQBRowTiles * kQT * (4 + 4);
 static_assert(kQT * kQBQPitch <= kQBInBytes, "transposed codes reuse the tile's buffer");
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t nbytes) {
@@ -267,7 +269,13 @@ __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
-__global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __restrict__ src, int64_t src_rows,
+// amax of packed bf16 pairs: max of |lo| and |hi| over the words, as bf16
+// bits (non-negative bf16 bit patterns order like their values)
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) { return __vmaxu2(m, w & 0x7FFF7FFFu); }
+__device__ __forceinline__ float bf16_bits_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_bits_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __restrict__ src, int64_t src_rows,
                                                               int cols, int k, const int32_t* __restrict__ row_id,
                                                               const float* __restrict__ row_w,
                                                               const int32_t* __restrict__ gofs, int G,
@@ -276,8 +284,8 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
                                                               uint8_t* __restrict__ codes_c,
                                                               uint8_t* __restrict__ sf_c, int32_t* err) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint16_t* s_in = reinterpret_cast<uint16_t*>(smem);                       // [kQBStages][128][128]
-    uint8_t* s_atom_r = smem + kQBStages * kQBInBytes;                        // [2][512]
+    uint16_t* s_in = reinterpret_cast<uint16_t*>(smem);                       // [2][128][128]
+    uint8_t* s_atom_r = smem + 2 * kQBInBytes;                                // [2][512]
     uint8_t* s_atom_c = s_atom_r + 2 * 512;                                   // [512]
     int32_t* s_src = reinterpret_cast<int32_t*>(s_atom_c + 512);              // [kQBRowTiles * 128]
     float* s_w = reinterpret_cast<float*>(s_src + kQBRowTiles * kQT);         // [kQBRowTiles * 128]
@@ -322,7 +330,7 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
     const int tc = tid & 15, tr = tid >> 4;
     const uint32_t s_in_addr = (uint32_t)__cvta_generic_to_shared(s_in);
     auto issue = [&](int i) {
-        const int buf = i % kQBStages;
+        const int buf = i & 1;
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             const int rl = tr + 16 * p;
@@ -334,73 +342,69 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
     __syncthreads();                          // the gather plan is complete
     issue(0);
     cp_async_commit();
-    if (nrt > 1) issue(1);
-    cp_async_commit();
     const int lane = tid & 31, warp = tid >> 5;
     for (int i = 0; i < nrt; ++i) {
         const int b = i & 1;
         const int64_t r0 = (rt0 + i) * kQT;
-        uint16_t* tile = s_in + (i % kQBStages) * (kQT * kQT);
+        uint16_t* tile = s_in + b * (kQT * kQT);
+        // the other buffer (tile i - 1) was released by the barrier that
+        // ended tile i - 1: start tile i + 1 there
+        if (i + 1 < nrt) issue(i + 1);
+        cp_async_commit();
         cp_async_wait1();                     // this thread's copies of tile i have landed
         // rowwise, over this thread's own chunks (scaled in place first)
-#pragma unroll
+#pragma unroll 2
         for (int p = 0; p < 8; ++p) {
             const int rl = tr + 16 * p;
             uint4* cp = reinterpret_cast<uint4*>(tile + rl * kQT + tc * 8);
-            float f[8];
-            unpack8(*cp, f);
+            uint4 v = *cp;
             if (row_w != nullptr) {
+                float f[8];
+                unpack8(v, f);
                 const float w = s_w[i * kQT + rl];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[e] *= w;
-                const uint4 v = pack8(f);
+                v = pack8(f);
                 *cp = v;
-                unpack8(v, f);
             }
             if (codes_r != nullptr) {
-                float amax = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-                const uint32_t sb = e8m0_scale_byte(amax);
+                uint32_t m = bf16x2_absmax(bf16x2_absmax(0u, v.x), v.y);
+                m = bf16x2_absmax(bf16x2_absmax(m, v.z), v.w);
+                m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                const uint32_t sb = e8m0_scale_byte(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16));
                 const float inv = e8m0_inv_scale(sb);
-                uint32_t q[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) q[e] = cvt_e4m3x2(f[2 * e] * inv, f[2 * e + 1] * inv);
-                codes_r[((r0 + rl) * cols + (int64_t)ct * kQT) / 8 + tc] =
-                    make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+                const uint32_t q0 = cvt_e4m3x2(bf16_bits_lo(v.x) * inv, bf16_bits_hi(v.x) * inv);
+                const uint32_t q1 = cvt_e4m3x2(bf16_bits_lo(v.y) * inv, bf16_bits_hi(v.y) * inv);
+                const uint32_t q2 = cvt_e4m3x2(bf16_bits_lo(v.z) * inv, bf16_bits_hi(v.z) * inv);
+                const uint32_t q3 = cvt_e4m3x2(bf16_bits_lo(v.w) * inv, bf16_bits_hi(v.w) * inv);
+                codes_r[((r0 + rl) * cols + (int64_t)ct * kQT) / 8 + tc] = make_uint2(q0 | (q1 << 16), q2 | (q3 << 16));
                 if ((tc & 3) == 0)
                     s_atom_r[b * 512 + (rl & 31) * 16 + ((rl >> 5) & 3) * 4 + (tc >> 2)] = (uint8_t)sb;
             }
         }
-        __syncthreads();                      // A: tile i (scaled) complete; tile i - 1 fully done
-        // the buffer of tile i - 1 is free (its transposed codes were stored
-        // before barrier A): start tile i + 2 there
-        if (i + 2 < nrt) issue(i + 2);
-        cp_async_commit();
+        __syncthreads();                      // A: tile i (scaled) complete
         uint32_t w0[8], w1[8];
         const int blk = warp & 3;                       // 32-row block
         const int col = (warp >> 2) * 64 + 2 * lane;    // two columns per lane
         if (codes_c != nullptr) {
-            float f0[32], f1[32];
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const uint32_t v = *reinterpret_cast<const uint32_t*>(tile + (blk * 32 + e) * kQT + col);
-                f0[e] = __uint_as_float(v << 16);
-                f1[e] = __uint_as_float(v & 0xFFFF0000u);
-                a0 = fmaxf(a0, fabsf(f0[e]));
-                a1 = fmaxf(a1, fabsf(f1[e]));
-            }
-            const uint32_t b0 = e8m0_scale_byte(a0), b1 = e8m0_scale_byte(a1);
+            const uint32_t* colp = reinterpret_cast<const uint32_t*>(tile + blk * 32 * kQT + col);
+            // pass 1: amax of both columns over the block, on packed bf16 bits
+            uint32_t m = 0;
+#pragma unroll 8
+            for (int e = 0; e < 32; ++e) m = bf16x2_absmax(m, colp[e * (kQT / 2)]);
+            const uint32_t b0 = e8m0_scale_byte(__uint_as_float((m & 0xFFFFu) << 16));
+            const uint32_t b1 = e8m0_scale_byte(__uint_as_float(m & 0xFFFF0000u));
             const float i0 = e8m0_inv_scale(b0), i1 = e8m0_inv_scale(b1);
+            // pass 2: codes, two rows per conversion
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                w0[e] = cvt_e4m3x2(f0[4 * e] * i0, f0[4 * e + 1] * i0) |
-                        (cvt_e4m3x2(f0[4 * e + 2] * i0, f0[4 * e + 3] * i0) << 16);
-                w1[e] = cvt_e4m3x2(f1[4 * e] * i1, f1[4 * e + 1] * i1) |
-                        (cvt_e4m3x2(f1[4 * e + 2] * i1, f1[4 * e + 3] * i1) << 16);
+                const uint32_t v0 = colp[(4 * e) * (kQT / 2)], v1 = colp[(4 * e + 1) * (kQT / 2)];
+                const uint32_t v2 = colp[(4 * e + 2) * (kQT / 2)], v3 = colp[(4 * e + 3) * (kQT / 2)];
+                w0[e] = cvt_e4m3x2(bf16_bits_lo(v0) * i0, bf16_bits_lo(v1) * i0) |
+                        (cvt_e4m3x2(bf16_bits_lo(v2) * i0, bf16_bits_lo(v3) * i0) << 16);
+                w1[e] = cvt_e4m3x2(bf16_bits_hi(v0) * i1, bf16_bits_hi(v1) * i1) |
+                        (cvt_e4m3x2(bf16_bits_hi(v2) * i1, bf16_bits_hi(v3) * i1) << 16);
             }
             s_atom_c[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b0;
             s_atom_c[((col + 1) & 31) * 16 + (((col + 1) >> 5) & 3) * 4 + blk] = (uint8_t)b1;
@@ -437,6 +441,7 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_quant_both(const uint16_t* __
                 reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_c)[lane];
             }
         }
+        __syncthreads();                      // D: tile i's buffer (transposed codes) and the atoms are free
     }
 }
 
