@@ -154,7 +154,7 @@ def run_gpu(args, rank, world, local_rank):
             dist.barrier()
 
     # per-GEMM events: the GEMM launches of a step, in issue order
-    gemm_names = ["up_fwd_swiglu", "down_fwd", "down_dgrad_swiglu_bwd", "down_wgrad", "up_dgrad", "up_wgrad"]
+    gemm_names = ["up_fwd_swiglu", "down_fwd", "down_dgrad", "down_wgrad", "up_dgrad", "up_wgrad"]
     gemm_flops = [4 * L.R * d * f, 2 * L.R * d * f, 2 * L.R * d * f, 2 * L.R * d * f, 4 * L.R * d * f,
                   4 * L.R * d * f]
     for _ in range(args.warmup):
@@ -233,7 +233,7 @@ def run_gpu(args, rank, world, local_rank):
     R, q = L.R, 1 + 1 / 32
     algo_bytes = (R * d * q + E * d * 2 * f * q + R * 2 * f * 2 + 2 * R * f * q        # up fwd + SwiGLU + MXFP8(h)
                   + R * f * q + E * f * d * q + R * d * 2                               # down fwd
-                  + R * d * q + E * f * d * q + R * 2 * f * 2 * 2                       # down dgrad + SwiGLU bwd
+                  + R * d * q + E * f * d * q + R * f * 4                               # down dgrad (fp32 dH)
                   + R * f * q + R * d * q + E * f * d * 2                               # dW2
                   + R * 2 * f * q + E * d * 2 * f * q + R * d * 2                       # up dgrad
                   + R * d * q + R * 2 * f * q + E * d * 2 * f * 2)                      # dW1

@@ -70,6 +70,22 @@ __device__ __forceinline__ float e8m0_inv_scale(uint32_t b) {
     return __uint_as_float((254u - b) << 23);
 }
 
+// sigmoid(x) with the fast exponential and division; x is clamped at -80
+// so that 1 + exp(-x) stays finite (sigmoid(-80) ~ 2e-35).
+__device__ __forceinline__ float fast_sigmoid(float x) {
+    return __fdividef(1.f, 1.f + __expf(-fmaxf(x, -80.f)));
+}
+
+// SwiGLU backward of one element: h = g * sigmoid(g) * u, upstream dh:
+// dg = dh * u * s * (1 + g * (1 - s)), du = dh * g * s with s = sigmoid(g).
+// Shared by the GEMM epilogue and the fused quantization so both produce
+// the same fp32 values.
+__device__ __forceinline__ void swiglu_bwd_pair(float g, float u, float dh, float& dg, float& du) {
+    const float s = fast_sigmoid(g);
+    dg = dh * u * s * (1.f + g * (1.f - s));
+    du = dh * g * s;
+}
+
 // Two fp32 -> two E4M3 bytes (round-to-nearest-even, saturate to +-448);
 // the byte of `lo` is the low byte of the result.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {

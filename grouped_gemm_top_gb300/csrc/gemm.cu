@@ -98,7 +98,9 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
 
 // --------------------------------------------------------------- kernel ----
 
-template <int BN>
+// EPI: the epilogue (moe_epilogue_t), fixed at compile time so each
+// instance keeps only its own epilogue's registers.
+template <int BN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
     using C = Cfg<BN>;
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 continue;
             }
             ApreChunk apre;
-            if (p.epi == MOE_EPI_SWIGLU_BWD) {
+            if constexpr (EPI == MOE_EPI_SWIGLU_BWD) {
                 if (t + gridDim.x < total) {      // FWD/DGRAD only: rows = m-tile * 128
                     int64_t mt;
                     int nt;
@@ -308,12 +310,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty);
             };
-            if (p.epi == MOE_EPI_SWIGLU_BWD) {
+            if constexpr (EPI == MOE_EPI_SWIGLU_BWD) {
                 epilogue_swiglu_bwd<BN>(p, tacc, row, ti.nt, half, release, apre);
-            } else if (BN == 256) {
-                epilogue_tile_staged(p, tacc, row, ti.nt, half, release);
+            } else if constexpr (BN == 256) {
+                epilogue_tile_staged<EPI>(p, tacc, row, ti.nt, half, release);
             } else {
-                epilogue_tile<BN>(p, tacc, row, ti.nt, half);
+                epilogue_tile<BN, EPI>(p, tacc, row, ti.nt, half);
                 release();
             }
             if (++acc == NACC) {
@@ -346,14 +348,39 @@ cudaError_t gemm_init_driver() {
     return cudaSuccess;
 }
 
+template <int BN, int EPI>
+static cudaError_t set_attr_1sm() {
+    return cudaFuncSetAttribute(gg::k_grouped_gemm<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gg::Cfg<BN>::SMEM_BYTES);
+}
+
 cudaError_t gemm_set_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(gg::k_grouped_gemm<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gg::Cfg<128>::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gg::k_grouped_gemm<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gg::Cfg<256>::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    const cudaError_t es[] = {set_attr_1sm<128, MOE_EPI_NONE>(),     set_attr_1sm<128, MOE_EPI_SWIGLU>(),
+                              set_attr_1sm<128, MOE_EPI_SWIGLU_BWD>(), set_attr_1sm<128, MOE_EPI_NONE_F32>(),
+                              set_attr_1sm<256, MOE_EPI_NONE>(),     set_attr_1sm<256, MOE_EPI_SWIGLU>(),
+                              set_attr_1sm<256, MOE_EPI_SWIGLU_BWD>(), set_attr_1sm<256, MOE_EPI_NONE_F32>()};
+    for (cudaError_t e : es)
+        if (e != cudaSuccess) return e;
     return gemm_set_attributes_2sm();
+}
+
+template <int BN>
+static void launch_1sm(int epilogue, int grid, const CUtensorMap& tmA, const CUtensorMap& tmB, const gg::Params& p,
+                       cudaStream_t s) {
+    using namespace gg;
+    switch (epilogue) {
+        case MOE_EPI_SWIGLU:
+            k_grouped_gemm<BN, MOE_EPI_SWIGLU><<<grid, THREADS, Cfg<BN>::SMEM_BYTES, s>>>(tmA, tmB, p);
+            break;
+        case MOE_EPI_SWIGLU_BWD:
+            k_grouped_gemm<BN, MOE_EPI_SWIGLU_BWD><<<grid, THREADS, Cfg<BN>::SMEM_BYTES, s>>>(tmA, tmB, p);
+            break;
+        case MOE_EPI_NONE_F32:
+            k_grouped_gemm<BN, MOE_EPI_NONE_F32><<<grid, THREADS, Cfg<BN>::SMEM_BYTES, s>>>(tmA, tmB, p);
+            break;
+        default:
+            k_grouped_gemm<BN, MOE_EPI_NONE><<<grid, THREADS, Cfg<BN>::SMEM_BYTES, s>>>(tmA, tmB, p);
+    }
 }
 
 // Kernel choice.  WGRAD runs on the CTA-pair kernel (gemm2sm.cu, 256 x 256
@@ -464,7 +491,8 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
         MOE_REQUIRE(epilogue == MOE_EPI_NONE, MOE_ERR_INVALID_ARG);
     } else {
         MOE_REQUIRE(b_layout == MOE_B_GNK || b_layout == MOE_B_NGK, MOE_ERR_INVALID_ARG);
-        MOE_REQUIRE(epilogue == MOE_EPI_NONE || epilogue == MOE_EPI_SWIGLU || epilogue == MOE_EPI_SWIGLU_BWD,
+        MOE_REQUIRE(epilogue == MOE_EPI_NONE || epilogue == MOE_EPI_SWIGLU || epilogue == MOE_EPI_SWIGLU_BWD ||
+                        epilogue == MOE_EPI_NONE_F32,
                     MOE_ERR_INVALID_ARG);
         if (epilogue == MOE_EPI_SWIGLU) MOE_REQUIRE(d2 != nullptr || hq.codes_row != nullptr, MOE_ERR_INVALID_ARG);
         if (epilogue == MOE_EPI_SWIGLU_BWD) MOE_REQUIRE(epi_aux != nullptr, MOE_ERR_INVALID_ARG);
@@ -570,12 +598,13 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
             const int64_t drows = mode == MOE_GEMM_WGRAD ? (int64_t)G * M : M;
             MOE_REQUIRE(make_d_map(&tmD, d, drows, N), MOE_ERR_CUDA);
         }
-        if (gemm_launch_2sm(bn2, tmA, tmB2, tmSFA, tmSFB, tmD, p, clusters, (cudaStream_t)stream) != cudaSuccess)
+        if (gemm_launch_2sm(bn2, epilogue, tmA, tmB2, tmSFA, tmSFB, tmD, p, clusters, (cudaStream_t)stream) !=
+            cudaSuccess)
             return MOE_ERR_CUDA;
     } else if (BN == 256)
-        k_grouped_gemm<256><<<grid, THREADS, Cfg<256>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);
+        launch_1sm<256>(epilogue, grid, tmA, tmB, p, (cudaStream_t)stream);
     else
-        k_grouped_gemm<128><<<grid, THREADS, Cfg<128>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);
+        launch_1sm<128>(epilogue, grid, tmA, tmB, p, (cudaStream_t)stream);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }

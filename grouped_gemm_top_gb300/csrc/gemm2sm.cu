@@ -207,7 +207,7 @@ __device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, co
     ti.nt = nt;
 }
 
-template <int BN>
+template <int BN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 continue;
             }
             ApreChunk apre;
-            if (p.epi == MOE_EPI_SWIGLU_BWD && ti.valid) {
+            if (EPI == MOE_EPI_SWIGLU_BWD && ti.valid) {
                 if (t + npairs < total) {
                     Tile2 tn;
                     get_tile2<BN>(p, s_gofs, s_pt, total_pm, t + npairs, rank, tn);
@@ -424,15 +424,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             };
             if (!ti.valid) {
                 release();
-            } else if (p.epi == MOE_EPI_SWIGLU_BWD) {
+            } else if constexpr (EPI == MOE_EPI_SWIGLU_BWD) {
                 epilogue_swiglu_bwd<BN>(p, tacc, row, ti.nt, half, release, apre);
-            } else if (BN == 256 && p.tma_store) {
+            } else if (BN == 256 && EPI == MOE_EPI_NONE && p.tma_store) {
                 epilogue_tile_tma(&tmD, smem_u32(smem + C::OFF_EPI + 4096 * ew), tacc, row - lane, ti.nt, half, lane,
                                   release);
-            } else if (BN == 256) {
-                epilogue_tile_staged(p, tacc, row, ti.nt, half, release);
+            } else if constexpr (BN == 256) {
+                epilogue_tile_staged<EPI>(p, tacc, row, ti.nt, half, release);
             } else {
-                epilogue_tile<BN>(p, tacc, row, ti.nt, half);
+                epilogue_tile<BN, EPI>(p, tacc, row, ti.nt, half);
                 release();
             }
             if (++acc == NACC) {
@@ -476,15 +476,22 @@ static cudaLaunchConfig_t launch_cfg(int clusters, cudaStream_t stream, cudaLaun
     return cfg;
 }
 
+template <int BN, int EPI>
+static cudaError_t set_attr_one() {
+    return cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gg::sm2::C2<BN>::SMEM_BYTES);
+}
+
 template <int BN>
 static cudaError_t set_attr_2sm(int* max_clusters) {
-    cudaError_t e = cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gg::sm2::C2<BN>::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    const cudaError_t es[] = {set_attr_one<BN, MOE_EPI_NONE>(), set_attr_one<BN, MOE_EPI_SWIGLU>(),
+                              set_attr_one<BN, MOE_EPI_SWIGLU_BWD>(), set_attr_one<BN, MOE_EPI_NONE_F32>()};
+    for (cudaError_t e : es)
+        if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_cfg<BN>(1024, nullptr, attr);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gg::sm2::k_grouped_gemm_2sm<BN>, &cfg);
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, gg::sm2::k_grouped_gemm_2sm<BN, MOE_EPI_NONE>, &cfg);
     if (e != cudaSuccess) return e;
     *max_clusters = n;
     if (getenv("MOE_DEBUG") != nullptr) fprintf(stderr, "libmoe: N=%d pair tiles: %d co-resident CTA pairs\n", BN, n);
@@ -499,16 +506,33 @@ cudaError_t gemm_set_attributes_2sm() {
 
 int gemm_max_clusters_2sm(int bn) { return g_max_clusters[bn == 256 ? 1 : 0]; }
 
-cudaError_t gemm_launch_2sm(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                            const CUtensorMap& tmSFB, const CUtensorMap& tmD, const gg::Params& p, int clusters,
-                            cudaStream_t stream) {
+template <int BN>
+static cudaError_t launch_2sm(int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                              const CUtensorMap& tmSFB, const CUtensorMap& tmD, const gg::Params& p, int clusters,
+                              cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
-    if (bn == 256) {
-        cudaLaunchConfig_t cfg = launch_cfg<256>(clusters, stream, attr);
-        return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<256>, tmA, tmB, tmSFA, tmSFB, tmD, p);
+    cudaLaunchConfig_t cfg = launch_cfg<BN>(clusters, stream, attr);
+    switch (epilogue) {
+        case MOE_EPI_SWIGLU:
+            return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<BN, MOE_EPI_SWIGLU>, tmA, tmB, tmSFA, tmSFB,
+                                      tmD, p);
+        case MOE_EPI_SWIGLU_BWD:
+            return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<BN, MOE_EPI_SWIGLU_BWD>, tmA, tmB, tmSFA,
+                                      tmSFB, tmD, p);
+        case MOE_EPI_NONE_F32:
+            return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<BN, MOE_EPI_NONE_F32>, tmA, tmB, tmSFA, tmSFB,
+                                      tmD, p);
+        default:
+            return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<BN, MOE_EPI_NONE>, tmA, tmB, tmSFA, tmSFB,
+                                      tmD, p);
     }
-    cudaLaunchConfig_t cfg = launch_cfg<128>(clusters, stream, attr);
-    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<128>, tmA, tmB, tmSFA, tmSFB, tmD, p);
+}
+
+cudaError_t gemm_launch_2sm(int bn, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                            const CUtensorMap& tmSFA, const CUtensorMap& tmSFB, const CUtensorMap& tmD,
+                            const gg::Params& p, int clusters, cudaStream_t stream) {
+    if (bn == 256) return launch_2sm<256>(epilogue, tmA, tmB, tmSFA, tmSFB, tmD, p, clusters, stream);
+    return launch_2sm<128>(epilogue, tmA, tmB, tmSFA, tmSFB, tmD, p, clusters, stream);
 }
 
 }  // namespace moe

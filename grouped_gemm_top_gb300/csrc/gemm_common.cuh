@@ -198,11 +198,6 @@ __device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// sigmoid(x) with the fast exponential and division; x is clamped at -80
-// so that 1 + exp(-x) stays finite (sigmoid(-80) ~ 2e-35).
-__device__ __forceinline__ float fast_sigmoid(float x) {
-    return __fdividef(1.f, 1.f + __expf(-fmaxf(x, -80.f)));
-}
 
 // Two bf16 (RNE) packed into one word, `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -323,10 +318,10 @@ __device__ __forceinline__ void h_quant_chunk(const Params& p, int64_t row, int6
 // quarter `quarter` (rows quarter*32 + lane of the tile) and column half
 // `half` of the tile.  `row` is this thread's output row, `nt` the tile
 // index along N.  Writes bf16 results with the fused activation.
-template <int BN>
+template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, int64_t row, int nt, int half) {
     float v[32];
-    if (p.epi == MOE_EPI_SWIGLU) {
+    if constexpr (EPI == MOE_EPI_SWIGLU) {
         // B rows interleave gate/up in 64-row chunks: accumulator columns
         // [128q, 128q+64) are gate, [128q+64, 128q+128) up
         const int64_t N = p.N, f = p.N / 2;
@@ -348,7 +343,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
                 h_quant_chunk(p, row, hcol, ph, (int)(threadIdx.x & 31));
             }
         }
-    } else if (p.epi == MOE_EPI_SWIGLU_BWD) {
+    } else if constexpr (EPI == MOE_EPI_SWIGLU_BWD) {
         const int64_t N = p.N, ld = 2 * (int64_t)p.N;
         for (int c = 0; c < BN / 64; ++c) {
             float g[32], u[32], dg[32], du[32];
@@ -359,12 +354,22 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
             load_row32(p.aux + row * ld + N + col, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float s = fast_sigmoid(g[i]);
-                dg[i] = v[i] * u[i] * s * (1.f + g[i] * (1.f - s));
-                du[i] = v[i] * g[i] * s;
+                swiglu_bwd_pair(g[i], u[i], v[i], dg[i], du[i]);
             }
             store_row32(p.d + row * ld + col, dg);
             store_row32(p.d + row * ld + N + col, du);
+        }
+    } else if constexpr (EPI == MOE_EPI_NONE_F32) {
+        float* out = reinterpret_cast<float*>(p.d) + row * p.N + (int64_t)nt * BN;
+        for (int c = 0; c < BN / 64; ++c) {
+            const int col32 = half * (BN / 2) + 32 * c;
+            tmem_ld32(tacc + col32, v);
+            uint32_t* o = reinterpret_cast<uint32_t*>(out + col32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_global_v8(o + 8 * q, __float_as_uint(v[8 * q]), __float_as_uint(v[8 * q + 1]),
+                             __float_as_uint(v[8 * q + 2]), __float_as_uint(v[8 * q + 3]), __float_as_uint(v[8 * q + 4]),
+                             __float_as_uint(v[8 * q + 5]), __float_as_uint(v[8 * q + 6]), __float_as_uint(v[8 * q + 7]));
         }
     } else {
         for (int c = 0; c < BN / 64; ++c) {
@@ -381,11 +386,11 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
 // bf16 (two TMEM loads in flight per wait), calls release() so the MMA warp
 // can reuse TMEM, and only then writes global memory, overlapped with the
 // next tile's MMAs.  SwiGLU-backward has its own pipelined epilogue below.
-template <typename Release>
+template <int EPI, typename Release>
 __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t tacc, int64_t row, int nt, int half,
                                                      Release release) {
     uint32_t ra[32], rb[32];
-    if (p.epi == MOE_EPI_SWIGLU) {
+    if constexpr (EPI == MOE_EPI_SWIGLU) {
         // units u = 2*half, 2*half+1: gate columns [128q + 32c, +32) and up
         // columns [128q + 64 + 32c, +32) with q = u / 2 = half, c = u % 2.
         // Chunk 0 is converted while chunk 1 is still in TMEM and written
@@ -437,6 +442,24 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
             const int lane = (int)(threadIdx.x & 31);
             h_quant_chunk(p, row, hcol, ph0, lane);
             h_quant_chunk(p, row, hcol + 32, ph, lane);
+        }
+    } else if constexpr (EPI == MOE_EPI_NONE_F32) {
+        // fp32 out: each 32-column chunk is stored as it is drained
+        uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<float*>(p.d) + row * p.N + (int64_t)nt * 256 +
+                                                    128 * half);
+#pragma unroll
+        for (int c = 0; c < 4; c += 2) {
+            tmem_ld32_issue(tacc + 128 * half + 32 * c, ra);
+            tmem_ld32_issue(tacc + 128 * half + 32 * (c + 1), rb);
+            tmem_wait_ld();
+            if (c == 2) release();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                st_global_v8(out + 32 * c + 8 * q, ra[8 * q], ra[8 * q + 1], ra[8 * q + 2], ra[8 * q + 3], ra[8 * q + 4],
+                             ra[8 * q + 5], ra[8 * q + 6], ra[8 * q + 7]);
+                st_global_v8(out + 32 * (c + 1) + 8 * q, rb[8 * q], rb[8 * q + 1], rb[8 * q + 2], rb[8 * q + 3],
+                             rb[8 * q + 4], rb[8 * q + 5], rb[8 * q + 6], rb[8 * q + 7]);
+            }
         }
     } else {
         uint32_t pk[64];
@@ -563,9 +586,7 @@ __device__ __forceinline__ void epilogue_swiglu_bwd(const Params& p, uint32_t ta
                 const float g = __uint_as_float(e ? (gw & 0xFFFF0000u) : (gw << 16));
                 const float u = __uint_as_float(e ? (uw & 0xFFFF0000u) : (uw << 16));
                 const float dh = __uint_as_float(r[2 * i + e]);
-                const float s = fast_sigmoid(g);
-                dg[e] = dh * u * s * (1.f + g * (1.f - s));
-                du[e] = dh * g * s;
+                swiglu_bwd_pair(g, u, dh, dg[e], du[e]);
             }
             pdg[i] = pack_bf16x2(dg[0], dg[1]);
             pdu[i] = pack_bf16x2(du[0], du[1]);
@@ -598,7 +619,7 @@ __device__ __forceinline__ void epilogue_zero(const Params& p, int64_t row, int 
 // Host side (gemm.cu)
 cudaError_t gemm_set_attributes_2sm();   // gemm2sm.cu
 int gemm_max_clusters_2sm(int bn);        // co-resident CTA pairs for N = bn pair tiles
-cudaError_t gemm_launch_2sm(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                            const CUtensorMap& tmSFB, const CUtensorMap& tmD, const gg::Params& p, int clusters,
-                            cudaStream_t stream);
+cudaError_t gemm_launch_2sm(int bn, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                            const CUtensorMap& tmSFA, const CUtensorMap& tmSFB, const CUtensorMap& tmD,
+                            const gg::Params& p, int clusters, cudaStream_t stream);
 }  // namespace moe

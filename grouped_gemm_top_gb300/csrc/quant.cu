@@ -445,8 +445,195 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
     }
 }
 
+// ---------------------------------------------------------------------------
+// SwiGLU backward fused with the two-axis quantization of its output.
+//
+// dA = [dgate | dup] ([M, 2f]) with dgate = dH*u*s*(1+g*(1-s)), dup = dH*g*s,
+// s = sigmoid(g), from the dgrad GEMM's fp32 dH [M, f] and the forward's
+// bf16 a_pre = [g | u] [M, 2f]; every element is rounded to bf16 and then
+// quantized exactly as mxfp8_gather_quantize quantizes a stored dA (rowwise
+// and group-columnwise), so dA never exists in bf16 in memory.  Moving this
+// elementwise step out of the dgrad GEMM's epilogue frees that GEMM's single
+// TMEM accumulator sooner; this pass has to touch dA anyway.
+//
+// A CTA owns one 128-column tile c0 of dH (hence output column tiles c0 of
+// dgate and f + c0 of dup, which need the same dH, g and u) and a run of
+// kQBRowTiles row tiles.  Per row tile each thread loads its eight 8-element
+// chunks of dH, g and u, computes dgate and dup, quantizes them rowwise from
+// registers and stages them in two shared-memory tiles for the columnwise
+// blocks, done as in k_quant_both.
+constexpr int kSBSmem = 2 * kQBInBytes + 4 * 512;
+
+__device__ __forceinline__ uint2 quant_row_chunk(uint4 v, uint32_t& sb_out) {
+    uint32_t m = bf16x2_absmax(bf16x2_absmax(0u, v.x), v.y);
+    m = bf16x2_absmax(bf16x2_absmax(m, v.z), v.w);
+    m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    const uint32_t sb = e8m0_scale_byte(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16));
+    const float inv = e8m0_inv_scale(sb);
+    const uint32_t q0 = cvt_e4m3x2(bf16_bits_lo(v.x) * inv, bf16_bits_hi(v.x) * inv);
+    const uint32_t q1 = cvt_e4m3x2(bf16_bits_lo(v.y) * inv, bf16_bits_hi(v.y) * inv);
+    const uint32_t q2 = cvt_e4m3x2(bf16_bits_lo(v.z) * inv, bf16_bits_hi(v.z) * inv);
+    const uint32_t q3 = cvt_e4m3x2(bf16_bits_lo(v.w) * inv, bf16_bits_hi(v.w) * inv);
+    sb_out = sb;
+    return make_uint2(q0 | (q1 << 16), q2 | (q3 << 16));
+}
+
+// columnwise block (32 rows `blk`, columns col and col + 1) of a bf16 tile in
+// shared memory: codes of the two columns (8 words each) and scale bytes
+__device__ __forceinline__ void quant_col_block(const uint16_t* tile, int blk, int col, uint32_t* w0, uint32_t* w1,
+                                                uint32_t& b0, uint32_t& b1) {
+    const uint32_t* colp = reinterpret_cast<const uint32_t*>(tile + blk * 32 * kQT + col);
+    uint32_t m = 0;
+#pragma unroll 8
+    for (int e = 0; e < 32; ++e) m = bf16x2_absmax(m, colp[e * (kQT / 2)]);
+    b0 = e8m0_scale_byte(__uint_as_float((m & 0xFFFFu) << 16));
+    b1 = e8m0_scale_byte(__uint_as_float(m & 0xFFFF0000u));
+    const float i0 = e8m0_inv_scale(b0), i1 = e8m0_inv_scale(b1);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t v0 = colp[(4 * e) * (kQT / 2)], v1 = colp[(4 * e + 1) * (kQT / 2)];
+        const uint32_t v2 = colp[(4 * e + 2) * (kQT / 2)], v3 = colp[(4 * e + 3) * (kQT / 2)];
+        w0[e] = cvt_e4m3x2(bf16_bits_lo(v0) * i0, bf16_bits_lo(v1) * i0) |
+                (cvt_e4m3x2(bf16_bits_lo(v2) * i0, bf16_bits_lo(v3) * i0) << 16);
+        w1[e] = cvt_e4m3x2(bf16_bits_hi(v0) * i1, bf16_bits_hi(v1) * i1) |
+                (cvt_e4m3x2(bf16_bits_hi(v2) * i1, bf16_bits_hi(v3) * i1) << 16);
+    }
+}
+
+__global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float* __restrict__ dH,
+                                                                    const uint16_t* __restrict__ a_pre, int f,
+                                                                    const int32_t* __restrict__ gofs, int G,
+                                                                    int64_t rows, uint16_t* __restrict__ dA,
+                                                                    uint2* __restrict__ codes_r,
+                                                                    uint8_t* __restrict__ sf_r,
+                                                                    uint8_t* __restrict__ codes_c,
+                                                                    uint8_t* __restrict__ sf_c, int32_t* err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint16_t* tiles = reinterpret_cast<uint16_t*>(smem);           // [2][128][128]: dgate, dup
+    uint8_t* s_atom_r = smem + 2 * kQBInBytes;                     // [2][512]
+    uint8_t* s_atom_c = s_atom_r + 2 * 512;                        // [2][512]
+    const int tid = threadIdx.x;
+    const int ct = blockIdx.y;                                     // column tile of dH / g / u
+    const int64_t c0 = (int64_t)ct * kQT;
+    const int64_t rt0 = (int64_t)blockIdx.x * kQBRowTiles;
+    const int64_t F = f, F2 = 2 * (int64_t)f;
+    const int out_tiles = (int)(F2 / kQT);
+    auto octile = [&](int t) { return t == 0 ? ct : ct + f / kQT; };   // output column tiles: dgate, dup
+
+    bool ok = true;
+    for (int i = tid; i <= G; i += kQBThreads) {
+        const int a = gofs[i];
+        if ((a & 127) != 0 || (i == 0 && a != 0)) ok = false;
+        if (i < G && gofs[i + 1] < a) ok = false;
+        if (i == G && (int64_t)a > rows) ok = false;
+    }
+    if (!__syncthreads_and(ok)) {
+        if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) set_err(err, MOE_ERR_BAD_OFFSETS);
+        return;
+    }
+    const int nrt = (int)min((int64_t)kQBRowTiles, (int64_t)gofs[G] / kQT - rt0);
+    if (nrt <= 0) return;
+
+    const int tc = tid & 15, tr = tid >> 4;
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int i = 0; i < nrt; ++i) {
+        const int64_t r0 = (rt0 + i) * kQT;
+        // dgate / dup of this thread's chunks: rowwise codes from registers,
+        // bf16 values into the two tiles
+#pragma unroll 2
+        for (int p = 0; p < 8; ++p) {
+            const int rl = tr + 16 * p;
+            const int64_t r = r0 + rl;
+            const float4* hp = reinterpret_cast<const float4*>(dH + r * F + c0 + tc * 8);
+            const float4 h0 = __ldg(hp), h1 = __ldg(hp + 1);
+            const uint4 gw = __ldg(reinterpret_cast<const uint4*>(a_pre + r * F2 + c0 + tc * 8));
+            const uint4 uw = __ldg(reinterpret_cast<const uint4*>(a_pre + r * F2 + F + c0 + tc * 8));
+            float gf[8], uf[8], dg[8], du[8];
+            const float hf[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+            unpack8(gw, gf);
+            unpack8(uw, uf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) swiglu_bwd_pair(gf[e], uf[e], hf[e], dg[e], du[e]);
+            const uint4 vg = pack8(dg), vu = pack8(du);
+            if (dA != nullptr) {
+                *reinterpret_cast<uint4*>(dA + r * F2 + c0 + tc * 8) = vg;
+                *reinterpret_cast<uint4*>(dA + r * F2 + F + c0 + tc * 8) = vu;
+            }
+            uint32_t sg, su;
+            const uint2 qg = quant_row_chunk(vg, sg);
+            const uint2 qu = quant_row_chunk(vu, su);
+            codes_r[(r * F2 + c0) / 8 + tc] = qg;
+            codes_r[(r * F2 + F + c0) / 8 + tc] = qu;
+            if ((tc & 3) == 0) {
+                const int ab = (rl & 31) * 16 + ((rl >> 5) & 3) * 4 + (tc >> 2);
+                s_atom_r[ab] = (uint8_t)sg;
+                s_atom_r[512 + ab] = (uint8_t)su;
+            }
+            *reinterpret_cast<uint4*>(tiles + rl * kQT + tc * 8) = vg;
+            *reinterpret_cast<uint4*>(tiles + kQT * kQT + rl * kQT + tc * 8) = vu;
+        }
+        __syncthreads();                      // A: both tiles complete
+        const int blk = warp & 3;
+        const int col = (warp >> 2) * 64 + 2 * lane;
+        uint32_t wg0[8], wg1[8], wu0[8], wu1[8];
+        uint32_t bg0, bg1, bu0, bu1;
+        quant_col_block(tiles, blk, col, wg0, wg1, bg0, bg1);
+        quant_col_block(tiles + kQT * kQT, blk, col, wu0, wu1, bu0, bu1);
+        const int a0 = (col & 31) * 16 + ((col >> 5) & 3) * 4 + blk;
+        const int a1 = ((col + 1) & 31) * 16 + (((col + 1) >> 5) & 3) * 4 + blk;
+        s_atom_c[a0] = (uint8_t)bg0;
+        s_atom_c[a1] = (uint8_t)bg1;
+        s_atom_c[512 + a0] = (uint8_t)bu0;
+        s_atom_c[512 + a1] = (uint8_t)bu1;
+        __syncthreads();                      // B: every thread is done reading both tiles
+        {
+            uint8_t* qg = reinterpret_cast<uint8_t*>(tiles);
+            uint8_t* qu = reinterpret_cast<uint8_t*>(tiles + kQT * kQT);
+            uint4* d;
+            d = reinterpret_cast<uint4*>(qg + col * kQBQPitch + blk * 32);
+            d[0] = make_uint4(wg0[0], wg0[1], wg0[2], wg0[3]);
+            d[1] = make_uint4(wg0[4], wg0[5], wg0[6], wg0[7]);
+            d = reinterpret_cast<uint4*>(qg + (col + 1) * kQBQPitch + blk * 32);
+            d[0] = make_uint4(wg1[0], wg1[1], wg1[2], wg1[3]);
+            d[1] = make_uint4(wg1[4], wg1[5], wg1[6], wg1[7]);
+            d = reinterpret_cast<uint4*>(qu + col * kQBQPitch + blk * 32);
+            d[0] = make_uint4(wu0[0], wu0[1], wu0[2], wu0[3]);
+            d[1] = make_uint4(wu0[4], wu0[5], wu0[6], wu0[7]);
+            d = reinterpret_cast<uint4*>(qu + (col + 1) * kQBQPitch + blk * 32);
+            d[0] = make_uint4(wu1[0], wu1[1], wu1[2], wu1[3]);
+            d[1] = make_uint4(wu1[4], wu1[5], wu1[6], wu1[7]);
+        }
+        __syncthreads();                      // C: transposed codes and atoms complete
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint8_t* s_q = reinterpret_cast<const uint8_t*>(tiles + t * kQT * kQT);
+            const int64_t oc = (int64_t)octile(t) * kQT;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int idx = tid + kQBThreads * p;
+                const int cl = idx >> 3, cv = idx & 7;
+                const uint4 q = *reinterpret_cast<const uint4*>(s_q + cl * kQBQPitch + cv * 16);
+                *reinterpret_cast<uint4*>(codes_c + (oc + cl) * rows + r0 + cv * 16) = q;
+            }
+        }
+        if (warp < 2) {
+            const int t = warp;
+            const int64_t atom = (int64_t)octile(t) * (rows / kQT) + r0 / kQT;
+            reinterpret_cast<uint4*>(sf_r + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_r + t * 512)[lane];
+        } else if (warp < 4) {
+            const int t = warp - 2;
+            const int64_t atom = (r0 / kQT) * (int64_t)out_tiles + octile(t);
+            reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_c + t * 512)[lane];
+        }
+        __syncthreads();                      // D: tiles and atoms are free
+    }
+}
+
 cudaError_t quant_set_attributes() {
-    return cudaFuncSetAttribute(k_quant_both, cudaFuncAttributeMaxDynamicSharedMemorySize, kQBSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_quant_both, cudaFuncAttributeMaxDynamicSharedMemorySize, kQBSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_swiglu_bwd_quant, cudaFuncAttributeMaxDynamicSharedMemorySize, kSBSmem);
 }
 
 }  // namespace moe
@@ -475,6 +662,27 @@ extern "C" moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows,
     k_quant_both<<<grid, kQBThreads, kQBSmem, (cudaStream_t)stream>>>((const uint16_t*)src, src_rows, cols, k, row_id,
                                                                      row_w, gofs, G, rows, (uint2*)codes_row,
                                                                      scales_row, codes_col, scales_col, err);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+extern "C" moe_status_t mxfp8_swiglu_bwd_quantize(const float* dH, const void* a_pre, int f, const int32_t* gofs,
+                                                  int G, int64_t rows, void* dA, uint8_t* codes_row,
+                                                  uint8_t* scales_row, uint8_t* codes_col, uint8_t* scales_col,
+                                                  int32_t* err, void* stream) {
+    using namespace moe;
+    MOE_REQUIRE(dH && a_pre && gofs && codes_row && scales_row && codes_col && scales_col, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(G >= 1 && G <= 4096 && f > 0 && rows > 0, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(f % kQT == 0 && rows % kQT == 0 && rows <= 0x7FFFFFFF && f / kQT <= 65535, MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(moe_aligned16(dH) && moe_aligned16(a_pre) && moe_aligned16(dA) && moe_aligned16(codes_row) &&
+                    moe_aligned16(scales_row) && moe_aligned16(codes_col) && moe_aligned16(scales_col),
+                MOE_ERR_ALIGNMENT);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    const int64_t row_runs = (rows / kQT + kQBRowTiles - 1) / kQBRowTiles;
+    dim3 grid((unsigned)row_runs, (unsigned)(f / kQT));
+    k_swiglu_bwd_quant<<<grid, kQBThreads, kSBSmem, (cudaStream_t)stream>>>(
+        dH, (const uint16_t*)a_pre, f, gofs, G, rows, (uint16_t*)dA, (uint2*)codes_row, scales_row, codes_col,
+        scales_col, err);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }

@@ -17,9 +17,10 @@ _SCORES = {"softmax": ops.MOE_SCORE_SOFTMAX, "sigmoid": ops.MOE_SCORE_SIGMOID}
 
 
 class MoELayer:
-    def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_h=False):
-        """store_h: also write h in bf16 (the step itself only needs its MXFP8
-        codes, which the up/gate GEMM's epilogue produces)."""
+    def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_intermediates=False):
+        """store_intermediates: also write h and dA in bf16 (the step itself
+        only needs their MXFP8 codes, which the up/gate GEMM's epilogue and
+        the fused SwiGLU-backward quantization produce)."""
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
         self.score = _SCORES[score]
         self.normalize = bool(normalize)
@@ -51,7 +52,7 @@ class MoELayer:
         # are quantized, along both axes, straight from x and dout)
         self.xq, self.xs = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.a_pre = z((M, 2 * f), torch.bfloat16)
-        self.h = z((M, f), torch.bfloat16) if store_h else None
+        self.h = z((M, f), torch.bfloat16) if store_intermediates else None
         self.hq, self.hs = z((M, f), torch.uint8), z((ops.sf_bytes(M, f),), torch.uint8)
         self.y_perm = z((M, d), torch.bfloat16)
         self.out = z((T, d), torch.bfloat16)
@@ -60,7 +61,8 @@ class MoELayer:
         self.dyq, self.dys = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.dyqT, self.dysT = z((d, M), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.hqT, self.hsT = z((f, M), torch.uint8), z((ops.sf_bytes(M, f),), torch.uint8)
-        self.dA = z((M, 2 * f), torch.bfloat16)
+        self.dH = z((M, f), torch.float32)
+        self.dA = z((M, 2 * f), torch.bfloat16) if store_intermediates else None
         self.dAq, self.dAs = z((M, 2 * f), torch.uint8), z((ops.sf_bytes(M, 2 * f),), torch.uint8)
         self.dAqT, self.dAsT = z((2 * f, M), torch.uint8), z((ops.sf_bytes(M, 2 * f),), torch.uint8)
         self.xqT, self.xsT = z((d, M), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
@@ -139,14 +141,16 @@ class MoELayer:
                             want_dy=False)
         ops.mxfp8_gather_quantize(self.dout, self.gofs, E, M, self.row_id, k, self.topk_w, True, True, self.dyq,
                                   self.dys, self.dyqT, self.dysT, err)
-        # dH = dY W2^T with the SwiGLU backward fused: dA = [dgate | dup]
+        # dH = dY W2^T (fp32)
         self._gemm(ops.MOE_GEMM_DGRAD, self.dyq, self.dys, self.W2d, self.W2d_s, ops.MOE_B_GNK,
-                   self.gofs, E, M, f, d, ops.MOE_EPI_SWIGLU_BWD, self.a_pre, self.dA, None, err)
+                   self.gofs, E, M, f, d, ops.MOE_EPI_NONE_F32, None, self.dH, None, err)
         # dW2_g = H_g^T dY_g
         self._gemm(ops.MOE_GEMM_WGRAD, self.hqT, self.hsT, self.dyqT, self.dysT, 0, self.gofs, E, f,
                    d, M, ops.MOE_EPI_NONE, None, self.dW2, None, err)
-        ops.mxfp8_gather_quantize(self.dA, self.gofs, E, M, None, 1, None, True, True, self.dAq, self.dAs,
-                                  self.dAqT, self.dAsT, err)
+        # dA = [dgate | dup] = SwiGLU backward of (a_pre, dH), quantized on
+        # both axes in the same pass
+        ops.mxfp8_swiglu_bwd_quantize(self.dH, self.a_pre, self.gofs, E, self.dA, False, self.dAq, self.dAs,
+                                      self.dAqT, self.dAsT, err)
         # dX_perm = dA W1^T
         self._gemm(ops.MOE_GEMM_DGRAD, self.dAq, self.dAs, self.W1d, self.W1d_s, ops.MOE_B_GNK,
                    self.gofs, E, M, d, 2 * f, ops.MOE_EPI_NONE, None, self.dx_perm, None, err)

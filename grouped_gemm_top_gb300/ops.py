@@ -32,7 +32,7 @@ MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_QUANT_ROWWISE, MOE_QUANT_COLWISE_GROUPED, MOE_QUANT_COLWISE_GLU = 0, 1, 2
 MOE_QUANT_COLWISE_BATCHED, MOE_QUANT_COLWISE_BATCHED_GLU = 3, 4
 MOE_GEMM_FWD, MOE_GEMM_DGRAD, MOE_GEMM_WGRAD = 0, 1, 2
-MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD = 0, 1, 2
+MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD, MOE_EPI_NONE_F32 = 0, 1, 2, 3
 MOE_B_GNK, MOE_B_NGK = 0, 1
 
 EXPORTS = [
@@ -40,7 +40,7 @@ EXPORTS = [
     "moe_route_workspace_size", "moe_permute_workspace_size", "moe_route_topk",
     "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
     "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_route_topk_noalloc",
-    "mxfp8_gather_quantize", "grouped_gemm_mxfp8_swiglu_quant",
+    "mxfp8_gather_quantize", "grouped_gemm_mxfp8_swiglu_quant", "mxfp8_swiglu_bwd_quantize",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -57,6 +57,7 @@ _SIGS = {
     "mxfp8_group_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
     "mxfp8_gather_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp,
                                      _vp]),
+    "mxfp8_swiglu_bwd_quantize": (_i32, [_vp, _vp, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "grouped_gemm_mxfp8_swiglu_quant": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _vp, _vp, _vp,
                                                _vp, _vp, _vp, _vp, _vp]),
     "grouped_gemm_mxfp8": (_i32, [_i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _i32, _vp, _vp,
@@ -221,6 +222,8 @@ def grouped_gemm_mxfp8(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilo
             d = _empty((G, M, N), torch.bfloat16, a)
         elif epilogue == MOE_EPI_SWIGLU_BWD:
             d = _empty((M, 2 * N), torch.bfloat16, a)
+        elif epilogue == MOE_EPI_NONE_F32:
+            d = _empty((M, N), torch.float32, a)
         else:
             d = _empty((M, N), torch.bfloat16, a)
     if epilogue == MOE_EPI_SWIGLU and d2 is None:
@@ -229,6 +232,25 @@ def grouped_gemm_mxfp8(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilo
                                                         _p(gofs), int(G), int(M), int(N), int(K), int(epilogue),
                                                         _p(epi_aux), _p(d), _p(d2), _p(err), _stream(stream)))
     return (d, d2) if epilogue == MOE_EPI_SWIGLU else d
+
+
+def mxfp8_swiglu_bwd_quantize(dH, a_pre, gofs, G, dA=None, want_dA=False, codes_row=None, scales_row=None,
+                              codes_col=None, scales_col=None, err=None, stream=None):
+    """MXFP8 (both axes) of dA = SwiGLU-backward(a_pre, dH); dA itself in bf16
+    only if want_dA or dA is given.  See include/moe.h.  Returns (dA or None,
+    codes_row, scales_row, codes_col, scales_col)."""
+    rows, f = dH.shape
+    if dA is None and want_dA:
+        dA = _empty((rows, 2 * f), torch.bfloat16, dH)
+    codes_row = codes_row if codes_row is not None else _empty((rows, 2 * f), torch.uint8, dH)
+    scales_row = scales_row if scales_row is not None else _empty((sf_bytes(rows, 2 * f),), torch.uint8, dH)
+    codes_col = codes_col if codes_col is not None else _empty((2 * f, rows), torch.uint8, dH)
+    scales_col = scales_col if scales_col is not None else _empty((sf_bytes(rows, 2 * f),), torch.uint8, dH)
+    _check("mxfp8_swiglu_bwd_quantize",
+           lib.mxfp8_swiglu_bwd_quantize(_p(dH), _p(a_pre), int(f), _p(gofs), int(G), int(rows), _p(dA),
+                                         _p(codes_row), _p(scales_row), _p(codes_col), _p(scales_col), _p(err),
+                                         _stream(stream)))
+    return dA, codes_row, scales_row, codes_col, scales_col
 
 
 def grouped_gemm_mxfp8_swiglu_quant(a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, a_pre=None, h=None, want_h=False,

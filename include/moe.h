@@ -102,7 +102,7 @@ typedef enum {
     MOE_QUANT_COLWISE_BATCHED_GLU = 4
 } moe_quant_axis_t;
 typedef enum { MOE_GEMM_FWD = 0, MOE_GEMM_DGRAD = 1, MOE_GEMM_WGRAD = 2 } moe_gemm_mode_t;
-typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1, MOE_EPI_SWIGLU_BWD = 2 } moe_epilogue_t;
+typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1, MOE_EPI_SWIGLU_BWD = 2, MOE_EPI_NONE_F32 = 3 } moe_epilogue_t;
 typedef enum {
     MOE_B_GNK = 0,  /* codes [G][N][K]: rowwise-quantized (scales: atom layout of
                        the [G*N, K] matrix)                                    */
@@ -237,6 +237,26 @@ MOE_API moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, in
                                    uint8_t* scales_col, int32_t* err, void* stream);
 
 /*
+ * mxfp8_swiglu_bwd_quantize -- the SwiGLU backward fused with the two-axis
+ * MXFP8 quantization of its result ([TE-JAX] "What specialized
+ * optimizations...": group-aware MXFP8 quantization; Figure 3's grouped MLP
+ * run backward).  dA = [dgate | dup] [rows, 2f] with, per element,
+ *   s = sigmoid(g), dgate = dH*u*s*(1 + g*(1 - s)), dup = dH*g*s
+ * where [g | u] = a_pre, computed in fp32 and rounded to bf16; dA is then
+ * quantized exactly as mxfp8_gather_quantize quantizes a stored [rows, 2f]
+ * bf16 matrix (both axes, group-aware columnwise blocks).
+ *   dH        [rows, f] fp32 (grouped_gemm_mxfp8 DGRAD with MOE_EPI_NONE_F32).
+ *   a_pre     [rows, 2f] bf16 (the up/gate GEMM's result).
+ *   dA        [rows, 2f] bf16 or NULL: the bf16 values, written only if given.
+ *   gofs      as for mxfp8_gather_quantize; rows >= gofs[G] untouched.
+ *   codes_row, scales_row, codes_col, scales_col   both axes, required.
+ * f % 128 == 0, rows % 128 == 0, 16-byte aligned pointers.
+ */
+MOE_API moe_status_t mxfp8_swiglu_bwd_quantize(const float* dH, const void* a_pre, int f, const int32_t* gofs,
+                                       int G, int64_t rows, void* dA, uint8_t* codes_row, uint8_t* scales_row,
+                                       uint8_t* codes_col, uint8_t* scales_col, int32_t* err, void* stream);
+
+/*
  * grouped_gemm_mxfp8 -- one launch for all experts' GEMMs, each over its own
  * rows only ([TE-JAX] "Optimization 1: Grouped GEMM"), MXFP8 block-scaled
  * operands, fp32 accumulation, bf16 output.  Group offsets are read on the
@@ -263,6 +283,9 @@ MOE_API moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, in
  *                                 [M, 2N] bf16 = [dgate | dup] with
  *                                 dgate = dH*u*s*(1+g*(1-s)), dup = dH*g*s,
  *                                 s = sigmoid(g).
+ *             MOE_EPI_NONE_F32:   d = D [M, N] fp32 (the accumulators as
+ *                                 they are; e.g. dH for
+ *                                 mxfp8_swiglu_bwd_quantize).
  *             N % 128 == 0 for every epilogue.
  * MOE_GEMM_WGRAD:
  *   a, a_sf   [M, K] columnwise codes (the transposed left operand, e.g.

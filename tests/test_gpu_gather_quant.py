@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import atoms_rows_subset, atoms_to_rowmajor, gpu_ops, padded_layout, to_np
+from helpers import assert_bf16_close, atoms_rows_subset, atoms_to_rowmajor, gpu_ops, padded_layout, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -194,3 +194,53 @@ def test_row_id_beyond_src_is_reported(ops):
     ref_rid = row_id.copy()
     ref_rid[bad] = -1
     _check_axes(ops, O.permute(to_np(x), ref_rid, k), gofs, rows, d, res)
+
+
+@pytest.mark.parametrize("sizes,f", [([128], 128), ([5, 0, 130, 127, 1], 256), ([1000, 0, 300], 2048)])
+def test_swiglu_bwd_quantize(ops, sizes, f):
+    """dA = SwiGLU-backward(a_pre, dH) in bf16 against the oracle, its codes
+    on both axes bit-exact against the oracle's quantization of that bf16
+    dA; the same codes without dA written; rows beyond the groups neither
+    read (NaN there) nor written."""
+    gofs = padded_layout(sizes)
+    Rp = int(gofs[-1])
+    rows = Rp + 256
+    g = torch.Generator(device="cuda")
+    g.manual_seed(f + len(sizes))
+    dH = torch.randn((rows, f), generator=g, device="cuda") * 3.0
+    a_pre = (torch.randn((rows, 2 * f), generator=g, device="cuda") * 2.0).to(torch.bfloat16)
+    dH[Rp:] = float("nan")
+    a_pre[Rp:] = float("nan")
+    gt = _dev(gofs, torch.int32)
+    cr = torch.full((rows, 2 * f), 0xAB, dtype=torch.uint8, device="cuda")
+    cc = torch.full((2 * f, rows), 0xAB, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dA, cr, sr, cc, sc = ops.mxfp8_swiglu_bwd_quantize(dH, a_pre, gt, len(sizes), want_dA=True, codes_row=cr,
+                                                       codes_col=cc, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = O.swiglu_bwd(to_np(a_pre)[:Rp], dH[:Rp].double().cpu().numpy())
+    assert_bf16_close(dA[:Rp], ref, what="dA")
+    _check_axes(ops, to_np(dA)[:Rp], gofs, rows, 2 * f, (cr, sr, cc, sc))
+    assert torch.all(cr[Rp:] == 0xAB) and torch.all(cc[:, Rp:] == 0xAB)
+    _, cr2, sr2, cc2, sc2 = ops.mxfp8_swiglu_bwd_quantize(dH, a_pre, gt, len(sizes))
+    torch.cuda.synchronize()
+    assert torch.equal(cr2[:Rp], cr[:Rp]) and torch.equal(cc2[:, :Rp], cc[:, :Rp])
+    assert np.array_equal(atoms_rows_subset(sr2.cpu().numpy(), rows, 2 * f, np.arange(Rp)),
+                          atoms_rows_subset(sr.cpu().numpy(), rows, 2 * f, np.arange(Rp)))
+    assert np.array_equal(atoms_to_rowmajor(sc2.cpu().numpy(), 2 * f, rows)[:, :Rp // 32],
+                          atoms_to_rowmajor(sc.cpu().numpy(), 2 * f, rows)[:, :Rp // 32])
+
+
+def test_swiglu_bwd_quantize_rejects_bad_offsets(ops):
+    f, rows = 128, 256
+    dH = torch.zeros((rows, f), device="cuda")
+    a_pre = torch.zeros((rows, 2 * f), dtype=torch.bfloat16, device="cuda")
+    cr = torch.full((rows, 2 * f), 0xAB, dtype=torch.uint8, device="cuda")
+    for bad in ([0, 100, 256], [0, 256, 128], [0, 128, 384], [64, 128, 256]):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ops.mxfp8_swiglu_bwd_quantize(dH, a_pre, _dev(np.array(bad), torch.int32), 2, codes_row=cr, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == ops.MOE_ERR_BAD_OFFSETS
+        assert torch.all(cr == 0xAB)
+

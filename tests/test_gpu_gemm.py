@@ -6,8 +6,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (assert_bf16_close, atoms_rows_subset, atoms_to_rowmajor, batched_weight_operand, glu_perm,
-                     gpu_ops, padded_layout, to_np)
+from helpers import (assert_bf16_close, assert_fp32_close, atoms_rows_subset, atoms_to_rowmajor,
+                     batched_weight_operand, glu_perm, gpu_ops, padded_layout, to_np)
 from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -201,6 +201,27 @@ def test_swiglu_bwd_epilogue(ops, sizes, K, f):
     dH = O.grouped_gemm(A, B, gofs)[:Rp]
     ref = O.swiglu_bwd(to_np(a_pre)[:Rp], dH)
     assert_bf16_close(dA[:Rp], ref, what="dA")
+
+
+@pytest.mark.parametrize("sizes,K,N", [([140, 260], 512, 256), ([300, 0, 5], 256, 384), ([129], 1024, 2048)])
+def test_dgrad_fp32_out(ops, sizes, K, N):
+    """MOE_EPI_NONE_F32: the fp32 accumulators as they are (dH for the fused
+    SwiGLU backward); rows beyond the groups untouched."""
+    G = len(sizes)
+    dy, gofs_t, gofs = _act(sizes, K, seed=45)
+    M = dy.shape[0]
+    dq, ds, A = _quant_rows(ops, dy)
+    W = synth.make_normal_bf16((G * N, K), 46, "cuda", std=0.5)
+    wq, ws_ = ops.mxfp8_group_quantize(W, ops.MOE_QUANT_ROWWISE)
+    Wd = O.mxfp8_dequantize_rows(wq.cpu().numpy(), atoms_to_rowmajor(ws_.cpu().numpy(), G * N, K))
+    B = np.transpose(Wd.reshape(G, N, K), (0, 2, 1))
+    d = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    ops.grouped_gemm_mxfp8(ops.MOE_GEMM_DGRAD, dq, ds, wq, ws_, ops.MOE_B_GNK, gofs_t, G, M, N, K,
+                           ops.MOE_EPI_NONE_F32, d=d)
+    torch.cuda.synchronize()
+    Rp = int(gofs[-1])
+    assert_fp32_close(d[:Rp], O.grouped_gemm(A, B, gofs)[:Rp], what="dH fp32")
+    assert torch.isnan(d[Rp:]).all()
 
 
 @pytest.mark.parametrize("sizes,Mo,No", [([128, 0, 384], 256, 256), ([5, 130, 0, 64], 128, 512),

@@ -19,7 +19,7 @@ def ops():
 
 def _layer(ops, T, d, E, k, f, score, norm, zipf=None, seed_offset=0):
     from grouped_gemm_top_gb300.layer import MoELayer
-    L = MoELayer(T, d, E, k, f, score, norm, store_h=True)
+    L = MoELayer(T, d, E, k, f, score, norm, store_intermediates=True)
     inp = synth.make_layer_inputs(T, d, E, f, "cuda", zipf_s=zipf, seed_offset=seed_offset)
     L.set_weights(inp["W1"], inp["W2"])
     L.logits.copy_(inp["logits"])
@@ -110,6 +110,7 @@ def test_tiny_layer_stagewise(ops, score, norm):
     assert np.array_equal(L.dyqT.cpu().numpy()[:, :Rp], dcq)
     assert np.array_equal(atoms_to_rowmajor(L.dysT.cpu().numpy(), d, M)[:, :Rp // 32], dcs)
     dH = O.grouped_gemm(O.mxfp8_dequantize_rows(dq, ds), _w_dgrad(L, 2), gofs)
+    assert_fp32_close(L.dH[:Rp], dH[:Rp], what="dH")
     dA = O.swiglu_bwd(to_np(L.a_pre)[:Rp], dH)
     assert_bf16_close(L.dA[:Rp], dA, what="dA")
     # wgrad dW2 = h^T dy per group (columnwise operands)
@@ -229,6 +230,7 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     assert_bf16_close(L.a_pre[rt], a_pre, what="a_pre rows")
     assert_bf16_close(L.h[rt], O.swiglu(a_pre), what="h rows")
     assert_bf16_close(L.y_perm[rt], y, what="y_perm rows")
+    assert_fp32_close(L.dH[rt], dH, what="dH rows")
     assert_bf16_close(L.dA[rt], O.swiglu_bwd(to_np(L.a_pre[rt]), dH), what="dA rows")
     assert_bf16_close(L.dx_perm[rt], dxp, what="dx_perm rows")
     # combine + combine bwd on sampled tokens
