@@ -537,18 +537,31 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
 
     const int tc = tid & 15, tr = tid >> 4;
     const int lane = tid & 31, warp = tid >> 5;
+    // raw inputs of one chunk: 8 dH (fp32), 8 g and 8 u (bf16) of row
+    // r0 + tr + 16p, columns c0 + tc*8 ...
+    auto load = [&](int64_t r0, int p, float4& h0, float4& h1, uint4& gw, uint4& uw) {
+        const int64_t r = r0 + tr + 16 * p;
+        const float4* hp = reinterpret_cast<const float4*>(dH + r * F + c0 + tc * 8);
+        h0 = __ldg(hp);
+        h1 = __ldg(hp + 1);
+        gw = __ldg(reinterpret_cast<const uint4*>(a_pre + r * F2 + c0 + tc * 8));
+        uw = __ldg(reinterpret_cast<const uint4*>(a_pre + r * F2 + F + c0 + tc * 8));
+    };
+    float4 h0, h1;
+    uint4 gw, uw;
     for (int i = 0; i < nrt; ++i) {
         const int64_t r0 = (rt0 + i) * kQT;
         // dgate / dup of this thread's chunks: rowwise codes from registers,
-        // bf16 values into the two tiles
-#pragma unroll 2
+        // bf16 values into the two tiles; chunk p + 1's loads are in flight
+        // while chunk p is computed
+        if (i == 0) load(r0, 0, h0, h1, gw, uw);     // later tiles: prefetched by the previous one
+#pragma unroll
         for (int p = 0; p < 8; ++p) {
             const int rl = tr + 16 * p;
             const int64_t r = r0 + rl;
-            const float4* hp = reinterpret_cast<const float4*>(dH + r * F + c0 + tc * 8);
-            const float4 h0 = __ldg(hp), h1 = __ldg(hp + 1);
-            const uint4 gw = __ldg(reinterpret_cast<const uint4*>(a_pre + r * F2 + c0 + tc * 8));
-            const uint4 uw = __ldg(reinterpret_cast<const uint4*>(a_pre + r * F2 + F + c0 + tc * 8));
+            float4 nh0, nh1;
+            uint4 ngw, nuw;
+            if (p + 1 < 8) load(r0, p + 1, nh0, nh1, ngw, nuw);
             float gf[8], uf[8], dg[8], du[8];
             const float hf[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
             unpack8(gw, gf);
@@ -572,7 +585,16 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
             }
             *reinterpret_cast<uint4*>(tiles + rl * kQT + tc * 8) = vg;
             *reinterpret_cast<uint4*>(tiles + kQT * kQT + rl * kQT + tc * 8) = vu;
+            if (p + 1 < 8) {
+                h0 = nh0;
+                h1 = nh1;
+                gw = ngw;
+                uw = nuw;
+            }
         }
+        // the next tile's first chunk is loaded while this tile's columnwise
+        // blocks are quantized and stored
+        if (i + 1 < nrt) load(r0 + kQT, 0, h0, h1, gw, uw);
         __syncthreads();                      // A: both tiles complete
         const int blk = warp & 3;
         const int col = (warp >> 2) * 64 + 2 * lane;
