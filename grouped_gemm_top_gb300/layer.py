@@ -203,6 +203,71 @@ class MoELayer:
                 outs.append(host_t)
         return tuple(outs)
 
+    # ------------------------------------------- pipelined host stepping ----
+    _IO = ("x", "logits", "dout", "out", "dx", "dlogits")
+
+    def enable_pipelining(self, warmup=1):
+        """Second set of input/output buffers and one CUDA graph per set, so
+        that run_pipelined() can copy step i+1's inputs in and step i-1's
+        outputs out while step i computes."""
+        if getattr(self, "_sets", None) is not None:
+            return
+        first = {n: getattr(self, n) for n in self._IO}
+        second = {n: torch.zeros_like(t) for n, t in first.items()}
+        graphs = []
+        for bufs in (first, second):
+            for n, t in bufs.items():
+                setattr(self, n, t)
+            self.graph = None
+            graphs.append(self.capture(warmup))
+        for n, t in first.items():
+            setattr(self, n, t)
+        self.graph = graphs[0]
+        self._sets = (first, second)
+        self._graphs = graphs
+        self._h2d_stream = torch.cuda.Stream(device=self.device)
+        self._d2h_stream = torch.cuda.Stream(device=self.device)
+
+    def run_pipelined(self, batches):
+        """Run one fwd+bwd step per element of `batches`, each a tuple
+        (x, logits, dout, out_host, dx_host, dlogits_host) of host tensors
+        (pinned, for asynchronous copies).  Step i uses buffer set i % 2: its
+        inputs are copied in on an input-copy stream (once step i-2's outputs
+        have left that set), the step's graph runs on the current stream, and
+        its outputs are copied out on an output-copy stream while step i+1
+        computes (the GPU's copy engines run both directions beside the
+        kernels).  Returns with the current stream ordered after the last
+        copy.  The weight gradients and the error word are those of the last
+        step."""
+        self.enable_pipelining()
+        comp = torch.cuda.current_stream(self.device)
+        h2d, d2h = self._h2d_stream, self._d2h_stream
+        free = [None, None]          # events: the set's outputs have been copied out
+        for i, (x, logits, dout, out_h, dx_h, dl_h) in enumerate(batches):
+            b = i % 2
+            bufs = self._sets[b]
+            with torch.cuda.stream(h2d):
+                if free[b] is not None:
+                    h2d.wait_event(free[b])
+                bufs["x"].copy_(x, non_blocking=True)
+                bufs["logits"].copy_(logits, non_blocking=True)
+                bufs["dout"].copy_(dout, non_blocking=True)
+                loaded = torch.cuda.Event()
+                loaded.record(h2d)
+            comp.wait_event(loaded)
+            self._graphs[b].replay()
+            done = torch.cuda.Event()
+            done.record(comp)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(done)
+                out_h.copy_(bufs["out"], non_blocking=True)
+                dx_h.copy_(bufs["dx"], non_blocking=True)
+                dl_h.copy_(bufs["dlogits"], non_blocking=True)
+                free[b] = torch.cuda.Event()
+                free[b].record(d2h)
+        comp.wait_stream(h2d)
+        comp.wait_stream(d2h)
+
     def check_err(self):
         v = int(self.err.item())
         if v != 0:

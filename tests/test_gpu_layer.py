@@ -158,6 +158,30 @@ def test_graph_replay_matches_eager(ops):
         assert torch.equal(a, b)
 
 
+def test_pipelined_steps_match_single_steps(ops):
+    """run_pipelined (double-buffered inputs/outputs, copies overlapping the
+    previous and next steps) returns for every step exactly what step()
+    returns for that batch alone."""
+    T, d, E, k, f = 256, 512, 8, 2, 256
+    L, inp = _layer(ops, T, d, E, k, f, "softmax", True)
+    batches, refs = [], []
+    for i in range(3):
+        x = synth.make_normal_bf16((T, d), 100 + i, "cuda").cpu().pin_memory()
+        logits = synth.make_logits(T, E, 200 + i, "cuda").cpu().pin_memory()
+        dout = synth.make_normal_bf16((T, d), 300 + i, "cuda").cpu().pin_memory()
+        refs.append(tuple(t.clone() for t in L.step(x, logits, dout)))
+        outs = (torch.empty((T, d), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((T, d), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((T, E), dtype=torch.float32).pin_memory())
+        batches.append((x, logits, dout) + outs)
+    L.run_pipelined(batches)
+    torch.cuda.synchronize()
+    L.check_err()
+    for b, ref in zip(batches, refs):
+        for got, want in zip(b[3:], ref):
+            assert torch.equal(got, want)
+
+
 def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     """Large workloads: exact routing/permute, sampled GEMM rows and
     sampled wgrad entries (each over its full contraction)."""
