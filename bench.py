@@ -183,11 +183,7 @@ def run_gpu(args, rank, world, local_rank):
         gemm_ms[i % GEMMS_PER_STEP] += s.elapsed_time(e)
     gemm_ms = [x / args.steps for x in gemm_ms]
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     ms_per_step = elapsed_ms / args.steps
 
     # ---- CUDA-graph replay of the same step (the whole step in one graph)
@@ -202,7 +198,7 @@ def run_gpu(args, rank, world, local_rank):
     g1.record(stream)
     torch.cuda.synchronize()
     L.check_err()
-    graph_ms = g0.elapsed_time(g1) / args.steps
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / args.steps
 
     # ---- end to end through the public API from pinned host buffers
     h_x = inp["x"].cpu().pin_memory()
@@ -223,7 +219,7 @@ def run_gpu(args, rank, world, local_rank):
     L.run_pipelined([batch] * args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
     h2d = h_x.numel() * 2 + h_l.numel() * 4 + h_d.numel() * 2
     d2h = h_out.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
 
@@ -244,7 +240,7 @@ def run_gpu(args, rank, world, local_rank):
     achieved = sum(gemm_flops) / (sum_gemm_ms * 1e-3) / 1e12
     per_launch = {n: {"ms": round(t, 4), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
                   for n, t, fl in zip(gemm_names, gemm_ms, gemm_flops)}
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms_per_step)
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -275,7 +271,7 @@ def run_gpu(args, rank, world, local_rank):
                                  round(sum(t["dram_read"] + t["dram_write"] for t in traffic) / len(traffic))),
                      "traffic_unit": "bytes per launch (DRAM read+write, ncu, mean of the step's 6 launches)",
                      "algorithmic_bytes_per_launch": round(algo_bytes / GEMMS_PER_STEP)},
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+        "e2e": {"value": round(job_tflops(flops, world, e2e_ms), 2), "unit": "TFLOPS",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk.summary(),
@@ -441,6 +437,24 @@ def run_reference(args):
                          "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time (every rank calls this): replicas run the same
+    step, and the job's step time is that of the slowest one."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step, world, ms_per_step):
+    """Whole-job throughput: every replica runs one step of flops_per_step in
+    the (slowest rank's) ms_per_step (weak scaling)."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
 
 
 def run_hbm_probe(nbytes=4 << 30, reps=10):
