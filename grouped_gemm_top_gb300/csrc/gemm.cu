@@ -81,7 +81,7 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
         ti.a_row = row;
         ti.out_row = row;
         ti.kbeg = 0;
-        ti.nk = (int)(p.K / BK);
+        ti.nk = (int)((p.K + (p.k_ceil ? BK - 1 : 0)) / BK);
     } else {
         const int64_t tpg = (int64_t)p.m_tiles * p.n_tiles;
         const int g = (int)(t / tpg);
@@ -99,8 +99,10 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
 // --------------------------------------------------------------- kernel ----
 
 // EPI: the epilogue (moe_epilogue_t), fixed at compile time so each
-// instance keeps only its own epilogue's registers.
-template <int BN, int EPI>
+// instance keeps only its own epilogue's registers.  BF16: plain bf16
+// operands (tcgen05.mma kind::f16, no scale factors; 64 elements per
+// 128-byte k-step), for the router's dense GEMMs.
+template <int BN, int EPI, bool BF16 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
     using C = Cfg<BN>;
@@ -134,7 +136,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         *abort_flag = 0;
         *bad_flag = 0;
     }
-    for (int i = threadIdx.x; i <= p.G; i += THREADS) s_gofs[i] = p.gofs[i];
+    if (p.gofs != nullptr) {
+        for (int i = threadIdx.x; i <= p.G; i += THREADS) s_gofs[i] = p.gofs[i];
+    } else if (threadIdx.x == 0) {      // dense: one group of all M rows
+        s_gofs[0] = 0;
+        s_gofs[1] = (int)p.M;
+    }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS));
@@ -186,17 +193,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t kg = ti.kbeg + ks;
                 const int kx = (int)(kg * BK);
                 const uint32_t fb = full_bar(stage);
-                mbar_expect_tx(fb, C::STAGE_TX);
+                mbar_expect_tx(fb, BF16 ? (uint32_t)(C::A_STAGE + C::B_STAGE) : C::STAGE_TX);
                 tma_load_2d(smem_u32(sA + stage * C::A_STAGE), &tmA, kx, (int)ti.a_row, fb);
                 const uint8_t* sfa = p.a_sf + kg * p.a_sf_kstride + (ti.a_row / 128) * 512;
                 const uint8_t* sfb = p.b_sf + (int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride;
-                bulk_load(smem_u32(sSFA + stage * SFA_STAGE), sfa, 512, fb);
+                if constexpr (!BF16) bulk_load(smem_u32(sSFA + stage * SFA_STAGE), sfa, 512, fb);
 #pragma unroll
                 for (int h = 0; h < BN / 128; ++h) {
                     const int brow = ti.b_row + 128 * h;
                     tma_load_3d(smem_u32(sB + stage * C::B_STAGE + h * 16384), &tmB, kx, brow, gB, fb);
-                    bulk_load(smem_u32(sSFB + stage * C::SFB_STAGE + h * 512), sfb + (int64_t)(brow / 128) * 512,
-                              512, fb);
+                    if constexpr (!BF16)
+                        bulk_load(smem_u32(sSFB + stage * C::SFB_STAGE + h * 512), sfb + (int64_t)(brow / 128) * 512,
+                                  512, fb);
                 }
                 pend[stage] = (int)phase;
                 if (++stage == STAGES) {
@@ -241,17 +249,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t t_sfa = tmem_base + C::SF0 + TMEM_SF_STRIDE * stage;
                 const uint32_t t_sfb = t_sfa + 4;
-                tc_cp_sf(t_sfa, desc_sf(smem_u32(sSFA + stage * SFA_STAGE)));
+                if constexpr (!BF16) {
+                    tc_cp_sf(t_sfa, desc_sf(smem_u32(sSFA + stage * SFA_STAGE)));
 #pragma unroll
-                for (int h = 0; h < BN / 128; ++h)
-                    tc_cp_sf(t_sfb + 4 * h, desc_sf(smem_u32(sSFB + stage * C::SFB_STAGE + 512 * h)));
+                    for (int h = 0; h < BN / 128; ++h)
+                        tc_cp_sf(t_sfb + 4 * h, desc_sf(smem_u32(sSFB + stage * C::SFB_STAGE + 512 * h)));
+                }
                 const uint64_t adesc = desc_sw128(smem_u32(sA + stage * C::A_STAGE));
                 const uint64_t bdesc = desc_sw128(smem_u32(sB + stage * C::B_STAGE));
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk) {
                     // advance 32 bytes along K inside the 128-byte swizzled row
-                    tc_mma(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
-                           make_idesc<BN>((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
+                    // (32 fp8 elements with block scales, or 16 bf16)
+                    if constexpr (BF16)
+                        tc_mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                                    make_idesc_bf16<BN>(), (ks | kk) != 0 ? 1u : 0u);
+                    else
+                        tc_mma(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                               make_idesc<BN>((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
                 }
                 issued = true;
                 tc_commit(empty_bar(stage));
@@ -358,7 +373,10 @@ cudaError_t gemm_set_attributes() {
     const cudaError_t es[] = {set_attr_1sm<128, MOE_EPI_NONE>(),     set_attr_1sm<128, MOE_EPI_SWIGLU>(),
                               set_attr_1sm<128, MOE_EPI_SWIGLU_BWD>(), set_attr_1sm<128, MOE_EPI_NONE_F32>(),
                               set_attr_1sm<256, MOE_EPI_NONE>(),     set_attr_1sm<256, MOE_EPI_SWIGLU>(),
-                              set_attr_1sm<256, MOE_EPI_SWIGLU_BWD>(), set_attr_1sm<256, MOE_EPI_NONE_F32>()};
+                              set_attr_1sm<256, MOE_EPI_SWIGLU_BWD>(), set_attr_1sm<256, MOE_EPI_NONE_F32>(),
+                              cudaFuncSetAttribute(gg::k_grouped_gemm<256, MOE_EPI_NONE_F32, true>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   gg::Cfg<256>::SMEM_BYTES)};
     for (cudaError_t e : es)
         if (e != cudaSuccess) return e;
     return gemm_set_attributes_2sm();
@@ -512,6 +530,9 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     p.b_sf = b_sf;
     p.d = (__nv_bfloat16*)d;
     p.d2 = (__nv_bfloat16*)d2;
+    p.n_out = N;
+    p.ldd = N;
+    p.k_ceil = 0;
     p.hq_r = hq.codes_row;
     p.hs_r = hq.scales_row;
     p.hq_c = hq.codes_col;
@@ -630,4 +651,47 @@ extern "C" moe_status_t grouped_gemm_mxfp8_swiglu_quant(const uint8_t* a, const 
     const HQuantOut hq = {h_codes_row, h_scales_row, h_codes_col, h_scales_col};
     return gemm_run(MOE_GEMM_FWD, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, MOE_EPI_SWIGLU, nullptr, a_pre, h, hq,
                     err, stream);
+}
+
+extern "C" moe_status_t gemm_bf16_nt(const void* a, const void* b, int64_t M, int N, int64_t K, float* d,
+                                     int32_t* err, void* stream) {
+    using namespace gg;
+    MOE_REQUIRE(a && b && d && M > 0 && N > 0 && K > 0, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(M % 128 == 0 && M <= 0x7FFFFF80LL && N % 8 == 0 && K % 8 == 0 && K <= (1LL << 30),
+                MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(moe_aligned16(a) && moe_aligned16(b) && (reinterpret_cast<uintptr_t>(d) & 31) == 0,
+                MOE_ERR_ALIGNMENT);
+    MOE_REQUIRE(device_initialized() && g_encode != nullptr, MOE_ERR_NOT_INITIALIZED);
+    // bf16 rows seen as bytes: K-steps of 128 bytes = 64 elements; columns of
+    // B past N (and bytes past 2K) are zero-filled by the TMA
+    const int64_t Kb = 2 * K;
+    const int Npad = (N + 255) / 256 * 256;
+    CUtensorMap tmA, tmB;
+    const uint64_t da[2] = {(uint64_t)Kb, (uint64_t)M}, sa[1] = {(uint64_t)Kb};
+    const uint64_t db[3] = {(uint64_t)Kb, (uint64_t)N, 1}, sb[2] = {(uint64_t)Kb, (uint64_t)Kb * N};
+    MOE_REQUIRE(make_map(&tmA, a, 2, da, sa) && make_map(&tmB, b, 3, db, sb), MOE_ERR_CUDA);
+    Params p{};
+    p.mode = MOE_GEMM_FWD;
+    p.epi = MOE_EPI_NONE_F32;
+    p.G = 1;
+    p.N = Npad;
+    p.M = M;
+    p.K = Kb;
+    p.gofs = nullptr;
+    p.d = (__nv_bfloat16*)d;
+    p.err = err;
+    p.timeout_ns = 2000000000ull;
+    p.band = 8;
+    p.n_tiles = Npad / 256;
+    p.n_out = N;
+    p.ldd = N;
+    p.k_ceil = 1;
+    const int sms = device_sm_count();
+    MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
+    const int64_t tiles = (M / BM) * p.n_tiles;
+    const int grid = (int)std::min<int64_t>(tiles, sms);
+    k_grouped_gemm<256, MOE_EPI_NONE_F32, true><<<grid, THREADS, Cfg<256>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB,
+                                                                                                          p);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
 }

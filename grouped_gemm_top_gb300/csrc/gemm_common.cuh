@@ -36,6 +36,11 @@ struct Params {
     uint64_t timeout_ns;
     int band;           // m-tiles per raster band (consecutive tiles share the B tile)
     int tma_store;      // pair kernel, BN = 256, MOE_EPI_NONE: write D through the TMA (tensor map tmD)
+    // bf16 operands (kind::f16): the columns of D that exist (n_out <= N,
+    // the rest of the tile is not stored) and D's row stride in elements
+    int n_out;
+    int64_t ldd;
+    int k_ceil;         // bf16 operands: the last k-step may reach past K (TMA fills zeros)
     // MOE_EPI_SWIGLU: MXFP8 of h (NULL = not produced): rowwise codes
     // [M, N/2] + scale atoms, columnwise (transposed) codes [N/2, M] + atoms
     uint8_t* hq_r;
@@ -167,6 +172,22 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
 template <int BN>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
     return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16 with bf16 A and B, fp32
+// D, both K-major, M = 128, N = BN.
+template <int BN>
+__device__ __forceinline__ uint32_t make_idesc_bf16() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
@@ -360,16 +381,18 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
             store_row32(p.d + row * ld + N + col, du);
         }
     } else if constexpr (EPI == MOE_EPI_NONE_F32) {
-        float* out = reinterpret_cast<float*>(p.d) + row * p.N + (int64_t)nt * BN;
+        float* out = reinterpret_cast<float*>(p.d) + row * p.ldd + (int64_t)nt * BN;
         for (int c = 0; c < BN / 64; ++c) {
             const int col32 = half * (BN / 2) + 32 * c;
             tmem_ld32(tacc + col32, v);
             uint32_t* o = reinterpret_cast<uint32_t*>(out + col32);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                st_global_v8(o + 8 * q, __float_as_uint(v[8 * q]), __float_as_uint(v[8 * q + 1]),
-                             __float_as_uint(v[8 * q + 2]), __float_as_uint(v[8 * q + 3]), __float_as_uint(v[8 * q + 4]),
-                             __float_as_uint(v[8 * q + 5]), __float_as_uint(v[8 * q + 6]), __float_as_uint(v[8 * q + 7]));
+                if (nt * BN + col32 + 8 * q < p.n_out)
+                    st_global_v8(o + 8 * q, __float_as_uint(v[8 * q]), __float_as_uint(v[8 * q + 1]),
+                                 __float_as_uint(v[8 * q + 2]), __float_as_uint(v[8 * q + 3]),
+                                 __float_as_uint(v[8 * q + 4]), __float_as_uint(v[8 * q + 5]),
+                                 __float_as_uint(v[8 * q + 6]), __float_as_uint(v[8 * q + 7]));
         }
     } else {
         for (int c = 0; c < BN / 64; ++c) {
@@ -444,9 +467,10 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
             h_quant_chunk(p, row, hcol + 32, ph, lane);
         }
     } else if constexpr (EPI == MOE_EPI_NONE_F32) {
-        // fp32 out: each 32-column chunk is stored as it is drained
-        uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<float*>(p.d) + row * p.N + (int64_t)nt * 256 +
-                                                    128 * half);
+        // fp32 out: each 32-column chunk is stored as it is drained; only
+        // columns < n_out exist (row stride ldd), in 8-column groups
+        const int col0 = nt * 256 + 128 * half;
+        uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<float*>(p.d) + row * p.ldd + col0);
 #pragma unroll
         for (int c = 0; c < 4; c += 2) {
             tmem_ld32_issue(tacc + 128 * half + 32 * c, ra);
@@ -455,10 +479,12 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
             if (c == 2) release();
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                st_global_v8(out + 32 * c + 8 * q, ra[8 * q], ra[8 * q + 1], ra[8 * q + 2], ra[8 * q + 3], ra[8 * q + 4],
-                             ra[8 * q + 5], ra[8 * q + 6], ra[8 * q + 7]);
-                st_global_v8(out + 32 * (c + 1) + 8 * q, rb[8 * q], rb[8 * q + 1], rb[8 * q + 2], rb[8 * q + 3],
-                             rb[8 * q + 4], rb[8 * q + 5], rb[8 * q + 6], rb[8 * q + 7]);
+                if (col0 + 32 * c + 8 * q < p.n_out)
+                    st_global_v8(out + 32 * c + 8 * q, ra[8 * q], ra[8 * q + 1], ra[8 * q + 2], ra[8 * q + 3],
+                                 ra[8 * q + 4], ra[8 * q + 5], ra[8 * q + 6], ra[8 * q + 7]);
+                if (col0 + 32 * (c + 1) + 8 * q < p.n_out)
+                    st_global_v8(out + 32 * (c + 1) + 8 * q, rb[8 * q], rb[8 * q + 1], rb[8 * q + 2], rb[8 * q + 3],
+                                 rb[8 * q + 4], rb[8 * q + 5], rb[8 * q + 6], rb[8 * q + 7]);
             }
         }
     } else {

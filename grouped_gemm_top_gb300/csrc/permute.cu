@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(256) k_perm_gather(const uint4* __restrict__ x
 
 // out[t] = sum_j w[t,j] * y[slot_of[t,j]] (fp32, j order); w == NULL -> 1.
 __global__ void __launch_bounds__(128) k_combine(const uint4* __restrict__ y, const int32_t* __restrict__ slot_of,
-                                                 const float* __restrict__ w, int d8, int k, uint4* __restrict__ out) {
+                                                 const float* __restrict__ w, const float4* __restrict__ add, int d8,
+                                                 int k, uint4* __restrict__ out) {
     const int t = blockIdx.x;
     __shared__ int s_slot[32];
     __shared__ float s_w[32];
@@ -162,8 +163,14 @@ __global__ void __launch_bounds__(128) k_combine(const uint4* __restrict__ y, co
     __syncthreads();
     for (int c = threadIdx.x; c < d8; c += blockDim.x) {
         float acc[8];
+        if (add != nullptr) {           // fp32 addend first, then the k terms in j order
+            const float4 a0 = __ldg(add + ((int64_t)t * d8 + c) * 2), a1 = __ldg(add + ((int64_t)t * d8 + c) * 2 + 1);
+            acc[0] = a0.x; acc[1] = a0.y; acc[2] = a0.z; acc[3] = a0.w;
+            acc[4] = a1.x; acc[5] = a1.y; acc[6] = a1.z; acc[7] = a1.w;
+        } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        }
         for (int j0 = 0; j0 < k; j0 += 8) {
             uint4 v[8];
 #pragma unroll
@@ -327,7 +334,67 @@ extern "C" moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t*
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
     if (T == 0) return MOE_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    k_combine<<<T, 128, 0, s>>>((const uint4*)y_perm, slot_of, topk_w, d / 8, k, (uint4*)out);
+    k_combine<<<T, 128, 0, s>>>((const uint4*)y_perm, slot_of, topk_w, nullptr, d / 8, k, (uint4*)out);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_unpermute_combine_add(const void* y_perm, const int32_t* slot_of, const float* topk_w,
+                                                  const float* addend, int T, int d, int k, void* out, int32_t* err,
+                                                  void* stream) {
+    (void)err;
+    MOE_REQUIRE(T >= 0 && d > 0 && k >= 1 && k <= 32, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(T == 0 || (y_perm && slot_of && out && addend), MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(d % 8 == 0 && moe_aligned16(y_perm) && moe_aligned16(out) && moe_aligned16(addend), MOE_ERR_ALIGNMENT);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    if (T == 0) return MOE_OK;
+    k_combine<<<T, 128, 0, (cudaStream_t)stream>>>((const uint4*)y_perm, slot_of, topk_w, (const float4*)addend, d / 8,
+                                                   k, (uint4*)out);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+// dst[c][r] = bf16(src[r][c]) (src bf16 or fp32): 32 x 32 tiles through
+// shared memory, coalesced on both sides.
+template <typename Src>
+__global__ void __launch_bounds__(256) k_transpose(const Src* __restrict__ src, int64_t rows, int64_t cols,
+                                                   uint16_t* __restrict__ dst) {
+    __shared__ uint16_t tile[32][33];
+    const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        const int64_t r = r0 + ty + i, c = c0 + tx;
+        uint16_t v = 0;
+        if (r < rows && c < cols) {
+            if constexpr (sizeof(Src) == 4) {
+                __nv_bfloat16 b = __float2bfloat16_rn(src[r * cols + c]);
+                v = *reinterpret_cast<uint16_t*>(&b);
+            } else {
+                v = src[r * cols + c];
+            }
+        }
+        tile[ty + i][tx] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        const int64_t c = c0 + ty + i, r = r0 + tx;
+        if (c < cols && r < rows) dst[c * rows + r] = tile[tx][ty + i];
+    }
+}
+
+extern "C" moe_status_t moe_transpose_bf16(const void* src, int src_fp32, int64_t rows, int64_t cols, void* dst,
+                                           void* stream) {
+    MOE_REQUIRE(src && dst && rows > 0 && cols > 0, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE((rows + 31) / 32 <= 65535 && (cols + 31) / 32 <= 0x7FFFFFFF, MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
+    if (src_fp32)
+        k_transpose<float><<<grid, 256, 0, (cudaStream_t)stream>>>((const float*)src, rows, cols, (uint16_t*)dst);
+    else
+        k_transpose<uint16_t><<<grid, 256, 0, (cudaStream_t)stream>>>((const uint16_t*)src, rows, cols,
+                                                                      (uint16_t*)dst);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }

@@ -41,6 +41,7 @@ EXPORTS = [
     "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
     "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_route_topk_noalloc",
     "mxfp8_gather_quantize", "grouped_gemm_mxfp8_swiglu_quant", "mxfp8_swiglu_bwd_quantize",
+    "gemm_bf16_nt", "moe_transpose_bf16", "moe_unpermute_combine_add",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -57,6 +58,9 @@ _SIGS = {
     "mxfp8_group_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
     "mxfp8_gather_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp,
                                      _vp]),
+    "gemm_bf16_nt": (_i32, [_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp]),
+    "moe_transpose_bf16": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
+    "moe_unpermute_combine_add": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "mxfp8_swiglu_bwd_quantize": (_i32, [_vp, _vp, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "grouped_gemm_mxfp8_swiglu_quant": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _vp, _vp, _vp,
                                                _vp, _vp, _vp, _vp, _vp]),
@@ -274,6 +278,34 @@ def grouped_gemm_mxfp8_swiglu_quant(a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K
                                                _p(h_scales_row), _p(h_codes_col), _p(h_scales_col), _p(err),
                                                _stream(stream)))
     return a_pre, h, h_codes_row, h_scales_row, h_codes_col, h_scales_col
+
+
+def gemm_bf16_nt(a, b, d=None, err=None, stream=None):
+    """d [M, N] fp32 = a [M, K] @ b [N, K]^T (bf16 operands).  See include/moe.h."""
+    M, K = a.shape
+    N = b.shape[0]
+    d = d if d is not None else _empty((M, N), torch.float32, a)
+    _check("gemm_bf16_nt", lib.gemm_bf16_nt(_p(a), _p(b), int(M), int(N), int(K), _p(d), _p(err), _stream(stream)))
+    return d
+
+
+def moe_transpose_bf16(src, dst=None, stream=None):
+    """dst [cols, rows] bf16 = src [rows, cols]^T (src bf16 or fp32)."""
+    rows, cols = src.shape
+    dst = dst if dst is not None else _empty((cols, rows), torch.bfloat16, src)
+    _check("moe_transpose_bf16", lib.moe_transpose_bf16(_p(src), int(src.dtype == torch.float32), int(rows),
+                                                        int(cols), _p(dst), _stream(stream)))
+    return dst
+
+
+def moe_unpermute_combine_add(y_perm, slot_of, topk_w, addend, out=None, err=None, stream=None):
+    T, k = slot_of.shape
+    d = y_perm.shape[1]
+    out = out if out is not None else _empty((T, d), torch.bfloat16, y_perm)
+    _check("moe_unpermute_combine_add", lib.moe_unpermute_combine_add(_p(y_perm), _p(slot_of), _p(topk_w),
+                                                                      _p(addend), T, d, k, _p(out), _p(err),
+                                                                      _stream(stream)))
+    return out
 
 
 def moe_unpermute_combine(y_perm, slot_of, topk_w, out=None, err=None, stream=None):

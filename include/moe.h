@@ -325,6 +325,38 @@ MOE_API moe_status_t grouped_gemm_mxfp8_swiglu_quant(const uint8_t* a, const uin
                                              uint8_t* h_scales_col, int32_t* err, void* stream);
 
 /*
+ * gemm_bf16_nt -- dense D = A * B^T with bf16 operands on the tensor cores
+ * (tcgen05.mma kind::f16, fp32 accumulation): the router's GEMMs ([TE-JAX]
+ * "Optimization 2": the fused router kernels assign tokens to experts from
+ * the router's scores; the logits are x * W_r).
+ *   a   [M, K] bf16 row-major (K contiguous); M % 128 == 0.
+ *   b   [N, K] bf16 row-major; N % 8 == 0 (any N: columns are computed in
+ *       256-wide tiles and the tile's columns >= N are not stored).
+ *   d   [M, N] fp32 row-major, 32-byte aligned: D[m, n] = sum_k a[m,k] b[n,k].
+ *   K % 8 == 0 (16-byte rows); a and b 16-byte aligned.
+ */
+MOE_API moe_status_t gemm_bf16_nt(const void* a, const void* b, int64_t M, int N, int64_t K, float* d, int32_t* err,
+                          void* stream);
+
+/*
+ * moe_transpose_bf16 -- dst [cols, rows] bf16 = transpose of src [rows,
+ * cols] (bf16, or fp32 rounded to bf16 nearest-even when src_fp32 != 0).
+ * The router backward's K-major operands (x^T, dlogits^T).
+ */
+MOE_API moe_status_t moe_transpose_bf16(const void* src, int src_fp32, int64_t rows, int64_t cols, void* dst,
+                                void* stream);
+
+/*
+ * moe_unpermute_combine_add -- moe_unpermute_combine plus an fp32 addend
+ * [T, d] (16-byte aligned): out[t] = bf16(addend[t] + sum_j w[t,j] y[slot(t,j)]),
+ * summed in fp32 in that order; the router's input gradient joins the
+ * experts' here.
+ */
+MOE_API moe_status_t moe_unpermute_combine_add(const void* y_perm, const int32_t* slot_of, const float* topk_w,
+                                       const float* addend, int T, int d, int k, void* out, int32_t* err,
+                                       void* stream);
+
+/*
  * moe_unpermute_combine -- local half of combine ([TE-JAX] "Optimization 2":
  * per-expert results are accumulated and restored to token order; [CH1]
  * §2.3.2: a sum weighted by the routing weights).

@@ -40,7 +40,7 @@ __all__ = [
     "mxfp8_dequantize_rows", "mxfp8_dequantize_cols", "route_topk", "group_counts",
     "group_offsets", "aligned_group_offsets", "permute_slots", "permute", "fp32_round", "permute_scaled_bf16",
     "grouped_gemm", "grouped_gemm_wgrad", "swiglu", "swiglu_bwd", "combine",
-    "combine_bwd", "route_bwd", "layer_forward", "layer_backward",
+    "combine_bwd", "route_bwd", "layer_forward", "layer_backward", "router_logits", "router_backward",
 ]
 
 MXFP8_BLOCK = 32          # [CH1] "低精度格式的缩放机制": one scale per group of 32
@@ -484,6 +484,31 @@ def route_bwd(logits, idx, dw, score="softmax", normalize=True):
 # Whole layer, unquantized fp64 (composition of the steps above; used to pin
 # the backward formulas by finite differences)
 # --------------------------------------------------------------------------
+
+# --------------------------------------------------------------------------
+# Router GEMM ([TE-JAX] "Optimization 2": "fused router kernels" assign the
+# tokens from the router's scores; the scores come from a learned linear
+# router, logits = x W_r)
+# --------------------------------------------------------------------------
+
+def router_logits(x, Wr):
+    """logits [T, E] = x [T, d] @ W_r [d, E].  Reading: the pages give no
+    router arithmetic; the operands are the step's bf16 activations and bf16
+    router weights, the product is exact in fp64 (the GPU accumulates in
+    fp32 and stores fp32 logits)."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(Wr, dtype=np.float64)
+
+
+def router_backward(x, Wr, dlogits):
+    """Gradients of ``router_logits``: dx_r = bf16(dlogits) @ W_r^T [T, d]
+    and dW_r = x^T @ bf16(dlogits) [d, E].  Reading: the backward GEMMs take
+    bf16 operands like the forward, so dlogits (fp32) is rounded to bf16
+    (nearest even) once; the products are exact in fp64."""
+    g = bf16_round(np.asarray(dlogits, dtype=np.float64))
+    x = np.asarray(x, dtype=np.float64)
+    Wr = np.asarray(Wr, dtype=np.float64)
+    return g @ Wr.T, x.T @ g
+
 
 def layer_forward(x, logits, W1, W2, k, score="softmax", normalize=True, align=1):
     """Dropless MoE layer, [TE-JAX] Figure 3: route, permute, grouped GEMM

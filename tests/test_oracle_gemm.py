@@ -143,3 +143,73 @@ def test_layer_padding_does_not_change_results():
     g2 = O.layer_backward(dout, logits, W1, W2, k, s2)
     for key in ("dx", "dlogits", "dW1", "dW2"):
         assert np.allclose(g1[key], g2[key], rtol=1e-12, atol=1e-12)
+
+
+def test_router_logits_by_hand_and_one_hot():
+    x = np.array([[1.0, 2.0, -3.0], [0.5, 0.0, 4.0]])
+    Wr = np.array([[1.0, 0.0], [0.0, 2.0], [1.0, -1.0]])
+    assert np.array_equal(O.router_logits(x, Wr), np.array([[1 - 3, 4 + 3], [0.5 + 4, -4.0]]))
+    # one-hot columns pick input features exactly
+    rng = np.random.default_rng(3)
+    xb = O.bf16_round(rng.standard_normal((16, 8)))
+    pick = np.array([5, 0, 7, 2])
+    oh = np.zeros((8, 4))
+    oh[pick, np.arange(4)] = 1.0
+    assert np.array_equal(O.router_logits(xb, oh), xb[:, pick])
+
+
+def test_router_backward_adjoint_and_bf16_rounding():
+    rng = np.random.default_rng(4)
+    T, d, E = 12, 10, 6
+    x = O.bf16_round(rng.standard_normal((T, d)))
+    Wr = O.bf16_round(rng.standard_normal((d, E)))
+    G = O.bf16_round(rng.standard_normal((T, E)))        # already bf16: no rounding
+    dx, dW = O.router_backward(x, Wr, G)
+    # <router_logits(x, W), G> = <x, dx> = <W, dW>
+    v = np.sum(O.router_logits(x, Wr) * G)
+    assert np.isclose(v, np.sum(x * dx), rtol=1e-12) and np.isclose(v, np.sum(Wr * dW), rtol=1e-12)
+    # dlogits are rounded to bf16 before the GEMMs: 1 + 2^-9 becomes 1
+    g = np.zeros((T, E))
+    g[0, 0] = 1.0 + 2.0 ** -9
+    dx1, _ = O.router_backward(x, Wr, g)
+    assert np.array_equal(dx1[0], Wr[:, 0])
+
+
+@pytest.mark.parametrize("score", ["softmax", "sigmoid"])
+def test_layer_with_router_finite_differences(score):
+    """The router's gradients close the layer's chain: L(x, W_r) =
+    <layer(x, router_logits(x, W_r)), dout>; dL/dx = dx_moe + dx_r and
+    dL/dW_r = dW_r, checked by central differences on the unquantized fp64
+    layer.  router_backward rounds dlogits to bf16 once, so the comparison
+    allows that rounding (rtol 1e-2)."""
+    rng = np.random.default_rng(5)
+    T, d, E, k, f = 6, 8, 5, 2, 4
+    x = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((d, E)) * 0.5
+    W1 = rng.standard_normal((E, d, 2 * f)) * 0.4
+    W2 = rng.standard_normal((E, f, d)) * 0.4
+    dout = rng.standard_normal((T, d))
+
+    def loss(x_, Wr_):
+        o, _ = O.layer_forward(x_, O.router_logits(x_, Wr_), W1, W2, k, score, True, align=1)
+        return float(np.sum(o * dout))
+
+    logits = O.router_logits(x, Wr)
+    out, saved = O.layer_forward(x, logits, W1, W2, k, score, True, align=1)
+    g = O.layer_backward(dout, logits, W1, W2, k, saved, score, True)
+    dx_r, dWr = O.router_backward(x, Wr, g["dlogits"])
+    gx, gW = g["dx"] + dx_r, dWr
+    eps = 1e-6
+    for (t, j) in [(0, 0), (3, 5), (5, 7)]:
+        xp, xm = x.copy(), x.copy()
+        xp[t, j] += eps
+        xm[t, j] -= eps
+        fd = (loss(xp, Wr) - loss(xm, Wr)) / (2 * eps)
+        assert np.isclose(fd, gx[t, j], rtol=1e-2, atol=1e-3 * (np.abs(gx).max() + 1e-12))
+    for (j, e) in [(0, 0), (4, 2), (7, 4)]:
+        Wp, Wm = Wr.copy(), Wr.copy()
+        Wp[j, e] += eps
+        Wm[j, e] -= eps
+        fd = (loss(x, Wp) - loss(x, Wm)) / (2 * eps)
+        assert np.isclose(fd, gW[j, e], rtol=1e-2, atol=1e-3 * (np.abs(gW).max() + 1e-12))
+
