@@ -17,10 +17,14 @@ _SCORES = {"softmax": ops.MOE_SCORE_SOFTMAX, "sigmoid": ops.MOE_SCORE_SIGMOID}
 
 
 class MoELayer:
-    def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_intermediates=False):
+    def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_intermediates=False,
+                 router=False):
         """store_intermediates: also write h and dA in bf16 (the step itself
         only needs their MXFP8 codes, which the up/gate GEMM's epilogue and
-        the fused SwiGLU-backward quantization produce)."""
+        the fused SwiGLU-backward quantization produce).
+        router: the step starts from x alone: logits = x W_r with a bf16
+        router weight W_r [d, E] (set_router_weights), and the backward adds
+        the router's input gradient to dx and computes dW_r [d, E] (fp32)."""
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
         self.score = _SCORES[score]
         self.normalize = bool(normalize)
@@ -71,6 +75,16 @@ class MoELayer:
         self.dlogits = z((T, E), torch.float32)
         self.dW1 = z((E, d, 2 * f), torch.bfloat16)
         self.dW2 = z((E, f, d), torch.bfloat16)
+        self.router = bool(router)
+        if self.router:
+            assert T % 128 == 0 and d % 8 == 0 and E % 8 == 0, "router GEMMs: T % 128, d % 8, E % 8"
+            self.Wr = z((d, E), torch.bfloat16)            # logits = x @ Wr
+            self.WrT = z((E, d), torch.bfloat16)
+            self.xT = z((d, T), torch.bfloat16)
+            self.dlogitsT = z((E, T), torch.bfloat16)
+            self.dlogits_bf = z((T, E), torch.bfloat16)
+            self.dx_r = z((T, d), torch.float32)
+            self.dWr = z((d, E), torch.float32)
         self.graph = None
         self.weights_ready = False
         # when a list, every grouped-GEMM launch of a step appends a pair of
@@ -96,6 +110,12 @@ class MoELayer:
         self.W2d, self.W2d_s = ops.mxfp8_group_quantize(W2v, ops.MOE_QUANT_ROWWISE, err=self.err)
         self.weights_ready = True
 
+    def set_router_weights(self, Wr):
+        """bf16 router weight W_r [d, E] (and its transposed copy)."""
+        assert self.router
+        self.Wr.copy_(Wr)
+        ops.moe_transpose_bf16(self.Wr, self.WrT)
+
     def _timed(self, fn, *args):
         if self.gemm_events is None:
             return fn(*args)
@@ -116,6 +136,8 @@ class MoELayer:
     def forward_(self):
         E, k, d, f, M = self.E, self.k, self.d, self.f, self.row_cap
         err = self.err
+        if self.router:      # logits = x W_r (bf16 operands, fp32 logits)
+            ops.gemm_bf16_nt(self.x, self.WrT, self.logits, err)
         ops.moe_route_topk(self.logits, k, self.score, self.normalize, self.topk_idx, self.topk_w, self.counts,
                            self.offsets, self.ws_route, err)
         ops.moe_permute(self.x, self.topk_idx, E, M, self.gofs, self.slot_of, self.row_id, None, False,
@@ -157,8 +179,17 @@ class MoELayer:
         # dW1_g = X_g^T dA_g
         self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, 0, self.gofs, E, d,
                    2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, err)
-        ops.moe_unpermute_combine(self.dx_perm, self.slot_of, None, self.dx, err)
         ops.moe_route_bwd(self.logits, self.topk_idx, self.dw, self.score, self.normalize, self.dlogits, err)
+        if self.router:
+            # dx_r = bf16(dlogits) W_r^T, dW_r = x^T bf16(dlogits); dx = dx_r + sum_j dX_perm[slot]
+            ops.moe_transpose_bf16(self.dlogits, self.dlogitsT)
+            ops.moe_transpose_bf16(self.dlogitsT, self.dlogits_bf)
+            ops.moe_transpose_bf16(self.x, self.xT)
+            ops.gemm_bf16_nt(self.dlogits_bf, self.Wr, self.dx_r, err)
+            ops.gemm_bf16_nt(self.xT, self.dlogitsT, self.dWr, err)
+            ops.moe_unpermute_combine_add(self.dx_perm, self.slot_of, None, self.dx_r, self.dx, err)
+        else:
+            ops.moe_unpermute_combine(self.dx_perm, self.slot_of, None, self.dx, err)
 
     def step_(self):
         """One fwd+bwd pass over the resident inputs (no allocation, no sync)."""
