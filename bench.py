@@ -42,6 +42,7 @@ WORKLOADS = {
 }
 METRIC = "MoE layer fwd+bwd TFLOPS (MXFP8 grouped GEMM) and % of dense peak, 1 GB300"
 KERNELS_PER_STEP = 18       # libmoe kernel launches in one fwd+bwd step (see layer.MoELayer)
+ROUTER_KERNELS = 6          # with the router: 3 bf16 GEMMs, 3 transposes (the dx combine takes the addend)
 GEMMS_PER_STEP = 6
 
 
@@ -137,7 +138,9 @@ def run_gpu(args, rank, world, local_rank):
     dev = f"cuda:{local_rank}"
     w = WORKLOADS[args.workload]
     T, d, E, k, f = w["T"], w["d"], w["E"], w["k"], w["f"]
-    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev)
+    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev, router=args.router)
+    if args.router:
+        L.set_router_weights(synth.make_normal_bf16((d, E), 5, dev, std=0.02))
     inp = synth.make_layer_inputs(T, d, E, f, dev, zipf_s=w["zipf"], seed_offset=rank)
     L.set_weights(inp["W1"], inp["W2"])
     del inp["W1"], inp["W2"]
@@ -165,6 +168,9 @@ def run_gpu(args, rank, world, local_rank):
     # ---- timed region: K eager steps, events around every GEMM launch
     ev_pairs = []
     L.gemm_events = ev_pairs
+    rev_pairs = []
+    if args.router:
+        L.router_events = rev_pairs
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
         barrier()
@@ -176,6 +182,7 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
     L.gemm_events = None
+    L.router_events = None
     L.check_err()
     elapsed_ms = t_start.elapsed_time(t_end)
     gemm_ms = [0.0] * GEMMS_PER_STEP
@@ -273,9 +280,28 @@ def run_gpu(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": round(algo_bytes / GEMMS_PER_STEP)},
         "e2e": {"value": round(job_tflops(flops, world, e2e_ms), 2), "unit": "TFLOPS",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (ROUTER_KERNELS if args.router else 0)) * args.steps,
         "clocks": clk.summary(),
     }
+    if args.router:
+        rnames = ["logits = x W_r", "dx_r = dlogits W_r^T", "dW_r = x^T dlogits"]
+        rms = [0.0] * 3
+        for i, (s_, e_) in enumerate(rev_pairs):
+            rms[i % 3] += s_.elapsed_time(e_)
+        rms = [x / args.steps for x in rms]
+        rflops = 2.0 * T * d * E
+        bf_peak = peaks["bf16_tflops_sustained"]
+        result["router"] = {
+            "included_in_step": True,
+            "gemm_per_launch": {n: {"ms": round(t, 4), "tflops": round(rflops / (t * 1e-3) / 1e12, 1)}
+                                for n, t in zip(rnames, rms)},
+            "roofline": {"bound": "tensor (bf16, kind::f16)", "achieved": round(3 * rflops / (sum(rms) * 1e-3) / 1e12, 1),
+                         "peak": bf_peak, "unit": "TFLOP/s",
+                         "frac": round(3 * rflops / (sum(rms) * 1e-3) / 1e12 / bf_peak, 4),
+                         "peak_source": f"{psrc} bf16 sustained"},
+            "flops_per_step": 3 * rflops,
+        }
+        result["config"]["router"] = "logits = x W_r (bf16 [d, E]) inside the step, with its backward"
     return result, L
 
 
@@ -494,6 +520,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="deepseek-v3", choices=sorted(WORKLOADS))
+    ap.add_argument("--router", action="store_true",
+                    help="include the router (logits = x W_r, bf16 tensor-core GEMMs, and its backward) in the "
+                         "step and report its GEMMs separately")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-experts", type=int, default=6)
     ap.add_argument("--gemm-point", nargs="+", type=int, metavar="G M_TOTAL N [K]",

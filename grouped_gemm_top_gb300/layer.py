@@ -90,6 +90,7 @@ class MoELayer:
         # when a list, every grouped-GEMM launch of a step appends a pair of
         # CUDA events recorded around it on the current stream
         self.gemm_events = None
+        self.router_events = None      # the same for the router's GEMMs
 
     # ------------------------------------------------------------ weights --
     def set_weights(self, W1, W2):
@@ -129,6 +130,16 @@ class MoELayer:
     def _gemm(self, *args):
         return self._timed(ops.grouped_gemm_mxfp8, *args)
 
+    def _router_gemm(self, *args):
+        if self.router_events is None:
+            return ops.gemm_bf16_nt(*args)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        r = ops.gemm_bf16_nt(*args)
+        e.record()
+        self.router_events.append((s, e))
+        return r
+
     def _gemm_swiglu_quant(self, *args):
         return self._timed(ops.grouped_gemm_mxfp8_swiglu_quant, *args)
 
@@ -137,7 +148,7 @@ class MoELayer:
         E, k, d, f, M = self.E, self.k, self.d, self.f, self.row_cap
         err = self.err
         if self.router:      # logits = x W_r (bf16 operands, fp32 logits)
-            ops.gemm_bf16_nt(self.x, self.WrT, self.logits, err)
+            self._router_gemm(self.x, self.WrT, self.logits, err)
         ops.moe_route_topk(self.logits, k, self.score, self.normalize, self.topk_idx, self.topk_w, self.counts,
                            self.offsets, self.ws_route, err)
         ops.moe_permute(self.x, self.topk_idx, E, M, self.gofs, self.slot_of, self.row_id, None, False,
@@ -185,8 +196,8 @@ class MoELayer:
             ops.moe_transpose_bf16(self.dlogits, self.dlogitsT)
             ops.moe_transpose_bf16(self.dlogitsT, self.dlogits_bf)
             ops.moe_transpose_bf16(self.x, self.xT)
-            ops.gemm_bf16_nt(self.dlogits_bf, self.Wr, self.dx_r, err)
-            ops.gemm_bf16_nt(self.xT, self.dlogitsT, self.dWr, err)
+            self._router_gemm(self.dlogits_bf, self.Wr, self.dx_r, err)
+            self._router_gemm(self.xT, self.dlogitsT, self.dWr, err)
             ops.moe_unpermute_combine_add(self.dx_perm, self.slot_of, None, self.dx_r, self.dx, err)
         else:
             ops.moe_unpermute_combine(self.dx_perm, self.slot_of, None, self.dx, err)
