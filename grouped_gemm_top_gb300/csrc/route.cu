@@ -287,6 +287,58 @@ extern "C" moe_status_t moe_route_bwd(const float* logits, const int32_t* topk_i
 }
 
 // ---------------------------------------------------------------------------
+// Shared experts: experts every token uses with weight 1 (DeepSeek-V3's
+// shared expert).  They join the routed choices as choices k .. k+S-1 of
+// every token (experts E .. E+S-1), so permute, the grouped GEMMs and the
+// combine treat them like routed experts whose group holds every token.
+namespace moe {
+
+__global__ void k_append_shared(const int32_t* __restrict__ idx, const float* __restrict__ w, int T, int k, int E,
+                                int S, int32_t* __restrict__ idx2, float* __restrict__ w2) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int k2 = k + S;
+    if (i >= (int64_t)T * k2) return;
+    const int64_t t = i / k2;
+    const int j = (int)(i - t * k2);
+    idx2[i] = j < k ? idx[t * k + j] : E + (j - k);
+    w2[i] = j < k ? w[t * k + j] : 1.f;
+}
+
+__global__ void k_drop_shared(const float* __restrict__ dw2, int T, int k, int S, float* __restrict__ dw) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)T * k) return;
+    const int64_t t = i / k;
+    dw[i] = dw2[t * (k + S) + (i - t * k)];
+}
+
+}  // namespace moe
+
+extern "C" moe_status_t moe_route_append_shared(const int32_t* topk_idx, const float* topk_w, int T, int k, int E,
+                                                int n_shared, int32_t* idx_out, float* w_out, void* stream) {
+    MOE_REQUIRE(T >= 0 && k >= 1 && E >= 1 && n_shared >= 1 && k + n_shared <= 32, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(T == 0 || (topk_idx && topk_w && idx_out && w_out), MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    if (T == 0) return MOE_OK;
+    const int64_t n = (int64_t)T * (k + n_shared);
+    moe::k_append_shared<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(topk_idx, topk_w, T, k, E,
+                                                                                        n_shared, idx_out, w_out);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+extern "C" moe_status_t moe_route_drop_shared(const float* dw_all, int T, int k, int n_shared, float* dw,
+                                              void* stream) {
+    MOE_REQUIRE(T >= 0 && k >= 1 && n_shared >= 1 && k + n_shared <= 32, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(T == 0 || (dw_all && dw), MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    if (T == 0) return MOE_OK;
+    const int64_t n = (int64_t)T * k;
+    moe::k_drop_shared<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(dw_all, T, k, n_shared, dw);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
 // moe_route_topk_noalloc: moe_route_topk without a caller workspace.
 //
 // Some callers have no way to give the library device memory: code behind a

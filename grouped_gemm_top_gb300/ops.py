@@ -41,7 +41,8 @@ EXPORTS = [
     "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
     "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_route_topk_noalloc",
     "mxfp8_gather_quantize", "grouped_gemm_mxfp8_swiglu_quant", "mxfp8_swiglu_bwd_quantize",
-    "gemm_bf16_nt", "moe_transpose_bf16", "moe_unpermute_combine_add",
+    "gemm_bf16_nt", "moe_transpose_bf16", "moe_unpermute_combine_add", "moe_route_append_shared",
+    "moe_route_drop_shared",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -59,6 +60,8 @@ _SIGS = {
     "mxfp8_gather_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp,
                                      _vp]),
     "gemm_bf16_nt": (_i32, [_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp]),
+    "moe_route_append_shared": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_route_drop_shared": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp]),
     "moe_transpose_bf16": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
     "moe_unpermute_combine_add": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "mxfp8_swiglu_bwd_quantize": (_i32, [_vp, _vp, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -278,6 +281,25 @@ def grouped_gemm_mxfp8_swiglu_quant(a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K
                                                _p(h_scales_row), _p(h_codes_col), _p(h_scales_col), _p(err),
                                                _stream(stream)))
     return a_pre, h, h_codes_row, h_scales_row, h_codes_col, h_scales_col
+
+
+def moe_route_append_shared(topk_idx, topk_w, E, n_shared, idx_out=None, w_out=None, stream=None):
+    """[T, k+S] choices: the routed ones, then the S shared experts E.. with weight 1."""
+    T, k = topk_idx.shape
+    idx_out = idx_out if idx_out is not None else _empty((T, k + n_shared), torch.int32, topk_idx)
+    w_out = w_out if w_out is not None else _empty((T, k + n_shared), torch.float32, topk_idx)
+    _check("moe_route_append_shared", lib.moe_route_append_shared(_p(topk_idx), _p(topk_w), T, k, int(E),
+                                                                  int(n_shared), _p(idx_out), _p(w_out),
+                                                                  _stream(stream)))
+    return idx_out, w_out
+
+
+def moe_route_drop_shared(dw_all, k, dw=None, stream=None):
+    T, k2 = dw_all.shape
+    dw = dw if dw is not None else _empty((T, k), torch.float32, dw_all)
+    _check("moe_route_drop_shared", lib.moe_route_drop_shared(_p(dw_all), T, int(k), int(k2 - k), _p(dw),
+                                                              _stream(stream)))
+    return dw
 
 
 def gemm_bf16_nt(a, b, d=None, err=None, stream=None):

@@ -394,6 +394,24 @@ MOE_API moe_status_t moe_route_bwd(const float* logits, const int32_t* topk_idx,
                            int32_t* err, void* stream);
 
 /*
+ * moe_route_append_shared -- shared experts (experts every token uses, with
+ * weight 1; DeepSeek-V3 has one, [CH1] §2.3.2 MoE structure) as extra
+ * choices: idx_out [T, k+S] = [topk_idx | E, E+1, .., E+S-1] and w_out
+ * [T, k+S] = [topk_w | 1, .., 1] per token (S = n_shared).  Permute, the
+ * grouped GEMMs (E+S groups) and the combine then need nothing else: each
+ * shared expert's group holds every token, and its output joins the
+ * combine with weight 1.  k + S <= 32.
+ */
+MOE_API moe_status_t moe_route_append_shared(const int32_t* topk_idx, const float* topk_w, int T, int k, int E,
+                                     int n_shared, int32_t* idx_out, float* w_out, void* stream);
+
+/*
+ * moe_route_drop_shared -- dw [T, k] = the routed columns of dw_all [T, k+S]
+ * (the shared choices' weights are constants; their dw is not used).
+ */
+MOE_API moe_status_t moe_route_drop_shared(const float* dw_all, int T, int k, int n_shared, float* dw, void* stream);
+
+/*
  * moe_route_topk_noalloc -- moe_route_topk for callers that cannot allocate.
  * (The pages have no counterpart: this is a calling convention, not a step of
  * the method.)  Some callers cannot hand the library any device memory

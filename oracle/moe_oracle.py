@@ -41,6 +41,7 @@ __all__ = [
     "group_offsets", "aligned_group_offsets", "permute_slots", "permute", "fp32_round", "permute_scaled_bf16",
     "grouped_gemm", "grouped_gemm_wgrad", "swiglu", "swiglu_bwd", "combine",
     "combine_bwd", "route_bwd", "layer_forward", "layer_backward", "router_logits", "router_backward",
+    "append_shared",
 ]
 
 MXFP8_BLOCK = 32          # [CH1] "低精度格式的缩放机制": one scale per group of 32
@@ -510,20 +511,36 @@ def router_backward(x, Wr, dlogits):
     return g @ Wr.T, x.T @ g
 
 
-def layer_forward(x, logits, W1, W2, k, score="softmax", normalize=True, align=1):
+def append_shared(idx, w, E, n_shared):
+    """Shared experts (every token uses them with weight 1; DeepSeek-V3's
+    shared expert, [CH1] §2.3.2) as extra choices: [idx | E .. E+S-1] and
+    [w | 1 .. 1] per token.  Reading: a shared expert is an FFN of the same
+    shape as a routed one whose output is added to the routed combine."""
+    idx = np.asarray(idx, dtype=np.int64)
+    w = np.asarray(w, dtype=np.float64)
+    T = idx.shape[0]
+    sh = np.broadcast_to(E + np.arange(n_shared), (T, n_shared))
+    return np.concatenate([idx, sh], axis=1), np.concatenate([w, np.ones((T, n_shared))], axis=1)
+
+
+def layer_forward(x, logits, W1, W2, k, score="softmax", normalize=True, align=1, n_shared=0):
     """Dropless MoE layer, [TE-JAX] Figure 3: route, permute, grouped GEMM
     (up/gate), SwiGLU, grouped GEMM (down), combine.  W1 [E, d, 2f],
-    W2 [E, f, d].  Returns out [T, d] and the saved activations."""
+    W2 [E, f, d] (the last n_shared experts are shared experts, see
+    ``append_shared``; logits cover the routed ones).  Returns out [T, d]
+    and the saved activations."""
     E = W1.shape[0]
     idx, w = route_topk(logits, k, score, normalize)
-    slot_of, row_id = permute_slots(idx, E, align)
-    gofs = aligned_group_offsets(group_counts(idx, E), align)
-    xp = permute(x, row_id, k)
+    idx_all, w_all = append_shared(idx, w, E - n_shared, n_shared) if n_shared else (idx, w)
+    k_all = k + n_shared
+    slot_of, row_id = permute_slots(idx_all, E, align)
+    gofs = aligned_group_offsets(group_counts(idx_all, E), align)
+    xp = permute(x, row_id, k_all)
     a = grouped_gemm(xp, W1, gofs)
     h = swiglu(a)
     y = grouped_gemm(h, W2, gofs)
-    out = combine(y, slot_of, w)
-    saved = dict(idx=idx, w=w, slot_of=slot_of, row_id=row_id, gofs=gofs, xp=xp, a=a, h=h, y=y)
+    out = combine(y, slot_of, w_all)
+    saved = dict(idx=idx, w=w_all, slot_of=slot_of, row_id=row_id, gofs=gofs, xp=xp, a=a, h=h, y=y)
     return out, saved
 
 
@@ -531,7 +548,8 @@ def layer_backward(dout, logits, W1, W2, k, saved, score="softmax", normalize=Tr
     """Backward of ``layer_forward`` (plain autograd, step by step)."""
     T = dout.shape[0]
     rows = saved["xp"].shape[0]
-    dy, dw = combine_bwd(dout, saved["y"], saved["slot_of"], saved["w"], rows)
+    dy, dw_all = combine_bwd(dout, saved["y"], saved["slot_of"], saved["w"], rows)
+    dw = dw_all[:, :k]           # the shared choices' weights are constants
     dh = grouped_gemm(dy, np.transpose(W2, (0, 2, 1)), saved["gofs"])
     dW2 = grouped_gemm_wgrad(saved["h"], dy, saved["gofs"])
     da = swiglu_bwd(saved["a"], dh)

@@ -213,3 +213,66 @@ def test_layer_with_router_finite_differences(score):
         fd = (loss(x, Wp) - loss(x, Wm)) / (2 * eps)
         assert np.isclose(fd, gW[j, e], rtol=1e-2, atol=1e-3 * (np.abs(gW).max() + 1e-12))
 
+
+def test_append_shared_by_hand():
+    idx = np.array([[2, 0], [1, 3]])
+    w = np.array([[0.7, 0.3], [0.6, 0.4]])
+    i2, w2 = O.append_shared(idx, w, 4, 2)
+    assert np.array_equal(i2, np.array([[2, 0, 4, 5], [1, 3, 4, 5]]))
+    assert np.array_equal(w2, np.array([[0.7, 0.3, 1.0, 1.0], [0.6, 0.4, 1.0, 1.0]]))
+
+
+def test_shared_expert_is_a_dense_ffn_added_to_the_routed_layer():
+    """With S shared experts the layer's output is the routed layer's plus,
+    for each shared expert, swiglu(x W1_s) W2_s on every token (computed
+    here densely, with no routing or permutation)."""
+    rng = np.random.default_rng(6)
+    T, d, E, k, f, S = 9, 8, 5, 2, 4, 2
+    x = rng.standard_normal((T, d))
+    logits = rng.standard_normal((T, E))
+    W1 = rng.standard_normal((E + S, d, 2 * f)) * 0.5
+    W2 = rng.standard_normal((E + S, f, d)) * 0.5
+    routed, _ = O.layer_forward(x, logits, W1[:E], W2[:E], k, align=4)
+    both, saved = O.layer_forward(x, logits, W1, W2, k, align=4, n_shared=S)
+    dense = sum(O.swiglu(x @ W1[E + s]) @ W2[E + s] for s in range(S))
+    assert np.allclose(both, routed + dense, rtol=1e-12, atol=1e-12)
+    # every token is in each shared expert's group
+    gofs = saved["gofs"]
+    assert all(gofs[E + s + 1] - gofs[E + s] >= T for s in range(S))
+
+
+def test_shared_expert_finite_differences():
+    rng = np.random.default_rng(7)
+    T, d, E, k, f, S = 6, 8, 4, 2, 4, 1
+    x = rng.standard_normal((T, d))
+    logits = rng.standard_normal((T, E))
+    W1 = rng.standard_normal((E + S, d, 2 * f)) * 0.4
+    W2 = rng.standard_normal((E + S, f, d)) * 0.4
+    dout = rng.standard_normal((T, d))
+    out, saved = O.layer_forward(x, logits, W1, W2, k, "sigmoid", True, align=1, n_shared=S)
+    g = O.layer_backward(dout, logits, W1, W2, k, saved, "sigmoid", True)
+
+    def loss(x_, l_, W1_):
+        o, _ = O.layer_forward(x_, l_, W1_, W2, k, "sigmoid", True, align=1, n_shared=S)
+        return float(np.sum(o * dout))
+
+    eps = 1e-6
+    for t, j in [(0, 1), (5, 7)]:
+        xp, xm = x.copy(), x.copy()
+        xp[t, j] += eps
+        xm[t, j] -= eps
+        assert np.isclose((loss(xp, logits, W1) - loss(xm, logits, W1)) / (2 * eps), g["dx"][t, j], rtol=1e-5,
+                          atol=1e-8)
+    for t, e in [(0, 0), (3, 2)]:
+        lp, lm = logits.copy(), logits.copy()
+        lp[t, e] += eps
+        lm[t, e] -= eps
+        assert np.isclose((loss(x, lp, W1) - loss(x, lm, W1)) / (2 * eps), g["dlogits"][t, e], rtol=1e-5,
+                          atol=1e-8)
+    # the shared expert's weights get gradients from every token
+    Wp, Wm = W1.copy(), W1.copy()
+    Wp[E, 3, 5] += eps
+    Wm[E, 3, 5] -= eps
+    assert np.isclose((loss(x, logits, Wp) - loss(x, logits, Wm)) / (2 * eps), g["dW1"][E, 3, 5], rtol=1e-5,
+                      atol=1e-8)
+
