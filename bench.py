@@ -138,10 +138,11 @@ def run_gpu(args, rank, world, local_rank):
     dev = f"cuda:{local_rank}"
     w = WORKLOADS[args.workload]
     T, d, E, k, f = w["T"], w["d"], w["E"], w["k"], w["f"]
-    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev, router=args.router)
+    S = args.shared_experts
+    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev, router=args.router, n_shared=S)
     if args.router:
         L.set_router_weights(synth.make_normal_bf16((d, E), 5, dev, std=0.02))
-    inp = synth.make_layer_inputs(T, d, E, f, dev, zipf_s=w["zipf"], seed_offset=rank)
+    inp = synth.make_layer_inputs(T, d, E, f, dev, zipf_s=w["zipf"], seed_offset=rank, n_shared=S)
     L.set_weights(inp["W1"], inp["W2"])
     del inp["W1"], inp["W2"]
     L.logits.copy_(inp["logits"])
@@ -232,17 +233,17 @@ def run_gpu(args, rank, world, local_rank):
 
     peaks, psrc = _peaks()
     mx_peak = 2.0 * peaks["bf16_tflops_sustained"]     # nominal fp8/bf16 dense ratio 4.5/2.25
-    traffic = _gemm_traffic() if args.workload == "deepseek-v3" else None
+    traffic = _gemm_traffic() if args.workload == "deepseek-v3" and not S else None
     # algorithmic bytes of the six GEMMs: fp8 operands (+1/32 scales) once,
     # bf16 outputs (and the SwiGLU-bwd input a_pre) once, h as its MXFP8
     # codes on both axes
-    R, q = L.R, 1 + 1 / 32
-    algo_bytes = (R * d * q + E * d * 2 * f * q + R * 2 * f * 2 + 2 * R * f * q        # up fwd + SwiGLU + MXFP8(h)
-                  + R * f * q + E * f * d * q + R * d * 2                               # down fwd
-                  + R * d * q + E * f * d * q + R * f * 4                               # down dgrad (fp32 dH)
-                  + R * f * q + R * d * q + E * f * d * 2                               # dW2
-                  + R * 2 * f * q + E * d * 2 * f * q + R * d * 2                       # up dgrad
-                  + R * d * q + R * 2 * f * q + E * d * 2 * f * 2)                      # dW1
+    R, q, Gw = L.R, 1 + 1 / 32, L.G          # rows and weight groups include the shared experts
+    algo_bytes = (R * d * q + Gw * d * 2 * f * q + R * 2 * f * 2 + 2 * R * f * q        # up fwd + SwiGLU + MXFP8(h)
+                  + R * f * q + Gw * f * d * q + R * d * 2                               # down fwd
+                  + R * d * q + Gw * f * d * q + R * f * 4                               # down dgrad (fp32 dH)
+                  + R * f * q + R * d * q + Gw * f * d * 2                               # dW2
+                  + R * 2 * f * q + Gw * d * 2 * f * q + R * d * 2                       # up dgrad
+                  + R * d * q + R * 2 * f * q + Gw * d * 2 * f * 2)                      # dW1
     sum_gemm_ms = sum(gemm_ms)
     achieved = sum(gemm_flops) / (sum_gemm_ms * 1e-3) / 1e12
     per_launch = {n: {"ms": round(t, 4), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
@@ -280,7 +281,7 @@ def run_gpu(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": round(algo_bytes / GEMMS_PER_STEP)},
         "e2e": {"value": round(job_tflops(flops, world, e2e_ms), 2), "unit": "TFLOPS",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (KERNELS_PER_STEP + (ROUTER_KERNELS if args.router else 0)) * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (ROUTER_KERNELS if args.router else 0) + (2 if S else 0)) * args.steps,
         "clocks": clk.summary(),
     }
     if args.router:
@@ -302,6 +303,9 @@ def run_gpu(args, rank, world, local_rank):
             "flops_per_step": 3 * rflops,
         }
         result["config"]["router"] = "logits = x W_r (bf16 [d, E]) inside the step, with its backward"
+    if S:
+        result["config"]["shared_experts"] = (f"{S} shared expert(s) of the routed experts' shape, every token, "
+                                              f"weight 1: {L.G} expert groups, {L.kk} rows per token")
     return result, L
 
 
@@ -513,6 +517,84 @@ def run_hbm_probe(nbytes=4 << 30, reps=10):
             "method": "torch fill_ of 4 GB (write-only) and copy_ of 2 GB into 2 GB (read+write bytes)"}
 
 
+def run_compare(args, capacity_factors=(1.0, 1.25)):
+    """The grouped dropless step against the prior-art ways of running the
+    same layer (grouped_gemm_top_gb300.comparators): a loop of per-expert
+    GEMMs with the counts read on the host every step, and capacity-based
+    MoE with static padded groups (graph-captured; drops what overflows).
+    Every arm is timed over args.steps steps after 3 warm-ups with CUDA
+    events on the launching stream; throughput counts the dropless FLOPs
+    18 T k d f for every arm, so padding and dropped tokens both show as
+    lost throughput."""
+    import torch
+
+    from grouped_gemm_top_gb300 import build as _b
+    if not os.path.exists(_b.LIB):
+        _b.build()
+    from grouped_gemm_top_gb300 import synth
+    from grouped_gemm_top_gb300.comparators import CapacityMoE, LoopMoE
+    from grouped_gemm_top_gb300.layer import MoELayer
+
+    w = WORKLOADS[args.workload]
+    T, d, E, k, f = w["T"], w["d"], w["E"], w["k"], w["f"]
+    dev = "cuda:0"
+    stream = torch.cuda.current_stream()
+    inp = synth.make_layer_inputs(T, d, E, f, dev, zipf_s=w["zipf"])
+
+    def load(L):
+        L.set_weights(inp["W1"], inp["W2"])
+        L.logits.copy_(inp["logits"])
+        L.x.copy_(inp["x"])
+        L.dout.copy_(inp["dout"])
+
+    def timed(fn, steps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / steps
+
+    flops = 18.0 * T * k * d * f
+
+    def arm(ms, **kw):
+        return dict(ms_per_step=round(ms, 4), tflops=round(flops / (ms * 1e-3) / 1e12, 1), **kw)
+
+    arms = {}
+    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev)
+    load(L)
+    arms["grouped_dropless_eager"] = arm(timed(L.step_, args.steps), launches_per_step=KERNELS_PER_STEP)
+    L.capture()
+    arms["grouped_dropless_graph"] = arm(timed(L.replay, args.steps), launches_per_step=KERNELS_PER_STEP)
+    L.check_err()
+    counts = L.counts.cpu()
+    L.graph = None
+    loop = LoopMoE(L)
+    loop.set_weights(inp["W1"], inp["W2"])
+    ms = timed(loop.step_, max(2, args.steps // 3))
+    L.check_err()
+    arms["loop_of_gemms"] = arm(ms, launches_per_step=loop.launches, host_syncs_per_step=1,
+                                note="counts copied to the host and synchronised every step; one GEMM per expert")
+    del loop, L
+    torch.cuda.empty_cache()
+    for cf in capacity_factors:
+        C = CapacityMoE(T, d, E, k, f, w["score"], w["normalize"], device=dev, capacity_factor=cf)
+        load(C)
+        C.capture()
+        ms = timed(C.replay, args.steps)
+        C.check_err()
+        arms[f"capacity_cf{cf}_graph"] = arm(ms, capacity_rows_per_expert=C.C, computed_rows=E * C.C,
+                                            routed_rows=T * k, dropped_fraction=round(C.dropped_fraction(), 5))
+        del C
+        torch.cuda.empty_cache()
+    return {"compare": {"workload": w["desc"], "flops_per_step_dropless": flops, "steps": args.steps,
+                        "max_expert_rows": int(counts.max()), "mean_expert_rows": T * k / E, "arms": arms}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -523,17 +605,25 @@ def main():
     ap.add_argument("--router", action="store_true",
                     help="include the router (logits = x W_r, bf16 tensor-core GEMMs, and its backward) in the "
                          "step and report its GEMMs separately")
+    ap.add_argument("--shared-experts", type=int, default=0, metavar="S",
+                    help="add S shared experts (every token, weight 1) as extra groups of the same grouped GEMMs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-experts", type=int, default=6)
     ap.add_argument("--gemm-point", nargs="+", type=int, metavar="G M_TOTAL N [K]",
                     help="time one standalone grouped GEMM fwd (K = N unless given) and print its line")
     ap.add_argument("--b-layout", default="gnk", choices=["ngk", "gnk"])
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
+    ap.add_argument("--compare", action="store_true",
+                    help="time the grouped dropless step against a per-expert GEMM loop and capacity-based MoE on "
+                         "the same workload and print one line")
     ap.add_argument("--hbm-probe", action="store_true",
                     help="measure write-only and copy HBM bandwidth (PyTorch fill/copy kernels) and print one line")
     args = ap.parse_args()
     if args.hbm_probe:
         print(json.dumps({"hbm_probe": run_hbm_probe()}), flush=True)
+        return
+    if args.compare:
+        print(json.dumps(run_compare(args)), flush=True)
         return
     if args.gemm_point or args.sweep:
         if args.gemm_point:

@@ -18,20 +18,28 @@ _SCORES = {"softmax": ops.MOE_SCORE_SOFTMAX, "sigmoid": ops.MOE_SCORE_SIGMOID}
 
 class MoELayer:
     def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_intermediates=False,
-                 router=False):
+                 router=False, n_shared=0, row_cap=None):
         """store_intermediates: also write h and dA in bf16 (the step itself
         only needs their MXFP8 codes, which the up/gate GEMM's epilogue and
         the fused SwiGLU-backward quantization produce).
         router: the step starts from x alone: logits = x W_r with a bf16
         router weight W_r [d, E] (set_router_weights), and the backward adds
-        the router's input gradient to dx and computes dW_r [d, E] (fp32)."""
+        the router's input gradient to dx and computes dW_r [d, E] (fp32).
+        n_shared: S shared experts that every token uses with weight 1
+        ([CH1] §2.3.2, DeepSeek-V3's shared expert).  They are expert groups
+        E .. E+S-1 of the same grouped GEMMs (weights [E+S, ...]), entered as
+        S extra choices per token, so the layer runs G = E+S groups over
+        T (k+S) rows; the router and its logits cover the E routed experts."""
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
+        self.S = int(n_shared)
+        self.G, self.kk = E + self.S, k + self.S      # expert groups, choices per token
         self.score = _SCORES[score]
         self.normalize = bool(normalize)
         self.device = torch.device(device)
         ops.moe_init(self.device.index or 0)
-        self.R = T * k
-        self.row_cap = ops.moe_row_capacity(T, E, k)
+        self.R = T * self.kk
+        self.row_cap = ops.moe_row_capacity(T, self.G, self.kk) if row_cap is None else int(row_cap)
+        G, kk = self.G, self.kk
         M, dev = self.row_cap, self.device
 
         def z(shape, dtype):
@@ -43,15 +51,22 @@ class MoELayer:
         self.dout = z((T, d), torch.bfloat16)
         # routing / layout
         self.err = z((1,), torch.int32)
-        self.topk_idx = z((T, k), torch.int32)
-        self.topk_w = z((T, k), torch.float32)
+        # route_idx / route_w: the router's top-k; topk_idx / topk_w: every
+        # choice the layer computes (the top-k, then the shared experts)
+        self.route_idx = z((T, k), torch.int32)
+        self.route_w = z((T, k), torch.float32)
+        if self.S:
+            self.topk_idx = z((T, kk), torch.int32)
+            self.topk_w = z((T, kk), torch.float32)
+        else:
+            self.topk_idx, self.topk_w = self.route_idx, self.route_w
         self.counts = z((E,), torch.int32)
         self.offsets = z((E + 1,), torch.int32)
-        self.gofs = z((E + 1,), torch.int32)
-        self.slot_of = z((T, k), torch.int32)
+        self.gofs = z((G + 1,), torch.int32)
+        self.slot_of = z((T, kk), torch.int32)
         self.row_id = z((M,), torch.int32)
         self.ws_route = z((ops.moe_route_workspace_size(T, E),), torch.uint8)
-        self.ws_perm = z((ops.moe_permute_workspace_size(T, E),), torch.uint8)
+        self.ws_perm = z((ops.moe_permute_workspace_size(T, G),), torch.uint8)
         # forward activations (x_perm and dy_perm never exist in bf16: both
         # are quantized, along both axes, straight from x and dout)
         self.xq, self.xs = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
@@ -61,6 +76,7 @@ class MoELayer:
         self.y_perm = z((M, d), torch.bfloat16)
         self.out = z((T, d), torch.bfloat16)
         # backward activations
+        self.dw_all = z((T, kk), torch.float32) if self.S else None
         self.dw = z((T, k), torch.float32)
         self.dyq, self.dys = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.dyqT, self.dysT = z((d, M), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
@@ -73,8 +89,8 @@ class MoELayer:
         self.dx_perm = z((M, d), torch.bfloat16)
         self.dx = z((T, d), torch.bfloat16)
         self.dlogits = z((T, E), torch.float32)
-        self.dW1 = z((E, d, 2 * f), torch.bfloat16)
-        self.dW2 = z((E, f, d), torch.bfloat16)
+        self.dW1 = z((G, d, 2 * f), torch.bfloat16)
+        self.dW2 = z((G, f, d), torch.bfloat16)
         self.router = bool(router)
         if self.router:
             assert T % 128 == 0 and d % 8 == 0 and E % 8 == 0, "router GEMMs: T % 128, d % 8, E % 8"
@@ -94,9 +110,10 @@ class MoELayer:
 
     # ------------------------------------------------------------ weights --
     def set_weights(self, W1, W2):
-        """Quantize bf16 W1 [E, d, 2f] and W2 [E, f, d] along both axes (done
-        once per weight update, outside the step)."""
-        E, d, f = self.E, self.d, self.f
+        """Quantize bf16 W1 [G, d, 2f] and W2 [G, f, d] along both axes (done
+        once per weight update, outside the step; G = E + n_shared, the
+        shared experts last)."""
+        E, d, f = self.G, self.d, self.f
         dev = self.device
         W1v = W1.reshape(E * d, 2 * f)
         W2v = W2.reshape(E * f, d)
@@ -144,15 +161,23 @@ class MoELayer:
         return self._timed(ops.grouped_gemm_mxfp8_swiglu_quant, *args)
 
     # ------------------------------------------------------------- step ----
-    def forward_(self):
-        E, k, d, f, M = self.E, self.k, self.d, self.f, self.row_cap
+    def route_permute_(self):
+        """Router GEMM (if any), top-k routing, shared choices (if any) and
+        the permutation: gofs, slot_of and row_id of the step."""
         err = self.err
         if self.router:      # logits = x W_r (bf16 operands, fp32 logits)
             self._router_gemm(self.x, self.WrT, self.logits, err)
-        ops.moe_route_topk(self.logits, k, self.score, self.normalize, self.topk_idx, self.topk_w, self.counts,
-                           self.offsets, self.ws_route, err)
-        ops.moe_permute(self.x, self.topk_idx, E, M, self.gofs, self.slot_of, self.row_id, None, False,
-                        self.ws_perm, err)
+        ops.moe_route_topk(self.logits, self.k, self.score, self.normalize, self.route_idx, self.route_w,
+                           self.counts, self.offsets, self.ws_route, err)
+        if self.S:
+            ops.moe_route_append_shared(self.route_idx, self.route_w, self.E, self.S, self.topk_idx, self.topk_w)
+        ops.moe_permute(self.x, self.topk_idx, self.G, self.row_cap, self.gofs, self.slot_of, self.row_id, None,
+                        False, self.ws_perm, err)
+
+    def forward_(self):
+        E, k, d, f, M = self.G, self.kk, self.d, self.f, self.row_cap
+        err = self.err
+        self.route_permute_()
         # x_perm = x[row_id // k], both axes: rowwise for the up GEMM, the
         # columnwise copy for the dW1 wgrad of the backward
         ops.mxfp8_gather_quantize(self.x, self.gofs, E, M, self.row_id, k, None, True, True, self.xq, self.xs,
@@ -166,12 +191,15 @@ class MoELayer:
         ops.moe_unpermute_combine(self.y_perm, self.slot_of, self.topk_w, self.out, err)
 
     def backward_(self):
-        E, k, d, f, M = self.E, self.k, self.d, self.f, self.row_cap
+        E, k, d, f, M = self.G, self.kk, self.d, self.f, self.row_cap
         err = self.err
         # dw = <dout, y_perm> per (token, choice); dy_perm = w * dout is only
         # ever materialised as its MXFP8 codes (both axes)
-        ops.moe_combine_bwd(self.dout, self.y_perm, self.slot_of, self.topk_w, None, None, E, None, self.dw, err,
+        dw = self.dw_all if self.S else self.dw
+        ops.moe_combine_bwd(self.dout, self.y_perm, self.slot_of, self.topk_w, None, None, E, None, dw, err,
                             want_dy=False)
+        if self.S:       # the shared choices' weights are constants
+            ops.moe_route_drop_shared(self.dw_all, self.k, self.dw)
         ops.mxfp8_gather_quantize(self.dout, self.gofs, E, M, self.row_id, k, self.topk_w, True, True, self.dyq,
                                   self.dys, self.dyqT, self.dysT, err)
         # dH = dY W2^T (fp32)
@@ -190,7 +218,7 @@ class MoELayer:
         # dW1_g = X_g^T dA_g
         self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, 0, self.gofs, E, d,
                    2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, err)
-        ops.moe_route_bwd(self.logits, self.topk_idx, self.dw, self.score, self.normalize, self.dlogits, err)
+        ops.moe_route_bwd(self.logits, self.route_idx, self.dw, self.score, self.normalize, self.dlogits, err)
         if self.router:
             # dx_r = bf16(dlogits) W_r^T, dW_r = x^T bf16(dlogits); dx = dx_r + sum_j dX_perm[slot]
             ops.moe_transpose_bf16(self.dlogits, self.dlogitsT)

@@ -58,15 +58,18 @@ def make_normal_bf16(shape, seed, device="cpu", std=1.0, chunk_elems=1 << 26):
     return out
 
 
-def make_layer_inputs(T, d, E, f, device="cpu", zipf_s=None, seed_offset=0, weights=True, w_std=0.02):
+def make_layer_inputs(T, d, E, f, device="cpu", zipf_s=None, seed_offset=0, weights=True, w_std=0.02, n_shared=0):
+    """Router logits [T, E], x and dout [T, d] (bf16, N(0, 1)) and, with
+    weights, W1 [E+S, d, 2f] and W2 [E+S, f, d] (bf16, N(0, w_std^2); the S
+    shared experts' weights last)."""
     inp = dict(
         logits=make_logits(T, E, SEED_LOGITS + seed_offset, device, zipf_s),
         x=make_normal_bf16((T, d), SEED_X + seed_offset, device),
         dout=make_normal_bf16((T, d), SEED_DOUT + seed_offset, device),
     )
     if weights:
-        inp["W1"] = make_normal_bf16((E, d, 2 * f), SEED_W1, device, std=w_std)
-        inp["W2"] = make_normal_bf16((E, f, d), SEED_W2, device, std=w_std)
+        inp["W1"] = make_normal_bf16((E + n_shared, d, 2 * f), SEED_W1, device, std=w_std)
+        inp["W2"] = make_normal_bf16((E + n_shared, f, d), SEED_W2, device, std=w_std)
     return inp
 
 

@@ -17,10 +17,10 @@ def ops():
     return gpu_ops()
 
 
-def _layer(ops, T, d, E, k, f, score, norm, zipf=None, seed_offset=0):
+def _layer(ops, T, d, E, k, f, score, norm, zipf=None, seed_offset=0, n_shared=0):
     from grouped_gemm_top_gb300.layer import MoELayer
-    L = MoELayer(T, d, E, k, f, score, norm, store_intermediates=True)
-    inp = synth.make_layer_inputs(T, d, E, f, "cuda", zipf_s=zipf, seed_offset=seed_offset)
+    L = MoELayer(T, d, E, k, f, score, norm, store_intermediates=True, n_shared=n_shared)
+    inp = synth.make_layer_inputs(T, d, E, f, "cuda", zipf_s=zipf, seed_offset=seed_offset, n_shared=n_shared)
     L.set_weights(inp["W1"], inp["W2"])
     L.logits.copy_(inp["logits"])
     L.x.copy_(inp["x"])
@@ -29,8 +29,8 @@ def _layer(ops, T, d, E, k, f, score, norm, zipf=None, seed_offset=0):
 
 
 def _w_fwd(L, which):
-    """Oracle B [E, K, N] from the fwd weight operand (columnwise codes)."""
-    E, d, f = L.E, L.d, L.f
+    """Oracle B [G, K, N] from the fwd weight operand (columnwise codes)."""
+    E, d, f = L.G, L.d, L.f
     if which == 1:
         q, s, K, N = L.W1f, L.W1f_s, d, 2 * f
     else:
@@ -40,8 +40,8 @@ def _w_fwd(L, which):
 
 
 def _w_dgrad(L, which):
-    """Oracle B [E, K, N] for dgrad from the rowwise weight copy."""
-    E, d, f = L.E, L.d, L.f
+    """Oracle B [G, K, N] for dgrad from the rowwise weight copy."""
+    E, d, f = L.G, L.d, L.f
     if which == 1:     # dXp = dA W1^T: B_g = W1_g^T, [2f, d]
         q, s, R, C = L.W1d, L.W1d_s, E * d, 2 * f
         W = O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), R, C)).reshape(E, d, 2 * f)
@@ -59,20 +59,26 @@ def _deq_actT(q, s, C, M, Rp):
     return O.mxfp8_dequantize_cols(q.cpu().numpy()[:, :Rp], atoms_to_rowmajor(s.cpu().numpy(), C, M)[:, :Rp // 32])
 
 
-@pytest.mark.parametrize("score,norm", [("softmax", True), ("sigmoid", True)])
-def test_tiny_layer_stagewise(ops, score, norm):
-    """Tiny dropless layer (T=256, d=512, E=8, top-2, f=256): every stage of
-    fwd and bwd against the oracle applied to the GPU's own stage inputs."""
-    T, d, E, k, f = 256, 512, 8, 2, 256
-    L, inp = _layer(ops, T, d, E, k, f, score, norm)
+@pytest.mark.parametrize("score,norm,S", [("softmax", True, 0), ("sigmoid", True, 0), ("softmax", True, 1),
+                                          ("sigmoid", True, 2)])
+def test_tiny_layer_stagewise(ops, score, norm, S):
+    """Tiny dropless layer (T=256, d=512, E=8, top-2, f=256, S shared
+    experts): every stage of fwd and bwd against the oracle applied to the
+    GPU's own stage inputs."""
+    T, d, E0, k0, f = 256, 512, 8, 2, 256
+    L, inp = _layer(ops, T, d, E0, k0, f, score, norm, n_shared=S)
+    E, k = E0 + S, k0 + S          # expert groups and choices per token
     L.step_()
     torch.cuda.synchronize()
     L.check_err()
     M = L.row_cap
     logits = inp["logits"].cpu().numpy()
-    idx, w = O.route_topk(logits, k, score, norm)
+    idx0, w0 = O.route_topk(logits, k0, score, norm)
+    assert np.array_equal(L.route_idx.cpu().numpy(), idx0)
+    assert np.max(np.abs(L.route_w.cpu().numpy() - w0)) <= 1e-6
+    idx, w = O.append_shared(idx0, L.route_w.cpu().numpy(), E0, S)
     assert np.array_equal(L.topk_idx.cpu().numpy(), idx)
-    assert np.max(np.abs(L.topk_w.cpu().numpy() - w)) <= 1e-6
+    assert np.array_equal(L.topk_w.cpu().numpy(), w)
     slot_of, row_id = O.permute_slots(idx, E, 128)
     gofs = O.aligned_group_offsets(O.group_counts(idx, E), 128)
     Rp = int(gofs[-1])
@@ -100,6 +106,9 @@ def test_tiny_layer_stagewise(ops, score, norm):
     assert_bf16_close(L.out, O.combine(to_np(L.y_perm)[:Rp], slot_of, wg), what="out")
     # ---- backward
     dy, dw = O.combine_bwd(to_np(inp["dout"]), to_np(L.y_perm)[:Rp], slot_of, wg, Rp)
+    if S:
+        assert_fp32_close(L.dw_all, dw, what="dw (every choice)")
+        dw = dw[:, :k0]
     assert_fp32_close(L.dw, dw, what="dw")
     # dy_perm (never stored) = bf16(fp32(w * dout)), quantized both ways
     dyg = O.permute_scaled_bf16(to_np(inp["dout"]), row_id, k, wg)
@@ -133,7 +142,7 @@ def test_tiny_layer_stagewise(ops, score, norm):
     for g in range(E):
         assert_bf16_close(L.dW1[g], dW1[g], what=f"dW1[{g}]")
     assert_bf16_close(L.dx, O.combine(to_np(L.dx_perm)[:Rp], slot_of, None), what="dx")
-    dl = O.route_bwd(logits, idx, L.dw.double().cpu().numpy(), score, norm)
+    dl = O.route_bwd(logits, idx0, L.dw.double().cpu().numpy(), score, norm)
     got = L.dlogits.double().cpu().numpy()
     assert np.max(np.abs(got - dl)) <= 1e-5 * (np.abs(dl).max() + 1e-30) + 1e-7
 
@@ -185,12 +194,15 @@ def test_pipelined_steps_match_single_steps(ops):
 def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     """Large workloads: exact routing/permute, sampled GEMM rows and
     sampled wgrad entries (each over its full contraction)."""
-    T, d, E, k, f, M = L.T, L.d, L.E, L.k, L.f, L.row_cap
+    T, d, E, k, f, M = L.T, L.d, L.G, L.kk, L.f, L.row_cap
     rng = np.random.default_rng(seed)
     logits = inp["logits"].cpu().numpy()
-    idx, w = O.route_topk(logits, k, score, norm)
-    assert np.array_equal(L.topk_idx.cpu().numpy(), idx)
-    assert np.max(np.abs(L.topk_w.cpu().numpy() - w)) <= 1e-6
+    idx, w = O.route_topk(logits, L.k, score, norm)
+    assert np.array_equal(L.route_idx.cpu().numpy(), idx)
+    assert np.max(np.abs(L.route_w.cpu().numpy() - w)) <= 1e-6
+    if L.S:
+        idx, w = O.append_shared(idx, L.route_w.cpu().numpy(), L.E, L.S)
+        assert np.array_equal(L.topk_idx.cpu().numpy(), idx)
     counts = O.group_counts(idx, E)
     gofs = O.aligned_group_offsets(counts, 128)
     assert np.array_equal(L.gofs.cpu().numpy(), gofs)
@@ -267,7 +279,7 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
     wg = L.topk_w.cpu().numpy().astype(np.float64)[tok]
     assert_bf16_close(to_np(L.out[tok_t]), O.combine(ysub, sl, wg), what="out tokens")
     _, rdw = O.combine_bwd(to_np(L.dout[tok_t]), ysub, sl, wg, len(need))
-    assert_fp32_close(L.dw.double().cpu().numpy()[tok], rdw, what="dw tokens")
+    assert_fp32_close(L.dw.double().cpu().numpy()[tok], rdw[:, :L.k], what="dw tokens")
     assert_bf16_close(to_np(L.dx[tok_t]), O.combine(to_np(L.dx_perm[need_t]), sl, None), what="dx tokens")
     # wgrad: sampled (g, m, n) entries over the full group contraction
     nonempty = np.nonzero(counts)[0]
@@ -297,13 +309,14 @@ def _sampled_checks(L, inp, score, norm, n_rows=256, n_w=64, seed=0):
             assert torch.all(dW[g] == 0)
 
 
-@pytest.mark.parametrize("name,T,d,E,k,f,score,zipf", [
-    ("mixtral-shaped", 8192, 4096, 8, 2, 14336, "softmax", None),
-    ("deepseek-v3-shaped", 24576, 7168, 256, 8, 2048, "sigmoid", None),
-    ("deepseek-v3-zipf", 24576, 7168, 256, 8, 2048, "sigmoid", 1.2),
+@pytest.mark.parametrize("name,T,d,E,k,f,score,zipf,S", [
+    ("mixtral-shaped", 8192, 4096, 8, 2, 14336, "softmax", None, 0),
+    ("deepseek-v3-shaped", 24576, 7168, 256, 8, 2048, "sigmoid", None, 0),
+    ("deepseek-v3-zipf", 24576, 7168, 256, 8, 2048, "sigmoid", 1.2, 0),
+    ("deepseek-v3-shared-expert", 24576, 7168, 256, 8, 2048, "sigmoid", None, 1),
 ])
-def test_large_layer_sampled(ops, name, T, d, E, k, f, score, zipf):
-    L, inp = _layer(ops, T, d, E, k, f, score, True, zipf=zipf)
+def test_large_layer_sampled(ops, name, T, d, E, k, f, score, zipf, S):
+    L, inp = _layer(ops, T, d, E, k, f, score, True, zipf=zipf, n_shared=S)
     L.step_()
     torch.cuda.synchronize()
     L.check_err()
