@@ -41,7 +41,8 @@ __all__ = [
     "group_offsets", "aligned_group_offsets", "permute_slots", "permute", "fp32_round", "permute_scaled_bf16",
     "grouped_gemm", "grouped_gemm_wgrad", "swiglu", "swiglu_bwd", "combine",
     "combine_bwd", "route_bwd", "layer_forward", "layer_backward", "router_logits", "router_backward",
-    "append_shared",
+    "append_shared", "NVFP4_BLOCK", "E2M1_MAX", "e2m1_value", "E2M1_VALUES", "e2m1_encode", "nvfp4_tensor_scale",
+    "nvfp4_quantize_rows", "nvfp4_dequantize_rows",
 ]
 
 MXFP8_BLOCK = 32          # [CH1] "低精度格式的缩放机制": one scale per group of 32
@@ -213,6 +214,108 @@ def mxfp8_dequantize_rows(codes, scales):
 def mxfp8_dequantize_cols(codes_t, scales_t):
     """Inverse of the columnwise layout: returns the [Rp, C] matrix."""
     return mxfp8_dequantize_rows(codes_t, scales_t).T
+
+
+# --------------------------------------------------------------------------
+# NVFP4 ([CH1] §1.1 precision table: FP4 is 4 bits, 1 sign + 2 exponent + 1
+# mantissa; "低精度格式的缩放机制": NVFP4 scales in two levels, an E4M3 scale
+# per small block for the relative sizes inside it and one FP32 scale for
+# the whole tensor's range; [TE-JAX] "What is the training performance
+# impact…": NVFP4 is planned next)
+# --------------------------------------------------------------------------
+
+NVFP4_BLOCK = 16    # Reading: the pages give no block size; 16 is the block the tensor cores' NVFP4 MMA scales
+E2M1_MAX = 6.0
+
+
+def e2m1_value(code: int) -> float:
+    """Value of one FP4 E2M1 code: bit 3 sign, bits 2-1 exponent, bit 0
+    mantissa ([CH1] §1.1: "FP4 4 (1+2+1)").  The exponent bias follows the
+    rule of the pages' FP32 example, 2^(n-1) - 1 = 1.  Reading (the pages give
+    only the split): as in E4M3, exponent field 0 holds the subnormals
+    m/2 * 2^(1-1), and every code is finite (no inf/NaN), so the largest
+    magnitude is 1.5 * 2^2 = 6."""
+    s = (code >> 3) & 1
+    e = (code >> 1) & 3
+    m = code & 1
+    if e == 0:
+        mag = (m / 2.0) * 2.0 ** (1 - 1)
+    else:
+        mag = (1.0 + m / 2.0) * 2.0 ** (e - 1)
+    return -mag if s else mag
+
+
+E2M1_VALUES = np.array([e2m1_value(c) for c in range(16)], dtype=np.float64)
+_E2M1_POS = E2M1_VALUES[:8]       # codes 0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6
+
+
+def e2m1_encode(v):
+    """Encode exact fp64 values to E2M1 codes: nearest value, ties to the even
+    code, magnitudes above 6 saturate to 6, the sign bit is kept (negatives
+    that round to zero give 0x8).  Reading: the same round-to-nearest-even
+    with saturation as the E4M3 cast."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    hi = np.clip(np.searchsorted(_E2M1_POS, a, side="left"), 0, 7)
+    lo = np.clip(hi - 1, 0, 7)
+    dlo = a - _E2M1_POS[lo]
+    dhi = _E2M1_POS[hi] - a
+    code = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a >= E2M1_MAX, 7, code)
+    sign = np.signbit(v).astype(np.int64)
+    return (code.astype(np.int64) | (sign << 3)).astype(np.uint8)
+
+
+def nvfp4_tensor_scale(amax):
+    """Per-tensor FP32 scale s_t of a tensor whose largest magnitude is amax.
+    Reading: the tensor-level scale maps the largest magnitude onto the top
+    of the two-level range, 6 (E2M1) x 448 (E4M3), i.e. s_t = amax / 2688,
+    computed in fp32 (it decides codes, so the oracle takes it in the
+    kernel's precision).  amax == 0 gives s_t = 0."""
+    return np.float32(np.float32(amax) / np.float32(E2M1_MAX * E4M3_MAX))
+
+
+def nvfp4_quantize_rows(x):
+    """Rowwise NVFP4 of x [R, C] (C % 16 == 0; exact bf16 values), blocks of
+    16 consecutive elements along each row (the contraction axis).
+
+    Steps, in fp32 where they decide a code:
+      s_t  = nvfp4_tensor_scale(max |x|)
+      per block b: t_b = fp32(fp32(amax_b / 6) / s_t);
+                   scale byte = E4M3 of t_b (nearest, ties to even, saturating
+                   at 448): the per-block scale s_b
+      per element: y = fp32(x / fp32(s_b * s_t)); code = e2m1_encode(y)
+    Reading: a block whose scale byte is zero (its amax is negligible next to
+    the tensor's) gets zero codes, so it dequantizes to zero.
+
+    Returns codes [R, C] u8 (one E2M1 code per element), scale bytes
+    [R, C/16] u8 (E4M3) and s_t (np.float32)."""
+    x = np.asarray(x, dtype=np.float64)
+    R, C = x.shape
+    assert C % NVFP4_BLOCK == 0
+    st = nvfp4_tensor_scale(np.max(np.abs(x)) if x.size else 0.0)
+    blocks = x.reshape(R, C // NVFP4_BLOCK, NVFP4_BLOCK)
+    codes = np.zeros(blocks.shape, dtype=np.uint8)
+    if st == 0:
+        return codes.reshape(R, C), np.zeros((R, C // NVFP4_BLOCK), dtype=np.uint8), st
+    amax_b = np.max(np.abs(blocks), axis=-1).astype(np.float32)
+    t_b = (amax_b / np.float32(E2M1_MAX)).astype(np.float32) / st
+    sbyte = e4m3_encode(t_b.astype(np.float32).astype(np.float64))
+    s_b = E4M3_VALUES[sbyte.astype(np.int64)].astype(np.float32)
+    denom = (s_b * st).astype(np.float32)
+    live = sbyte != 0
+    y = (blocks[live].astype(np.float32) / denom[live][:, None]).astype(np.float32)
+    codes[live] = e2m1_encode(y.astype(np.float64))
+    return codes.reshape(R, C), sbyte, st
+
+
+def nvfp4_dequantize_rows(codes, scales, st):
+    """value = E2M1(code) * E4M3(scale of its block) * s_t, in fp64."""
+    codes = np.asarray(codes)
+    R, C = codes.shape
+    vals = E2M1_VALUES[codes.astype(np.int64)].reshape(R, C // NVFP4_BLOCK, NVFP4_BLOCK)
+    sb = E4M3_VALUES[np.asarray(scales).astype(np.int64)]
+    return (vals * sb[..., None]).reshape(R, C) * float(st)
 
 
 # --------------------------------------------------------------------------
