@@ -279,32 +279,37 @@ def nvfp4_quantize_rows(x):
     """Rowwise NVFP4 of x [R, C] (C % 16 == 0; exact bf16 values), blocks of
     16 consecutive elements along each row (the contraction axis).
 
-    Steps, in fp32 where they decide a code:
-      s_t  = nvfp4_tensor_scale(max |x|)
-      per block b: t_b = fp32(fp32(amax_b / 6) / s_t);
-                   scale byte = E4M3 of t_b (nearest, ties to even, saturating
-                   at 448): the per-block scale s_b
-      per element: y = fp32(x / fp32(s_b * s_t)); code = e2m1_encode(y)
-    Reading: a block whose scale byte is zero (its amax is negligible next to
-    the tensor's) gets zero codes, so it dequantizes to zero.
+    Steps, each rounded to fp32 where it decides a code (the kernel's
+    precision; the order is a reading -- the pages give only the two levels):
+      s_t = nvfp4_tensor_scale(max |x|)   (decode scale, fp32)
+      enc = 2688 / max |x|                (encode factor, fp32)
+      per block b: t_b = (amax_b / 6) * enc; scale byte = E4M3 of t_b
+                   (nearest, ties to even, saturating at 448); its value s_b
+                   r_b = enc / s_b
+      per element: code = e2m1_encode(x * r_b)
+    so that x ~ E2M1(code) * s_b * s_t.  A block whose scale byte is zero (its
+    amax is negligible next to the tensor's) gets zero codes and dequantizes
+    to zero; an all-zero tensor gives s_t = 0 and zero codes.
 
     Returns codes [R, C] u8 (one E2M1 code per element), scale bytes
     [R, C/16] u8 (E4M3) and s_t (np.float32)."""
     x = np.asarray(x, dtype=np.float64)
     R, C = x.shape
     assert C % NVFP4_BLOCK == 0
-    st = nvfp4_tensor_scale(np.max(np.abs(x)) if x.size else 0.0)
+    f32 = np.float32
+    amax_t = f32(np.max(np.abs(x)) if x.size else 0.0)
+    st = nvfp4_tensor_scale(amax_t)
     blocks = x.reshape(R, C // NVFP4_BLOCK, NVFP4_BLOCK)
     codes = np.zeros(blocks.shape, dtype=np.uint8)
     if st == 0:
         return codes.reshape(R, C), np.zeros((R, C // NVFP4_BLOCK), dtype=np.uint8), st
-    amax_b = np.max(np.abs(blocks), axis=-1).astype(np.float32)
-    t_b = (amax_b / np.float32(E2M1_MAX)).astype(np.float32) / st
-    sbyte = e4m3_encode(t_b.astype(np.float32).astype(np.float64))
-    s_b = E4M3_VALUES[sbyte.astype(np.int64)].astype(np.float32)
-    denom = (s_b * st).astype(np.float32)
+    enc = f32(f32(E2M1_MAX * E4M3_MAX) / amax_t)
+    amax_b = np.max(np.abs(blocks), axis=-1).astype(f32)
+    t_b = ((amax_b / f32(E2M1_MAX)).astype(f32) * enc).astype(f32)
+    sbyte = e4m3_encode(t_b.astype(np.float64))
     live = sbyte != 0
-    y = (blocks[live].astype(np.float32) / denom[live][:, None]).astype(np.float32)
+    r_b = (enc / E4M3_VALUES[sbyte[live].astype(np.int64)].astype(f32)).astype(f32)
+    y = (blocks[live].astype(f32) * r_b[:, None]).astype(f32)
     codes[live] = e2m1_encode(y.astype(np.float64))
     return codes.reshape(R, C), sbyte, st
 
