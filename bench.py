@@ -438,6 +438,64 @@ def run_gemm_point(G, M_total, NK, seed=0, steps=10, warmup=3, device="cuda:0", 
             "peak_tflops": mx_peak, "peak_source": f"2 x {psrc} bf16 burst", "empty_groups": int((sizes == 0).sum())}
 
 
+def run_gemm_point_nvfp4(G, M_total, N, K, seed=0, steps=10, warmup=3, device="cuda:0"):
+    """Standalone NVFP4 grouped GEMM (fwd): the same Dirichlet(0.3) groups as
+    run_gemm_point, A and B ~ N(0,1) quantized by nvfp4_quantize (E2M1 codes,
+    UE4M3 scales per 16, fp32 tensor scales), bf16 out.  The peak is the
+    measured bf16 burst rate times the nominal dense FP4/BF16 ratio
+    (13.5 / 2.25 PF/s = 6)."""
+    import numpy as np
+    import torch
+
+    from grouped_gemm_top_gb300 import ops, synth
+    ops.moe_init(torch.device(device).index or 0)
+    sizes = synth.dirichlet_group_sizes(G, M_total, 0.3, seed)
+    gofs = np.concatenate([[0], np.cumsum((sizes + 127) // 128 * 128)])
+    M = int(gofs[-1])
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device=device)
+    src = synth.make_normal_bf16((M_total, K), seed + 100, device)
+    r = 0
+    for g, m in enumerate(sizes):
+        x[int(gofs[g]):int(gofs[g]) + int(m)] = src[r:r + int(m)]
+        r += int(m)
+    del src
+    gofs_t = torch.tensor(gofs, dtype=torch.int32, device=device)
+    aq, asf, ast = ops.nvfp4_quantize(x)
+    del x
+    W = synth.make_normal_bf16((G * N, K), seed + 200, device)
+    bq, bsf, bst = ops.nvfp4_quantize(W)
+    del W
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def launch():
+        ops.grouped_gemm_nvfp4(ops.MOE_GEMM_FWD, aq, asf, ast, bq, bsf, bst, gofs_t, G, M, N, K, d=d, err=err)
+
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, int(err.item())
+    ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    flops = 2.0 * M_total * N * K
+    byts = G * N * K * (0.5 + 1 / 16) + M_total * K * (0.5 + 1 / 16) + M_total * N * 2
+    peaks, psrc = _peaks()
+    fp4_peak = 6.0 * peaks["bf16_tflops"]
+    t_roof = max(flops / (fp4_peak * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+    return {"format": "nvfp4", "G": G, "M_total": M_total, "N": N, "K": K, "ms": round(ms, 4),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 1), "frac_flops": round(flops / (ms * 1e-3) / 1e12 / fp4_peak, 4),
+            "frac_roofline": round(t_roof / (ms * 1e-3), 4), "algorithmic_gb": round(byts / 1e9, 3),
+            "peak_tflops": fp4_peak, "peak_source": f"6 x {psrc} bf16 burst (nominal dense FP4/BF16 13.5/2.25)",
+            "empty_groups": int((sizes == 0).sum())}
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -612,6 +670,8 @@ def main():
     ap.add_argument("--gemm-point", nargs="+", type=int, metavar="G M_TOTAL N [K]",
                     help="time one standalone grouped GEMM fwd (K = N unless given) and print its line")
     ap.add_argument("--b-layout", default="gnk", choices=["ngk", "gnk"])
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="with --gemm-point / --sweep: the NVFP4 grouped GEMM (E2M1, UE4M3 scales per 16) instead")
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
     ap.add_argument("--compare", action="store_true",
                     help="time the grouped dropless step against a per-expert GEMM loop and capacity-based MoE on "
@@ -632,8 +692,11 @@ def main():
         else:
             pts = [(G, M, NK, NK) for G in (8, 64, 256) for NK in (2048, 7168) for M in (16384, 65536, 262144)]
         for i, (G, M, N, K) in enumerate(pts):
-            r = run_gemm_point(G, M, N, seed=i, steps=args.steps, warmup=max(args.warmup, 3), K=K,
-                               b_layout=args.b_layout)
+            if args.nvfp4:
+                r = run_gemm_point_nvfp4(G, M, N, K, seed=i, steps=args.steps, warmup=max(args.warmup, 3))
+            else:
+                r = run_gemm_point(G, M, N, seed=i, steps=args.steps, warmup=max(args.warmup, 3), K=K,
+                                   b_layout=args.b_layout)
             print(json.dumps({"sweep_point": r}), flush=True)
             import torch
             torch.cuda.empty_cache()

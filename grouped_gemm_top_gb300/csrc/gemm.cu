@@ -34,29 +34,37 @@ namespace gg {
 // Tile configurations.  BN = 128 keeps two accumulators in TMEM so the
 // epilogue of one tile overlaps the mainloop of the next; BN = 256 halves
 // the A re-reads but has a single accumulator.
-template <int BN_>
+// Operand formats of the 1-SM kernel.
+enum { FMT_MXF8 = 0, FMT_BF16 = 1, FMT_NVF4 = 2 };
+
+template <int BN_, int FMT = FMT_MXF8>
 struct Cfg {
     static constexpr int BN = BN_;
     static constexpr int NACC = BN_ == 128 ? 2 : 1;
     static constexpr int STAGES = BN_ == 128 ? 6 : 4;
     static constexpr int A_STAGE = BM * BK;
     static constexpr int B_STAGE = BN_ * BK;
-    static constexpr int SFB_STAGE = (BN_ / 128) * 512;
-    static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
-    // TMEM: accumulators at [0, NACC*BN); stage s scales at SF0 + 16 s (A: 4
-    // columns, B: BN/32 columns), so a stage's scale columns are rewritten
-    // only after the MMAs that read them completed.
+    // scale bytes per 128 rows and k-step: MXFP8 one 512-byte atom (4
+    // blocks of 32), NVFP4 four atoms (16 blocks of 16 E2M1 values: a
+    // 128-byte k-step holds 256 of them)
+    static constexpr int SFA_STG = FMT == FMT_NVF4 ? 4 * SFA_STAGE : SFA_STAGE;
+    static constexpr int SFB_STAGE = (BN_ / 128) * SFA_STG;
+    static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STG + SFB_STAGE;
+    // TMEM: accumulators at [0, NACC*BN); stage s scales at SF0 + SF_COLS s
+    // (MXFP8: A 4 columns, B BN/32; NVFP4: A 16, B BN/8), so a stage's scale
+    // columns are rewritten only after the MMAs that read them completed.
+    static constexpr uint32_t SF_COLS = FMT == FMT_NVF4 ? 16 + 16 * (BN_ / 128) : TMEM_SF_STRIDE;
     static constexpr uint32_t SF0 = NACC * BN_;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STG;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
     static constexpr int NBAR = 2 * STAGES + 2 * NACC + 1;
     static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
     static constexpr int OFF_GOFS = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = OFF_GOFS + (MAX_G + 1) * 4 + 1024;   // + alignment slack
-    static_assert(SF0 + STAGES * TMEM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
+    static_assert(SF0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -99,13 +107,18 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
 // --------------------------------------------------------------- kernel ----
 
 // EPI: the epilogue (moe_epilogue_t), fixed at compile time so each
-// instance keeps only its own epilogue's registers.  BF16: plain bf16
-// operands (tcgen05.mma kind::f16, no scale factors; 64 elements per
-// 128-byte k-step), for the router's dense GEMMs.
-template <int BN, int EPI, bool BF16 = false>
+// instance keeps only its own epilogue's registers.  FMT: FMT_MXF8 (E4M3
+// with E8M0 scales per 32, kind::mxf8f6f4); FMT_BF16 (plain bf16 operands,
+// kind::f16, no scale factors; 64 elements per 128-byte k-step), for the
+// router's dense GEMMs; FMT_NVF4 (packed E2M1 with UE4M3 scales per 16 and
+// per-tensor fp32 scales, kind::mxf4nvf4; 256 elements per 128-byte
+// k-step, plain epilogues only).
+template <int BN, int EPI, int FMT = FMT_MXF8>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, FMT>;
+    constexpr bool BF16 = FMT == FMT_BF16, NVF4 = FMT == FMT_NVF4;
+    static_assert(!NVF4 || (BN == 256 && (EPI == MOE_EPI_NONE || EPI == MOE_EPI_NONE_F32)), "NVFP4 instances");
     constexpr int STAGES = C::STAGES, NACC = C::NACC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -195,16 +208,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t fb = full_bar(stage);
                 mbar_expect_tx(fb, BF16 ? (uint32_t)(C::A_STAGE + C::B_STAGE) : C::STAGE_TX);
                 tma_load_2d(smem_u32(sA + stage * C::A_STAGE), &tmA, kx, (int)ti.a_row, fb);
-                const uint8_t* sfa = p.a_sf + kg * p.a_sf_kstride + (ti.a_row / 128) * 512;
+                const uint8_t* sfa = p.a_sf + kg * p.a_sf_kstride + (ti.a_row / 128) * C::SFA_STG;
                 const uint8_t* sfb = p.b_sf + (int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride;
-                if constexpr (!BF16) bulk_load(smem_u32(sSFA + stage * SFA_STAGE), sfa, 512, fb);
+                if constexpr (!BF16) bulk_load(smem_u32(sSFA + stage * C::SFA_STG), sfa, C::SFA_STG, fb);
 #pragma unroll
                 for (int h = 0; h < BN / 128; ++h) {
                     const int brow = ti.b_row + 128 * h;
                     tma_load_3d(smem_u32(sB + stage * C::B_STAGE + h * 16384), &tmB, kx, brow, gB, fb);
                     if constexpr (!BF16)
-                        bulk_load(smem_u32(sSFB + stage * C::SFB_STAGE + h * 512), sfb + (int64_t)(brow / 128) * 512,
-                                  512, fb);
+                        bulk_load(smem_u32(sSFB + stage * C::SFB_STAGE + h * C::SFA_STG),
+                                  sfb + (int64_t)(brow / 128) * C::SFA_STG, C::SFA_STG, fb);
                 }
                 pend[stage] = (int)phase;
                 if (++stage == STAGES) {
@@ -247,10 +260,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t t_sfa = tmem_base + C::SF0 + TMEM_SF_STRIDE * stage;
-                const uint32_t t_sfb = t_sfa + 4;
-                if constexpr (!BF16) {
-                    tc_cp_sf(t_sfa, desc_sf(smem_u32(sSFA + stage * SFA_STAGE)));
+                const uint32_t t_sfa = tmem_base + C::SF0 + C::SF_COLS * stage;
+                const uint32_t t_sfb = t_sfa + (NVF4 ? 16 : 4);
+                if constexpr (NVF4) {
+                    // atom j (64 K-elements) of A -> columns t_sfa + 4j; atom
+                    // j of B rows [128h, 128h + 128) -> t_sfb + 8j + 4h, so
+                    // the MMA over K-elements [64j, 64j + 64) reads A's 4
+                    // columns at t_sfa + 4j and B's 8 at t_sfb + 8j
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        tc_cp_sf(t_sfa + 4 * j, desc_sf(smem_u32(sSFA + stage * C::SFA_STG + 512 * j)));
+#pragma unroll
+                        for (int h = 0; h < BN / 128; ++h)
+                            tc_cp_sf(t_sfb + 8 * j + 4 * h,
+                                     desc_sf(smem_u32(sSFB + stage * C::SFB_STAGE + h * C::SFA_STG + 512 * j)));
+                    }
+                } else if constexpr (!BF16) {
+                    tc_cp_sf(t_sfa, desc_sf(smem_u32(sSFA + stage * C::SFA_STG)));
 #pragma unroll
                     for (int h = 0; h < BN / 128; ++h)
                         tc_cp_sf(t_sfb + 4 * h, desc_sf(smem_u32(sSFB + stage * C::SFB_STAGE + 512 * h)));
@@ -260,10 +286,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 32; ++kk) {
                     // advance 32 bytes along K inside the 128-byte swizzled row
-                    // (32 fp8 elements with block scales, or 16 bf16)
+                    // (32 fp8 elements with block scales, 16 bf16, or 64
+                    // packed E2M1 elements)
                     if constexpr (BF16)
                         tc_mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
                                     make_idesc_bf16<BN>(), (ks | kk) != 0 ? 1u : 0u);
+                    else if constexpr (NVF4)
+                        tc_mma_nvf4(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                                    make_idesc_nvf4<BN>(), t_sfa + 4 * kk, t_sfb + 8 * kk, (ks | kk) != 0 ? 1u : 0u);
                     else
                         tc_mma(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
                                make_idesc<BN>((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
@@ -328,7 +358,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if constexpr (EPI == MOE_EPI_SWIGLU_BWD) {
                 epilogue_swiglu_bwd<BN>(p, tacc, row, ti.nt, half, release, apre);
             } else if constexpr (BN == 256) {
-                epilogue_tile_staged<EPI>(p, tacc, row, ti.nt, half, release);
+                epilogue_tile_staged<EPI, NVF4>(p, tacc, row, ti.nt, half, release);
             } else {
                 epilogue_tile<BN, EPI>(p, tacc, row, ti.nt, half);
                 release();
@@ -374,9 +404,15 @@ cudaError_t gemm_set_attributes() {
                               set_attr_1sm<128, MOE_EPI_SWIGLU_BWD>(), set_attr_1sm<128, MOE_EPI_NONE_F32>(),
                               set_attr_1sm<256, MOE_EPI_NONE>(),     set_attr_1sm<256, MOE_EPI_SWIGLU>(),
                               set_attr_1sm<256, MOE_EPI_SWIGLU_BWD>(), set_attr_1sm<256, MOE_EPI_NONE_F32>(),
-                              cudaFuncSetAttribute(gg::k_grouped_gemm<256, MOE_EPI_NONE_F32, true>,
+                              cudaFuncSetAttribute(gg::k_grouped_gemm<256, MOE_EPI_NONE_F32, gg::FMT_BF16>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   gg::Cfg<256>::SMEM_BYTES)};
+                                                   gg::Cfg<256, gg::FMT_BF16>::SMEM_BYTES),
+                              cudaFuncSetAttribute(gg::k_grouped_gemm<256, MOE_EPI_NONE, gg::FMT_NVF4>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   gg::Cfg<256, gg::FMT_NVF4>::SMEM_BYTES),
+                              cudaFuncSetAttribute(gg::k_grouped_gemm<256, MOE_EPI_NONE_F32, gg::FMT_NVF4>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   gg::Cfg<256, gg::FMT_NVF4>::SMEM_BYTES)};
     for (cudaError_t e : es)
         if (e != cudaSuccess) return e;
     return gemm_set_attributes_2sm();
@@ -690,8 +726,68 @@ extern "C" moe_status_t gemm_bf16_nt(const void* a, const void* b, int64_t M, in
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     const int64_t tiles = (M / BM) * p.n_tiles;
     const int grid = (int)std::min<int64_t>(tiles, sms);
-    k_grouped_gemm<256, MOE_EPI_NONE_F32, true><<<grid, THREADS, Cfg<256>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB,
-                                                                                                          p);
+    k_grouped_gemm<256, MOE_EPI_NONE_F32, FMT_BF16>
+        <<<grid, THREADS, Cfg<256, FMT_BF16>::SMEM_BYTES, (cudaStream_t)stream>>>(tmA, tmB, p);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+
+extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uint8_t* a_sf, const float* a_scale,
+                                           const uint8_t* b, const uint8_t* b_sf, const float* b_scale,
+                                           const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
+                                           void* d, int32_t* err, void* stream) {
+    using namespace gg;
+    MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(epilogue == MOE_EPI_NONE || epilogue == MOE_EPI_NONE_F32, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(a && a_sf && a_scale && b && b_sf && b_scale && gofs && d, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(G >= 1 && G <= MAX_G && M > 0 && N > 0 && K > 0, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(M % 128 == 0 && N % 256 == 0 && K % 256 == 0 && M <= 0x7FFFFF80LL && K <= (1LL << 30),
+                MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(moe_aligned16(a) && moe_aligned16(b) && moe_aligned16(a_sf) && moe_aligned16(b_sf) &&
+                    (reinterpret_cast<uintptr_t>(d) & 31) == 0 && (reinterpret_cast<uintptr_t>(a_scale) & 3) == 0 &&
+                    (reinterpret_cast<uintptr_t>(b_scale) & 3) == 0,
+                MOE_ERR_ALIGNMENT);
+    MOE_REQUIRE(device_initialized() && g_encode != nullptr, MOE_ERR_NOT_INITIALIZED);
+    // packed E2M1 rows seen as bytes: K/2 bytes per row, 128-byte k-steps
+    const int64_t Kb = K / 2;
+    CUtensorMap tmA, tmB;
+    const uint64_t da[2] = {(uint64_t)Kb, (uint64_t)M}, sa[1] = {(uint64_t)Kb};
+    const uint64_t db[3] = {(uint64_t)Kb, (uint64_t)N, (uint64_t)G}, sb[2] = {(uint64_t)Kb, (uint64_t)N * Kb};
+    MOE_REQUIRE(make_map(&tmA, a, 2, da, sa) && make_map(&tmB, b, 3, db, sb), MOE_ERR_CUDA);
+    Params p{};
+    p.mode = mode;
+    p.epi = epilogue;
+    p.G = G;
+    p.N = N;
+    p.M = M;
+    p.K = Kb;
+    p.gofs = gofs;
+    p.a_sf = a_sf;
+    p.b_sf = b_sf;
+    // NVFP4 scale atoms: [k-step][row tile][4 x 512]; B's rows are the G*N
+    // rows of the [G][N] weight operand
+    p.a_sf_kstride = (M / 128) * 2048;
+    p.b_sf_kstride = (int64_t)G * (N / 128) * 2048;
+    p.b_sf_gstride = (int64_t)(N / 128) * 2048;
+    p.alpha_a = a_scale;
+    p.alpha_b = b_scale;
+    p.d = (__nv_bfloat16*)d;
+    p.err = err;
+    p.timeout_ns = 2000000000ull;
+    p.band = 8;
+    if (const char* e = getenv("MOE_GEMM_BAND")) p.band = std::max(1, atoi(e));
+    p.n_tiles = N / 256;
+    p.n_out = N;
+    p.ldd = N;
+    const int sms = device_sm_count();
+    MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
+    const int64_t tiles = (M / BM) * p.n_tiles;
+    const int grid = (int)std::min<int64_t>(tiles, sms);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (epilogue == MOE_EPI_NONE_F32)
+        k_grouped_gemm<256, MOE_EPI_NONE_F32, FMT_NVF4><<<grid, THREADS, Cfg<256, FMT_NVF4>::SMEM_BYTES, s>>>(tmA, tmB, p);
+    else
+        k_grouped_gemm<256, MOE_EPI_NONE, FMT_NVF4><<<grid, THREADS, Cfg<256, FMT_NVF4>::SMEM_BYTES, s>>>(tmA, tmB, p);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }

@@ -47,6 +47,10 @@ struct Params {
     uint8_t* hs_r;
     uint8_t* hq_c;
     uint8_t* hs_c;
+    // NVFP4 operands: the per-tensor fp32 scales of A and B (device
+    // pointers); the epilogue multiplies the accumulator by their product
+    const float* alpha_a;
+    const float* alpha_b;
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -187,6 +191,25 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma.kind::mxf4nvf4 with E2M1 A and B
+// (format 1), UE4M3 block scales (scale format 0, scale_vec::4X: four
+// 16-element blocks per K = 64 MMA, so the scale ids are 0), fp32 D, both
+// K-major, M = 128, N = BN.
+template <int BN>
+__device__ __forceinline__ uint32_t make_idesc_nvf4() {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");
 }
 
@@ -409,9 +432,21 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tacc, in
 // bf16 (two TMEM loads in flight per wait), calls release() so the MMA warp
 // can reuse TMEM, and only then writes global memory, overlapped with the
 // next tile's MMAs.  SwiGLU-backward has its own pipelined epilogue below.
-template <int EPI, typename Release>
+// SCALED (NVFP4 operands, MOE_EPI_NONE / MOE_EPI_NONE_F32 only): every
+// accumulator is multiplied by alpha_a * alpha_b before it is stored.
+template <bool SCALED>
+__device__ __forceinline__ void scale_acc(const Params& p, uint32_t* r) {
+    if constexpr (SCALED) {
+        const float al = __fmul_rn(__ldg(p.alpha_a), __ldg(p.alpha_b));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), al));
+    }
+}
+
+template <int EPI, bool SCALED = false, typename Release>
 __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t tacc, int64_t row, int nt, int half,
                                                      Release release) {
+    static_assert(!SCALED || EPI == MOE_EPI_NONE || EPI == MOE_EPI_NONE_F32, "scaled epilogue: plain outputs only");
     uint32_t ra[32], rb[32];
     if constexpr (EPI == MOE_EPI_SWIGLU) {
         // units u = 2*half, 2*half+1: gate columns [128q + 32c, +32) and up
@@ -477,6 +512,8 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
             tmem_ld32_issue(tacc + 128 * half + 32 * (c + 1), rb);
             tmem_wait_ld();
             if (c == 2) release();
+            scale_acc<SCALED>(p, ra);
+            scale_acc<SCALED>(p, rb);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (col0 + 32 * c + 8 * q < p.n_out)
@@ -495,6 +532,8 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
             tmem_ld32_issue(tacc + 128 * half + 32 * (c + 1), rb);
             tmem_wait_ld();
             if (c == 2) release();
+            scale_acc<SCALED>(p, ra);
+            scale_acc<SCALED>(p, rb);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 pk[16 * c + i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));

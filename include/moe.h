@@ -438,6 +438,74 @@ MOE_API moe_status_t moe_route_topk_noalloc(const float* logits, int T, int E, i
                                             int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                                             int32_t* err, void* stream);
 
+/*
+ * ---------------------------------------------------------------- NVFP4 --
+ * [CH1] §1.1 precision table: FP4 is 4 bits, 1 sign + 2 exponent + 1
+ * mantissa (E2M1, values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives);
+ * "低精度格式的缩放机制": NVFP4 has two scales, an E4M3 scale per small
+ * block and one FP32 scale per tensor.  [TE-JAX] "What is the training
+ * performance impact…": NVFP4 is planned next for the expert GEMMs.
+ * Block size 16 along the contraction axis (the tensor cores' NVFP4 MMA).
+ *
+ * Code layout: row-major [rows, cols / 2] bytes; element 2j of a row in the
+ * low nibble of byte j, element 2j+1 in the high nibble.
+ * Scale layout: 16-element block b of row r lives at byte
+ *   ((b / 16) * (rows / 128) + r / 128) * 2048 + ((b / 4) % 4) * 512
+ *   + (r % 32) * 16 + ((r / 32) % 4) * 4 + b % 4,
+ * i.e. per 256-column k-step and 128-row tile four 512-byte atoms (one per
+ * 64 columns) in the tensor cores' scale-factor layout.
+ */
+
+/* nvfp4_sf_bytes -- bytes of the scale array of a [rows, cols] matrix
+ * (rows * cols / 16), or -1 unless rows % 128 == 0 and cols % 256 == 0. */
+MOE_API int64_t nvfp4_sf_bytes(int64_t rows, int cols);
+
+/*
+ * nvfp4_quantize -- two-level NVFP4 of a bf16 matrix, blocks of 16 along
+ * each row.  In fp32, each step rounded to nearest:
+ *   amax = max |src|; s_t = amax / 2688; enc = 2688 / amax (2688 = 6 * 448)
+ *   per block: t_b = (amax_b / 6) * enc; scale byte = E4M3(t_b), nearest,
+ *              ties to even, saturating at 448; r_b = enc / E4M3 value
+ *   per element: code = E2M1(x * r_b), nearest, ties to even, saturating at 6
+ * so that x ~ E2M1(code) * scale * s_t.  A block whose scale byte is 0 gets
+ * zero codes; an all-zero matrix gives s_t = 0.
+ *   src           [rows, cols] bf16 row-major, 16-byte aligned; rows % 128
+ *                 == 0, rows / 128 <= 65535, cols % 256 == 0.
+ *   codes         [rows, cols / 2] bytes (layout above), written.
+ *   scales        nvfp4_sf_bytes(rows, cols) bytes (layout above), written.
+ *   tensor_scale  one float (device), written with s_t.
+ *   amax_ws       one uint32 of device scratch (zeroed and used by the call;
+ *                 calls that may overlap on the GPU need their own word).
+ * Two launches (the amax reduction, then the quantization) after a 4-byte
+ * memset; no allocation, no host sync.  err is unused (no device-side
+ * checks); host-checkable errors are returned.
+ */
+MOE_API moe_status_t nvfp4_quantize(const void* src, int64_t rows, int cols, uint8_t* codes, uint8_t* scales,
+                                    float* tensor_scale, uint32_t* amax_ws, int32_t* err, void* stream);
+
+/*
+ * grouped_gemm_nvfp4 -- the grouped GEMM of grouped_gemm_mxfp8 (modes FWD
+ * and DGRAD: D[r, :] = A[r, :] * B_g^T for rows r of group g) with NVFP4
+ * operands on the tensor cores (tcgen05.mma kind::mxf4nvf4, UE4M3 block
+ * scales, fp32 accumulation); the epilogue multiplies by a_scale * b_scale.
+ *   a, a_sf, a_scale   nvfp4_quantize output for A [M, K].
+ *   b, b_sf, b_scale   nvfp4_quantize output for the [G * N, K] matrix whose
+ *                      rows g*N .. g*N+N-1 are B_g ([G][N][K]; one tensor
+ *                      scale for every expert's weights).
+ *   gofs, G            as grouped_gemm_mxfp8 (0 = gofs[0], monotone,
+ *                      multiples of 128, gofs[G] <= M; device-checked into
+ *                      err as MOE_ERR_BAD_OFFSETS).
+ *   M % 128 == 0, N % 256 == 0, K % 256 == 0.
+ *   epilogue           MOE_EPI_NONE (d bf16 [M, N]) or MOE_EPI_NONE_F32 (d
+ *                      fp32 [M, N]); d 32-byte aligned.  Rows >= gofs[G]
+ *                      are not written.
+ * Every wait inside the kernel is bounded (MOE_ERR_DEVICE_TIMEOUT in err).
+ */
+MOE_API moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uint8_t* a_sf, const float* a_scale,
+                                        const uint8_t* b, const uint8_t* b_sf, const float* b_scale,
+                                        const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
+                                        void* d, int32_t* err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
