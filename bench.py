@@ -35,6 +35,10 @@ WORKLOADS = {
     "deepseek-v3-small": dict(T=1536, d=7168, E=16, k=8, f=2048, score="sigmoid", normalize=True, zipf=None,
                               desc="DeepSeek-V3 expert shapes with 16 experts and 1536 tokens (same 768 rows per "
                                    "expert; profiling case): d=7168, top-8 sigmoid, f=2048"),
+    "deepseek-v3-zipf": dict(T=24576, d=7168, E=256, k=8, f=2048, score="sigmoid", normalize=True, zipf=1.2,
+                             desc="DeepSeek-V3-shaped layer fwd+bwd with Zipf(1.2)-skewed routing (logit bias "
+                                  "-1.2 ln rank_e, rank a seeded permutation): T=24576, d=7168, E=256, top-8 "
+                                  "sigmoid normalised, f=2048"),
     "mixtral": dict(T=8192, d=4096, E=8, k=2, f=14336, score="softmax", normalize=True, zipf=None,
                     desc="Mixtral-shaped layer fwd+bwd: T=8192, d=4096, E=8, top-2 softmax, f=14336"),
     "tiny": dict(T=256, d=512, E=8, k=2, f=256, score="softmax", normalize=True, zipf=None,
@@ -575,6 +579,64 @@ def run_hbm_probe(nbytes=4 << 30, reps=10):
             "method": "torch fill_ of 4 GB (write-only) and copy_ of 2 GB into 2 GB (read+write bytes)"}
 
 
+def run_seeds(args):
+    """The whole step captured once in a CUDA graph and replayed over
+    args.seeds routing draws (seed i: the workload's logits with seed i, so
+    for the Zipf workload a different expert order and skew each time);
+    only the logits buffer changes between seeds, the graph does not (the
+    group sizes never reach the host).  Per seed: replay time (CUDA events
+    over args.steps replays after one warm replay), the largest expert's
+    share of the tokens and the number of experts with no rows.  Reports
+    the median over seeds."""
+    import torch
+
+    from grouped_gemm_top_gb300 import build as _b
+    if not os.path.exists(_b.LIB):
+        _b.build()
+    from grouped_gemm_top_gb300 import synth
+    from grouped_gemm_top_gb300.layer import MoELayer
+
+    w = WORKLOADS[args.workload]
+    T, d, E, k, f = w["T"], w["d"], w["E"], w["k"], w["f"]
+    dev = "cuda:0"
+    stream = torch.cuda.current_stream()
+    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev)
+    inp = synth.make_layer_inputs(T, d, E, f, dev, zipf_s=w["zipf"])
+    L.set_weights(inp["W1"], inp["W2"])
+    L.x.copy_(inp["x"])
+    L.dout.copy_(inp["dout"])
+    L.logits.copy_(inp["logits"])
+    del inp
+    for _ in range(3):
+        L.step_()
+    L.capture()
+    flops = L.flops_per_step()
+    per_seed = []
+    with ClockSampler(0) as clk:
+        for seed in range(args.seeds):
+            L.logits.copy_(synth.make_logits(T, E, synth.SEED_LOGITS + seed, dev, w["zipf"]))
+            L.replay()
+            torch.cuda.synchronize()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(args.steps):
+                L.replay()
+            s1.record(stream)
+            torch.cuda.synchronize()
+            L.check_err()
+            counts = L.counts.cpu()
+            ms = s0.elapsed_time(s1) / args.steps
+            per_seed.append({"seed": seed, "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                             "top_expert_token_share": round(int(counts.max()) / T, 4),
+                             "empty_experts": int((counts == 0).sum())})
+    ms_sorted = sorted(p["ms"] for p in per_seed)
+    med = statistics.median(ms_sorted)
+    return {"seeds": {"workload": w["desc"], "n_seeds": args.seeds, "replays_per_seed": args.steps,
+                      "median_ms": round(med, 4), "median_tflops": round(flops / (med * 1e-3) / 1e12, 1),
+                      "min_ms": ms_sorted[0], "max_ms": ms_sorted[-1], "per_seed": per_seed,
+                      "clocks": clk.summary(), "timing": "one CUDA graph of the whole fwd+bwd step, replayed"}}
+
+
 def run_compare(args, capacity_factors=(1.0, 1.25)):
     """The grouped dropless step against the prior-art ways of running the
     same layer (grouped_gemm_top_gb300.comparators): a loop of per-expert
@@ -673,6 +735,9 @@ def main():
     ap.add_argument("--nvfp4", action="store_true",
                     help="with --gemm-point / --sweep: the NVFP4 grouped GEMM (E2M1, UE4M3 scales per 16) instead")
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
+    ap.add_argument("--seeds", type=int, default=0, metavar="S",
+                    help="replay the captured step over S routing seeds (e.g. --workload deepseek-v3-zipf "
+                         "--seeds 20) and print the median; one line")
     ap.add_argument("--compare", action="store_true",
                     help="time the grouped dropless step against a per-expert GEMM loop and capacity-based MoE on "
                          "the same workload and print one line")
@@ -684,6 +749,9 @@ def main():
         return
     if args.compare:
         print(json.dumps(run_compare(args)), flush=True)
+        return
+    if args.seeds:
+        print(json.dumps(run_seeds(args)), flush=True)
         return
     if args.gemm_point or args.sweep:
         if args.gemm_point:
