@@ -42,7 +42,7 @@ __all__ = [
     "grouped_gemm", "grouped_gemm_wgrad", "swiglu", "swiglu_bwd", "combine",
     "combine_bwd", "route_bwd", "layer_forward", "layer_backward", "router_logits", "router_backward",
     "append_shared", "NVFP4_BLOCK", "E2M1_MAX", "e2m1_value", "E2M1_VALUES", "e2m1_encode", "nvfp4_tensor_scale",
-    "nvfp4_quantize_rows", "nvfp4_dequantize_rows",
+    "nvfp4_quantize_rows", "nvfp4_dequantize_rows", "nvfp4_quantize_cols_grouped", "nvfp4_dequantize_cols",
 ]
 
 MXFP8_BLOCK = 32          # [CH1] "低精度格式的缩放机制": one scale per group of 32
@@ -321,6 +321,37 @@ def nvfp4_dequantize_rows(codes, scales, st):
     vals = E2M1_VALUES[codes.astype(np.int64)].reshape(R, C // NVFP4_BLOCK, NVFP4_BLOCK)
     sb = E4M3_VALUES[np.asarray(scales).astype(np.int64)]
     return (vals * sb[..., None]).reshape(R, C) * float(st)
+
+
+def nvfp4_quantize_cols_grouped(x, offsets):
+    """Group-aware columnwise NVFP4 (the wgrad operands): blocks of 16
+    consecutive rows of ONE group, starting at the group's first row, a
+    group's tail block padded with zeros; one tensor scale for the whole
+    matrix (the same s_t as the rowwise quantization of x).
+
+    Reading: the group-aware layout of the MXFP8 columnwise quantization with
+    the NVFP4 block of 16 (group g at padded_offsets[g] = sum_{h<g}
+    ceil16(m_h)); every other step is nvfp4_quantize_rows applied to the
+    transposed padded matrix, whose zero padding changes no block amax.
+
+    Returns codes [C, Rp] u8 (one code per element, transposed), scales
+    [C, Rp/16] u8, s_t and padded_offsets [G+1]."""
+    x = np.asarray(x, dtype=np.float64)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    C = x.shape[1]
+    sizes = offsets[1:] - offsets[:-1]
+    padded = np.concatenate([[0], np.cumsum((sizes + NVFP4_BLOCK - 1) // NVFP4_BLOCK * NVFP4_BLOCK)])
+    Rp = int(padded[-1])
+    xp = np.zeros((Rp, C), dtype=np.float64)
+    for g in range(len(sizes)):
+        xp[padded[g]:padded[g] + sizes[g]] = x[offsets[g]:offsets[g + 1]]
+    codes, scales, st = nvfp4_quantize_rows(xp.T)
+    return codes, scales, st, padded
+
+
+def nvfp4_dequantize_cols(codes_t, scales_t, st):
+    """Inverse of the columnwise layout: returns the [Rp, C] matrix."""
+    return nvfp4_dequantize_rows(codes_t, scales_t, st).T
 
 
 # --------------------------------------------------------------------------

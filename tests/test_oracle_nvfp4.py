@@ -115,3 +115,39 @@ def test_nvfp4_blocks_run_along_rows():
 def test_nvfp4_zero_tensor():
     q, s, st = O.nvfp4_quantize_rows(np.zeros((2, 32)))
     assert st == 0 and not q.any() and not s.any()
+
+
+def test_nvfp4_cols_grouped_reduces_to_rowwise_of_the_transpose():
+    """With every group a multiple of 16 rows there is no padding: the
+    columnwise codes are the rowwise codes of x transposed, with the same
+    tensor scale as the rowwise quantization of x."""
+    rng = np.random.default_rng(21)
+    x = _bf16(rng.standard_normal((96, 32)) * np.exp(rng.uniform(-2, 2, (96, 1))))
+    q, s, st, padded = O.nvfp4_quantize_cols_grouped(x, [0, 32, 32, 96])
+    qr, sr, st_r = O.nvfp4_quantize_rows(x.T)
+    assert np.array_equal(padded, [0, 32, 32, 96])
+    assert np.array_equal(q, qr) and np.array_equal(s, sr) and st == st_r
+    assert st == O.nvfp4_quantize_rows(x)[2]
+
+
+def test_nvfp4_cols_grouped_blocks_restart_at_group_starts():
+    """A group of 20 rows takes two blocks (16 + 4 rows, zero-padded to 16);
+    the next group starts a fresh block: scaling its rows changes only its
+    blocks' scale bytes, and the padding rows dequantize to zero."""
+    rng = np.random.default_rng(8)
+    x = _bf16(rng.standard_normal((36, 16)))
+    x[0, 0] = 64.0                                   # the tensor maximum sits in group 0
+    q, s, st, padded = O.nvfp4_quantize_cols_grouped(x, [0, 20, 36])
+    assert np.array_equal(padded, [0, 32, 48]) and q.shape == (16, 48) and s.shape == (16, 3)
+    back = O.nvfp4_dequantize_cols(q, s, st)
+    assert not back[20:32].any()                     # padding of group 0's tail block
+    y = x.copy()
+    y[20:36] *= 0.5                                  # group 1 only (exact)
+    _, s2, st2, _ = O.nvfp4_quantize_cols_grouped(y, [0, 20, 36])
+    assert st2 == st
+    assert np.array_equal(s2[:, :2], s[:, :2]) and not np.array_equal(s2[:, 2], s[:, 2])
+    # every element within one unit (s_b * s_t) of its value
+    unit = np.repeat(O.E4M3_VALUES[s.astype(np.int64)], 16, axis=1).T * float(st)
+    xpad = np.zeros((48, 16))
+    xpad[:20], xpad[32:48] = x[:20], x[20:36]
+    assert np.all(np.abs(back - xpad) <= unit * (1 + 1e-9))
