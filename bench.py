@@ -500,6 +500,67 @@ def run_gemm_point_nvfp4(G, M_total, N, K, seed=0, steps=10, warmup=3, device="c
             "empty_groups": int((sizes == 0).sum())}
 
 
+def run_wgrad_point(G, M_total, Mo, No, seed=0, steps=10, warmup=3, device="cuda:0"):
+    """Standalone weight-gradient GEMM dW_g = X_g^T dY_g over Dirichlet(0.3)
+    groups of M_total rows (X [rows, Mo], dY [rows, No] ~ N(0,1), rows laid
+    out at 128-row group offsets), in MXFP8 (group-aware columnwise MXFP8
+    operands) and in NVFP4 (group-aware columnwise NVFP4): one line with
+    both.  Peaks as for the fwd points (2x / 6x the measured bf16 burst)."""
+    import numpy as np
+    import torch
+
+    from grouped_gemm_top_gb300 import ops, synth
+    ops.moe_init(torch.device(device).index or 0)
+    sizes = synth.dirichlet_group_sizes(G, M_total, 0.3, seed)
+    gofs = np.concatenate([[0], np.cumsum((sizes + 127) // 128 * 128)])
+    rows = (int(gofs[-1]) + 255) // 256 * 256
+    gofs_t = torch.tensor(gofs, dtype=torch.int32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def grouped(cols, sd):
+        x = torch.zeros((rows, cols), dtype=torch.bfloat16, device=device)
+        src = synth.make_normal_bf16((M_total, cols), sd, device)
+        r = 0
+        for g, m in enumerate(sizes):
+            x[int(gofs[g]):int(gofs[g]) + int(m)] = src[r:r + int(m)]
+            r += int(m)
+        return x
+
+    X, Y = grouped(Mo, seed + 300), grouped(No, seed + 400)
+    _, _, xq8, xs8 = ops.mxfp8_gather_quantize(X, gofs_t, G, rows, None, 1, None, False, True, err=err)
+    _, _, yq8, ys8 = ops.mxfp8_gather_quantize(Y, gofs_t, G, rows, None, 1, None, False, True, err=err)
+    xq4, xs4, xt4 = ops.nvfp4_quantize_cols(X, gofs_t, G, err=err)
+    yq4, ys4, yt4 = ops.nvfp4_quantize_cols(Y, gofs_t, G, err=err)
+    del X, Y
+    d = torch.empty((G, Mo, No), dtype=torch.bfloat16, device=device)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, int(err.item())
+        return a.elapsed_time(b) / steps
+
+    ms8 = timed(lambda: ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, xq8, xs8, yq8, ys8, 0, gofs_t, G, Mo, No, rows,
+                                               d=d, err=err))
+    ms4 = timed(lambda: ops.grouped_gemm_nvfp4(ops.MOE_GEMM_WGRAD, xq4, xs4, xt4, yq4, ys4, yt4, gofs_t, G, Mo, No,
+                                               rows, d=d, err=err))
+    flops = 2.0 * M_total * Mo * No
+    peaks, psrc = _peaks()
+    return {"G": G, "M_total": M_total, "M": Mo, "N": No, "mxfp8_ms": round(ms8, 4),
+            "mxfp8_tflops": round(flops / (ms8 * 1e-3) / 1e12, 1), "nvfp4_ms": round(ms4, 4),
+            "nvfp4_tflops": round(flops / (ms4 * 1e-3) / 1e12, 1),
+            "nvfp4_frac_of_fp4_peak": round(flops / (ms4 * 1e-3) / 1e12 / (6.0 * peaks["bf16_tflops"]), 4),
+            "mxfp8_frac_of_mxfp8_peak": round(flops / (ms8 * 1e-3) / 1e12 / (2.0 * peaks["bf16_tflops"]), 4),
+            "output_gb": round(G * Mo * No * 2 / 1e9, 3), "peak_source": f"{psrc} bf16 burst x 2 (MXFP8) / x 6 (FP4)"}
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -732,6 +793,8 @@ def main():
     ap.add_argument("--gemm-point", nargs="+", type=int, metavar="G M_TOTAL N [K]",
                     help="time one standalone grouped GEMM fwd (K = N unless given) and print its line")
     ap.add_argument("--b-layout", default="gnk", choices=["ngk", "gnk"])
+    ap.add_argument("--wgrad-point", nargs=4, type=int, metavar=("G", "M_TOTAL", "M", "N"),
+                    help="time the weight-gradient grouped GEMM in MXFP8 and in NVFP4 and print one line")
     ap.add_argument("--nvfp4", action="store_true",
                     help="with --gemm-point / --sweep: the NVFP4 grouped GEMM (E2M1, UE4M3 scales per 16) instead")
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
@@ -752,6 +815,11 @@ def main():
         return
     if args.seeds:
         print(json.dumps(run_seeds(args)), flush=True)
+        return
+    if args.wgrad_point:
+        G, Mt, Mo, No = args.wgrad_point
+        print(json.dumps({"wgrad_point": run_wgrad_point(G, Mt, Mo, No, steps=args.steps,
+                                                         warmup=max(args.warmup, 3))}), flush=True)
         return
     if args.gemm_point or args.sweep:
         if args.gemm_point:

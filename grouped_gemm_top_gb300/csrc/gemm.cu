@@ -76,10 +76,15 @@ struct Tile {
     int nk;           // number of k-steps
     int64_t out_row;  // first output row
     int nt;           // tile index along N
+    int kq;           // NVFP4 WGRAD: 64-row MMAs in the last k-step (4, or 2 for a group ending half-way)
 };
 
-template <int BN>
+// NVF4: NVFP4 WGRAD counts its contraction in rows (k-steps of 256 rows,
+// 128 packed bytes), so kbeg is the group's first row and a group whose
+// row count is an odd multiple of 128 ends with a half k-step.
+template <int BN, bool NVF4 = false>
 __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int64_t total_mt, int64_t t, Tile& ti) {
+    ti.kq = 4;
     int64_t mt;
     int nt;
     if (p.mode != MOE_GEMM_WGRAD) {
@@ -96,8 +101,15 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
         band_decode(t - (int64_t)g * tpg, p.m_tiles, p.n_tiles, p.band, mt, nt);
         ti.g = g;
         ti.a_row = mt * BM;
-        ti.kbeg = s_gofs[g] / BK;
-        ti.nk = (s_gofs[g + 1] - s_gofs[g]) / BK;
+        if constexpr (NVF4) {
+            const int rows = s_gofs[g + 1] - s_gofs[g];
+            ti.kbeg = s_gofs[g];
+            ti.nk = (rows + 255) / 256;
+            ti.kq = (rows & 255) != 0 ? 2 : 4;
+        } else {
+            ti.kbeg = s_gofs[g] / BK;
+            ti.nk = (s_gofs[g + 1] - s_gofs[g]) / BK;
+        }
         ti.out_row = (int64_t)g * p.M + mt * BM;
     }
     ti.b_row = nt * BN;
@@ -196,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool aborted = false;
         for (int64_t t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
             Tile ti;
-            get_tile<BN>(p, s_gofs, total_mt, t, ti);
+            get_tile<BN, NVF4>(p, s_gofs, total_mt, t, ti);
             const int gB = p.mode == MOE_GEMM_WGRAD ? 0 : ti.g;
             for (int ks = 0; ks < ti.nk; ++ks) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, p, abort_flag)) {
@@ -204,20 +216,59 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 const int64_t kg = ti.kbeg + ks;
-                const int kx = (int)(kg * BK);
                 const uint32_t fb = full_bar(stage);
-                mbar_expect_tx(fb, BF16 ? (uint32_t)(C::A_STAGE + C::B_STAGE) : C::STAGE_TX);
-                tma_load_2d(smem_u32(sA + stage * C::A_STAGE), &tmA, kx, (int)ti.a_row, fb);
-                const uint8_t* sfa = p.a_sf + kg * p.a_sf_kstride + (ti.a_row / 128) * C::SFA_STG;
-                const uint8_t* sfb = p.b_sf + (int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride;
-                if constexpr (!BF16) bulk_load(smem_u32(sSFA + stage * C::SFA_STG), sfa, C::SFA_STG, fb);
+                if constexpr (NVF4) {
+                    // k-step = 128 packed bytes = 256 elements = four 64-element
+                    // scale atoms; WGRAD steps start at the group's rows (a
+                    // multiple of 128 rows, so possibly mid-chunk) and the
+                    // last one may hold only two atoms
+                    const bool wg = p.mode == MOE_GEMM_WGRAD;
+                    const int nq = (wg && ks == ti.nk - 1) ? ti.kq : 4;
+                    const int kx = wg ? (int)((ti.kbeg + 256 * (int64_t)ks) / 2) : (int)(kg * BK);
+                    const int64_t a0 = wg ? (ti.kbeg + 256 * (int64_t)ks) / 64 : 4 * kg;
+                    mbar_expect_tx(fb, (uint32_t)(C::A_STAGE + C::B_STAGE + nq * 512 * (1 + BN / 128)));
+                    tma_load_2d(smem_u32(sA + stage * C::A_STAGE), &tmA, kx, (int)ti.a_row, fb);
+                    const bool whole = nq == 4 && (a0 & 3) == 0;
+                    const uint8_t* sfa = p.a_sf + (ti.a_row / 128) * 2048;
+                    if (whole) {
+                        bulk_load(smem_u32(sSFA + stage * C::SFA_STG), sfa + (a0 >> 2) * p.a_sf_kstride, 2048, fb);
+                    } else {
+                        for (int j = 0; j < nq; ++j) {
+                            const int64_t a = a0 + j;
+                            bulk_load(smem_u32(sSFA + stage * C::SFA_STG + 512 * j),
+                                      sfa + (a >> 2) * p.a_sf_kstride + (a & 3) * 512, 512, fb);
+                        }
+                    }
 #pragma unroll
-                for (int h = 0; h < BN / 128; ++h) {
-                    const int brow = ti.b_row + 128 * h;
-                    tma_load_3d(smem_u32(sB + stage * C::B_STAGE + h * 16384), &tmB, kx, brow, gB, fb);
-                    if constexpr (!BF16)
-                        bulk_load(smem_u32(sSFB + stage * C::SFB_STAGE + h * C::SFA_STG),
-                                  sfb + (int64_t)(brow / 128) * C::SFA_STG, C::SFA_STG, fb);
+                    for (int h = 0; h < BN / 128; ++h) {
+                        const int brow = ti.b_row + 128 * h;
+                        tma_load_3d(smem_u32(sB + stage * C::B_STAGE + h * 16384), &tmB, kx, brow, gB, fb);
+                        const uint8_t* sfb = p.b_sf + (int64_t)gB * p.b_sf_gstride + (int64_t)(brow / 128) * 2048;
+                        const uint32_t dst = smem_u32(sSFB + stage * C::SFB_STAGE + h * C::SFA_STG);
+                        if (whole) {
+                            bulk_load(dst, sfb + (a0 >> 2) * p.b_sf_kstride, 2048, fb);
+                        } else {
+                            for (int j = 0; j < nq; ++j) {
+                                const int64_t a = a0 + j;
+                                bulk_load(dst + 512 * j, sfb + (a >> 2) * p.b_sf_kstride + (a & 3) * 512, 512, fb);
+                            }
+                        }
+                    }
+                } else {
+                    const int kx = (int)(kg * BK);
+                    mbar_expect_tx(fb, BF16 ? (uint32_t)(C::A_STAGE + C::B_STAGE) : C::STAGE_TX);
+                    tma_load_2d(smem_u32(sA + stage * C::A_STAGE), &tmA, kx, (int)ti.a_row, fb);
+                    const uint8_t* sfa = p.a_sf + kg * p.a_sf_kstride + (ti.a_row / 128) * C::SFA_STG;
+                    const uint8_t* sfb = p.b_sf + (int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride;
+                    if constexpr (!BF16) bulk_load(smem_u32(sSFA + stage * C::SFA_STG), sfa, C::SFA_STG, fb);
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h) {
+                        const int brow = ti.b_row + 128 * h;
+                        tma_load_3d(smem_u32(sB + stage * C::B_STAGE + h * 16384), &tmB, kx, brow, gB, fb);
+                        if constexpr (!BF16)
+                            bulk_load(smem_u32(sSFB + stage * C::SFB_STAGE + h * C::SFA_STG),
+                                      sfb + (int64_t)(brow / 128) * C::SFA_STG, C::SFA_STG, fb);
+                    }
                 }
                 pend[stage] = (int)phase;
                 if (++stage == STAGES) {
@@ -246,7 +297,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool issued = false;
         for (int64_t t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
             Tile ti;
-            get_tile<BN>(p, s_gofs, total_mt, t, ti);
+            get_tile<BN, NVF4>(p, s_gofs, total_mt, t, ti);
             if (ti.nk == 0) continue;
             if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, p, abort_flag)) {
                 aborted = true;
@@ -262,6 +313,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t t_sfa = tmem_base + C::SF0 + C::SF_COLS * stage;
                 const uint32_t t_sfb = t_sfa + (NVF4 ? 16 : 4);
+                // NVFP4: 64-element MMAs in this k-step (WGRAD's last step
+                // of a group ending half-way has 2)
+                const int nq = (NVF4 && p.mode == MOE_GEMM_WGRAD && ks == ti.nk - 1) ? ti.kq : 4;
                 if constexpr (NVF4) {
                     // atom j (64 K-elements) of A -> columns t_sfa + 4j; atom
                     // j of B rows [128h, 128h + 128) -> t_sfb + 8j + 4h, so
@@ -269,11 +323,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // columns at t_sfa + 4j and B's 8 at t_sfb + 8j
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        tc_cp_sf(t_sfa + 4 * j, desc_sf(smem_u32(sSFA + stage * C::SFA_STG + 512 * j)));
+                        if (j < nq) {
+                            tc_cp_sf(t_sfa + 4 * j, desc_sf(smem_u32(sSFA + stage * C::SFA_STG + 512 * j)));
 #pragma unroll
-                        for (int h = 0; h < BN / 128; ++h)
-                            tc_cp_sf(t_sfb + 8 * j + 4 * h,
-                                     desc_sf(smem_u32(sSFB + stage * C::SFB_STAGE + h * C::SFA_STG + 512 * j)));
+                            for (int h = 0; h < BN / 128; ++h)
+                                tc_cp_sf(t_sfb + 8 * j + 4 * h,
+                                         desc_sf(smem_u32(sSFB + stage * C::SFB_STAGE + h * C::SFA_STG + 512 * j)));
+                        }
                     }
                 } else if constexpr (!BF16) {
                     tc_cp_sf(t_sfa, desc_sf(smem_u32(sSFA + stage * C::SFA_STG)));
@@ -291,9 +347,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if constexpr (BF16)
                         tc_mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
                                     make_idesc_bf16<BN>(), (ks | kk) != 0 ? 1u : 0u);
-                    else if constexpr (NVF4)
-                        tc_mma_nvf4(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
-                                    make_idesc_nvf4<BN>(), t_sfa + 4 * kk, t_sfb + 8 * kk, (ks | kk) != 0 ? 1u : 0u);
+                    else if constexpr (NVF4) {
+                        if (kk < nq)
+                            tc_mma_nvf4(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                                        make_idesc_nvf4<BN>(), t_sfa + 4 * kk, t_sfb + 8 * kk,
+                                        (ks | kk) != 0 ? 1u : 0u);
+                    }
                     else
                         tc_mma(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
                                make_idesc<BN>((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
@@ -330,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
             Tile ti;
-            get_tile<BN>(p, s_gofs, total_mt, t, ti);
+            get_tile<BN, NVF4>(p, s_gofs, total_mt, t, ti);
             const int64_t row = ti.out_row + quarter * 32 + lane;
             if (ti.nk == 0) {   // WGRAD of an empty group
                 epilogue_zero<BN>(p, row, ti.nt, half);
@@ -737,7 +796,7 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
                                            const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
                                            void* d, int32_t* err, void* stream) {
     using namespace gg;
-    MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD || mode == MOE_GEMM_WGRAD, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(epilogue == MOE_EPI_NONE || epilogue == MOE_EPI_NONE_F32, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(a && a_sf && a_scale && b && b_sf && b_scale && gofs && d, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(G >= 1 && G <= MAX_G && M > 0 && N > 0 && K > 0, MOE_ERR_INVALID_ARG);
@@ -748,11 +807,16 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
                     (reinterpret_cast<uintptr_t>(b_scale) & 3) == 0,
                 MOE_ERR_ALIGNMENT);
     MOE_REQUIRE(device_initialized() && g_encode != nullptr, MOE_ERR_NOT_INITIALIZED);
-    // packed E2M1 rows seen as bytes: K/2 bytes per row, 128-byte k-steps
+    const bool wg = mode == MOE_GEMM_WGRAD;
+    // packed E2M1 rows seen as bytes: K/2 bytes per row, 128-byte k-steps.
+    // FWD/DGRAD: A [M, K], B [G][N][K]; WGRAD: A [M, K] and B [N, K] are the
+    // transposed (columnwise) codes of the two row-permuted operands, K the
+    // rows, D [G][M][N] (each group's contraction runs over its own rows)
     const int64_t Kb = K / 2;
     CUtensorMap tmA, tmB;
     const uint64_t da[2] = {(uint64_t)Kb, (uint64_t)M}, sa[1] = {(uint64_t)Kb};
-    const uint64_t db[3] = {(uint64_t)Kb, (uint64_t)N, (uint64_t)G}, sb[2] = {(uint64_t)Kb, (uint64_t)N * Kb};
+    const uint64_t db[3] = {(uint64_t)Kb, (uint64_t)N, wg ? 1ull : (uint64_t)G},
+                   sb[2] = {(uint64_t)Kb, (uint64_t)N * Kb};
     MOE_REQUIRE(make_map(&tmA, a, 2, da, sa) && make_map(&tmB, b, 3, db, sb), MOE_ERR_CUDA);
     Params p{};
     p.mode = mode;
@@ -760,15 +824,15 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
     p.G = G;
     p.N = N;
     p.M = M;
-    p.K = Kb;
+    p.K = wg ? K : Kb;      // WGRAD: rows (the offsets' bound); FWD/DGRAD: bytes (k-steps of 128)
     p.gofs = gofs;
     p.a_sf = a_sf;
     p.b_sf = b_sf;
-    // NVFP4 scale atoms: [k-step][row tile][4 x 512]; B's rows are the G*N
-    // rows of the [G][N] weight operand
+    // NVFP4 scale atoms: [k-step][row tile][4 x 512]; FWD/DGRAD: B's rows are
+    // the G*N rows of the [G][N] weight operand
     p.a_sf_kstride = (M / 128) * 2048;
-    p.b_sf_kstride = (int64_t)G * (N / 128) * 2048;
-    p.b_sf_gstride = (int64_t)(N / 128) * 2048;
+    p.b_sf_kstride = (wg ? 1 : (int64_t)G) * (N / 128) * 2048;
+    p.b_sf_gstride = wg ? 0 : (int64_t)(N / 128) * 2048;
     p.alpha_a = a_scale;
     p.alpha_b = b_scale;
     p.d = (__nv_bfloat16*)d;
@@ -777,12 +841,13 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
     p.band = 8;
     if (const char* e = getenv("MOE_GEMM_BAND")) p.band = std::max(1, atoi(e));
     p.n_tiles = N / 256;
+    p.m_tiles = (int)(M / BM);
     p.n_out = N;
     p.ldd = N;
     const int sms = device_sm_count();
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
-    const int64_t tiles = (M / BM) * p.n_tiles;
-    const int grid = (int)std::min<int64_t>(tiles, sms);
+    const int64_t tiles = wg ? (int64_t)G * p.m_tiles * p.n_tiles : (M / BM) * p.n_tiles;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
     cudaStream_t s = (cudaStream_t)stream;
     if (epilogue == MOE_EPI_NONE_F32)
         k_grouped_gemm<256, MOE_EPI_NONE_F32, FMT_NVF4><<<grid, THREADS, Cfg<256, FMT_NVF4>::SMEM_BYTES, s>>>(tmA, tmB, p);

@@ -107,6 +107,98 @@ __global__ void __launch_bounds__(256) k_quant(const __nv_bfloat16* __restrict__
         *reinterpret_cast<uint32_t*>(scales + base + (2 * half + j) * 512) = sw[j];
 }
 
+// Max |x| over the rows [0, lim) of a [rows, cols] bf16 matrix, lim =
+// min(gofs[G], rows) read on the device (0 when the offsets are invalid).
+__global__ void __launch_bounds__(256) k_amax_rows(const uint4* __restrict__ src, int cols, int64_t rows,
+                                                   const int32_t* __restrict__ gofs, int G,
+                                                   uint32_t* __restrict__ amax_bits) {
+    const int64_t lim = min((int64_t)max(gofs[G], 0), rows);
+    const int64_t n16 = lim * cols / 8;
+    uint32_t m = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(src + i);
+        m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+    }
+    uint32_t mm = max(m & 0xFFFFu, m >> 16);
+    mm = __reduce_max_sync(0xffffffffu, mm);
+    if ((threadIdx.x & 31) == 0 && mm != 0) atomicMax(amax_bits, mm);
+}
+
+// Group-aware columnwise quantization: blocks of 16 rows along each column
+// (the contraction axis of the weight gradient).  Groups start at multiples
+// of 128 rows, so no block crosses a group; rows >= gofs[G] count as zeros.
+// One CTA per (64-column, 256-row) tile staged in shared memory; thread
+// (c, q) quantizes rows [64 q, 64 q + 64) of column c: four blocks, 32 bytes
+// of codes (transposed output) and one 4-byte scale word (one atom row).
+__global__ void __launch_bounds__(256) k_quant_cols(const __nv_bfloat16* __restrict__ src, int64_t rows, int cols,
+                                                    const int32_t* __restrict__ gofs, int G,
+                                                    const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes,
+                                                    uint8_t* __restrict__ scales, float* __restrict__ tensor_scale,
+                                                    int32_t* __restrict__ err) {
+    __shared__ __align__(16) uint16_t tile[256][64];
+    __shared__ int s_ok;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_ok = 1;
+    __syncthreads();
+    // offsets: 0 first, monotone, multiples of 128, inside the buffer
+    for (int g = tid; g < G; g += blockDim.x) {
+        const int lo = gofs[g], hi = gofs[g + 1];
+        if ((g == 0 && lo != 0) || hi < lo || (hi & 127) != 0 || (int64_t)hi > rows) s_ok = 0;
+    }
+    __syncthreads();
+    const bool ok = s_ok != 0;
+    if (!ok && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) set_err(err, MOE_ERR_BAD_OFFSETS);
+    const int64_t lim = ok ? (int64_t)gofs[G] : 0;
+    const float amax = ok ? bf16_bits_to_float(*amax_bits) : 0.f;
+    const float enc = amax > 0.f ? __fdiv_rn(kRange, amax) : 0.f;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *tensor_scale = amax > 0.f ? __fdiv_rn(amax, kRange) : 0.f;
+    const int64_t r0 = (int64_t)blockIdx.y * 256;
+    const int c0 = blockIdx.x * 64;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 32 * i + (tid >> 3), ch = tid & 7;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r0 + r < lim) v = __ldg(reinterpret_cast<const uint4*>(src + (r0 + r) * cols + c0) + ch);
+        *reinterpret_cast<uint4*>(&tile[r][8 * ch]) = v;
+    }
+    __syncthreads();
+    const int c = tid & 63, q = tid >> 6;
+    const int64_t cc = c0 + c;
+    uint32_t qw[8];
+    uint32_t sw = 0u;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = bf16_bits_to_float(tile[64 * q + 16 * b + i][c]);
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(f[i]));
+        uint32_t byte = 0u;
+        float rb = 0.f;
+        if (enc > 0.f) {
+            const float tb = __fmul_rn(__fdiv_rn(am, 6.0f), enc);
+            byte = cvt_e4m3x2(tb, 0.f) & 0x7Fu;
+            if (byte != 0u) rb = __fdiv_rn(enc, e4m3_value(byte));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(f[i], rb);
+        qw[2 * b] = byte != 0u ? cvt_e2m1x8(f) : 0u;
+        qw[2 * b + 1] = byte != 0u ? cvt_e2m1x8(f + 8) : 0u;
+        sw |= byte << (8 * b);
+    }
+    uint4* o = reinterpret_cast<uint4*>(codes + cc * (rows / 2) + (r0 + 64 * q) / 2);
+    o[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    o[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    // [256-row k-step][128-column tile of the transposed matrix][4 atoms][512]
+    const int64_t off = ((int64_t)blockIdx.y * (cols / 128) + cc / 128) * 2048 + q * 512 + (cc & 31) * 16 +
+                        ((cc >> 5) & 3) * 4;
+    *reinterpret_cast<uint32_t*>(scales + off) = sw;
+}
+
 }  // namespace nvf4
 }  // namespace moe
 
@@ -138,3 +230,27 @@ extern "C" moe_status_t nvfp4_quantize(const void* src, int64_t rows, int cols, 
         reinterpret_cast<const __nv_bfloat16*>(src), rows, cols, amax_ws, codes, scales, tensor_scale);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
+
+extern "C" moe_status_t nvfp4_quantize_cols(const void* src, int64_t rows, int cols, const int32_t* gofs, int G,
+                                            uint8_t* codes_t, uint8_t* scales_t, float* tensor_scale,
+                                            uint32_t* amax_ws, int32_t* err, void* stream) {
+    MOE_REQUIRE(src && gofs && codes_t && scales_t && tensor_scale && amax_ws, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(rows > 0 && cols > 0 && G >= 1 && G <= 4096, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(rows % 256 == 0 && cols % 128 == 0 && rows / 256 <= 65535 && rows <= 0x7FFFFF00LL,
+                MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(moe_aligned16(src) && moe_aligned16(codes_t) && moe_aligned16(scales_t), MOE_ERR_ALIGNMENT);
+    MOE_REQUIRE((reinterpret_cast<uintptr_t>(amax_ws) & 3u) == 0 && (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) == 0,
+                MOE_ERR_ALIGNMENT);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemsetAsync(amax_ws, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    const int sms = device_sm_count();
+    const int64_t want = (rows * (int64_t)cols / 8 + 255) / 256;
+    const int grid = (int)std::min<int64_t>(want, (int64_t)(sms > 0 ? sms : 148) * 8);
+    nvf4::k_amax_rows<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), cols, rows, gofs, G, amax_ws);
+    nvf4::k_quant_cols<<<dim3((unsigned)(cols / 64), (unsigned)(rows / 256)), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(src), rows, cols, gofs, G, amax_ws, codes_t, scales_t, tensor_scale,
+        err);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+

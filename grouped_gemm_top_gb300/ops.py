@@ -42,7 +42,7 @@ EXPORTS = [
     "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_route_topk_noalloc",
     "mxfp8_gather_quantize", "grouped_gemm_mxfp8_swiglu_quant", "mxfp8_swiglu_bwd_quantize",
     "gemm_bf16_nt", "moe_transpose_bf16", "moe_unpermute_combine_add", "moe_route_append_shared",
-    "moe_route_drop_shared", "nvfp4_sf_bytes", "nvfp4_quantize", "grouped_gemm_nvfp4",
+    "moe_route_drop_shared", "nvfp4_sf_bytes", "nvfp4_quantize", "grouped_gemm_nvfp4", "nvfp4_quantize_cols",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -75,6 +75,7 @@ _SIGS = {
     "moe_route_topk_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_sf_bytes": (_i64, [_i64, _i32]),
     "nvfp4_quantize": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "nvfp4_quantize_cols": (_i32, [_vp, _i64, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "grouped_gemm_nvfp4": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i64, _i32, _vp, _vp,
                                   _vp]),
 }
@@ -406,11 +407,28 @@ def nvfp4_quantize(x, codes=None, scales=None, tensor_scale=None, amax_ws=None, 
     return codes, scales, tensor_scale
 
 
+def nvfp4_quantize_cols(x, gofs, G, codes_t=None, scales_t=None, tensor_scale=None, amax_ws=None, err=None,
+                        stream=None):
+    """Group-aware columnwise NVFP4 of bf16 x [rows, cols] (rows % 256, cols %
+    128; groups at multiples of 128 rows).  See include/moe.h.  Returns
+    (codes_t [cols, rows/2] u8, scales_t u8, tensor_scale float32 [1])."""
+    rows, cols = x.shape
+    codes_t = codes_t if codes_t is not None else _empty((cols, rows // 2), torch.uint8, x)
+    scales_t = scales_t if scales_t is not None else _empty((max(nvfp4_sf_bytes(cols, rows), 0),), torch.uint8, x)
+    tensor_scale = tensor_scale if tensor_scale is not None else _empty((1,), torch.float32, x)
+    amax_ws = amax_ws if amax_ws is not None else _empty((1,), torch.int32, x)
+    _check("nvfp4_quantize_cols", lib.nvfp4_quantize_cols(_p(x), int(rows), int(cols), _p(gofs), int(G),
+                                                          _p(codes_t), _p(scales_t), _p(tensor_scale),
+                                                          _p(amax_ws), _p(err), _stream(stream)))
+    return codes_t, scales_t, tensor_scale
+
+
 def grouped_gemm_nvfp4(mode, a, a_sf, a_scale, b, b_sf, b_scale, gofs, G, M, N, K, epilogue=MOE_EPI_NONE, d=None,
                        err=None, stream=None):
     """See include/moe.h.  Allocates d when not given."""
     if d is None:
-        d = _empty((M, N), torch.float32 if epilogue == MOE_EPI_NONE_F32 else torch.bfloat16, a)
+        shape = (G, M, N) if mode == MOE_GEMM_WGRAD else (M, N)
+        d = _empty(shape, torch.float32 if epilogue == MOE_EPI_NONE_F32 else torch.bfloat16, a)
     _check("grouped_gemm_nvfp4", lib.grouped_gemm_nvfp4(int(mode), _p(a), _p(a_sf), _p(a_scale), _p(b), _p(b_sf),
                                                         _p(b_scale), _p(gofs), int(G), int(M), int(N), int(K),
                                                         int(epilogue), _p(d), _p(err), _stream(stream)))

@@ -484,22 +484,52 @@ MOE_API moe_status_t nvfp4_quantize(const void* src, int64_t rows, int cols, uin
                                     float* tensor_scale, uint32_t* amax_ws, int32_t* err, void* stream);
 
 /*
- * grouped_gemm_nvfp4 -- the grouped GEMM of grouped_gemm_mxfp8 (modes FWD
- * and DGRAD: D[r, :] = A[r, :] * B_g^T for rows r of group g) with NVFP4
+ * nvfp4_quantize_cols -- group-aware columnwise NVFP4 of a row-permuted
+ * bf16 matrix (the weight-gradient operands): blocks of 16 rows of one
+ * group along each column, codes written transposed.  Groups start at
+ * multiples of 128 rows (gofs as for the grouped GEMM), so no block
+ * crosses a group; rows >= gofs[G] are quantized as zeros.  The tensor
+ * amax, the fp32 steps and the rounding are those of nvfp4_quantize, over
+ * rows [0, gofs[G]).
+ *   src           [rows, cols] bf16, 16-byte aligned; rows % 256 == 0,
+ *                 cols % 128 == 0.
+ *   gofs, G       group offsets (device, G + 1 values, 1 <= G <= 4096):
+ *                 gofs[0] == 0, monotone, multiples of 128, gofs[G] <= rows;
+ *                 otherwise MOE_ERR_BAD_OFFSETS in err and zero output.
+ *   codes_t       [cols, rows / 2] bytes: row c holds column c of src, two
+ *                 rows per byte (row 2j in the low nibble).
+ *   scales_t      nvfp4_sf_bytes(cols, rows) bytes: the scale layout above
+ *                 for the [cols, rows] matrix.
+ *   tensor_scale  one float (device), written; amax_ws one uint32 of
+ *                 device scratch (zeroed and used by the call).
+ */
+MOE_API moe_status_t nvfp4_quantize_cols(const void* src, int64_t rows, int cols, const int32_t* gofs, int G,
+                                         uint8_t* codes_t, uint8_t* scales_t, float* tensor_scale,
+                                         uint32_t* amax_ws, int32_t* err, void* stream);
+
+/*
+ * grouped_gemm_nvfp4 -- the grouped GEMM of grouped_gemm_mxfp8 with NVFP4
  * operands on the tensor cores (tcgen05.mma kind::mxf4nvf4, UE4M3 block
  * scales, fp32 accumulation); the epilogue multiplies by a_scale * b_scale.
+ * FWD / DGRAD: D[r, :] = A[r, :] * B_g^T for the rows r of group g.
  *   a, a_sf, a_scale   nvfp4_quantize output for A [M, K].
  *   b, b_sf, b_scale   nvfp4_quantize output for the [G * N, K] matrix whose
  *                      rows g*N .. g*N+N-1 are B_g ([G][N][K]; one tensor
  *                      scale for every expert's weights).
- *   gofs, G            as grouped_gemm_mxfp8 (0 = gofs[0], monotone,
- *                      multiples of 128, gofs[G] <= M; device-checked into
- *                      err as MOE_ERR_BAD_OFFSETS).
- *   M % 128 == 0, N % 256 == 0, K % 256 == 0.
- *   epilogue           MOE_EPI_NONE (d bf16 [M, N]) or MOE_EPI_NONE_F32 (d
- *                      fp32 [M, N]); d 32-byte aligned.  Rows >= gofs[G]
- *                      are not written.
- * Every wait inside the kernel is bounded (MOE_ERR_DEVICE_TIMEOUT in err).
+ *   gofs, G            0 = gofs[0], monotone, multiples of 128, gofs[G] <= M.
+ *   d                  [M, N]; rows >= gofs[G] are not written.
+ * WGRAD: D_g[m, n] = sum over the rows r of group g of A^T[r, m] B^T[r, n]
+ * (the weight gradient; each group's contraction is its own rows).
+ *   a, a_sf, a_scale   nvfp4_quantize_cols output for the row-permuted
+ *                      [K, M] operand (codes [M, K / 2]).
+ *   b, b_sf, b_scale   nvfp4_quantize_cols output for the [K, N] operand.
+ *   gofs, G            as above with gofs[G] <= K; a group of an odd number
+ *                      of 128-row tiles ends with a half 256-row k-step.
+ *   d                  [G, M, N]; an empty group's D_g is written as zeros.
+ * All modes: M % 128 == 0, N % 256 == 0, K % 256 == 0; epilogue
+ * MOE_EPI_NONE (bf16 d) or MOE_EPI_NONE_F32 (fp32 d); d 32-byte aligned;
+ * bad offsets -> MOE_ERR_BAD_OFFSETS in err; every wait inside the kernel is
+ * bounded (MOE_ERR_DEVICE_TIMEOUT in err).
  */
 MOE_API moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uint8_t* a_sf, const float* a_scale,
                                         const uint8_t* b, const uint8_t* b_sf, const float* b_scale,

@@ -133,3 +133,83 @@ def test_nvfp4_grouped_gemm_bad_offsets(ops):
                            o["M"], 256, 256, ops.MOE_EPI_NONE, err=err)
     torch.cuda.synchronize()
     assert err.item() == ops.MOE_ERR_BAD_OFFSETS
+
+
+def _grouped_rows(sizes, cols, seed, extra=256):
+    """Row-permuted bf16 matrix: group g's rows at padded_layout offsets,
+    zero padding rows, a buffer of a multiple of 256 rows."""
+    gofs = padded_layout(sizes)
+    rows = (int(gofs[-1]) + extra + 255) // 256 * 256
+    x = _input(rows, cols, seed).float()
+    for g, m in enumerate(sizes):
+        x[int(gofs[g]) + m:int(gofs[g + 1])] = 0.0
+    x[int(gofs[-1]):] = 0.0
+    return x.bfloat16(), gofs
+
+
+@pytest.mark.parametrize("sizes,cols", [([128, 0, 384], 128), ([300, 17, 0, 900, 128], 384), ([700, 1500], 2048)])
+def test_nvfp4_quantize_cols_bit_exact(ops, sizes, cols):
+    x, gofs = _grouped_rows(sizes, cols, sum(sizes) + cols)
+    rows = x.shape[0]
+    gofs_t = torch.from_numpy(gofs.astype(np.int32)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales, st = ops.nvfp4_quantize_cols(x, gofs_t, len(sizes), err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    R = int(gofs[-1])
+    xs = to_np(x)
+    # the oracle on the ragged groups (padding rows dropped) lays them out at
+    # 16-row offsets; the GPU's 128-row layout holds the same blocks
+    starts = gofs[:-1]
+    ragged = np.concatenate([xs[int(starts[g]):int(starts[g]) + m] for g, m in enumerate(sizes)])
+    roff = np.concatenate([[0], np.cumsum(sizes)])
+    q, s, st_ref, padded = O.nvfp4_quantize_cols_grouped(ragged, roff)
+    assert np.float32(st.item()) == st_ref
+    got_q = unpack_codes(codes.cpu().numpy())                   # [cols, rows]
+    got_s = nvfp4_atoms_to_rowmajor(scales.cpu().numpy(), cols, rows)
+    for g, m in enumerate(sizes):
+        nb = (m + 15) // 16
+        lo, plo = int(gofs[g]), int(padded[g])
+        assert np.array_equal(got_q[:, lo:lo + 16 * nb], q[:, plo:plo + 16 * nb]), g
+        assert np.array_equal(got_s[:, lo // 16:lo // 16 + nb], s[:, plo // 16:plo // 16 + nb]), g
+        assert not got_q[:, lo + 16 * nb:int(gofs[g + 1])].any()   # whole padding blocks
+    assert not got_q[:, R:].any() and not got_s[:, R // 16:].any()
+
+
+def test_nvfp4_quantize_cols_bad_offsets(ops):
+    x = torch.ones((256, 128), dtype=torch.bfloat16, device="cuda")
+    bad = torch.tensor([0, 100, 256], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales, st = ops.nvfp4_quantize_cols(x, bad, 2, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == ops.MOE_ERR_BAD_OFFSETS and not codes.any() and st.item() == 0.0
+
+
+@pytest.mark.parametrize("sizes,M,N", [([128, 256, 0, 384], 256, 256), ([300, 17, 0, 900, 128], 384, 512),
+                                       ([700, 1500, 260], 2048, 512)])
+def test_nvfp4_wgrad_matches_oracle(ops, sizes, M, N):
+    """dB_g = A_g^T G_g over each group's rows, from the columnwise NVFP4
+    codes of both row-permuted operands (groups of odd and even numbers of
+    128-row tiles, an empty group)."""
+    X, gofs = _grouped_rows(sizes, M, 11 + M)
+    Y, _ = _grouped_rows(sizes, N, 12 + N)
+    K = X.shape[0]
+    G = len(sizes)
+    gofs_t = torch.from_numpy(gofs.astype(np.int32)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    aq, asf, ast = ops.nvfp4_quantize_cols(X, gofs_t, G, err=err)
+    bq, bsf, bst = ops.nvfp4_quantize_cols(Y, gofs_t, G, err=err)
+    d = torch.full((G, M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    ops.grouped_gemm_nvfp4(ops.MOE_GEMM_WGRAD, aq, asf, ast, bq, bsf, bst, gofs_t, G, M, N, K, ops.MOE_EPI_NONE, d, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    Ad = O.nvfp4_dequantize_cols(unpack_codes(aq.cpu().numpy()), nvfp4_atoms_to_rowmajor(asf.cpu().numpy(), M, K),
+                                 np.float32(ast.item()))                    # [K, M]
+    Bd = O.nvfp4_dequantize_cols(unpack_codes(bq.cpu().numpy()), nvfp4_atoms_to_rowmajor(bsf.cpu().numpy(), N, K),
+                                 np.float32(bst.item()))                    # [K, N]
+    ref = O.grouped_gemm_wgrad(Ad, Bd, gofs)
+    for g in range(G):
+        if sizes[g] == 0:
+            assert torch.all(d[g] == 0)
+        else:
+            assert_bf16_close(d[g], ref[g], what=f"nvfp4 dW[{g}]")
