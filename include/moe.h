@@ -9,9 +9,11 @@
  *            "Optimization 2: Expert parallelism to integrate Dispatch and
  *            Combine".
  *   [CH1]    AI Systems Performance Engineering ch.1 ("第一章：介绍与 AI 系统
- *            概览"): §1.1 "数据精度" (FP8 E4M3 = 1+4+3 bits) and
- *            "低精度格式的缩放机制" (MXFP8: one scale per block of 32);
- *            §2.3.2 "MoE 推理优化" (combine = router-weighted sum).
+ *            概览"): §1.1 "数据精度" (FP8 E4M3 = 1+4+3 bits, FP4 = 1+2+1) and
+ *            "低精度格式的缩放机制" (MXFP8: one scale per block of 32; NVFP4:
+ *            an E4M3 scale per block plus an FP32 scale per tensor);
+ *            §2.3.2 "MoE 推理优化" (combine = router-weighted sum; DeepSeek-V3's
+ *            shared expert).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -41,7 +43,8 @@
  * are zero padding, so a 128-row GEMM tile never straddles two groups and a
  * 32-row quantization block never crosses a group boundary.  An empty group
  * has no rows.  Buffers are sized for moe_row_capacity(T, E, k) rows; rows at
- * or beyond gofs[E] are never read or written by any call.
+ * or beyond gofs[E] are never read or written by any call (the transposed
+ * NVFP4 output of nvfp4_quantize_cols states its own rule).
  *
  * MXFP8 tensors
  * -------------
