@@ -846,9 +846,28 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
     p.ldd = N;
     const int sms = device_sm_count();
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
+    cudaStream_t s = (cudaStream_t)stream;
+    // FWD / DGRAD run on the 1-SM kernel; MOE_GEMM_2SM=256 (or 128) selects
+    // the CTA-pair kernel's NVFP4 instance (256 x 256 pair tiles, half of B
+    // per SM), kept for measurement: at the DeepSeek-V3 shapes it was slower
+    // (a group's odd last 128-row tile idles half a pair tile) and on dense
+    // shapes it only matched the 1-SM kernel
+    if (!wg && gemm_2sm_mode() > 0 && gemm_max_clusters_2sm(256) > 0) {
+        CUtensorMap tmB2, tmSFA, tmSFB;
+        MOE_REQUIRE(make_map(&tmB2, b, 3, db, sb, 128), MOE_ERR_CUDA);
+        MOE_REQUIRE(make_sf_map(&tmSFA, a_sf, M * K / 16 / 512, 8) &&
+                        make_sf_map(&tmSFB, b_sf, (int64_t)G * N * K / 16 / 512, 16),
+                    MOE_ERR_CUDA);
+        if (getenv("MOE_GEMM_BAND") == nullptr) p.band = 4;
+        const int64_t upper_pairs = (M / BM) * (int64_t)p.n_tiles;
+        const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm(256));
+        if (gemm_launch_2sm_nvf4(epilogue, tmA, tmB2, tmSFA, tmSFB, p, clusters, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        MOE_CHECK_LAUNCH();
+        return MOE_OK;
+    }
     const int64_t tiles = wg ? (int64_t)G * p.m_tiles * p.n_tiles : (M / BM) * p.n_tiles;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
-    cudaStream_t s = (cudaStream_t)stream;
     if (epilogue == MOE_EPI_NONE_F32)
         k_grouped_gemm<256, MOE_EPI_NONE_F32, FMT_NVF4><<<grid, THREADS, Cfg<256, FMT_NVF4>::SMEM_BYTES, s>>>(tmA, tmB, p);
     else

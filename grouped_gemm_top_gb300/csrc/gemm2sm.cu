@@ -39,7 +39,10 @@ namespace sm2 {
 // Pair-tile configurations: N = 256 (one accumulator per CTA) or N = 128
 // (two accumulators per CTA, so the epilogue of one tile overlaps the
 // mainloop of the next).  Each CTA loads BN/2 rows of B.
-template <int BN_>
+// NVF4: NVFP4 operands (packed E2M1, UE4M3 scales per 16, kind::mxf4nvf4):
+// four scale atoms per 128 rows and k-step instead of one, plain epilogues
+// only (no TMA-store staging).
+template <int BN_, bool NVF4 = false>
 struct C2 {
     static constexpr int BN = BN_;
     static constexpr int BH = BN_ / 2;                  // B rows per CTA
@@ -47,12 +50,13 @@ struct C2 {
     static constexpr int STAGES = BN_ == 128 ? 8 : 5;
     static constexpr int A_STAGE = BM * BK;             // this CTA's 128 A rows
     static constexpr int B_STAGE = BH * BK;             // this CTA's half of B
-    static constexpr int SFA_BYTES = 512;
-    static constexpr int SFB_BYTES = (BN_ / 128) * 512; // scales of all BN B rows
+    static constexpr int SFA_BYTES = NVF4 ? 2048 : 512;
+    static constexpr int SFB_BYTES = (BN_ / 128) * SFA_BYTES;   // scales of all BN B rows
     static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_BYTES + SFB_BYTES;
     static constexpr uint32_t SF0 = NACC * BN_;         // TMEM: accumulators, then scales
+    static constexpr uint32_t SF_COLS = NVF4 ? 16 + 16 * (BN_ / 128) : TMEM_SF_STRIDE;
     // TMA-store staging of the epilogue (N = 256): 4 KB per epilogue warp
-    static constexpr int EPI_BYTES = BN_ == 256 ? EPI_WARPS * 4096 : 0;
+    static constexpr int EPI_BYTES = (BN_ == 256 && !NVF4) ? EPI_WARPS * 4096 : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;       // 1024-byte aligned
@@ -65,7 +69,7 @@ struct C2 {
     static constexpr int OFF_PT = OFF_GOFS + (MAX_G + 1) * 4;
     static constexpr int SMEM_BYTES = OFF_PT + (MAX_G + 1) * 4 + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static_assert(SF0 + STAGES * TMEM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
+    static_assert(SF0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(OFF_EPI % 1024 == 0, "swizzled staging alignment");
 };
 
@@ -158,6 +162,21 @@ __device__ __forceinline__ void tc_commit_both(uint32_t bar) {
 __device__ __forceinline__ void tc_commit_local2(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+__device__ __forceinline__ void tc_mma2_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+// M = 256, N = BN, E2M1 A and B, UE4M3 scales (scale_vec::4X, ids 0)
+template <int BN>
+__device__ __forceinline__ uint32_t make_idesc2_nvf4() {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
 // M = 256 (two CTAs x 128 rows), N = BN
 template <int BN>
 __device__ __forceinline__ uint32_t make_idesc2(uint32_t sf_id) {
@@ -207,12 +226,13 @@ __device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, co
     ti.nt = nt;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool NVF4 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                        const __grid_constant__ CUtensorMap tmD, const Params p) {
-    using C = C2<BN>;
+    using C = C2<BN, NVF4>;
+    static_assert(!NVF4 || (BN == 256 && (EPI == MOE_EPI_NONE || EPI == MOE_EPI_NONE_F32)), "NVFP4 pair instances");
     constexpr int STAGES = C::STAGES, NACC = C::NACC, BH = C::BH;
     constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_SFA = C::OFF_SFA, OFF_SFB = C::OFF_SFB;
     constexpr int OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC, OFF_GOFS = C::OFF_GOFS, OFF_PT = C::OFF_PT;
@@ -315,10 +335,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                              fb);
                 // scale atoms as rows of 256 bytes: atom i = rows 2i, 2i+1; the
                 // two B atoms of the pair tile are adjacent in every layout
-                const int64_t atom_a = (kg * p.a_sf_kstride) / 512 + ti.a_row / 128;
-                const int64_t atom_b = ((int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride) / 512 + ti.b_row_pair / 128;
-                tma2_load_2d(smem_u32(smem + OFF_SFA + stage * SFA_BYTES), &tmSFA, 0, (int)(2 * atom_a), fb);
-                tma2_load_2d(smem_u32(smem + OFF_SFB + stage * SFB_BYTES), &tmSFB, 0, (int)(2 * atom_b), fb);
+                // (NVFP4: a k-step's four atoms of a 128-row tile are 2 KB in
+                // a row, the pair tile's two row tiles 4 KB)
+                const int64_t sfa_row = (kg * p.a_sf_kstride + (ti.a_row / 128) * SFA_BYTES) / 256;
+                const int64_t sfb_row =
+                    ((int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride + (ti.b_row_pair / 128) * SFA_BYTES) / 256;
+                tma2_load_2d(smem_u32(smem + OFF_SFA + stage * SFA_BYTES), &tmSFA, 0, (int)sfa_row, fb);
+                tma2_load_2d(smem_u32(smem + OFF_SFB + stage * SFB_BYTES), &tmSFB, 0, (int)sfb_row, fb);
                 pend[stage] = (int)phase;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -356,18 +379,35 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t t_sfa = tmem_base + C::SF0 + TMEM_SF_STRIDE * stage;
-                const uint32_t t_sfb = t_sfa + 4;
+                const uint32_t t_sfa = tmem_base + C::SF0 + C::SF_COLS * stage;
+                const uint32_t t_sfb = t_sfa + (NVF4 ? 16 : 4);
+                const uint32_t s_sfa = smem_u32(smem + OFF_SFA + stage * SFA_BYTES);
                 const uint32_t s_sfb = smem_u32(smem + OFF_SFB + stage * SFB_BYTES);
-                tc_cp_sf2(t_sfa, desc_sf(smem_u32(smem + OFF_SFA + stage * SFA_BYTES)));
-#pragma unroll
-                for (int h = 0; h < BN / 128; ++h) tc_cp_sf2(t_sfb + 4 * h, desc_sf(s_sfb + 512 * h));
                 const uint64_t adesc = desc_sw128(smem_u32(smem + OFF_A + stage * A_STAGE));
                 const uint64_t bdesc = desc_sw128(smem_u32(smem + OFF_B + stage * B_STAGE));
+                if constexpr (NVF4) {
+                    // atom j (64 K-elements): A -> t_sfa + 4j, B rows
+                    // [128h, 128h + 128) -> t_sfb + 8j + 4h; MMA j reads them
 #pragma unroll
-                for (int kk = 0; kk < BK / 32; ++kk)
-                    tc_mma2(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
-                            make_idesc2<BN>((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
+                    for (int j = 0; j < 4; ++j) {
+                        tc_cp_sf2(t_sfa + 4 * j, desc_sf(s_sfa + 512 * j));
+#pragma unroll
+                        for (int h = 0; h < BN / 128; ++h)
+                            tc_cp_sf2(t_sfb + 8 * j + 4 * h, desc_sf(s_sfb + 2048 * h + 512 * j));
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma2_nvf4(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                                     make_idesc2_nvf4<BN>(), t_sfa + 4 * kk, t_sfb + 8 * kk, (ks | kk) != 0 ? 1u : 0u);
+                } else {
+                    tc_cp_sf2(t_sfa, desc_sf(s_sfa));
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h) tc_cp_sf2(t_sfb + 4 * h, desc_sf(s_sfb + 512 * h));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; ++kk)
+                        tc_mma2(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
+                                make_idesc2<BN>((uint32_t)kk), t_sfa, t_sfb, (ks | kk) != 0 ? 1u : 0u);
+                }
                 issued = true;
                 tc_commit_both(empty_bar(stage));
                 if (++stage == STAGES) {
@@ -426,11 +466,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 release();
             } else if constexpr (EPI == MOE_EPI_SWIGLU_BWD) {
                 epilogue_swiglu_bwd<BN>(p, tacc, row, ti.nt, half, release, apre);
-            } else if (BN == 256 && EPI == MOE_EPI_NONE && p.tma_store) {
+            } else if (!NVF4 && BN == 256 && EPI == MOE_EPI_NONE && p.tma_store) {
                 epilogue_tile_tma(&tmD, smem_u32(smem + C::OFF_EPI + 4096 * ew), tacc, row - lane, ti.nt, half, lane,
                                   release);
             } else if constexpr (BN == 256) {
-                epilogue_tile_staged<EPI>(p, tacc, row, ti.nt, half, release);
+                epilogue_tile_staged<EPI, NVF4>(p, tacc, row, ti.nt, half, release);
             } else {
                 epilogue_tile<BN, EPI>(p, tacc, row, ti.nt, half);
                 release();
@@ -501,7 +541,32 @@ static cudaError_t set_attr_2sm(int* max_clusters) {
 cudaError_t gemm_set_attributes_2sm() {
     cudaError_t e = set_attr_2sm<128>(&g_max_clusters[0]);
     if (e != cudaSuccess) return e;
-    return set_attr_2sm<256>(&g_max_clusters[1]);
+    e = set_attr_2sm<256>(&g_max_clusters[1]);
+    if (e != cudaSuccess) return e;
+    const cudaError_t es[] = {
+        cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm<256, MOE_EPI_NONE, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, gg::sm2::C2<256, true>::SMEM_BYTES),
+        cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm<256, MOE_EPI_NONE_F32, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, gg::sm2::C2<256, true>::SMEM_BYTES)};
+    for (cudaError_t x : es)
+        if (x != cudaSuccess) return x;
+    return cudaSuccess;
+}
+
+// NVFP4 pair kernel (N = 256, MOE_EPI_NONE or MOE_EPI_NONE_F32); `clusters`
+// must not exceed gemm_max_clusters_2sm(256) (its shared memory is smaller,
+// so as many pairs are co-resident).
+cudaError_t gemm_launch_2sm_nvf4(int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 const CUtensorMap& tmSFA, const CUtensorMap& tmSFB, const gg::Params& p,
+                                 int clusters, cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_cfg<256>(clusters, stream, attr);
+    cfg.dynamicSmemBytes = gg::sm2::C2<256, true>::SMEM_BYTES;
+    if (epilogue == MOE_EPI_NONE_F32)
+        return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<256, MOE_EPI_NONE_F32, true>, tmA, tmB, tmSFA,
+                                  tmSFB, tmA, p);
+    return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<256, MOE_EPI_NONE, true>, tmA, tmB, tmSFA, tmSFB, tmA,
+                              p);
 }
 
 int gemm_max_clusters_2sm(int bn) { return g_max_clusters[bn == 256 ? 1 : 0]; }

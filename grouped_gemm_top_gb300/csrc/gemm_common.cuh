@@ -687,4 +687,7 @@ int gemm_max_clusters_2sm(int bn);        // co-resident CTA pairs for N = bn pa
 cudaError_t gemm_launch_2sm(int bn, int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
                             const CUtensorMap& tmSFA, const CUtensorMap& tmSFB, const CUtensorMap& tmD,
                             const gg::Params& p, int clusters, cudaStream_t stream);
+cudaError_t gemm_launch_2sm_nvf4(int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 const CUtensorMap& tmSFA, const CUtensorMap& tmSFB, const gg::Params& p,
+                                 int clusters, cudaStream_t stream);
 }  // namespace moe
