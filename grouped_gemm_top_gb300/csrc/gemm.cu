@@ -875,3 +875,37 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }
+
+namespace moe {
+namespace gg {
+// One thread waits, with the GEMM kernels' bounded wait, on an mbarrier
+// that nothing arrives at: the wait must give up after timeout_ns, record
+// MOE_ERR_DEVICE_TIMEOUT and return, leaving the context usable.
+__global__ void k_wait_selftest(uint64_t timeout_ns, int32_t* err, int32_t* completed) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_flag = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Params p{};
+        p.err = err;
+        p.timeout_ns = timeout_ns;
+        *completed = mbar_wait(smem_u32(&bar), 0u, p, &abort_flag) ? 1 : 0;
+    }
+}
+}  // namespace gg
+}  // namespace moe
+
+extern "C" moe_status_t moe_selftest_bounded_wait(uint64_t timeout_ns, int32_t* err, int32_t* completed,
+                                                  void* stream) {
+    MOE_REQUIRE(err && completed && timeout_ns > 0 && timeout_ns <= 10000000000ull, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
+    gg::k_wait_selftest<<<1, 32, 0, (cudaStream_t)stream>>>(timeout_ns, err, completed);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+}
+

@@ -109,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
             const uint64_t now = globaltimer_ns();
             if (start == 0) {
                 start = now;
-            } else if (now - start > p.timeout_ns) {
+            } else if (now - start > p.timeout_ns || it >= kMaxSpin) {
                 set_err(p.err, MOE_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
                 return false;

@@ -82,6 +82,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait.  Returns false when the CTA is aborting (timeout here or
 // elsewhere in the CTA).
+// Besides the time limit (p.timeout_ns of the global nanosecond timer) a
+// wait gives up after kMaxSpin polls, so it ends even if the timer stood still.
+constexpr uint32_t kMaxSpin = 1u << 28;
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Params& p, volatile int* abort_flag) {
     uint64_t start = 0;
     for (uint32_t it = 0;; ++it) {
@@ -91,7 +95,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const P
             const uint64_t now = globaltimer_ns();
             if (start == 0) {
                 start = now;
-            } else if (now - start > p.timeout_ns) {
+            } else if (now - start > p.timeout_ns || it >= kMaxSpin) {
                 set_err(p.err, MOE_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
                 return false;

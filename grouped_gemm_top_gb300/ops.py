@@ -43,6 +43,7 @@ EXPORTS = [
     "mxfp8_gather_quantize", "grouped_gemm_mxfp8_swiglu_quant", "mxfp8_swiglu_bwd_quantize",
     "gemm_bf16_nt", "moe_transpose_bf16", "moe_unpermute_combine_add", "moe_route_append_shared",
     "moe_route_drop_shared", "nvfp4_sf_bytes", "nvfp4_quantize", "grouped_gemm_nvfp4", "nvfp4_quantize_cols",
+    "moe_selftest_bounded_wait",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -74,6 +75,7 @@ _SIGS = {
     "moe_route_bwd": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_route_topk_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_sf_bytes": (_i64, [_i64, _i32]),
+    "moe_selftest_bounded_wait": (_i32, [ctypes.c_uint64, _vp, _vp, _vp]),
     "nvfp4_quantize": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_quantize_cols": (_i32, [_vp, _i64, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "grouped_gemm_nvfp4": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i64, _i32, _vp, _vp,
@@ -433,4 +435,10 @@ def grouped_gemm_nvfp4(mode, a, a_sf, a_scale, b, b_sf, b_scale, gofs, G, M, N, 
                                                         _p(b_scale), _p(gofs), int(G), int(M), int(N), int(K),
                                                         int(epilogue), _p(d), _p(err), _stream(stream)))
     return d
+
+
+def moe_selftest_bounded_wait(timeout_ns, err, completed, stream=None):
+    """A bounded wait on an mbarrier that nothing arrives at (include/moe.h)."""
+    _check("moe_selftest_bounded_wait", lib.moe_selftest_bounded_wait(int(timeout_ns), _p(err), _p(completed),
+                                                                      _stream(stream)))
 
