@@ -91,10 +91,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -104,7 +104,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     uint64_t start = 0;
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 255u) == 255u) {
+        if ((it & 15u) == 15u) {
             if (*abort_flag) return false;
             const uint64_t now = globaltimer_ns();
             if (start == 0) {

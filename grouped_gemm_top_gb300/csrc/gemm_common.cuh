@@ -68,14 +68,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// A waiting thread may sleep up to this long in one poll (it is woken when
+// the phase completes), so idle warps do not take issue slots.
+constexpr uint32_t kSuspendNs = 50000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -84,13 +87,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // elsewhere in the CTA).
 // Besides the time limit (p.timeout_ns of the global nanosecond timer) a
 // wait gives up after kMaxSpin polls, so it ends even if the timer stood still.
-constexpr uint32_t kMaxSpin = 1u << 28;
+constexpr uint32_t kMaxSpin = 1u << 22;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Params& p, volatile int* abort_flag) {
     uint64_t start = 0;
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u) {
+        if ((it & 15u) == 15u) {
             if (*abort_flag) return false;
             const uint64_t now = globaltimer_ns();
             if (start == 0) {

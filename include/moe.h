@@ -544,7 +544,7 @@ MOE_API moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uint8_
  * bounded waits without a GPU fault: one thread waits, with the same
  * bounded wait the GEMM kernels use, on an mbarrier that nothing arrives
  * at.  After timeout_ns (1 ns .. 10 s) of the device's nanosecond timer, or
- * 2^28 polls, the wait gives up: *completed = 0 and MOE_ERR_DEVICE_TIMEOUT is
+ * 2^22 polls, the wait gives up: *completed = 0 and MOE_ERR_DEVICE_TIMEOUT is
  * written into err (first error wins), and the kernel returns, so the
  * context stays usable.  err and completed are device int32 words.  (The
  * pages have no counterpart: this is a test hook of the library.)
