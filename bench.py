@@ -235,6 +235,24 @@ def run_gpu(args, rank, world, local_rank):
     h2d = h_x.numel() * 2 + h_l.numel() * 4 + h_d.numel() * 2
     d2h = h_out.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
 
+    # the host link alone (same pinned buffers, no kernels): end to end is
+    # bounded by max(device step, copy time) when the copies overlap
+    def link_ms(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(reps):
+            fn()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        return c0.elapsed_time(c1) / reps
+
+    h2d_ms = link_ms(lambda: (L.x.copy_(h_x, non_blocking=True), L.logits.copy_(h_l, non_blocking=True),
+                              L.dout.copy_(h_d, non_blocking=True)))
+    d2h_ms = link_ms(lambda: (h_out.copy_(L.out, non_blocking=True), h_dx.copy_(L.dx, non_blocking=True),
+                              h_dl.copy_(L.dlogits, non_blocking=True)))
+
     peaks, psrc = _peaks()
     mx_peak = 2.0 * peaks["bf16_tflops_sustained"]     # nominal fp8/bf16 dense ratio 4.5/2.25
     traffic = _gemm_traffic() if args.workload == "deepseek-v3" and not S else None
@@ -284,7 +302,8 @@ def run_gpu(args, rank, world, local_rank):
                      "traffic_unit": "bytes per launch (DRAM read+write, ncu, mean of the step's 6 launches)",
                      "algorithmic_bytes_per_launch": round(algo_bytes / GEMMS_PER_STEP)},
         "e2e": {"value": round(job_tflops(flops, world, e2e_ms), 2), "unit": "TFLOPS",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_gbs": round(h2d / (h2d_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (d2h_ms * 1e-3) / 1e9, 1)},
         "gpu_launches": (KERNELS_PER_STEP + (ROUTER_KERNELS if args.router else 0) + (2 if S else 0)) * args.steps,
         "clocks": clk.summary(),
     }
