@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (assert_bf16_close, assert_fp32_close, atoms_to_rowmajor, batched_weight_operand, deq_rows,
+from helpers import (assert_bf16_close, assert_fp32_close, atoms_to_rowmajor, batched_weight_operand,
                      glu_perm, gpu_ops, to_np)
 from grouped_gemm_top_gb300 import synth
 

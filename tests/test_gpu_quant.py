@@ -5,7 +5,6 @@ import torch
 
 import oracle as O
 from helpers import atoms_to_rowmajor, atoms_rows_subset, glu_perm, gpu_ops, padded_layout, to_np
-from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
