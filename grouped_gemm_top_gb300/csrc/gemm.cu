@@ -678,7 +678,7 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {
         p.n_tiles = N / bn2;
-        if (getenv("MOE_GEMM_BAND") == nullptr) p.band = 4;
+        if (getenv("MOE_GEMM_BAND") == nullptr) p.band = 2;     // measured: 2 beat 4, 8 and 16
         const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles
                                                            : (M / BM) * (int64_t)p.n_tiles;
         const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm(bn2));
