@@ -635,7 +635,9 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     p.aux = (const __nv_bfloat16*)epi_aux;
     p.err = err;
     p.timeout_ns = 2000000000ull;   // 2 s per wait
-    p.band = 4;                       // m-tiles per raster band (measured: 4 beat 8 by 0.2 ms a step)
+    // m-tiles per raster band: 3 for long contractions, 4 for K <= 2048
+    // (measured on the DeepSeek-V3 layer against 2, 4, 8, 16 and 32)
+    p.band = K <= 2048 ? 4 : 3;
     if (const char* e = getenv("MOE_GEMM_BAND")) p.band = std::max(1, atoi(e));
     p.n_tiles = N / BN;
     int64_t upper_tiles;
