@@ -61,12 +61,14 @@ def _deq_actT(q, s, C, M, Rp):
 
 @pytest.mark.parametrize("score,norm,S,T,E0,k0", [("softmax", True, 0, 256, 8, 2), ("sigmoid", True, 0, 256, 8, 2),
                                                  ("softmax", True, 1, 256, 8, 2), ("sigmoid", True, 2, 256, 8, 2),
-                                                 ("softmax", False, 0, 1000, 5, 3), ("sigmoid", True, 1, 77, 6, 4)])
+                                                 ("softmax", False, 0, 1000, 5, 3), ("sigmoid", True, 1, 77, 6, 4),
+                                                 ("softmax", True, 0, 256, 4, 4), ("sigmoid", False, 0, 300, 1, 1)])
 def test_tiny_layer_stagewise(ops, score, norm, S, T, E0, k0):
     """Small dropless layers (d=512, f=256; T tokens, E0 routed experts,
     top-k0, S shared experts; T=1000 and T=77 give ragged groups and a
-    token count that is not a multiple of any tile): every stage of fwd
-    and bwd against the oracle applied to the GPU's own stage inputs."""
+    token count that is not a multiple of any tile; k = E sends every token
+    to every expert; E = k = 1 is a dense FFN): every stage of fwd and bwd
+    against the oracle applied to the GPU's own stage inputs."""
     d, f = 512, 256
     L, inp = _layer(ops, T, d, E0, k0, f, score, norm, n_shared=S)
     E, k = E0 + S, k0 + S          # expert groups and choices per token
