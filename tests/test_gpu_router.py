@@ -62,15 +62,16 @@ def test_combine_add(ops):
     assert_bf16_close(out, ref, what="combine + addend")
 
 
-@pytest.mark.parametrize("score", ["softmax", "sigmoid"])
-def test_tiny_layer_with_router_stagewise(ops, score):
+@pytest.mark.parametrize("score,S", [("softmax", 0), ("sigmoid", 0), ("sigmoid", 1)])
+def test_tiny_layer_with_router_stagewise(ops, score, S):
     """logits = x W_r on the GPU (fp32, against the oracle on the same bf16
-    operands), routing from the GPU's logits bit-exact, the router backward
-    from the GPU's dlogits, and dx = dx_moe + dx_r."""
+    operands), routing from the GPU's logits bit-exact (with S shared
+    experts appended), the router backward from the GPU's dlogits, and
+    dx = dx_moe + dx_r."""
     from grouped_gemm_top_gb300.layer import MoELayer
     T, d, E, k, f = 256, 512, 8, 2, 256
-    L = MoELayer(T, d, E, k, f, score, True, router=True)
-    inp = synth.make_layer_inputs(T, d, E, f, "cuda")
+    L = MoELayer(T, d, E, k, f, score, True, router=True, n_shared=S)
+    inp = synth.make_layer_inputs(T, d, E, f, "cuda", n_shared=S)
     L.set_weights(inp["W1"], inp["W2"])
     Wr = synth.make_normal_bf16((d, E), 21, "cuda", std=0.05)
     L.set_router_weights(Wr)
@@ -83,7 +84,9 @@ def test_tiny_layer_with_router_stagewise(ops, score):
     assert_fp32_close(L.logits, O.router_logits(x, Wn), what="logits")
     logits = L.logits.cpu().numpy()
     idx, w = O.route_topk(logits, k, score, True)
-    assert np.array_equal(L.topk_idx.cpu().numpy(), idx)
+    assert np.array_equal(L.route_idx.cpu().numpy(), idx)
+    idx_all, _ = O.append_shared(idx, w, E, S)
+    assert np.array_equal(L.topk_idx.cpu().numpy(), idx_all)
     dl = L.dlogits.double().cpu().numpy()
     dx_r, dWr = O.router_backward(x, Wn, dl)
     assert_fp32_close(L.dx_r, dx_r, what="dx_r")
