@@ -221,16 +221,17 @@ def run_gpu(args, rank, world, local_rank):
     h_dl = torch.empty((T, E), dtype=torch.float32).pin_memory()
     # steps through MoELayer.run_pipelined: every step copies its inputs in
     # and its outputs out; step i+1's input copy and step i-1's output copy
-    # overlap step i's kernels (double-buffered device inputs and outputs)
+    # overlap step i's kernels (three sets of device inputs and outputs)
     batch = (h_x, h_l, h_d, h_out, h_dx, h_dl)
-    L.run_pipelined([batch] * 2)
+    L.run_pipelined([batch] * 3)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    e0.record(stream)
-    L.run_pipelined([batch] * args.steps)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk_e2e:
+        barrier()
+        e0.record(stream)
+        L.run_pipelined([batch] * args.steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
     h2d = h_x.numel() * 2 + h_l.numel() * 4 + h_d.numel() * 2
     d2h = h_out.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
@@ -303,7 +304,8 @@ def run_gpu(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": round(algo_bytes / GEMMS_PER_STEP)},
         "e2e": {"value": round(job_tflops(flops, world, e2e_ms), 2), "unit": "TFLOPS",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "h2d_gbs": round(h2d / (h2d_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (d2h_ms * 1e-3) / 1e9, 1)},
+                "h2d_gbs": round(h2d / (h2d_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (d2h_ms * 1e-3) / 1e9, 1),
+                "clocks": clk_e2e.summary()},
         "gpu_launches": (KERNELS_PER_STEP + (ROUTER_KERNELS if args.router else 0) + (2 if S else 0)) * args.steps,
         "clocks": clk.summary(),
     }

@@ -276,16 +276,20 @@ class MoELayer:
     # ------------------------------------------- pipelined host stepping ----
     _IO = ("x", "logits", "dout", "out", "dx", "dlogits")
 
-    def enable_pipelining(self, warmup=1):
-        """Second set of input/output buffers and one CUDA graph per set, so
-        that run_pipelined() can copy step i+1's inputs in and step i-1's
-        outputs out while step i computes."""
+    def enable_pipelining(self, warmup=1, nsets=3):
+        """nsets buffer sets of the step's inputs and outputs and one CUDA
+        graph per set, so that run_pipelined() can copy later steps' inputs
+        in and earlier steps' outputs out while a step computes.  With three
+        sets, step i's inputs wait for step i-3's outputs to leave, so the
+        copies have two steps' compute time to finish (with two, a slow host
+        link would have to move one step's outputs and the next inputs within
+        a single step)."""
         if getattr(self, "_sets", None) is not None:
             return
         first = {n: getattr(self, n) for n in self._IO}
-        second = {n: torch.zeros_like(t) for n, t in first.items()}
+        sets = [first] + [{n: torch.zeros_like(t) for n, t in first.items()} for _ in range(nsets - 1)]
         graphs = []
-        for bufs in (first, second):
+        for bufs in sets:
             for n, t in bufs.items():
                 setattr(self, n, t)
             self.graph = None
@@ -293,7 +297,7 @@ class MoELayer:
         for n, t in first.items():
             setattr(self, n, t)
         self.graph = graphs[0]
-        self._sets = (first, second)
+        self._sets = tuple(sets)
         self._graphs = graphs
         self._h2d_stream = torch.cuda.Stream(device=self.device)
         self._d2h_stream = torch.cuda.Stream(device=self.device)
@@ -301,20 +305,21 @@ class MoELayer:
     def run_pipelined(self, batches):
         """Run one fwd+bwd step per element of `batches`, each a tuple
         (x, logits, dout, out_host, dx_host, dlogits_host) of host tensors
-        (pinned, for asynchronous copies).  Step i uses buffer set i % 2: its
-        inputs are copied in on an input-copy stream (once step i-2's outputs
-        have left that set), the step's graph runs on the current stream, and
-        its outputs are copied out on an output-copy stream while step i+1
-        computes (the GPU's copy engines run both directions beside the
-        kernels).  Returns with the current stream ordered after the last
-        copy.  The weight gradients and the error word are those of the last
-        step."""
+        (pinned, for asynchronous copies).  Step i uses buffer set i % nsets:
+        its inputs are copied in on an input-copy stream (once the outputs of
+        the last step that used the set have been copied out), the step's
+        graph runs on the current stream, and its outputs are copied out on
+        an output-copy stream while later steps compute (the GPU's copy
+        engines run both directions beside the kernels).  Returns with the
+        current stream ordered after the last copy.  The weight gradients
+        and the error word are those of the last step."""
         self.enable_pipelining()
         comp = torch.cuda.current_stream(self.device)
         h2d, d2h = self._h2d_stream, self._d2h_stream
-        free = [None, None]          # events: the set's outputs have been copied out
+        nsets = len(self._sets)
+        free = [None] * nsets        # events: the set's outputs have been copied out
         for i, (x, logits, dout, out_h, dx_h, dl_h) in enumerate(batches):
-            b = i % 2
+            b = i % nsets
             bufs = self._sets[b]
             with torch.cuda.stream(h2d):
                 if free[b] is not None:
