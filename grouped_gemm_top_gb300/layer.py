@@ -259,7 +259,11 @@ class MoELayer:
     # ------------------------------------------------------- public API ----
     def step(self, x, logits, dout, out_host=None, dx_host=None, dlogits_host=None):
         """End-to-end step from host (or device) tensors: copy the inputs in,
-        run fwd+bwd, copy out, dx and dlogits back.  Returns those three."""
+        run fwd+bwd, copy out, dx and dlogits back.  Returns those three.
+        Outputs for which a host tensor is given are copied asynchronously
+        into it (pinned memory): synchronize the current stream before
+        reading them; the others are returned as new CPU tensors (a
+        synchronous copy)."""
         self.x.copy_(x, non_blocking=True)
         self.logits.copy_(logits, non_blocking=True)
         self.dout.copy_(dout, non_blocking=True)
