@@ -458,8 +458,10 @@ def permute(x, row_id, k):
 
 def fp32_round(x):
     """Round fp64 values to the nearest fp32 value, ties to even (IEEE-754
-    binary32: 24 significant bits)."""
-    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+    binary32: 24 significant bits); magnitudes beyond the fp32 range become
+    inf, as the cast does."""
+    with np.errstate(over="ignore"):
+        return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
 
 
 def permute_scaled_bf16(src, row_id, k, w):
