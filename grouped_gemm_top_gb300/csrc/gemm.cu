@@ -799,7 +799,8 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
                                            void* d, int32_t* err, void* stream) {
     using namespace gg;
     MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD || mode == MOE_GEMM_WGRAD, MOE_ERR_INVALID_ARG);
-    MOE_REQUIRE(epilogue == MOE_EPI_NONE || epilogue == MOE_EPI_NONE_F32, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(epilogue == MOE_EPI_NONE || (epilogue == MOE_EPI_NONE_F32 && mode != MOE_GEMM_WGRAD),
+                MOE_ERR_INVALID_ARG);      // WGRAD writes bf16 (an empty group's tile is zero-filled as bf16)
     MOE_REQUIRE(a && a_sf && a_scale && b && b_sf && b_scale && gofs && d, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(G >= 1 && G <= MAX_G && M > 0 && N > 0 && K > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(M % 128 == 0 && N % 256 == 0 && K % 256 == 0 && M <= 0x7FFFFF80LL && K <= (1LL << 30),

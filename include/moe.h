@@ -530,7 +530,8 @@ MOE_API moe_status_t nvfp4_quantize_cols(const void* src, int64_t rows, int cols
  *                      of 128-row tiles ends with a half 256-row k-step.
  *   d                  [G, M, N]; an empty group's D_g is written as zeros.
  * All modes: M % 128 == 0, N % 256 == 0, K % 256 == 0; epilogue
- * MOE_EPI_NONE (bf16 d) or MOE_EPI_NONE_F32 (fp32 d); d 32-byte aligned;
+ * MOE_EPI_NONE (bf16 d) or, for FWD and DGRAD, MOE_EPI_NONE_F32 (fp32 d);
+ * d 32-byte aligned;
  * bad offsets -> MOE_ERR_BAD_OFFSETS in err; every wait inside the kernel is
  * bounded (MOE_ERR_DEVICE_TIMEOUT in err).
  */

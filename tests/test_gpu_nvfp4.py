@@ -213,3 +213,15 @@ def test_nvfp4_wgrad_matches_oracle(ops, sizes, M, N):
             assert torch.all(d[g] == 0)
         else:
             assert_bf16_close(d[g], ref[g], what=f"nvfp4 dW[{g}]")
+
+
+def test_nvfp4_wgrad_rejects_fp32_output(ops):
+    """The weight gradient is written in bf16 (an empty group's tile is
+    zero-filled in bf16): fp32 output is refused on the host."""
+    X, gofs = _grouped_rows([128, 0], 128, 3)
+    gofs_t = torch.from_numpy(gofs.astype(np.int32)).cuda()
+    aq, asf, ast = ops.nvfp4_quantize_cols(X, gofs_t, 2)
+    with pytest.raises(ops.MoEError):
+        ops.grouped_gemm_nvfp4(ops.MOE_GEMM_WGRAD, aq, asf, ast, aq, asf, ast, gofs_t, 2, 128, 256, X.shape[0],
+                               ops.MOE_EPI_NONE_F32)
+
