@@ -95,6 +95,28 @@ def test_fwd_ngk(ops, sizes, K, N):
         assert torch.all(d[gofs[g] + m:gofs[g + 1]] == 0)
 
 
+def test_fwd_max_groups(ops):
+    """1024 groups (the largest G the kernels take), most of them empty or a
+    few rows: the group offsets all fit the kernel's shared copy and every
+    tile finds its group; G = 1025 is refused on the host."""
+    rng = np.random.default_rng(5)
+    G, K, N = 1024, 128, 256
+    sizes = np.where(rng.random(G) < 0.7, 0, rng.integers(1, 40, G)).tolist()
+    x, gofs_t, gofs = _act(sizes, K, seed=31)
+    M = x.shape[0]
+    xq, xs, A = _quant_rows(ops, x)
+    bq, bs, B = _weights(ops, G, K, N, seed=32, layout=ops.MOE_B_GNK)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, ops.MOE_B_GNK, gofs_t, G, M, N, K, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    Rp = int(gofs[-1])
+    assert_bf16_close(d[:Rp], O.grouped_gemm(A, B, gofs)[:Rp], what="fwd, 1024 groups")
+    gofs2 = torch.cat([gofs_t, gofs_t[-1:]])
+    with pytest.raises(ops.MoEError):
+        ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, xq, xs, bq, bs, ops.MOE_B_GNK, gofs2, G + 1, M, N, K, err=err)
+
+
 @pytest.mark.parametrize("sizes,K,N", [([300, 0, 5], 512, 256), ([1000, 24], 1024, 768)])
 def test_fwd_gnk_batched_weights(ops, sizes, K, N):
     G = len(sizes)
