@@ -67,7 +67,8 @@ def test_route_empty_batch(ops):
     assert counts.sum().item() == 0 and offsets.cpu().tolist() == [0] * 9
 
 
-@pytest.mark.parametrize("T,E,k,d", [(256, 8, 2, 512), (1000, 64, 6, 256), (24576, 256, 8, 7168), (3, 8, 2, 128)])
+@pytest.mark.parametrize("T,E,k,d", [(256, 8, 2, 512), (1000, 64, 6, 256), (24576, 256, 8, 7168), (3, 8, 2, 128),
+                                     (500, 1024, 32, 128)])       # the largest E and k
 def test_permute(ops, T, E, k, d):
     logits = synth.make_logits(T, E, 0, "cuda")
     x = synth.make_normal_bf16((T, d), 1, "cuda")
