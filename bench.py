@@ -797,6 +797,65 @@ def run_compare(args, capacity_factors=(1.0, 1.25)):
                         "max_expert_rows": int(counts.max()), "mean_expert_rows": T * k / E, "arms": arms}}
 
 
+def run_vendor_point(M, N, K, steps=10, warmup=3, device="cuda:0"):
+    """One dense MXFP8 GEMM D[M,N] = A[M,K] B[N,K]^T (bf16 out) timed two
+    ways on the same E4M3 codes: the library's block-scaled GEMM
+    (torch._scaled_mm with E8M0 scales per 32, which calls cuBLASLt) and our
+    grouped GEMM with one group.  This is context for the grouped kernel's
+    roofline fraction: the rate a vendor GEMM reaches on this GPU for the
+    same contraction.  The library's scales are all 1.0 (the values do not
+    change the time); A is larger than L2, so no flush is needed."""
+    import torch
+
+    from grouped_gemm_top_gb300 import ops, synth
+    ops.moe_init(torch.device(device).index or 0)
+    a = synth.make_normal_bf16((M, K), 1, device)
+    aq, asf = ops.mxfp8_group_quantize(a, ops.MOE_QUANT_ROWWISE)
+    del a
+    b = synth.make_normal_bf16((N, K), 2, device)
+    bq, bsf = ops.mxfp8_group_quantize(b, ops.MOE_QUANT_ROWWISE)
+    del b
+    gofs = torch.tensor([0, M], dtype=torch.int32, device=device)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(steps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / steps
+
+    flops = 2.0 * M * N * K
+    peaks, psrc = _peaks()
+    mx_peak = 2.0 * peaks["bf16_tflops"]
+    out = {"M": M, "N": N, "K": K, "peak_tflops": mx_peak, "peak_source": f"2 x {psrc} bf16 burst"}
+    ms = timed(lambda: ops.grouped_gemm_mxfp8(ops.MOE_GEMM_FWD, aq, asf, bq, bsf, ops.MOE_B_GNK, gofs, 1,
+                                              M, N, K, d=d, err=err))
+    assert int(err.item()) == 0, int(err.item())
+    out["ours"] = {"ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+    try:
+        def round_up(v, m):
+            return (v + m - 1) // m * m
+        sa = torch.full((round_up(M, 128) * round_up(K // 32, 4),), 127, dtype=torch.uint8, device=device)
+        sb = torch.full((round_up(N, 128) * round_up(K // 32, 4),), 127, dtype=torch.uint8, device=device)
+        sa, sb = sa.view(torch.float8_e8m0fnu), sb.view(torch.float8_e8m0fnu)
+        A8, B8 = aq.view(torch.float8_e4m3fn), bq.view(torch.float8_e4m3fn).t()   # B column-major [K, N]
+        ms = timed(lambda: torch._scaled_mm(A8, B8, sa, sb, out_dtype=torch.bfloat16))
+        out["library"] = {"call": "torch._scaled_mm (cuBLASLt, MXFP8 1x32)", "ms": round(ms, 4),
+                          "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+        out["ours_over_library"] = round(out["library"]["ms"] / out["ours"]["ms"], 3)
+    except Exception as e:          # the installed torch may not offer MXFP8 _scaled_mm
+        out["library"] = {"unavailable": f"{type(e).__name__}: {str(e).splitlines()[0][:200]}"}
+    out["frac_ours"] = round(out["ours"]["tflops"] / mx_peak, 4)
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -825,6 +884,9 @@ def main():
     ap.add_argument("--compare", action="store_true",
                     help="time the grouped dropless step against a per-expert GEMM loop and capacity-based MoE on "
                          "the same workload and print one line")
+    ap.add_argument("--vendor-point", nargs=3, type=int, metavar=("M", "N", "K"),
+                    help="time one dense MXFP8 GEMM with the library's block-scaled GEMM (torch._scaled_mm) and "
+                         "with ours (one group) and print one line")
     ap.add_argument("--hbm-probe", action="store_true",
                     help="measure write-only and copy HBM bandwidth (PyTorch fill/copy kernels) and print one line")
     args = ap.parse_args()
@@ -833,6 +895,10 @@ def main():
         return
     if args.compare:
         print(json.dumps(run_compare(args)), flush=True)
+        return
+    if args.vendor_point:
+        print(json.dumps({"vendor_point": run_vendor_point(*args.vendor_point, steps=args.steps,
+                                                           warmup=max(args.warmup, 3))}), flush=True)
         return
     if args.seeds:
         print(json.dumps(run_seeds(args)), flush=True)
