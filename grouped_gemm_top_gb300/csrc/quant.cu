@@ -269,9 +269,15 @@ __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
-// amax of packed bf16 pairs: max of |lo| and |hi| over the words, as bf16
-// bits (non-negative bf16 bit patterns order like their values)
-__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) { return __vmaxu2(m, w & 0x7FFF7FFFu); }
+// amax of packed bf16 pairs, one instruction per word: each half of the
+// result has the larger magnitude of the two inputs' halves (and the XOR
+// of their signs, so mask the sign bits with 0x7FFF7FFF before use; the
+// masked halves are bf16 bits of the block maxima).  Finite inputs.
+__device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 __device__ __forceinline__ float bf16_bits_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_bits_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -368,10 +374,9 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
                 *cp = v;
             }
             if (codes_r != nullptr) {
-                uint32_t m = bf16x2_absmax(bf16x2_absmax(0u, v.x), v.y);
-                m = bf16x2_absmax(bf16x2_absmax(m, v.z), v.w);
-                m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-                m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                uint32_t m = bf16x2_maxabs(bf16x2_maxabs(v.x, v.y), bf16x2_maxabs(v.z, v.w));
+                m = bf16x2_maxabs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                m = bf16x2_maxabs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2)) & 0x7FFF7FFFu;
                 const uint32_t sb = e8m0_scale_byte(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16));
                 const float inv = e8m0_inv_scale(sb);
                 const uint32_t q0 = cvt_e4m3x2(bf16_bits_lo(v.x) * inv, bf16_bits_hi(v.x) * inv);
@@ -392,7 +397,8 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
             // pass 1: amax of both columns over the block, on packed bf16 bits
             uint32_t m = 0;
 #pragma unroll 8
-            for (int e = 0; e < 32; ++e) m = bf16x2_absmax(m, colp[e * (kQT / 2)]);
+            for (int e = 0; e < 32; ++e) m = bf16x2_maxabs(m, colp[e * (kQT / 2)]);
+            m &= 0x7FFF7FFFu;
             const uint32_t b0 = e8m0_scale_byte(__uint_as_float((m & 0xFFFFu) << 16));
             const uint32_t b1 = e8m0_scale_byte(__uint_as_float(m & 0xFFFF0000u));
             const float i0 = e8m0_inv_scale(b0), i1 = e8m0_inv_scale(b1);
@@ -465,10 +471,9 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
 constexpr int kSBSmem = 2 * kQBInBytes + 4 * 512;
 
 __device__ __forceinline__ uint2 quant_row_chunk(uint4 v, uint32_t& sb_out) {
-    uint32_t m = bf16x2_absmax(bf16x2_absmax(0u, v.x), v.y);
-    m = bf16x2_absmax(bf16x2_absmax(m, v.z), v.w);
-    m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    uint32_t m = bf16x2_maxabs(bf16x2_maxabs(v.x, v.y), bf16x2_maxabs(v.z, v.w));
+    m = bf16x2_maxabs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = bf16x2_maxabs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2)) & 0x7FFF7FFFu;
     const uint32_t sb = e8m0_scale_byte(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16));
     const float inv = e8m0_inv_scale(sb);
     const uint32_t q0 = cvt_e4m3x2(bf16_bits_lo(v.x) * inv, bf16_bits_hi(v.x) * inv);
@@ -486,7 +491,8 @@ __device__ __forceinline__ void quant_col_block(const uint16_t* tile, int blk, i
     const uint32_t* colp = reinterpret_cast<const uint32_t*>(tile + blk * 32 * kQT + col);
     uint32_t m = 0;
 #pragma unroll 8
-    for (int e = 0; e < 32; ++e) m = bf16x2_absmax(m, colp[e * (kQT / 2)]);
+    for (int e = 0; e < 32; ++e) m = bf16x2_maxabs(m, colp[e * (kQT / 2)]);
+    m &= 0x7FFF7FFFu;
     b0 = e8m0_scale_byte(__uint_as_float((m & 0xFFFFu) << 16));
     b1 = e8m0_scale_byte(__uint_as_float(m & 0xFFFF0000u));
     const float i0 = e8m0_inv_scale(b0), i1 = e8m0_inv_scale(b1);
