@@ -278,6 +278,12 @@ __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
     asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+// 32 bytes to a 32-byte aligned global address in one instruction
+__device__ __forceinline__ void st_global_32B(void* dst, const uint32_t* q) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(q[0]), "r"(q[1]),
+                 "r"(q[2]), "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7])
+                 : "memory");
+}
 __device__ __forceinline__ float bf16_bits_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_bits_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -332,7 +338,20 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
         s_src[j] = (int32_t)sr;                // < 2^31: checked on the host
         s_w[j] = w;
     }
-    // copy assignment: chunk p of a thread = row tr + 16p, 8 columns at tc*8
+    // Row/block assignment (copy and rowwise pass): a thread owns row qr
+    // of the tile and its 32-element blocks qb and qb + 2 (4 x 16 bytes
+    // each).  The 8 threads of a quarter warp hold rows qr + 32t (t = 0..3)
+    // of blocks qb = 0, 1 (or 2, 3).  The tile sits in shared memory with
+    // its 16-byte chunks swizzled by 32-row block: chunk c of row r is
+    // stored at chunk c ^ ((r >> 5) & 3).  The rowwise 16-byte reads of a
+    // quarter warp then fall on 8 distinct bank groups, and the columnwise
+    // pass (one 32-row block per warp) reads with a per-thread constant
+    // offset.
+    const int qr = (tid >> 3) + 32 * (tid & 3), qb = (tid >> 2) & 1;
+    const int qsw = (qr >> 5) & 3;
+    // copy assignment (16 threads per row, 16 contiguous bytes each, so
+    // every copy instruction reads whole 256-byte row segments): chunk p of
+    // a thread = chunk tc of row tr + 16p
     const int tc = tid & 15, tr = tid >> 4;
     const uint32_t s_in_addr = (uint32_t)__cvta_generic_to_shared(s_in);
     auto issue = [&](int i) {
@@ -342,7 +361,8 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
             const int rl = tr + 16 * p;
             const int64_t sr = s_src[i * kQT + rl];
             const uint16_t* g = src + (sr >= 0 ? sr : 0) * cols + (int64_t)ct * kQT + tc * 8;
-            cp_async16(s_in_addr + (uint32_t)(buf * kQBInBytes + (rl * kQT + tc * 8) * 2), g, sr >= 0 ? 16u : 0u);
+            const int pc = tc ^ ((rl >> 5) & 3);
+            cp_async16(s_in_addr + (uint32_t)(buf * kQBInBytes + (rl * kQT + pc * 8) * 2), g, sr >= 0 ? 16u : 0u);
         }
     };
     __syncthreads();                          // the gather plan is complete
@@ -358,34 +378,50 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
         if (i + 1 < nrt) issue(i + 1);
         cp_async_commit();
         cp_async_wait1();                     // this thread's copies of tile i have landed
-        // rowwise, over this thread's own chunks (scaled in place first)
-#pragma unroll 2
-        for (int p = 0; p < 8; ++p) {
-            const int rl = tr + 16 * p;
-            uint4* cp = reinterpret_cast<uint4*>(tile + rl * kQT + tc * 8);
-            uint4 v = *cp;
-            if (row_w != nullptr) {
-                float f[8];
-                unpack8(v, f);
-                const float w = s_w[i * kQT + rl];
+        __syncthreads();                      // ... and every other thread's
+        // rowwise, over this thread's own blocks (scaled in place first):
+        // one 32-element block per step, so one scale per block and thread
+        uint8_t* crow = reinterpret_cast<uint8_t*>(codes_r) + (r0 + qr) * cols + (int64_t)ct * kQT;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] *= w;
-                v = pack8(f);
-                *cp = v;
+        for (int u = 0; u < 2; ++u) {
+            const int qbu = qb + 2 * u;
+            uint4 v[4];
+            uint4* cp[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                cp[j] = reinterpret_cast<uint4*>(tile + qr * kQT + (((4 * qbu + j) ^ qsw) * 8));
+                v[j] = *cp[j];
+            }
+            if (row_w != nullptr) {
+                const float w = s_w[i * kQT + qr];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float f[8];
+                    unpack8(v[j], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] *= w;
+                    v[j] = pack8(f);
+                    *cp[j] = v[j];
+                }
             }
             if (codes_r != nullptr) {
-                uint32_t m = bf16x2_maxabs(bf16x2_maxabs(v.x, v.y), bf16x2_maxabs(v.z, v.w));
-                m = bf16x2_maxabs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-                m = bf16x2_maxabs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2)) & 0x7FFF7FFFu;
+                uint32_t m = bf16x2_maxabs(bf16x2_maxabs(v[0].x, v[0].y), bf16x2_maxabs(v[0].z, v[0].w));
+#pragma unroll
+                for (int j = 1; j < 4; ++j)
+                    m = bf16x2_maxabs(m, bf16x2_maxabs(bf16x2_maxabs(v[j].x, v[j].y), bf16x2_maxabs(v[j].z, v[j].w)));
+                m &= 0x7FFF7FFFu;
                 const uint32_t sb = e8m0_scale_byte(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16));
                 const float inv = e8m0_inv_scale(sb);
-                const uint32_t q0 = cvt_e4m3x2(bf16_bits_lo(v.x) * inv, bf16_bits_hi(v.x) * inv);
-                const uint32_t q1 = cvt_e4m3x2(bf16_bits_lo(v.y) * inv, bf16_bits_hi(v.y) * inv);
-                const uint32_t q2 = cvt_e4m3x2(bf16_bits_lo(v.z) * inv, bf16_bits_hi(v.z) * inv);
-                const uint32_t q3 = cvt_e4m3x2(bf16_bits_lo(v.w) * inv, bf16_bits_hi(v.w) * inv);
-                codes_r[((r0 + rl) * cols + (int64_t)ct * kQT) / 8 + tc] = make_uint2(q0 | (q1 << 16), q2 | (q3 << 16));
-                if ((tc & 3) == 0)
-                    s_atom_r[b * 512 + (rl & 31) * 16 + ((rl >> 5) & 3) * 4 + (tc >> 2)] = (uint8_t)sb;
+                uint32_t q[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    q[2 * j] = cvt_e4m3x2(bf16_bits_lo(v[j].x) * inv, bf16_bits_hi(v[j].x) * inv) |
+                               (cvt_e4m3x2(bf16_bits_lo(v[j].y) * inv, bf16_bits_hi(v[j].y) * inv) << 16);
+                    q[2 * j + 1] = cvt_e4m3x2(bf16_bits_lo(v[j].z) * inv, bf16_bits_hi(v[j].z) * inv) |
+                                   (cvt_e4m3x2(bf16_bits_lo(v[j].w) * inv, bf16_bits_hi(v[j].w) * inv) << 16);
+                }
+                st_global_32B(crow + qbu * 32, q);   // one whole 32-byte sector
+                s_atom_r[b * 512 + (qr & 31) * 16 + qsw * 4 + qbu] = (uint8_t)sb;
             }
         }
         __syncthreads();                      // A: tile i (scaled) complete
@@ -393,7 +429,10 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
         const int blk = warp & 3;                       // 32-row block
         const int col = (warp >> 2) * 64 + 2 * lane;    // two columns per lane
         if (codes_c != nullptr) {
-            const uint32_t* colp = reinterpret_cast<const uint32_t*>(tile + blk * 32 * kQT + col);
+            // the block's rows are swizzled by blk: columns col, col + 1 sit
+            // in chunk (col / 8) ^ blk
+            const uint32_t* colp = reinterpret_cast<const uint32_t*>(tile + blk * 32 * kQT +
+                                                                     (((col >> 3) ^ blk) << 3) + (col & 7));
             // pass 1: amax of both columns over the block, on packed bf16 bits
             uint32_t m = 0;
 #pragma unroll 8
@@ -680,6 +719,7 @@ extern "C" moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows,
     MOE_REQUIRE(codes_row != nullptr || codes_col != nullptr, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(rows % kQT == 0 && cols % kQT == 0, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(cols / kQT <= 65535 && rows <= 0x7FFFFFFF, MOE_ERR_UNSUPPORTED);
+    MOE_REQUIRE(codes_row == nullptr || (reinterpret_cast<uintptr_t>(codes_row) & 31) == 0, MOE_ERR_ALIGNMENT);
     MOE_REQUIRE(moe_aligned16(src) && (codes_row == nullptr || (moe_aligned16(codes_row) && moe_aligned16(scales_row))) &&
                     (codes_col == nullptr || (moe_aligned16(codes_col) && moe_aligned16(scales_col))),
                 MOE_ERR_ALIGNMENT);

@@ -231,7 +231,8 @@ MOE_API moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols,
  *             both NULL.
  *   codes_col, scales_col   exactly MOE_QUANT_COLWISE_GROUPED's output for
  *             P (codes [cols, rows]), or both NULL.  At least one pair.
- * All pointers are device pointers; outputs 16-byte aligned.
+ * All pointers are device pointers; outputs 16-byte aligned, codes_row
+ * 32-byte aligned (MOE_ERR_ALIGNMENT otherwise).
  */
 MOE_API moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, int cols, int k,
                                    const int32_t* row_id,
