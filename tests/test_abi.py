@@ -64,6 +64,11 @@ def test_host_only_calls_and_argument_checks(lib_path):
                                 ctypes.c_void_p(16), 0, ctypes.c_void_p(16), 4, 256, 256, 256, 0, None,
                                 ctypes.c_void_p(16), None, None, None)
     assert st == ops.MOE_ERR_ALIGNMENT
+    # the gathered quantization writes rowwise codes as 32-byte sectors:
+    # a 16-byte aligned codes_row is refused
+    st = lib.mxfp8_gather_quantize(ctypes.c_void_p(64), 256, 128, 1, None, None, ctypes.c_void_p(64), 1, 256,
+                                   ctypes.c_void_p(48), ctypes.c_void_p(64), None, None, None, None)
+    assert st == ops.MOE_ERR_ALIGNMENT
 
 
 def test_product_does_not_import_the_oracle():
