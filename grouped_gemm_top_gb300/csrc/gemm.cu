@@ -539,14 +539,15 @@ static bool make_sf_map(CUtensorMap* m, const void* base, int64_t atoms, int box
     return r == CUDA_SUCCESS;
 }
 
-// bf16 output [rows, N] for TMA stores: 32-row x 64-column boxes (128-byte
-// rows, 128-byte swizzle).
+// bf16 output [rows, N] for TMA stores: 32-row x kEpiBoxCols-column boxes
+// (rows of 128 bytes with the 128-byte swizzle, or 64 with the 64-byte one).
 static bool make_d_map(CUtensorMap* m, void* base, int64_t rows, int N) {
     cuuint64_t gdim[2] = {(cuuint64_t)N, (cuuint64_t)rows}, gstr[1] = {(cuuint64_t)N * 2};
-    cuuint32_t box[2] = {64, 32}, estr[2] = {1, 1};
+    cuuint32_t box[2] = {(cuuint32_t)gg::kEpiBoxCols, 32}, estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstr, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          gg::kEpiBoxCols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

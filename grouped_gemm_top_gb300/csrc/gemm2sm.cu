@@ -47,7 +47,7 @@ struct C2 {
     static constexpr int BN = BN_;
     static constexpr int BH = BN_ / 2;                  // B rows per CTA
     static constexpr int NACC = BN_ == 128 ? 2 : 1;
-    static constexpr int STAGES = BN_ == 128 ? 8 : 5;
+    static constexpr int STAGES = BN_ == 128 ? 8 : (NVF4 || kEpiBoxCols == 64 ? 5 : 6);
     static constexpr int A_STAGE = BM * BK;             // this CTA's 128 A rows
     static constexpr int B_STAGE = BH * BK;             // this CTA's half of B
     static constexpr int SFA_BYTES = NVF4 ? 2048 : 512;
@@ -55,8 +55,8 @@ struct C2 {
     static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_BYTES + SFB_BYTES;
     static constexpr uint32_t SF0 = NACC * BN_;         // TMEM: accumulators, then scales
     static constexpr uint32_t SF_COLS = NVF4 ? 16 + 16 * (BN_ / 128) : TMEM_SF_STRIDE;
-    // TMA-store staging of the epilogue (N = 256): 4 KB per epilogue warp
-    static constexpr int EPI_BYTES = (BN_ == 256 && !NVF4) ? EPI_WARPS * 4096 : 0;
+    // TMA-store staging of the epilogue (N = 256): one box per epilogue warp
+    static constexpr int EPI_BYTES = (BN_ == 256 && !NVF4) ? EPI_WARPS * kEpiBoxBytes : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;       // 1024-byte aligned
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else if constexpr (EPI == MOE_EPI_SWIGLU_BWD) {
                 epilogue_swiglu_bwd<BN>(p, tacc, row, ti.nt, half, release, apre);
             } else if (!NVF4 && BN == 256 && EPI == MOE_EPI_NONE && p.tma_store) {
-                epilogue_tile_tma(&tmD, smem_u32(smem + C::OFF_EPI + 4096 * ew), tacc, row - lane, ti.nt, half, lane,
+                epilogue_tile_tma(&tmD, smem_u32(smem + C::OFF_EPI + kEpiBoxBytes * ew), tacc, row - lane, ti.nt, half, lane,
                                   release);
             } else if constexpr (BN == 256) {
                 epilogue_tile_staged<EPI, NVF4>(p, tacc, row, ti.nt, half, release);

@@ -17,6 +17,11 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_STRIDE = 16;       // TMEM columns of scales per pipeline stage
 constexpr int MAX_G = 1024;
 constexpr int EPI_WARPS = 8;                  // two warps per TMEM lane quarter
+// CTA-pair kernel, TMA-store epilogue: each epilogue warp stages 32-row x
+// kEpiBoxCols-column bf16 boxes (64: 4 KB, 128-byte swizzle; 32: 2 KB,
+// 64-byte swizzle, which leaves room for a sixth pipeline stage)
+constexpr int kEpiBoxCols = 32;
+constexpr int kEpiBoxBytes = 32 * kEpiBoxCols * 2;
 constexpr int THREADS = 128 + 32 * EPI_WARPS;
 
 struct Params {
@@ -557,12 +562,11 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, uint32_t t
 
 // TMA-store epilogue for 256-wide tiles without activation: the warp drains
 // its 32 rows x 128 columns into registers as packed bf16 and releases TMEM
-// (as epilogue_tile_staged), then writes two 32 x 64 boxes through its
-// 4 KB staging buffer `buf` (1024-byte aligned, 128-byte swizzle: 16-byte
-// chunk c of row r sits at chunk c ^ (r % 8), which is also conflict-free
-// for the row-per-lane shared stores) with TMA stores.  The TMA writes whole
-// 128-byte lines; the warp's stores are asynchronous and the buffer is
-// reused once the previous store has read it.  `row0` is the warp's first
+// (as epilogue_tile_staged), then writes 32 x kEpiBoxCols boxes through
+// its staging buffer `buf` (kEpiBoxBytes, 1024-byte aligned, swizzled as
+// the tensor map says) with TMA stores.  The warp's stores are
+// asynchronous and the buffer is reused once the previous store has read
+// it.  `row0` is the warp's first
 // output row.
 template <typename Release>
 __device__ __forceinline__ void epilogue_tile_tma(const CUtensorMap* tmD, uint32_t buf, uint32_t tacc, int64_t row0,
@@ -580,19 +584,25 @@ __device__ __forceinline__ void epilogue_tile_tma(const CUtensorMap* tmD, uint32
             pk[16 * (c + 1) + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
         }
     }
-    const uint32_t rowaddr = buf + (uint32_t)lane * 128u;
+    // box rows of kEpiBoxCols * 2 bytes; 16-byte chunk c of row r sits at
+    // c ^ (r % 8) (128-byte swizzle) or c ^ ((r / 2) % 4) (64-byte swizzle),
+    // conflict-free for the row-per-lane stores either way
+    constexpr int CH = kEpiBoxCols / 8;                 // 16-byte chunks per row
+    const uint32_t rowaddr = buf + (uint32_t)lane * (uint32_t)(kEpiBoxCols * 2);
+    const uint32_t sw = CH == 8 ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 1) & 3);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < 128 / kEpiBoxCols; ++j) {
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-            st_shared_v4(rowaddr + ((uint32_t)(c ^ (lane & 7)) << 4), pk[32 * j + 4 * c], pk[32 * j + 4 * c + 1],
-                         pk[32 * j + 4 * c + 2], pk[32 * j + 4 * c + 3]);
+        for (int c = 0; c < CH; ++c) {
+            const int w = (kEpiBoxCols / 2) * j + 4 * c;
+            st_shared_v4(rowaddr + (((uint32_t)c ^ sw) << 4), pk[w], pk[w + 1], pk[w + 2], pk[w + 3]);
+        }
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(tmD, buf, nt * 256 + 128 * half + 64 * j, (int)row0);
+            tma_store_2d(tmD, buf, nt * 256 + 128 * half + kEpiBoxCols * j, (int)row0);
             bulk_commit_group();
         }
     }
