@@ -500,10 +500,11 @@ static void launch_1sm(int epilogue, int grid, const CUtensorMap& tmA, const CUt
 // pair tiles, TMA-store epilogue): its short contraction (one group's rows)
 // makes the 1-SM kernel wait on operand loads, and the pair halves each SM's
 // operand traffic.  FWD and DGRAD run on the 1-SM kernel with 128 x 256
-// tiles, except plain-epilogue ones with K <= 2048: a group's last 128-row
-// tile leaves half of a 256-row pair tile idle, which cost more than the
-// pair kernel saved on the longer contractions and with the fused
-// epilogues (measured on the DeepSeek-V3 layer).  The
+// tiles, except plain-epilogue ones with K <= 2048 over many rows: a
+// group's last 128-row tile leaves half of a 256-row pair tile idle, which
+// cost more than the pair kernel saved on the longer contractions, with the
+// fused epilogues, on small problems and with small groups (measured on
+// the DeepSeek-V3 layer and the grouped GEMM sweep).  The
 // environment variable MOE_GEMM_2SM forces one kernel for every mode, for
 // measurement: 0 = 1-SM, 256 = 256 x 256 pair tiles, 128 = 256 x 128 pair
 // tiles with two TMEM accumulators per CTA.  WGRAD with M % 256 != 0 always
@@ -678,10 +679,12 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     const int grid = (int)(upper_tiles < sms ? (upper_tiles > 0 ? upper_tiles : 1) : sms);
     int sel = gemm_2sm_mode();
-    // the CTA-pair kernel for the weight gradients and for plain-epilogue
-    // FWD/DGRAD with short contractions (K <= 2048), where its lower fixed
+    // the CTA-pair kernel for the weight gradients, and for plain-epilogue
+    // FWD/DGRAD with short contractions (K <= 2048) over many rows (at
+    // least 65,536, and 512 per group on average): there its lower fixed
     // cost per tile outweighs a group's half-idle odd last pair tile
-    if (sel < 0) sel = (mode == MOE_GEMM_WGRAD || (epilogue == MOE_EPI_NONE && K <= 2048 && N % 256 == 0)) ? 256 : 0;
+    const bool pair_fwd = epilogue == MOE_EPI_NONE && K <= 2048 && N % 256 == 0 && M >= 65536 && M >= 512LL * G;
+    if (sel < 0) sel = (mode == MOE_GEMM_WGRAD || pair_fwd) ? 256 : 0;
     const int bn2 = sel == 256 && N % 256 == 0 ? 256 : 128;
     const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {
