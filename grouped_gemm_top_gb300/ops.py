@@ -206,7 +206,8 @@ def mxfp8_gather_quantize(src, gofs, G, rows, row_id=None, k=1, row_w=None, roww
                           codes_row=None, scales_row=None, codes_col=None, scales_col=None, err=None, stream=None):
     """Rowwise and/or group-aware columnwise MXFP8 codes of the permuted
     matrix whose row s is src[row_id[s] // k] (times row_w[row_id[s]]), or
-    src[s] without row_id.  See include/moe.h.  Returns
+    src[s] without row_id.  See include/moe.h (a given codes_row must be
+    32-byte aligned, as fresh torch allocations are).  Returns
     (codes_row, scales_row, codes_col, scales_col), None for an axis not
     asked for."""
     cols = src.shape[1]
