@@ -43,3 +43,40 @@ def test_reference_arm_is_silent_on_other_ranks():
     r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_gemm_traffic_is_dropped_once_the_kernels_change(tmp_path):
+    """The roofline's `traffic` comes from recorded ncu counters only while
+    the GEMM sources still hash to the value recorded with them."""
+    import hashlib
+    import shutil
+    bench = _bench_module()
+    root = tmp_path / "repo"
+    csrc = root / "grouped_gemm_top_gb300" / "csrc"
+    shutil.copytree(os.path.join(ROOT, "grouped_gemm_top_gb300", "csrc"), csrc)
+    h = hashlib.sha256()
+    for fn in ["common.cuh", "gemm_common.cuh", "gemm.cu", "gemm2sm.cu"]:
+        h.update((csrc / fn).read_bytes())
+    (root / "profiles").mkdir()
+    rec = {"kernel_source_hash": h.hexdigest()[:16], "gemm_launches": [{"dram_read": 1.0, "dram_write": 2.0}] * 6}
+    (root / "profiles" / "gemm_traffic.json").write_text(json.dumps(rec))
+    bench.ROOT = str(root)
+    assert bench._gemm_traffic() == rec["gemm_launches"]
+    with open(csrc / "gemm.cu", "a") as f:
+        f.write("\n// edited\n")
+    assert bench._gemm_traffic() is None
+
+
+def test_peaks_fall_back_when_the_measured_file_is_absent(tmp_path):
+    bench = _bench_module()
+    bench.ROOT = str(tmp_path)
+    peaks, src = bench._peaks()
+    assert src == "fallback" and peaks["hbm_gbs"] == 6800.0 and peaks["bf16_tflops"] == 1900.0
