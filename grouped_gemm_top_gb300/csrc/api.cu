@@ -13,6 +13,7 @@ static std::mutex g_mu;
 cudaError_t gemm_set_attributes();   // gemm.cu
 cudaError_t quant_set_attributes();  // quant.cu
 cudaError_t gemm_init_driver();      // gemm.cu
+void route_scratch_forget(int device);  // route.cu
 
 int device_sm_count() {
     int dev = 0;
@@ -28,7 +29,7 @@ bool device_initialized() {
 
 }  // namespace moe
 
-extern "C" int moe_abi_version(void) { return 100; }
+extern "C" int moe_abi_version(void) { return 101; }
 
 extern "C" const char* moe_status_string(int s) {
     switch (s) {
@@ -47,12 +48,18 @@ extern "C" const char* moe_status_string(int s) {
     }
 }
 
+// Every call redoes the per-device set-up (kernel attributes, SM count) in
+// the context that is current now, so a caller that reset the device
+// (cudaDeviceReset) calls moe_init again and the library works in the new
+// primary context; the address of the no-allocation routing scratch is
+// looked up again on its next call for the same reason.
 extern "C" moe_status_t moe_init(int device) {
     using namespace moe;
     if (device < 0 || device >= kMaxDevices) return MOE_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_mu);
     if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
-    if (g_init[device]) return MOE_OK;
+    g_init[device] = false;
+    route_scratch_forget(device);
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return MOE_ERR_CUDA;
     int major = 0, minor = 0;
@@ -72,4 +79,19 @@ extern "C" int64_t moe_row_capacity(int T, int E, int k) {
     const int64_t R = (int64_t)T * k;
     const int64_t pad = 127 * (R < E ? R : (int64_t)E);
     return (R + pad + 127) / 128 * 128;
+}
+
+extern "C" size_t moe_workspace_size(int op, int T, int d, int E, int k, int f) {
+    if (T < 0 || d < 1 || E < 1 || k < 1 || f < 1) return (size_t)-1;
+    switch (op) {
+        case MOE_OP_ROUTE_TOPK: return moe_route_workspace_size(T, E);
+        case MOE_OP_PERMUTE: return moe_permute_workspace_size(T, E);
+        case MOE_OP_GROUP_QUANTIZE:
+        case MOE_OP_GATHER_QUANTIZE:
+        case MOE_OP_GROUPED_GEMM:
+        case MOE_OP_UNPERMUTE_COMBINE:
+        case MOE_OP_COMBINE_BWD:
+        case MOE_OP_ROUTE_BWD: return 0;
+        default: return (size_t)-1;
+    }
 }

@@ -2,7 +2,8 @@
 //
 // [TE-JAX] "Optimization 1: Grouped GEMM": every expert's GEMM runs in one
 // kernel call, each over its actual rows, and only regions with valid tokens
-// are computed; "On Blackwell ... MXFP8 block scaling for expert matmuls".
+// are computed; on Blackwell the expert GEMMs take MXFP8 operands with block
+// scales (same section).
 // [TE-JAX] Figure 3: the grouped MLP is two grouped GEMMs (up/gate, down);
 // the SwiGLU between them is fused into the up/gate epilogue here.
 //
@@ -22,7 +23,6 @@
 // counts.  Every mbarrier wait is bounded: on timeout the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM
 // and returns.
-#include <stdlib.h>
 
 #include <algorithm>
 
@@ -504,31 +504,36 @@ static void launch_1sm(int epilogue, int grid, const CUtensorMap& tmA, const CUt
 // group's last 128-row tile leaves half of a 256-row pair tile idle, which
 // cost more than the pair kernel saved on the longer contractions, with the
 // fused epilogues, on small problems and with small groups (measured on
-// the DeepSeek-V3 layer and the grouped GEMM sweep).  The
-// environment variable MOE_GEMM_2SM forces one kernel for every mode, for
-// measurement: 0 = 1-SM, 256 = 256 x 256 pair tiles, 128 = 256 x 128 pair
-// tiles with two TMEM accumulators per CTA.  WGRAD with M % 256 != 0 always
-// uses the 1-SM kernel.
-static int gemm_2sm_mode() {
-    static int mode = [] {
-        const char* e = getenv("MOE_GEMM_2SM");
-        if (e == nullptr) return -1;
-        const int v = atoi(e);
-        return v == 256 ? 256 : (v == 128 ? 128 : 0);
-    }();
-    return mode;
+// the DeepSeek-V3 layer and the grouped GEMM sweep).  A caller can force one
+// kernel per call through moe_gemm_opts_t (the measured alternatives stay
+// selectable and parity-tested); WGRAD with M % 256 != 0 always uses the
+// 1-SM kernel.
+struct GemmChoice {
+    int sel;              // 0 = 1-SM kernel; 256 / 128 = CTA pair with 256- / 128-wide tiles
+    int bn_1sm;           // 1-SM tile width: 256, or 128 (two TMEM accumulators)
+    int band;             // m-tiles per raster band, 0 = the kernel's default
+    bool register_stores; // pair kernel, plain epilogue: register-staged stores instead of TMA stores
+};
+
+static bool gemm_opts_valid(const moe_gemm_opts_t* o) {
+    return o == nullptr || (o->kernel >= MOE_GEMM_KERNEL_AUTO && o->kernel <= MOE_GEMM_KERNEL_PAIR_N128 &&
+                            o->band >= 0 && o->band <= 64 && (o->register_stores == 0 || o->register_stores == 1));
 }
 
-// Tile width used by grouped_gemm_mxfp8: 256 (one TMEM accumulator; on
-// GB300 the 128-wide MMA is operand-bandwidth bound and ran at ~0.64x the
-// 256-wide rate) unless the environment variable MOE_GEMM_BN=128 selects the
-// double-buffered 128-wide tile (kept for measurement).
-static int gemm_bn() {
-    static int bn = [] {
-        const char* e = getenv("MOE_GEMM_BN");
-        return (e != nullptr && atoi(e) == 128) ? 128 : 256;
-    }();
-    return bn;
+// sel = -1 leaves the choice to the default rule of the call.
+static GemmChoice gemm_choice(const moe_gemm_opts_t* o) {
+    GemmChoice c{-1, 256, 0, false};
+    if (o == nullptr) return c;
+    switch (o->kernel) {
+        case MOE_GEMM_KERNEL_1SM: c.sel = 0; break;
+        case MOE_GEMM_KERNEL_1SM_N128: c.sel = 0; c.bn_1sm = 128; break;
+        case MOE_GEMM_KERNEL_PAIR: c.sel = 256; break;
+        case MOE_GEMM_KERNEL_PAIR_N128: c.sel = 128; break;
+        default: break;
+    }
+    c.band = o->band;
+    c.register_stores = o->register_stores != 0;
+    return c;
 }
 
 // Scale atoms (512 bytes each) seen as a 2-D uint8 tensor of 256-byte rows:
@@ -552,16 +557,6 @@ static bool make_d_map(CUtensorMap* m, void* base, int64_t rows, int N) {
                           gg::kEpiBoxCols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-// TMA-store epilogue of the pair kernel (MOE_EPI_NONE, N = 256): on unless
-// the environment variable MOE_GEMM_TMA_STORE=0 (kept for measurement).
-static bool gemm_tma_store() {
-    static bool on = [] {
-        const char* e = getenv("MOE_GEMM_TMA_STORE");
-        return e == nullptr || atoi(e) != 0;
-    }();
-    return on;
 }
 
 // rank-2/3 uint8 tensor map, 128x128 boxes, 128-byte swizzle
@@ -591,14 +586,16 @@ struct HQuantOut {
 
 static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
                              int b_layout, const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
-                             const void* epi_aux, void* d, void* d2, const HQuantOut& hq, int32_t* err,
-                             void* stream) {
+                             const void* epi_aux, void* d, void* d2, const HQuantOut& hq,
+                             const moe_gemm_opts_t* opts, int32_t* err, void* stream) {
     using namespace gg;
+    MOE_REQUIRE(gemm_opts_valid(opts), MOE_ERR_INVALID_ARG);
+    const GemmChoice choice = gemm_choice(opts);
     MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD || mode == MOE_GEMM_WGRAD, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(a && a_sf && b && b_sf && gofs && d, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(G >= 1 && G <= MAX_G && M > 0 && N > 0 && K > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(M % 128 == 0 && K % BK == 0 && N % 128 == 0, MOE_ERR_UNSUPPORTED);
-    const int BN = (gemm_bn() == 256 && N % 256 == 0) ? 256 : 128;
+    const int BN = (choice.bn_1sm == 256 && N % 256 == 0) ? 256 : 128;
     MOE_REQUIRE(K <= 0x7FFFFF80LL && M <= 0x7FFFFF80LL, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(moe_aligned16(a) && moe_aligned16(b) && moe_aligned16(a_sf) && moe_aligned16(b_sf) &&
                     moe_aligned16(d) && (d2 == nullptr || moe_aligned16(d2)) &&
@@ -641,8 +638,7 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     p.timeout_ns = 2000000000ull;   // 2 s per wait
     // m-tiles per raster band: 3 for long contractions, 4 for K <= 2048
     // (measured on the DeepSeek-V3 layer against 2, 4, 8, 16 and 32)
-    p.band = K <= 2048 ? 4 : 3;
-    if (const char* e = getenv("MOE_GEMM_BAND")) p.band = std::max(1, atoi(e));
+    p.band = choice.band > 0 ? choice.band : (K <= 2048 ? 4 : 3);
     p.n_tiles = N / BN;
     int64_t upper_tiles;
     if (mode == MOE_GEMM_WGRAD) {
@@ -678,7 +674,7 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     const int sms = device_sm_count();
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     const int grid = (int)(upper_tiles < sms ? (upper_tiles > 0 ? upper_tiles : 1) : sms);
-    int sel = gemm_2sm_mode();
+    int sel = choice.sel;
     // the CTA-pair kernel for the weight gradients, and for plain-epilogue
     // FWD/DGRAD with short contractions (K <= 2048) over many rows (at
     // least 65,536, and 512 per group on average): there its lower fixed
@@ -689,7 +685,7 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {
         p.n_tiles = N / bn2;
-        if (getenv("MOE_GEMM_BAND") == nullptr) p.band = 2;     // measured: 2 beat 4, 8 and 16
+        p.band = choice.band > 0 ? choice.band : 2;     // measured: 2 beat 4, 8 and 16
         const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles
                                                            : (M / BM) * (int64_t)p.n_tiles;
         const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm(bn2));
@@ -720,7 +716,7 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
                     MOE_ERR_CUDA);
         // D through the TMA: bf16 [rows, N] in 32-row x 64-column boxes
         CUtensorMap tmD = tmA;
-        p.tma_store = bn2 == 256 && epilogue == MOE_EPI_NONE && gemm_tma_store();
+        p.tma_store = bn2 == 256 && epilogue == MOE_EPI_NONE && !choice.register_stores;
         if (p.tma_store) {
             const int64_t drows = mode == MOE_GEMM_WGRAD ? (int64_t)G * M : M;
             MOE_REQUIRE(make_d_map(&tmD, d, drows, N), MOE_ERR_CUDA);
@@ -736,13 +732,37 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     return MOE_OK;
 }
 
+extern "C" moe_status_t grouped_gemm_mxfp8_ex(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                                              const uint8_t* b_sf, int b_layout, const int32_t* gofs, int G,
+                                              int64_t M, int N, int64_t K, int epilogue, const void* epi_aux, void* d,
+                                              void* d2, const moe_gemm_opts_t* opts, int32_t* err, void* stream) {
+    if (epilogue == MOE_EPI_SWIGLU && d2 == nullptr) return MOE_ERR_INVALID_ARG;
+    const HQuantOut none = {nullptr, nullptr, nullptr, nullptr};
+    return gemm_run(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilogue, epi_aux, d, d2, none, opts, err,
+                    stream);
+}
+
 extern "C" moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
                                            const uint8_t* b_sf, int b_layout, const int32_t* gofs, int G, int64_t M,
                                            int N, int64_t K, int epilogue, const void* epi_aux, void* d, void* d2,
                                            int32_t* err, void* stream) {
-    if (epilogue == MOE_EPI_SWIGLU && d2 == nullptr) return MOE_ERR_INVALID_ARG;
-    const HQuantOut none = {nullptr, nullptr, nullptr, nullptr};
-    return gemm_run(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilogue, epi_aux, d, d2, none, err, stream);
+    return grouped_gemm_mxfp8_ex(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilogue, epi_aux, d, d2,
+                                 nullptr, err, stream);
+}
+
+extern "C" moe_status_t grouped_gemm_mxfp8_swiglu_quant_ex(const uint8_t* a, const uint8_t* a_sf,
+                                                           const uint8_t* b, const uint8_t* b_sf, int b_layout,
+                                                           const int32_t* gofs, int G, int64_t M, int N, int64_t K,
+                                                           void* a_pre, void* h, uint8_t* h_codes_row,
+                                                           uint8_t* h_scales_row, uint8_t* h_codes_col,
+                                                           uint8_t* h_scales_col, const moe_gemm_opts_t* opts,
+                                                           int32_t* err, void* stream) {
+    MOE_REQUIRE(h_codes_row && h_scales_row && h_codes_col && h_scales_col, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(N > 0 && N % 256 == 0, MOE_ERR_UNSUPPORTED);      // f = N/2 a multiple of 128
+    MOE_REQUIRE((reinterpret_cast<uintptr_t>(h_codes_row) & 31) == 0, MOE_ERR_ALIGNMENT);
+    const HQuantOut hq = {h_codes_row, h_scales_row, h_codes_col, h_scales_col};
+    return gemm_run(MOE_GEMM_FWD, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, MOE_EPI_SWIGLU, nullptr, a_pre, h, hq,
+                    opts, err, stream);
 }
 
 extern "C" moe_status_t grouped_gemm_mxfp8_swiglu_quant(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
@@ -751,12 +771,8 @@ extern "C" moe_status_t grouped_gemm_mxfp8_swiglu_quant(const uint8_t* a, const 
                                                         uint8_t* h_codes_row, uint8_t* h_scales_row,
                                                         uint8_t* h_codes_col, uint8_t* h_scales_col, int32_t* err,
                                                         void* stream) {
-    MOE_REQUIRE(h_codes_row && h_scales_row && h_codes_col && h_scales_col, MOE_ERR_INVALID_ARG);
-    MOE_REQUIRE(N > 0 && N % 256 == 0, MOE_ERR_UNSUPPORTED);      // f = N/2 a multiple of 128
-    MOE_REQUIRE((reinterpret_cast<uintptr_t>(h_codes_row) & 31) == 0, MOE_ERR_ALIGNMENT);
-    const HQuantOut hq = {h_codes_row, h_scales_row, h_codes_col, h_scales_col};
-    return gemm_run(MOE_GEMM_FWD, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, MOE_EPI_SWIGLU, nullptr, a_pre, h, hq,
-                    err, stream);
+    return grouped_gemm_mxfp8_swiglu_quant_ex(a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, a_pre, h, h_codes_row,
+                                              h_scales_row, h_codes_col, h_scales_col, nullptr, err, stream);
 }
 
 extern "C" moe_status_t gemm_bf16_nt(const void* a, const void* b, int64_t M, int N, int64_t K, float* d,
@@ -802,11 +818,14 @@ extern "C" moe_status_t gemm_bf16_nt(const void* a, const void* b, int64_t M, in
     return MOE_OK;
 }
 
-extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uint8_t* a_sf, const float* a_scale,
-                                           const uint8_t* b, const uint8_t* b_sf, const float* b_scale,
-                                           const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
-                                           void* d, int32_t* err, void* stream) {
+extern "C" moe_status_t grouped_gemm_nvfp4_ex(int mode, const uint8_t* a, const uint8_t* a_sf,
+                                              const float* a_scale, const uint8_t* b, const uint8_t* b_sf,
+                                              const float* b_scale, const int32_t* gofs, int G, int64_t M, int N,
+                                              int64_t K, int epilogue, void* d, const moe_gemm_opts_t* opts,
+                                              int32_t* err, void* stream) {
     using namespace gg;
+    MOE_REQUIRE(gemm_opts_valid(opts), MOE_ERR_INVALID_ARG);
+    const GemmChoice choice = gemm_choice(opts);
     MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD || mode == MOE_GEMM_WGRAD, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(epilogue == MOE_EPI_NONE || (epilogue == MOE_EPI_NONE_F32 && mode != MOE_GEMM_WGRAD),
                 MOE_ERR_INVALID_ARG);      // WGRAD writes bf16 (an empty group's tile is zero-filled as bf16)
@@ -850,8 +869,7 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
     p.d = (__nv_bfloat16*)d;
     p.err = err;
     p.timeout_ns = 2000000000ull;
-    p.band = 8;
-    if (const char* e = getenv("MOE_GEMM_BAND")) p.band = std::max(1, atoi(e));
+    p.band = choice.band > 0 ? choice.band : 8;
     p.n_tiles = N / 256;
     p.m_tiles = (int)(M / BM);
     p.n_out = N;
@@ -859,18 +877,18 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
     const int sms = device_sm_count();
     MOE_REQUIRE(sms > 0, MOE_ERR_NOT_INITIALIZED);
     cudaStream_t s = (cudaStream_t)stream;
-    // FWD / DGRAD run on the 1-SM kernel; MOE_GEMM_2SM=256 (or 128) selects
-    // the CTA-pair kernel's NVFP4 instance (256 x 256 pair tiles, half of B
-    // per SM), kept for measurement: at the DeepSeek-V3 shapes it was slower
-    // (a group's odd last 128-row tile idles half a pair tile) and on dense
-    // shapes it only matched the 1-SM kernel
-    if (!wg && gemm_2sm_mode() > 0 && gemm_max_clusters_2sm(256) > 0) {
+    // FWD / DGRAD run on the 1-SM kernel; MOE_GEMM_KERNEL_PAIR (or _PAIR_N128)
+    // selects the CTA-pair kernel's NVFP4 instance (256 x 256 pair tiles,
+    // half of B per SM), kept for measurement: at the DeepSeek-V3 shapes it
+    // was slower (a group's odd last 128-row tile idles half a pair tile) and
+    // on dense shapes it only matched the 1-SM kernel
+    if (!wg && choice.sel > 0 && gemm_max_clusters_2sm(256) > 0) {
         CUtensorMap tmB2, tmSFA, tmSFB;
         MOE_REQUIRE(make_map(&tmB2, b, 3, db, sb, 128), MOE_ERR_CUDA);
         MOE_REQUIRE(make_sf_map(&tmSFA, a_sf, M * K / 16 / 512, 8) &&
                         make_sf_map(&tmSFB, b_sf, (int64_t)G * N * K / 16 / 512, 16),
                     MOE_ERR_CUDA);
-        if (getenv("MOE_GEMM_BAND") == nullptr) p.band = 4;
+        p.band = choice.band > 0 ? choice.band : 4;
         const int64_t upper_pairs = (M / BM) * (int64_t)p.n_tiles;
         const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm(256));
         if (gemm_launch_2sm_nvf4(epilogue, tmA, tmB2, tmSFA, tmSFB, p, clusters, s) != cudaSuccess)
@@ -886,6 +904,14 @@ extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uin
         k_grouped_gemm<256, MOE_EPI_NONE, FMT_NVF4><<<grid, THREADS, Cfg<256, FMT_NVF4>::SMEM_BYTES, s>>>(tmA, tmB, p);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
+}
+
+extern "C" moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uint8_t* a_sf, const float* a_scale,
+                                           const uint8_t* b, const uint8_t* b_sf, const float* b_scale,
+                                           const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
+                                           void* d, int32_t* err, void* stream) {
+    return grouped_gemm_nvfp4_ex(mode, a, a_sf, a_scale, b, b_sf, b_scale, gofs, G, M, N, K, epilogue, d, nullptr,
+                                 err, stream);
 }
 
 namespace moe {

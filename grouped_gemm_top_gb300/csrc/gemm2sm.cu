@@ -27,8 +27,6 @@
 // A group's rows are 128-aligned, so a 256-row pair tile may have only its
 // first half inside the group; the second CTA then multiplies duplicate rows
 // and discards them (its stores are skipped).
-#include <stdio.h>
-#include <stdlib.h>
 
 #include "gemm_common.cuh"
 
@@ -534,7 +532,6 @@ static cudaError_t set_attr_2sm(int* max_clusters) {
     const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, gg::sm2::k_grouped_gemm_2sm<BN, MOE_EPI_NONE>, &cfg);
     if (e != cudaSuccess) return e;
     *max_clusters = n;
-    if (getenv("MOE_DEBUG") != nullptr) fprintf(stderr, "libmoe: N=%d pair tiles: %d co-resident CTA pairs\n", BN, n);
     return cudaSuccess;
 }
 

@@ -42,8 +42,13 @@ __global__ void __launch_bounds__(kPermTok) k_perm_rank(const int32_t* __restric
     if (t < T) {
         for (int j = 0; j < k; ++j) {
             const int e = topk_idx[(size_t)t * k + j];
+            // the same test as the mask pass: an expert out of range or named
+            // a second time by this token gets no rank (slot -1), so no two
+            // choices share a row
+            bool ok = e >= 0 && e < E;
+            for (int j2 = 0; j2 < j && ok; ++j2) ok = topk_idx[(size_t)t * k + j2] != e;
             int r = -1;
-            if (e >= 0 && e < E) {
+            if (ok) {
                 r = __popc(s_mask[e * 4 + word] & (bit - 1u));
                 for (int w = 0; w < word; ++w) r += __popc(s_mask[e * 4 + w]);
             }

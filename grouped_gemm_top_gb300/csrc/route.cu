@@ -1,7 +1,7 @@
 // Router: top-k selection + weights + per-expert counts/offsets, and the
-// router backward.  [TE-JAX] intro ("a learned router ... decides which
-// Top-K experts to activate") and "Optimization 2" ("the fused router
-// kernels assign each token to its experts").
+// router backward.  [TE-JAX] introduction (a trained router picks the top-k
+// experts that process each token) and "Optimization 2" (the routing step
+// runs as fused router kernels that map tokens to experts).
 //
 // One warp owns one token: lane l holds logits of experts l, l+32, ...; the
 // k winners are found by k rounds of a warp argmax (ties -> lower index).
@@ -354,6 +354,14 @@ constexpr size_t kRouteScratchInts = (size_t)1 << 18;   // 1 MiB: ceil(T / 128) 
 static __device__ __align__(256) int32_t g_route_scratch[kRouteScratchInts];
 static int32_t* g_route_scratch_dev[64] = {nullptr};     // device address of the array, per device
 static std::mutex g_route_scratch_mu;
+
+// moe_init drops the cached address, so the next call looks it up again in
+// the context current then (after a device reset the old one is stale).
+void route_scratch_forget(int device) {
+    if (device < 0 || device >= 64) return;
+    std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+    g_route_scratch_dev[device] = nullptr;
+}
 }  // namespace moe
 
 extern "C" moe_status_t moe_route_topk_noalloc(const float* logits, int T, int E, int k, int score, int normalize,
@@ -369,17 +377,19 @@ extern "C" moe_status_t moe_route_topk_noalloc(const float* logits, int T, int E
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    int32_t* hist = nullptr;
     {
-        // first call on this device: host code cannot use the array's name as
-        // a device pointer, so look its address up once (device current)
+        // first call on this device since moe_init: host code cannot use the
+        // array's name as a device pointer, so look its address up (device
+        // current) and keep it
         std::lock_guard<std::mutex> lock(g_route_scratch_mu);
         if (g_route_scratch_dev[dev] == nullptr) {
             void* ptr = nullptr;
             if (cudaGetSymbolAddress(&ptr, g_route_scratch) != cudaSuccess || ptr == nullptr) return MOE_ERR_CUDA;
             g_route_scratch_dev[dev] = static_cast<int32_t*>(ptr);
         }
+        hist = g_route_scratch_dev[dev];
     }
-    int32_t* hist = g_route_scratch_dev[dev];
     cudaStream_t s = (cudaStream_t)stream;
     // every histogram entry read below is written first in the same call, so
     // what a previous call left in the array does not matter

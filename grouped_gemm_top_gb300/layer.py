@@ -107,6 +107,9 @@ class MoELayer:
         # CUDA events recorded around it on the current stream
         self.gemm_events = None
         self.router_events = None      # the same for the router's GEMMs
+        # when a dict, the memory-bound launches of a step (quantizations,
+        # combines) append their event pairs under their names
+        self.mem_events = None
 
     # ------------------------------------------------------------ weights --
     def set_weights(self, W1, W2):
@@ -142,6 +145,16 @@ class MoELayer:
         r = fn(*args)
         e.record()
         self.gemm_events.append((s, e))
+        return r
+
+    def _mem(self, name, fn, *args, **kw):
+        if self.mem_events is None:
+            return fn(*args, **kw)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        r = fn(*args, **kw)
+        e.record()
+        self.mem_events.setdefault(name, []).append((s, e))
         return r
 
     def _gemm(self, *args):
@@ -180,15 +193,15 @@ class MoELayer:
         self.route_permute_()
         # x_perm = x[row_id // k], both axes: rowwise for the up GEMM, the
         # columnwise copy for the dW1 wgrad of the backward
-        ops.mxfp8_gather_quantize(self.x, self.gofs, E, M, self.row_id, k, None, True, True, self.xq, self.xs,
-                                  self.xqT, self.xsT, err)
+        self._mem("quant_x", ops.mxfp8_gather_quantize, self.x, self.gofs, E, M, self.row_id, k, None, True, True,
+                  self.xq, self.xs, self.xqT, self.xsT, err)
         # up/gate GEMM; its SwiGLU epilogue writes a_pre and h's MXFP8 codes
         # on both axes (h itself only if store_h)
         self._gemm_swiglu_quant(self.xq, self.xs, self.W1f, self.W1f_s, ops.MOE_B_GNK, self.gofs, E, M, 2 * f, d,
                                 self.a_pre, self.h, False, self.hq, self.hs, self.hqT, self.hsT, err)
         self._gemm(ops.MOE_GEMM_FWD, self.hq, self.hs, self.W2f, self.W2f_s, ops.MOE_B_GNK, self.gofs,
                    E, M, d, f, ops.MOE_EPI_NONE, None, self.y_perm, None, err)
-        ops.moe_unpermute_combine(self.y_perm, self.slot_of, self.topk_w, self.out, err)
+        self._mem("combine_out", ops.moe_unpermute_combine, self.y_perm, self.slot_of, self.topk_w, self.out, err)
 
     def backward_(self):
         E, k, d, f, M = self.G, self.kk, self.d, self.f, self.row_cap
@@ -196,12 +209,12 @@ class MoELayer:
         # dw = <dout, y_perm> per (token, choice); dy_perm = w * dout is only
         # ever materialised as its MXFP8 codes (both axes)
         dw = self.dw_all if self.S else self.dw
-        ops.moe_combine_bwd(self.dout, self.y_perm, self.slot_of, self.topk_w, None, None, E, None, dw, err,
-                            want_dy=False)
+        self._mem("combine_bwd_dw", ops.moe_combine_bwd, self.dout, self.y_perm, self.slot_of, self.topk_w, None,
+                  None, E, None, dw, err, want_dy=False)
         if self.S:       # the shared choices' weights are constants
             ops.moe_route_drop_shared(self.dw_all, self.k, self.dw)
-        ops.mxfp8_gather_quantize(self.dout, self.gofs, E, M, self.row_id, k, self.topk_w, True, True, self.dyq,
-                                  self.dys, self.dyqT, self.dysT, err)
+        self._mem("quant_dy", ops.mxfp8_gather_quantize, self.dout, self.gofs, E, M, self.row_id, k, self.topk_w,
+                  True, True, self.dyq, self.dys, self.dyqT, self.dysT, err)
         # dH = dY W2^T (fp32)
         self._gemm(ops.MOE_GEMM_DGRAD, self.dyq, self.dys, self.W2d, self.W2d_s, ops.MOE_B_GNK,
                    self.gofs, E, M, f, d, ops.MOE_EPI_NONE_F32, None, self.dH, None, err)
@@ -210,8 +223,8 @@ class MoELayer:
                    d, M, ops.MOE_EPI_NONE, None, self.dW2, None, err)
         # dA = [dgate | dup] = SwiGLU backward of (a_pre, dH), quantized on
         # both axes in the same pass
-        ops.mxfp8_swiglu_bwd_quantize(self.dH, self.a_pre, self.gofs, E, self.dA, False, self.dAq, self.dAs,
-                                      self.dAqT, self.dAsT, err)
+        self._mem("swiglu_bwd_quant_dA", ops.mxfp8_swiglu_bwd_quantize, self.dH, self.a_pre, self.gofs, E, self.dA,
+                  False, self.dAq, self.dAs, self.dAqT, self.dAsT, err)
         # dX_perm = dA W1^T
         self._gemm(ops.MOE_GEMM_DGRAD, self.dAq, self.dAs, self.W1d, self.W1d_s, ops.MOE_B_GNK,
                    self.gofs, E, M, d, 2 * f, ops.MOE_EPI_NONE, None, self.dx_perm, None, err)
@@ -228,7 +241,7 @@ class MoELayer:
             self._router_gemm(self.xT, self.dlogitsT, self.dWr, err)
             ops.moe_unpermute_combine_add(self.dx_perm, self.slot_of, None, self.dx_r, self.dx, err)
         else:
-            ops.moe_unpermute_combine(self.dx_perm, self.slot_of, None, self.dx, err)
+            self._mem("combine_dx", ops.moe_unpermute_combine, self.dx_perm, self.slot_of, None, self.dx, err)
 
     def step_(self):
         """One fwd+bwd pass over the resident inputs (no allocation, no sync)."""

@@ -34,6 +34,10 @@ MOE_QUANT_COLWISE_BATCHED, MOE_QUANT_COLWISE_BATCHED_GLU = 3, 4
 MOE_GEMM_FWD, MOE_GEMM_DGRAD, MOE_GEMM_WGRAD = 0, 1, 2
 MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD, MOE_EPI_NONE_F32 = 0, 1, 2, 3
 MOE_B_GNK, MOE_B_NGK = 0, 1
+MOE_GEMM_KERNEL_AUTO, MOE_GEMM_KERNEL_1SM, MOE_GEMM_KERNEL_1SM_N128 = 0, 1, 2
+MOE_GEMM_KERNEL_PAIR, MOE_GEMM_KERNEL_PAIR_N128 = 3, 4
+(MOE_OP_ROUTE_TOPK, MOE_OP_PERMUTE, MOE_OP_GROUP_QUANTIZE, MOE_OP_GATHER_QUANTIZE, MOE_OP_GROUPED_GEMM,
+ MOE_OP_UNPERMUTE_COMBINE, MOE_OP_COMBINE_BWD, MOE_OP_ROUTE_BWD) = range(8)
 
 EXPORTS = [
     "moe_abi_version", "moe_status_string", "moe_init", "moe_row_capacity",
@@ -43,10 +47,29 @@ EXPORTS = [
     "mxfp8_gather_quantize", "grouped_gemm_mxfp8_swiglu_quant", "mxfp8_swiglu_bwd_quantize",
     "gemm_bf16_nt", "moe_transpose_bf16", "moe_unpermute_combine_add", "moe_route_append_shared",
     "moe_route_drop_shared", "nvfp4_sf_bytes", "nvfp4_quantize", "grouped_gemm_nvfp4", "nvfp4_quantize_cols",
-    "moe_selftest_bounded_wait",
+    "moe_selftest_bounded_wait", "moe_workspace_size", "mxfp8_scale_layout", "grouped_gemm_mxfp8_ex",
+    "grouped_gemm_mxfp8_swiglu_quant_ex", "grouped_gemm_nvfp4_ex", "moe_hbm_fill",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+
+
+class GemmOpts(ctypes.Structure):
+    """moe_gemm_opts_t (include/moe.h): per-call grouped-GEMM kernel choice."""
+    _fields_ = [("kernel", ctypes.c_int), ("band", ctypes.c_int), ("register_stores", ctypes.c_int)]
+
+
+_GEMM_KERNELS = {"auto": MOE_GEMM_KERNEL_AUTO, "1sm": MOE_GEMM_KERNEL_1SM, "1sm_n128": MOE_GEMM_KERNEL_1SM_N128,
+                 "pair": MOE_GEMM_KERNEL_PAIR, "pair_n128": MOE_GEMM_KERNEL_PAIR_N128}
+
+
+def gemm_opts(kernel="auto", band=0, register_stores=False):
+    """A GemmOpts for the opts= argument of the grouped-GEMM wrappers;
+    kernel is one of "auto", "1sm", "1sm_n128", "pair", "pair_n128" (or the
+    MOE_GEMM_KERNEL_* value)."""
+    k = _GEMM_KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+    return GemmOpts(k, int(band), int(bool(register_stores)))
+
 
 _SIGS = {
     "moe_abi_version": (_i32, []),
@@ -80,6 +103,15 @@ _SIGS = {
     "nvfp4_quantize_cols": (_i32, [_vp, _i64, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "grouped_gemm_nvfp4": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i64, _i32, _vp, _vp,
                                   _vp]),
+    "moe_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "mxfp8_scale_layout": (_i32, [_vp, _i64, _i32, _i32, _vp, _vp]),
+    "grouped_gemm_mxfp8_ex": (_i32, [_i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _i32, _vp, _vp,
+                                     _vp, _vp, _vp, _vp]),
+    "grouped_gemm_mxfp8_swiglu_quant_ex": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i64, _vp, _vp,
+                                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "grouped_gemm_nvfp4_ex": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i64, _i32, _vp,
+                                     _vp, _vp, _vp]),
+    "moe_hbm_fill": (_i32, [_vp, _sz, ctypes.c_uint32, _i32, _vp]),
 }
 
 
@@ -144,6 +176,28 @@ def moe_route_workspace_size(T: int, E: int) -> int:
 
 def moe_permute_workspace_size(T: int, E: int) -> int:
     return int(lib.moe_permute_workspace_size(T, E))
+
+
+def moe_workspace_size(op: int, T: int, d: int, E: int, k: int, f: int) -> int:
+    """Workspace bytes of call `op` (MOE_OP_*); -1 for an unknown op or bad sizes."""
+    v = int(lib.moe_workspace_size(int(op), int(T), int(d), int(E), int(k), int(f)))
+    return -1 if v == ctypes.c_size_t(-1).value else v
+
+
+def mxfp8_scale_layout(src, rows, cols, to_canonical=True, dst=None, stream=None):
+    """Scales of a [rows, cols] matrix quantized along cols: atom layout ->
+    canonical [rows, cols/32] (to_canonical) or back.  See include/moe.h."""
+    dst = dst if dst is not None else _empty((rows * (cols // 32),), torch.uint8, src)
+    _check("mxfp8_scale_layout", lib.mxfp8_scale_layout(_p(src), int(rows), int(cols), int(bool(to_canonical)),
+                                                        _p(dst), _stream(stream)))
+    return dst
+
+
+def moe_hbm_fill(dst, value=0, method=0, stream=None):
+    """Write the 32-bit value over all of dst's bytes (write-only stream)."""
+    nbytes = dst.numel() * dst.element_size()
+    _check("moe_hbm_fill", lib.moe_hbm_fill(_p(dst), nbytes, ctypes.c_uint32(int(value) & 0xFFFFFFFF).value,
+                                            int(method), _stream(stream)))
 
 
 def _empty(shape, dtype, like):
@@ -230,8 +284,9 @@ def mxfp8_gather_quantize(src, gofs, G, rows, row_id=None, k=1, row_w=None, roww
 
 
 def grouped_gemm_mxfp8(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilogue=MOE_EPI_NONE,
-                       epi_aux=None, d=None, d2=None, err=None, stream=None):
-    """See include/moe.h.  Allocates d (and d2 for SwiGLU) when not given."""
+                       epi_aux=None, d=None, d2=None, err=None, stream=None, opts=None):
+    """See include/moe.h.  Allocates d (and d2 for SwiGLU) when not given.
+    opts: a GemmOpts (gemm_opts()) selects grouped_gemm_mxfp8_ex."""
     if d is None:
         if mode == MOE_GEMM_WGRAD:
             d = _empty((G, M, N), torch.bfloat16, a)
@@ -243,9 +298,13 @@ def grouped_gemm_mxfp8(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilo
             d = _empty((M, N), torch.bfloat16, a)
     if epilogue == MOE_EPI_SWIGLU and d2 is None:
         d2 = _empty((M, N // 2), torch.bfloat16, a)
-    _check("grouped_gemm_mxfp8", lib.grouped_gemm_mxfp8(int(mode), _p(a), _p(a_sf), _p(b), _p(b_sf), int(b_layout),
-                                                        _p(gofs), int(G), int(M), int(N), int(K), int(epilogue),
-                                                        _p(epi_aux), _p(d), _p(d2), _p(err), _stream(stream)))
+    args = (int(mode), _p(a), _p(a_sf), _p(b), _p(b_sf), int(b_layout), _p(gofs), int(G), int(M), int(N), int(K),
+            int(epilogue), _p(epi_aux), _p(d), _p(d2))
+    if opts is None:
+        _check("grouped_gemm_mxfp8", lib.grouped_gemm_mxfp8(*args, _p(err), _stream(stream)))
+    else:
+        _check("grouped_gemm_mxfp8_ex", lib.grouped_gemm_mxfp8_ex(*args, ctypes.byref(opts), _p(err),
+                                                                  _stream(stream)))
     return (d, d2) if epilogue == MOE_EPI_SWIGLU else d
 
 
@@ -270,7 +329,7 @@ def mxfp8_swiglu_bwd_quantize(dH, a_pre, gofs, G, dA=None, want_dA=False, codes_
 
 def grouped_gemm_mxfp8_swiglu_quant(a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, a_pre=None, h=None, want_h=False,
                                     h_codes_row=None, h_scales_row=None, h_codes_col=None, h_scales_col=None,
-                                    err=None, stream=None):
+                                    err=None, stream=None, opts=None):
     """Up/gate GEMM with the SwiGLU epilogue writing a_pre [M, N] and the
     MXFP8 codes of h on both axes (h bf16 [M, N/2] only if want_h or h is
     given).  See include/moe.h.  Returns (a_pre, h or None, codes_row,
@@ -283,11 +342,14 @@ def grouped_gemm_mxfp8_swiglu_quant(a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K
     h_scales_row = h_scales_row if h_scales_row is not None else _empty((sf_bytes(M, f),), torch.uint8, a)
     h_codes_col = h_codes_col if h_codes_col is not None else _empty((f, M), torch.uint8, a)
     h_scales_col = h_scales_col if h_scales_col is not None else _empty((sf_bytes(M, f),), torch.uint8, a)
-    _check("grouped_gemm_mxfp8_swiglu_quant",
-           lib.grouped_gemm_mxfp8_swiglu_quant(_p(a), _p(a_sf), _p(b), _p(b_sf), int(b_layout), _p(gofs), int(G),
-                                               int(M), int(N), int(K), _p(a_pre), _p(h), _p(h_codes_row),
-                                               _p(h_scales_row), _p(h_codes_col), _p(h_scales_col), _p(err),
-                                               _stream(stream)))
+    args = (_p(a), _p(a_sf), _p(b), _p(b_sf), int(b_layout), _p(gofs), int(G), int(M), int(N), int(K), _p(a_pre),
+            _p(h), _p(h_codes_row), _p(h_scales_row), _p(h_codes_col), _p(h_scales_col))
+    if opts is None:
+        _check("grouped_gemm_mxfp8_swiglu_quant",
+               lib.grouped_gemm_mxfp8_swiglu_quant(*args, _p(err), _stream(stream)))
+    else:
+        _check("grouped_gemm_mxfp8_swiglu_quant_ex",
+               lib.grouped_gemm_mxfp8_swiglu_quant_ex(*args, ctypes.byref(opts), _p(err), _stream(stream)))
     return a_pre, h, h_codes_row, h_scales_row, h_codes_col, h_scales_col
 
 
@@ -427,14 +489,18 @@ def nvfp4_quantize_cols(x, gofs, G, codes_t=None, scales_t=None, tensor_scale=No
 
 
 def grouped_gemm_nvfp4(mode, a, a_sf, a_scale, b, b_sf, b_scale, gofs, G, M, N, K, epilogue=MOE_EPI_NONE, d=None,
-                       err=None, stream=None):
+                       err=None, stream=None, opts=None):
     """See include/moe.h.  Allocates d when not given."""
     if d is None:
         shape = (G, M, N) if mode == MOE_GEMM_WGRAD else (M, N)
         d = _empty(shape, torch.float32 if epilogue == MOE_EPI_NONE_F32 else torch.bfloat16, a)
-    _check("grouped_gemm_nvfp4", lib.grouped_gemm_nvfp4(int(mode), _p(a), _p(a_sf), _p(a_scale), _p(b), _p(b_sf),
-                                                        _p(b_scale), _p(gofs), int(G), int(M), int(N), int(K),
-                                                        int(epilogue), _p(d), _p(err), _stream(stream)))
+    args = (int(mode), _p(a), _p(a_sf), _p(a_scale), _p(b), _p(b_sf), _p(b_scale), _p(gofs), int(G), int(M), int(N),
+            int(K), int(epilogue), _p(d))
+    if opts is None:
+        _check("grouped_gemm_nvfp4", lib.grouped_gemm_nvfp4(*args, _p(err), _stream(stream)))
+    else:
+        _check("grouped_gemm_nvfp4_ex", lib.grouped_gemm_nvfp4_ex(*args, ctypes.byref(opts), _p(err),
+                                                                  _stream(stream)))
     return d
 
 

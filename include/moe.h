@@ -114,6 +114,57 @@ typedef enum {
                        layout of the [N, G*K] matrix)                          */
 } moe_b_layout_t;
 
+/*
+ * Grouped-GEMM kernel selection, per call (the *_ex entry points; the plain
+ * entry points use MOE_GEMM_KERNEL_AUTO).  AUTO applies the library's own
+ * rule, the kernel measured fastest for the call's mode and shape: WGRAD on
+ * the CTA pair; plain-epilogue FWD/DGRAD with K <= 2048, >= 65,536 rows and
+ * >= 512 rows per group on the CTA pair; everything else on the 1-SM kernel.
+ * The other values force one kernel; every kernel computes the same
+ * results (the parity tests run each of them).
+ */
+typedef enum {
+    MOE_GEMM_KERNEL_AUTO = 0,
+    MOE_GEMM_KERNEL_1SM = 1,       /* one CTA per 128 x 256 tile (128 x 128 if N % 256 != 0) */
+    MOE_GEMM_KERNEL_1SM_N128 = 2,  /* one CTA per 128 x 128 tile, two TMEM accumulators */
+    MOE_GEMM_KERNEL_PAIR = 3,      /* a CTA pair (tcgen05 cta_group::2) per 256 x 256 tile
+                                      (256 x 128 if N % 256 != 0) */
+    MOE_GEMM_KERNEL_PAIR_N128 = 4  /* a CTA pair per 256 x 128 tile, two accumulators per CTA */
+} moe_gemm_kernel_t;
+
+/*
+ * Options of one grouped-GEMM call (NULL = all defaults).
+ *   kernel           moe_gemm_kernel_t.  WGRAD with M % 256 != 0 runs on the
+ *                    1-SM kernel whatever is asked, and so does any call if
+ *                    no CTA pair fits on the device.  NVFP4 has no 128-wide
+ *                    instances: 1SM_N128 runs as 1SM, PAIR_N128 as PAIR.
+ *   band             m-tiles per raster band of the persistent tile order
+ *                    (consecutive tiles walk the n-tiles of a band of m-tiles
+ *                    that share them), 1..64; 0 = the kernel's measured
+ *                    default.
+ *   register_stores  1: the CTA-pair kernel's plain bf16 epilogue stores
+ *                    from registers instead of staging through shared memory
+ *                    for TMA stores; 0 = default (TMA stores).
+ * Values out of range return MOE_ERR_INVALID_ARG.
+ */
+typedef struct {
+    int kernel;
+    int band;
+    int register_stores;
+} moe_gemm_opts_t;
+
+/* Calls that may take a workspace (moe_workspace_size). */
+typedef enum {
+    MOE_OP_ROUTE_TOPK = 0,
+    MOE_OP_PERMUTE = 1,
+    MOE_OP_GROUP_QUANTIZE = 2,
+    MOE_OP_GATHER_QUANTIZE = 3,
+    MOE_OP_GROUPED_GEMM = 4,
+    MOE_OP_UNPERMUTE_COMBINE = 5,
+    MOE_OP_COMBINE_BWD = 6,
+    MOE_OP_ROUTE_BWD = 7
+} moe_op_t;
+
 /* Version of this ABI (major*100 + minor). */
 MOE_API int moe_abi_version(void);
 
@@ -121,8 +172,12 @@ MOE_API int moe_abi_version(void);
 MOE_API const char* moe_status_string(int status);
 
 /* Select `device`, cache its SM count and set kernel attributes (large shared
- * memory).  Idempotent; call it once per device before the first call on
- * that device and outside any stream capture. */
+ * memory).  Call it once per device before the first call on that device,
+ * outside any stream capture.  Calling it again is harmless: every call
+ * redoes the set-up in the context current at the time, so a process that
+ * resets the device (cudaDeviceReset) calls moe_init again before using the
+ * library.  The library works in the runtime API's primary context of each
+ * device. */
 MOE_API moe_status_t moe_init(int device);
 
 /* Rows a permuted buffer needs: ceil128(T*k + 127*min(E, T*k)). */
@@ -134,8 +189,21 @@ MOE_API size_t moe_route_workspace_size(int T, int E);
 MOE_API size_t moe_permute_workspace_size(int T, int E);
 
 /*
- * moe_route_topk -- the router's top-k ([TE-JAX] intro and "Optimization 2":
- * the fused router kernels assign each token to its Top-K experts).
+ * moe_workspace_size -- device workspace bytes that call `op` (moe_op_t)
+ * needs for a layer of T tokens, hidden size d, E expert groups (routed plus
+ * shared), top-k and expert FFN width f.  Only MOE_OP_ROUTE_TOPK
+ * (= moe_route_workspace_size(T, E)) and MOE_OP_PERMUTE
+ * (= moe_permute_workspace_size(T, E)) take a workspace; every other op
+ * returns 0 (its only scratch is the caller's outputs).  Returns (size_t)-1
+ * for an unknown op or sizes out of range (T < 0, d, E, k or f < 1).  Host
+ * only, no device call.
+ */
+MOE_API size_t moe_workspace_size(int op, int T, int d, int E, int k, int f);
+
+/*
+ * moe_route_topk -- the router's top-k ([TE-JAX] introduction: the router
+ * picks k experts per token; "Optimization 2": routing runs as fused router
+ * kernels).
  *   logits   [T, E] fp32.
  *   topk_idx [T, k] int32 out: the k largest logits per token, in
  *            descending order; equal logits go to the lower expert index.
@@ -145,6 +213,8 @@ MOE_API size_t moe_permute_workspace_size(int T, int E);
  *   counts   [E] int32 out: pairs routed to each expert (sum = T*k).
  *   offsets  [E+1] int32 out: exclusive prefix sum of counts (unpadded).
  *   ws       >= moe_route_workspace_size(T, E) bytes.
+ *   err      not written: routing has no device-side checks (finite logits
+ *            are the caller's contract); may be NULL.
  * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), T >= 0.
  */
 MOE_API moe_status_t moe_route_topk(const float* logits, int T, int E, int k, int score, int normalize,
@@ -204,6 +274,32 @@ MOE_API moe_status_t moe_permute(const void* x, int T, int d, int E, int k, cons
 MOE_API moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols, int axis,
                                   const int32_t* gofs, int G, uint8_t* codes, uint8_t* scales,
                                   int32_t* err, void* stream);
+/*
+ * Padded offsets of the group-aware columnwise output.  The plain definition
+ * of the group-aware quantization pads group g's tail block and places the
+ * group at sum_{h<g} ceil32(m_h) rows.  Here the permute already places
+ * every group at a multiple of 128 rows (gofs, moe_permute), which is a
+ * multiple of 32, with zero rows after its m_g routed rows: the padded
+ * offsets of this output ARE gofs, so no separate array is returned.  Block
+ * j of group g covers rows gofs[g] + 32 j ..; blocks past ceil32(m_g) rows
+ * of the group hold only zero rows (scale byte 0, codes 0).
+ *
+ * Scale layout.  Every call here reads and writes scales in the atom layout
+ * (the tensor cores' order, above), so no conversion runs on the hot path;
+ * mxfp8_scale_layout converts to and from the canonical row-major
+ * [rows, cols / 32] layout for callers that want it.
+ */
+
+/*
+ * mxfp8_scale_layout -- converts the scales of a [rows, cols] matrix
+ * quantized along cols between the atom layout and the canonical row-major
+ * layout, where byte r * (cols / 32) + b is the scale of row r, block b.
+ *   to_canonical 1: src = atoms, dst = canonical; 0: the reverse.
+ *   src, dst     rows * cols / 32 bytes each (device), not overlapping.
+ * rows % 128 == 0, cols % 128 == 0.  Pure data movement, one launch.
+ */
+MOE_API moe_status_t mxfp8_scale_layout(const uint8_t* src, int64_t rows, int cols, int to_canonical, uint8_t* dst,
+                                        void* stream);
 
 /*
  * mxfp8_gather_quantize -- the rowwise and the group-aware columnwise MXFP8
@@ -306,6 +402,13 @@ MOE_API moe_status_t grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_
                                 int epilogue, const void* epi_aux, void* d, void* d2,
                                 int32_t* err, void* stream);
 
+/* grouped_gemm_mxfp8 with per-call kernel options (moe_gemm_opts_t, may be
+ * NULL = grouped_gemm_mxfp8). */
+MOE_API moe_status_t grouped_gemm_mxfp8_ex(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                                           const uint8_t* b_sf, int b_layout, const int32_t* gofs, int G, int64_t M,
+                                           int N, int64_t K, int epilogue, const void* epi_aux, void* d, void* d2,
+                                           const moe_gemm_opts_t* opts, int32_t* err, void* stream);
+
 /*
  * grouped_gemm_mxfp8_swiglu_quant -- the up/gate GEMM (MOE_GEMM_FWD,
  * MOE_EPI_SWIGLU) with the MXFP8 quantization of h fused into its epilogue
@@ -327,6 +430,14 @@ MOE_API moe_status_t grouped_gemm_mxfp8_swiglu_quant(const uint8_t* a, const uin
                                              int64_t M, int N, int64_t K, void* a_pre, void* h,
                                              uint8_t* h_codes_row, uint8_t* h_scales_row, uint8_t* h_codes_col,
                                              uint8_t* h_scales_col, int32_t* err, void* stream);
+
+/* grouped_gemm_mxfp8_swiglu_quant with per-call kernel options (may be NULL). */
+MOE_API moe_status_t grouped_gemm_mxfp8_swiglu_quant_ex(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                                                        const uint8_t* b_sf, int b_layout, const int32_t* gofs, int G,
+                                                        int64_t M, int N, int64_t K, void* a_pre, void* h,
+                                                        uint8_t* h_codes_row, uint8_t* h_scales_row,
+                                                        uint8_t* h_codes_col, uint8_t* h_scales_col,
+                                                        const moe_gemm_opts_t* opts, int32_t* err, void* stream);
 
 /*
  * gemm_bf16_nt -- dense D = A * B^T with bf16 operands on the tensor cores
@@ -372,7 +483,13 @@ MOE_API moe_status_t moe_unpermute_combine(const void* y_perm, const int32_t* sl
                                    int T, int d, int k, void* out, int32_t* err, void* stream);
 
 /*
- * moe_combine_bwd -- adjoint of the weighted combine.
+ * moe_combine_bwd -- adjoint of the weighted combine of
+ * moe_unpermute_combine ([TE-JAX] "Optimization 2" and [CH1] §2.3.2 define
+ * the forward combine, a sum weighted by the routing weights; the pages give
+ * no backward.  Reading: the backward of every step is the plain gradient of
+ * its forward, with the MXFP8 quantization passed through as the identity,
+ * and the product w * dout is rounded once to fp32 and then to bf16, the
+ * activations' type).
  *   dy_perm[slot_of[t, j]] = bf16(w[t, j] * dout[t]); padding rows (row_id
  *   == -1, below gofs[E]) are written as zeros.
  *   dw[t, j] = <dout[t], y_perm[slot_of[t, j]]> (fp32).
@@ -387,7 +504,11 @@ MOE_API moe_status_t moe_combine_bwd(const void* dout, const void* y_perm, const
 
 /*
  * moe_route_bwd -- gradient of the routing weights with respect to the
- * logits.  dlogits [T, E] fp32 out (every entry written).
+ * logits (the backward of moe_route_topk's weights: [TE-JAX] introduction
+ * and "Optimization 2" define the forward routing, the pages give no
+ * backward.  Reading: the plain gradient of the forward scores; the top-k
+ * selection itself is piecewise constant and has none).
+ * dlogits [T, E] fp32 out (every entry written).
  *   softmax+normalize: dl_i = w_i (dw_i - sum_j w_j dw_j) on the chosen, 0 else
  *   softmax raw:       dl_m = p_m ([m chosen] dw_m - sum_j p_j dw_j) for all m
  *   sigmoid+normalize: dl_i = s_i (1-s_i) (dw_i - sum_j w_j dw_j) / sum s
@@ -430,9 +551,12 @@ MOE_API moe_status_t moe_route_drop_shared(const float* dw_all, int T, int k, in
  * keeps until the process exits.
  *   Limit: ceil(T / 128) * E <= 262144 (e.g. T = 131072 with E = 256);
  *   larger sizes return MOE_ERR_WORKSPACE without launching anything.
- *   It calls no allocator.  Its first call on a device looks up the array's
- *   device address (cudaGetSymbolAddress); make that first call before any
- *   stream capture.  moe_init must have been called for the device.
+ *   It calls no allocator.  Its first call on a device after moe_init looks
+ *   up the array's device address (cudaGetSymbolAddress) and keeps it; make
+ *   that first call before any stream capture.  moe_init must have been
+ *   called for the device (it drops the kept address, so after a device
+ *   reset and a new moe_init the address is looked up again).
+ *   err is not written (as for moe_route_topk); it may be NULL.
  *   Every call uses the same array, so calls that may overlap on the GPU
  *   (different streams, or several host threads) race with each other; order
  *   them on one stream.  The array keeps the previous call's contents, which
@@ -541,6 +665,12 @@ MOE_API moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uint8_
                                         const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
                                         void* d, int32_t* err, void* stream);
 
+/* grouped_gemm_nvfp4 with per-call kernel options (may be NULL). */
+MOE_API moe_status_t grouped_gemm_nvfp4_ex(int mode, const uint8_t* a, const uint8_t* a_sf, const float* a_scale,
+                                           const uint8_t* b, const uint8_t* b_sf, const float* b_scale,
+                                           const int32_t* gofs, int G, int64_t M, int N, int64_t K, int epilogue,
+                                           void* d, const moe_gemm_opts_t* opts, int32_t* err, void* stream);
+
 /*
  * moe_selftest_bounded_wait -- checks the failure path of the kernels'
  * bounded waits without a GPU fault: one thread waits, with the same
@@ -552,6 +682,21 @@ MOE_API moe_status_t grouped_gemm_nvfp4(int mode, const uint8_t* a, const uint8_
  * pages have no counterpart: this is a test hook of the library.)
  */
 MOE_API moe_status_t moe_selftest_bounded_wait(uint64_t timeout_ns, int32_t* err, int32_t* completed, void* stream);
+
+/*
+ * moe_hbm_fill -- writes the 32-bit `value`, repeated, over `bytes` bytes at
+ * dst: a write-only stream with no reads, the measuring stick for the
+ * write-heavy quantization kernels (and a plain device memset).  (The pages
+ * have no counterpart: this is a measuring tool of the library.)
+ *   method 0: every thread stores 16-byte vectors (st.global.v4), 4 per
+ *             loop trip, grid-stride over the buffer, 8 CTAs of 256
+ *             threads per SM;
+ *   method 1: each CTA fills a 32 KB shared-memory buffer once and writes it
+ *             out with bulk asynchronous copies (cp.async.bulk
+ *             .global.shared::cta) of 32 KB, grid-stride, one CTA per SM.
+ * dst 16-byte aligned, bytes % 16 == 0.  One launch, no allocation.
+ */
+MOE_API moe_status_t moe_hbm_fill(void* dst, size_t bytes, uint32_t value, int method, void* stream);
 
 #ifdef __cplusplus
 }

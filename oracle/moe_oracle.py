@@ -628,9 +628,9 @@ def route_bwd(logits, idx, dw, score="softmax", normalize=True):
 # --------------------------------------------------------------------------
 
 # --------------------------------------------------------------------------
-# Router GEMM ([TE-JAX] "Optimization 2": "fused router kernels" assign the
-# tokens from the router's scores; the scores come from a learned linear
-# router, logits = x W_r)
+# Router GEMM ([TE-JAX] "Optimization 2": the routing step is done by fused
+# router kernels working from the router's scores.  Reading: the scores come
+# from a learned linear router, logits = x W_r)
 # --------------------------------------------------------------------------
 
 def router_logits(x, Wr):

@@ -2,6 +2,7 @@
 comparison rules of the parity tests.  No step of the method lives here."""
 from __future__ import annotations
 
+import functools
 import os
 import sys
 
@@ -33,6 +34,22 @@ def atoms_rows_subset(atoms, rows, cols, row_idx):
     b = np.arange(nb)[None, :]
     off = ((b // 4) * (rows // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
     return atoms[off]
+
+
+def atoms_block_range(atoms, rows, cols, b_lo, b_hi):
+    """Canonical scales [rows, b_hi - b_lo] of blocks b_lo .. b_hi-1 of every
+    row of a [rows, cols] matrix whose scales are in the atom layout."""
+    atoms = np.asarray(atoms, dtype=np.uint8).reshape(-1)
+    r = np.arange(rows)[:, None]
+    b = np.arange(b_lo, b_hi)[None, :]
+    off = ((b // 4) * (rows // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
+    return atoms[off]
+
+
+def bf16_bits_of(t):
+    """Bit patterns (numpy u16) of a bf16 torch tensor."""
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
 def to_np(t):
@@ -87,6 +104,24 @@ def gpu_ops():
     from grouped_gemm_top_gb300 import ops
     ops.moe_init(0)
     return ops
+
+
+class KernelOps:
+    """The ops module with every grouped-GEMM call bound to one kernel
+    choice (moe_gemm_opts_t through the *_ex entry points), so a test file
+    can run its whole GEMM suite once per kernel in one process."""
+    GEMMS = ("grouped_gemm_mxfp8", "grouped_gemm_mxfp8_swiglu_quant", "grouped_gemm_nvfp4")
+
+    def __init__(self, ops, kernel):
+        self._ops = ops
+        self.kernel = kernel
+        self._opts = ops.gemm_opts(kernel)
+
+    def __getattr__(self, name):
+        v = getattr(self._ops, name)
+        if name in self.GEMMS:
+            return functools.partial(v, opts=self._opts)
+        return v
 
 
 def padded_layout(sizes, align=128):

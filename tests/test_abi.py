@@ -22,9 +22,13 @@ def _declared():
 
 
 def test_header_declares_the_entry_points():
+    """The calls of the boundary: init, workspace sizing, routing, permute,
+    group-aware quantization, the grouped GEMM (fwd, dgrad, wgrad), combine
+    and the two backward helpers."""
     names = set(_declared())
-    for n in ("moe_route_topk", "moe_permute", "mxfp8_group_quantize", "grouped_gemm_mxfp8",
-              "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd", "moe_init"):
+    for n in ("moe_init", "moe_workspace_size", "moe_route_topk", "moe_permute", "mxfp8_group_quantize",
+              "grouped_gemm_mxfp8", "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd",
+              "mxfp8_scale_layout"):
         assert n in names
 
 
@@ -37,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib_path):
 def test_binding_matches_header(lib_path):
     from grouped_gemm_top_gb300 import ops
     assert set(ops.EXPORTS) == set(_declared())
-    assert ops.moe_abi_version() == 100
+    assert ops.moe_abi_version() == 101
 
 
 def test_host_only_calls_and_argument_checks(lib_path):
@@ -47,6 +51,15 @@ def test_host_only_calls_and_argument_checks(lib_path):
     assert ops.moe_row_capacity(24576, 256, 8) == 229120
     assert ops.moe_row_capacity(1, 8, 2) == 256               # 2 pairs: at most 2 groups of 128 rows
     assert ops.moe_route_workspace_size(24576, 256) == 192 * 256 * 4
+    # moe_workspace_size dispatches over the calls: only routing and permute take one
+    assert ops.moe_workspace_size(ops.MOE_OP_ROUTE_TOPK, 24576, 7168, 256, 8, 2048) == 192 * 256 * 4
+    assert ops.moe_workspace_size(ops.MOE_OP_PERMUTE, 24576, 7168, 256, 8, 2048) == \
+        ops.moe_permute_workspace_size(24576, 256)
+    for op in (ops.MOE_OP_GROUP_QUANTIZE, ops.MOE_OP_GATHER_QUANTIZE, ops.MOE_OP_GROUPED_GEMM,
+               ops.MOE_OP_UNPERMUTE_COMBINE, ops.MOE_OP_COMBINE_BWD, ops.MOE_OP_ROUTE_BWD):
+        assert ops.moe_workspace_size(op, 24576, 7168, 256, 8, 2048) == 0
+    assert ops.moe_workspace_size(99, 256, 512, 8, 2, 256) == -1
+    assert ops.moe_workspace_size(ops.MOE_OP_ROUTE_TOPK, 256, 512, 0, 2, 256) == -1
     assert ops.status_string(ops.MOE_ERR_BAD_OFFSETS).startswith("group offsets")
     # NULL pointers / bad sizes are rejected before any device work
     st = lib.moe_route_topk(None, 16, 8, 2, 0, 1, None, None, None, None, None, 0, None, None)
@@ -69,6 +82,26 @@ def test_host_only_calls_and_argument_checks(lib_path):
     st = lib.mxfp8_gather_quantize(ctypes.c_void_p(64), 256, 128, 1, None, None, ctypes.c_void_p(64), 1, 256,
                                    ctypes.c_void_p(48), ctypes.c_void_p(64), None, None, None, None)
     assert st == ops.MOE_ERR_ALIGNMENT
+    # kernel options out of range are refused before anything else runs
+    bad = ops.gemm_opts("pair")
+    bad.kernel = 9
+    st = lib.grouped_gemm_mxfp8_ex(0, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                   ctypes.c_void_p(16), 0, ctypes.c_void_p(16), 4, 256, 256, 256, 0, None,
+                                   ctypes.c_void_p(16), None, ctypes.byref(bad), None, None)
+    assert st == ops.MOE_ERR_INVALID_ARG
+    st = lib.mxfp8_scale_layout(ctypes.c_void_p(16), 100, 128, 1, ctypes.c_void_p(16), None)
+    assert st == ops.MOE_ERR_UNSUPPORTED                       # rows % 128 != 0
+    st = lib.moe_hbm_fill(ctypes.c_void_p(16), 24, 0, 0, None)
+    assert st == ops.MOE_ERR_UNSUPPORTED                       # bytes % 16 != 0
+
+
+def test_no_environment_variables_in_the_library():
+    """Kernel variants are chosen per call (moe_gemm_opts_t), never by the
+    environment: no getenv in the CUDA sources."""
+    csrc = os.path.join(ROOT, "grouped_gemm_top_gb300", "csrc")
+    for fn in os.listdir(csrc):
+        with open(os.path.join(csrc, fn)) as f:
+            assert "getenv" not in f.read(), fn
 
 
 def test_product_does_not_import_the_oracle():

@@ -1,21 +1,24 @@
 """Grouped MXFP8 GEMM (tcgen05) vs the fp64 oracle on the GPU's own
 dequantized operands: fwd, dgrad (both weight layouts), wgrad, SwiGLU and
-SwiGLU-backward epilogues, empty groups, padding rows, several tiles."""
+SwiGLU-backward epilogues, empty groups, padding rows, several tiles.  The
+whole file runs once per kernel: the library's own choice ("auto"), the
+1-SM kernel with 256- and 128-wide tiles, and the CTA-pair kernel with
+256- and 128-wide tiles (chosen per call through moe_gemm_opts_t)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
-from helpers import (assert_bf16_close, assert_fp32_close, atoms_rows_subset, atoms_to_rowmajor,
+from helpers import (KernelOps, assert_bf16_close, assert_fp32_close, atoms_rows_subset, atoms_to_rowmajor,
                      batched_weight_operand, glu_perm, gpu_ops, padded_layout, to_np)
 from grouped_gemm_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def ops():
-    return gpu_ops()
+@pytest.fixture(scope="module", params=["auto", "1sm", "1sm_n128", "pair", "pair_n128"])
+def ops(request):
+    return KernelOps(gpu_ops(), request.param)
 
 
 def _act(sizes, K, seed, row_cap=None):
@@ -278,6 +281,14 @@ def test_wgrad(ops, sizes, Mo, No):
             assert torch.all(d[g] == 0)
         else:
             assert_bf16_close(d[g], ref[g], what=f"wgrad g={g}")
+    if ops.kernel == "pair":
+        # the pair kernel's register-staged stores write the same bytes as its TMA stores
+        d2 = torch.full((G, Mo, No), 3.0, dtype=torch.bfloat16, device="cuda")
+        ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, aq, as_, gq, gs, 0, gofs_t, G, Mo, No, Kc, d=d2, err=err,
+                               opts=ops.gemm_opts("pair", register_stores=True))
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(d2, d)
 
 
 def test_bad_offsets_reported_not_faulting(ops):

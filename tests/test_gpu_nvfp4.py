@@ -99,13 +99,14 @@ def _operands(ops, sizes, N, K, seed):
     ([700, 1500, 260], 2048, 7168),
 ])
 @pytest.mark.parametrize("mode", ["fwd", "dgrad"])
-def test_nvfp4_grouped_gemm_matches_oracle(ops, sizes, N, K, mode):
+@pytest.mark.parametrize("kernel", ["auto", "pair"])     # the 1-SM kernel (default) and the CTA-pair instance
+def test_nvfp4_grouped_gemm_matches_oracle(ops, sizes, N, K, mode, kernel):
     o = _operands(ops, sizes, N, K, sum(sizes) + N)
     m = ops.MOE_GEMM_FWD if mode == "fwd" else ops.MOE_GEMM_DGRAD
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     d = torch.full((o["M"], N), 7.0, dtype=torch.bfloat16, device="cuda")
     ops.grouped_gemm_nvfp4(m, o["aq"], o["asf"], o["ast"], o["bq"], o["bsf"], o["bst"], o["gofs_t"], o["G"], o["M"],
-                           N, K, ops.MOE_EPI_NONE, d, err)
+                           N, K, ops.MOE_EPI_NONE, d, err, opts=ops.gemm_opts(kernel))
     torch.cuda.synchronize()
     assert err.item() == 0
     R = int(o["gofs"][-1])
@@ -114,11 +115,13 @@ def test_nvfp4_grouped_gemm_matches_oracle(ops, sizes, N, K, mode):
     assert torch.all(d[R:] == 7.0)                              # rows outside every group untouched
 
 
-def test_nvfp4_grouped_gemm_fp32_out(ops):
+@pytest.mark.parametrize("kernel", ["auto", "pair"])
+def test_nvfp4_grouped_gemm_fp32_out(ops, kernel):
     o = _operands(ops, [256, 128, 512], 256, 512, 77)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     d = ops.grouped_gemm_nvfp4(ops.MOE_GEMM_FWD, o["aq"], o["asf"], o["ast"], o["bq"], o["bsf"], o["bst"],
-                               o["gofs_t"], o["G"], o["M"], 256, 512, ops.MOE_EPI_NONE_F32, err=err)
+                               o["gofs_t"], o["G"], o["M"], 256, 512, ops.MOE_EPI_NONE_F32, err=err,
+                               opts=ops.gemm_opts(kernel))
     torch.cuda.synchronize()
     assert err.item() == 0
     R = int(o["gofs"][-1])

@@ -97,3 +97,25 @@ def test_permute_rejects_bad_expert_index(ops):
     ops.moe_permute(x, idx, 8, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == ops.MOE_ERR_BAD_EXPERT
+
+
+def test_permute_duplicate_choice_gets_no_slot(ops):
+    """A token that names one expert twice: the error word says so, the
+    repeated choice (and an out-of-range one) gets slot -1, and the valid
+    choices keep distinct slots whose row_id entries point back at them."""
+    idx = torch.tensor([[0, 1], [2, 9], [3, 3], [1, 3]], dtype=torch.int32, device="cuda")
+    x = torch.ones((4, 128), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gofs, slot_of, row_id, _ = ops.moe_permute(x, idx, 8, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == ops.MOE_ERR_BAD_EXPERT
+    s = slot_of.cpu().numpy()
+    assert s[1, 1] == -1 and s[2, 1] == -1              # out of range; repeated expert 3
+    valid = [(t, j) for t in range(4) for j in range(2) if s[t, j] >= 0]
+    assert len(valid) == 6 and len({s[t, j] for t, j in valid}) == 6
+    rid = row_id.cpu().numpy()
+    for t, j in valid:
+        assert rid[s[t, j]] == t * 2 + j
+    # counts (and so the group offsets) see each valid choice once
+    g = gofs.cpu().numpy()
+    assert g[-1] == 128 * 4            # experts 0, 1, 2, 3 hold rows
