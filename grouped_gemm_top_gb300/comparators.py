@@ -77,6 +77,14 @@ class LoopMoE:
     def _sf(t, s, e, c):
         return t[s * c // 32:e * c // 32]
 
+    def _sfc(self, t, s, e, c):
+        """Per-expert slice of a columnwise scale buffer of the layer's layout
+        (tile-224: whole k-blocks of ceil(c / 224) 1024-byte tiles)."""
+        if not self.L.wgrad_t224:
+            return self._sf(t, s, e, c)
+        tb = (c + 223) // 224 * 1024
+        return t[s // 128 * tb:e // 128 * tb]
+
     def step_(self):
         """One fwd+bwd step: route and permute once, read the group offsets
         on the host, then per expert its quantizations and GEMMs."""
@@ -103,21 +111,22 @@ class LoopMoE:
         ops.moe_combine_bwd(L.dout, L.y_perm, L.slot_of, L.topk_w, None, None, G, None, L.dw, err, want_dy=False)
         for g, s, e in live:
             m, gt = e - s, self.tab[(e - s) // 128]
-            dyqT, dysT = cols(L.dyqT, s, e, d), sf(L.dysT, s, e, d)
+            dyqT, dysT = cols(L.dyqT, s, e, d), self._sfc(L.dysT, s, e, d)
             ops.mxfp8_gather_quantize(L.dout, gt, 1, m, L.row_id[s:e], k, L.topk_w, True, True, L.dyq[s:e],
-                                      sf(L.dys, s, e, d), dyqT, dysT, err)
+                                      sf(L.dys, s, e, d), dyqT, dysT, err, col_sf_layout=L.col_sf)
             ops.grouped_gemm_mxfp8(ops.MOE_GEMM_DGRAD, L.dyq[s:e], sf(L.dys, s, e, d), self.W2d[g], self.W2d_s[g],
                                    B, gt, 1, m, f, d, ops.MOE_EPI_NONE_F32, None, L.dH[s:e], None, err)
-            ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, cols(L.hqT, s, e, f), sf(L.hsT, s, e, f), dyqT, dysT, 0, gt,
-                                   1, f, d, m, ops.MOE_EPI_NONE, None, L.dW2[g:g + 1], None, err)
-            dAqT, dAsT = cols(L.dAqT, s, e, 2 * f), sf(L.dAsT, s, e, 2 * f)
+            ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, cols(L.hqT, s, e, f), sf(L.hsT, s, e, f), dyqT, dysT, L.wgrad_b,
+                                   gt, 1, f, d, m, ops.MOE_EPI_NONE, None, L.dW2[g:g + 1], None, err)
+            dAqT, dAsT = cols(L.dAqT, s, e, 2 * f), self._sfc(L.dAsT, s, e, 2 * f)
             ops.mxfp8_swiglu_bwd_quantize(L.dH[s:e], L.a_pre[s:e], gt, 1, None if L.dA is None else L.dA[s:e],
-                                          False, L.dAq[s:e], sf(L.dAs, s, e, 2 * f), dAqT, dAsT, err)
+                                          False, L.dAq[s:e], sf(L.dAs, s, e, 2 * f), dAqT, dAsT, err,
+                                          col_sf_layout=L.col_sf)
             ops.grouped_gemm_mxfp8(ops.MOE_GEMM_DGRAD, L.dAq[s:e], sf(L.dAs, s, e, 2 * f), self.W1d[g],
                                    self.W1d_s[g], B, gt, 1, m, d, 2 * f, ops.MOE_EPI_NONE, None, L.dx_perm[s:e], None,
                                    err)
-            ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, cols(L.xqT, s, e, d), sf(L.xsT, s, e, d), dAqT, dAsT, 0, gt,
-                                   1, d, 2 * f, m, ops.MOE_EPI_NONE, None, L.dW1[g:g + 1], None, err)
+            ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, cols(L.xqT, s, e, d), sf(L.xsT, s, e, d), dAqT, dAsT,
+                                   L.wgrad_b, gt, 1, d, 2 * f, m, ops.MOE_EPI_NONE, None, L.dW1[g:g + 1], None, err)
         for g in range(G):           # an expert without tokens has zero weight gradients
             if go[g + 1] == go[g]:
                 L.dW1[g].zero_()

@@ -601,8 +601,10 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
                     moe_aligned16(d) && (d2 == nullptr || moe_aligned16(d2)) &&
                     (epi_aux == nullptr || moe_aligned16(epi_aux)),
                 MOE_ERR_ALIGNMENT);
+    const bool t224 = mode == MOE_GEMM_WGRAD && b_layout == MOE_B_SF_TILE224;
     if (mode == MOE_GEMM_WGRAD) {
         MOE_REQUIRE(epilogue == MOE_EPI_NONE, MOE_ERR_INVALID_ARG);
+        MOE_REQUIRE(b_layout == MOE_B_GNK || b_layout == MOE_B_NGK || t224, MOE_ERR_INVALID_ARG);
     } else {
         MOE_REQUIRE(b_layout == MOE_B_GNK || b_layout == MOE_B_NGK, MOE_ERR_INVALID_ARG);
         MOE_REQUIRE(epilogue == MOE_EPI_NONE || epilogue == MOE_EPI_SWIGLU || epilogue == MOE_EPI_SWIGLU_BWD ||
@@ -612,6 +614,7 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
         if (epilogue == MOE_EPI_SWIGLU_BWD) MOE_REQUIRE(epi_aux != nullptr, MOE_ERR_INVALID_ARG);
     }
     MOE_REQUIRE(device_initialized() && g_encode != nullptr, MOE_ERR_NOT_INITIALIZED);
+    if (t224) MOE_REQUIRE(M % 256 == 0 && gemm_max_clusters_2sm(224) > 0, MOE_ERR_UNSUPPORTED);
 
     CUtensorMap tmA, tmB;
     Params p{};
@@ -681,13 +684,15 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     // cost per tile outweighs a group's half-idle odd last pair tile
     const bool pair_fwd = epilogue == MOE_EPI_NONE && K <= 2048 && N % 256 == 0 && M >= 65536 && M >= 512LL * G;
     if (sel < 0) sel = (mode == MOE_GEMM_WGRAD || pair_fwd) ? 256 : 0;
-    const int bn2 = sel == 256 && N % 256 == 0 ? 256 : 128;
+    if (t224) sel = 224;      // the scale layout of b fixes the tile
+    const int bn2 = sel == 224 ? 224 : (sel == 256 && N % 256 == 0 ? 256 : 128);
     const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
     if (two_sm) {
-        p.n_tiles = N / bn2;
+        p.n_tiles = (N + bn2 - 1) / bn2;
         p.band = choice.band > 0 ? choice.band : 2;     // measured: 2 beat 4, 8 and 16
         const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles
                                                            : (M / BM) * (int64_t)p.n_tiles;
+        if (t224) p.b_sf_kstride = (int64_t)p.n_tiles * 1024;     // tile-224 layout of b's scales
         const int clusters = (int)std::min<int64_t>(std::max<int64_t>(upper_pairs, 1), gemm_max_clusters_2sm(bn2));
         // B boxes of bn2/2 rows (each CTA of the pair loads half of the tile's B rows)
         CUtensorMap tmB2;
@@ -709,14 +714,16 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
         // atoms in the scale arrays (bounds of the scale tensor maps)
         const int64_t atoms_a = (K / 128) * (M / 128);
         int64_t atoms_b;
-        if (mode == MOE_GEMM_WGRAD) atoms_b = (K / 128) * (N / 128);
+        if (t224) atoms_b = (K / 128) * (int64_t)p.n_tiles * 2;
+        else if (mode == MOE_GEMM_WGRAD) atoms_b = (K / 128) * (N / 128);
         else atoms_b = (int64_t)G * (K / 128) * (N / 128);
         CUtensorMap tmSFA, tmSFB;
-        MOE_REQUIRE(make_sf_map(&tmSFA, a_sf, atoms_a, 2) && make_sf_map(&tmSFB, b_sf, atoms_b, 2 * (bn2 / 128)),
+        MOE_REQUIRE(make_sf_map(&tmSFA, a_sf, atoms_a, 2) &&
+                        make_sf_map(&tmSFB, b_sf, atoms_b, 2 * ((bn2 + 127) / 128)),
                     MOE_ERR_CUDA);
         // D through the TMA: bf16 [rows, N] in 32-row x 64-column boxes
         CUtensorMap tmD = tmA;
-        p.tma_store = bn2 == 256 && epilogue == MOE_EPI_NONE && !choice.register_stores;
+        p.tma_store = (bn2 == 256 && epilogue == MOE_EPI_NONE && !choice.register_stores) || bn2 == 224;
         if (p.tma_store) {
             const int64_t drows = mode == MOE_GEMM_WGRAD ? (int64_t)G * M : M;
             MOE_REQUIRE(make_d_map(&tmD, d, drows, N), MOE_ERR_CUDA);

@@ -34,9 +34,16 @@ namespace moe {
 namespace gg {
 namespace sm2 {
 
-// Pair-tile configurations: N = 256 (one accumulator per CTA) or N = 128
-// (two accumulators per CTA, so the epilogue of one tile overlaps the
-// mainloop of the next).  Each CTA loads BN/2 rows of B.
+// Pair-tile configurations: N = 256 (one accumulator per CTA), N = 128 or
+// N = 224 (two accumulators per CTA, so the epilogue of one tile overlaps
+// the mainloop of the next).  Each CTA loads BN/2 rows of B.  Two 256-column
+// accumulators would fill all 512 TMEM columns and leave none for the block
+// scales; two of 224 columns leave 64, room for five stages of scales (A: 4
+// columns, B: 8).  N = 224 serves the weight gradients (MOE_GEMM_WGRAD),
+// whose short contractions (one group's rows) otherwise leave the tensor
+// pipe idle while the single accumulator is drained; its B scales come in
+// the tile-224 layout (two atoms per 224 rows, include/moe.h), since 224-row
+// tiles do not start on the 128-row atoms of the plain layout.
 // NVF4: NVFP4 operands (packed E2M1, UE4M3 scales per 16, kind::mxf4nvf4):
 // four scale atoms per 128 rows and k-step instead of one, plain epilogues
 // only (no TMA-store staging).
@@ -44,17 +51,18 @@ template <int BN_, bool NVF4 = false>
 struct C2 {
     static constexpr int BN = BN_;
     static constexpr int BH = BN_ / 2;                  // B rows per CTA
-    static constexpr int NACC = BN_ == 128 ? 2 : 1;
-    static constexpr int STAGES = BN_ == 128 ? 8 : (NVF4 || kEpiBoxCols == 64 ? 5 : 6);
+    static constexpr int NACC = BN_ == 256 ? 1 : 2;
+    static constexpr int STAGES = BN_ == 128 ? 8 : (BN_ == 224 || NVF4 || kEpiBoxCols == 64 ? 5 : 6);
     static constexpr int A_STAGE = BM * BK;             // this CTA's 128 A rows
     static constexpr int B_STAGE = BH * BK;             // this CTA's half of B
     static constexpr int SFA_BYTES = NVF4 ? 2048 : 512;
-    static constexpr int SFB_BYTES = (BN_ / 128) * SFA_BYTES;   // scales of all BN B rows
+    static constexpr int SFB_BYTES = ((BN_ + 127) / 128) * SFA_BYTES;   // scales of all BN B rows
     static constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_BYTES + SFB_BYTES;
     static constexpr uint32_t SF0 = NACC * BN_;         // TMEM: accumulators, then scales
-    static constexpr uint32_t SF_COLS = NVF4 ? 16 + 16 * (BN_ / 128) : TMEM_SF_STRIDE;
-    // TMA-store staging of the epilogue (N = 256): one box per epilogue warp
-    static constexpr int EPI_BYTES = (BN_ == 256 && !NVF4) ? EPI_WARPS * kEpiBoxBytes : 0;
+    static constexpr uint32_t SF_COLS = NVF4 ? 16 + 16 * (BN_ / 128) : (BN_ == 224 ? 12 : TMEM_SF_STRIDE);
+    // TMA-store staging of the epilogue: one box per epilogue warp (N = 256),
+    // two that alternate (N = 224, whose smaller stages leave the room)
+    static constexpr int EPI_BYTES = (BN_ >= 224 && !NVF4) ? EPI_WARPS * kEpiBoxBytes * (BN_ == 224 ? 2 : 1) : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;       // 1024-byte aligned
@@ -231,6 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                        const __grid_constant__ CUtensorMap tmD, const Params p) {
     using C = C2<BN, NVF4>;
     static_assert(!NVF4 || (BN == 256 && (EPI == MOE_EPI_NONE || EPI == MOE_EPI_NONE_F32)), "NVFP4 pair instances");
+    static_assert(BN != 224 || (EPI == MOE_EPI_NONE && !NVF4), "224-wide pair tiles: weight gradients, bf16 out");
     constexpr int STAGES = C::STAGES, NACC = C::NACC, BH = C::BH;
     constexpr int OFF_A = C::OFF_A, OFF_B = C::OFF_B, OFF_SFA = C::OFF_SFA, OFF_SFB = C::OFF_SFB;
     constexpr int OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC, OFF_GOFS = C::OFF_GOFS, OFF_PT = C::OFF_PT;
@@ -336,8 +345,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // (NVFP4: a k-step's four atoms of a 128-row tile are 2 KB in
                 // a row, the pair tile's two row tiles 4 KB)
                 const int64_t sfa_row = (kg * p.a_sf_kstride + (ti.a_row / 128) * SFA_BYTES) / 256;
-                const int64_t sfb_row =
-                    ((int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride + (ti.b_row_pair / 128) * SFA_BYTES) / 256;
+                // (tile-224 layout: the tile's two atoms at nt * 1024 of the k-step)
+                const int64_t sfb_tile = BN == 224 ? (int64_t)ti.nt * 1024 : (int64_t)(ti.b_row_pair / 128) * SFA_BYTES;
+                const int64_t sfb_row = ((int64_t)gB * p.b_sf_gstride + kg * p.b_sf_kstride + sfb_tile) / 256;
                 tma2_load_2d(smem_u32(smem + OFF_SFA + stage * SFA_BYTES), &tmSFA, 0, (int)sfa_row, fb);
                 tma2_load_2d(smem_u32(smem + OFF_SFB + stage * SFB_BYTES), &tmSFB, 0, (int)sfb_row, fb);
                 pend[stage] = (int)phase;
@@ -400,7 +410,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 } else {
                     tc_cp_sf2(t_sfa, desc_sf(s_sfa));
 #pragma unroll
-                    for (int h = 0; h < BN / 128; ++h) tc_cp_sf2(t_sfb + 4 * h, desc_sf(s_sfb + 512 * h));
+                    for (int h = 0; h < (BN + 127) / 128; ++h) tc_cp_sf2(t_sfb + 4 * h, desc_sf(s_sfb + 512 * h));
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; ++kk)
                         tc_mma2(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk),
@@ -433,13 +443,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int quarter = ew & 3, half = ew >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t nbox = 0;       // TMA-store boxes this warp has issued (224-wide tiles)
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         for (int64_t t = pair; t < total; t += npairs) {
             Tile2 ti;
             get_tile2<BN>(p, s_gofs, s_pt, total_pm, t, rank, ti);
             const int64_t row = ti.out_row + quarter * 32 + lane;
             if (ti.nk == 0) {
-                epilogue_zero<BN>(p, row, ti.nt, half);
+                if constexpr (BN == 224)
+                    epilogue_zero224(p, row, ti.nt, half);
+                else
+                    epilogue_zero<BN>(p, row, ti.nt, half);
                 continue;
             }
             ApreChunk apre;
@@ -464,6 +478,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 release();
             } else if constexpr (EPI == MOE_EPI_SWIGLU_BWD) {
                 epilogue_swiglu_bwd<BN>(p, tacc, row, ti.nt, half, release, apre);
+            } else if constexpr (BN == 224) {
+                epilogue_tile_tma224(&tmD, smem_u32(smem + C::OFF_EPI + 2 * kEpiBoxBytes * ew), tacc, row - lane,
+                                     ti.nt, half, lane, p.N, nbox, release);
             } else if (!NVF4 && BN == 256 && EPI == MOE_EPI_NONE && p.tma_store) {
                 epilogue_tile_tma(&tmD, smem_u32(smem + C::OFF_EPI + kEpiBoxBytes * ew), tacc, row - lane, ti.nt, half, lane,
                                   release);
@@ -496,7 +513,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace sm2
 }  // namespace gg
 
-static int g_max_clusters[2] = {0, 0};   // [N = 128, N = 256]
+static int g_max_clusters[3] = {0, 0, 0};   // [N = 128, N = 256, N = 224]
 
 template <int BN>
 static cudaLaunchConfig_t launch_cfg(int clusters, cudaStream_t stream, cudaLaunchAttribute* attr) {
@@ -540,6 +557,15 @@ cudaError_t gemm_set_attributes_2sm() {
     if (e != cudaSuccess) return e;
     e = set_attr_2sm<256>(&g_max_clusters[1]);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm<224, MOE_EPI_NONE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gg::sm2::C2<224>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = launch_cfg<224>(1024, nullptr, attr);
+        e = cudaOccupancyMaxActiveClusters(&g_max_clusters[2], gg::sm2::k_grouped_gemm_2sm<224, MOE_EPI_NONE>, &cfg);
+        if (e != cudaSuccess) return e;
+    }
     const cudaError_t es[] = {
         cudaFuncSetAttribute(gg::sm2::k_grouped_gemm_2sm<256, MOE_EPI_NONE, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, gg::sm2::C2<256, true>::SMEM_BYTES),
@@ -566,7 +592,7 @@ cudaError_t gemm_launch_2sm_nvf4(int epilogue, const CUtensorMap& tmA, const CUt
                               p);
 }
 
-int gemm_max_clusters_2sm(int bn) { return g_max_clusters[bn == 256 ? 1 : 0]; }
+int gemm_max_clusters_2sm(int bn) { return g_max_clusters[bn == 256 ? 1 : (bn == 224 ? 2 : 0)]; }
 
 template <int BN>
 static cudaError_t launch_2sm(int epilogue, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
@@ -594,6 +620,12 @@ cudaError_t gemm_launch_2sm(int bn, int epilogue, const CUtensorMap& tmA, const 
                             const CUtensorMap& tmSFA, const CUtensorMap& tmSFB, const CUtensorMap& tmD,
                             const gg::Params& p, int clusters, cudaStream_t stream) {
     if (bn == 256) return launch_2sm<256>(epilogue, tmA, tmB, tmSFA, tmSFB, tmD, p, clusters, stream);
+    if (bn == 224) {
+        if (epilogue != MOE_EPI_NONE) return cudaErrorInvalidValue;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = launch_cfg<224>(clusters, stream, attr);
+        return cudaLaunchKernelEx(&cfg, gg::sm2::k_grouped_gemm_2sm<224, MOE_EPI_NONE>, tmA, tmB, tmSFA, tmSFB, tmD, p);
+    }
     return launch_2sm<128>(epilogue, tmA, tmB, tmSFA, tmSFB, tmD, p, clusters, stream);
 }
 

@@ -144,6 +144,10 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// all but the most recent committed bulk store have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_group_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // the bulk stores committed so far are complete
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // this thread's shared-memory writes become visible to the TMA (async proxy)
@@ -608,6 +612,73 @@ __device__ __forceinline__ void epilogue_tile_tma(const CUtensorMap* tmD, uint32
     }
 }
 
+// TMA-store epilogue for the 224-wide weight-gradient tiles of the CTA-pair
+// kernel (two accumulators, plain bf16 output).  The tile's 224 columns are
+// seven 32-column chunks: the warps of column half 0 drain chunks 0-3, those
+// of half 1 chunks 4-6, into packed bf16 registers; then TMEM is released
+// and the chunks go out as 32 x 32 boxes through the warp's two staging
+// buffers `buf` and `buf + kEpiBoxBytes` in turn, across tiles (`nbox`
+// counts the warp's boxes, so consecutive boxes always use different
+// buffers and a buffer is rewritten only once the store issued from it two
+// boxes earlier has read it).  Boxes at or past column N (the last tile of
+// an N that 224 does not divide) are not stored.
+template <typename Release>
+__device__ __forceinline__ void epilogue_tile_tma224(const CUtensorMap* tmD, uint32_t buf, uint32_t tacc,
+                                                     int64_t row0, int nt, int half, int lane, int N,
+                                                     uint32_t& nbox, Release release) {
+    static_assert(kEpiBoxCols == 32, "224-wide tiles are stored as 32-column boxes");
+    const int c0 = 4 * half;
+    const int nch = half == 0 ? 4 : 3;
+    uint32_t ra[32], rb[32], pk[64];
+    tmem_ld32_issue(tacc + 32 * c0, ra);
+    tmem_ld32_issue(tacc + 32 * (c0 + 1), rb);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        pk[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+        pk[16 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+    }
+    if (nch == 4) {
+        tmem_ld32_issue(tacc + 32 * (c0 + 2), ra);
+        tmem_ld32_issue(tacc + 32 * (c0 + 3), rb);
+        tmem_wait_ld();
+        release();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            pk[32 + i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+            pk[48 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+        }
+    } else {
+        tmem_ld32_issue(tacc + 32 * (c0 + 2), ra);
+        tmem_wait_ld();
+        release();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[32 + i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+    }
+    constexpr int CH = kEpiBoxCols / 8;                 // 16-byte chunks per box row
+    const uint32_t rowaddr = buf + (uint32_t)lane * (uint32_t)(kEpiBoxCols * 2);
+    const uint32_t sw = (uint32_t)((lane >> 1) & 3);    // 64-byte swizzle
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int col = nt * 224 + 32 * (c0 + j);
+        if (j >= nch || col >= N) break;                // warp-uniform
+        if (lane == 0) bulk_wait_group_read1();
+        __syncwarp();
+        const uint32_t bj = (nbox++ & 1u) * (uint32_t)kEpiBoxBytes;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int w = 16 * j + 4 * c;
+            st_shared_v4(rowaddr + bj + (((uint32_t)c ^ sw) << 4), pk[w], pk[w + 1], pk[w + 2], pk[w + 3]);
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmD, buf + bj, col, (int)row0);
+            bulk_commit_group();
+        }
+    }
+}
+
 // SwiGLU-backward epilogue, software-pipelined: the bf16 gate/up values of
 // a 32-column chunk (a_pre, global memory) are loaded one chunk ahead, the
 // first chunk before the accumulator is ready (swiglu_bwd_prefetch), so the
@@ -694,6 +765,19 @@ __device__ __forceinline__ void epilogue_zero(const Params& p, int64_t row, int 
 #pragma unroll
     for (int i = 0; i < 32; ++i) z[i] = 0.f;
     for (int c = 0; c < BN / 64; ++c) store_row32(p.d + row * p.N + (int64_t)nt * BN + half * (BN / 2) + 32 * c, z);
+}
+
+// Zero fill of an empty group's 224-wide weight-gradient tile (the chunks of
+// column half `half`, as in epilogue_tile_tma224, below column N).
+__device__ __forceinline__ void epilogue_zero224(const Params& p, int64_t row, int nt, int half) {
+    float z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+    const int c0 = 4 * half, nch = half == 0 ? 4 : 3;
+    for (int j = 0; j < nch; ++j) {
+        const int col = nt * 224 + 32 * (c0 + j);
+        if (col < p.N) store_row32(p.d + row * p.N + col, z);
+    }
 }
 
 }  // namespace gg

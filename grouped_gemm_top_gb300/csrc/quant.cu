@@ -285,6 +285,27 @@ __device__ __forceinline__ void st_global_32B(void* dst, const uint32_t* q) {
                  : "memory");
 }
 __device__ __forceinline__ float bf16_bits_lo(uint32_t w) { return __uint_as_float(w << 16); }
+
+// The scales of a 128-column tile of the transposed (columnwise) output,
+// staged as one atom (column cl, blocks 0..3 at (cl % 32) * 16 +
+// ((cl / 32) % 4) * 4), written in the tile-224 layout instead (moe.h):
+// column c0 + cl is row c = c0 + cl of the [R, C] transposed matrix, in
+// 224-row tile c / 224; its four block scales stay one 4-byte word.  One
+// warp, four columns per lane.
+__device__ __forceinline__ void store_col_scales_t224(uint8_t* sf_c, const uint8_t* s_atom, int64_t kb, int64_t c0,
+                                                      int R, int lane) {
+    const int64_t T = (R + 223) / 224;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int cl = lane + 32 * q;
+        const int64_t c = c0 + cl;
+        const int64_t t = c / 224;
+        const int rp = (int)(c - 224 * t);
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(s_atom + (cl & 31) * 16 + ((cl >> 5) & 3) * 4);
+        *reinterpret_cast<uint32_t*>(sf_c + (kb * T + t) * 1024 + (rp >> 7) * 512 + (rp & 31) * 16 +
+                                     ((rp >> 5) & 3) * 4) = w;
+    }
+}
 __device__ __forceinline__ float bf16_bits_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __restrict__ src, int64_t src_rows,
@@ -294,7 +315,8 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
                                                               int64_t rows, uint2* __restrict__ codes_r,
                                                               uint8_t* __restrict__ sf_r,
                                                               uint8_t* __restrict__ codes_c,
-                                                              uint8_t* __restrict__ sf_c, int32_t* err) {
+                                                              uint8_t* __restrict__ sf_c, int sf_c_t224,
+                                                              int32_t* err) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* s_in = reinterpret_cast<uint16_t*>(smem);                       // [2][128][128]
     uint8_t* s_atom_r = smem + 2 * kQBInBytes;                                // [2][512]
@@ -482,8 +504,12 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
             }
         } else if (warp == 1) {
             if (codes_c != nullptr) {
-                const int64_t atom = (r0 / kQT) * (int64_t)ntiles + ct;
-                reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_c)[lane];
+                if (sf_c_t224)
+                    store_col_scales_t224(sf_c, s_atom_c, r0 / kQT, (int64_t)ct * kQT, cols, lane);
+                else {
+                    const int64_t atom = (r0 / kQT) * (int64_t)ntiles + ct;
+                    reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_c)[lane];
+                }
             }
         }
         __syncthreads();                      // D: tile i's buffer (transposed codes) and the atoms are free
@@ -553,7 +579,8 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
                                                                     uint2* __restrict__ codes_r,
                                                                     uint8_t* __restrict__ sf_r,
                                                                     uint8_t* __restrict__ codes_c,
-                                                                    uint8_t* __restrict__ sf_c, int32_t* err) {
+                                                                    uint8_t* __restrict__ sf_c, int sf_c_t224,
+                                                                    int32_t* err) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* tiles = reinterpret_cast<uint16_t*>(smem);           // [2][128][128]: dgate, dup
     uint8_t* s_atom_r = smem + 2 * kQBInBytes;                     // [2][512]
@@ -690,8 +717,13 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
             reinterpret_cast<uint4*>(sf_r + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_r + t * 512)[lane];
         } else if (warp < 4) {
             const int t = warp - 2;
-            const int64_t atom = (r0 / kQT) * (int64_t)out_tiles + octile(t);
-            reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_c + t * 512)[lane];
+            if (sf_c_t224) {
+                store_col_scales_t224(sf_c, s_atom_c + t * 512, r0 / kQT, (int64_t)octile(t) * kQT, (int)F2, lane);
+            } else {
+                const int64_t atom = (r0 / kQT) * (int64_t)out_tiles + octile(t);
+                reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] =
+                    reinterpret_cast<const uint4*>(s_atom_c + t * 512)[lane];
+            }
         }
         __syncthreads();                      // D: tiles and atoms are free
     }
@@ -705,11 +737,13 @@ cudaError_t quant_set_attributes() {
 
 }  // namespace moe
 
-extern "C" moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, int cols, int k,
-                                              const int32_t* row_id, const float* row_w, const int32_t* gofs, int G,
-                                              int64_t rows, uint8_t* codes_row, uint8_t* scales_row,
-                                              uint8_t* codes_col, uint8_t* scales_col, int32_t* err, void* stream) {
+extern "C" moe_status_t mxfp8_gather_quantize_ex(const void* src, int64_t src_rows, int cols, int k,
+                                                 const int32_t* row_id, const float* row_w, const int32_t* gofs,
+                                                 int G, int64_t rows, uint8_t* codes_row, uint8_t* scales_row,
+                                                 uint8_t* codes_col, uint8_t* scales_col, int col_sf_layout,
+                                                 int32_t* err, void* stream) {
     using namespace moe;
+    MOE_REQUIRE(col_sf_layout == MOE_SF_ATOMS || col_sf_layout == MOE_SF_TILE224, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(src && gofs && G >= 1 && G <= 4096 && cols > 0 && rows > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(row_id != nullptr || row_w == nullptr, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(row_id == nullptr || (k >= 1 && src_rows >= 0 && src_rows <= 0x7FFFFFFF), MOE_ERR_INVALID_ARG);
@@ -729,16 +763,27 @@ extern "C" moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows,
     dim3 grid((unsigned)row_runs, (unsigned)(cols / kQT));
     k_quant_both<<<grid, kQBThreads, kQBSmem, (cudaStream_t)stream>>>((const uint16_t*)src, src_rows, cols, k, row_id,
                                                                      row_w, gofs, G, rows, (uint2*)codes_row,
-                                                                     scales_row, codes_col, scales_col, err);
+                                                                     scales_row, codes_col, scales_col,
+                                                                     col_sf_layout == MOE_SF_TILE224 ? 1 : 0, err);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }
 
-extern "C" moe_status_t mxfp8_swiglu_bwd_quantize(const float* dH, const void* a_pre, int f, const int32_t* gofs,
-                                                  int G, int64_t rows, void* dA, uint8_t* codes_row,
-                                                  uint8_t* scales_row, uint8_t* codes_col, uint8_t* scales_col,
-                                                  int32_t* err, void* stream) {
+extern "C" moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, int cols, int k,
+                                              const int32_t* row_id, const float* row_w, const int32_t* gofs, int G,
+                                              int64_t rows, uint8_t* codes_row, uint8_t* scales_row,
+                                              uint8_t* codes_col, uint8_t* scales_col, int32_t* err, void* stream) {
+    return mxfp8_gather_quantize_ex(src, src_rows, cols, k, row_id, row_w, gofs, G, rows, codes_row, scales_row,
+                                    codes_col, scales_col, MOE_SF_ATOMS, err, stream);
+}
+
+extern "C" moe_status_t mxfp8_swiglu_bwd_quantize_ex(const float* dH, const void* a_pre, int f,
+                                                     const int32_t* gofs, int G, int64_t rows, void* dA,
+                                                     uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
+                                                     uint8_t* scales_col, int col_sf_layout, int32_t* err,
+                                                     void* stream) {
     using namespace moe;
+    MOE_REQUIRE(col_sf_layout == MOE_SF_ATOMS || col_sf_layout == MOE_SF_TILE224, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(dH && a_pre && gofs && codes_row && scales_row && codes_col && scales_col, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(G >= 1 && G <= 4096 && f > 0 && rows > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(f % kQT == 0 && rows % kQT == 0 && rows <= 0x7FFFFFFF && f / kQT <= 65535, MOE_ERR_UNSUPPORTED);
@@ -750,7 +795,15 @@ extern "C" moe_status_t mxfp8_swiglu_bwd_quantize(const float* dH, const void* a
     dim3 grid((unsigned)row_runs, (unsigned)(f / kQT));
     k_swiglu_bwd_quant<<<grid, kQBThreads, kSBSmem, (cudaStream_t)stream>>>(
         dH, (const uint16_t*)a_pre, f, gofs, G, rows, (uint16_t*)dA, (uint2*)codes_row, scales_row, codes_col,
-        scales_col, err);
+        scales_col, col_sf_layout == MOE_SF_TILE224 ? 1 : 0, err);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
+}
+
+extern "C" moe_status_t mxfp8_swiglu_bwd_quantize(const float* dH, const void* a_pre, int f, const int32_t* gofs,
+                                                  int G, int64_t rows, void* dA, uint8_t* codes_row,
+                                                  uint8_t* scales_row, uint8_t* codes_col, uint8_t* scales_col,
+                                                  int32_t* err, void* stream) {
+    return mxfp8_swiglu_bwd_quantize_ex(dH, a_pre, f, gofs, G, rows, dA, codes_row, scales_row, codes_col,
+                                        scales_col, MOE_SF_ATOMS, err, stream);
 }

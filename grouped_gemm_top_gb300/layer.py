@@ -78,13 +78,24 @@ class MoELayer:
         # backward activations
         self.dw_all = z((T, kk), torch.float32) if self.S else None
         self.dw = z((T, k), torch.float32)
+        # the weight gradients' right operands (dy_perm^T, dA^T) carry their
+        # scales in the tile-224 layout when both weight-gradient GEMMs can run
+        # 256 x 224 pair tiles (their M = f and d multiples of 256): two TMEM
+        # accumulators hide each short tile's drain
+        self.wgrad_t224 = d % 256 == 0 and f % 256 == 0
+        self.col_sf = ops.MOE_SF_TILE224 if self.wgrad_t224 else ops.MOE_SF_ATOMS
+        self.wgrad_b = ops.MOE_B_SF_TILE224 if self.wgrad_t224 else ops.MOE_B_GNK
+
+        def sfc(C):              # bytes of the columnwise scales of a [M, C] matrix
+            return ops.sf_bytes_tile224(C, M) if self.wgrad_t224 else ops.sf_bytes(M, C)
+
         self.dyq, self.dys = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
-        self.dyqT, self.dysT = z((d, M), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
+        self.dyqT, self.dysT = z((d, M), torch.uint8), z((sfc(d),), torch.uint8)
         self.hqT, self.hsT = z((f, M), torch.uint8), z((ops.sf_bytes(M, f),), torch.uint8)
         self.dH = z((M, f), torch.float32)
         self.dA = z((M, 2 * f), torch.bfloat16) if store_intermediates else None
         self.dAq, self.dAs = z((M, 2 * f), torch.uint8), z((ops.sf_bytes(M, 2 * f),), torch.uint8)
-        self.dAqT, self.dAsT = z((2 * f, M), torch.uint8), z((ops.sf_bytes(M, 2 * f),), torch.uint8)
+        self.dAqT, self.dAsT = z((2 * f, M), torch.uint8), z((sfc(2 * f),), torch.uint8)
         self.xqT, self.xsT = z((d, M), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.dx_perm = z((M, d), torch.bfloat16)
         self.dx = z((T, d), torch.bfloat16)
@@ -214,22 +225,22 @@ class MoELayer:
         if self.S:       # the shared choices' weights are constants
             ops.moe_route_drop_shared(self.dw_all, self.k, self.dw)
         self._mem("quant_dy", ops.mxfp8_gather_quantize, self.dout, self.gofs, E, M, self.row_id, k, self.topk_w,
-                  True, True, self.dyq, self.dys, self.dyqT, self.dysT, err)
+                  True, True, self.dyq, self.dys, self.dyqT, self.dysT, err, col_sf_layout=self.col_sf)
         # dH = dY W2^T (fp32)
         self._gemm(ops.MOE_GEMM_DGRAD, self.dyq, self.dys, self.W2d, self.W2d_s, ops.MOE_B_GNK,
                    self.gofs, E, M, f, d, ops.MOE_EPI_NONE_F32, None, self.dH, None, err)
         # dW2_g = H_g^T dY_g
-        self._gemm(ops.MOE_GEMM_WGRAD, self.hqT, self.hsT, self.dyqT, self.dysT, 0, self.gofs, E, f,
+        self._gemm(ops.MOE_GEMM_WGRAD, self.hqT, self.hsT, self.dyqT, self.dysT, self.wgrad_b, self.gofs, E, f,
                    d, M, ops.MOE_EPI_NONE, None, self.dW2, None, err)
         # dA = [dgate | dup] = SwiGLU backward of (a_pre, dH), quantized on
         # both axes in the same pass
         self._mem("swiglu_bwd_quant_dA", ops.mxfp8_swiglu_bwd_quantize, self.dH, self.a_pre, self.gofs, E, self.dA,
-                  False, self.dAq, self.dAs, self.dAqT, self.dAsT, err)
+                  False, self.dAq, self.dAs, self.dAqT, self.dAsT, err, col_sf_layout=self.col_sf)
         # dX_perm = dA W1^T
         self._gemm(ops.MOE_GEMM_DGRAD, self.dAq, self.dAs, self.W1d, self.W1d_s, ops.MOE_B_GNK,
                    self.gofs, E, M, d, 2 * f, ops.MOE_EPI_NONE, None, self.dx_perm, None, err)
         # dW1_g = X_g^T dA_g
-        self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, 0, self.gofs, E, d,
+        self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, self.wgrad_b, self.gofs, E, d,
                    2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, err)
         ops.moe_route_bwd(self.logits, self.route_idx, self.dw, self.score, self.normalize, self.dlogits, err)
         if self.router:

@@ -33,7 +33,8 @@ MOE_QUANT_ROWWISE, MOE_QUANT_COLWISE_GROUPED, MOE_QUANT_COLWISE_GLU = 0, 1, 2
 MOE_QUANT_COLWISE_BATCHED, MOE_QUANT_COLWISE_BATCHED_GLU = 3, 4
 MOE_GEMM_FWD, MOE_GEMM_DGRAD, MOE_GEMM_WGRAD = 0, 1, 2
 MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD, MOE_EPI_NONE_F32 = 0, 1, 2, 3
-MOE_B_GNK, MOE_B_NGK = 0, 1
+MOE_B_GNK, MOE_B_NGK, MOE_B_SF_TILE224 = 0, 1, 2
+MOE_SF_ATOMS, MOE_SF_TILE224 = 0, 1
 MOE_GEMM_KERNEL_AUTO, MOE_GEMM_KERNEL_1SM, MOE_GEMM_KERNEL_1SM_N128 = 0, 1, 2
 MOE_GEMM_KERNEL_PAIR, MOE_GEMM_KERNEL_PAIR_N128 = 3, 4
 (MOE_OP_ROUTE_TOPK, MOE_OP_PERMUTE, MOE_OP_GROUP_QUANTIZE, MOE_OP_GATHER_QUANTIZE, MOE_OP_GROUPED_GEMM,
@@ -48,7 +49,8 @@ EXPORTS = [
     "gemm_bf16_nt", "moe_transpose_bf16", "moe_unpermute_combine_add", "moe_route_append_shared",
     "moe_route_drop_shared", "nvfp4_sf_bytes", "nvfp4_quantize", "grouped_gemm_nvfp4", "nvfp4_quantize_cols",
     "moe_selftest_bounded_wait", "moe_workspace_size", "mxfp8_scale_layout", "grouped_gemm_mxfp8_ex",
-    "grouped_gemm_mxfp8_swiglu_quant_ex", "grouped_gemm_nvfp4_ex", "moe_hbm_fill",
+    "grouped_gemm_mxfp8_swiglu_quant_ex", "grouped_gemm_nvfp4_ex", "moe_hbm_fill", "mxfp8_gather_quantize_ex",
+    "mxfp8_swiglu_bwd_quantize_ex",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -112,6 +114,10 @@ _SIGS = {
     "grouped_gemm_nvfp4_ex": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i64, _i32, _vp,
                                      _vp, _vp, _vp]),
     "moe_hbm_fill": (_i32, [_vp, _sz, ctypes.c_uint32, _i32, _vp]),
+    "mxfp8_gather_quantize_ex": (_i32, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32,
+                                        _vp, _vp]),
+    "mxfp8_swiglu_bwd_quantize_ex": (_i32, [_vp, _vp, _i32, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
+                                            _vp]),
 }
 
 
@@ -241,6 +247,13 @@ def sf_bytes(rows: int, cols: int) -> int:
     return rows * (cols // 32)
 
 
+def sf_bytes_tile224(rows: int, cols: int) -> int:
+    """Bytes of the tile-224 scale layout of a [rows, cols] matrix quantized
+    along cols (include/moe.h): (cols / 128) k-blocks of ceil(rows / 224)
+    tiles of 1024 bytes."""
+    return (cols // 128) * ((rows + 223) // 224) * 1024
+
+
 def mxfp8_group_quantize(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, codes=None, scales=None, err=None,
                          stream=None):
     rows, cols = x.shape
@@ -257,13 +270,15 @@ def mxfp8_group_quantize(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, codes=None, 
 
 
 def mxfp8_gather_quantize(src, gofs, G, rows, row_id=None, k=1, row_w=None, rowwise=True, colwise=True,
-                          codes_row=None, scales_row=None, codes_col=None, scales_col=None, err=None, stream=None):
+                          codes_row=None, scales_row=None, codes_col=None, scales_col=None, err=None, stream=None,
+                          col_sf_layout=MOE_SF_ATOMS):
     """Rowwise and/or group-aware columnwise MXFP8 codes of the permuted
     matrix whose row s is src[row_id[s] // k] (times row_w[row_id[s]]), or
     src[s] without row_id.  See include/moe.h (a given codes_row must be
-    32-byte aligned, as fresh torch allocations are).  Returns
-    (codes_row, scales_row, codes_col, scales_col), None for an axis not
-    asked for."""
+    32-byte aligned, as fresh torch allocations are).  col_sf_layout
+    MOE_SF_TILE224 writes the columnwise scales in the tile-224 layout
+    (mxfp8_gather_quantize_ex).  Returns (codes_row, scales_row, codes_col,
+    scales_col), None for an axis not asked for."""
     cols = src.shape[1]
     if rowwise:
         codes_row = codes_row if codes_row is not None else _empty((rows, cols), torch.uint8, src)
@@ -272,14 +287,18 @@ def mxfp8_gather_quantize(src, gofs, G, rows, row_id=None, k=1, row_w=None, roww
         codes_row = scales_row = None
     if colwise:
         codes_col = codes_col if codes_col is not None else _empty((cols, rows), torch.uint8, src)
-        scales_col = scales_col if scales_col is not None else _empty((sf_bytes(rows, cols),), torch.uint8, src)
+        nsc = sf_bytes_tile224(cols, rows) if col_sf_layout == MOE_SF_TILE224 else sf_bytes(rows, cols)
+        scales_col = scales_col if scales_col is not None else torch.zeros((nsc,), dtype=torch.uint8,
+                                                                           device=src.device)
     else:
         codes_col = scales_col = None
-    _check("mxfp8_gather_quantize", lib.mxfp8_gather_quantize(_p(src), src.shape[0], cols, int(k), _p(row_id),
-                                                              _p(row_w), _p(gofs),
-                                                              int(G), int(rows), _p(codes_row), _p(scales_row),
-                                                              _p(codes_col), _p(scales_col), _p(err),
-                                                              _stream(stream)))
+    args = (_p(src), src.shape[0], cols, int(k), _p(row_id), _p(row_w), _p(gofs), int(G), int(rows), _p(codes_row),
+            _p(scales_row), _p(codes_col), _p(scales_col))
+    if col_sf_layout == MOE_SF_ATOMS:
+        _check("mxfp8_gather_quantize", lib.mxfp8_gather_quantize(*args, _p(err), _stream(stream)))
+    else:
+        _check("mxfp8_gather_quantize_ex", lib.mxfp8_gather_quantize_ex(*args, int(col_sf_layout), _p(err),
+                                                                        _stream(stream)))
     return codes_row, scales_row, codes_col, scales_col
 
 
@@ -309,7 +328,7 @@ def grouped_gemm_mxfp8(mode, a, a_sf, b, b_sf, b_layout, gofs, G, M, N, K, epilo
 
 
 def mxfp8_swiglu_bwd_quantize(dH, a_pre, gofs, G, dA=None, want_dA=False, codes_row=None, scales_row=None,
-                              codes_col=None, scales_col=None, err=None, stream=None):
+                              codes_col=None, scales_col=None, err=None, stream=None, col_sf_layout=MOE_SF_ATOMS):
     """MXFP8 (both axes) of dA = SwiGLU-backward(a_pre, dH); dA itself in bf16
     only if want_dA or dA is given.  See include/moe.h.  Returns (dA or None,
     codes_row, scales_row, codes_col, scales_col)."""
@@ -319,11 +338,15 @@ def mxfp8_swiglu_bwd_quantize(dH, a_pre, gofs, G, dA=None, want_dA=False, codes_
     codes_row = codes_row if codes_row is not None else _empty((rows, 2 * f), torch.uint8, dH)
     scales_row = scales_row if scales_row is not None else _empty((sf_bytes(rows, 2 * f),), torch.uint8, dH)
     codes_col = codes_col if codes_col is not None else _empty((2 * f, rows), torch.uint8, dH)
-    scales_col = scales_col if scales_col is not None else _empty((sf_bytes(rows, 2 * f),), torch.uint8, dH)
-    _check("mxfp8_swiglu_bwd_quantize",
-           lib.mxfp8_swiglu_bwd_quantize(_p(dH), _p(a_pre), int(f), _p(gofs), int(G), int(rows), _p(dA),
-                                         _p(codes_row), _p(scales_row), _p(codes_col), _p(scales_col), _p(err),
-                                         _stream(stream)))
+    nsc = sf_bytes_tile224(2 * f, rows) if col_sf_layout == MOE_SF_TILE224 else sf_bytes(rows, 2 * f)
+    scales_col = scales_col if scales_col is not None else torch.zeros((nsc,), dtype=torch.uint8, device=dH.device)
+    args = (_p(dH), _p(a_pre), int(f), _p(gofs), int(G), int(rows), _p(dA), _p(codes_row), _p(scales_row),
+            _p(codes_col), _p(scales_col))
+    if col_sf_layout == MOE_SF_ATOMS:
+        _check("mxfp8_swiglu_bwd_quantize", lib.mxfp8_swiglu_bwd_quantize(*args, _p(err), _stream(stream)))
+    else:
+        _check("mxfp8_swiglu_bwd_quantize_ex",
+               lib.mxfp8_swiglu_bwd_quantize_ex(*args, int(col_sf_layout), _p(err), _stream(stream)))
     return dA, codes_row, scales_row, codes_col, scales_col
 
 

@@ -109,10 +109,32 @@ typedef enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU = 1, MOE_EPI_SWIGLU_BWD = 2, MOE
 typedef enum {
     MOE_B_GNK = 0,  /* codes [G][N][K]: rowwise-quantized (scales: atom layout of
                        the [G*N, K] matrix)                                    */
-    MOE_B_NGK = 1   /* codes [N][G*K]: the columnwise (transposed) output of a
+    MOE_B_NGK = 1,  /* codes [N][G*K]: the columnwise (transposed) output of a
                        [G*K, N] weight with group offsets g*K (scales: atom
                        layout of the [N, G*K] matrix)                          */
+    MOE_B_SF_TILE224 = 2  /* MOE_GEMM_WGRAD only: b's scales in the tile-224
+                       layout (below); selects 256 x 224 CTA-pair tiles with
+                       two TMEM accumulators per CTA                           */
 } moe_b_layout_t;
+
+/*
+ * Scale layouts of a quantized matrix Q [R, C] (blocks of 32 along C):
+ *   MOE_SF_ATOMS     the atom layout (above).
+ *   MOE_SF_TILE224   rows in tiles of 224: for k-block kb (128 columns, 4
+ *                    blocks) and row tile t (rows [224 t, 224 t + 224)),
+ *                    1024 bytes at (kb * ceil(R / 224) + t) * 1024; inside, row
+ *                    r' = r - 224 t, block b at
+ *                        (r' / 128) * 512 + (r' % 32) * 16 + ((r' / 32) % 4) * 4
+ *                          + (b % 4),
+ *                    i.e. the atom layout of each tile on its own, two atoms
+ *                    per tile (rows 224..255 of the second atom unused).
+ *                    Size (C / 128) * ceil(R / 224) * 1024 bytes.  This is the
+ *                    layout the 224-wide weight-gradient tiles read for their
+ *                    right operand (MOE_B_SF_TILE224): a 224-row tile starts on
+ *                    an atom of its own, which 224-row tiles of the plain atom
+ *                    layout do not.
+ */
+typedef enum { MOE_SF_ATOMS = 0, MOE_SF_TILE224 = 1 } moe_sf_layout_t;
 
 /*
  * Grouped-GEMM kernel selection, per call (the *_ex entry points; the plain
@@ -336,6 +358,18 @@ MOE_API moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, in
                                    uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col,
                                    uint8_t* scales_col, int32_t* err, void* stream);
 
+/* mxfp8_gather_quantize with the layout of scales_col chosen (moe_sf_layout_t):
+ * MOE_SF_TILE224 writes the columnwise scales in the tile-224 layout of the
+ * [cols, rows] transposed matrix ((rows / 128) * ceil(cols / 224) * 1024
+ * bytes; bytes of rows >= cols in the last tile are not written), the
+ * right-operand scales of grouped_gemm_mxfp8 WGRAD with MOE_B_SF_TILE224.
+ * The codes and the rowwise output are unchanged. */
+MOE_API moe_status_t mxfp8_gather_quantize_ex(const void* src, int64_t src_rows, int cols, int k,
+                                              const int32_t* row_id, const float* row_w, const int32_t* gofs, int G,
+                                              int64_t rows, uint8_t* codes_row, uint8_t* scales_row,
+                                              uint8_t* codes_col, uint8_t* scales_col, int col_sf_layout,
+                                              int32_t* err, void* stream);
+
 /*
  * mxfp8_swiglu_bwd_quantize -- the SwiGLU backward fused with the two-axis
  * MXFP8 quantization of its result ([TE-JAX] "What specialized
@@ -355,6 +389,13 @@ MOE_API moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, in
 MOE_API moe_status_t mxfp8_swiglu_bwd_quantize(const float* dH, const void* a_pre, int f, const int32_t* gofs,
                                        int G, int64_t rows, void* dA, uint8_t* codes_row, uint8_t* scales_row,
                                        uint8_t* codes_col, uint8_t* scales_col, int32_t* err, void* stream);
+
+/* mxfp8_swiglu_bwd_quantize with the layout of scales_col chosen, as for
+ * mxfp8_gather_quantize_ex (the transposed matrix is [2f, rows]). */
+MOE_API moe_status_t mxfp8_swiglu_bwd_quantize_ex(const float* dH, const void* a_pre, int f, const int32_t* gofs,
+                                                  int G, int64_t rows, void* dA, uint8_t* codes_row,
+                                                  uint8_t* scales_row, uint8_t* codes_col, uint8_t* scales_col,
+                                                  int col_sf_layout, int32_t* err, void* stream);
 
 /*
  * grouped_gemm_mxfp8 -- one launch for all experts' GEMMs, each over its own
@@ -391,7 +432,12 @@ MOE_API moe_status_t mxfp8_swiglu_bwd_quantize(const float* dH, const void* a_pr
  *   a, a_sf   [M, K] columnwise codes (the transposed left operand, e.g.
  *             h^T); K = row capacity; group g contracts over columns
  *             [gofs[g], gofs[g+1]).
- *   b, b_sf   [N, K] columnwise codes of the right operand (b_layout unused).
+ *   b, b_sf   [N, K] columnwise codes of the right operand.  b_layout
+ *             MOE_B_GNK or MOE_B_NGK: b_sf in the atom layout;
+ *             MOE_B_SF_TILE224: b_sf in the tile-224 layout of the [N, K]
+ *             matrix (M % 256 == 0 then; the call runs 256 x 224 CTA-pair
+ *             tiles whatever the options ask, or returns MOE_ERR_UNSUPPORTED
+ *             where no CTA pair fits).
  *   d         [G, M, N] bf16: d[g] = A_g * B_g^T over the group's rows;
  *             an empty group writes zeros.  M % 128 == 0, N % 128 == 0.
  * d, d2, epi_aux: 16-byte aligned.  Launch: one persistent CTA per SM.

@@ -46,6 +46,52 @@ def atoms_block_range(atoms, rows, cols, b_lo, b_hi):
     return atoms[off]
 
 
+def rowmajor_to_tile224(canon):
+    """Canonical scales [R, C/32] -> the tile-224 layout of include/moe.h
+    (for k-block kb and 224-row tile t, 1024 bytes at (kb * T + t) * 1024,
+    the atom layout of the tile's rows on their own; unused bytes zero)."""
+    canon = np.asarray(canon, dtype=np.uint8)
+    R, nb = canon.shape
+    T = (R + 223) // 224
+    out = np.zeros((nb // 4) * T * 1024, dtype=np.uint8)
+    r = np.arange(R)[:, None]
+    b = np.arange(nb)[None, :]
+    t, rp = r // 224, r % 224
+    off = ((b // 4) * T + t) * 1024 + (rp // 128) * 512 + (rp % 32) * 16 + ((rp // 32) % 4) * 4 + (b % 4)
+    out[off] = canon
+    return out
+
+
+def tile224_to_rowmajor(buf, R, C):
+    """Inverse of rowmajor_to_tile224 for a [R, C] matrix (C % 128 == 0)."""
+    buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
+    T = (R + 223) // 224
+    r = np.arange(R)[:, None]
+    b = np.arange(C // 32)[None, :]
+    t, rp = r // 224, r % 224
+    off = ((b // 4) * T + t) * 1024 + (rp // 128) * 512 + (rp % 32) * 16 + ((rp // 32) % 4) * 4 + (b % 4)
+    return buf[off]
+
+
+def tile224_block_range(buf, R, C, b_lo, b_hi, rows=None):
+    """Canonical scales [len(rows), b_hi - b_lo] (rows default: all R) of
+    blocks b_lo .. b_hi-1 of a [R, C] matrix whose scales are in the tile-224
+    layout."""
+    buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
+    T = (R + 223) // 224
+    r = (np.arange(R) if rows is None else np.asarray(rows))[:, None]
+    b = np.arange(b_lo, b_hi)[None, :]
+    t, rp = r // 224, r % 224
+    off = ((b // 4) * T + t) * 1024 + (rp // 128) * 512 + (rp % 32) * 16 + ((rp // 32) % 4) * 4 + (b % 4)
+    return buf[off]
+
+
+def colwise_scales_rowmajor(buf, C, M, tile224):
+    """Canonical [C, M/32] scales of a columnwise (transposed) output [C, M]
+    in the atom layout or, when tile224, the tile-224 layout."""
+    return tile224_to_rowmajor(buf, C, M) if tile224 else atoms_to_rowmajor(buf, C, M)
+
+
 def bf16_bits_of(t):
     """Bit patterns (numpy u16) of a bf16 torch tensor."""
     import torch

@@ -46,10 +46,15 @@ def sampled_checks(L, inp, score, norm, n_rows=256, n_groups=None, seed=0):
     assert np.array_equal(L.xq[rt].cpu().numpy(), rq)
     # per sampled row: the row's group weights, fetched group by group
 
-    def take_sf(atoms_t, rows_total, r_idx, b_lo, b_hi):
+    def take_sf(atoms_t, rows_total, r_idx, b_lo, b_hi, tile224=False):
         r = np.asarray(r_idx)[:, None]
         b = np.arange(b_lo, b_hi)[None, :]
-        off = ((b // 4) * (rows_total // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
+        if tile224:           # the tile-224 layout of the weight gradients' right operands
+            T, rp = (rows_total + 223) // 224, r % 224
+            off = ((b // 4) * T + r // 224) * 1024 + (rp // 128) * 512 + (rp % 32) * 16 + ((rp // 32) % 4) * 4 \
+                + (b % 4)
+        else:
+            off = ((b // 4) * (rows_total // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
         return atoms_t[torch.from_numpy(off.reshape(-1)).cuda()].cpu().numpy().reshape(off.shape)
 
     def b_fwd(q, s, g, K, N, glu):   # per-expert codes [E][N][K] -> logical [K, N] of group g
@@ -121,7 +126,7 @@ def sampled_checks(L, inp, score, norm, n_rows=256, n_groups=None, seed=0):
             aq = aT[torch.from_numpy(ms).cuda(), lo:hi].cpu().numpy()
             bq = bT[torch.from_numpy(ns).cuda(), lo:hi].cpu().numpy()
             asc = take_sf(asT, Mo, ms, lo // 32, hi // 32)
-            bsc = take_sf(bsT, No, ns, lo // 32, hi // 32)
+            bsc = take_sf(bsT, No, ns, lo // 32, hi // 32, L.wgrad_t224)
             Ah = O.mxfp8_dequantize_rows(aq, asc)      # [8, rows of g]
             Bh = O.mxfp8_dequantize_rows(bq, bsc)
             ref = Ah @ Bh.T

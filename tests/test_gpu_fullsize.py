@@ -23,7 +23,7 @@ import torch
 
 import oracle as O
 from helpers import (assert_bf16_close, atoms_block_range, atoms_rows_subset, atoms_to_rowmajor, bf16_bits_of,
-                     gpu_ops, to_np)
+                     colwise_scales_rowmajor, gpu_ops, tile224_block_range, to_np)
 from layer_checks import sampled_checks
 from parity_pool import OraclePool, bf16_bits
 from grouped_gemm_top_gb300 import synth
@@ -71,10 +71,12 @@ def _routing(L, inp, score):
 
 def _quantized(L):
     """name -> (rowwise codes, rowwise scale atoms, columnwise codes, columnwise
-    scale atoms, columns) of the step's four quantized activations."""
-    d, f = L.d, L.f
-    return {"x_perm": (L.xq, L.xs, L.xqT, L.xsT, d), "h": (L.hq, L.hs, L.hqT, L.hsT, f),
-            "dy_perm": (L.dyq, L.dys, L.dyqT, L.dysT, d), "dA": (L.dAq, L.dAs, L.dAqT, L.dAsT, 2 * f)}
+    scales, columns, columnwise scales in the tile-224 layout) of the step's
+    four quantized activations (dy_perm and dA, the weight gradients' right
+    operands, carry the layer's tile-224 scales)."""
+    d, f, t = L.d, L.f, L.wgrad_t224
+    return {"x_perm": (L.xq, L.xs, L.xqT, L.xsT, d, False), "h": (L.hq, L.hs, L.hqT, L.hsT, f, False),
+            "dy_perm": (L.dyq, L.dys, L.dyqT, L.dysT, d, t), "dA": (L.dAq, L.dAs, L.dAqT, L.dAsT, 2 * f, t)}
 
 
 def test_mixtral_every_code_and_scale_both_axes(ops, pool):
@@ -94,12 +96,12 @@ def test_mixtral_every_code_and_scale_both_axes(ops, pool):
         "dA": lambda: bf16_bits_of(L.dA[:Rp]),
     }
     bad = []
-    for name, (q, s, qT, sT, C) in _quantized(L).items():
+    for name, (q, s, qT, sT, C, t224) in _quantized(L).items():
         src = sources[name]()
         assert src.shape == (Rp, C)
         bad += pool.check_both_axes(name, src, gofs, q[:Rp].cpu().numpy(),
                                     atoms_to_rowmajor(s.cpu().numpy(), M, C)[:Rp], qT[:, :Rp].cpu().numpy(),
-                                    atoms_to_rowmajor(sT.cpu().numpy(), C, M)[:, :Rp // 32])
+                                    colwise_scales_rowmajor(sT.cpu().numpy(), C, M, t224)[:, :Rp // 32])
     assert not bad, bad[:8]
 
 
@@ -122,7 +124,7 @@ def test_deepseek_whole_groups_both_axes(ops, pool, zipf):
     xn, dn = to_np(inp["x"]), to_np(inp["dout"])
     wg = L.topk_w.cpu().numpy().astype(np.float64)
     quant = _quantized(L)
-    atoms = {name: (s.cpu().numpy(), sT.cpu().numpy()) for name, (_, s, _, sT, _) in quant.items()}
+    atoms = {name: (s.cpu().numpy(), sT.cpu().numpy()) for name, (_, s, _, sT, _, _) in quant.items()}
     bad = []
     for g in groups:
         lo, hi = int(gofs[g]), int(gofs[g + 1])
@@ -133,12 +135,13 @@ def test_deepseek_whole_groups_both_axes(ops, pool, zipf):
             "dy_perm": lambda: bf16_bits(O.permute_scaled_bf16(dn, rid, k, wg)),
             "dA": lambda: bf16_bits_of(L.dA[lo:hi]),
         }
-        for name, (q, _, qT, _, C) in quant.items():
+        for name, (q, _, qT, _, C, t224) in quant.items():
             s_at, sT_at = atoms[name]
+            col_sc = (tile224_block_range(sT_at, C, M, lo // 32, hi // 32) if t224
+                      else atoms_block_range(sT_at, C, M, lo // 32, hi // 32))
             bad += pool.check_both_axes(f"{name} group {g} ({counts[g]} rows)", sources[name](),
                                         np.array([0, hi - lo]), q[lo:hi].cpu().numpy(),
-                                        atoms_rows_subset(s_at, M, C, rows), qT[:, lo:hi].cpu().numpy(),
-                                        atoms_block_range(sT_at, C, M, lo // 32, hi // 32))
+                                        atoms_rows_subset(s_at, M, C, rows), qT[:, lo:hi].cpu().numpy(), col_sc)
     assert not bad, bad[:8]
 
 

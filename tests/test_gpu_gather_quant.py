@@ -244,3 +244,62 @@ def test_swiglu_bwd_quantize_rejects_bad_offsets(ops):
         assert int(err.item()) == ops.MOE_ERR_BAD_OFFSETS
         assert torch.all(cr == 0xAB)
 
+
+
+@pytest.mark.parametrize("d", [128, 384, 896, 7168])
+def test_gather_scaled_tile224_scales(ops, d):
+    """The columnwise scales in the tile-224 layout (the weight gradients'
+    right operand): the same bytes as the atom layout's, moved to the
+    224-row tiles (ragged last tile for d = 128, 384), bit-exact against
+    the oracle; codes unchanged; the bytes past the matrix's rows untouched."""
+    from helpers import tile224_to_rowmajor
+    T, E, k = 600, 8, 2
+    idx, w, slot_of, row_id, gofs = _routing(T, E, k, 5, 0.5)
+    Rp = int(gofs[-1])
+    rows = Rp + 128
+    x = _varied(T, d, 7)
+    rid = np.full(rows, -1, dtype=np.int32)
+    rid[:Rp] = row_id
+    gt, rt, wt = _dev(gofs, torch.int32), _dev(rid, torch.int32), _dev(w, torch.float32)
+    ref = ops.mxfp8_gather_quantize(x, gt, E, rows, rt, k, wt, True, True)
+    nsc = ops.sf_bytes_tile224(d, rows)
+    sc224 = torch.full((nsc,), 0xCD, dtype=torch.uint8, device="cuda")
+    res = ops.mxfp8_gather_quantize(x, gt, E, rows, rt, k, wt, True, True, scales_col=sc224,
+                                    col_sf_layout=ops.MOE_SF_TILE224)
+    torch.cuda.synchronize()
+    assert torch.equal(res[2][:, :Rp], ref[2][:, :Rp]) and torch.equal(res[0][:Rp], ref[0][:Rp])
+    got = tile224_to_rowmajor(sc224.cpu().numpy(), d, rows)[:, :Rp // 32]
+    assert np.array_equal(got, atoms_to_rowmajor(ref[3].cpu().numpy(), d, rows)[:, :Rp // 32])
+    P = O.permute_scaled_bf16(to_np(x), row_id, k, w.astype(np.float64))
+    _, cs, _ = O.mxfp8_quantize_cols_grouped(P, gofs)
+    assert np.array_equal(got, cs)
+    if d % 224:                  # rows of the last tile past d: never written
+        T224 = (d + 223) // 224
+        t = d // 224
+        rp = np.arange(d - 224 * t, 224)
+        off = (np.arange(Rp // 128)[:, None] * T224 + t) * 1024 + ((rp // 128) * 512 + (rp % 32) * 16 +
+                                                                   ((rp // 32) % 4) * 4)[None, :]
+        assert np.all(sc224.cpu().numpy()[off] == 0xCD)
+
+
+def test_swiglu_bwd_tile224_scales(ops):
+    """mxfp8_swiglu_bwd_quantize with the tile-224 columnwise scales: the
+    atom layout's bytes, moved (2f = 512: a ragged last tile)."""
+    from helpers import tile224_to_rowmajor
+    sizes, f = [300, 0, 129], 256
+    gofs = padded_layout(sizes)
+    Rp = int(gofs[-1])
+    rows = Rp + 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    dH = torch.randn((rows, f), generator=g, device="cuda")
+    a_pre = torch.randn((rows, 2 * f), generator=g, device="cuda").to(torch.bfloat16)
+    gt = _dev(gofs, torch.int32)
+    _, cr, sr, cc, sc = ops.mxfp8_swiglu_bwd_quantize(dH, a_pre, gt, len(sizes))
+    _, cr2, sr2, cc2, sc2 = ops.mxfp8_swiglu_bwd_quantize(dH, a_pre, gt, len(sizes),
+                                                          col_sf_layout=ops.MOE_SF_TILE224)
+    torch.cuda.synchronize()
+    assert sc2.numel() == ops.sf_bytes_tile224(2 * f, rows)
+    assert torch.equal(cc2[:, :Rp], cc[:, :Rp]) and torch.equal(cr2[:Rp], cr[:Rp])
+    assert np.array_equal(tile224_to_rowmajor(sc2.cpu().numpy(), 2 * f, rows)[:, :Rp // 32],
+                          atoms_to_rowmajor(sc.cpu().numpy(), 2 * f, rows)[:, :Rp // 32])

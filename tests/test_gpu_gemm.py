@@ -291,6 +291,44 @@ def test_wgrad(ops, sizes, Mo, No):
         assert torch.equal(d2, d)
 
 
+@pytest.mark.parametrize("sizes,Mo,No", [([128, 0, 384], 256, 256), ([5, 130, 0, 64], 256, 512),
+                                         ([900, 31], 512, 896), ([300], 256, 384), ([0, 0], 256, 4096)])
+def test_wgrad_tile224(ops, sizes, Mo, No):
+    """The weight gradient with b's scales in the tile-224 layout: 256 x 224
+    CTA-pair tiles with two accumulators, whatever kernel the options ask
+    for.  No = 384 and 4096 end in a partial 224-column tile (its columns
+    past No are neither computed into d nor written); empty groups give
+    zeros.  The scale bytes are the GPU quantizer's, moved to the tile-224
+    layout on the host."""
+    from helpers import rowmajor_to_tile224
+    G = len(sizes)
+    a, gofs_t, gofs = _act(sizes, Mo, seed=81)
+    g_, _, _ = _act(sizes, No, seed=82, row_cap=a.shape[0])
+    Kc = a.shape[0]
+    aq, as_ = ops.mxfp8_group_quantize(a, ops.MOE_QUANT_COLWISE_GROUPED, gofs_t, G)
+    gq, gs = ops.mxfp8_group_quantize(g_, ops.MOE_QUANT_COLWISE_GROUPED, gofs_t, G)
+    torch.cuda.synchronize()
+    G_can = atoms_to_rowmajor(gs.cpu().numpy(), No, Kc)
+    gs224 = torch.from_numpy(rowmajor_to_tile224(G_can)).cuda()
+    Rp = int(gofs[-1])
+    d = torch.full((G, Mo, No), 3.0, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, aq, as_, gq, gs224, ops.MOE_B_SF_TILE224, gofs_t, G, Mo, No, Kc, d=d,
+                           err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    if Rp:
+        Ah = O.mxfp8_dequantize_cols(aq.cpu().numpy()[:, :Rp],
+                                     atoms_to_rowmajor(as_.cpu().numpy(), Mo, Kc)[:, :Rp // 32])
+        Gh = O.mxfp8_dequantize_cols(gq.cpu().numpy()[:, :Rp], G_can[:, :Rp // 32])
+        ref = O.grouped_gemm_wgrad(Ah, Gh, gofs)
+    for g in range(G):
+        if sizes[g] == 0:
+            assert torch.all(d[g] == 0)
+        else:
+            assert_bf16_close(d[g], ref[g], what=f"wgrad tile-224 g={g}")
+
+
 def test_bad_offsets_reported_not_faulting(ops):
     sizes, K, N = [128, 128], 128, 256
     x, gofs_t, gofs = _act(sizes, K, seed=61)

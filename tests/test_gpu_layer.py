@@ -6,7 +6,7 @@ import torch
 
 import oracle as O
 from helpers import (assert_bf16_close, assert_fp32_close, atoms_to_rowmajor, batched_weight_operand,
-                     glu_perm, gpu_ops, to_np)
+                     colwise_scales_rowmajor, glu_perm, gpu_ops, to_np)
 from layer_checks import sampled_checks
 from grouped_gemm_top_gb300 import synth
 
@@ -56,8 +56,9 @@ def _deq_act(q, s, M, C):
     return O.mxfp8_dequantize_rows(q.cpu().numpy(), atoms_to_rowmajor(s.cpu().numpy(), M, C))
 
 
-def _deq_actT(q, s, C, M, Rp):
-    return O.mxfp8_dequantize_cols(q.cpu().numpy()[:, :Rp], atoms_to_rowmajor(s.cpu().numpy(), C, M)[:, :Rp // 32])
+def _deq_actT(q, s, C, M, Rp, tile224=False):
+    sc = colwise_scales_rowmajor(s.cpu().numpy(), C, M, tile224)
+    return O.mxfp8_dequantize_cols(q.cpu().numpy()[:, :Rp], sc[:, :Rp // 32])
 
 
 @pytest.mark.parametrize("score,norm,S,T,E0,k0", [("softmax", True, 0, 256, 8, 2), ("sigmoid", True, 0, 256, 8, 2),
@@ -122,14 +123,14 @@ def test_tiny_layer_stagewise(ops, score, norm, S, T, E0, k0):
     assert np.array_equal(L.dyq.cpu().numpy()[:Rp], dq)
     dcq, dcs, _ = O.mxfp8_quantize_cols_grouped(dyg, gofs)
     assert np.array_equal(L.dyqT.cpu().numpy()[:, :Rp], dcq)
-    assert np.array_equal(atoms_to_rowmajor(L.dysT.cpu().numpy(), d, M)[:, :Rp // 32], dcs)
+    assert np.array_equal(colwise_scales_rowmajor(L.dysT.cpu().numpy(), d, M, L.wgrad_t224)[:, :Rp // 32], dcs)
     dH = O.grouped_gemm(O.mxfp8_dequantize_rows(dq, ds), _w_dgrad(L, 2), gofs)
     assert_fp32_close(L.dH[:Rp], dH[:Rp], what="dH")
     dA = O.swiglu_bwd(to_np(L.a_pre)[:Rp], dH)
     assert_bf16_close(L.dA[:Rp], dA, what="dA")
     # wgrad dW2 = h^T dy per group (columnwise operands)
     Hh = _deq_actT(L.hqT, L.hsT, f, M, Rp)
-    DYh = _deq_actT(L.dyqT, L.dysT, d, M, Rp)
+    DYh = _deq_actT(L.dyqT, L.dysT, d, M, Rp, L.wgrad_t224)
     rq2, rs2, _ = O.mxfp8_quantize_cols_grouped(to_np(L.h)[:Rp], gofs)
     assert np.array_equal(L.hqT.cpu().numpy()[:, :Rp], rq2)
     dW2 = O.grouped_gemm_wgrad(Hh, DYh, gofs)
@@ -137,12 +138,13 @@ def test_tiny_layer_stagewise(ops, score, norm, S, T, E0, k0):
         assert_bf16_close(L.dW2[g], dW2[g], what=f"dW2[{g}]")
     daq, das = O.mxfp8_quantize_rows(to_np(L.dA)[:Rp])
     assert np.array_equal(L.dAq.cpu().numpy()[:Rp], daq)
-    dacq, _, _ = O.mxfp8_quantize_cols_grouped(to_np(L.dA)[:Rp], gofs)
+    dacq, dacs, _ = O.mxfp8_quantize_cols_grouped(to_np(L.dA)[:Rp], gofs)
     assert np.array_equal(L.dAqT.cpu().numpy()[:, :Rp], dacq)
+    assert np.array_equal(colwise_scales_rowmajor(L.dAsT.cpu().numpy(), 2 * f, M, L.wgrad_t224)[:, :Rp // 32], dacs)
     dXp = O.grouped_gemm(O.mxfp8_dequantize_rows(daq, das), _w_dgrad(L, 1), gofs)
     assert_bf16_close(L.dx_perm[:Rp], dXp, what="dx_perm")
     Xh = _deq_actT(L.xqT, L.xsT, d, M, Rp)
-    DAh = _deq_actT(L.dAqT, L.dAsT, 2 * f, M, Rp)
+    DAh = _deq_actT(L.dAqT, L.dAsT, 2 * f, M, Rp, L.wgrad_t224)
     dW1 = O.grouped_gemm_wgrad(Xh, DAh, gofs)
     for g in range(E):
         assert_bf16_close(L.dW1[g], dW1[g], what=f"dW1[{g}]")
