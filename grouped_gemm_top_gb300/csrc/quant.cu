@@ -243,14 +243,15 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
 // checks the group offsets once (in parallel), looks up the source row and
 // weight of all its rows once, and streams its row tiles through a
 // two-stage cp.async pipeline (the copy of tile i+1 is in flight while tile
-// i is quantized; padding rows are zero-filled by the copy; the transposed
-// codes of tile i are staged in tile i's own buffer), three CTAs per SM.
-// Block maxima are taken on the packed bf16 bits (two values per
-// instruction); a column block is read twice from shared memory (maximum,
-// then codes) to keep registers low enough for three CTAs per SM.  Per
-// tile it writes the rowwise codes and scale atom of its 128 rows and the
-// columnwise (transposed) codes and atom of its 128 columns.  Consecutive
-// CTAs take consecutive row runs of the same column tile, so the CTAs
+// i is quantized; padding rows are zero-filled by the copy), three CTAs per
+// SM, three CTA barriers per tile.  Block maxima are taken on the packed
+// bf16 bits (two values per instruction); a column block is read twice from
+// shared memory (maximum, then codes) to keep registers low enough for three
+// CTAs per SM.  Per tile it writes the rowwise codes and scale atom of its
+// 128 rows and the columnwise (transposed) codes and atom of its 128
+// columns; each 32-row block of a column is one 32-byte sector of the
+// transposed output, stored from the registers of the lane that encoded it.
+// Consecutive CTAs take consecutive row runs of the same column tile, so the CTAs
 // resident at a time cover all rows of one or two column tiles: a gathered
 // source row, read by up to k row tiles, is re-read from L2 (one column tile
 // of x is 6 MB at T = 24576).
@@ -259,9 +260,7 @@ namespace moe {
 constexpr int kQBThreads = 256;
 constexpr int kQBRowTiles = 8;                      // row tiles per CTA (at most)
 constexpr int kQBInBytes = kQT * kQT * 2;           // one bf16 tile, unpadded
-constexpr int kQBQPitch = kQT + 16;                 // transposed-code rows (bytes)
 constexpr int kQBSmem = 2 * kQBInBytes + 2 * 512 + 512 + kQBRowTiles * kQT * (4 + 4);
-static_assert(kQT * kQBQPitch <= kQBInBytes, "transposed codes reuse the tile's buffer");
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t nbytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(g), "r"(nbytes) : "memory");
@@ -475,27 +474,15 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
             }
             s_atom_c[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b0;
             s_atom_c[((col + 1) & 31) * 16 + (((col + 1) >> 5) & 3) * 4 + blk] = (uint8_t)b1;
+            // the 32 codes of each column's block are one 32-byte sector of the
+            // transposed output: stored straight from registers
+            uint8_t* dst = codes_c + ((int64_t)ct * kQT + col) * rows + r0 + 32 * blk;
+            st_global_32B(dst, w0);
+            st_global_32B(dst + rows, w1);
         }
-        __syncthreads();                      // B: every thread is done reading tile i
-        uint8_t* s_q = reinterpret_cast<uint8_t*>(tile);   // [128][kQBQPitch] over tile i's buffer
-        if (codes_c != nullptr) {
-            uint4* d0 = reinterpret_cast<uint4*>(s_q + col * kQBQPitch + blk * 32);
-            uint4* d1 = reinterpret_cast<uint4*>(s_q + (col + 1) * kQBQPitch + blk * 32);
-            d0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-            d0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
-            d1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-            d1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
-        }
-        __syncthreads();                      // C: transposed codes and both atoms complete
-        if (codes_c != nullptr) {
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const int idx = tid + kQBThreads * p;
-                const int cl = idx >> 3, cv = idx & 7;
-                const uint4 q = *reinterpret_cast<const uint4*>(s_q + cl * kQBQPitch + cv * 16);
-                *reinterpret_cast<uint4*>(codes_c + ((int64_t)ct * kQT + cl) * rows + r0 + cv * 16) = q;
-            }
-        }
+        // B: every thread is done reading tile i (its buffer may be refilled)
+        // and both atoms are complete
+        __syncthreads();
         if (warp == 0) {
             if (codes_r != nullptr) {
                 const int64_t atom = (int64_t)ct * (rows / kQT) + r0 / kQT;
@@ -512,7 +499,8 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
                 }
             }
         }
-        __syncthreads();                      // D: tile i's buffer (transposed codes) and the atoms are free
+        // the atoms are rewritten no earlier than the next tile's barrier A
+        // (s_atom_c) or two tiles on (s_atom_r, double-buffered)
     }
 }
 
@@ -532,8 +520,9 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
 // kQBRowTiles row tiles.  Per row tile each thread loads its eight 8-element
 // chunks of dH, g and u, computes dgate and dup, quantizes them rowwise from
 // registers and stages them in two shared-memory tiles for the columnwise
-// blocks, done as in k_quant_both.
-constexpr int kSBSmem = 2 * kQBInBytes + 4 * 512;
+// blocks, done as in k_quant_both (the atoms double-buffered by tile
+// parity, two CTA barriers per tile).
+constexpr int kSBSmem = 2 * kQBInBytes + 8 * 512;
 
 __device__ __forceinline__ uint2 quant_row_chunk(uint4 v, uint32_t& sb_out) {
     uint32_t m = bf16x2_maxabs(bf16x2_maxabs(v.x, v.y), bf16x2_maxabs(v.z, v.w));
@@ -583,8 +572,10 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
                                                                     int32_t* err) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* tiles = reinterpret_cast<uint16_t*>(smem);           // [2][128][128]: dgate, dup
-    uint8_t* s_atom_r = smem + 2 * kQBInBytes;                     // [2][512]
-    uint8_t* s_atom_c = s_atom_r + 2 * 512;                        // [2][512]
+    // atoms of the dgate / dup tiles, double-buffered by tile parity so the
+    // next tile's passes may write while this tile's atoms are stored
+    uint8_t* const s_atom_r0 = smem + 2 * kQBInBytes;              // [2 parities][2 tiles][512]
+    uint8_t* const s_atom_c0 = s_atom_r0 + 4 * 512;                // [2 parities][2 tiles][512]
     const int tid = threadIdx.x;
     const int ct = blockIdx.y;                                     // column tile of dH / g / u
     const int64_t c0 = (int64_t)ct * kQT;
@@ -623,6 +614,8 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
     uint4 gw, uw;
     for (int i = 0; i < nrt; ++i) {
         const int64_t r0 = (rt0 + i) * kQT;
+        uint8_t* const s_atom_r = s_atom_r0 + (i & 1) * 1024;
+        uint8_t* const s_atom_c = s_atom_c0 + (i & 1) * 1024;
         // dgate / dup of this thread's chunks: rowwise codes from registers,
         // bf16 values into the two tiles; chunk p + 1's loads are in flight
         // while chunk p is computed
@@ -680,37 +673,19 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
         s_atom_c[a1] = (uint8_t)bg1;
         s_atom_c[512 + a0] = (uint8_t)bu0;
         s_atom_c[512 + a1] = (uint8_t)bu1;
-        __syncthreads();                      // B: every thread is done reading both tiles
         {
-            uint8_t* qg = reinterpret_cast<uint8_t*>(tiles);
-            uint8_t* qu = reinterpret_cast<uint8_t*>(tiles + kQT * kQT);
-            uint4* d;
-            d = reinterpret_cast<uint4*>(qg + col * kQBQPitch + blk * 32);
-            d[0] = make_uint4(wg0[0], wg0[1], wg0[2], wg0[3]);
-            d[1] = make_uint4(wg0[4], wg0[5], wg0[6], wg0[7]);
-            d = reinterpret_cast<uint4*>(qg + (col + 1) * kQBQPitch + blk * 32);
-            d[0] = make_uint4(wg1[0], wg1[1], wg1[2], wg1[3]);
-            d[1] = make_uint4(wg1[4], wg1[5], wg1[6], wg1[7]);
-            d = reinterpret_cast<uint4*>(qu + col * kQBQPitch + blk * 32);
-            d[0] = make_uint4(wu0[0], wu0[1], wu0[2], wu0[3]);
-            d[1] = make_uint4(wu0[4], wu0[5], wu0[6], wu0[7]);
-            d = reinterpret_cast<uint4*>(qu + (col + 1) * kQBQPitch + blk * 32);
-            d[0] = make_uint4(wu1[0], wu1[1], wu1[2], wu1[3]);
-            d[1] = make_uint4(wu1[4], wu1[5], wu1[6], wu1[7]);
+            // each column's 32 codes of this block: one 32-byte sector of the
+            // transposed output, stored straight from registers
+            uint8_t* dg = codes_c + ((int64_t)octile(0) * kQT + col) * rows + r0 + 32 * blk;
+            uint8_t* du = codes_c + ((int64_t)octile(1) * kQT + col) * rows + r0 + 32 * blk;
+            st_global_32B(dg, wg0);
+            st_global_32B(dg + rows, wg1);
+            st_global_32B(du, wu0);
+            st_global_32B(du + rows, wu1);
         }
-        __syncthreads();                      // C: transposed codes and atoms complete
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const uint8_t* s_q = reinterpret_cast<const uint8_t*>(tiles + t * kQT * kQT);
-            const int64_t oc = (int64_t)octile(t) * kQT;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const int idx = tid + kQBThreads * p;
-                const int cl = idx >> 3, cv = idx & 7;
-                const uint4 q = *reinterpret_cast<const uint4*>(s_q + cl * kQBQPitch + cv * 16);
-                *reinterpret_cast<uint4*>(codes_c + (oc + cl) * rows + r0 + cv * 16) = q;
-            }
-        }
+        // B: both tiles are read (the next tile may overwrite them) and this
+        // tile's atoms are complete
+        __syncthreads();
         if (warp < 2) {
             const int t = warp;
             const int64_t atom = (int64_t)octile(t) * (rows / kQT) + r0 / kQT;
@@ -725,7 +700,7 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
                     reinterpret_cast<const uint4*>(s_atom_c + t * 512)[lane];
             }
         }
-        __syncthreads();                      // D: tiles and atoms are free
+        // this tile's atoms are rewritten two tiles on (double-buffered)
     }
 }
 
@@ -754,6 +729,7 @@ extern "C" moe_status_t mxfp8_gather_quantize_ex(const void* src, int64_t src_ro
     MOE_REQUIRE(rows % kQT == 0 && cols % kQT == 0, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(cols / kQT <= 65535 && rows <= 0x7FFFFFFF, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(codes_row == nullptr || (reinterpret_cast<uintptr_t>(codes_row) & 31) == 0, MOE_ERR_ALIGNMENT);
+    MOE_REQUIRE(codes_col == nullptr || (reinterpret_cast<uintptr_t>(codes_col) & 31) == 0, MOE_ERR_ALIGNMENT);
     MOE_REQUIRE(moe_aligned16(src) && (codes_row == nullptr || (moe_aligned16(codes_row) && moe_aligned16(scales_row))) &&
                     (codes_col == nullptr || (moe_aligned16(codes_col) && moe_aligned16(scales_col))),
                 MOE_ERR_ALIGNMENT);
@@ -788,7 +764,8 @@ extern "C" moe_status_t mxfp8_swiglu_bwd_quantize_ex(const float* dH, const void
     MOE_REQUIRE(G >= 1 && G <= 4096 && f > 0 && rows > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(f % kQT == 0 && rows % kQT == 0 && rows <= 0x7FFFFFFF && f / kQT <= 65535, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(moe_aligned16(dH) && moe_aligned16(a_pre) && moe_aligned16(dA) && moe_aligned16(codes_row) &&
-                    moe_aligned16(scales_row) && moe_aligned16(codes_col) && moe_aligned16(scales_col),
+                    moe_aligned16(scales_row) && (reinterpret_cast<uintptr_t>(codes_col) & 31) == 0 &&
+                    moe_aligned16(scales_col),
                 MOE_ERR_ALIGNMENT);
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
     const int64_t row_runs = (rows / kQT + kQBRowTiles - 1) / kQBRowTiles;

@@ -349,8 +349,8 @@ MOE_API moe_status_t mxfp8_scale_layout(const uint8_t* src, int64_t rows, int co
  *             both NULL.
  *   codes_col, scales_col   exactly MOE_QUANT_COLWISE_GROUPED's output for
  *             P (codes [cols, rows]), or both NULL.  At least one pair.
- * All pointers are device pointers; outputs 16-byte aligned, codes_row
- * 32-byte aligned (MOE_ERR_ALIGNMENT otherwise).
+ * All pointers are device pointers; outputs 16-byte aligned, codes_row and
+ * codes_col 32-byte aligned (MOE_ERR_ALIGNMENT otherwise).
  */
 MOE_API moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, int cols, int k,
                                    const int32_t* row_id,
@@ -384,7 +384,8 @@ MOE_API moe_status_t mxfp8_gather_quantize_ex(const void* src, int64_t src_rows,
  *   dA        [rows, 2f] bf16 or NULL: the bf16 values, written only if given.
  *   gofs      as for mxfp8_gather_quantize; rows >= gofs[G] untouched.
  *   codes_row, scales_row, codes_col, scales_col   both axes, required.
- * f % 128 == 0, rows % 128 == 0, 16-byte aligned pointers.
+ * f % 128 == 0, rows % 128 == 0, 16-byte aligned pointers (codes_col
+ * 32-byte aligned).
  */
 MOE_API moe_status_t mxfp8_swiglu_bwd_quantize(const float* dH, const void* a_pre, int f, const int32_t* gofs,
                                        int G, int64_t rows, void* dA, uint8_t* codes_row, uint8_t* scales_row,
