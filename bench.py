@@ -612,7 +612,10 @@ def run_wgrad_point(G, M_total, Mo, No, seed=0, steps=10, warmup=3, device="cuda
     groups of M_total rows (X [rows, Mo], dY [rows, No] ~ N(0,1), rows laid
     out at 128-row group offsets), in MXFP8 (group-aware columnwise MXFP8
     operands) and in NVFP4 (group-aware columnwise NVFP4): one line with
-    both.  Peaks as for the fwd points (2x / 6x the measured bf16 burst)."""
+    both.  The MXFP8 figure is the layer's own form when M is a multiple of
+    256 (256 x 224 CTA-pair tiles, dY's scales in the tile-224 layout);
+    `mxfp8_tile256_ms` is the 256-wide single-accumulator form beside it.
+    Peaks as for the fwd points (2x / 6x the measured bf16 burst)."""
     import numpy as np
     import torch
 
@@ -636,6 +639,10 @@ def run_wgrad_point(G, M_total, Mo, No, seed=0, steps=10, warmup=3, device="cuda
     X, Y = grouped(Mo, seed + 300), grouped(No, seed + 400)
     _, _, xq8, xs8 = ops.mxfp8_gather_quantize(X, gofs_t, G, rows, None, 1, None, False, True, err=err)
     _, _, yq8, ys8 = ops.mxfp8_gather_quantize(Y, gofs_t, G, rows, None, 1, None, False, True, err=err)
+    t224 = Mo % 256 == 0
+    if t224:
+        _, _, yq8t, ys8t = ops.mxfp8_gather_quantize(Y, gofs_t, G, rows, None, 1, None, False, True, err=err,
+                                                     col_sf_layout=ops.MOE_SF_TILE224)
     xq4, xs4, xt4 = ops.nvfp4_quantize_cols(X, gofs_t, G, err=err)
     yq4, ys4, yt4 = ops.nvfp4_quantize_cols(Y, gofs_t, G, err=err)
     del X, Y
@@ -654,14 +661,20 @@ def run_wgrad_point(G, M_total, Mo, No, seed=0, steps=10, warmup=3, device="cuda
         assert int(err.item()) == 0, int(err.item())
         return a.elapsed_time(b) / steps
 
-    ms8 = timed(lambda: ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, xq8, xs8, yq8, ys8, 0, gofs_t, G, Mo, No, rows,
-                                               d=d, err=err))
+    ms256 = timed(lambda: ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, xq8, xs8, yq8, ys8, ops.MOE_B_GNK, gofs_t, G,
+                                                 Mo, No, rows, d=d, err=err))
+    ms8 = ms256
+    if t224:
+        ms8 = timed(lambda: ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, xq8, xs8, yq8t, ys8t, ops.MOE_B_SF_TILE224,
+                                                   gofs_t, G, Mo, No, rows, d=d, err=err))
     ms4 = timed(lambda: ops.grouped_gemm_nvfp4(ops.MOE_GEMM_WGRAD, xq4, xs4, xt4, yq4, ys4, yt4, gofs_t, G, Mo, No,
                                                rows, d=d, err=err))
     flops = 2.0 * M_total * Mo * No
     peaks, psrc = _peaks()
     return {"G": G, "M_total": M_total, "M": Mo, "N": No, "mxfp8_ms": round(ms8, 4),
-            "mxfp8_tflops": round(flops / (ms8 * 1e-3) / 1e12, 1), "nvfp4_ms": round(ms4, 4),
+            "mxfp8_tflops": round(flops / (ms8 * 1e-3) / 1e12, 1),
+            "mxfp8_tiles": "256x224 pair, two accumulators" if t224 else "256x256 pair",
+            "mxfp8_tile256_ms": round(ms256, 4), "nvfp4_ms": round(ms4, 4),
             "nvfp4_tflops": round(flops / (ms4 * 1e-3) / 1e12, 1),
             "nvfp4_frac_of_fp4_peak": round(flops / (ms4 * 1e-3) / 1e12 / (6.0 * peaks["bf16_tflops"]), 4),
             "mxfp8_frac_of_mxfp8_peak": round(flops / (ms8 * 1e-3) / 1e12 / (2.0 * peaks["bf16_tflops"]), 4),
@@ -980,7 +993,7 @@ def main():
                     help="time one dense MXFP8 GEMM with the library's block-scaled GEMM (torch._scaled_mm) and "
                          "with ours (one group) and print one line")
     ap.add_argument("--hbm-probe", action="store_true",
-                    help="measure write-only and copy HBM bandwidth (PyTorch fill/copy kernels) and print one line")
+                    help="measure write-only (moe_hbm_fill) and copy (torch copy_) HBM bandwidth and print one line")
     args = ap.parse_args()
     if args.hbm_probe:
         print(json.dumps({"hbm_probe": run_hbm_probe()}), flush=True)
@@ -997,8 +1010,10 @@ def main():
         return
     if args.wgrad_point:
         G, Mt, Mo, No = args.wgrad_point
-        print(json.dumps({"wgrad_point": run_wgrad_point(G, Mt, Mo, No, steps=args.steps,
-                                                         warmup=max(args.warmup, 3))}), flush=True)
+        with ClockSampler(0) as clk:
+            r = run_wgrad_point(G, Mt, Mo, No, steps=args.steps, warmup=max(args.warmup, 3))
+        r["clocks"] = clk.summary()
+        print(json.dumps({"wgrad_point": r}), flush=True)
         return
     if args.gemm_point or args.sweep:
         if args.gemm_point:
@@ -1007,11 +1022,13 @@ def main():
         else:
             pts = [(G, M, NK, NK) for G in (8, 64, 256) for NK in (2048, 7168) for M in (16384, 65536, 262144)]
         for i, (G, M, N, K) in enumerate(pts):
-            if args.nvfp4:
-                r = run_gemm_point_nvfp4(G, M, N, K, seed=i, steps=args.steps, warmup=max(args.warmup, 3))
-            else:
-                r = run_gemm_point(G, M, N, seed=i, steps=args.steps, warmup=max(args.warmup, 3), K=K,
-                                   b_layout=args.b_layout)
+            with ClockSampler(0) as clk:
+                if args.nvfp4:
+                    r = run_gemm_point_nvfp4(G, M, N, K, seed=i, steps=args.steps, warmup=max(args.warmup, 3))
+                else:
+                    r = run_gemm_point(G, M, N, seed=i, steps=args.steps, warmup=max(args.warmup, 3), K=K,
+                                       b_layout=args.b_layout)
+            r["clocks"] = clk.summary()
             print(json.dumps({"sweep_point": r}), flush=True)
             import torch
             torch.cuda.empty_cache()
