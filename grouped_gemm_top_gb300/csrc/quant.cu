@@ -244,7 +244,8 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
 // weight of all its rows once, and streams its row tiles through a
 // two-stage cp.async pipeline (the copy of tile i+1 is in flight while tile
 // i is quantized; padding rows are zero-filled by the copy), three CTAs per
-// SM, three CTA barriers per tile.  Block maxima are taken on the packed
+// SM, three CTA barriers per tile with router weights, two without.  Block
+// maxima are taken on the packed
 // bf16 bits (two values per instruction); a column block is read twice from
 // shared memory (maximum, then codes) to keep registers low enough for three
 // CTAs per SM.  Per tile it writes the rowwise codes and scale atom of its
@@ -306,6 +307,24 @@ __device__ __forceinline__ void store_col_scales_t224(uint8_t* sf_c, const uint8
     }
 }
 __device__ __forceinline__ float bf16_bits_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// Scaling by 2^-e, two bf16 values per instruction.  The product of a bf16
+// value and a power of two is exact whenever it is a normal bf16, and every
+// element of a block scales to at most 448 in magnitude; a product below the
+// smallest normal bf16 (2^-126) is far below half the smallest E4M3
+// subnormal (2^-10), so it encodes as a signed zero either way.  The codes
+// are therefore those of the fp32 product x * 2^-e.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// bf16x2 pair of 2^(127 - b) for the scale bytes of the low and high halves
+// (the bf16 bits of e8m0_inv_scale)
+__device__ __forceinline__ uint32_t inv_bf16x2(uint32_t b_lo, uint32_t b_hi) {
+    return ((254u - b_lo) << 7) | ((254u - b_hi) << 23);
+}
+// E4M3 codes of the two (already scaled) bf16 values of a word, low in byte 0
+__device__ __forceinline__ uint32_t e4m3x2_of(uint32_t w) { return cvt_e4m3x2(bf16_bits_lo(w), bf16_bits_hi(w)); }
 
 __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __restrict__ src, int64_t src_rows,
                                                               int cols, int k, const int32_t* __restrict__ row_id,
@@ -432,20 +451,21 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
                     m = bf16x2_maxabs(m, bf16x2_maxabs(bf16x2_maxabs(v[j].x, v[j].y), bf16x2_maxabs(v[j].z, v[j].w)));
                 m &= 0x7FFF7FFFu;
                 const uint32_t sb = e8m0_scale_byte(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16));
-                const float inv = e8m0_inv_scale(sb);
+                const uint32_t s2 = inv_bf16x2(sb, sb);
                 uint32_t q[8];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    q[2 * j] = cvt_e4m3x2(bf16_bits_lo(v[j].x) * inv, bf16_bits_hi(v[j].x) * inv) |
-                               (cvt_e4m3x2(bf16_bits_lo(v[j].y) * inv, bf16_bits_hi(v[j].y) * inv) << 16);
-                    q[2 * j + 1] = cvt_e4m3x2(bf16_bits_lo(v[j].z) * inv, bf16_bits_hi(v[j].z) * inv) |
-                                   (cvt_e4m3x2(bf16_bits_lo(v[j].w) * inv, bf16_bits_hi(v[j].w) * inv) << 16);
+                    q[2 * j] = e4m3x2_of(bf16x2_mul(v[j].x, s2)) | (e4m3x2_of(bf16x2_mul(v[j].y, s2)) << 16);
+                    q[2 * j + 1] = e4m3x2_of(bf16x2_mul(v[j].z, s2)) | (e4m3x2_of(bf16x2_mul(v[j].w, s2)) << 16);
                 }
                 st_global_32B(crow + qbu * 32, q);   // one whole 32-byte sector
                 s_atom_r[b * 512 + (qr & 31) * 16 + qsw * 4 + qbu] = (uint8_t)sb;
             }
         }
-        __syncthreads();                      // A: tile i (scaled) complete
+        // A: tile i, scaled in place by the router weights, is complete.
+        // Without weights the rowwise pass writes nothing the columnwise
+        // pass reads: the tile is complete since the barrier above.
+        if (row_w != nullptr) __syncthreads();
         uint32_t w0[8], w1[8];
         const int blk = warp & 3;                       // 32-row block
         const int col = (warp >> 2) * 64 + 2 * lane;    // two columns per lane
@@ -454,23 +474,31 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
             // in chunk (col / 8) ^ blk
             const uint32_t* colp = reinterpret_cast<const uint32_t*>(tile + blk * 32 * kQT +
                                                                      (((col >> 3) ^ blk) << 3) + (col & 7));
-            // pass 1: amax of both columns over the block, on packed bf16 bits
-            uint32_t m = 0;
-#pragma unroll 8
-            for (int e = 0; e < 32; ++e) m = bf16x2_maxabs(m, colp[e * (kQT / 2)]);
-            m &= 0x7FFF7FFFu;
+            // pass 1: amax of both columns over the block, on packed bf16 bits,
+            // in four independent chains
+            uint32_t ma = 0, mb = 0, mc = 0, md = 0;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                ma = bf16x2_maxabs(ma, colp[e * (kQT / 2)]);
+                mb = bf16x2_maxabs(mb, colp[(e + 1) * (kQT / 2)]);
+                mc = bf16x2_maxabs(mc, colp[(e + 2) * (kQT / 2)]);
+                md = bf16x2_maxabs(md, colp[(e + 3) * (kQT / 2)]);
+            }
+            const uint32_t m = bf16x2_maxabs(bf16x2_maxabs(ma, mb), bf16x2_maxabs(mc, md)) & 0x7FFF7FFFu;
             const uint32_t b0 = e8m0_scale_byte(__uint_as_float((m & 0xFFFFu) << 16));
             const uint32_t b1 = e8m0_scale_byte(__uint_as_float(m & 0xFFFF0000u));
-            const float i0 = e8m0_inv_scale(b0), i1 = e8m0_inv_scale(b1);
+            const uint32_t s2 = inv_bf16x2(b0, b1);
             // pass 2: codes, two rows per conversion
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const uint32_t v0 = colp[(4 * e) * (kQT / 2)], v1 = colp[(4 * e + 1) * (kQT / 2)];
-                const uint32_t v2 = colp[(4 * e + 2) * (kQT / 2)], v3 = colp[(4 * e + 3) * (kQT / 2)];
-                w0[e] = cvt_e4m3x2(bf16_bits_lo(v0) * i0, bf16_bits_lo(v1) * i0) |
-                        (cvt_e4m3x2(bf16_bits_lo(v2) * i0, bf16_bits_lo(v3) * i0) << 16);
-                w1[e] = cvt_e4m3x2(bf16_bits_hi(v0) * i1, bf16_bits_hi(v1) * i1) |
-                        (cvt_e4m3x2(bf16_bits_hi(v2) * i1, bf16_bits_hi(v3) * i1) << 16);
+                const uint32_t v0 = bf16x2_mul(colp[(4 * e) * (kQT / 2)], s2);
+                const uint32_t v1 = bf16x2_mul(colp[(4 * e + 1) * (kQT / 2)], s2);
+                const uint32_t v2 = bf16x2_mul(colp[(4 * e + 2) * (kQT / 2)], s2);
+                const uint32_t v3 = bf16x2_mul(colp[(4 * e + 3) * (kQT / 2)], s2);
+                w0[e] = cvt_e4m3x2(bf16_bits_lo(v0), bf16_bits_lo(v1)) |
+                        (cvt_e4m3x2(bf16_bits_lo(v2), bf16_bits_lo(v3)) << 16);
+                w1[e] = cvt_e4m3x2(bf16_bits_hi(v0), bf16_bits_hi(v1)) |
+                        (cvt_e4m3x2(bf16_bits_hi(v2), bf16_bits_hi(v3)) << 16);
             }
             s_atom_c[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b0;
             s_atom_c[((col + 1) & 31) * 16 + (((col + 1) >> 5) & 3) * 4 + blk] = (uint8_t)b1;
@@ -518,10 +546,12 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
 // A CTA owns one 128-column tile c0 of dH (hence output column tiles c0 of
 // dgate and f + c0 of dup, which need the same dH, g and u) and a run of
 // kQBRowTiles row tiles.  Per row tile each thread loads its eight 8-element
-// chunks of dH, g and u, computes dgate and dup, quantizes them rowwise from
-// registers and stages them in two shared-memory tiles for the columnwise
-// blocks, done as in k_quant_both (the atoms double-buffered by tile
-// parity, two CTA barriers per tile).
+// chunks of dH, g and u (two chunks ahead of the one it computes: the pass
+// streams from DRAM, and two CTAs per SM with 128 registers keep more bytes
+// in flight than three with one chunk ahead), computes dgate and dup,
+// quantizes them rowwise from registers and stages them in two
+// shared-memory tiles for the columnwise blocks, done as in k_quant_both
+// (the atoms double-buffered by tile parity, two CTA barriers per tile).
 constexpr int kSBSmem = 2 * kQBInBytes + 8 * 512;
 
 __device__ __forceinline__ uint2 quant_row_chunk(uint4 v, uint32_t& sb_out) {
@@ -529,11 +559,11 @@ __device__ __forceinline__ uint2 quant_row_chunk(uint4 v, uint32_t& sb_out) {
     m = bf16x2_maxabs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     m = bf16x2_maxabs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2)) & 0x7FFF7FFFu;
     const uint32_t sb = e8m0_scale_byte(__uint_as_float(max(m & 0xFFFFu, m >> 16) << 16));
-    const float inv = e8m0_inv_scale(sb);
-    const uint32_t q0 = cvt_e4m3x2(bf16_bits_lo(v.x) * inv, bf16_bits_hi(v.x) * inv);
-    const uint32_t q1 = cvt_e4m3x2(bf16_bits_lo(v.y) * inv, bf16_bits_hi(v.y) * inv);
-    const uint32_t q2 = cvt_e4m3x2(bf16_bits_lo(v.z) * inv, bf16_bits_hi(v.z) * inv);
-    const uint32_t q3 = cvt_e4m3x2(bf16_bits_lo(v.w) * inv, bf16_bits_hi(v.w) * inv);
+    const uint32_t s2 = inv_bf16x2(sb, sb);
+    const uint32_t q0 = e4m3x2_of(bf16x2_mul(v.x, s2));
+    const uint32_t q1 = e4m3x2_of(bf16x2_mul(v.y, s2));
+    const uint32_t q2 = e4m3x2_of(bf16x2_mul(v.z, s2));
+    const uint32_t q3 = e4m3x2_of(bf16x2_mul(v.w, s2));
     sb_out = sb;
     return make_uint2(q0 | (q1 << 16), q2 | (q3 << 16));
 }
@@ -549,19 +579,21 @@ __device__ __forceinline__ void quant_col_block(const uint16_t* tile, int blk, i
     m &= 0x7FFF7FFFu;
     b0 = e8m0_scale_byte(__uint_as_float((m & 0xFFFFu) << 16));
     b1 = e8m0_scale_byte(__uint_as_float(m & 0xFFFF0000u));
-    const float i0 = e8m0_inv_scale(b0), i1 = e8m0_inv_scale(b1);
+    const uint32_t s2 = inv_bf16x2(b0, b1);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        const uint32_t v0 = colp[(4 * e) * (kQT / 2)], v1 = colp[(4 * e + 1) * (kQT / 2)];
-        const uint32_t v2 = colp[(4 * e + 2) * (kQT / 2)], v3 = colp[(4 * e + 3) * (kQT / 2)];
-        w0[e] = cvt_e4m3x2(bf16_bits_lo(v0) * i0, bf16_bits_lo(v1) * i0) |
-                (cvt_e4m3x2(bf16_bits_lo(v2) * i0, bf16_bits_lo(v3) * i0) << 16);
-        w1[e] = cvt_e4m3x2(bf16_bits_hi(v0) * i1, bf16_bits_hi(v1) * i1) |
-                (cvt_e4m3x2(bf16_bits_hi(v2) * i1, bf16_bits_hi(v3) * i1) << 16);
+        const uint32_t v0 = bf16x2_mul(colp[(4 * e) * (kQT / 2)], s2);
+        const uint32_t v1 = bf16x2_mul(colp[(4 * e + 1) * (kQT / 2)], s2);
+        const uint32_t v2 = bf16x2_mul(colp[(4 * e + 2) * (kQT / 2)], s2);
+        const uint32_t v3 = bf16x2_mul(colp[(4 * e + 3) * (kQT / 2)], s2);
+        w0[e] = cvt_e4m3x2(bf16_bits_lo(v0), bf16_bits_lo(v1)) |
+                (cvt_e4m3x2(bf16_bits_lo(v2), bf16_bits_lo(v3)) << 16);
+        w1[e] = cvt_e4m3x2(bf16_bits_hi(v0), bf16_bits_hi(v1)) |
+                (cvt_e4m3x2(bf16_bits_hi(v2), bf16_bits_hi(v3)) << 16);
     }
 }
 
-__global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float* __restrict__ dH,
+__global__ void __launch_bounds__(kQBThreads, 2) k_swiglu_bwd_quant(const float* __restrict__ dH,
                                                                     const uint16_t* __restrict__ a_pre, int f,
                                                                     const int32_t* __restrict__ gofs, int G,
                                                                     int64_t rows, uint16_t* __restrict__ dA,
@@ -610,23 +642,30 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
         gw = __ldg(reinterpret_cast<const uint4*>(a_pre + r * F2 + c0 + tc * 8));
         uw = __ldg(reinterpret_cast<const uint4*>(a_pre + r * F2 + F + c0 + tc * 8));
     };
-    float4 h0, h1;
-    uint4 gw, uw;
+    // two chunks in flight: chunk p in set p & 1 while chunk p + 1 is loaded
+    // in the other and chunk p + 2 into temporaries
+    float4 H0[2], H1[2];
+    uint4 GW[2], UW[2];
     for (int i = 0; i < nrt; ++i) {
         const int64_t r0 = (rt0 + i) * kQT;
         uint8_t* const s_atom_r = s_atom_r0 + (i & 1) * 1024;
         uint8_t* const s_atom_c = s_atom_c0 + (i & 1) * 1024;
         // dgate / dup of this thread's chunks: rowwise codes from registers,
-        // bf16 values into the two tiles; chunk p + 1's loads are in flight
-        // while chunk p is computed
-        if (i == 0) load(r0, 0, h0, h1, gw, uw);     // later tiles: prefetched by the previous one
+        // bf16 values into the two tiles; the loads of chunks p + 1 and
+        // p + 2 are in flight while chunk p is computed
+        if (i == 0) {                         // later tiles: prefetched by the previous one
+            load(r0, 0, H0[0], H1[0], GW[0], UW[0]);
+            load(r0, 1, H0[1], H1[1], GW[1], UW[1]);
+        }
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             const int rl = tr + 16 * p;
             const int64_t r = r0 + rl;
             float4 nh0, nh1;
             uint4 ngw, nuw;
-            if (p + 1 < 8) load(r0, p + 1, nh0, nh1, ngw, nuw);
+            if (p + 2 < 8) load(r0, p + 2, nh0, nh1, ngw, nuw);
+            const float4 h0 = H0[p & 1], h1 = H1[p & 1];
+            const uint4 gw = GW[p & 1], uw = UW[p & 1];
             float gf[8], uf[8], dg[8], du[8];
             const float hf[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
             unpack8(gw, gf);
@@ -650,16 +689,19 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_swiglu_bwd_quant(const float*
             }
             *reinterpret_cast<uint4*>(tiles + rl * kQT + tc * 8) = vg;
             *reinterpret_cast<uint4*>(tiles + kQT * kQT + rl * kQT + tc * 8) = vu;
-            if (p + 1 < 8) {
-                h0 = nh0;
-                h1 = nh1;
-                gw = ngw;
-                uw = nuw;
+            if (p + 2 < 8) {
+                H0[p & 1] = nh0;
+                H1[p & 1] = nh1;
+                GW[p & 1] = ngw;
+                UW[p & 1] = nuw;
             }
         }
-        // the next tile's first chunk is loaded while this tile's columnwise
-        // blocks are quantized and stored
-        if (i + 1 < nrt) load(r0 + kQT, 0, h0, h1, gw, uw);
+        // the next tile's first two chunks are loaded while this tile's
+        // columnwise blocks are quantized and stored
+        if (i + 1 < nrt) {
+            load(r0 + kQT, 0, H0[0], H1[0], GW[0], UW[0]);
+            load(r0 + kQT, 1, H0[1], H1[1], GW[1], UW[1]);
+        }
         __syncthreads();                      // A: both tiles complete
         const int blk = warp & 3;
         const int col = (warp >> 2) * 64 + 2 * lane;

@@ -18,7 +18,7 @@ _SCORES = {"softmax": ops.MOE_SCORE_SOFTMAX, "sigmoid": ops.MOE_SCORE_SIGMOID}
 
 class MoELayer:
     def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_intermediates=False,
-                 router=False, n_shared=0, row_cap=None):
+                 router=False, n_shared=0, row_cap=None, wgrad_tiles=None):
         """store_intermediates: also write h and dA in bf16 (the step itself
         only needs their MXFP8 codes, which the up/gate GEMM's epilogue and
         the fused SwiGLU-backward quantization produce).
@@ -29,7 +29,9 @@ class MoELayer:
         ([CH1] §2.3.2, DeepSeek-V3's shared expert).  They are expert groups
         E .. E+S-1 of the same grouped GEMMs (weights [E+S, ...]), entered as
         S extra choices per token, so the layer runs G = E+S groups over
-        T (k+S) rows; the router and its logits cover the E routed experts."""
+        T (k+S) rows; the router and its logits cover the E routed experts.
+        wgrad_tiles: 224 or 256 forces the weight-gradient GEMMs' pair-tile
+        width; None chooses (see below)."""
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
         self.S = int(n_shared)
         self.G, self.kk = E + self.S, k + self.S      # expert groups, choices per token
@@ -80,9 +82,20 @@ class MoELayer:
         self.dw = z((T, k), torch.float32)
         # the weight gradients' right operands (dy_perm^T, dA^T) carry their
         # scales in the tile-224 layout when both weight-gradient GEMMs can run
-        # 256 x 224 pair tiles (their M = f and d multiples of 256): two TMEM
-        # accumulators hide each short tile's drain
-        self.wgrad_t224 = d % 256 == 0 and f % 256 == 0
+        # 256 x 224 pair tiles (their M = f and d multiples of 256) and the
+        # groups are short on average (at most 1024 rows: eight 128-deep
+        # k-steps a tile).  Two TMEM accumulators hide each short tile's
+        # drain; a long contraction loses more to the narrower MMA (1/8 of
+        # the tensor rate) than its single drain costs.
+        can224 = d % 256 == 0 and f % 256 == 0
+        if wgrad_tiles is None:
+            self.wgrad_t224 = can224 and self.R <= 1024 * self.G
+        elif wgrad_tiles in (224, 256):
+            if wgrad_tiles == 224 and not can224:
+                raise ValueError("224-wide weight-gradient tiles need d and f multiples of 256")
+            self.wgrad_t224 = wgrad_tiles == 224
+        else:
+            raise ValueError("wgrad_tiles: None, 224 or 256")
         self.col_sf = ops.MOE_SF_TILE224 if self.wgrad_t224 else ops.MOE_SF_ATOMS
         self.wgrad_b = ops.MOE_B_SF_TILE224 if self.wgrad_t224 else ops.MOE_B_GNK
 

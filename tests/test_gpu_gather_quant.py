@@ -137,6 +137,28 @@ def test_plain_both_axes_skip_tail(ops, sizes, cols):
     assert np.all(atoms_to_rowmajor(sc.cpu().numpy(), cols, rows)[:, Rp // 32:] == 0xCD)
 
 
+def test_plain_both_axes_subnormal_blocks(ops):
+    """Blocks whose elements are bf16 subnormals (scale byte 0: they scale by
+    2^127 into the E4M3 normal range) and blocks of subnormals around a tiny
+    normal maximum, on both axes; exact against the oracle."""
+    rows, cols = 256, 256
+    rng = np.random.default_rng(17)
+    bits = (rng.integers(0x3C00, 0x4400, size=(rows, cols)) | (rng.integers(0, 2, size=(rows, cols)) << 15))
+    sub = rng.integers(1, 0x80, size=(32, 32)) | (rng.integers(0, 2, size=(32, 32)) << 15)
+    bits[0:32, 0:32] = sub                                   # all-subnormal blocks (rows and columns)
+    bits[64:96, 64:96] = sub[::-1]
+    for i in range(32):                                      # a tiny normal maximum in every row and column
+        bits[64 + i, 64 + (5 * i) % 32] = 0x0380 | (int(rng.integers(0, 2)) << 15)   # 2^-120
+    bits[128:160, 32:64] = sub.T                             # subnormals next to normal values
+    x = torch.tensor(bits.astype(np.int32), dtype=torch.int32).to(torch.int16).view(torch.bfloat16).cuda()
+    gofs = np.array([0, rows])
+    res = ops.mxfp8_gather_quantize(x, _dev(gofs, torch.int32), 1, rows)
+    torch.cuda.synchronize()
+    P = to_np(x).astype(np.float64)
+    assert np.count_nonzero((P != 0) & (np.abs(P) < 2.0 ** -126)) > 2000
+    _check_axes(ops, P, gofs, rows, cols, res)
+
+
 @pytest.mark.parametrize("rowwise,colwise", [(True, False), (False, True)])
 def test_single_axis(ops, rowwise, colwise):
     idx, w, slot_of, row_id, gofs = _routing(400, 8, 2, seed=21)
