@@ -79,6 +79,27 @@ struct Tile {
     int kq;           // NVFP4 WGRAD: 64-row MMAs in the last k-step (4, or 2 for a group ending half-way)
 };
 
+// FWD / DGRAD tile t -> (m-tile, n-tile), in raster bands of p.band
+// m-tiles (consecutive tiles walk the n-tiles of a band, which share each B
+// tile).  With p.group_bands the tiles are taken group by group (group g
+// owns m-tiles gofs[g]/128 .. gofs[g+1]/128 and their n_tiles tiles each, so
+// the group of tile t is the group of row (t / n_tiles) * 128) and the bands
+// restart at each group's first m-tile: a band never mixes two experts'
+// weight blocks, and a band as wide as the group streams that group's
+// weights from DRAM once.
+__device__ __forceinline__ void fwd_tile_mn(const Params& p, const int* s_gofs, int64_t total_mt, int64_t t,
+                                            int64_t& mt, int& nt) {
+    if (!p.group_bands) {
+        band_decode(t, total_mt, p.n_tiles, p.band, mt, nt);
+        return;
+    }
+    const int g = find_group(s_gofs, p.G, (t / p.n_tiles) * BM);
+    const int64_t m0 = s_gofs[g] / BM, mg = (s_gofs[g + 1] - s_gofs[g]) / BM;
+    int64_t ml;
+    band_decode(t - m0 * p.n_tiles, mg, p.n_tiles, p.band, ml, nt);
+    mt = m0 + ml;
+}
+
 // NVF4: NVFP4 WGRAD counts its contraction in rows (k-steps of 256 rows,
 // 128 packed bytes), so kbeg is the group's first row and a group whose
 // row count is an odd multiple of 128 ends with a half k-step.
@@ -88,7 +109,7 @@ __device__ __forceinline__ void get_tile(const Params& p, const int* s_gofs, int
     int64_t mt;
     int nt;
     if (p.mode != MOE_GEMM_WGRAD) {
-        band_decode(t, total_mt, p.n_tiles, p.band, mt, nt);
+        fwd_tile_mn(p, s_gofs, total_mt, t, mt, nt);
         const int64_t row = mt * BM;
         ti.g = find_group(s_gofs, p.G, row);
         ti.a_row = row;
@@ -400,7 +421,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (t + gridDim.x < total) {      // FWD/DGRAD only: rows = m-tile * 128
                     int64_t mt;
                     int nt;
-                    band_decode(t + gridDim.x, total_mt, p.n_tiles, p.band, mt, nt);
+                    fwd_tile_mn(p, s_gofs, total_mt, t + gridDim.x, mt, nt);
                     swiglu_bwd_prefetch_l2<BN>(p, mt * BM + quarter * 32 + lane, nt, half);
                 }
                 swiglu_bwd_prefetch<BN>(p, row, ti.nt, half, 0, apre);
@@ -640,7 +661,14 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     p.err = err;
     p.timeout_ns = 2000000000ull;   // 2 s per wait
     // m-tiles per raster band: 3 for long contractions, 4 for K <= 2048
-    // (measured on the DeepSeek-V3 layer against 2, 4, 8, 16 and 32)
+    // (measured on the DeepSeek-V3 layer against 2, 4, 8, 16 and 32).  The
+    // fp32-output dgrad takes group-aligned bands: its DRAM reads fall from
+    // 6.3 to 5.6 GB a launch at the DeepSeek-V3 shape, its time is the same.
+    // The other GEMMs keep bands across group boundaries: group-aligned
+    // bands made the plain dgrad 3 % slower, and the SwiGLU up/gate GEMM
+    // 1-3 % slower even with bands of a whole group, which cut its reads
+    // from 12.6 to 9.4 GB (it is not bound by DRAM).
+    p.group_bands = mode != MOE_GEMM_WGRAD && epilogue == MOE_EPI_NONE_F32;
     p.band = choice.band > 0 ? choice.band : (K <= 2048 ? 4 : 3);
     p.n_tiles = N / BN;
     int64_t upper_tiles;

@@ -40,6 +40,7 @@ struct Params {
     int32_t* err;
     uint64_t timeout_ns;
     int band;           // m-tiles per raster band (consecutive tiles share the B tile)
+    int group_bands;    // 1-SM FWD / DGRAD: bands restart at each group's first m-tile
     int tma_store;      // pair kernel, BN = 256, MOE_EPI_NONE: write D through the TMA (tensor map tmD)
     // bf16 operands (kind::f16): the columns of D that exist (n_out <= N,
     // the rest of the tile is not stored) and D's row stride in elements

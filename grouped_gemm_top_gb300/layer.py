@@ -228,6 +228,13 @@ class MoELayer:
         self._mem("combine_out", ops.moe_unpermute_combine, self.y_perm, self.slot_of, self.topk_w, self.out, err)
 
     def backward_(self):
+        self.backward_outputs_()
+        self.backward_dw1_()
+
+    def backward_outputs_(self):
+        """The backward up to the step's outputs dx and dlogits (and dW2):
+        everything but the last weight gradient, so that dx and dlogits can
+        leave the GPU while dW1 is computed."""
         E, k, d, f, M = self.G, self.kk, self.d, self.f, self.row_cap
         err = self.err
         # dw = <dout, y_perm> per (token, choice); dy_perm = w * dout is only
@@ -252,9 +259,6 @@ class MoELayer:
         # dX_perm = dA W1^T
         self._gemm(ops.MOE_GEMM_DGRAD, self.dAq, self.dAs, self.W1d, self.W1d_s, ops.MOE_B_GNK,
                    self.gofs, E, M, d, 2 * f, ops.MOE_EPI_NONE, None, self.dx_perm, None, err)
-        # dW1_g = X_g^T dA_g
-        self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, self.wgrad_b, self.gofs, E, d,
-                   2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, err)
         ops.moe_route_bwd(self.logits, self.route_idx, self.dw, self.score, self.normalize, self.dlogits, err)
         if self.router:
             # dx_r = bf16(dlogits) W_r^T, dW_r = x^T bf16(dlogits); dx = dx_r + sum_j dX_perm[slot]
@@ -266,6 +270,12 @@ class MoELayer:
             ops.moe_unpermute_combine_add(self.dx_perm, self.slot_of, None, self.dx_r, self.dx, err)
         else:
             self._mem("combine_dx", ops.moe_unpermute_combine, self.dx_perm, self.slot_of, None, self.dx, err)
+
+    def backward_dw1_(self):
+        """The last weight gradient, dW1_g = X_g^T dA_g."""
+        E, d, f, M = self.G, self.d, self.f, self.row_cap
+        self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, self.wgrad_b, self.gofs, E, d,
+                   2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, self.err)
 
     def step_(self):
         """One fwd+bwd pass over the resident inputs (no allocation, no sync)."""
@@ -318,26 +328,35 @@ class MoELayer:
     _IO = ("x", "logits", "dout", "out", "dx", "dlogits")
 
     def enable_pipelining(self, warmup=1, nsets=3):
-        """nsets buffer sets of the step's inputs and outputs and one CUDA
-        graph per set, so that run_pipelined() can copy later steps' inputs
-        in and earlier steps' outputs out while a step computes.  With three
-        sets, step i's inputs wait for step i-3's outputs to leave, so the
-        copies have two steps' compute time to finish (with two, a slow host
-        link would have to move one step's outputs and the next inputs within
-        a single step)."""
+        """nsets buffer sets of the step's inputs and outputs, and per set
+        three CUDA graphs (forward; backward up to dx and dlogits; dW1), so
+        that run_pipelined() can copy later steps' inputs in and earlier
+        steps' outputs out while a step computes.  With three sets, step i's
+        inputs wait for step i-3's outputs to leave, so the copies have two
+        steps' compute time to finish (with two, a slow host link would have
+        to move one step's outputs and the next inputs within a single
+        step)."""
         if getattr(self, "_sets", None) is not None:
             return
         first = {n: getattr(self, n) for n in self._IO}
         sets = [first] + [{n: torch.zeros_like(t) for n, t in first.items()} for _ in range(nsets - 1)]
-        graphs = []
+        parts = (self.forward_, self.backward_outputs_, self.backward_dw1_)
+        graphs, whole = [], []
         for bufs in sets:
             for n, t in bufs.items():
                 setattr(self, n, t)
             self.graph = None
-            graphs.append(self.capture(warmup))
+            whole.append(self.capture(warmup))      # also the warm-up of this set
+            gs = []
+            for fn in parts:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn()
+                gs.append(g)
+            graphs.append(tuple(gs))
         for n, t in first.items():
             setattr(self, n, t)
-        self.graph = graphs[0]
+        self.graph = whole[0]
         self._sets = tuple(sets)
         self._graphs = graphs
         self._h2d_stream = torch.cuda.Stream(device=self.device)
@@ -348,39 +367,53 @@ class MoELayer:
         (x, logits, dout, out_host, dx_host, dlogits_host) of host tensors
         (pinned, for asynchronous copies).  Step i uses buffer set i % nsets:
         its inputs are copied in on an input-copy stream (once the outputs of
-        the last step that used the set have been copied out), the step's
-        graph runs on the current stream, and its outputs are copied out on
-        an output-copy stream while later steps compute (the GPU's copy
-        engines run both directions beside the kernels).  Returns with the
-        current stream ordered after the last copy.  The weight gradients
-        and the error word are those of the last step."""
+        the last step that used the set have been copied out), its graphs
+        run on the current stream, and its outputs are copied out on an
+        output-copy stream while later work computes (the GPU's copy engines
+        run both directions beside the kernels).  Within a step the forward
+        waits only for x and logits (dout arrives meanwhile), out leaves
+        while the backward runs, and dx and dlogits leave while dW1 is
+        computed.  Returns with the current stream ordered after the last
+        copy.  The weight gradients and the error word are those of the last
+        step."""
         self.enable_pipelining()
         comp = torch.cuda.current_stream(self.device)
         h2d, d2h = self._h2d_stream, self._d2h_stream
         nsets = len(self._sets)
         free = [None] * nsets        # events: the set's outputs have been copied out
+
+        def mark(stream):
+            e = torch.cuda.Event()
+            e.record(stream)
+            return e
+
         for i, (x, logits, dout, out_h, dx_h, dl_h) in enumerate(batches):
             b = i % nsets
             bufs = self._sets[b]
+            g_fwd, g_bwd, g_dw1 = self._graphs[b]
             with torch.cuda.stream(h2d):
                 if free[b] is not None:
                     h2d.wait_event(free[b])
-                bufs["x"].copy_(x, non_blocking=True)
                 bufs["logits"].copy_(logits, non_blocking=True)
+                bufs["x"].copy_(x, non_blocking=True)
+                fwd_in = mark(h2d)
                 bufs["dout"].copy_(dout, non_blocking=True)
-                loaded = torch.cuda.Event()
-                loaded.record(h2d)
-            comp.wait_event(loaded)
-            self._graphs[b].replay()
-            done = torch.cuda.Event()
-            done.record(comp)
+                bwd_in = mark(h2d)
+            comp.wait_event(fwd_in)
+            g_fwd.replay()
+            fwd_done = mark(comp)
             with torch.cuda.stream(d2h):
-                d2h.wait_event(done)
+                d2h.wait_event(fwd_done)
                 out_h.copy_(bufs["out"], non_blocking=True)
+            comp.wait_event(bwd_in)
+            g_bwd.replay()
+            bwd_done = mark(comp)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(bwd_done)
                 dx_h.copy_(bufs["dx"], non_blocking=True)
                 dl_h.copy_(bufs["dlogits"], non_blocking=True)
-                free[b] = torch.cuda.Event()
-                free[b].record(d2h)
+                free[b] = mark(d2h)
+            g_dw1.replay()
         comp.wait_stream(h2d)
         comp.wait_stream(d2h)
 
