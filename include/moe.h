@@ -163,7 +163,9 @@ typedef enum {
  *   band             m-tiles per raster band of the persistent tile order
  *                    (consecutive tiles walk the n-tiles of a band of m-tiles
  *                    that share them), 1..64; 0 = the kernel's measured
- *                    default.
+ *                    default.  On the 1-SM kernel the bands of the fp32
+ *                    output (MOE_EPI_NONE_F32) restart at every group's first
+ *                    m-tile; elsewhere they run across group boundaries.
  *   register_stores  1: the CTA-pair kernel's plain bf16 epilogue stores
  *                    from registers instead of staging through shared memory
  *                    for TMA stores; 0 = default (TMA stores).
