@@ -24,10 +24,12 @@ __device__ bool gofs_valid(const int32_t* gofs, int G, int64_t rows) {
 
 // Rowwise: tile = 128 rows x 128 cols.  256 threads; a thread owns 8
 // consecutive elements, four neighbouring threads form one 32-element block.
+// canon: scales in the canonical row-major [rows, cols / 32] layout instead
+// of the atom layout.
 __global__ void __launch_bounds__(256) k_quant_rows(const uint4* __restrict__ x, int64_t rows, int cols,
                                                     const int32_t* __restrict__ gofs, int G,
                                                     uint2* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                    int32_t* err) {
+                                                    int canon, int32_t* err) {
     __shared__ __align__(16) uint8_t s_atom[512];
     const int64_t r0 = (int64_t)blockIdx.y * kQT;
     const int c0 = blockIdx.x * kQT;
@@ -60,11 +62,14 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint4* __restrict__ x,
         codes[(r * cols + c0) / 8 + tc] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
         if ((tc & 3) == 0) {
             const int kb = tc >> 2;          // local block 0..3
-            s_atom[(rl & 31) * 16 + ((rl >> 5) & 3) * 4 + kb] = (uint8_t)b;
+            if (canon)
+                scales[r * (cols / 32) + c0 / 32 + kb] = (uint8_t)b;
+            else
+                s_atom[(rl & 31) * 16 + ((rl >> 5) & 3) * 4 + kb] = (uint8_t)b;
         }
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
+    if (!canon && threadIdx.x < 32) {
         const int64_t atom = (int64_t)(c0 / kQT) * (rows / kQT) + r0 / kQT;
         reinterpret_cast<uint4*>(scales + atom * 512)[threadIdx.x] = reinterpret_cast<const uint4*>(s_atom)[threadIdx.x];
     }
@@ -85,10 +90,12 @@ constexpr int kColTiles = 4;
 // With batch_rows = Kg > 0 the input is G equal groups of Kg rows and the
 // output is batched per group: codes [G][cols][Kg] (each group's transposed
 // block contiguous) and scales in the atom layout of the [G*cols, Kg] matrix.
+// canon: scales in the canonical row-major layout of the output matrix
+// ([cols, rows], or [G * cols, batch_rows] batched) instead of the atoms.
 __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x, int64_t rows, int cols,
                                                     const int32_t* __restrict__ gofs, int G, int glu,
                                                     int64_t batch_rows, uint8_t* __restrict__ codes,
-                                                    uint8_t* __restrict__ scales, int32_t* err) {
+                                                    uint8_t* __restrict__ scales, int canon, int32_t* err) {
     // the input tile [row][col] and, after it has been consumed, the output
     // codes tile [col][row] share one buffer
     __shared__ __align__(16) uint8_t s_buf[kQT * (kQT + 8) * 2];
@@ -152,7 +159,23 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x,
                 const uint32_t hi = cvt_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
                 w[h][i] = lo | (hi << 16);
             }
-            s_atom[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b;
+            if (canon) {
+                // output row and 32-row block of this (column, block) pair
+                int64_t orow, ob, kout;
+                if (batch_rows > 0) {
+                    const int64_t g = r0 / batch_rows;
+                    orow = g * cols + c0 + col;
+                    ob = (r0 - g * batch_rows) / 32 + blk;
+                    kout = batch_rows;
+                } else {
+                    orow = c0 + col;
+                    ob = r0 / 32 + blk;
+                    kout = rows;
+                }
+                scales[orow * (kout / 32) + ob] = (uint8_t)b;
+            } else {
+                s_atom[(col & 31) * 16 + ((col >> 5) & 3) * 4 + blk] = (uint8_t)b;
+            }
         }
         __syncthreads();     // every thread is done reading the input tile
 #pragma unroll
@@ -180,7 +203,7 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x,
             }
             *reinterpret_cast<uint4*>(codes + dst) = q;
         }
-        if (threadIdx.x < 32) {
+        if (!canon && threadIdx.x < 32) {
             int64_t atom;
             if (batch_rows > 0) {
                 const int64_t g = r0 / batch_rows, kk = r0 - g * batch_rows;
@@ -198,9 +221,19 @@ __global__ void __launch_bounds__(256) k_quant_cols(const uint4* __restrict__ x,
 
 using namespace moe;
 
-extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols, int axis, const int32_t* gofs,
-                                             int G, uint8_t* codes, uint8_t* scales, int32_t* err, void* stream) {
+// padded group offsets of an mxfp8_group_quantize output: gofs, or g * Kg
+// for the batched axes
+__global__ void k_padded_offsets(const int32_t* __restrict__ gofs, int G, int64_t batch_rows, int32_t* out) {
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g <= G; g += gridDim.x * blockDim.x)
+        out[g] = batch_rows > 0 ? (int32_t)(g * batch_rows) : gofs[g];
+}
+
+extern "C" moe_status_t mxfp8_group_quantize_ex(const void* x, int64_t rows, int cols, int axis,
+                                                const int32_t* gofs, int G, uint8_t* codes, uint8_t* scales,
+                                                int32_t* padded_offsets, int scale_layout, int32_t* err,
+                                                void* stream) {
     MOE_REQUIRE(x && codes && scales, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(scale_layout == MOE_SF_ATOMS || scale_layout == MOE_SF_CANONICAL, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(rows >= 0 && cols > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(rows % kQT == 0 && cols % kQT == 0, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(rows / kQT <= 65535 && cols / kQT <= 65535, MOE_ERR_UNSUPPORTED);
@@ -210,22 +243,33 @@ extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int co
     const bool batched = axis == MOE_QUANT_COLWISE_BATCHED || axis == MOE_QUANT_COLWISE_BATCHED_GLU;
     if (batched) MOE_REQUIRE(G >= 1 && rows % G == 0 && (rows / G) % kQT == 0, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(gofs == nullptr || (G >= 1 && G <= 4096), MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(padded_offsets == nullptr || batched || gofs != nullptr, MOE_ERR_INVALID_ARG);
+    const int canon = scale_layout == MOE_SF_CANONICAL ? 1 : 0;
     MOE_REQUIRE(moe_aligned16(x) && moe_aligned16(codes) && moe_aligned16(scales), MOE_ERR_ALIGNMENT);
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
-    if (rows == 0) return MOE_OK;
     cudaStream_t s = (cudaStream_t)stream;
+    if (padded_offsets != nullptr) {
+        k_padded_offsets<<<1, 256, 0, s>>>(gofs, G, batched ? rows / G : 0, padded_offsets);
+        MOE_CHECK_LAUNCH();
+    }
+    if (rows == 0) return MOE_OK;
     if (axis == MOE_QUANT_ROWWISE) {
         dim3 grid(cols / kQT, (unsigned)(rows / kQT));
-        k_quant_rows<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, (uint2*)codes, scales, err);
+        k_quant_rows<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, gofs, G, (uint2*)codes, scales, canon, err);
     } else {
         dim3 grid((unsigned)((rows / kQT + kColTiles - 1) / kColTiles), cols / kQT);
         const int glu = (axis == MOE_QUANT_COLWISE_GLU || axis == MOE_QUANT_COLWISE_BATCHED_GLU) ? 1 : 0;
         // batched outputs use equal groups of rows / G rows (gofs, if given, only bounds the rows read)
         k_quant_cols<<<grid, 256, 0, s>>>((const uint4*)x, rows, cols, batched ? nullptr : gofs, G, glu,
-                                          batched ? rows / G : 0, codes, scales, err);
+                                          batched ? rows / G : 0, codes, scales, canon, err);
     }
     MOE_CHECK_LAUNCH();
     return MOE_OK;
+}
+
+extern "C" moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols, int axis, const int32_t* gofs,
+                                             int G, uint8_t* codes, uint8_t* scales, int32_t* err, void* stream) {
+    return mxfp8_group_quantize_ex(x, rows, cols, axis, gofs, G, codes, scales, nullptr, MOE_SF_ATOMS, err, stream);
 }
 
 // ---------------------------------------------------------------------------

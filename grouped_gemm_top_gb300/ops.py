@@ -34,7 +34,7 @@ MOE_QUANT_COLWISE_BATCHED, MOE_QUANT_COLWISE_BATCHED_GLU = 3, 4
 MOE_GEMM_FWD, MOE_GEMM_DGRAD, MOE_GEMM_WGRAD = 0, 1, 2
 MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD, MOE_EPI_NONE_F32 = 0, 1, 2, 3
 MOE_B_GNK, MOE_B_NGK, MOE_B_SF_TILE224 = 0, 1, 2
-MOE_SF_ATOMS, MOE_SF_TILE224 = 0, 1
+MOE_SF_ATOMS, MOE_SF_TILE224, MOE_SF_CANONICAL = 0, 1, 2
 MOE_GEMM_KERNEL_AUTO, MOE_GEMM_KERNEL_1SM, MOE_GEMM_KERNEL_1SM_N128 = 0, 1, 2
 MOE_GEMM_KERNEL_PAIR, MOE_GEMM_KERNEL_PAIR_N128 = 3, 4
 (MOE_OP_ROUTE_TOPK, MOE_OP_PERMUTE, MOE_OP_GROUP_QUANTIZE, MOE_OP_GATHER_QUANTIZE, MOE_OP_GROUPED_GEMM,
@@ -50,7 +50,7 @@ EXPORTS = [
     "moe_route_drop_shared", "nvfp4_sf_bytes", "nvfp4_quantize", "grouped_gemm_nvfp4", "nvfp4_quantize_cols",
     "moe_selftest_bounded_wait", "moe_workspace_size", "mxfp8_scale_layout", "grouped_gemm_mxfp8_ex",
     "grouped_gemm_mxfp8_swiglu_quant_ex", "grouped_gemm_nvfp4_ex", "moe_hbm_fill", "mxfp8_gather_quantize_ex",
-    "mxfp8_swiglu_bwd_quantize_ex",
+    "mxfp8_swiglu_bwd_quantize_ex", "mxfp8_group_quantize_ex",
 ]
 
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -83,6 +83,7 @@ _SIGS = {
     "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_permute": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "mxfp8_group_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "mxfp8_group_quantize_ex": (_i32, [_vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
     "mxfp8_gather_quantize": (_i32, [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp,
                                      _vp]),
     "gemm_bf16_nt": (_i32, [_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp]),
@@ -256,6 +257,8 @@ def sf_bytes_tile224(rows: int, cols: int) -> int:
 
 def mxfp8_group_quantize(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, codes=None, scales=None, err=None,
                          stream=None):
+    """See include/moe.h.  Returns (codes, scales) with the scales in the
+    atom layout."""
     rows, cols = x.shape
     if axis == MOE_QUANT_ROWWISE:
         codes = codes if codes is not None else _empty((rows, cols), torch.uint8, x)
@@ -267,6 +270,29 @@ def mxfp8_group_quantize(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, codes=None, 
     _check("mxfp8_group_quantize", lib.mxfp8_group_quantize(_p(x), rows, cols, int(axis), _p(gofs), int(G),
                                                             _p(codes), _p(scales), _p(err), _stream(stream)))
     return codes, scales
+
+
+def mxfp8_group_quantize_ex(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, scale_layout=MOE_SF_CANONICAL,
+                            want_padded_offsets=True, codes=None, scales=None, padded_offsets=None, err=None,
+                            stream=None):
+    """mxfp8_group_quantize with the scale layout chosen (MOE_SF_ATOMS or
+    MOE_SF_CANONICAL, row-major [R, C / 32] of the output matrix) and the
+    padded group offsets written out.  Returns (codes, scales,
+    padded_offsets or None)."""
+    rows, cols = x.shape
+    if axis == MOE_QUANT_ROWWISE:
+        codes = codes if codes is not None else _empty((rows, cols), torch.uint8, x)
+    elif axis in (MOE_QUANT_COLWISE_BATCHED, MOE_QUANT_COLWISE_BATCHED_GLU):
+        codes = codes if codes is not None else _empty((G, cols, rows // G), torch.uint8, x)
+    else:
+        codes = codes if codes is not None else _empty((cols, rows), torch.uint8, x)
+    scales = scales if scales is not None else _empty((sf_bytes(rows, cols),), torch.uint8, x)
+    if padded_offsets is None and want_padded_offsets:
+        padded_offsets = _empty((int(G) + 1,), torch.int32, x)
+    _check("mxfp8_group_quantize_ex",
+           lib.mxfp8_group_quantize_ex(_p(x), rows, cols, int(axis), _p(gofs), int(G), _p(codes), _p(scales),
+                                       _p(padded_offsets), int(scale_layout), _p(err), _stream(stream)))
+    return codes, scales, padded_offsets
 
 
 def mxfp8_gather_quantize(src, gofs, G, rows, row_id=None, k=1, row_w=None, rowwise=True, colwise=True,

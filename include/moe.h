@@ -133,8 +133,11 @@ typedef enum {
  *                    right operand (MOE_B_SF_TILE224): a 224-row tile starts on
  *                    an atom of its own, which 224-row tiles of the plain atom
  *                    layout do not.
+ *   MOE_SF_CANONICAL row-major [R, C / 32]: byte r * (C / 32) + b is the scale
+ *                    of row r, block b (mxfp8_group_quantize_ex only; the
+ *                    GEMMs read the atom layout, mxfp8_scale_layout converts).
  */
-typedef enum { MOE_SF_ATOMS = 0, MOE_SF_TILE224 = 1 } moe_sf_layout_t;
+typedef enum { MOE_SF_ATOMS = 0, MOE_SF_TILE224 = 1, MOE_SF_CANONICAL = 2 } moe_sf_layout_t;
 
 /*
  * Grouped-GEMM kernel selection, per call (the *_ex entry points; the plain
@@ -299,19 +302,41 @@ MOE_API moe_status_t mxfp8_group_quantize(const void* x, int64_t rows, int cols,
                                   const int32_t* gofs, int G, uint8_t* codes, uint8_t* scales,
                                   int32_t* err, void* stream);
 /*
+ * mxfp8_group_quantize_ex -- mxfp8_group_quantize with the padded group
+ * offsets as an output and the scale layout chosen.
+ *   padded_offsets  [G+1] int32 out (device) or NULL: the first row of group
+ *                   g in the blocked axis of the output, i.e. where its
+ *                   blocks start (the column of the transposed columnwise
+ *                   codes; the row of the rowwise codes).  For the grouped
+ *                   axes these are gofs (the groups already start at
+ *                   multiples of 128, see below); for the batched axes
+ *                   g * rows / G.  Needs gofs unless the axis is batched.
+ *   scale_layout    MOE_SF_ATOMS (as mxfp8_group_quantize) or
+ *                   MOE_SF_CANONICAL: row-major [R, C / 32] for the output
+ *                   matrix Q [R, C] quantized along C, where Q is [rows, cols]
+ *                   for MOE_QUANT_ROWWISE, [cols, rows] for the columnwise
+ *                   axes and [G * cols, rows / G] for the batched ones (the
+ *                   same bytes as the atoms, placed in row order).
+ */
+MOE_API moe_status_t mxfp8_group_quantize_ex(const void* x, int64_t rows, int cols, int axis,
+                                             const int32_t* gofs, int G, uint8_t* codes, uint8_t* scales,
+                                             int32_t* padded_offsets, int scale_layout, int32_t* err,
+                                             void* stream);
+/*
  * Padded offsets of the group-aware columnwise output.  The plain definition
  * of the group-aware quantization pads group g's tail block and places the
  * group at sum_{h<g} ceil32(m_h) rows.  Here the permute already places
  * every group at a multiple of 128 rows (gofs, moe_permute), which is a
  * multiple of 32, with zero rows after its m_g routed rows: the padded
- * offsets of this output ARE gofs, so no separate array is returned.  Block
- * j of group g covers rows gofs[g] + 32 j ..; blocks past ceil32(m_g) rows
- * of the group hold only zero rows (scale byte 0, codes 0).
+ * offsets of this output ARE gofs (mxfp8_group_quantize_ex writes them out
+ * as padded_offsets).  Block j of group g covers rows gofs[g] + 32 j ..;
+ * blocks past ceil32(m_g) rows of the group hold only zero rows (scale
+ * byte 0, codes 0).
  *
- * Scale layout.  Every call here reads and writes scales in the atom layout
- * (the tensor cores' order, above), so no conversion runs on the hot path;
- * mxfp8_scale_layout converts to and from the canonical row-major
- * [rows, cols / 32] layout for callers that want it.
+ * Scale layout.  The hot path reads and writes scales in the atom layout
+ * (the tensor cores' order, above), so no conversion runs there;
+ * mxfp8_group_quantize_ex writes the canonical row-major [R, C / 32] layout
+ * on request, and mxfp8_scale_layout converts between the two.
  */
 
 /*

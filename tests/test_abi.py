@@ -28,7 +28,7 @@ def test_header_declares_the_entry_points():
     names = set(_declared())
     for n in ("moe_init", "moe_workspace_size", "moe_route_topk", "moe_permute", "mxfp8_group_quantize",
               "grouped_gemm_mxfp8", "moe_unpermute_combine", "moe_combine_bwd", "moe_route_bwd",
-              "mxfp8_scale_layout"):
+              "mxfp8_scale_layout", "mxfp8_group_quantize_ex"):
         assert n in names
 
 
@@ -93,6 +93,12 @@ def test_host_only_calls_and_argument_checks(lib_path):
     assert st == ops.MOE_ERR_UNSUPPORTED                       # rows % 128 != 0
     st = lib.moe_hbm_fill(ctypes.c_void_p(16), 24, 0, 0, None)
     assert st == ops.MOE_ERR_UNSUPPORTED                       # bytes % 16 != 0
+    p16 = ctypes.c_void_p(16)
+    st = lib.mxfp8_group_quantize_ex(p16, 128, 128, ops.MOE_QUANT_ROWWISE, None, 0, p16, p16, None, 7, None, None)
+    assert st == ops.MOE_ERR_INVALID_ARG                       # unknown scale layout
+    st = lib.mxfp8_group_quantize_ex(p16, 128, 128, ops.MOE_QUANT_COLWISE_GROUPED, None, 1, p16, p16, p16,
+                                     ops.MOE_SF_CANONICAL, None, None)
+    assert st == ops.MOE_ERR_INVALID_ARG                       # padded offsets of a grouped axis need gofs
 
 
 def test_no_environment_variables_in_the_library():

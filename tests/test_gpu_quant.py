@@ -154,3 +154,46 @@ def test_colwise_batched_per_group_blocks(ops, G, K, N, glu):
     for g in range(G):
         rq, rs, _ = O.mxfp8_quantize_cols_grouped(xn[g * K:(g + 1) * K], np.array([0, K]))
         assert np.array_equal(qn[g], rq[perm]) and np.array_equal(sn[g], rs[perm])
+
+
+def test_ex_canonical_scales_and_padded_offsets(ops):
+    """mxfp8_group_quantize_ex: the canonical row-major scales are the atom
+    scales in row order (and the oracle's), the codes are unchanged, and the
+    padded offsets of the grouped axes are the group offsets."""
+    sizes, cols = [5, 0, 130, 127, 1], 256
+    gofs = padded_layout(sizes)
+    Rp = int(gofs[-1])
+    x = torch.zeros((Rp, cols), dtype=torch.bfloat16, device="cuda")
+    src = _varied(Rp, cols, seed=21)
+    for g, m in enumerate(sizes):
+        x[gofs[g]:gofs[g] + m] = src[gofs[g]:gofs[g] + m]
+    gt = torch.tensor(gofs, dtype=torch.int32, device="cuda")
+    G = len(sizes)
+    for axis in (ops.MOE_QUANT_ROWWISE, ops.MOE_QUANT_COLWISE_GROUPED, ops.MOE_QUANT_COLWISE_GLU):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q_at, s_at = ops.mxfp8_group_quantize(x, axis, gt, G, err=err)
+        q_ca, s_ca, po = ops.mxfp8_group_quantize_ex(x, axis, gt, G, ops.MOE_SF_CANONICAL, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(q_at, q_ca)
+        assert np.array_equal(po.cpu().numpy(), gofs)
+        R, C = (Rp, cols) if axis == ops.MOE_QUANT_ROWWISE else (cols, Rp)
+        assert np.array_equal(s_ca.cpu().numpy().reshape(R, C // 32), atoms_to_rowmajor(s_at.cpu().numpy(), R, C))
+    _, rs = O.mxfp8_quantize_rows(to_np(x))
+    _, s_ca, _ = ops.mxfp8_group_quantize_ex(x, ops.MOE_QUANT_ROWWISE, gt, G, ops.MOE_SF_CANONICAL)
+    torch.cuda.synchronize()
+    assert np.array_equal(s_ca.cpu().numpy().reshape(Rp, cols // 32), rs)
+
+
+@pytest.mark.parametrize("glu", [False, True])
+def test_ex_batched_canonical_and_offsets(ops, glu):
+    G, K, N = 3, 256, 384
+    x = _varied(G * K, N, seed=31)
+    axis = ops.MOE_QUANT_COLWISE_BATCHED_GLU if glu else ops.MOE_QUANT_COLWISE_BATCHED
+    q_at, s_at = ops.mxfp8_group_quantize(x, axis, None, G)
+    q_ca, s_ca, po = ops.mxfp8_group_quantize_ex(x, axis, None, G, ops.MOE_SF_CANONICAL)
+    torch.cuda.synchronize()
+    assert torch.equal(q_at, q_ca)
+    assert np.array_equal(po.cpu().numpy(), np.arange(0, (G + 1) * K, K))
+    assert np.array_equal(s_ca.cpu().numpy().reshape(G * N, K // 32),
+                          atoms_to_rowmajor(s_at.cpu().numpy(), G * N, K))
