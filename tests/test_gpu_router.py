@@ -95,3 +95,31 @@ def test_tiny_layer_with_router_stagewise(ops, score, S):
     Rp = int(L.gofs[-1].item())
     ref_dx = O.combine(to_np(L.dx_perm)[:Rp], slot_of, None) + L.dx_r.double().cpu().numpy()
     assert_bf16_close(L.dx, ref_dx, what="dx = dx_moe + dx_r")
+
+
+def test_pipelined_steps_with_router_and_shared_expert_match_single_steps(ops):
+    """run_pipelined (three graphs per buffer set: forward, backward to dx and
+    dlogits, dW1) on the layer with its router and a shared expert returns
+    for every step what step() returns for that batch alone."""
+    from grouped_gemm_top_gb300.layer import MoELayer
+    T, d, E, k, f, S = 256, 512, 8, 2, 256, 1
+    L = MoELayer(T, d, E, k, f, "sigmoid", True, router=True, n_shared=S)
+    inp = synth.make_layer_inputs(T, d, E, f, "cuda", n_shared=S)
+    L.set_weights(inp["W1"], inp["W2"])
+    L.set_router_weights(synth.make_normal_bf16((d, E), 21, "cuda", std=0.05))
+    batches, refs = [], []
+    for i in range(4):
+        x = synth.make_normal_bf16((T, d), 400 + i, "cuda").cpu().pin_memory()
+        logits = torch.zeros((T, E), dtype=torch.float32).pin_memory()      # the router computes them
+        dout = synth.make_normal_bf16((T, d), 500 + i, "cuda").cpu().pin_memory()
+        refs.append(tuple(t.clone() for t in L.step(x, logits, dout)))
+        outs = (torch.empty((T, d), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((T, d), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((T, E), dtype=torch.float32).pin_memory())
+        batches.append((x, logits, dout) + outs)
+    L.run_pipelined(batches)
+    torch.cuda.synchronize()
+    L.check_err()
+    for b, ref in zip(batches, refs):
+        for got, want in zip(b[3:], ref):
+            assert torch.equal(got, want)
