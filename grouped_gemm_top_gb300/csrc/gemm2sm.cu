@@ -61,8 +61,11 @@ struct C2 {
     static constexpr uint32_t SF0 = NACC * BN_;         // TMEM: accumulators, then scales
     static constexpr uint32_t SF_COLS = NVF4 ? 16 + 16 * (BN_ / 128) : (BN_ == 224 ? 12 : TMEM_SF_STRIDE);
     // TMA-store staging of the epilogue: one box per epilogue warp (N = 256),
-    // two that alternate (N = 224, whose smaller stages leave the room)
-    static constexpr int EPI_BYTES = (BN_ >= 224 && !NVF4) ? EPI_WARPS * kEpiBoxBytes * (BN_ == 224 ? 2 : 1) : 0;
+    // two that alternate and one box of zeros for the tiles of empty groups
+    // (N = 224, whose smaller stages leave the room)
+    static constexpr int EPI_BYTES =
+        (BN_ >= 224 && !NVF4) ? EPI_WARPS * kEpiBoxBytes * (BN_ == 224 ? 2 : 1) + (BN_ == 224 ? kEpiBoxBytes : 0) : 0;
+    static constexpr int OFF_ZERO_IN_EPI = EPI_WARPS * kEpiBoxBytes * (BN_ == 224 ? 2 : 1);
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;       // 1024-byte aligned
@@ -278,6 +281,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         *bad_flag = 0;
     }
     for (int i = threadIdx.x; i <= p.G; i += THREADS) s_gofs[i] = p.gofs[i];
+    const uint32_t zbox = smem_u32(smem + C::OFF_EPI + C::OFF_ZERO_IN_EPI);   // the box of zeros
+    if constexpr (BN == 224) {
+        if (threadIdx.x < kEpiBoxBytes / 16) st_shared_v4(zbox + 16u * threadIdx.x, 0u, 0u, 0u, 0u);
+        fence_proxy_async_shared();      // visible to the TMA stores that read it
+    }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS));
@@ -449,9 +457,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             Tile2 ti;
             get_tile2<BN>(p, s_gofs, s_pt, total_pm, t, rank, ti);
             const int64_t row = ti.out_row + quarter * 32 + lane;
-            if (ti.nk == 0) {
+            if (ti.nk == 0) {      // an empty group's weight gradient: zeros
                 if constexpr (BN == 224)
-                    epilogue_zero224(p, row, ti.nt, half);
+                    epilogue_zero_tma<224>(&tmD, zbox, row - lane, ti.nt, half, lane, p.N);
                 else
                     epilogue_zero<BN>(p, row, ti.nt, half);
                 continue;

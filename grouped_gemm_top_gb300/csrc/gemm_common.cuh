@@ -768,18 +768,31 @@ __device__ __forceinline__ void epilogue_zero(const Params& p, int64_t row, int 
     for (int c = 0; c < BN / 64; ++c) store_row32(p.d + row * p.N + (int64_t)nt * BN + half * (BN / 2) + 32 * c, z);
 }
 
-// Zero fill of an empty group's 224-wide weight-gradient tile (the chunks of
-// column half `half`, as in epilogue_tile_tma224, below column N).
-__device__ __forceinline__ void epilogue_zero224(const Params& p, int64_t row, int nt, int half) {
-    float z[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = 0.f;
-    const int c0 = 4 * half, nch = half == 0 ? 4 : 3;
-    for (int j = 0; j < nch; ++j) {
-        const int col = nt * 224 + 32 * (c0 + j);
-        if (col < p.N) store_row32(p.d + row * p.N + col, z);
+// Zero fill of an empty group's weight-gradient tile through TMA stores of a
+// shared-memory box of zeros (32 rows x kEpiBoxCols columns, written once at
+// kernel start): the 32-column boxes of column half `half` of a BN-wide tile
+// (224: chunks 0-3 and 4-6), boxes at or past column N skipped.  One lane
+// issues the stores; they complete with the warp's other bulk stores.  (With
+// many empty groups, as under skewed routing, per-thread zero stores took
+// 1.3 ms more of the DeepSeek-V3 step's weight gradients.)
+template <int BN>
+__device__ __forceinline__ void epilogue_zero_tma(const CUtensorMap* tmD, uint32_t zbox, int64_t row0, int nt,
+                                                  int half, int lane, int N) {
+    static_assert(kEpiBoxCols == 32, "32-column zero boxes");
+    const int c0 = 4 * half;
+    const int nch = BN == 224 && half == 1 ? 3 : 4;
+    if (lane == 0) {
+        for (int j = 0; j < nch; ++j) {
+            const int col = nt * BN + 32 * (c0 + j);
+            if (col < N) {
+                tma_store_2d(tmD, zbox, col, (int)row0);
+                bulk_commit_group();
+            }
+        }
     }
+    __syncwarp();
 }
+
 
 }  // namespace gg
 
