@@ -460,6 +460,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (ti.nk == 0) {      // an empty group's weight gradient: zeros
                 if constexpr (BN == 224)
                     epilogue_zero_tma<224>(&tmD, zbox, row - lane, ti.nt, half, lane, p.N);
+                else if (!NVF4 && BN == 256 && p.tma_store)
+                    epilogue_zero_tma256(&tmD, smem_u32(smem + C::OFF_EPI + kEpiBoxBytes * ew), row - lane, ti.nt,
+                                         half, lane);
                 else
                     epilogue_zero<BN>(p, row, ti.nt, half);
                 continue;

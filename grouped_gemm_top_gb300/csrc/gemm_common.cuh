@@ -613,6 +613,29 @@ __device__ __forceinline__ void epilogue_tile_tma(const CUtensorMap* tmD, uint32
     }
 }
 
+// Zero fill of an empty group's 256-wide weight-gradient tile through the
+// warp's own staging box: once the box's earlier stores have read it, the
+// warp writes zeros into it and stores it four times (the 32-column boxes of
+// its column half).  The next use of the box for data waits for these
+// stores first, as it waits for any earlier one.
+__device__ __forceinline__ void epilogue_zero_tma256(const CUtensorMap* tmD, uint32_t buf, int64_t row0, int nt,
+                                                     int half, int lane) {
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
+    const uint32_t rowaddr = buf + (uint32_t)lane * (uint32_t)(kEpiBoxCols * 2);
+#pragma unroll
+    for (int c = 0; c < kEpiBoxCols / 8; ++c) st_shared_v4(rowaddr + 16u * c, 0u, 0u, 0u, 0u);
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < 128 / kEpiBoxCols; ++j) {
+            tma_store_2d(tmD, buf, nt * 256 + 128 * half + kEpiBoxCols * j, (int)row0);
+            bulk_commit_group();
+        }
+    }
+}
+
 // TMA-store epilogue for the 224-wide weight-gradient tiles of the CTA-pair
 // kernel (two accumulators, plain bf16 output).  The tile's 224 columns are
 // seven 32-column chunks: the warps of column half 0 drain chunks 0-3, those
