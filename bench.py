@@ -46,6 +46,7 @@ WORKLOADS = {
 }
 METRIC = "MoE layer fwd+bwd TFLOPS (MXFP8 grouped GEMM) and % of dense peak, 1 GB300"
 KERNELS_PER_STEP = 18       # libmoe kernel launches in one fwd+bwd step (see layer.MoELayer)
+WGRAD_SPLIT_KERNELS = 2     # a second launch per weight gradient when they are split by group size
 ROUTER_KERNELS = 6          # with the router: 3 bf16 GEMMs, 3 transposes (the dx combine takes the addend)
 GEMMS_PER_STEP = 6
 
@@ -143,7 +144,8 @@ def run_gpu(args, rank, world, local_rank):
     w = WORKLOADS[args.workload]
     T, d, E, k, f = w["T"], w["d"], w["E"], w["k"], w["f"]
     S = args.shared_experts
-    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev, router=args.router, n_shared=S)
+    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev, router=args.router, n_shared=S,
+                 wgrad224_rows=args.wgrad224_rows)
     if args.router:
         L.set_router_weights(synth.make_normal_bf16((d, E), 5, dev, std=0.02))
     inp = synth.make_layer_inputs(T, d, E, f, dev, zipf_s=w["zipf"], seed_offset=rank, n_shared=S)
@@ -321,7 +323,8 @@ def run_gpu(args, rank, world, local_rank):
                 "h2d_gbs": round(h2d / (h2d_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (d2h_ms * 1e-3) / 1e9, 1),
                 "clocks": clk_e2e.summary()},
         "roofline_memory": memory_roofline(L, mem_ms, Rp, peaks, psrc, write_ceiling),
-        "gpu_launches": (KERNELS_PER_STEP + (ROUTER_KERNELS if args.router else 0) + (2 if S else 0)) * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (ROUTER_KERNELS if args.router else 0) + (2 if S else 0) +
+                         (WGRAD_SPLIT_KERNELS if L.wgrad_split else 0)) * args.steps,
         "clocks": clk.summary(),
     }
     if args.router:
@@ -787,7 +790,7 @@ def run_seeds(args):
     T, d, E, k, f = w["T"], w["d"], w["E"], w["k"], w["f"]
     dev = "cuda:0"
     stream = torch.cuda.current_stream()
-    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev)
+    L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev, wgrad224_rows=args.wgrad224_rows)
     inp = synth.make_layer_inputs(T, d, E, f, dev, zipf_s=w["zipf"])
     L.set_weights(inp["W1"], inp["W2"])
     L.x.copy_(inp["x"])
@@ -874,9 +877,10 @@ def run_compare(args, capacity_factors=(1.0, 1.25)):
     arms = {}
     L = MoELayer(T, d, E, k, f, w["score"], w["normalize"], device=dev)
     load(L)
-    arms["grouped_dropless_eager"] = arm(timed(L.step_, args.steps), launches_per_step=KERNELS_PER_STEP)
+    per_step = KERNELS_PER_STEP + (WGRAD_SPLIT_KERNELS if L.wgrad_split else 0)
+    arms["grouped_dropless_eager"] = arm(timed(L.step_, args.steps), launches_per_step=per_step)
     L.capture()
-    arms["grouped_dropless_graph"] = arm(timed(L.replay, args.steps), launches_per_step=KERNELS_PER_STEP)
+    arms["grouped_dropless_graph"] = arm(timed(L.replay, args.steps), launches_per_step=per_step)
     L.check_err()
     counts = L.counts.cpu()
     L.graph = None
@@ -983,6 +987,9 @@ def main():
     ap.add_argument("--nvfp4", action="store_true",
                     help="with --gemm-point / --sweep: the NVFP4 grouped GEMM (E2M1, UE4M3 scales per 16) instead")
     ap.add_argument("--sweep", action="store_true", help="the 18-point grouped GEMM sweep, one line per point")
+    ap.add_argument("--wgrad224-rows", type=int, nargs=2, default=None, metavar=("LO", "HI"),
+                    help="only groups of LO <= rows < HI (HI 0: unbounded) take 224-wide weight-gradient tiles, "
+                         "the rest 256-wide ones (0 0: all 224; default: the layer's WGRAD224_ROWS)")
     ap.add_argument("--seeds", type=int, default=0, metavar="S",
                     help="replay the captured step over S routing seeds (e.g. --workload deepseek-v3-zipf "
                          "--seeds 20) and print the median; one line")

@@ -534,17 +534,21 @@ struct GemmChoice {
     int bn_1sm;           // 1-SM tile width: 256, or 128 (two TMEM accumulators)
     int band;             // m-tiles per raster band, 0 = the kernel's default
     bool register_stores; // pair kernel, plain epilogue: register-staged stores instead of TMA stores
+    int wg_lo, wg_hi;     // WGRAD group filter by row count (0, 0 = every group)
 };
 
 static bool gemm_opts_valid(const moe_gemm_opts_t* o) {
     return o == nullptr || (o->kernel >= MOE_GEMM_KERNEL_AUTO && o->kernel <= MOE_GEMM_KERNEL_PAIR_N128 &&
-                            o->band >= 0 && o->band <= 64 && (o->register_stores == 0 || o->register_stores == 1));
+                            o->band >= 0 && o->band <= 64 && (o->register_stores == 0 || o->register_stores == 1) &&
+                            o->wgrad_rows_lo >= 0 && o->wgrad_rows_hi >= 0);
 }
 
 // sel = -1 leaves the choice to the default rule of the call.
 static GemmChoice gemm_choice(const moe_gemm_opts_t* o) {
-    GemmChoice c{-1, 256, 0, false};
+    GemmChoice c{-1, 256, 0, false, 0, 0};
     if (o == nullptr) return c;
+    c.wg_lo = o->wgrad_rows_lo;
+    c.wg_hi = o->wgrad_rows_hi;
     switch (o->kernel) {
         case MOE_GEMM_KERNEL_1SM: c.sel = 0; break;
         case MOE_GEMM_KERNEL_1SM_N128: c.sel = 0; c.bn_1sm = 128; break;
@@ -613,6 +617,8 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     MOE_REQUIRE(gemm_opts_valid(opts), MOE_ERR_INVALID_ARG);
     const GemmChoice choice = gemm_choice(opts);
     MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD || mode == MOE_GEMM_WGRAD, MOE_ERR_INVALID_ARG);
+    const bool wg_filter = choice.wg_lo > 0 || choice.wg_hi > 0;
+    MOE_REQUIRE(!wg_filter || mode == MOE_GEMM_WGRAD, MOE_ERR_UNSUPPORTED);
     MOE_REQUIRE(a && a_sf && b && b_sf && gofs && d, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(G >= 1 && G <= MAX_G && M > 0 && N > 0 && K > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(M % 128 == 0 && K % BK == 0 && N % 128 == 0, MOE_ERR_UNSUPPORTED);
@@ -715,7 +721,11 @@ static moe_status_t gemm_run(int mode, const uint8_t* a, const uint8_t* a_sf, co
     if (t224) sel = 224;      // the scale layout of b fixes the tile
     const int bn2 = sel == 224 ? 224 : (sel == 256 && N % 256 == 0 ? 256 : 128);
     const bool two_sm = sel != 0 && gemm_max_clusters_2sm(bn2) > 0 && (mode != MOE_GEMM_WGRAD || M % 256 == 0);
+    MOE_REQUIRE(!wg_filter || two_sm, MOE_ERR_UNSUPPORTED);   // only the pair kernel filters groups
     if (two_sm) {
+        p.wg_filter = wg_filter ? 1 : 0;
+        p.wg_lo = choice.wg_lo;
+        p.wg_hi = choice.wg_hi;
         p.n_tiles = (N + bn2 - 1) / bn2;
         p.band = choice.band > 0 ? choice.band : 2;     // measured: 2 beat 4, 8 and 16
         const int64_t upper_pairs = mode == MOE_GEMM_WGRAD ? (int64_t)G * (M / 256) * p.n_tiles
@@ -861,6 +871,7 @@ extern "C" moe_status_t grouped_gemm_nvfp4_ex(int mode, const uint8_t* a, const 
     using namespace gg;
     MOE_REQUIRE(gemm_opts_valid(opts), MOE_ERR_INVALID_ARG);
     const GemmChoice choice = gemm_choice(opts);
+    MOE_REQUIRE(choice.wg_lo == 0 && choice.wg_hi == 0, MOE_ERR_UNSUPPORTED);   // group filter: MXFP8 pair kernel only
     MOE_REQUIRE(mode == MOE_GEMM_FWD || mode == MOE_GEMM_DGRAD || mode == MOE_GEMM_WGRAD, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(epilogue == MOE_EPI_NONE || (epilogue == MOE_EPI_NONE_F32 && mode != MOE_GEMM_WGRAD),
                 MOE_ERR_INVALID_ARG);      // WGRAD writes bf16 (an empty group's tile is zero-filled as bf16)

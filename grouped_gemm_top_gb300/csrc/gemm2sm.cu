@@ -220,10 +220,13 @@ __device__ __forceinline__ void get_tile2(const Params& p, const int* s_gofs, co
         ti.kbeg = 0;
         ti.nk = (int)(p.K / BK);
     } else {
+        // WGRAD: the tiles of group g (or of the gi-th group that passes
+        // the row filter, listed in s_pt) are [gi * tpg, (gi + 1) * tpg)
         const int64_t mp = p.M / 256;
         const int64_t tpg = mp * p.n_tiles;
-        const int g = (int)(t / tpg);
-        band_decode(t - (int64_t)g * tpg, mp, p.n_tiles, p.band, pm, nt);
+        const int gi = (int)(t / tpg);
+        const int g = p.wg_filter ? s_pt[gi] : gi;
+        band_decode(t - (int64_t)gi * tpg, mp, p.n_tiles, p.band, pm, nt);
         ti.g = g;
         ti.valid = true;
         ti.a_row = pm * 256 + 128 * rank;
@@ -302,13 +305,27 @@ __global__ void __launch_bounds__(THREADS, 1)
             *bad_flag = 1;
             if (blockIdx.x == 0) set_err(p.err, MOE_ERR_BAD_OFFSETS);
         }
-        // pair tiles per group: ceil(rows / 256)
-        int acc = 0;
-        for (int g = 0; g < p.G; ++g) {
-            s_pt[g] = acc;
-            acc += ok ? (s_gofs[g + 1] - s_gofs[g] + 255) / 256 : 0;
+        if (p.mode != MOE_GEMM_WGRAD) {
+            // pair tiles per group: ceil(rows / 256)
+            int acc = 0;
+            for (int g = 0; g < p.G; ++g) {
+                s_pt[g] = acc;
+                acc += ok ? (s_gofs[g + 1] - s_gofs[g] + 255) / 256 : 0;
+            }
+            s_pt[p.G] = acc;
+        } else if (p.wg_filter) {
+            // the groups whose row count passes the filter, in order; their
+            // number at s_pt[G]
+            int n = 0;
+            for (int g = 0; g < p.G && ok; ++g) {
+                const int r = s_gofs[g + 1] - s_gofs[g];
+                const bool in = p.wg_hi == 0 ? r >= p.wg_lo
+                                             : (p.wg_lo < p.wg_hi ? (r >= p.wg_lo && r < p.wg_hi)
+                                                                  : (r < p.wg_hi || r >= p.wg_lo));
+                if (in) s_pt[n++] = g;
+            }
+            s_pt[p.G] = n;
         }
-        s_pt[p.G] = acc;
     }
     tc_fence_before();
     __syncthreads();
@@ -317,8 +334,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const bool bad = *bad_flag != 0;
     const int64_t total_pm = p.mode == MOE_GEMM_WGRAD ? 0 : (int64_t)s_pt[p.G];
+    const int64_t wg_groups = p.mode == MOE_GEMM_WGRAD ? (p.wg_filter ? (int64_t)s_pt[p.G] : (int64_t)p.G) : 0;
     const int64_t total = bad ? 0
-                              : (p.mode == MOE_GEMM_WGRAD ? (int64_t)p.G * (p.M / 256) * p.n_tiles
+                              : (p.mode == MOE_GEMM_WGRAD ? wg_groups * (p.M / 256) * p.n_tiles
                                                           : total_pm * p.n_tiles);
 
     if (warp == 0 && lane == 0) {

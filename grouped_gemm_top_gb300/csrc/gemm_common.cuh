@@ -42,6 +42,11 @@ struct Params {
     int band;           // m-tiles per raster band (consecutive tiles share the B tile)
     int group_bands;    // 1-SM FWD / DGRAD: bands restart at each group's first m-tile
     int tma_store;      // pair kernel, BN = 256, MOE_EPI_NONE: write D through the TMA (tensor map tmD)
+    // WGRAD on the pair kernel: only the groups whose row count r passes
+    // the filter (moe_gemm_opts_t: hi == 0: r >= lo; lo < hi: lo <= r < hi;
+    // 0 < hi <= lo: r < hi or r >= lo); wg_filter = 0 when every group is
+    // computed
+    int wg_filter, wg_lo, wg_hi;
     // bf16 operands (kind::f16): the columns of D that exist (n_out <= N,
     // the rest of the tile is not stored) and D's row stride in elements
     int n_out;

@@ -377,7 +377,8 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
                                                               int64_t rows, uint2* __restrict__ codes_r,
                                                               uint8_t* __restrict__ sf_r,
                                                               uint8_t* __restrict__ codes_c,
-                                                              uint8_t* __restrict__ sf_c, int sf_c_t224,
+                                                              uint8_t* __restrict__ sf_c,
+                                                              uint8_t* __restrict__ sf_c224,
                                                               int32_t* err) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* s_in = reinterpret_cast<uint16_t*>(smem);                       // [2][128][128]
@@ -561,14 +562,15 @@ __global__ void __launch_bounds__(kQBThreads, 3) k_quant_both(const uint16_t* __
                 reinterpret_cast<uint4*>(sf_r + atom * 512)[lane] =
                     reinterpret_cast<const uint4*>(s_atom_r + b * 512)[lane];
             }
-        } else if (warp == 1) {
-            if (codes_c != nullptr) {
-                if (sf_c_t224)
-                    store_col_scales_t224(sf_c, s_atom_c, r0 / kQT, (int64_t)ct * kQT, cols, lane);
-                else {
-                    const int64_t atom = (r0 / kQT) * (int64_t)ntiles + ct;
-                    reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_c)[lane];
-                }
+        } else if (warp == 1 || warp == 2) {
+            // columnwise scales: the tile-224 layout (warp 1) and/or the atom
+            // layout (warp 1 if it is the only one, else warp 2)
+            const bool atoms = sf_c != nullptr && (warp == 2) == (sf_c224 != nullptr);
+            if (warp == 1 && sf_c224 != nullptr)
+                store_col_scales_t224(sf_c224, s_atom_c, r0 / kQT, (int64_t)ct * kQT, cols, lane);
+            if (atoms) {
+                const int64_t atom = (r0 / kQT) * (int64_t)ntiles + ct;
+                reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_c)[lane];
             }
         }
         // the atoms are rewritten no earlier than the next tile's barrier A
@@ -644,7 +646,8 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_swiglu_bwd_quant(const float*
                                                                     uint2* __restrict__ codes_r,
                                                                     uint8_t* __restrict__ sf_r,
                                                                     uint8_t* __restrict__ codes_c,
-                                                                    uint8_t* __restrict__ sf_c, int sf_c_t224,
+                                                                    uint8_t* __restrict__ sf_c,
+                                                                    uint8_t* __restrict__ sf_c224,
                                                                     int32_t* err) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* tiles = reinterpret_cast<uint16_t*>(smem);           // [2][128][128]: dgate, dup
@@ -776,17 +779,36 @@ __global__ void __launch_bounds__(kQBThreads, 2) k_swiglu_bwd_quant(const float*
             const int t = warp;
             const int64_t atom = (int64_t)octile(t) * (rows / kQT) + r0 / kQT;
             reinterpret_cast<uint4*>(sf_r + atom * 512)[lane] = reinterpret_cast<const uint4*>(s_atom_r + t * 512)[lane];
-        } else if (warp < 4) {
-            const int t = warp - 2;
-            if (sf_c_t224) {
-                store_col_scales_t224(sf_c, s_atom_c + t * 512, r0 / kQT, (int64_t)octile(t) * kQT, (int)F2, lane);
-            } else {
+        } else if (warp < 6) {
+            // columnwise scales of output tile t: the tile-224 layout (warps
+            // 2, 3) and/or the atom layout (warps 2, 3 if it is the only one,
+            // else warps 4, 5)
+            const int t = warp & 1;
+            const bool atoms = sf_c != nullptr && (warp >= 4) == (sf_c224 != nullptr);
+            if (warp < 4 && sf_c224 != nullptr)
+                store_col_scales_t224(sf_c224, s_atom_c + t * 512, r0 / kQT, (int64_t)octile(t) * kQT, (int)F2, lane);
+            if (atoms) {
                 const int64_t atom = (r0 / kQT) * (int64_t)out_tiles + octile(t);
                 reinterpret_cast<uint4*>(sf_c + atom * 512)[lane] =
                     reinterpret_cast<const uint4*>(s_atom_c + t * 512)[lane];
             }
         }
         // this tile's atoms are rewritten two tiles on (double-buffered)
+    }
+}
+
+// Where the columnwise scales of a [rows, cols] quantization go (moe_sf_layout_t
+// of the transposed [cols, rows] matrix): the atom layout, the tile-224 layout,
+// or both, the tile-224 bytes first.
+static void col_scale_outputs(uint8_t* scales_col, int layout, int64_t rows, int64_t cols, uint8_t*& atoms,
+                              uint8_t*& t224) {
+    atoms = t224 = nullptr;
+    if (scales_col == nullptr) return;
+    if (layout == MOE_SF_ATOMS) {
+        atoms = scales_col;
+    } else {
+        t224 = scales_col;
+        if (layout == MOE_SF_TILE224_AND_ATOMS) atoms = scales_col + (rows / kQT) * ((cols + 223) / 224) * 1024;
     }
 }
 
@@ -804,7 +826,9 @@ extern "C" moe_status_t mxfp8_gather_quantize_ex(const void* src, int64_t src_ro
                                                  uint8_t* codes_col, uint8_t* scales_col, int col_sf_layout,
                                                  int32_t* err, void* stream) {
     using namespace moe;
-    MOE_REQUIRE(col_sf_layout == MOE_SF_ATOMS || col_sf_layout == MOE_SF_TILE224, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(col_sf_layout == MOE_SF_ATOMS || col_sf_layout == MOE_SF_TILE224 ||
+                    col_sf_layout == MOE_SF_TILE224_AND_ATOMS,
+                MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(src && gofs && G >= 1 && G <= 4096 && cols > 0 && rows > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(row_id != nullptr || row_w == nullptr, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(row_id == nullptr || (k >= 1 && src_rows >= 0 && src_rows <= 0x7FFFFFFF), MOE_ERR_INVALID_ARG);
@@ -823,10 +847,11 @@ extern "C" moe_status_t mxfp8_gather_quantize_ex(const void* src, int64_t src_ro
     const int64_t row_runs = (rows / kQT + kQBRowTiles - 1) / kQBRowTiles;
     MOE_REQUIRE(row_runs <= 0x7FFFFFFF, MOE_ERR_UNSUPPORTED);
     dim3 grid((unsigned)row_runs, (unsigned)(cols / kQT));
+    uint8_t *sf_atoms = nullptr, *sf_t224 = nullptr;
+    col_scale_outputs(scales_col, col_sf_layout, rows, cols, sf_atoms, sf_t224);
     k_quant_both<<<grid, kQBThreads, kQBSmem, (cudaStream_t)stream>>>((const uint16_t*)src, src_rows, cols, k, row_id,
                                                                      row_w, gofs, G, rows, (uint2*)codes_row,
-                                                                     scales_row, codes_col, scales_col,
-                                                                     col_sf_layout == MOE_SF_TILE224 ? 1 : 0, err);
+                                                                     scales_row, codes_col, sf_atoms, sf_t224, err);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }
@@ -845,7 +870,9 @@ extern "C" moe_status_t mxfp8_swiglu_bwd_quantize_ex(const float* dH, const void
                                                      uint8_t* scales_col, int col_sf_layout, int32_t* err,
                                                      void* stream) {
     using namespace moe;
-    MOE_REQUIRE(col_sf_layout == MOE_SF_ATOMS || col_sf_layout == MOE_SF_TILE224, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(col_sf_layout == MOE_SF_ATOMS || col_sf_layout == MOE_SF_TILE224 ||
+                    col_sf_layout == MOE_SF_TILE224_AND_ATOMS,
+                MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(dH && a_pre && gofs && codes_row && scales_row && codes_col && scales_col, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(G >= 1 && G <= 4096 && f > 0 && rows > 0, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(f % kQT == 0 && rows % kQT == 0 && rows <= 0x7FFFFFFF && f / kQT <= 65535, MOE_ERR_UNSUPPORTED);
@@ -856,9 +883,11 @@ extern "C" moe_status_t mxfp8_swiglu_bwd_quantize_ex(const float* dH, const void
     MOE_REQUIRE(device_initialized(), MOE_ERR_NOT_INITIALIZED);
     const int64_t row_runs = (rows / kQT + kQBRowTiles - 1) / kQBRowTiles;
     dim3 grid((unsigned)row_runs, (unsigned)(f / kQT));
+    uint8_t *sf_atoms = nullptr, *sf_t224 = nullptr;
+    col_scale_outputs(scales_col, col_sf_layout, rows, 2 * (int64_t)f, sf_atoms, sf_t224);
     k_swiglu_bwd_quant<<<grid, kQBThreads, kSBSmem, (cudaStream_t)stream>>>(
         dH, (const uint16_t*)a_pre, f, gofs, G, rows, (uint16_t*)dA, (uint2*)codes_row, scales_row, codes_col,
-        scales_col, col_sf_layout == MOE_SF_TILE224 ? 1 : 0, err);
+        sf_atoms, sf_t224, err);
     MOE_CHECK_LAUNCH();
     return MOE_OK;
 }

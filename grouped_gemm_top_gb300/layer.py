@@ -15,10 +15,20 @@ from . import ops
 
 _SCORES = {"softmax": ops.MOE_SCORE_SOFTMAX, "sigmoid": ops.MOE_SCORE_SIGMOID}
 
+# When the weight gradients use 224-wide tiles, only the groups with
+# lo <= rows < hi (padded rows; hi = 0: no upper bound) do; the others take
+# 256 x 256 tiles in a second launch (MoELayer wgrad224_rows).  Measured on
+# the DeepSeek-V3 step: balanced routing (every group 640-896 rows) runs as
+# with 224-wide tiles throughout; Zipf(1.2)-skewed routing, whose few large
+# groups want the full-width MMA and whose many small ones the fewer, wider
+# tiles, 28.25-28.28 ms against 29.10-29.16 ms (all 224) and 28.15-28.34 ms
+# (all 256).
+WGRAD224_ROWS = (512, 4096)
+
 
 class MoELayer:
     def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_intermediates=False,
-                 router=False, n_shared=0, row_cap=None, wgrad_tiles=None):
+                 router=False, n_shared=0, row_cap=None, wgrad_tiles=None, wgrad224_rows=None):
         """store_intermediates: also write h and dA in bf16 (the step itself
         only needs their MXFP8 codes, which the up/gate GEMM's epilogue and
         the fused SwiGLU-backward quantization produce).
@@ -31,7 +41,12 @@ class MoELayer:
         S extra choices per token, so the layer runs G = E+S groups over
         T (k+S) rows; the router and its logits cover the E routed experts.
         wgrad_tiles: 224 or 256 forces the weight-gradient GEMMs' pair-tile
-        width; None chooses (see below)."""
+        width; None chooses (see below).
+        wgrad224_rows: (lo, hi) with 224-wide weight-gradient tiles, only
+        the groups of lo <= rows < hi (hi = 0: no upper bound) use them, the
+        others 256-wide tiles in a second launch per weight gradient (the
+        device picks the groups from the step's offsets); (0, 0) = every
+        group on the 224-wide tiles; None = WGRAD224_ROWS."""
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
         self.S = int(n_shared)
         self.G, self.kk = E + self.S, k + self.S      # expert groups, choices per token
@@ -96,11 +111,26 @@ class MoELayer:
             self.wgrad_t224 = wgrad_tiles == 224
         else:
             raise ValueError("wgrad_tiles: None, 224 or 256")
-        self.col_sf = ops.MOE_SF_TILE224 if self.wgrad_t224 else ops.MOE_SF_ATOMS
+        # Under skewed routing a few groups hold thousands of rows; their
+        # long contractions run faster on the full-width 256 x 256 tiles, so
+        # each weight gradient is split in two launches by group size, the
+        # right operands' scales written in both layouts.
+        lo, hi = WGRAD224_ROWS if wgrad224_rows is None else (int(wgrad224_rows[0]), int(wgrad224_rows[1]))
+        if lo < 0 or hi < 0 or (hi and hi <= lo):
+            raise ValueError("wgrad224_rows: 0 <= lo, and hi == 0 or hi > lo")
+        self.wgrad_split = self.wgrad_t224 and (lo > 0 or hi > 0)
+        self.wgrad224_rows = (lo, hi) if self.wgrad_split else (0, 0)
+        if self.wgrad_split:
+            self.col_sf = ops.MOE_SF_TILE224_AND_ATOMS
+            # the 256-wide launch takes the complement: rows < lo or rows >= hi
+            self.wg_224 = ops.gemm_opts(wgrad_rows=(lo, hi))
+            self.wg_256 = ops.gemm_opts(wgrad_rows=(hi, lo) if hi else (0, lo))
+        else:
+            self.col_sf = ops.MOE_SF_TILE224 if self.wgrad_t224 else ops.MOE_SF_ATOMS
         self.wgrad_b = ops.MOE_B_SF_TILE224 if self.wgrad_t224 else ops.MOE_B_GNK
 
         def sfc(C):              # bytes of the columnwise scales of a [M, C] matrix
-            return ops.sf_bytes_tile224(C, M) if self.wgrad_t224 else ops.sf_bytes(M, C)
+            return ops.col_sf_bytes(self.col_sf, M, C)
 
         self.dyq, self.dys = z((M, d), torch.uint8), z((ops.sf_bytes(M, d),), torch.uint8)
         self.dyqT, self.dysT = z((d, M), torch.uint8), z((sfc(d),), torch.uint8)
@@ -197,6 +227,23 @@ class MoELayer:
     def _gemm_swiglu_quant(self, *args):
         return self._timed(ops.grouped_gemm_mxfp8_swiglu_quant, *args)
 
+    def _wgrad(self, a, a_sf, b, b_sf, Mo, No, d_out):
+        """d_out[g] = A_g B_g^T over each group's rows (one timed launch, or
+        the 224-wide launch over the groups in the wgrad224_rows band and the
+        256-wide one over the rest, under a single pair of events)."""
+        E, K, err = self.G, self.row_cap, self.err
+        if not self.wgrad_split:
+            return self._gemm(ops.MOE_GEMM_WGRAD, a, a_sf, b, b_sf, self.wgrad_b, self.gofs, E, Mo, No, K,
+                              ops.MOE_EPI_NONE, None, d_out, None, err)
+        n224 = ops.sf_bytes_tile224(No, K)
+
+        def both():
+            ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, a, a_sf, b, b_sf[:n224], ops.MOE_B_SF_TILE224, self.gofs, E,
+                                   Mo, No, K, ops.MOE_EPI_NONE, None, d_out, None, err, opts=self.wg_224)
+            ops.grouped_gemm_mxfp8(ops.MOE_GEMM_WGRAD, a, a_sf, b, b_sf[n224:], ops.MOE_B_GNK, self.gofs, E,
+                                   Mo, No, K, ops.MOE_EPI_NONE, None, d_out, None, err, opts=self.wg_256)
+        return self._timed(both)
+
     # ------------------------------------------------------------- step ----
     def route_permute_(self):
         """Router GEMM (if any), top-k routing, shared choices (if any) and
@@ -250,8 +297,7 @@ class MoELayer:
         self._gemm(ops.MOE_GEMM_DGRAD, self.dyq, self.dys, self.W2d, self.W2d_s, ops.MOE_B_GNK,
                    self.gofs, E, M, f, d, ops.MOE_EPI_NONE_F32, None, self.dH, None, err)
         # dW2_g = H_g^T dY_g
-        self._gemm(ops.MOE_GEMM_WGRAD, self.hqT, self.hsT, self.dyqT, self.dysT, self.wgrad_b, self.gofs, E, f,
-                   d, M, ops.MOE_EPI_NONE, None, self.dW2, None, err)
+        self._wgrad(self.hqT, self.hsT, self.dyqT, self.dysT, f, d, self.dW2)
         # dA = [dgate | dup] = SwiGLU backward of (a_pre, dH), quantized on
         # both axes in the same pass
         self._mem("swiglu_bwd_quant_dA", ops.mxfp8_swiglu_bwd_quantize, self.dH, self.a_pre, self.gofs, E, self.dA,
@@ -273,9 +319,7 @@ class MoELayer:
 
     def backward_dw1_(self):
         """The last weight gradient, dW1_g = X_g^T dA_g."""
-        E, d, f, M = self.G, self.d, self.f, self.row_cap
-        self._gemm(ops.MOE_GEMM_WGRAD, self.xqT, self.xsT, self.dAqT, self.dAsT, self.wgrad_b, self.gofs, E, d,
-                   2 * f, M, ops.MOE_EPI_NONE, None, self.dW1, None, self.err)
+        self._wgrad(self.xqT, self.xsT, self.dAqT, self.dAsT, self.d, 2 * self.f, self.dW1)
 
     def step_(self):
         """One fwd+bwd pass over the resident inputs (no allocation, no sync)."""

@@ -34,7 +34,7 @@ MOE_QUANT_COLWISE_BATCHED, MOE_QUANT_COLWISE_BATCHED_GLU = 3, 4
 MOE_GEMM_FWD, MOE_GEMM_DGRAD, MOE_GEMM_WGRAD = 0, 1, 2
 MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_SWIGLU_BWD, MOE_EPI_NONE_F32 = 0, 1, 2, 3
 MOE_B_GNK, MOE_B_NGK, MOE_B_SF_TILE224 = 0, 1, 2
-MOE_SF_ATOMS, MOE_SF_TILE224, MOE_SF_CANONICAL = 0, 1, 2
+MOE_SF_ATOMS, MOE_SF_TILE224, MOE_SF_CANONICAL, MOE_SF_TILE224_AND_ATOMS = 0, 1, 2, 3
 MOE_GEMM_KERNEL_AUTO, MOE_GEMM_KERNEL_1SM, MOE_GEMM_KERNEL_1SM_N128 = 0, 1, 2
 MOE_GEMM_KERNEL_PAIR, MOE_GEMM_KERNEL_PAIR_N128 = 3, 4
 (MOE_OP_ROUTE_TOPK, MOE_OP_PERMUTE, MOE_OP_GROUP_QUANTIZE, MOE_OP_GATHER_QUANTIZE, MOE_OP_GROUPED_GEMM,
@@ -58,19 +58,22 @@ _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_s
 
 class GemmOpts(ctypes.Structure):
     """moe_gemm_opts_t (include/moe.h): per-call grouped-GEMM kernel choice."""
-    _fields_ = [("kernel", ctypes.c_int), ("band", ctypes.c_int), ("register_stores", ctypes.c_int)]
+    _fields_ = [("kernel", ctypes.c_int), ("band", ctypes.c_int), ("register_stores", ctypes.c_int),
+                ("wgrad_rows_lo", ctypes.c_int), ("wgrad_rows_hi", ctypes.c_int)]
 
 
 _GEMM_KERNELS = {"auto": MOE_GEMM_KERNEL_AUTO, "1sm": MOE_GEMM_KERNEL_1SM, "1sm_n128": MOE_GEMM_KERNEL_1SM_N128,
                  "pair": MOE_GEMM_KERNEL_PAIR, "pair_n128": MOE_GEMM_KERNEL_PAIR_N128}
 
 
-def gemm_opts(kernel="auto", band=0, register_stores=False):
+def gemm_opts(kernel="auto", band=0, register_stores=False, wgrad_rows=(0, 0)):
     """A GemmOpts for the opts= argument of the grouped-GEMM wrappers;
     kernel is one of "auto", "1sm", "1sm_n128", "pair", "pair_n128" (or the
-    MOE_GEMM_KERNEL_* value)."""
+    MOE_GEMM_KERNEL_* value); wgrad_rows = (lo, hi): WGRAD computes only the
+    groups with lo <= rows and (hi == 0 or rows < hi)."""
     k = _GEMM_KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
-    return GemmOpts(k, int(band), int(bool(register_stores)))
+    lo, hi = wgrad_rows
+    return GemmOpts(k, int(band), int(bool(register_stores)), int(lo), int(hi))
 
 
 _SIGS = {
@@ -255,6 +258,18 @@ def sf_bytes_tile224(rows: int, cols: int) -> int:
     return (cols // 128) * ((rows + 223) // 224) * 1024
 
 
+def col_sf_bytes(layout: int, rows: int, cols: int) -> int:
+    """Bytes of the columnwise scales of a [rows, cols] quantization (the
+    transposed [cols, rows] matrix) in moe_sf_layout_t `layout`; for
+    MOE_SF_TILE224_AND_ATOMS the atom layout starts at
+    sf_bytes_tile224(cols, rows)."""
+    if layout == MOE_SF_TILE224:
+        return sf_bytes_tile224(cols, rows)
+    if layout == MOE_SF_TILE224_AND_ATOMS:
+        return sf_bytes_tile224(cols, rows) + sf_bytes(rows, cols)
+    return sf_bytes(rows, cols)
+
+
 def mxfp8_group_quantize(x, axis=MOE_QUANT_ROWWISE, gofs=None, G=0, codes=None, scales=None, err=None,
                          stream=None):
     """See include/moe.h.  Returns (codes, scales) with the scales in the
@@ -302,7 +317,8 @@ def mxfp8_gather_quantize(src, gofs, G, rows, row_id=None, k=1, row_w=None, roww
     matrix whose row s is src[row_id[s] // k] (times row_w[row_id[s]]), or
     src[s] without row_id.  See include/moe.h (a given codes_row must be
     32-byte aligned, as fresh torch allocations are).  col_sf_layout
-    MOE_SF_TILE224 writes the columnwise scales in the tile-224 layout
+    MOE_SF_TILE224 writes the columnwise scales in the tile-224 layout,
+    MOE_SF_TILE224_AND_ATOMS that and the atom layout after it
     (mxfp8_gather_quantize_ex).  Returns (codes_row, scales_row, codes_col,
     scales_col), None for an axis not asked for."""
     cols = src.shape[1]
@@ -313,7 +329,7 @@ def mxfp8_gather_quantize(src, gofs, G, rows, row_id=None, k=1, row_w=None, roww
         codes_row = scales_row = None
     if colwise:
         codes_col = codes_col if codes_col is not None else _empty((cols, rows), torch.uint8, src)
-        nsc = sf_bytes_tile224(cols, rows) if col_sf_layout == MOE_SF_TILE224 else sf_bytes(rows, cols)
+        nsc = col_sf_bytes(col_sf_layout, rows, cols)
         scales_col = scales_col if scales_col is not None else torch.zeros((nsc,), dtype=torch.uint8,
                                                                            device=src.device)
     else:
@@ -364,7 +380,7 @@ def mxfp8_swiglu_bwd_quantize(dH, a_pre, gofs, G, dA=None, want_dA=False, codes_
     codes_row = codes_row if codes_row is not None else _empty((rows, 2 * f), torch.uint8, dH)
     scales_row = scales_row if scales_row is not None else _empty((sf_bytes(rows, 2 * f),), torch.uint8, dH)
     codes_col = codes_col if codes_col is not None else _empty((2 * f, rows), torch.uint8, dH)
-    nsc = sf_bytes_tile224(2 * f, rows) if col_sf_layout == MOE_SF_TILE224 else sf_bytes(rows, 2 * f)
+    nsc = col_sf_bytes(col_sf_layout, rows, 2 * f)
     scales_col = scales_col if scales_col is not None else torch.zeros((nsc,), dtype=torch.uint8, device=dH.device)
     args = (_p(dH), _p(a_pre), int(f), _p(gofs), int(G), int(rows), _p(dA), _p(codes_row), _p(scales_row),
             _p(codes_col), _p(scales_col))

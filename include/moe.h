@@ -136,8 +136,20 @@ typedef enum {
  *   MOE_SF_CANONICAL row-major [R, C / 32]: byte r * (C / 32) + b is the scale
  *                    of row r, block b (mxfp8_group_quantize_ex only; the
  *                    GEMMs read the atom layout, mxfp8_scale_layout converts).
+ *   MOE_SF_TILE224_AND_ATOMS  both: the tile-224 layout in the first
+ *                    (C / 128) * ceil(R / 224) * 1024 bytes, the atom layout
+ *                    right after it (columnwise scales of
+ *                    mxfp8_gather_quantize_ex and mxfp8_swiglu_bwd_quantize_ex
+ *                    only), for weight gradients that run some groups on the
+ *                    224-wide tiles and the others on 256-wide ones
+ *                    (moe_gemm_opts_t.wgrad_rows_lo / _hi).
  */
-typedef enum { MOE_SF_ATOMS = 0, MOE_SF_TILE224 = 1, MOE_SF_CANONICAL = 2 } moe_sf_layout_t;
+typedef enum {
+    MOE_SF_ATOMS = 0,
+    MOE_SF_TILE224 = 1,
+    MOE_SF_CANONICAL = 2,
+    MOE_SF_TILE224_AND_ATOMS = 3
+} moe_sf_layout_t;
 
 /*
  * Grouped-GEMM kernel selection, per call (the *_ex entry points; the plain
@@ -172,12 +184,30 @@ typedef enum {
  *   register_stores  1: the CTA-pair kernel's plain bf16 epilogue stores
  *                    from registers instead of staging through shared memory
  *                    for TMA stores; 0 = default (TMA stores).
+ *   wgrad_rows_lo, wgrad_rows_hi
+ *                    MOE_GEMM_WGRAD only: compute only the groups whose row
+ *                    count r = gofs[g+1] - gofs[g] passes the filter
+ *                      hi == 0:       r >= lo
+ *                      lo < hi:       lo <= r < hi
+ *                      0 < hi <= lo:  r < hi or r >= lo
+ *                    and leave d[g] of every other group as it is.  Swapping
+ *                    lo and hi gives the complement, so two calls cover every
+ *                    group once, e.g. the mid-size groups on 224-wide tiles
+ *                    (MOE_B_SF_TILE224) and the rest on 256-wide tiles.  The
+ *                    choice is made on the device from gofs (no host round
+ *                    trip).  0, 0 = every group; lo, hi >= 0.  Only the
+ *                    CTA-pair kernels filter: a call that runs on the 1-SM
+ *                    kernel (M % 256 != 0, MOE_GEMM_KERNEL_1SM*, NVFP4)
+ *                    returns MOE_ERR_UNSUPPORTED, as does a filter on FWD or
+ *                    DGRAD.
  * Values out of range return MOE_ERR_INVALID_ARG.
  */
 typedef struct {
     int kernel;
     int band;
     int register_stores;
+    int wgrad_rows_lo;
+    int wgrad_rows_hi;
 } moe_gemm_opts_t;
 
 /* Calls that may take a workspace (moe_workspace_size). */
@@ -389,8 +419,10 @@ MOE_API moe_status_t mxfp8_gather_quantize(const void* src, int64_t src_rows, in
  * MOE_SF_TILE224 writes the columnwise scales in the tile-224 layout of the
  * [cols, rows] transposed matrix ((rows / 128) * ceil(cols / 224) * 1024
  * bytes; bytes of rows >= cols in the last tile are not written), the
- * right-operand scales of grouped_gemm_mxfp8 WGRAD with MOE_B_SF_TILE224.
- * The codes and the rowwise output are unchanged. */
+ * right-operand scales of grouped_gemm_mxfp8 WGRAD with MOE_B_SF_TILE224;
+ * MOE_SF_TILE224_AND_ATOMS writes that and, right after it, the atom layout
+ * ((rows / 32) * cols more bytes).  The codes and the rowwise output are
+ * unchanged; MOE_SF_CANONICAL is not accepted here (MOE_ERR_INVALID_ARG). */
 MOE_API moe_status_t mxfp8_gather_quantize_ex(const void* src, int64_t src_rows, int cols, int k,
                                               const int32_t* row_id, const float* row_w, const int32_t* gofs, int G,
                                               int64_t rows, uint8_t* codes_row, uint8_t* scales_row,

@@ -118,7 +118,10 @@ def sampled_checks(L, inp, score, norm, n_rows=256, n_groups=None, seed=0):
             aT, asT, bT, bsT, Mo, No, dW = L.hqT, L.hsT, L.dyqT, L.dysT, f, d, L.dW2
         else:
             aT, asT, bT, bsT, Mo, No, dW = L.xqT, L.xsT, L.dAqT, L.dAsT, d, 2 * f, L.dW1
-        gs = rng.choice(nonempty, size=min(4, len(nonempty)), replace=False)
+        # the largest group always (under skew it runs on the 256-wide tiles
+        # of a split weight gradient), and random others
+        big = int(nonempty[np.argmax(counts[nonempty])])
+        gs = np.unique(np.concatenate([[big], rng.choice(nonempty, size=min(4, len(nonempty)), replace=False)]))
         for g in gs:
             lo, hi = int(gofs[g]), int(gofs[g + 1])
             ms = rng.choice(Mo, size=8, replace=False)

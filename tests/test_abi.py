@@ -89,6 +89,33 @@ def test_host_only_calls_and_argument_checks(lib_path):
                                    ctypes.c_void_p(16), 0, ctypes.c_void_p(16), 4, 256, 256, 256, 0, None,
                                    ctypes.c_void_p(16), None, ctypes.byref(bad), None, None)
     assert st == ops.MOE_ERR_INVALID_ARG
+    # the weight-gradient group filter: lo, hi >= 0; only WGRAD
+    for lo, hi in ((-1, 0), (0, -512)):
+        bad = ops.gemm_opts("auto", wgrad_rows=(lo, hi))
+        st = lib.grouped_gemm_mxfp8_ex(2, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                       ctypes.c_void_p(16), 0, ctypes.c_void_p(16), 4, 256, 256, 256, 0, None,
+                                       ctypes.c_void_p(16), None, ctypes.byref(bad), None, None)
+        assert st == ops.MOE_ERR_INVALID_ARG, (lo, hi)
+    fwd_filter = ops.gemm_opts("auto", wgrad_rows=(0, 512))
+    st = lib.grouped_gemm_mxfp8_ex(0, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                   ctypes.c_void_p(16), 0, ctypes.c_void_p(16), 4, 256, 256, 256, 0, None,
+                                   ctypes.c_void_p(16), None, ctypes.byref(fwd_filter), None, None)
+    assert st == ops.MOE_ERR_UNSUPPORTED
+    # both columnwise scale layouts: accepted by the fused quantizers (the
+    # call then stops at the next check, rows % 128 != 0), refused by the
+    # plain one.  Every call here must fail before any device work, also in
+    # a process that has initialised the library: the pointers are fake.
+    p64 = ctypes.c_void_p(64)
+    for layout, want in ((ops.MOE_SF_TILE224_AND_ATOMS, ops.MOE_ERR_UNSUPPORTED),
+                         (ops.MOE_SF_CANONICAL, ops.MOE_ERR_INVALID_ARG)):
+        st = lib.mxfp8_gather_quantize_ex(p64, 100, 128, 1, None, None, p64, 1, 100, p64, p64, p64, p64, layout,
+                                          None, None)
+        assert st == want, layout
+    st = lib.mxfp8_group_quantize_ex(ctypes.c_void_p(16), 128, 128, ops.MOE_QUANT_ROWWISE, None, 0,
+                                     ctypes.c_void_p(16), ctypes.c_void_p(16), None,
+                                     ops.MOE_SF_TILE224_AND_ATOMS, None, None)
+    assert st == ops.MOE_ERR_INVALID_ARG
+    assert ops.col_sf_bytes(ops.MOE_SF_TILE224_AND_ATOMS, 256, 448) == 2 * 2 * 1024 + 256 * 14
     st = lib.mxfp8_scale_layout(ctypes.c_void_p(16), 100, 128, 1, ctypes.c_void_p(16), None)
     assert st == ops.MOE_ERR_UNSUPPORTED                       # rows % 128 != 0
     st = lib.moe_hbm_fill(ctypes.c_void_p(16), 24, 0, 0, None)

@@ -139,6 +139,13 @@ def test_deepseek_whole_groups_both_axes(ops, pool, zipf):
             s_at, sT_at = atoms[name]
             col_sc = (tile224_block_range(sT_at, C, M, lo // 32, hi // 32) if t224
                       else atoms_block_range(sT_at, C, M, lo // 32, hi // 32))
+            if t224 and L.col_sf == ops.MOE_SF_TILE224_AND_ATOMS:
+                # the atom copy after the tile-224 bytes (the split weight
+                # gradients' 256-wide launch reads it): the same scales
+                n224 = ops.sf_bytes_tile224(C, M)
+                at = atoms_block_range(sT_at[n224:], C, M, lo // 32, hi // 32)
+                if not np.array_equal(at, col_sc):
+                    bad.append(f"{name} group {g}: atom copy of the columnwise scales differs")
             bad += pool.check_both_axes(f"{name} group {g} ({counts[g]} rows)", sources[name](),
                                         np.array([0, hi - lo]), q[lo:hi].cpu().numpy(),
                                         atoms_rows_subset(s_at, M, C, rows), qT[:, lo:hi].cpu().numpy(), col_sc)

@@ -325,3 +325,66 @@ def test_swiglu_bwd_tile224_scales(ops):
     assert torch.equal(cc2[:, :Rp], cc[:, :Rp]) and torch.equal(cr2[:Rp], cr[:Rp])
     assert np.array_equal(tile224_to_rowmajor(sc2.cpu().numpy(), 2 * f, rows)[:, :Rp // 32],
                           atoms_to_rowmajor(sc.cpu().numpy(), 2 * f, rows)[:, :Rp // 32])
+
+
+@pytest.mark.parametrize("d", [384, 7168])
+def test_gather_scaled_both_scale_layouts(ops, d):
+    """MOE_SF_TILE224_AND_ATOMS: the tile-224 bytes, then the atom layout,
+    each bit-exact as the single-layout calls write them (same fill for the
+    bytes neither writes); codes unchanged."""
+    T, E, k = 600, 8, 2
+    idx, w, slot_of, row_id, gofs = _routing(T, E, k, 5, 0.5)
+    Rp = int(gofs[-1])
+    rows = Rp + 128
+    x = _varied(T, d, 11)
+    rid = np.full(rows, -1, dtype=np.int32)
+    rid[:Rp] = row_id
+    gt, rt, wt = _dev(gofs, torch.int32), _dev(rid, torch.int32), _dev(w, torch.float32)
+    n224, nat = ops.sf_bytes_tile224(d, rows), ops.sf_bytes(rows, d)
+    assert ops.col_sf_bytes(ops.MOE_SF_TILE224_AND_ATOMS, rows, d) == n224 + nat
+
+    def run(layout, n):
+        sc = torch.full((n,), 0xCD, dtype=torch.uint8, device="cuda")
+        r = ops.mxfp8_gather_quantize(x, gt, E, rows, rt, k, wt, True, True, scales_col=sc, col_sf_layout=layout)
+        return r[0], r[2], sc
+
+    q_at, qc_at, sc_at = run(ops.MOE_SF_ATOMS, nat)
+    q_224, qc_224, sc_224 = run(ops.MOE_SF_TILE224, n224)
+    q_b, qc_b, sc_b = run(ops.MOE_SF_TILE224_AND_ATOMS, n224 + nat)
+    torch.cuda.synchronize()
+    assert torch.equal(q_b[:Rp], q_at[:Rp]) and torch.equal(qc_b[:, :Rp], qc_at[:, :Rp])
+    assert torch.equal(sc_b[:n224], sc_224)
+    assert torch.equal(sc_b[n224:], sc_at)
+    P = O.permute_scaled_bf16(to_np(x), row_id, k, w.astype(np.float64))
+    _, cs, _ = O.mxfp8_quantize_cols_grouped(P, gofs)
+    assert np.array_equal(atoms_to_rowmajor(sc_b[n224:].cpu().numpy(), d, rows)[:, :Rp // 32], cs)
+
+
+def test_swiglu_bwd_both_scale_layouts(ops):
+    """mxfp8_swiglu_bwd_quantize with MOE_SF_TILE224_AND_ATOMS: the
+    tile-224 bytes, then the atom layout, as the single-layout calls write
+    them."""
+    sizes, f = [300, 0, 129, 700], 384
+    gofs = padded_layout(sizes)
+    Rp = int(gofs[-1])
+    rows = Rp + 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    dH = torch.randn((rows, f), generator=g, device="cuda")
+    a_pre = torch.randn((rows, 2 * f), generator=g, device="cuda").to(torch.bfloat16)
+    gt = _dev(gofs, torch.int32)
+    n224, nat = ops.sf_bytes_tile224(2 * f, rows), ops.sf_bytes(rows, 2 * f)
+
+    def run(layout, n):
+        sc = torch.full((n,), 0xCD, dtype=torch.uint8, device="cuda")
+        _, cr, _, cc, _ = ops.mxfp8_swiglu_bwd_quantize(dH, a_pre, gt, len(sizes), scales_col=sc,
+                                                        col_sf_layout=layout)
+        return cr, cc, sc
+
+    cr_at, cc_at, sc_at = run(ops.MOE_SF_ATOMS, nat)
+    _, _, sc_224 = run(ops.MOE_SF_TILE224, n224)
+    cr_b, cc_b, sc_b = run(ops.MOE_SF_TILE224_AND_ATOMS, n224 + nat)
+    torch.cuda.synchronize()
+    assert torch.equal(cr_b[:Rp], cr_at[:Rp]) and torch.equal(cc_b[:, :Rp], cc_at[:, :Rp])
+    assert torch.equal(sc_b[:n224], sc_224)
+    assert torch.equal(sc_b[n224:], sc_at)

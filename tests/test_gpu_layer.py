@@ -212,3 +212,40 @@ def test_large_layer_sampled(ops, name, T, d, E, k, f, score, zipf, S):
     sampled_checks(L, inp, score, True)
     del L, inp
     torch.cuda.empty_cache()
+
+
+def test_wgrad_split_matches_single_launch(ops):
+    """Skewed routing over 8 experts (T = 4096, top-2: groups of 256 to 3328
+    padded rows): with the weight gradients split (224-wide tiles for the
+    groups in the layer's WGRAD224_ROWS band, 256-wide tiles for the rest),
+    the band's groups equal the single 224-wide launch's bit for bit and the
+    rest within bf16 rounding; all of them against the oracle on sampled
+    entries (the largest group always)."""
+    from grouped_gemm_top_gb300.layer import MoELayer, WGRAD224_ROWS
+    T, d, E, k, f = 4096, 512, 8, 2, 256
+    inp = synth.make_layer_inputs(T, d, E, f, "cuda", zipf_s=1.2)
+    layers = []
+    for band in (None, (0, 0)):
+        L = MoELayer(T, d, E, k, f, "softmax", True, store_intermediates=True, wgrad224_rows=band)
+        L.set_weights(inp["W1"], inp["W2"])
+        L.logits.copy_(inp["logits"])
+        L.x.copy_(inp["x"])
+        L.dout.copy_(inp["dout"])
+        L.step_()
+        torch.cuda.synchronize()
+        L.check_err()
+        layers.append(L)
+    Ls, Lu = layers
+    assert Ls.wgrad_t224 and Ls.wgrad_split and Ls.wgrad224_rows == WGRAD224_ROWS and not Lu.wgrad_split
+    rows = np.diff(Ls.gofs.cpu().numpy())
+    assert np.array_equal(rows, np.diff(Lu.gofs.cpu().numpy()))
+    lo, hi = WGRAD224_ROWS
+    band = (rows >= lo) & ((rows < hi) if hi else True)
+    assert band.sum() >= 2 and (~band).sum() >= 2          # both launches have work
+    for a, b, name in ((Ls.dW1, Lu.dW1, "dW1"), (Ls.dW2, Lu.dW2, "dW2")):
+        for g in range(E):
+            if band[g]:
+                assert torch.equal(a[g], b[g]), f"{name} g={g}"
+            else:
+                assert_bf16_close(a[g], to_np(b[g]), what=f"{name} g={g} (256-wide vs 224-wide)")
+    sampled_checks(Ls, inp, "softmax", True)
