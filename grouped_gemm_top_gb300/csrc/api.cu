@@ -29,7 +29,7 @@ bool device_initialized() {
 
 }  // namespace moe
 
-extern "C" int moe_abi_version(void) { return 101; }
+extern "C" int moe_abi_version(void) { return 200; }
 
 extern "C" const char* moe_status_string(int s) {
     switch (s) {

@@ -222,7 +222,9 @@ typedef enum {
     MOE_OP_ROUTE_BWD = 7
 } moe_op_t;
 
-/* Version of this ABI (major*100 + minor). */
+/* Version of this ABI (major*100 + minor): 200.  2.0 grew moe_gemm_opts_t
+ * by wgrad_rows_lo / wgrad_rows_hi (a caller built against the 1.x struct
+ * passes too few bytes) and added MOE_SF_TILE224_AND_ATOMS. */
 MOE_API int moe_abi_version(void);
 
 /* Human-readable name of a status code (static string). */

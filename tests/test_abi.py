@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib_path):
 def test_binding_matches_header(lib_path):
     from grouped_gemm_top_gb300 import ops
     assert set(ops.EXPORTS) == set(_declared())
-    assert ops.moe_abi_version() == 101
+    assert ops.moe_abi_version() == 200
 
 
 def test_host_only_calls_and_argument_checks(lib_path):
