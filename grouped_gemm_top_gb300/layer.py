@@ -26,6 +26,13 @@ _SCORES = {"softmax": ops.MOE_SCORE_SOFTMAX, "sigmoid": ops.MOE_SCORE_SIGMOID}
 WGRAD224_ROWS = (512, 4096)
 
 
+def wgrad_band_filters(lo, hi):
+    """The weight-gradient group filters (moe_gemm_opts_t wgrad_rows_lo,
+    wgrad_rows_hi) of the 224-wide launch over the groups of lo <= rows < hi
+    (hi = 0: no upper bound) and of the 256-wide launch over all the others."""
+    return (lo, hi), ((hi, lo) if hi else (0, lo))
+
+
 class MoELayer:
     def __init__(self, T, d, E, k, f, score="softmax", normalize=True, device="cuda:0", store_intermediates=False,
                  router=False, n_shared=0, row_cap=None, wgrad_tiles=None, wgrad224_rows=None):
@@ -122,9 +129,9 @@ class MoELayer:
         self.wgrad224_rows = (lo, hi) if self.wgrad_split else (0, 0)
         if self.wgrad_split:
             self.col_sf = ops.MOE_SF_TILE224_AND_ATOMS
-            # the 256-wide launch takes the complement: rows < lo or rows >= hi
-            self.wg_224 = ops.gemm_opts(wgrad_rows=(lo, hi))
-            self.wg_256 = ops.gemm_opts(wgrad_rows=(hi, lo) if hi else (0, lo))
+            f224, f256 = wgrad_band_filters(lo, hi)
+            self.wg_224 = ops.gemm_opts(wgrad_rows=f224)
+            self.wg_256 = ops.gemm_opts(wgrad_rows=f256)
         else:
             self.col_sf = ops.MOE_SF_TILE224 if self.wgrad_t224 else ops.MOE_SF_ATOMS
         self.wgrad_b = ops.MOE_B_SF_TILE224 if self.wgrad_t224 else ops.MOE_B_GNK
